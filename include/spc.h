@@ -1,0 +1,243 @@
+/*
+ * spc.h -- C ABI of the SpeContext decode-step hot path on GB300 (sm_103a).
+ *
+ * The method (pages cited by title and section):
+ *   [Blog]    "ASPLOS'26 | SpeContext 让小模型先圈出重要 KV Cache" (marsggbo blog)
+ *   [Summary] "SpeContext: Enabling Efficient Long-context Reasoning with
+ *             Speculative Context Sparsity in LLMs" (paperlayer.ai summary of
+ *             arXiv 2512.00722v1)
+ *   [SparseSpec-L] news post on SparseSpec-L (only its "sinks + recent window
+ *             + top-K" retained set is used here)
+ *
+ * One decode step, per [Blog] §4: the lightweight retrieval head scores the
+ * whole context and selects positions for the NEXT step (spc_score_select);
+ * only positions not already resident are loaded (spc_elastic_diff, then
+ * spc_gather_kv on a second stream); the LLM attends over the sparse KV that
+ * the previous step prepared (spc_sparse_decode_attn).
+ *
+ * Conventions shared by every call:
+ *   - All tensors are row-major, contiguous, and live in device memory unless
+ *     a comment says otherwise. bf16 values are bfloat16 bit patterns
+ *     (uint16). d (head dimension) must be 128.
+ *   - The caller owns every buffer. The library never allocates or frees
+ *     memory and keeps no per-call state: scratch space comes from the
+ *     caller's workspace.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy
+ *     default stream). Arguments are validated on the host before anything is
+ *     launched; a rejected call launches nothing and returns a negative code.
+ *   - Returns SPC_OK or a negative spc_status. An error raised by a kernel
+ *     after launch surfaces at the caller's next synchronisation (CUDA error)
+ *     or in the workspace status word (spc_score_select).
+ *   - Calls on the same stream may be captured into a CUDA graph once each
+ *     entry point has been called once outside capture (the first call sets
+ *     kernel attributes).
+ */
+#ifndef SPC_H_
+#define SPC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum spc_status {
+  SPC_OK = 0,
+  SPC_ERR_INVALID_ARG = -1, /* null or misaligned pointer, bad flag          */
+  SPC_ERR_SHAPE = -2,       /* unsupported or inconsistent sizes            */
+  SPC_ERR_CUDA = -3,        /* a CUDA runtime call or a launch failed        */
+  SPC_ERR_TIMEOUT = -4,     /* a device-side wait gave up (status word only) */
+  SPC_ERR_WORKSPACE = -5,   /* workspace missing or too small                */
+  SPC_ERR_OVERFLOW = -6     /* appending would exceed the capacity (status)  */
+} spc_status;
+
+/* Limits checked on the host. */
+#define SPC_HEAD_DIM 128
+#define SPC_MAX_CAP 262144      /* positions per request                      */
+#define SPC_MAX_BUDGET 4096     /* KV budget per KV head                       */
+#define SPC_MAX_BATCH 64
+#define SPC_MAX_GROUP 64        /* query heads per KV head (1,2,4,8,16,32,64) */
+
+/* Human-readable name of a status code. Never NULL. */
+const char* spc_status_string(int status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int spc_version(void);
+
+/* ------------------------------------------------------------------------
+ * Retrieval head: projection, per-head softmax over the context, GQA group
+ * max, forced set + Top-K.
+ *   [Blog] §5 (C1): the head keeps the embedding and the Q/K projections and
+ *   computes attention weights; selection is per head; for GQA the weights of
+ *   a group's query heads are combined by an element-wise max and Top-K is
+ *   taken per group; MQA is one group. [Summary] §4.3 (same, "attention
+ *   weights"). [Blog] §2: softmax(QK^T/sqrt(d)); the KV budget K is the number
+ *   of positions kept per head per step. Sinks and recent window:
+ *   [SparseSpec-L], [Summary] §2.2 (StreamingLLM's initial tokens + window).
+ *
+ * Computes, for every request b and KV head g (G = n_q / n_kv):
+ *   q[b,h,:]   = x_b . Wq[:, h*d:(h+1)*d]                     (fp32, unrounded)
+ *   if append and len[b] < cap:
+ *     K_dlm[b,g,len[b],:] = bf16_rne(x_b . Wk[:, g*d:(g+1)*d]);  len[b] += 1
+ *   P_h[p]     = softmax_p(q[b,h] . K_dlm[b,g(h),p] / sqrt(d)),  p < len[b]
+ *   s_g[p]     = max_{h in g} P_h[p]
+ *   selected[b,g,:] = all p < len (if len <= budget), else
+ *                     F U top_{budget-|F|}{ s_g[p] : p not in F },
+ *                     F = {0..n_sink-1} U {len-n_recent..len-1};
+ *                     ties go to the lower position; ascending; -1 padded.
+ *
+ * x          bf16 [B][H] head input of this step.
+ * Wq         bf16 [H][n_q*d]; Wk bf16 [H][n_kv*d] (may be NULL if !append).
+ * K_dlm      bf16 [B][n_kv][cap][d] key cache of the retrieval head, 16-byte
+ *            aligned; row len[b] of every head is written when appending.
+ * len        int32 [B] context lengths, device memory; read at the start,
+ *            incremented by one per request when appending (after every
+ *            kernel of this call has read it).
+ * q_out      optional fp32 [B][n_q][d] projected queries (NULL: not written).
+ * scores_out optional fp32 [B][n_kv][cap]: s_g[p] for p < len (NULL: not
+ *            written; entries p >= len are left untouched).
+ * selected   int32 [B][n_kv][budget] output.
+ * workspace  device scratch of at least spc_score_select_workspace_size()
+ *            bytes, 256-byte aligned, ZERO-FILLED BEFORE ITS FIRST USE; every
+ *            call leaves it ready for the next one. Its first int32 is the
+ *            device status word: 0, or SPC_ERR_TIMEOUT / SPC_ERR_OVERFLOW set
+ *            by a kernel; the caller reads and clears it.
+ * Limits: d = 128; n_q % n_kv == 0 with G in {1,2,4,8,16,32,64}; H % 8 == 0;
+ *         1 <= B <= 64; 1 <= budget <= min(cap, 4096); cap <= 262144;
+ *         n_sink + n_recent <= budget.
+ * Concurrent calls must use distinct workspaces.
+ * ---------------------------------------------------------------------- */
+size_t spc_score_select_workspace_size(int B, int H, int n_q, int n_kv, int d, int cap,
+                                       int budget);
+
+int spc_score_select(const void* x, const void* Wq, const void* Wk, void* K_dlm, int32_t* len,
+                     int append, int B, int H, int n_q, int n_kv, int d, int cap, int budget,
+                     int n_sink, int n_recent, float* q_out, float* scores_out,
+                     int32_t* selected, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Elastic loading: the set difference between the new selection and the
+ * resident slots. [Blog] §6 (C2): to_load = S_now - S_last, worked example
+ * S_last={1,8,21,35}, S_now={1,8,21,50} -> {50}; [Summary] §5.4: reuse the
+ * resident entries, fetch only the absent ones, in place under a fixed budget.
+ *
+ * Per (b, g), with S = {selected[b,g,i] >= 0} and slot s holding
+ * slot_pos_prev[b,g,s] (-1 = empty):
+ *   kept  = slots whose position is in S (their position is unchanged);
+ *   free  = all other slots, ascending slot index;
+ *   loads = S minus the kept positions, in the order they appear in
+ *           `selected` (ascending positions for spc_score_select's output);
+ *   load i goes to free slot i: load_slot[i], load_pos[i], i < n_load[b,g];
+ *   slot_pos_next = slot_pos_prev with each free slot set to its load, or -1.
+ *
+ * selected       int32 [B][n_kv][budget]; distinct positions or -1; positions
+ *                outside [0, cap) are ignored.
+ * slot_pos_prev  int32 [B][n_kv][budget]; distinct positions or -1.
+ * slot_pos_next  int32 [B][n_kv][budget] output; may alias slot_pos_prev.
+ * load_slot, load_pos int32 [B][n_kv][budget] outputs (entries >= n_load are
+ *                not written); n_load int32 [B][n_kv] output.
+ * A second call with the same selection and the new slot map yields n_load = 0.
+ * Limits: budget <= 4096, cap <= 262144.
+ * ---------------------------------------------------------------------- */
+int spc_elastic_diff(const int32_t* selected, const int32_t* slot_pos_prev,
+                     int32_t* slot_pos_next, int32_t* load_slot, int32_t* load_pos,
+                     int32_t* n_load, int B, int n_kv, int budget, int cap, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Gather of the missing K/V rows from pinned host memory into the resident
+ * slots, in place, by a kernel that reads host memory directly (no copy
+ * engine). [Blog] §4 (asynchronous prefetcher on another CUDA stream), §7
+ * (an offloaded layer keeps a budget-sized workspace in GPU memory);
+ * [Summary] §5.1 (prefetch concurrent with compute), §5.4 (in place).
+ *
+ * For model layers l in [layer_lo, layer_hi) held in host memory by request b
+ * (view.layer0 <= l < view.layer0 + view.n_layers), for kv in {K, V}, KV head
+ * g and i < n_load[b,g]:
+ *   slots[l', kv, g, load_slot[b,g,i], :] = host[l', kv, g, load_pos[b,g,i], :]
+ * with l' = l - view.layer0. Each row is d bf16 (256 bytes), copied bit-exact.
+ *
+ * views      device array [B] of spc_gather_view.
+ * host       device-visible address of mapped pinned host memory (see
+ *            spc_host_device_pointer), bf16 [n_layers][2][n_kv][cap][d],
+ *            16-byte aligned.
+ * slots      device memory bf16 [n_layers][2][n_kv][budget][d], 16-byte aligned.
+ * The slots being overwritten must not be read concurrently: order this call
+ * after the attention that reads the previous contents (an event).
+ * Limits: B * n_kv <= 1024, budget <= 4096.
+ * ---------------------------------------------------------------------- */
+typedef struct spc_gather_view {
+  const void* host;
+  void* slots;
+  int32_t layer0;
+  int32_t n_layers;
+  int64_t reserved;
+} spc_gather_view;
+
+int spc_gather_kv(const spc_gather_view* views, int layer_lo, int layer_hi,
+                  const int32_t* load_slot, const int32_t* load_pos, const int32_t* n_load,
+                  int B, int n_kv, int d, int cap, int budget, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Sparse GQA decode attention over the resident budget. [Blog] §2 formula
+ * over the kept rows; §4: the LLM forward uses the sparse KV prepared in the
+ * previous iteration; [Summary] §4.3: for GQA the selected KV serves every
+ * query head of its group.
+ *
+ * For layers l < n_layers, request b, query head h (g = h / G):
+ *   rows R = { i : slot_pos[b,g,i] >= 0 }     (view.use_slots = 1: row i of
+ *                                              the view is slot i)
+ *          = { selected[b,g,i] : >= 0 }       (view.use_slots = 0: positions
+ *                                              into a full cache)
+ *   out[l,b,h,:] = sum_{r in R} softmax_r(scale * q[l,b,h] . K[g,r]) V[g,r]
+ *   (zeros when R is empty).
+ *
+ * q          bf16 [n_layers][B][n_q][d] LLM queries.
+ * views      device array [n_layers][B] of spc_kv_view; k, v point at
+ *            bf16 [n_kv][rows][d], 16-byte aligned.
+ * selected, slot_pos int32 [B][n_kv][budget] (shared by all layers).
+ * out        fp32 [n_layers][B][n_q][d].
+ * workspace  device scratch of spc_sparse_decode_attn_workspace_size() bytes,
+ *            256-byte aligned, ZERO-FILLED BEFORE ITS FIRST USE (calls leave
+ *            it ready).
+ * Limits: d = 128, G in {1,2,4,8,16,32,64}, budget <= 4096.
+ * ---------------------------------------------------------------------- */
+typedef struct spc_kv_view {
+  const void* k;
+  const void* v;
+  int64_t rows;
+  int32_t use_slots;
+  int32_t reserved;
+} spc_kv_view;
+
+size_t spc_sparse_decode_attn_workspace_size(int n_layers, int B, int n_q, int n_kv, int d,
+                                             int budget);
+
+int spc_sparse_decode_attn(const void* q, const spc_kv_view* views, const int32_t* selected,
+                           const int32_t* slot_pos, int n_layers, int B, int n_q, int n_kv,
+                           int d, int budget, float scale, float* out, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Helpers (no counterpart on the pages).
+ * ---------------------------------------------------------------------- */
+
+/* Device-visible address of pinned host memory allocated with
+ * cudaHostAlloc/cudaMallocHost or registered with cudaHostRegister
+ * (cudaHostGetDevicePointer). Returns SPC_ERR_CUDA for other memory. */
+int spc_host_device_pointer(void* host_ptr, void** device_ptr);
+
+/* Streams `bytes` (a multiple of 16) from `src` (device memory or a
+ * device-visible host address) with 16-byte loads over `n_blocks` CTAs of 512
+ * threads, folding the data into sink[blockIdx] so no load is dropped. Used to
+ * measure the HBM and host-link read bandwidth the kernels are compared with.
+ * sink: uint32 [n_blocks]. src 16-byte aligned. */
+int spc_stream_read(const void* src, size_t bytes, uint32_t* sink, int n_blocks, void* stream);
+
+/* Number of streaming multiprocessors of the current device (0 on error). */
+int spc_device_sm_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPC_H_ */

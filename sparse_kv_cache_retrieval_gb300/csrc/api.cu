@@ -1,0 +1,184 @@
+// C ABI entry points of libspc: argument validation on the host, then the
+// launches. Every check runs before any CUDA call, so a rejected call touches
+// neither the device nor the stream.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "spc.h"
+#include "spc_device.cuh"
+#include "spc_internal.h"
+
+namespace spc {
+
+int device_sm_count() {
+  static int cached_dev = -1, cached = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev != cached_dev) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached = n;
+    cached_dev = dev;
+  }
+  return cached;
+}
+
+// ---------------------------------------------------------------- stream read
+__global__ void __launch_bounds__(512) stream_read_kernel(const uint4* __restrict__ src, size_t n16,
+                                                          uint32_t* sink) {
+  uint32_t acc = 0;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < n16; i += 4 * stride) {
+    const uint4 a = ldg_stream(src + i), b = ldg_stream(src + i + stride);
+    const uint4 c = ldg_stream(src + i + 2 * stride), d = ldg_stream(src + i + 3 * stride);
+    acc ^= a.x ^ a.y ^ a.z ^ a.w ^ b.x ^ b.y ^ b.z ^ b.w ^ c.x ^ c.y ^ c.z ^ c.w ^ d.x ^ d.y ^ d.z ^ d.w;
+  }
+  for (; i < n16; i += stride) {
+    const uint4 a = ldg_stream(src + i);
+    acc ^= a.x ^ a.y ^ a.z ^ a.w;
+  }
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) acc ^= __shfl_xor_sync(0xffffffffu, acc, m);
+  __shared__ uint32_t s[16];
+  if ((threadIdx.x & 31) == 0) s[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t r = 0;
+    for (int w = 0; w < 16; ++w) r ^= s[w];
+    sink[blockIdx.x] = r;
+  }
+}
+
+int stream_read_launch(const void* src, size_t bytes, uint32_t* sink, int n_blocks, void* stream) {
+  stream_read_kernel<<<n_blocks, 512, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(src), bytes / 16, sink);
+  return cudaGetLastError() == cudaSuccess ? SPC_OK : SPC_ERR_CUDA;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static bool group_ok(int n_q, int n_kv) {
+  if (n_q < 1 || n_kv < 1 || n_q % n_kv) return false;
+  const int G = n_q / n_kv;
+  return G == 1 || G == 2 || G == 4 || G == 8 || G == 16 || G == 32 || G == 64;
+}
+
+}  // namespace spc
+
+using namespace spc;
+
+extern "C" {
+
+const char* spc_status_string(int status) {
+  switch (status) {
+    case SPC_OK: return "ok";
+    case SPC_ERR_INVALID_ARG: return "invalid argument (null or misaligned pointer, bad flag)";
+    case SPC_ERR_SHAPE: return "unsupported or inconsistent sizes";
+    case SPC_ERR_CUDA: return "CUDA runtime or launch error";
+    case SPC_ERR_TIMEOUT: return "a device-side wait timed out";
+    case SPC_ERR_WORKSPACE: return "workspace missing or too small";
+    case SPC_ERR_OVERFLOW: return "append would exceed the cache capacity";
+    default: return "unknown status";
+  }
+}
+
+int spc_version(void) { return 100; }
+
+int spc_device_sm_count(void) { return device_sm_count(); }
+
+size_t spc_score_select_workspace_size(int B, int H, int n_q, int n_kv, int d, int cap, int budget) {
+  (void)budget;
+  if (B < 1 || B > SPC_MAX_BATCH || H < 1 || d != SPC_HEAD_DIM || !group_ok(n_q, n_kv) || cap < 1)
+    return 0;
+  return score_select_workspace(B, H, n_q, n_kv, cap);
+}
+
+int spc_score_select(const void* x, const void* Wq, const void* Wk, void* K_dlm, int32_t* len,
+                     int append, int B, int H, int n_q, int n_kv, int d, int cap, int budget,
+                     int n_sink, int n_recent, float* q_out, float* scores_out,
+                     int32_t* selected, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!x || !Wq || !K_dlm || !len || !selected) return SPC_ERR_INVALID_ARG;
+  if (append != 0 && append != 1) return SPC_ERR_INVALID_ARG;
+  if (append && !Wk) return SPC_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(Wq) || (Wk && !aligned16(Wk)) || !aligned16(K_dlm) ||
+      (q_out && !aligned16(q_out)))
+    return SPC_ERR_INVALID_ARG;
+  if (d != SPC_HEAD_DIM || !group_ok(n_q, n_kv)) return SPC_ERR_SHAPE;
+  if (B < 1 || B > SPC_MAX_BATCH || H < 8 || H % 8) return SPC_ERR_SHAPE;
+  if (cap < 1 || cap > SPC_MAX_CAP) return SPC_ERR_SHAPE;
+  if (budget < 1 || budget > SPC_MAX_BUDGET || budget > cap) return SPC_ERR_SHAPE;
+  if (n_sink < 0 || n_recent < 0 || n_sink + n_recent > budget) return SPC_ERR_SHAPE;
+  const size_t need = score_select_workspace(B, H, n_q, n_kv, cap);
+  if (!workspace || workspace_bytes < need) return SPC_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SPC_ERR_INVALID_ARG;
+  ScoreSelectCall c{};
+  c.x = x; c.Wq = Wq; c.Wk = Wk; c.K_dlm = K_dlm; c.len = len; c.append = append;
+  c.B = B; c.H = H; c.n_q = n_q; c.n_kv = n_kv; c.cap = cap; c.budget = budget;
+  c.n_sink = n_sink; c.n_recent = n_recent; c.q_out = q_out; c.scores_out = scores_out;
+  c.selected = selected; c.workspace = workspace; c.stream = stream;
+  return score_select_launch(c);
+}
+
+int spc_elastic_diff(const int32_t* selected, const int32_t* slot_pos_prev, int32_t* slot_pos_next,
+                     int32_t* load_slot, int32_t* load_pos, int32_t* n_load, int B, int n_kv,
+                     int budget, int cap, void* stream) {
+  if (!selected || !slot_pos_prev || !slot_pos_next || !load_slot || !load_pos || !n_load)
+    return SPC_ERR_INVALID_ARG;
+  if (B < 1 || n_kv < 1 || (long long)B * n_kv > 65535) return SPC_ERR_SHAPE;
+  if (budget < 1 || budget > SPC_MAX_BUDGET || cap < 1 || cap > SPC_MAX_CAP) return SPC_ERR_SHAPE;
+  return elastic_diff_launch(selected, slot_pos_prev, slot_pos_next, load_slot, load_pos, n_load, B,
+                             n_kv, budget, cap, stream);
+}
+
+int spc_gather_kv(const spc_gather_view* views, int layer_lo, int layer_hi, const int32_t* load_slot,
+                  const int32_t* load_pos, const int32_t* n_load, int B, int n_kv, int d, int cap,
+                  int budget, void* stream) {
+  if (!views || !load_slot || !load_pos || !n_load) return SPC_ERR_INVALID_ARG;
+  if (d != SPC_HEAD_DIM) return SPC_ERR_SHAPE;
+  if (B < 1 || B > SPC_MAX_BATCH || n_kv < 1 || B * n_kv > 1024) return SPC_ERR_SHAPE;
+  if (layer_lo < 0 || layer_hi < layer_lo) return SPC_ERR_SHAPE;
+  if (budget < 1 || budget > SPC_MAX_BUDGET || cap < 1 || cap > SPC_MAX_CAP) return SPC_ERR_SHAPE;
+  return gather_launch(views, layer_lo, layer_hi, load_slot, load_pos, n_load, B, n_kv, cap, budget,
+                       stream);
+}
+
+size_t spc_sparse_decode_attn_workspace_size(int n_layers, int B, int n_q, int n_kv, int d, int budget) {
+  if (n_layers < 1 || B < 1 || d != SPC_HEAD_DIM || !group_ok(n_q, n_kv) || budget < 1) return 0;
+  return attn_workspace(n_layers, B, n_q, n_kv, budget);
+}
+
+int spc_sparse_decode_attn(const void* q, const spc_kv_view* views, const int32_t* selected,
+                           const int32_t* slot_pos, int n_layers, int B, int n_q, int n_kv, int d,
+                           int budget, float scale, float* out, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  if (!q || !views || !selected || !slot_pos || !out) return SPC_ERR_INVALID_ARG;
+  if (d != SPC_HEAD_DIM || !group_ok(n_q, n_kv)) return SPC_ERR_SHAPE;
+  if (n_layers < 1 || B < 1 || B > SPC_MAX_BATCH || (long long)n_layers * B > 65535) return SPC_ERR_SHAPE;
+  if (n_kv > 65535 || budget < 1 || budget > SPC_MAX_BUDGET) return SPC_ERR_SHAPE;
+  if (!(scale > 0.f)) return SPC_ERR_INVALID_ARG;
+  const size_t need = attn_workspace(n_layers, B, n_q, n_kv, budget);
+  if (!workspace || workspace_bytes < need) return SPC_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SPC_ERR_INVALID_ARG;
+  return attn_launch(q, views, selected, slot_pos, n_layers, B, n_q, n_kv, budget, scale, out,
+                     workspace, stream);
+}
+
+int spc_host_device_pointer(void* host_ptr, void** device_ptr) {
+  if (!host_ptr || !device_ptr) return SPC_ERR_INVALID_ARG;
+  void* p = nullptr;
+  if (cudaHostGetDevicePointer(&p, host_ptr, 0) != cudaSuccess) {
+    cudaGetLastError();
+    return SPC_ERR_CUDA;
+  }
+  *device_ptr = p;
+  return SPC_OK;
+}
+
+int spc_stream_read(const void* src, size_t bytes, uint32_t* sink, int n_blocks, void* stream) {
+  if (!src || !sink || !aligned16(src)) return SPC_ERR_INVALID_ARG;
+  if (bytes % 16 || n_blocks < 1 || n_blocks > 65535) return SPC_ERR_SHAPE;
+  return stream_read_launch(src, bytes, sink, n_blocks, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,110 @@
+// Gather of the missing K/V rows from pinned host memory into the resident
+// HBM slots, in place, without the copy engines.
+//
+// Method: "ASPLOS'26 | SpeContext 让小模型先圈出重要 KV Cache" (marsggbo blog)
+// §4 (the asynchronous prefetcher moves the missing KV from CPU to GPU on a
+// second CUDA stream), §6 (only S_now - S_last is moved), §7 (an offloaded
+// layer keeps a budget-sized workspace on the GPU); "SpeContext: Enabling
+// Efficient Long-context Reasoning with Speculative Context Sparsity in LLMs"
+// (paperlayer.ai summary) §5.1, §5.4 (loads performed in place).
+//
+// GB300 design: the host store is mapped pinned memory read over the
+// NVLink-C2C / PCIe link by ordinary 16-byte loads. A work item is one
+// 256-byte row (one layer, K or V, one KV head, one position) copied by a
+// half-warp; items are laid out (layer, K/V, flattened load index) and spread
+// over a grid-stride loop with 4 rows in flight per half-warp, so the link
+// sees thousands of independent 256-byte reads at once. The flattened load
+// index j maps back to (request, KV head, i) through a prefix sum of n_load
+// kept in shared memory.
+#include "spc_device.cuh"
+#include "spc_internal.h"
+
+namespace spc {
+
+constexpr int kGatherThreads = 256;
+constexpr int kGatherUnroll = 4;
+constexpr int kGatherMaxSeg = 1024;
+
+__global__ void __launch_bounds__(kGatherThreads)
+gather_kernel(const spc_gather_view* __restrict__ views, int layer_lo, int layer_hi,
+              const int32_t* __restrict__ load_slot, const int32_t* __restrict__ load_pos,
+              const int32_t* __restrict__ n_load, int B, int n_kv, int cap, int K) {
+  __shared__ int pre[kGatherMaxSeg + 1];
+  __shared__ int scratch[33];
+  __shared__ spc_gather_view sv[SPC_MAX_BATCH];
+  const int nseg = B * n_kv;
+  const int tid = threadIdx.x;
+
+  for (int i = tid; i < B; i += kGatherThreads) sv[i] = views[i];
+  int run = 0;
+  for (int c0 = 0; c0 < nseg; c0 += kGatherThreads) {
+    const int v = (c0 + tid < nseg) ? n_load[c0 + tid] : 0;
+    int tot;
+    const int ex = block_excl_scan(v, scratch, &tot);
+    if (c0 + tid < nseg) pre[c0 + tid] = run + ex;
+    run += tot;
+  }
+  if (tid == 0) pre[nseg] = run;
+  __syncthreads();
+
+  const int R = run;
+  const long long per_layer = 2ll * R;
+  const long long total = (long long)(layer_hi - layer_lo) * per_layer;
+  const int l16 = tid & 15;
+  const long long hw0 = ((long long)blockIdx.x * kGatherThreads + tid) >> 4;
+  const long long nhw = ((long long)gridDim.x * kGatherThreads) >> 4;
+
+  for (long long item0 = hw0; item0 < total; item0 += nhw * kGatherUnroll) {
+    uint4 v[kGatherUnroll];
+    uint16_t* dst[kGatherUnroll];
+#pragma unroll
+    for (int u = 0; u < kGatherUnroll; ++u) {
+      dst[u] = nullptr;
+      const long long item = item0 + u * nhw;
+      if (item >= total) continue;
+      const long long lq = item / per_layer;
+      const int layer = layer_lo + (int)lq;
+      const int rem = (int)(item - lq * per_layer);
+      const int kv = rem >= R ? 1 : 0;
+      const int j = rem - kv * R;
+      // largest seg with pre[seg] <= j (segments with no load have equal bounds)
+      int lo = 0, hi = nseg - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pre[mid] <= j) lo = mid; else hi = mid - 1;
+      }
+      const int seg = lo, i = j - pre[seg];
+      const int b = seg / n_kv, g = seg - b * n_kv;
+      const spc_gather_view vw = sv[b];
+      const int lrel = layer - vw.layer0;
+      if (lrel < 0 || lrel >= vw.n_layers) continue;
+      const size_t li = (size_t)seg * K + i;
+      const int pos = load_pos[li];
+      const int slot = load_slot[li];
+      const size_t hrow = (((size_t)lrel * 2 + kv) * n_kv + g) * cap + pos;
+      const size_t srow = (((size_t)lrel * 2 + kv) * n_kv + g) * K + slot;
+      v[u] = ldg_stream(static_cast<const uint16_t*>(vw.host) + hrow * kD + l16 * 8);
+      dst[u] = static_cast<uint16_t*>(vw.slots) + srow * kD + l16 * 8;
+    }
+#pragma unroll
+    for (int u = 0; u < kGatherUnroll; ++u)
+      if (dst[u]) stg_v4(dst[u], v[u]);
+  }
+}
+
+int gather_launch(const spc_gather_view* views, int layer_lo, int layer_hi, const int32_t* load_slot,
+                  const int32_t* load_pos, const int32_t* n_load, int B, int n_kv, int cap,
+                  int budget, void* stream) {
+  if (layer_hi <= layer_lo) return SPC_OK;
+  const long long max_items = (long long)(layer_hi - layer_lo) * 2 * B * n_kv * budget;
+  const long long per_block = (kGatherThreads / 16) * kGatherUnroll;
+  long long grid = (max_items + per_block - 1) / per_block;
+  const long long cap_grid = 8ll * device_sm_count();
+  if (grid > cap_grid) grid = cap_grid;
+  if (grid < 1) grid = 1;
+  gather_kernel<<<(int)grid, kGatherThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      views, layer_lo, layer_hi, load_slot, load_pos, n_load, B, n_kv, cap, budget);
+  return cudaGetLastError() == cudaSuccess ? SPC_OK : SPC_ERR_CUDA;
+}
+
+}  // namespace spc

@@ -1,0 +1,717 @@
+// Retrieval head on GB300: Q/K projection, key scan with per-head logsumexp
+// partials, GQA group score and forced-set + Top-K selection.
+//
+// Method: "ASPLOS'26 | SpeContext 让小模型先圈出重要 KV Cache" (marsggbo blog)
+// §5 (C1 lightweight retrieval head: keep the Q/K projections and the
+// attention weights; head-level selection; GQA takes an element-wise max over
+// a group's query heads, then Top-K per group; MQA is one group) and §2
+// (softmax(QK^T/sqrt(d)), Top-K under the KV budget); "SpeContext: Enabling
+// Efficient Long-context Reasoning with Speculative Context Sparsity in LLMs"
+// (paperlayer.ai summary) §4.3. Forced sinks + recent window: SparseSpec-L news
+// post and the same summary §2.2.
+//
+// GB300 design:
+//  * proj_kernel: split-K GEMV over [W_q | W_k] (HBM-bound on the weights at
+//    small batch), 16-byte loads, deterministic last-block reduction of the
+//    split partials; the appended key row is rounded to bf16 and written in
+//    place.
+//  * scan_kernel: persistent CTAs; one producer warp streams 32 KiB tiles of
+//    128 consecutive key rows into a 3-stage shared-memory ring with
+//    cp.async.bulk (TMA engine, mbarrier completion); 4 consumer warps form
+//    the dot products on CUDA cores (q in registers, fp32 accumulate) with a
+//    lane-rotated row order so that a half-warp reduce-scatter needs no
+//    selects; base-2 logits go to scratch and per-warp (max, sum 2^(l-max))
+//    partials give the logsumexp.
+//  * select_kernel: one thread-block cluster (up to 8 CTAs) per (request,
+//    KV head); keys live in shared memory; the logsumexp partials, the 4
+//    radix-select histograms (8-bit digits, warp-aggregated with match.any)
+//    and the compaction counts are combined across the cluster through
+//    distributed shared memory; the ordered compaction keeps positions
+//    ascending and resolves ties at the K-th key to the lower position.
+#include <cooperative_groups.h>
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "spc_device.cuh"
+#include "spc_internal.h"
+
+namespace cg = cooperative_groups;
+
+namespace spc {
+
+__device__ __forceinline__ int effective_len(const int32_t* len, int b, int append, int cap) {
+  int L = len[b];
+  L = L < 0 ? 0 : (L > cap ? cap : L);
+  return (append && L < cap) ? L + 1 : L;
+}
+
+// ============================================================== projection
+struct ProjArgs {
+  const uint16_t* x;
+  const uint16_t* Wq;
+  const uint16_t* Wk;
+  uint16_t* K_dlm;
+  const int32_t* len;
+  float* q_ws;
+  float* q_out;
+  float* part;
+  uint32_t* counters;
+  int* status;
+  int B, H, Nq, Nk, Ntot, n_kv, cap, S, Hc;
+};
+
+constexpr int kProjThreads = 256;
+constexpr int kProjTile = 128;
+constexpr int kProjBB = 16;  // batch rows per block (grid.z covers B)
+
+template <int BB>
+__device__ __forceinline__ void proj_fma(float (&acc)[BB][8], const uint4& w, const float* xr) {
+  float v[8];
+  unpack8(w, v);
+#pragma unroll
+  for (int bb = 0; bb < BB; ++bb) {
+    const float xv = xr[bb];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[bb][e] = fmaf(v[e], xv, acc[bb][e]);
+  }
+}
+
+template <int BB>
+__global__ void __launch_bounds__(kProjThreads) proj_kernel(ProjArgs a) {
+  extern __shared__ float psm[];
+  __shared__ int s_last;
+  const int tile = blockIdx.x, split = blockIdx.y, b0 = blockIdx.z * BB;
+  const int col0 = tile * kProjTile;
+  const bool is_k = col0 >= a.Nq;
+  const uint16_t* W = is_k ? a.Wk : a.Wq;
+  const int ld = is_k ? a.Nk : a.Nq;
+  const int wcol0 = is_k ? col0 - a.Nq : col0;
+  const int r_begin = split * a.Hc;
+  const int nr = max(0, min(a.H, r_begin + a.Hc) - r_begin);
+
+  float* xs = psm;                       // [Hc][BB]
+  float* red = psm + a.Hc * BB;          // [8 warps][BB][128]
+  for (int i = threadIdx.x; i < nr * BB; i += kProjThreads) {
+    const int r = i / BB, bb = i - r * BB, b = b0 + bb;
+    xs[i] = (b < a.B) ? __uint_as_float(uint32_t(a.x[(size_t)b * a.H + r_begin + r]) << 16) : 0.f;
+  }
+  __syncthreads();
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, l16 = lane & 15;
+  float acc[BB][8];
+#pragma unroll
+  for (int bb = 0; bb < BB; ++bb)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[bb][e] = 0.f;
+
+  const uint16_t* wp = W + (size_t)r_begin * ld + wcol0 + l16 * 8;
+  int r = warp * 2 + (lane >> 4);
+  for (; r + 48 < nr; r += 64) {
+    const uint4 w0 = ldg_stream(wp + (size_t)r * ld);
+    const uint4 w1 = ldg_stream(wp + (size_t)(r + 16) * ld);
+    const uint4 w2 = ldg_stream(wp + (size_t)(r + 32) * ld);
+    const uint4 w3 = ldg_stream(wp + (size_t)(r + 48) * ld);
+    proj_fma<BB>(acc, w0, xs + r * BB);
+    proj_fma<BB>(acc, w1, xs + (r + 16) * BB);
+    proj_fma<BB>(acc, w2, xs + (r + 32) * BB);
+    proj_fma<BB>(acc, w3, xs + (r + 48) * BB);
+  }
+  for (; r < nr; r += 16) proj_fma<BB>(acc, ldg_stream(wp + (size_t)r * ld), xs + r * BB);
+
+  // the two half-warps hold the same 128 columns: fold them, then across warps
+#pragma unroll
+  for (int bb = 0; bb < BB; ++bb)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[bb][e] += __shfl_xor_sync(0xffffffffu, acc[bb][e], 16);
+  if (lane < 16) {
+#pragma unroll
+    for (int bb = 0; bb < BB; ++bb) {
+      float4* dst = reinterpret_cast<float4*>(red + (warp * BB + bb) * kProjTile + l16 * 8);
+      dst[0] = make_float4(acc[bb][0], acc[bb][1], acc[bb][2], acc[bb][3]);
+      dst[1] = make_float4(acc[bb][4], acc[bb][5], acc[bb][6], acc[bb][7]);
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < BB * kProjTile; i += kProjThreads) {
+    const int bb = i / kProjTile, c = i - bb * kProjTile;
+    if (b0 + bb >= a.B) continue;
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < kProjThreads / 32; ++w) s += red[(w * BB + bb) * kProjTile + c];
+    a.part[((size_t)split * a.B + b0 + bb) * a.Ntot + col0 + c] = s;
+  }
+
+  // deterministic cross-block reduction: the last split block of this tile
+  // sums the partials in split order and writes the result
+  __threadfence();
+  __syncthreads();
+  const int ctr = tile * gridDim.z + blockIdx.z;
+  if (threadIdx.x == 0) s_last = (atomicAdd(&a.counters[ctr], 1u) == (uint32_t)(a.S - 1));
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int i = threadIdx.x; i < BB * kProjTile; i += kProjThreads) {
+    const int bb = i / kProjTile, c = i - bb * kProjTile, b = b0 + bb;
+    if (b >= a.B) continue;
+    float s = 0.f;
+    for (int sp = 0; sp < a.S; ++sp) s += __ldcg(a.part + ((size_t)sp * a.B + b) * a.Ntot + col0 + c);
+    if (!is_k) {
+      a.q_ws[(size_t)b * a.Nq + col0 + c] = s;
+      if (a.q_out) a.q_out[(size_t)b * a.Nq + col0 + c] = s;
+    } else {
+      const int g = wcol0 / kD;
+      const int L = a.len[b];
+      if (L >= 0 && L < a.cap) {
+        const __nv_bfloat16 h = __float2bfloat16_rn(s);
+        a.K_dlm[(((size_t)b * a.n_kv + g) * a.cap + L) * kD + c] = __bfloat16_as_ushort(h);
+      } else if (c == 0) {
+        set_status(a.status, SPC_ERR_OVERFLOW);
+      }
+    }
+  }
+  if (threadIdx.x == 0) a.counters[ctr] = 0u;
+}
+
+// ============================================================== key scan
+struct ScanArgs {
+  const uint16_t* K;
+  const float* q;
+  const int32_t* len;
+  float* logits;
+  float2* part;
+  int* status;
+  int n_q, n_kv, cap, n_tiles, total_tiles, append, n_parts;
+  float qscale;
+};
+
+constexpr int kScanRows = 128;
+constexpr int kScanCWarps = 4;
+constexpr int kScanThreads = (kScanCWarps + 1) * 32;
+constexpr int kScanStages = 3;
+constexpr uint32_t kScanTileBytes = kScanRows * kRowBytes;
+constexpr long long kWaitLimit = 4000000000ll;  // clock cycles (~2 s)
+
+template <int G>
+struct ScanShape {
+  static constexpr int HB = G < 8 ? G : 8;         // heads per register block
+  static constexpr int R = HB <= 4 ? 16 : 8;       // rows per half-warp batch
+  static constexpr int NB = 16 / R;                // batches per half-warp per tile
+  static constexpr int NHB = G / HB;
+  static constexpr int PPT = kScanCWarps * NB;     // lse partials per tile
+};
+
+template <int G>
+__global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
+  using S = ScanShape<G>;
+  extern __shared__ __align__(128) uint8_t scan_smem[];
+  uint4* tiles = reinterpret_cast<uint4*>(scan_smem);
+  uint64_t* full = reinterpret_cast<uint64_t*>(scan_smem + kScanStages * kScanTileBytes);
+  uint64_t* empty = full + kScanStages;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kScanStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kScanCWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kScanCWarps) {
+    // ---------------- producer: one lane issues the bulk copies
+    if (lane != 0) return;
+    int it = 0;
+    for (int t = blockIdx.x; t < a.total_tiles; t += gridDim.x) {
+      const int seg = t / a.n_tiles, tile = t - seg * a.n_tiles;
+      const int b = seg / a.n_kv;
+      const int L = effective_len(a.len, b, a.append, a.cap);
+      const int row0 = tile * kScanRows;
+      if (row0 >= L) continue;
+      const int nrows = min(kScanRows, L - row0);
+      const int s = it % kScanStages;
+      const uint32_t ph = (it / kScanStages) & 1;
+      if (!mbar_wait_bounded(&empty[s], ph ^ 1, kWaitLimit)) {
+        set_status(a.status, SPC_ERR_TIMEOUT);
+        break;
+      }
+      mbar_arrive_expect_tx(&full[s], nrows * kRowBytes);
+      bulk_g2s(tiles + (size_t)s * kScanRows * 16, a.K + ((size_t)seg * a.cap + row0) * kD,
+               nrows * kRowBytes, &full[s]);
+      ++it;
+    }
+    // wait (bounded) until every copy issued has landed before leaving
+    for (int k = max(0, it - kScanStages); k < it; ++k)
+      mbar_wait_bounded(&full[k % kScanStages], (k / kScanStages) & 1, kWaitLimit);
+    return;
+  }
+
+  // ---------------- consumers
+  const int hwi = warp * 2 + (lane >> 4);  // half-warp 0..7 -> rows [hwi*16, hwi*16+16)
+  const int l16 = lane & 15;
+  float qr[S::HB][8];
+  int cur_seg = -1;
+  int it = 0;
+  for (int t = blockIdx.x; t < a.total_tiles; t += gridDim.x) {
+    const int seg = t / a.n_tiles, tile = t - seg * a.n_tiles;
+    const int b = seg / a.n_kv, g = seg - b * a.n_kv;
+    const int L = effective_len(a.len, b, a.append, a.cap);
+    const int row0 = tile * kScanRows;
+    if (row0 >= L) continue;
+    const int nrows = min(kScanRows, L - row0);
+    const int s = it % kScanStages;
+    const uint32_t ph = (it / kScanStages) & 1;
+    if (!mbar_wait_bounded(&full[s], ph, kWaitLimit)) {
+      set_status(a.status, SPC_ERR_TIMEOUT);
+      break;
+    }
+    const uint4* tb = tiles + (size_t)s * kScanRows * 16;
+    const float* qg = a.q + ((size_t)b * a.n_q + (size_t)g * G) * kD + l16 * 8;
+
+    for (int bt = 0; bt < S::NB; ++bt) {
+#pragma unroll 1
+      for (int hb = 0; hb < S::NHB; ++hb) {
+        if (S::NHB > 1 || seg != cur_seg) {
+#pragma unroll
+          for (int h = 0; h < S::HB; ++h) {
+            const float4 q0 = __ldg(reinterpret_cast<const float4*>(qg + (size_t)(hb * S::HB + h) * kD));
+            const float4 q1 = __ldg(reinterpret_cast<const float4*>(qg + (size_t)(hb * S::HB + h) * kD + 4));
+            qr[h][0] = q0.x * a.qscale; qr[h][1] = q0.y * a.qscale;
+            qr[h][2] = q0.z * a.qscale; qr[h][3] = q0.w * a.qscale;
+            qr[h][4] = q1.x * a.qscale; qr[h][5] = q1.y * a.qscale;
+            qr[h][6] = q1.z * a.qscale; qr[h][7] = q1.w * a.qscale;
+          }
+        }
+        float acc[S::R][S::HB];
+        const int rbase = hwi * 16 + bt * S::R;
+#pragma unroll
+        for (int j = 0; j < S::R; ++j) {
+          // lane l16 reads chunk l16 of row (j ^ l16): conflict-free, and the
+          // reduce-scatter below then needs compile-time indices only
+          const uint4 w = tb[(rbase + (j ^ (l16 & (S::R - 1)))) * 16 + l16];
+          float v[8];
+          unpack8(w, v);
+#pragma unroll
+          for (int h = 0; h < S::HB; ++h) {
+            float d0 = v[0] * qr[h][0];
+#pragma unroll
+            for (int e = 1; e < 8; ++e) d0 = fmaf(v[e], qr[h][e], d0);
+            acc[j][h] = d0;
+          }
+        }
+        // reduce-scatter over rows: lane keeps row (j ^ l16) for j < m
+#pragma unroll
+        for (int m = S::R / 2; m >= 1; m >>= 1) {
+#pragma unroll
+          for (int j = 0; j < m; ++j)
+#pragma unroll
+            for (int h = 0; h < S::HB; ++h)
+              acc[j][h] += __shfl_xor_sync(0xffffffffu, acc[j + m][h], m);
+        }
+        // lanes l16 and l16 ^ R.. hold the same row: finish over the rest
+#pragma unroll
+        for (int m = S::R; m < 16; m <<= 1)
+#pragma unroll
+          for (int h = 0; h < S::HB; ++h) acc[0][h] += __shfl_xor_sync(0xffffffffu, acc[0][h], m);
+
+        const int rloc = rbase + (l16 & (S::R - 1));
+        const bool own = (l16 < S::R) && (rloc < nrows);
+#pragma unroll
+        for (int h = 0; h < S::HB; ++h) {
+          const int hq = g * G + hb * S::HB + h;
+          if (own) a.logits[((size_t)b * a.n_q + hq) * a.cap + row0 + rloc] = acc[0][h];
+          float mm = own ? acc[0][h] : -INFINITY;
+          float ss = own ? 1.f : 0.f;
+          warp_lse2(mm, ss);
+          if (lane == h)
+            a.part[((size_t)b * a.n_q + hq) * a.n_parts + (size_t)tile * S::PPT + warp * S::NB + bt] =
+                make_float2(mm, ss);
+        }
+      }
+    }
+    cur_seg = seg;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    ++it;
+  }
+}
+
+// ============================================================== select
+struct SelArgs {
+  const float* logits;
+  const float2* part;
+  int32_t* len;
+  float* scores_out;
+  int32_t* selected;
+  uint32_t* done;
+  int B, n_q, n_kv, G, cap, K, n_sink, n_recent, append, P, n_parts, ppt;
+};
+
+constexpr int kSelThreads = 512;
+
+__device__ __forceinline__ bool is_forced(int p, int L, int n_sink, int n_recent) {
+  return p < n_sink || p >= L - n_recent;
+}
+
+__global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a) {
+  cg::cluster_group cluster = cg::this_cluster();
+  const int C = (int)cluster.num_blocks();
+  const int cr = (int)cluster.block_rank();
+  const int seg = blockIdx.x / C;
+  const int b = seg / a.n_kv, g = seg - b * a.n_kv;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  extern __shared__ uint32_t keys[];          // [P]
+  __shared__ uint32_t hist[2][256];
+  __shared__ float lse_m[SPC_MAX_GROUP], lse_s[SPC_MAX_GROUP], lse2[SPC_MAX_GROUP];
+  __shared__ int scratch[33];
+  __shared__ int s_digit, s_rem, s_last;
+  __shared__ int s_counts[2];
+
+  const int L = effective_len(a.len, b, a.append, a.cap);
+  const int lo = cr * a.P;
+  const int hi = min(lo + a.P, L);
+  int32_t* out = a.selected + (size_t)seg * a.K;
+
+  // ---- 1. logsumexp per query head of the group, partials split over the cluster
+  const int n_valid_parts = ((L + kScanRows - 1) / kScanRows) * a.ppt;
+  for (int h = warp; h < a.G; h += kSelThreads / 32) {
+    const float2* ph = a.part + ((size_t)b * a.n_q + (size_t)g * a.G + h) * a.n_parts;
+    float m = -INFINITY, s = 0.f;
+    for (int i = cr * 32 + lane; i < n_valid_parts; i += C * 32) {
+      const float2 v = __ldcg(ph + i);
+      lse2_combine(m, s, v.x, v.y);
+    }
+    warp_lse2(m, s);
+    if (lane == 0) { lse_m[h] = m; lse_s[h] = s; }
+  }
+  cluster.sync();
+  if (tid < a.G) {
+    float m = -INFINITY, s = 0.f;
+    for (int c = 0; c < C; ++c)
+      lse2_combine(m, s, *cluster.map_shared_rank(&lse_m[tid], c), *cluster.map_shared_rank(&lse_s[tid], c));
+    lse2[tid] = (s > 0.f) ? m + log2f(s) : INFINITY;
+  }
+  __syncthreads();
+
+  // ---- 2. group score s = max_h (l_h - lse_h) (base 2) and order keys
+  const float* lg = a.logits + ((size_t)b * a.n_q + (size_t)g * a.G) * a.cap;
+  for (int i = tid; i < a.P; i += kSelThreads) {
+    const int p = lo + i;
+    uint32_t key = 0;
+    if (p < L) {
+      float sc = -INFINITY;
+      for (int h = 0; h < a.G; ++h) sc = fmaxf(sc, __ldcg(lg + (size_t)h * a.cap + p) - lse2[h]);
+      if (a.scores_out) a.scores_out[(size_t)seg * a.cap + p] = exp2f(sc);
+      if (!is_forced(p, L, a.n_sink, a.n_recent)) key = order_key(sc);
+    }
+    keys[i] = key;
+  }
+
+  if (L <= a.K) {
+    // everything fits in the budget: keep [0, L), pad with -1
+    for (int p = lo + tid; p < hi; p += kSelThreads) out[p] = p;
+    if (cr == 0)
+      for (int i = L + tid; i < a.K; i += kSelThreads) out[i] = -1;
+  } else {
+    __syncthreads();
+    // ---- 3. radix select of the (K - |F|)-th largest key, 8-bit digits
+    const int Kp = a.K - (a.n_sink + a.n_recent);
+    uint32_t prefix = 0, mask = 0;
+    int rem = Kp;
+    if (Kp > 0) {
+      for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
+        uint32_t* hb = hist[pass & 1];
+        if (tid < 256) hb[tid] = 0;
+        __syncthreads();
+        for (int base = 0; base < a.P; base += kSelThreads) {
+          const int i = base + tid;
+          const uint32_t key = i < a.P ? keys[i] : 0u;
+          const int digit = (key != 0u && (key & mask) == prefix) ? int((key >> shift) & 255u) : 256;
+          const unsigned peers = __match_any_sync(0xffffffffu, digit);
+          if (digit < 256 && lane == __ffs(peers) - 1) atomicAdd(&hb[digit], (uint32_t)__popc(peers));
+        }
+        cluster.sync();
+        // suffix counts over digits 255..0; thread t handles digit 255 - t
+        int tot = 0;
+        if (tid < 256)
+          for (int c = 0; c < C; ++c) tot += (int)*cluster.map_shared_rank(&hb[255 - tid], c);
+        const int incl = warp_incl_scan(tot);
+        if (lane == 31 && warp < 8) scratch[warp] = incl;
+        __syncthreads();
+        if (tid < 256) {
+          int before = 0;
+          for (int w = 0; w < warp; ++w) before += scratch[w];
+          const int sfx = before + incl;  // keys with digit >= 255 - tid
+          if (sfx >= rem && sfx - tot < rem) {
+            s_digit = 255 - tid;
+            s_rem = rem - (sfx - tot);
+          }
+        }
+        __syncthreads();
+        prefix |= (uint32_t)s_digit << shift;
+        mask |= 255u << shift;
+        rem = s_rem;
+        __syncthreads();
+      }
+    } else {
+      prefix = 0xffffffffu;
+      rem = 0;
+    }
+    const uint32_t T = prefix;
+    const int need_eq = rem;
+
+    // ---- 4. per-CTA counts, exchanged across the cluster
+    int n_base = 0, n_eq = 0;
+    for (int i = tid; i < a.P; i += kSelThreads) {
+      const int p = lo + i;
+      if (p >= L) break;
+      const uint32_t key = keys[i];
+      if (is_forced(p, L, a.n_sink, a.n_recent) || (key != 0u && key > T)) ++n_base;
+      else if (Kp > 0 && key != 0u && key == T) ++n_eq;
+    }
+    int tb_total, te_total;
+    block_excl_scan(n_base, scratch, &tb_total);
+    block_excl_scan(n_eq, scratch, &te_total);
+    if (tid == 0) { s_counts[0] = tb_total; s_counts[1] = te_total; }
+    cluster.sync();
+    int out_base = 0, eq_before = 0;
+    for (int c = 0; c < cr; ++c) {
+      const int cb = *cluster.map_shared_rank(&s_counts[0], c);
+      const int ce = *cluster.map_shared_rank(&s_counts[1], c);
+      const int take_c = max(0, min(need_eq - eq_before, ce));
+      out_base += cb + take_c;
+      eq_before += ce;
+    }
+    const int take = max(0, min(need_eq - eq_before, te_total));
+
+    // ---- 5. ordered compaction, 4 consecutive positions per thread per round
+    int run_eq = 0, run_sel = 0;
+    for (int base = 0; base < a.P; base += kSelThreads * 4) {
+      const int i0 = base + tid * 4;
+      uint32_t kk[4];
+      bool forced[4];
+      int ecount = 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int i = i0 + k, p = lo + i;
+        const bool in = (i < a.P) && (p < L);
+        kk[k] = in ? keys[i] : 0u;
+        forced[k] = in && is_forced(p, L, a.n_sink, a.n_recent);
+        ecount += (Kp > 0 && kk[k] != 0u && kk[k] == T) ? 1 : 0;
+      }
+      int etot;
+      int erank = run_eq + block_excl_scan(ecount, scratch, &etot);
+      bool sel[4];
+      int scount = 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const bool eq = (Kp > 0 && kk[k] != 0u && kk[k] == T);
+        const bool gt = (kk[k] != 0u && kk[k] > T);
+        sel[k] = forced[k] || gt || (eq && erank < take);
+        if (eq) ++erank;
+        scount += sel[k] ? 1 : 0;
+      }
+      int stot;
+      int srank = run_sel + block_excl_scan(scount, scratch, &stot);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (sel[k]) out[out_base + srank++] = lo + i0 + k;
+      run_eq += etot;
+      run_sel += stot;
+    }
+  }
+  // keep this CTA's shared memory alive until every remote read is done
+  cluster.sync();
+
+  if (a.append) {
+    if (tid == 0) {
+      __threadfence();
+      s_last = (atomicAdd(a.done, 1u) == gridDim.x - 1);
+    }
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      for (int bb = tid; bb < a.B; bb += kSelThreads) {
+        const int L0 = a.len[bb];
+        if (L0 >= 0 && L0 < a.cap) a.len[bb] = L0 + 1;
+      }
+      if (tid == 0) *a.done = 0u;
+    }
+  }
+}
+
+// ============================================================== host side
+struct ScoreLayout {
+  size_t status, done, counters, q, part_proj, logits, part_scan, total;
+  int S, Hc, n_col_tiles, bz, n_tiles, ppt, n_parts;
+};
+
+static int proj_splits(int H) {
+  int S = H / 512;
+  return S < 1 ? 1 : (S > 16 ? 16 : S);
+}
+
+static int scan_ppt(int G) { return kScanCWarps * ((G < 8 ? G : 8) <= 4 ? 1 : 2); }
+
+static ScoreLayout score_layout(int B, int H, int n_q, int n_kv, int cap) {
+  ScoreLayout l{};
+  const int Nq = n_q * kD, Nk = n_kv * kD, Ntot = Nq + Nk;
+  l.S = proj_splits(H);
+  l.Hc = (H + l.S - 1) / l.S;
+  l.n_col_tiles = Ntot / kProjTile;
+  l.bz = (B + kProjBB - 1) / kProjBB;
+  l.n_tiles = (cap + kScanRows - 1) / kScanRows;
+  l.ppt = scan_ppt(n_q / n_kv);
+  l.n_parts = l.n_tiles * l.ppt;
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off = (off + bytes + 255) & ~size_t(255); return o; };
+  l.status = take(2 * sizeof(int));
+  l.done = l.status + sizeof(int);
+  l.counters = take(sizeof(uint32_t) * (size_t)l.n_col_tiles * 4 /* grid.z <= 4 */);
+  l.q = take(sizeof(float) * (size_t)B * Nq);
+  l.part_proj = take(sizeof(float) * (size_t)l.S * B * Ntot);
+  l.logits = take(sizeof(float) * (size_t)B * n_q * cap);
+  l.part_scan = take(sizeof(float2) * (size_t)B * n_q * l.n_parts);
+  l.total = off;
+  return l;
+}
+
+size_t score_select_workspace(int B, int H, int n_q, int n_kv, int cap) {
+  return score_layout(B, H, n_q, n_kv, cap).total;
+}
+
+template <int G>
+static cudaError_t launch_scan(const ScanArgs& sa, int grid, cudaStream_t st) {
+  const size_t smem = kScanStages * kScanTileBytes + 2 * kScanStages * sizeof(uint64_t);
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(scan_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  scan_kernel<G><<<grid, kScanThreads, smem, st>>>(sa);
+  return cudaGetLastError();
+}
+
+template <int BB>
+static cudaError_t launch_proj(const ProjArgs& pa, dim3 grid, size_t smem, cudaStream_t st) {
+  static size_t attr = 0;
+  if (smem > attr) {
+    cudaError_t e = cudaFuncSetAttribute(proj_kernel<BB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr = smem;
+  }
+  proj_kernel<BB><<<grid, kProjThreads, smem, st>>>(pa);
+  return cudaGetLastError();
+}
+
+int score_select_launch(const ScoreSelectCall& c) {
+  const ScoreLayout l = score_layout(c.B, c.H, c.n_q, c.n_kv, c.cap);
+  uint8_t* ws = static_cast<uint8_t*>(c.workspace);
+  cudaStream_t st = static_cast<cudaStream_t>(c.stream);
+  const int G = c.n_q / c.n_kv;
+  const int Nq = c.n_q * kD, Nk = c.n_kv * kD;
+  int* status = reinterpret_cast<int*>(ws + l.status);
+  cudaError_t e;
+
+  // ---- projection
+  {
+    ProjArgs pa{};
+    pa.x = static_cast<const uint16_t*>(c.x);
+    pa.Wq = static_cast<const uint16_t*>(c.Wq);
+    pa.Wk = static_cast<const uint16_t*>(c.Wk);
+    pa.K_dlm = static_cast<uint16_t*>(c.K_dlm);
+    pa.len = c.len;
+    pa.q_ws = reinterpret_cast<float*>(ws + l.q);
+    pa.q_out = c.q_out;
+    pa.part = reinterpret_cast<float*>(ws + l.part_proj);
+    pa.counters = reinterpret_cast<uint32_t*>(ws + l.counters);
+    pa.status = status;
+    pa.B = c.B; pa.H = c.H; pa.Nq = Nq; pa.Nk = Nk; pa.Ntot = Nq + Nk; pa.n_kv = c.n_kv;
+    pa.cap = c.cap; pa.S = l.S; pa.Hc = l.Hc;
+    const int n_tiles = (Nq + (c.append ? Nk : 0)) / kProjTile;
+    const int bb = c.B <= 1 ? 1 : c.B <= 2 ? 2 : c.B <= 4 ? 4 : c.B <= 8 ? 8 : 16;
+    const dim3 grid(n_tiles, l.S, (c.B + bb - 1) / bb);
+    const size_t smem = sizeof(float) * ((size_t)l.Hc * bb + (kProjThreads / 32) * bb * kProjTile);
+    switch (bb) {
+      case 1: e = launch_proj<1>(pa, grid, smem, st); break;
+      case 2: e = launch_proj<2>(pa, grid, smem, st); break;
+      case 4: e = launch_proj<4>(pa, grid, smem, st); break;
+      case 8: e = launch_proj<8>(pa, grid, smem, st); break;
+      default: e = launch_proj<16>(pa, grid, smem, st); break;
+    }
+    if (e != cudaSuccess) return SPC_ERR_CUDA;
+  }
+
+  // ---- key scan
+  {
+    ScanArgs sa{};
+    sa.K = static_cast<const uint16_t*>(c.K_dlm);
+    sa.q = reinterpret_cast<const float*>(ws + l.q);
+    sa.len = c.len;
+    sa.logits = reinterpret_cast<float*>(ws + l.logits);
+    sa.part = reinterpret_cast<float2*>(ws + l.part_scan);
+    sa.status = status;
+    sa.n_q = c.n_q; sa.n_kv = c.n_kv; sa.cap = c.cap; sa.n_tiles = l.n_tiles;
+    sa.total_tiles = c.B * c.n_kv * l.n_tiles; sa.append = c.append; sa.n_parts = l.n_parts;
+    sa.qscale = kLog2e / sqrtf((float)kD);
+    int grid = 2 * device_sm_count();
+    if (grid < 1) grid = 1;
+    if (grid > sa.total_tiles) grid = sa.total_tiles;
+    switch (G) {
+      case 1: e = launch_scan<1>(sa, grid, st); break;
+      case 2: e = launch_scan<2>(sa, grid, st); break;
+      case 4: e = launch_scan<4>(sa, grid, st); break;
+      case 8: e = launch_scan<8>(sa, grid, st); break;
+      case 16: e = launch_scan<16>(sa, grid, st); break;
+      case 32: e = launch_scan<32>(sa, grid, st); break;
+      default: e = launch_scan<64>(sa, grid, st); break;
+    }
+    if (e != cudaSuccess) return SPC_ERR_CUDA;
+  }
+
+  // ---- group score + select (one cluster per (request, KV head))
+  {
+    SelArgs sa{};
+    sa.logits = reinterpret_cast<const float*>(ws + l.logits);
+    sa.part = reinterpret_cast<const float2*>(ws + l.part_scan);
+    sa.len = c.len;
+    sa.scores_out = c.scores_out;
+    sa.selected = c.selected;
+    sa.done = reinterpret_cast<uint32_t*>(ws + l.done);
+    sa.B = c.B; sa.n_q = c.n_q; sa.n_kv = c.n_kv; sa.G = G; sa.cap = c.cap; sa.K = c.budget;
+    sa.n_sink = c.n_sink; sa.n_recent = c.n_recent; sa.append = c.append;
+    sa.n_parts = l.n_parts; sa.ppt = l.ppt;
+    int C = (c.cap + 8191) / 8192;
+    C = C < 1 ? 1 : (C > 8 ? 8 : C);
+    int P = (c.cap + C - 1) / C;
+    P = (P + 3) & ~3;
+    sa.P = P;
+    const size_t smem = sizeof(uint32_t) * (size_t)P;
+    static size_t attr = 0;
+    if (smem > attr) {
+      e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return SPC_ERR_CUDA;
+      attr = smem;
+    }
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(c.B * c.n_kv * C);
+    cfg.blockDim = dim3(kSelThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = C;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, select_kernel, sa);
+    if (e != cudaSuccess) return SPC_ERR_CUDA;
+  }
+  return SPC_OK;
+}
+
+}  // namespace spc

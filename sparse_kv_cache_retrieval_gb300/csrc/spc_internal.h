@@ -1,0 +1,46 @@
+// Host-side declarations shared by the translation units of libspc.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "spc.h"
+
+namespace spc {
+
+struct ScoreSelectCall {
+  const void* x;
+  const void* Wq;
+  const void* Wk;
+  void* K_dlm;
+  int32_t* len;
+  int append;
+  int B, H, n_q, n_kv, cap, budget, n_sink, n_recent;
+  float* q_out;
+  float* scores_out;
+  int32_t* selected;
+  void* workspace;
+  void* stream;
+};
+
+size_t score_select_workspace(int B, int H, int n_q, int n_kv, int cap);
+int score_select_launch(const ScoreSelectCall& c);
+
+int elastic_diff_launch(const int32_t* selected, const int32_t* prev, int32_t* next,
+                        int32_t* load_slot, int32_t* load_pos, int32_t* n_load, int B, int n_kv,
+                        int budget, int cap, void* stream);
+
+int gather_launch(const spc_gather_view* views, int layer_lo, int layer_hi, const int32_t* load_slot,
+                  const int32_t* load_pos, const int32_t* n_load, int B, int n_kv, int cap,
+                  int budget, void* stream);
+
+size_t attn_workspace(int n_layers, int B, int n_q, int n_kv, int budget);
+int attn_launch(const void* q, const spc_kv_view* views, const int32_t* selected,
+                const int32_t* slot_pos, int n_layers, int B, int n_q, int n_kv, int budget,
+                float scale, float* out, void* workspace, void* stream);
+
+int stream_read_launch(const void* src, size_t bytes, uint32_t* sink, int n_blocks, void* stream);
+
+int device_sm_count();
+
+}  // namespace spc
