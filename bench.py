@@ -1,0 +1,455 @@
+"""Decode-step benchmark of the SpeContext hot path on GB300.
+
+One step = retrieval head (projection + key scan + group score + Top-K),
+elastic diff, and for every LLM layer sparse GQA attention (stream A) and the
+in-place host gather of the next step's missing rows (stream B), exactly as a
+decode step runs; steps are captured in a CUDA graph and replayed.
+
+Default workload: batch 1, context 32768, Llama3.1-8B-shaped GQA (32/8 heads,
+d = 128), budget 2048 per KV head, 32-layer LLM KV (4 GiB) in pinned host
+memory, drift 0.9, 1% planted hot positions, seed 1 (synthetic data).
+
+Prints one JSON line. `--impl reference` times the CPU oracle instead (the
+reference arm: a plain float64 numpy implementation, single-threaded).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-step select+load+attn us/step; key-scan GB/s & gather GB/s vs roofline"
+UNIT = "us/step"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=64)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="cfg2")
+    ap.add_argument("--layers-per-launch", type=int, default=4)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-sample-steps", type=int, default=2)
+    ap.add_argument("--oracle-sample-layers", type=int, default=2)
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- distributed
+def dist_setup(n):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        sm, mx, reasons = [], 0.0, set()
+        if self.path and os.path.exists(self.path):
+            for line in open(self.path):
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    sm.append(float(f[1]))
+                    mx = max(mx, float(f[2]))
+                except ValueError:
+                    continue
+                names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+                for nm, v in zip(names, f[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(nm)
+            os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx or None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- peaks
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        return {}
+
+
+def host_link_peak(pipe, spc, torch):
+    """Zero-copy streaming read of pinned host memory, and pinned H2D memcpy."""
+    hs = next(h for h in pipe.host_stores if h is not None)
+    nbytes = min(hs.numel() * 2, 1 << 30) // 16 * 16
+    dptr = spc.spc_host_device_pointer(hs)
+    sm = spc.spc_device_sm_count()
+    best_zc = 0.0
+    for nblk in (sm * 4, sm * 8):
+        sink = torch.zeros(nblk, dtype=torch.int32, device="cuda")
+        for rep in range(4):
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            spc.spc_stream_read(dptr, nbytes, sink, nblk)
+            e.record()
+            torch.cuda.synchronize()
+            if rep:
+                best_zc = max(best_zc, nbytes / (s.elapsed_time(e) * 1e-3) / 1e9)
+    dst = torch.empty(nbytes // 2, dtype=torch.int16, device="cuda")
+    src = hs.view(-1)[: nbytes // 2]
+    best_ce = 0.0
+    for rep in range(4):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        dst.copy_(src, non_blocking=True)
+        e.record()
+        torch.cuda.synchronize()
+        if rep:
+            best_ce = max(best_ce, nbytes / (s.elapsed_time(e) * 1e-3) / 1e9)
+    del dst
+    return best_zc, best_ce
+
+
+def hbm_read_peak(spc, torch):
+    """Streaming read of a 2 GiB device buffer with the same 16-byte load kernel."""
+    n = 2 << 30
+    buf = torch.empty(n // 2, dtype=torch.int16, device="cuda")
+    buf.fill_(1)
+    sm = spc.spc_device_sm_count()
+    sink = torch.zeros(sm * 8, dtype=torch.int32, device="cuda")
+    best = 0.0
+    for rep in range(5):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        spc.spc_stream_read(buf, n, sink, sm * 8)
+        e.record()
+        torch.cuda.synchronize()
+        if rep:
+            best = max(best, n / (s.elapsed_time(e) * 1e-3) / 1e9)
+    del buf
+    return best
+
+
+# ---------------------------------------------------------------- oracle (CPU) leg
+def oracle_sample(cfg_key: str, steps: int, layers: int) -> dict:
+    """Time the oracle on a bounded sample of the workload, single-threaded.
+
+    Runs in a child process with one BLAS/OpenMP thread. The sample is the
+    full retrieval head (all positions, all heads) plus diff, gather and
+    attention for `layers` of the workload's layers; the per-layer part is
+    scaled to all layers to give us/step.
+    """
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    code = f"""
+import json, math, sys, time
+sys.path.insert(0, {ROOT!r})
+import numpy as np
+import oracle.spc_oracle as O
+from sparse_kv_cache_retrieval_gb300.configs import CONFIGS
+from sparse_kv_cache_retrieval_gb300.synth import make_inputs, fill_llm_kv
+cfg = CONFIGS[{cfg_key!r}]
+S, Ls = {steps}, {layers}
+inp = make_inputs(cfg, steps=S, n_layers=Ls)
+stores = []
+for b in range(cfg.B):
+    st = np.empty((Ls, 2, cfg.n_kv, cfg.cap, cfg.d), np.uint16)
+    fill_llm_kv(cfg, b, 0, st)
+    stores.append(st)
+ost = O.DecodeState(inp.K_dlm, inp.lens, stores, [min(g, Ls) for g in cfg.gpu_layers], cfg.budget,
+                    cfg.n_sink, cfg.n_recent)
+ost.diff_and_gather(ost.score_select(inp.x[0], inp.Wq, inp.Wk, cfg.n_q, False)[4])
+t_head = t_layers = 0.0
+for t in range(S):
+    t0 = time.perf_counter()
+    sel = ost.score_select(inp.x[t + 1], inp.Wq, inp.Wk, cfg.n_q, cfg.append)[4]
+    t1 = time.perf_counter()
+    ost.attention(inp.q_llm[t, :Ls], 1 / math.sqrt(cfg.d))
+    ost.diff_and_gather(sel)
+    t2 = time.perf_counter()
+    t_head += t1 - t0
+    t_layers += t2 - t1
+per_step_us = (t_head + t_layers * cfg.n_layers / Ls) / S * 1e6
+print(json.dumps({{"us_per_step": per_step_us, "head_s": t_head, "layers_s": t_layers}}))
+"""
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=900)
+    if r.returncode != 0:
+        raise RuntimeError("oracle sample failed:\n" + r.stderr[-2000:])
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    res["sample"] = (f"{steps} decode steps of the full workload's retrieval head (all positions and "
+                     f"heads) + diff/gather/attention on {layers} of the layers, per-layer time scaled "
+                     f"to all layers; float64 numpy, 1 thread")
+    return res
+
+
+def reference_arm(args, rank, world):
+    from sparse_kv_cache_retrieval_gb300.configs import CONFIGS, describe
+    if rank != 0:
+        return
+    cfg = CONFIGS[args.config]
+    runs = max(1, args.steps // 32) if args.steps > 0 else 1
+    t0 = time.time()
+    res = oracle_sample(args.config, args.oracle_sample_steps, args.oracle_sample_layers)
+    value = res["us_per_step"]
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.oracle_sample_steps, "warmup": 0,
+            "ms_per_step": round(value / 1e3, 3), "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": describe(cfg),
+            "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": res["sample"]},
+            "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": round(time.time() - t0, 1)}
+    del runs
+    print(json.dumps(line))
+
+
+# ---------------------------------------------------------------- our arm
+def our_arm(args, rank, world, local):
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from sparse_kv_cache_retrieval_gb300 import binding as spc
+    from sparse_kv_cache_retrieval_gb300.configs import CONFIGS, describe
+    from sparse_kv_cache_retrieval_gb300.pipeline import DecodePipeline
+    from sparse_kv_cache_retrieval_gb300.synth import make_inputs
+
+    torch.cuda.set_device(local)
+    cfg = CONFIGS[args.config]
+    W, K = max(3, args.warmup), args.steps
+    inp = make_inputs(cfg, steps=W + K)
+    pipe = DecodePipeline(cfg, inp, layers_per_launch=args.layers_per_launch, timing=True)
+    nload_hist = torch.zeros((W + K, cfg.B, cfg.n_kv), dtype=torch.int32, device="cuda")
+
+    # per-step record of n_load (a device copy node inside the graph)
+    orig_step = pipe.step
+
+    def step_with_record(t):
+        orig_step(t)
+        with torch.cuda.stream(pipe.sA):
+            nload_hist[t].copy_(pipe.n_load[(t + 1) % 2])
+    pipe.step = step_with_record
+
+    pipe.prologue()
+    g_warm = pipe.capture(0, W)
+    pipe.reset_timing()
+    g_timed = pipe.capture(W, K)
+    timed_events = list(pipe._timed)
+    g_warm.replay()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(pipe.sA)
+    g_timed.replay()
+    end.record(pipe.sA)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms_total = start.elapsed_time(end)
+    ms_total = max_over_ranks(ms_total, world)
+
+    # per-kernel times from the events inside the timed graph
+    kern = {}
+    timing_src = "events inside the timed graph"
+    try:
+        for kind, s, e in timed_events:
+            r = kern.setdefault(kind, {"launches": 0, "total_ms": 0.0})
+            r["launches"] += 1
+            r["total_ms"] += s.elapsed_time(e)
+    except RuntimeError:
+        kern = {}
+        timing_src = "separate eager pass (graph timing events unsupported)"
+        pipe.prologue()
+        pipe.reset_timing()
+        pipe.run(0, min(K, 16))
+        torch.cuda.synchronize()
+        for kind, s, e in pipe._timed:
+            r = kern.setdefault(kind, {"launches": 0, "total_ms": 0.0})
+            r["launches"] += 1
+            r["total_ms"] += s.elapsed_time(e)
+    for r in kern.values():
+        r["mean_us"] = r["total_ms"] * 1e3 / max(1, r["launches"])
+
+    # algorithmic bytes
+    nl = nload_hist[W:].cpu().numpy().astype(np.int64)           # [K][B][n_kv]
+    host_layers = np.array([cfg.n_layers - pipe.gpu_layers[b] for b in range(cfg.B)])
+    gathered = int((nl.sum(axis=2) * host_layers[None, :]).sum() * 2 * 256)
+    full_reload = int(K * cfg.B * cfg.n_kv * cfg.budget * host_layers.mean() * 2 * 256)
+    overlap = 1.0 - nl.sum() / (K * cfg.B * cfg.n_kv * min(cfg.budget, min(cfg.lens)))
+    lens_now = pipe.len.cpu().numpy()
+    scan_bytes = int(sum(int(L) for L in lens_now) * cfg.n_kv * 256)   # fixed-length workloads
+    n_gather_launches = kern.get("gather", {}).get("launches", 1)
+    rows_kept = cfg.B * cfg.n_kv * min(cfg.budget, int(min(lens_now)))
+    attn_bytes_per_layer = rows_kept * 512 + cfg.B * cfg.n_q * 128 * (2 + 4)
+    peaks = measured_peaks()
+    hbm_peak = peaks.get("hbm_gbs")
+    zc_peak, ce_peak = host_link_peak(pipe, spc, torch)
+    hbm_read = hbm_read_peak(spc, torch)
+
+    def gbs(nbytes, us):
+        return nbytes / (us * 1e-6) / 1e9 if us > 0 else 0.0
+
+    kinfo = {}
+    if "key_scan" in kern:
+        a = gbs(scan_bytes, kern["key_scan"]["mean_us"])
+        kinfo["key_scan"] = {"bound": "hbm", "achieved": round(a, 1), "peak": hbm_peak, "unit": "GB/s",
+                             "frac": round(a / hbm_peak, 3) if hbm_peak else None,
+                             "algorithmic_bytes": scan_bytes, "mean_us": round(kern["key_scan"]["mean_us"], 2)}
+    if "gather" in kern:
+        per_launch = gathered / max(1, n_gather_launches)
+        a = gbs(per_launch, kern["gather"]["mean_us"])
+        kinfo["gather"] = {"bound": "host_link", "achieved": round(a, 1), "peak": round(zc_peak, 1),
+                           "unit": "GB/s", "frac": round(a / zc_peak, 3) if zc_peak else None,
+                           "algorithmic_bytes": int(per_launch), "mean_us": round(kern["gather"]["mean_us"], 2)}
+    if "attention" in kern:
+        per_launch = attn_bytes_per_layer * args.layers_per_launch
+        a = gbs(per_launch, kern["attention"]["mean_us"])
+        kinfo["attention"] = {"bound": "hbm", "achieved": round(a, 1), "peak": hbm_peak, "unit": "GB/s",
+                              "frac": round(a / hbm_peak, 3) if hbm_peak else None,
+                              "algorithmic_bytes": per_launch, "mean_us": round(kern["attention"]["mean_us"], 2)}
+    for k in ("project", "select", "diff"):
+        if k in kern:
+            kinfo[k] = {"mean_us": round(kern[k]["mean_us"], 2), "launches": kern[k]["launches"]}
+    dominant = max(kern, key=lambda k: kern[k]["total_ms"]) if kern else None
+    roof = None
+    if dominant in ("gather", "key_scan", "attention"):
+        r = kinfo[dominant]
+        roof = {"kernel": dominant, "bound": r["bound"], "achieved": r["achieved"], "peak": r["peak"],
+                "unit": "GB/s", "frac": r["frac"], "traffic": None,
+                "peak_source": "measured in this run (zero-copy read of pinned host memory)"
+                if r["bound"] == "host_link" else "MEASURED_PEAKS.json hbm_gbs"}
+
+    us_step = ms_total * 1e3 / K
+    value = us_step / world
+
+    # e2e: same step through the public pipeline API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        pipe.step = orig_step
+        pipe.timing = False
+        pipe.enable_host_io()
+        pipe.prologue()
+        ge_w = pipe.capture(0, W)
+        ge_t = pipe.capture(W, K)
+        ge_w.replay()
+        torch.cuda.synchronize()
+        s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        s2.record(pipe.sA)
+        ge_t.replay()
+        e2.record(pipe.sA)
+        torch.cuda.synchronize()
+        ms_e2e = max_over_ranks(s2.elapsed_time(e2), world)
+        e2e = {"value": round(ms_e2e * 1e3 / K / world, 2), "unit": UNIT,
+               "h2d_bytes_per_step": pipe.h2d_bytes_per_step, "d2h_bytes_per_step": pipe.d2h_bytes_per_step}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        try:
+            res = oracle_sample(args.config, args.oracle_sample_steps, args.oracle_sample_layers)
+            cpu = {"value": round(res["us_per_step"], 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+                   "sample": res["sample"]}
+        except Exception as ex:  # reported, never fatal for the GPU number
+            cpu = {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": f"failed: {ex}"[:300]}
+
+    if rank != 0:
+        return
+    config = describe(cfg)
+    config.update({"layers_per_launch": args.layers_per_launch,
+                   "l2": "inputs larger than L2: each step reads the 64 MiB key cache, 256 MiB of "
+                         "slots and writes the gathered rows (> 129 MB L2)",
+                   "graph": "CUDA graph per step range, two streams", "kernel_timing": timing_src})
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": round(us_step / 1e3, 4), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 in, fp32 accumulate", "data": "synthetic",
+        "config": config,
+        "tokens_per_s": round(cfg.B * world * 1e6 / us_step, 1),
+        "gpu_launches": int(sum(r["launches"] for r in kern.values())) if kern else None,
+        "roofline": roof, "kernels": kinfo,
+        "peaks": {"hbm_copy_gbs": hbm_peak, "hbm_stream_read_gbs": round(hbm_read, 1),
+                  "host_zero_copy_read_gbs": round(zc_peak, 1), "host_h2d_memcpy_gbs": round(ce_peak, 1)},
+        "elastic": {"gathered_bytes_per_step": gathered // K, "full_reload_bytes_per_step": full_reload // K,
+                    "transfer_saved": round(1 - gathered / max(1, full_reload), 3),
+                    "adjacent_overlap": round(float(overlap), 3)},
+        "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        reference_arm(args, rank, world)
+    else:
+        our_arm(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -116,6 +116,20 @@ int spc_score_select(const void* x, const void* Wq, const void* Wk, void* K_dlm,
                      int n_sink, int n_recent, float* q_out, float* scores_out,
                      int32_t* selected, void* workspace, size_t workspace_bytes, void* stream);
 
+/* The same call restricted to some of its three kernels, run in order:
+ * SPC_STAGE_PROJECT (projection and append), SPC_STAGE_SCAN (key scan and
+ * per-head logsumexp partials), SPC_STAGE_SELECT (group score, Top-K, len
+ * update). Calling the stages one by one on one stream with one workspace
+ * gives the same result as spc_score_select; used to time each kernel. */
+#define SPC_STAGE_PROJECT 1
+#define SPC_STAGE_SCAN 2
+#define SPC_STAGE_SELECT 4
+int spc_score_select_stages(const void* x, const void* Wq, const void* Wk, void* K_dlm, int32_t* len,
+                            int append, int B, int H, int n_q, int n_kv, int d, int cap, int budget,
+                            int n_sink, int n_recent, float* q_out, float* scores_out,
+                            int32_t* selected, void* workspace, size_t workspace_bytes,
+                            void* stream, int stages);
+
 /* ------------------------------------------------------------------------
  * Elastic loading: the set difference between the new selection and the
  * resident slots. [Blog] §6 (C2): to_load = S_now - S_last, worked example

@@ -92,11 +92,12 @@ def head_probabilities(q: np.ndarray, K_bits: np.ndarray, length: int) -> np.nda
     P = np.zeros((n_q, length), np.float64)
     if length == 0:
         return P
-    for h in range(n_q):
-        K = bf16_to_f64(K_bits[h // G, :length])
-        logits = (K @ q[h]) / math.sqrt(d)
-        w = np.exp(logits - logits.max())
-        P[h] = w / w.sum()
+    for g in range(n_kv):
+        K = bf16_to_f64(K_bits[g, :length])
+        for h in range(g * G, (g + 1) * G):
+            logits = (K @ q[h]) / math.sqrt(d)
+            w = np.exp(logits - logits.max())
+            P[h] = w / w.sum()
     return P
 
 

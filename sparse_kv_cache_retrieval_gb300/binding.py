@@ -37,6 +37,8 @@ SIGNATURES = {
     "spc_score_select_workspace_size": (ctypes.c_size_t, [_I] * 7),
     "spc_score_select": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P,
                               _P, ctypes.c_size_t, _P]),
+    "spc_score_select_stages": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P,
+                                     _P, _P, ctypes.c_size_t, _P, _I]),
     "spc_elastic_diff": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "spc_gather_kv": (_I, [_P, _I, _I, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "spc_sparse_decode_attn_workspace_size": (ctypes.c_size_t, [_I] * 6),
@@ -116,6 +118,20 @@ def spc_score_select(x, Wq, Wk, K_dlm, len, append, B, H, n_q, n_kv, d, cap, bud
         _ptr(x), _ptr(Wq), _ptr(Wk), _ptr(K_dlm), _ptr(len), int(append), B, H, n_q, n_kv, d, cap,
         budget, n_sink, n_recent, _ptr(q_out), _ptr(scores_out), _ptr(selected), _ptr(workspace),
         workspace_bytes, _stream(stream)))
+
+
+SPC_STAGE_PROJECT, SPC_STAGE_SCAN, SPC_STAGE_SELECT = 1, 2, 4
+
+
+def spc_score_select_stages(x, Wq, Wk, K_dlm, len, append, B, H, n_q, n_kv, d, cap, budget, n_sink,
+                            n_recent, q_out, scores_out, selected, workspace, workspace_bytes=None,
+                            stream=None, stages=7) -> None:
+    if workspace_bytes is None:
+        workspace_bytes = _nbytes(workspace)
+    _check("spc_score_select_stages", lib().spc_score_select_stages(
+        _ptr(x), _ptr(Wq), _ptr(Wk), _ptr(K_dlm), _ptr(len), int(append), B, H, n_q, n_kv, d, cap,
+        budget, n_sink, n_recent, _ptr(q_out), _ptr(scores_out), _ptr(selected), _ptr(workspace),
+        workspace_bytes, _stream(stream), int(stages)))
 
 
 def spc_elastic_diff(selected, slot_pos_prev, slot_pos_next, load_slot, load_pos, n_load, B, n_kv,

@@ -94,12 +94,14 @@ size_t spc_score_select_workspace_size(int B, int H, int n_q, int n_kv, int d, i
   return score_select_workspace(B, H, n_q, n_kv, cap);
 }
 
-int spc_score_select(const void* x, const void* Wq, const void* Wk, void* K_dlm, int32_t* len,
-                     int append, int B, int H, int n_q, int n_kv, int d, int cap, int budget,
-                     int n_sink, int n_recent, float* q_out, float* scores_out,
-                     int32_t* selected, void* workspace, size_t workspace_bytes, void* stream) {
+int spc_score_select_stages(const void* x, const void* Wq, const void* Wk, void* K_dlm, int32_t* len,
+                            int append, int B, int H, int n_q, int n_kv, int d, int cap, int budget,
+                            int n_sink, int n_recent, float* q_out, float* scores_out,
+                            int32_t* selected, void* workspace, size_t workspace_bytes,
+                            void* stream, int stages) {
   if (!x || !Wq || !K_dlm || !len || !selected) return SPC_ERR_INVALID_ARG;
   if (append != 0 && append != 1) return SPC_ERR_INVALID_ARG;
+  if (stages < 1 || stages > 7) return SPC_ERR_INVALID_ARG;
   if (append && !Wk) return SPC_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(Wq) || (Wk && !aligned16(Wk)) || !aligned16(K_dlm) ||
       (q_out && !aligned16(q_out)))
@@ -116,8 +118,17 @@ int spc_score_select(const void* x, const void* Wq, const void* Wk, void* K_dlm,
   c.x = x; c.Wq = Wq; c.Wk = Wk; c.K_dlm = K_dlm; c.len = len; c.append = append;
   c.B = B; c.H = H; c.n_q = n_q; c.n_kv = n_kv; c.cap = cap; c.budget = budget;
   c.n_sink = n_sink; c.n_recent = n_recent; c.q_out = q_out; c.scores_out = scores_out;
-  c.selected = selected; c.workspace = workspace; c.stream = stream;
+  c.selected = selected; c.workspace = workspace; c.stream = stream; c.stages = stages;
   return score_select_launch(c);
+}
+
+int spc_score_select(const void* x, const void* Wq, const void* Wk, void* K_dlm, int32_t* len,
+                     int append, int B, int H, int n_q, int n_kv, int d, int cap, int budget,
+                     int n_sink, int n_recent, float* q_out, float* scores_out,
+                     int32_t* selected, void* workspace, size_t workspace_bytes, void* stream) {
+  return spc_score_select_stages(x, Wq, Wk, K_dlm, len, append, B, H, n_q, n_kv, d, cap, budget,
+                                 n_sink, n_recent, q_out, scores_out, selected, workspace,
+                                 workspace_bytes, stream, SPC_STAGE_PROJECT | SPC_STAGE_SCAN | SPC_STAGE_SELECT);
 }
 
 int spc_elastic_diff(const int32_t* selected, const int32_t* slot_pos_prev, int32_t* slot_pos_next,

@@ -517,7 +517,10 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a) {
       int srank = run_sel + block_excl_scan(scount, scratch, &stot);
 #pragma unroll
       for (int k = 0; k < 4; ++k)
-        if (sel[k]) out[out_base + srank++] = lo + i0 + k;
+        if (sel[k]) {
+          if (out_base + srank < a.K) out[out_base + srank] = lo + i0 + k;
+          ++srank;
+        }
       run_eq += etot;
       run_sel += stot;
     }
@@ -617,7 +620,7 @@ int score_select_launch(const ScoreSelectCall& c) {
   cudaError_t e;
 
   // ---- projection
-  {
+  if (c.stages & SPC_STAGE_PROJECT) {
     ProjArgs pa{};
     pa.x = static_cast<const uint16_t*>(c.x);
     pa.Wq = static_cast<const uint16_t*>(c.Wq);
@@ -646,7 +649,7 @@ int score_select_launch(const ScoreSelectCall& c) {
   }
 
   // ---- key scan
-  {
+  if (c.stages & SPC_STAGE_SCAN) {
     ScanArgs sa{};
     sa.K = static_cast<const uint16_t*>(c.K_dlm);
     sa.q = reinterpret_cast<const float*>(ws + l.q);
@@ -673,7 +676,7 @@ int score_select_launch(const ScoreSelectCall& c) {
   }
 
   // ---- group score + select (one cluster per (request, KV head))
-  {
+  if (c.stages & SPC_STAGE_SELECT) {
     SelArgs sa{};
     sa.logits = reinterpret_cast<const float*>(ws + l.logits);
     sa.part = reinterpret_cast<const float2*>(ws + l.part_scan);

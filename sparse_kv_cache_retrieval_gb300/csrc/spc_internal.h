@@ -21,6 +21,7 @@ struct ScoreSelectCall {
   int32_t* selected;
   void* workspace;
   void* stream;
+  int stages;
 };
 
 size_t score_select_workspace(int B, int H, int n_q, int n_kv, int cap);

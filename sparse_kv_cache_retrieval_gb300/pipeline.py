@@ -1,0 +1,312 @@
+"""The decode step on two CUDA streams: select for the next step, diff, and
+per layer chunk attention (stream A) followed by the in-place gather of the
+next step's missing rows (stream B).
+
+Method ordering: "ASPLOS'26 | SpeContext 让小模型先圈出重要 KV Cache"
+(marsggbo blog) §4 -- the retrieval head predicts the positions of step t+1
+while the LLM runs step t on the sparse KV prepared at step t-1, and the
+prefetcher moves only the missing rows on another CUDA stream; §6 -- only
+S_now - S_last is loaded; "SpeContext: Enabling Efficient Long-context
+Reasoning with Speculative Context Sparsity in LLMs" (paperlayer.ai summary)
+§5.1 and §5.4 (in place). The pages omit the pipeline warm-up; here a
+prologue runs the head once on the last prompt token and loads its whole
+selection before the first decode step.
+
+Ordering (per layer chunk c, step t, parity p = t % 2):
+  A: score_select(x_{t+1}) -> selected[1-p]; diff(selected[1-p], slot_pos[p])
+     -> slot_pos[1-p], loads[1-p]; for each chunk c: wait gather(c, t-1);
+     attention(c, selected[p], slot_pos[p]); record attn(c, t)
+  B: wait attn(c, t); gather(c, loads[1-p]) into the slots; record gather(c, t)
+The in-place overwrite of chunk c therefore always follows the attention that
+reads the old rows, and the next step's attention on c always follows it.
+
+PyTorch provides device memory, pinned host memory, streams, events and CUDA
+graphs; every step of the method runs in libspc's kernels.
+"""
+from __future__ import annotations
+
+import math
+from typing import Dict, List, Optional
+
+import numpy as np
+import torch
+
+from . import binding as spc
+from .configs import Workload
+from .synth import Inputs, fill_llm_kv
+
+_BF16_ROW = 256  # bytes of one K or V row at d = 128
+
+
+def _dev_u16(a: np.ndarray, device) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device)
+
+
+class DecodePipeline:
+    """Device-resident state and the pipelined decode step for one workload.
+
+    ``inputs`` comes from ``synth.make_inputs``; ``n_layers`` may be smaller
+    than the workload's to keep tests small. LLM K/V of layers
+    [0, gpu_layers[b]) lives in HBM (attention reads it by position); the
+    other layers live in pinned host memory (``host_stores``) and are reached
+    through budget-sized HBM slots.
+    """
+
+    def __init__(self, cfg: Workload, inputs: Inputs, *, device: str = "cuda",
+                 n_layers: Optional[int] = None, layers_per_launch: int = 4,
+                 host_io: bool = False, timing: bool = False, fill_threads: Optional[int] = None):
+        self.cfg = cfg
+        self.inp = inputs
+        self.dev = torch.device(device)
+        self.L = cfg.n_layers if n_layers is None else n_layers
+        self.B, self.H, self.n_q, self.n_kv, self.d = cfg.B, cfg.H, cfg.n_q, cfg.n_kv, cfg.d
+        self.K, self.cap = cfg.budget, cfg.cap
+        self.G = cfg.G
+        self.scale = 1.0 / math.sqrt(self.d)
+        self.gpu_layers = [min(int(g), self.L) for g in cfg.gpu_layers]
+        self.host_io = host_io
+        self.timing = timing
+        dev = self.dev
+        B, L, K, n_kv, d, cap = self.B, self.L, self.K, self.n_kv, self.d, self.cap
+
+        # retrieval head
+        self.Wq = _dev_u16(inputs.Wq, dev)
+        self.Wk = _dev_u16(inputs.Wk, dev)
+        self.K_dlm = _dev_u16(inputs.K_dlm, dev)
+        self.len = torch.from_numpy(inputs.lens.astype(np.int32)).to(dev)
+        self.ws_score = torch.zeros(spc.spc_score_select_workspace_size(B, self.H, self.n_q, n_kv, d, cap, K),
+                                    dtype=torch.uint8, device=dev)
+        n_steps = inputs.q_llm.shape[0]
+        self.x_dev = _dev_u16(inputs.x, dev)                                  # [steps+1][B][H]
+        self.q_dev = _dev_u16(inputs.q_llm[:, :L], dev)                       # [steps][L][B][n_q][d]
+        self.n_steps = n_steps
+
+        # selection state, double-buffered by step parity
+        def i32(*shape, fill=0):
+            return torch.full(shape, fill, dtype=torch.int32, device=dev)
+        self.selected = i32(2, B, n_kv, K, fill=-1)
+        self.slot_pos = i32(2, B, n_kv, K, fill=-1)
+        self.load_slot = i32(2, B, n_kv, K)
+        self.load_pos = i32(2, B, n_kv, K)
+        self.n_load = i32(2, B, n_kv)
+        self.out = torch.zeros(L, B, self.n_q, d, dtype=torch.float32, device=dev)
+
+        # LLM KV: HBM full caches, pinned host stores, HBM slots
+        self.hbm: List[Optional[torch.Tensor]] = []
+        self.host_stores: List[Optional[torch.Tensor]] = []
+        self.slots: List[Optional[torch.Tensor]] = []
+        host_dev_ptrs, slot_ptrs, layer0, n_host = [], [], [], []
+        for b in range(B):
+            ng = self.gpu_layers[b]
+            nh = L - ng
+            if ng > 0:
+                buf = np.empty((ng, 2, n_kv, cap, d), np.uint16)
+                fill_llm_kv(cfg, b, 0, buf, threads=fill_threads)
+                self.hbm.append(_dev_u16(buf, dev))
+                del buf
+            else:
+                self.hbm.append(None)
+            if nh > 0:
+                hs = torch.empty((nh, 2, n_kv, cap, d), dtype=torch.int16, pin_memory=True)
+                fill_llm_kv(cfg, b, ng, hs.numpy().view(np.uint16), threads=fill_threads)
+                self.host_stores.append(hs)
+                sl = torch.zeros((nh, 2, n_kv, K, d), dtype=torch.int16, device=dev)
+                self.slots.append(sl)
+                host_dev_ptrs.append(spc.spc_host_device_pointer(hs))
+                slot_ptrs.append(sl.data_ptr())
+            else:
+                self.host_stores.append(None)
+                self.slots.append(None)
+                host_dev_ptrs.append(0)
+                slot_ptrs.append(0)
+            layer0.append(ng)
+            n_host.append(nh)
+        self.gviews = spc.to_device_bytes(spc.gather_views(host_dev_ptrs, slot_ptrs, layer0, n_host), dev)
+
+        # attention views [L][B]
+        kp, vp, rows, use = [], [], [], []
+        for l in range(L):
+            for b in range(B):
+                ng = self.gpu_layers[b]
+                if l < ng:
+                    base = self.hbm[b][l]
+                    kp.append(base[0].data_ptr()); vp.append(base[1].data_ptr())
+                    rows.append(cap); use.append(0)
+                else:
+                    base = self.slots[b][l - ng]
+                    kp.append(base[0].data_ptr()); vp.append(base[1].data_ptr())
+                    rows.append(K); use.append(1)
+        self.aviews = spc.to_device_bytes(spc.kv_views(kp, vp, rows, use), dev)
+        self.aview_stride = 32 * B
+
+        # layer chunks, streams, events
+        lc = max(1, min(layers_per_launch, L))
+        self.chunks = [(l0, min(L, l0 + lc)) for l0 in range(0, L, lc)]
+        self.ws_attn = torch.zeros(spc.spc_sparse_decode_attn_workspace_size(lc, B, self.n_q, n_kv, d, K),
+                                   dtype=torch.uint8, device=dev)
+        self.sA = torch.cuda.Stream(device=dev)
+        self.sB = torch.cuda.Stream(device=dev)
+        self.e_attn = [torch.cuda.Event() for _ in self.chunks]
+        self.e_gath = [torch.cuda.Event() for _ in self.chunks]
+        self._gather_pending = [False] * len(self.chunks)
+
+        self.host_io = False
+        if host_io:
+            self.enable_host_io()
+        self.h2d_bytes_per_step = (B * self.H + L * B * self.n_q * d) * 2
+        self.d2h_bytes_per_step = L * B * self.n_q * d * 4 + B * n_kv * K * 4
+
+        # optional timing events: (stream, kind, start, end) per launch
+        self._timed: List[tuple] = []
+        self._prologue_done = False
+
+    def enable_host_io(self) -> None:
+        """Switch to end-to-end mode: every step copies its head input and LLM
+        queries from pinned host memory and copies its attention output and
+        selection back to pinned host memory, all on stream A."""
+        if self.host_io:
+            return
+        inputs, B, L, d, dev = self.inp, self.B, self.L, self.d, self.dev
+        n_steps = self.n_steps
+        self.x_host = torch.from_numpy(inputs.x.view(np.int16).copy()).pin_memory()
+        self.q_host = torch.from_numpy(np.ascontiguousarray(inputs.q_llm[:, :L]).view(np.int16)).pin_memory()
+        self.x_stage = torch.empty(B, self.H, dtype=torch.int16, device=dev)
+        self.q_stage = torch.empty(L, B, self.n_q, d, dtype=torch.int16, device=dev)
+        self.out_host = torch.empty((n_steps, L, B, self.n_q, d), dtype=torch.float32).pin_memory()
+        self.sel_host = torch.empty((n_steps, B, self.n_kv, self.K), dtype=torch.int32).pin_memory()
+        self.host_io = True
+
+    # ------------------------------------------------------------------ pieces
+    def _score_select(self, x, out_sel, append: int, stream, stages: int = 7, q_out=None, scores_out=None):
+        c = self.cfg
+        spc.spc_score_select_stages(x, self.Wq, self.Wk, self.K_dlm, self.len, append, self.B, self.H,
+                                    self.n_q, self.n_kv, self.d, self.cap, self.K, c.n_sink, c.n_recent,
+                                    q_out, scores_out, out_sel, self.ws_score, stream=stream,
+                                    stages=stages)
+
+    def _diff(self, pn, p, stream):
+        spc.spc_elastic_diff(self.selected[pn], self.slot_pos[p], self.slot_pos[pn], self.load_slot[pn],
+                             self.load_pos[pn], self.n_load[pn], self.B, self.n_kv, self.K, self.cap,
+                             stream=stream)
+
+    def _gather(self, pn, l0, l1, stream):
+        spc.spc_gather_kv(self.gviews, l0, l1, self.load_slot[pn], self.load_pos[pn], self.n_load[pn],
+                          self.B, self.n_kv, self.d, self.cap, self.K, stream=stream)
+
+    def _attn(self, q_layers, p, l0, l1, stream):
+        views = self.aviews.data_ptr() + l0 * self.aview_stride
+        spc.spc_sparse_decode_attn(q_layers[l0].data_ptr(), views, self.selected[p], self.slot_pos[p],
+                                   l1 - l0, self.B, self.n_q, self.n_kv, self.d, self.K, self.scale,
+                                   self.out[l0].data_ptr(), self.ws_attn, stream=stream)
+
+    @staticmethod
+    def _timing_event():
+        # inside a CUDA graph a timing event must become a record node
+        try:
+            return torch.cuda.Event(enable_timing=True, external=True)
+        except TypeError:
+            return torch.cuda.Event(enable_timing=True)
+
+    def _timed_call(self, kind, stream, fn):
+        if not self.timing:
+            fn()
+            return
+        s, e = self._timing_event(), self._timing_event()
+        s.record(stream)
+        fn()
+        e.record(stream)
+        self._timed.append((kind, s, e))
+
+    # ------------------------------------------------------------------ steps
+    def prologue(self) -> None:
+        """Head on the last prompt token; load its whole selection (no append)."""
+        sA = self.sA
+        with torch.cuda.stream(sA):
+            self.len.copy_(torch.from_numpy(self.inp.lens.astype(np.int32)))
+            self.slot_pos[1].fill_(-1)
+            self._score_select(self.x_dev[0], self.selected[0], 0, sA)
+            self._diff(0, 1, sA)
+            self._gather(0, 0, self.L, sA)
+        sA.synchronize()
+        self._gather_pending = [False] * len(self.chunks)
+        self._prologue_done = True
+
+    def step(self, t: int) -> None:
+        """Issue decode step t (uses inputs x[t+1] and q_llm[t])."""
+        sA, sB = self.sA, self.sB
+        p, pn = t % 2, (t + 1) % 2
+        append = 1 if self.cfg.append else 0
+        if self.host_io:
+            with torch.cuda.stream(sA):
+                self.x_stage.copy_(self.x_host[t + 1], non_blocking=True)
+                self.q_stage.copy_(self.q_host[t], non_blocking=True)
+            x, q_layers = self.x_stage, self.q_stage
+        else:
+            x, q_layers = self.x_dev[t + 1], self.q_dev[t]
+        if self.timing:
+            self._timed_call("project", sA, lambda: self._score_select(x, self.selected[pn], append, sA, 1))
+            self._timed_call("key_scan", sA, lambda: self._score_select(x, self.selected[pn], append, sA, 2))
+            self._timed_call("select", sA, lambda: self._score_select(x, self.selected[pn], append, sA, 4))
+        else:
+            self._score_select(x, self.selected[pn], append, sA)
+        self._timed_call("diff", sA, lambda: self._diff(pn, p, sA))
+        for c, (l0, l1) in enumerate(self.chunks):
+            if self._gather_pending[c]:
+                sA.wait_event(self.e_gath[c])
+            self._timed_call("attention", sA, lambda: self._attn(q_layers, p, l0, l1, sA))
+            self.e_attn[c].record(sA)
+            sB.wait_event(self.e_attn[c])
+            self._timed_call("gather", sB, lambda: self._gather(pn, l0, l1, sB))
+            self.e_gath[c].record(sB)
+            self._gather_pending[c] = True
+        if self.host_io:
+            with torch.cuda.stream(sA):
+                self.out_host[t].copy_(self.out, non_blocking=True)
+                self.sel_host[t].copy_(self.selected[pn], non_blocking=True)
+
+    def join(self) -> None:
+        self.sA.wait_stream(self.sB)
+
+    def run(self, t0: int, n: int) -> None:
+        for t in range(t0, t0 + n):
+            self.step(t)
+        self.join()
+
+    def capture(self, t0: int, n: int) -> torch.cuda.CUDAGraph:
+        """A CUDA graph of steps [t0, t0+n) (both streams, forked and joined)."""
+        g = torch.cuda.CUDAGraph()
+        self.sA.wait_stream(self.sB)
+        saved = list(self._gather_pending)
+        self._gather_pending = [False] * len(self.chunks)
+        with torch.cuda.graph(g, stream=self.sA):
+            self.sB.wait_stream(self.sA)
+            for t in range(t0, t0 + n):
+                self.step(t)
+            self.sA.wait_stream(self.sB)
+        self._gather_pending = [False] * len(self.chunks)
+        del saved
+        return g
+
+    def timed_summary(self) -> Dict[str, dict]:
+        """Per kernel kind: launches and mean duration (ms) of the timed calls."""
+        res: Dict[str, dict] = {}
+        for kind, s, e in self._timed:
+            r = res.setdefault(kind, {"launches": 0, "total_ms": 0.0})
+            r["launches"] += 1
+            r["total_ms"] += s.elapsed_time(e)
+        for r in res.values():
+            r["mean_ms"] = r["total_ms"] / max(1, r["launches"])
+        return res
+
+    def reset_timing(self) -> None:
+        self._timed = []
+
+    # ------------------------------------------------------------------ accounting
+    def loads_per_step(self, parity: int) -> np.ndarray:
+        return self.n_load[parity].cpu().numpy()
+
+    def key_scan_bytes(self, lens) -> int:
+        return int(sum(int(L) for L in lens) * self.n_kv * self.d * 2)
+
+
+__all__ = ["DecodePipeline"]

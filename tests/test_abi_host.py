@@ -1,0 +1,133 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library must load, export every function include/spc.h declares, and
+reject bad arguments before touching the device: each call below returns
+its error code from host validation, so no kernel is launched.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__
+from sparse_kv_cache_retrieval_gb300 import binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    __graft_entry__.build()
+    return B.lib()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "spc.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(spc_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_four_hot_path_calls():
+    names = declared_functions()
+    for n in ("spc_score_select", "spc_elastic_diff", "spc_gather_kv", "spc_sparse_decode_attn"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in spc.h but not exported"
+        assert n in B.SIGNATURES, f"{n} has no binding signature"
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5, -6, 42):
+        assert lib.spc_status_string(code)
+
+
+def test_workspace_sizes(lib):
+    ws = B.spc_score_select_workspace_size(1, 4096, 32, 8, 128, 32768, 2048)
+    # at least the fp32 logits of every query head over the capacity
+    assert ws >= 32 * 32768 * 4
+    assert B.spc_score_select_workspace_size(1, 4096, 32, 8, 64, 32768, 2048) == 0
+    assert B.spc_score_select_workspace_size(1, 4096, 30, 8, 128, 32768, 2048) == 0
+    assert B.spc_sparse_decode_attn_workspace_size(1, 1, 32, 8, 128, 2048) > 0
+    assert B.spc_sparse_decode_attn_workspace_size(1, 1, 32, 8, 96, 2048) == 0
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: validation fails first
+
+
+def _score(lib, **kw):
+    a = dict(x=FAKE, Wq=FAKE, Wk=FAKE, K=FAKE, len=FAKE, append=0, B=1, H=4096, n_q=32, n_kv=8,
+             d=128, cap=4096, budget=512, n_sink=4, n_recent=64, q_out=None, scores=None,
+             sel=FAKE, ws=FAKE, ws_bytes=0, stream=None)
+    a.update(kw)
+    return lib.spc_score_select(a["x"], a["Wq"], a["Wk"], a["K"], a["len"], a["append"], a["B"],
+                                a["H"], a["n_q"], a["n_kv"], a["d"], a["cap"], a["budget"],
+                                a["n_sink"], a["n_recent"], a["q_out"], a["scores"], a["sel"],
+                                a["ws"], a["ws_bytes"], a["stream"])
+
+
+def test_score_select_rejects_bad_arguments(lib):
+    assert _score(lib, x=None) == -1
+    assert _score(lib, append=2) == -1
+    assert _score(lib, append=1, Wk=None) == -1
+    assert _score(lib, K=FAKE + 8) == -1                 # misaligned key cache
+    assert _score(lib, d=64) == -2
+    assert _score(lib, n_q=30) == -2                     # n_q % n_kv != 0
+    assert _score(lib, n_q=24, n_kv=8) == -2             # G = 3 unsupported
+    assert _score(lib, budget=8192) == -2                # budget > max
+    assert _score(lib, budget=5000, cap=4096) == -2
+    assert _score(lib, cap=300000) == -2                 # cap > max
+    assert _score(lib, n_sink=500, n_recent=64) == -2    # forced set > budget
+    assert _score(lib, B=0) == -2
+    assert _score(lib, H=4095) == -2
+    assert _score(lib) == -5                             # workspace too small
+    assert lib.spc_score_select_stages(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 1, 4096, 32, 8, 128, 4096,
+                                       512, 4, 64, None, None, FAKE, FAKE, 1 << 40, None, 0) == -1
+
+
+def test_diff_gather_attention_reject_bad_arguments(lib):
+    assert lib.spc_elastic_diff(None, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 8, 512, 4096, None) == -1
+    assert lib.spc_elastic_diff(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 8, 5000, 4096, None) == -2
+    assert lib.spc_elastic_diff(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 8, 512, 1 << 20, None) == -2
+    assert lib.spc_gather_kv(None, 0, 1, FAKE, FAKE, FAKE, 1, 8, 128, 4096, 512, None) == -1
+    assert lib.spc_gather_kv(FAKE, 0, 1, FAKE, FAKE, FAKE, 1, 8, 64, 4096, 512, None) == -2
+    assert lib.spc_gather_kv(FAKE, 2, 1, FAKE, FAKE, FAKE, 1, 8, 128, 4096, 512, None) == -2
+    assert lib.spc_gather_kv(FAKE, 0, 1, FAKE, FAKE, FAKE, 64, 32, 128, 4096, 512, None) == -2
+    assert lib.spc_sparse_decode_attn(None, FAKE, FAKE, FAKE, 1, 1, 32, 8, 128, 512, 0.1, FAKE,
+                                      FAKE, 1 << 30, None) == -1
+    assert lib.spc_sparse_decode_attn(FAKE, FAKE, FAKE, FAKE, 1, 1, 32, 8, 128, 512, -1.0, FAKE,
+                                      FAKE, 1 << 30, None) == -1
+    assert lib.spc_sparse_decode_attn(FAKE, FAKE, FAKE, FAKE, 1, 1, 32, 8, 128, 512, 0.1, FAKE,
+                                      FAKE, 0, None) == -5
+    assert lib.spc_sparse_decode_attn(FAKE, FAKE, FAKE, FAKE, 1, 1, 48, 8, 128, 512, 0.1, FAKE,
+                                      FAKE, 1 << 30, None) == -2
+    assert lib.spc_stream_read(FAKE, 17, FAKE, 1, None) == -2
+    assert lib.spc_stream_read(FAKE + 4, 16, FAKE, 1, None) == -1
+
+
+def test_binding_raises_spc_error(lib):
+    with pytest.raises(B.SpcError) as ei:
+        B.spc_elastic_diff(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 8, 5000, 4096, stream=0)
+    assert ei.value.status == -2
+
+
+def test_view_struct_layouts():
+    assert B.GATHER_VIEW_DTYPE.itemsize == 32
+    assert B.KV_VIEW_DTYPE.itemsize == 32
+    v = B.kv_views([1, 2], [3, 4], [5, 6], [1, 0])
+    raw = v.view(ctypes.c_uint64 * 4 if False else "u8").reshape(2, 4)
+    assert raw[0, 0] == 1 and raw[0, 1] == 3 and raw[0, 2] == 5 and (raw[0, 3] & 0xFFFFFFFF) == 1
+
+
+def test_product_path_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "sparse_kv_cache_retrieval_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")) and f != "smoke.py":
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f

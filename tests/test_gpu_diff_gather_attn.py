@@ -1,0 +1,218 @@
+"""GPU parity of spc_elastic_diff, spc_gather_kv and spc_sparse_decode_attn
+against the CPU oracle, through the C ABI, on seeded synthetic inputs.
+
+Bars: load lists, slot maps and gathered bytes bit-exact; attention within
+1e-2 absolute (the stated bar) and, tighter, within 2e-5 + 1e-4 |o| (fp32
+accumulation over at most 4096 rows of unit-scale products).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.spc_oracle as O
+from oracle.checks import ATTN_ATOL
+from sparse_kv_cache_retrieval_gb300 import binding as spc
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def i32(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(DEV)
+
+
+def random_state(rng, B, n_kv, K, cap, churn=0.3, empty=0.05, n_sel=None):
+    """Seeded selection/slot-map pairs with the structure a decode produces."""
+    sel = np.full((B, n_kv, K), -1, np.int64)
+    prev = np.full((B, n_kv, K), -1, np.int64)
+    for b in range(B):
+        for g in range(n_kv):
+            m = K if n_sel is None else n_sel
+            old = rng.choice(cap, size=K, replace=False)
+            keep = old[rng.random(K) > churn]
+            fresh = np.setdiff1d(rng.choice(cap, size=min(cap, 2 * K), replace=False), old)
+            new = np.concatenate([keep, fresh])[:m]
+            new = np.sort(rng.permutation(new)[:m])
+            sel[b, g, :new.size] = new
+            p = old.copy()
+            p[rng.random(K) < empty] = -1
+            prev[b, g] = p
+    return sel, prev
+
+
+def run_diff(sel, prev, cap, inplace=False):
+    B, n_kv, K = sel.shape
+    s, p = i32(sel), i32(prev)
+    nxt = p if inplace else torch.full_like(p, -9)
+    ls = torch.full_like(p, -9)
+    lp = torch.full_like(p, -9)
+    nl = torch.full((B, n_kv), -9, dtype=torch.int32, device=DEV)
+    spc.spc_elastic_diff(s, p, nxt, ls, lp, nl, B, n_kv, K, cap)
+    torch.cuda.synchronize()
+    return ls.cpu().numpy(), lp.cpu().numpy(), nxt.cpu().numpy(), nl.cpu().numpy()
+
+
+@pytest.mark.parametrize("B,n_kv,K,cap,churn,inplace", [
+    (1, 8, 2048, 32768, 0.2, False),
+    (2, 3, 100, 400, 0.5, True),
+    (16, 8, 1024, 16384, 0.3, False),
+    (1, 1, 4096, 262144, 0.9, False),      # maximum budget and capacity
+    (3, 2, 64, 64, 1.0, False),           # every slot empty or replaced
+    (2, 2, 1, 5, 0.5, True),
+])
+def test_elastic_diff_bit_exact(B, n_kv, K, cap, churn, inplace):
+    rng = np.random.default_rng(1000 + K + cap)
+    sel, prev = random_state(rng, B, n_kv, K, cap, churn)
+    ls, lp, nxt, nl = run_diff(sel, prev, cap, inplace)
+    for b in range(B):
+        for g in range(n_kv):
+            ols, olp, onxt = O.elastic_diff(sel[b, g], prev[b, g])
+            n = nl[b, g]
+            assert n == olp.size
+            assert np.array_equal(ls[b, g, :n], ols) and np.array_equal(lp[b, g, :n], olp)
+            assert np.array_equal(nxt[b, g], onxt)
+
+
+def test_elastic_diff_worked_example_and_idempotence():
+    sel = np.array([[[1, 8, 21, 50]]])
+    prev = np.array([[[1, 8, 21, 35]]])
+    ls, lp, nxt, nl = run_diff(sel, prev, 64)
+    assert nl[0, 0] == 1 and lp[0, 0, 0] == 50 and ls[0, 0, 0] == 3
+    assert nxt[0, 0].tolist() == [1, 8, 21, 50]
+    ls, lp, nxt2, nl = run_diff(sel, nxt, 64)
+    assert nl[0, 0] == 0 and np.array_equal(nxt2, nxt)
+
+
+def test_elastic_diff_partial_selection():
+    rng = np.random.default_rng(7)
+    sel, prev = random_state(rng, 2, 4, 256, 3000, 0.4, n_sel=170)
+    ls, lp, nxt, nl = run_diff(sel, prev, 3000)
+    for b in range(2):
+        for g in range(4):
+            ols, olp, onxt = O.elastic_diff(sel[b, g], prev[b, g])
+            assert np.array_equal(lp[b, g, :nl[b, g]], olp) and np.array_equal(nxt[b, g], onxt)
+
+
+def test_gather_bit_exact_over_layers_and_requests():
+    rng = np.random.default_rng(11)
+    B, n_kv, K, cap, L = 3, 4, 96, 700, 5
+    layer0 = [0, 2, 5]                      # request 2 keeps every layer in HBM
+    stores, slots, hptr, sptr = [], [], [], []
+    for b in range(B):
+        nh = L - layer0[b]
+        if nh == 0:
+            stores.append(None); slots.append(None); hptr.append(0); sptr.append(0)
+            continue
+        hs = torch.empty((nh, 2, n_kv, cap, 128), dtype=torch.int16, pin_memory=True)
+        hs.numpy()[:] = rng.integers(-32768, 32767, hs.shape, dtype=np.int16)
+        sl = torch.zeros((nh, 2, n_kv, K, 128), dtype=torch.int16, device=DEV)
+        stores.append(hs); slots.append(sl)
+        hptr.append(spc.spc_host_device_pointer(hs)); sptr.append(sl.data_ptr())
+    views = spc.to_device_bytes(spc.gather_views(hptr, sptr, layer0, [L - v for v in layer0]), DEV)
+    sel, prev = random_state(rng, B, n_kv, K, cap, 0.5)
+    loads = [[O.elastic_diff(sel[b, g], prev[b, g]) for g in range(n_kv)] for b in range(B)]
+    ls = np.zeros((B, n_kv, K), np.int32)
+    lp = np.zeros((B, n_kv, K), np.int32)
+    nl = np.zeros((B, n_kv), np.int32)
+    for b in range(B):
+        for g in range(n_kv):
+            a, p, _ = loads[b][g]
+            ls[b, g, :a.size], lp[b, g, :p.size], nl[b, g] = a, p, a.size
+    ls_d, lp_d, nl_d = i32(ls), i32(lp), i32(nl)
+    # two launches over layer ranges [0, 3) and [3, 5)
+    spc.spc_gather_kv(views, 0, 3, ls_d, lp_d, nl_d, B, n_kv, 128, cap, K)
+    spc.spc_gather_kv(views, 3, 5, ls_d, lp_d, nl_d, B, n_kv, 128, cap, K)
+    torch.cuda.synchronize()
+    for b in range(B):
+        if slots[b] is None:
+            continue
+        got = slots[b].cpu().numpy().view(np.uint16)
+        want = np.zeros_like(got)
+        O.gather(stores[b].numpy().view(np.uint16), want, [x[0] for x in loads[b]],
+                 [x[1] for x in loads[b]])
+        assert np.array_equal(got, want)
+
+
+def _attn_case(rng, L, B, n_q, n_kv, K, cap, use_slots, n_valid=None, empty_group=False):
+    """Returns GPU output and oracle output for one attention launch."""
+    d = 128
+    caches, kp, vp, rows, use = [], [], [], [], []
+    for l in range(L):
+        for b in range(B):
+            nrows = K if use_slots else cap
+            kv = rng.standard_normal((2, n_kv, nrows, d)).astype(np.float32)
+            bits = O.round_to_bf16(kv.astype(np.float64))
+            t = torch.from_numpy(bits.view(np.int16)).to(DEV)
+            caches.append((bits, t))
+            kp.append(t[0].data_ptr()); vp.append(t[1].data_ptr()); rows.append(nrows); use.append(use_slots)
+    views = spc.to_device_bytes(spc.kv_views(kp, vp, rows, use), DEV)
+    q = O.round_to_bf16(rng.standard_normal((L, B, n_q, d)) * 1.5)
+    sel = np.full((B, n_kv, K), -1, np.int64)
+    slot = np.full((B, n_kv, K), -1, np.int64)
+    kept = []
+    for b in range(B):
+        kb = []
+        for g in range(n_kv):
+            m = K if n_valid is None else n_valid
+            if empty_group and g == 0:
+                m = 0
+            pos = np.sort(rng.choice(cap, size=m, replace=False))
+            sel[b, g, :m] = pos
+            sl = rng.choice(K, size=m, replace=False)
+            slot[b, g, sl] = pos
+            kb.append(np.sort(sl) if use_slots else pos)
+        kept.append(kb)
+    out = torch.full((L, B, n_q, d), 7.0, dtype=torch.float32, device=DEV)
+    ws = torch.zeros(spc.spc_sparse_decode_attn_workspace_size(L, B, n_q, n_kv, d, K), dtype=torch.uint8,
+                     device=DEV)
+    qd = torch.from_numpy(q.view(np.int16)).to(DEV)
+    scale = 1 / math.sqrt(d)
+    spc.spc_sparse_decode_attn(qd, views, i32(sel), i32(slot), L, B, n_q, n_kv, d, K, scale, out, ws)
+    spc.spc_sparse_decode_attn(qd, views, i32(sel), i32(slot), L, B, n_q, n_kv, d, K, scale, out, ws)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    want = np.zeros_like(got, dtype=np.float64)
+    for l in range(L):
+        for b in range(B):
+            bits = caches[l * B + b][0]
+            want[l, b] = O.sparse_attention(q[l, b], bits[0], bits[1], kept[b], scale)
+    return got, want
+
+
+ATTN_CASES = [
+    # L, B, n_q, n_kv, K, cap, use_slots, n_valid
+    (1, 1, 32, 8, 2048, 4096, 1, None),      # bench shape, one layer (split over the budget)
+    (4, 1, 32, 8, 2048, 4096, 1, 1500),      # 4 layers per launch, partly empty slots
+    (2, 2, 32, 8, 1000, 3000, 0, None),      # positions into a full cache, budget not /64
+    (1, 3, 4, 4, 130, 500, 1, None),         # MHA
+    (1, 2, 8, 4, 200, 700, 0, 150),          # G = 2
+    (1, 1, 64, 8, 4096, 8192, 1, None),      # 70B shape, max budget
+    (1, 1, 64, 1, 512, 2000, 0, None),       # MQA
+    (1, 1, 16, 1, 64, 100, 1, 1),            # one kept row per group
+]
+
+
+@pytest.mark.parametrize("L,B,n_q,n_kv,K,cap,use_slots,n_valid", ATTN_CASES)
+def test_attention_parity(L, B, n_q, n_kv, K, cap, use_slots, n_valid):
+    rng = np.random.default_rng(L * 1000 + n_q * 10 + K)
+    got, want = _attn_case(rng, L, B, n_q, n_kv, K, cap, use_slots, n_valid)
+    err = np.abs(got - want)
+    assert err.max() <= ATTN_ATOL
+    assert np.all(err <= 2e-5 + 1e-4 * np.abs(want)), f"max err {err.max():.3g}"
+
+
+def test_attention_empty_group_is_zero():
+    rng = np.random.default_rng(5)
+    got, want = _attn_case(rng, 1, 1, 8, 2, 128, 300, 1, None, empty_group=True)
+    assert np.all(got[0, 0, :4] == 0.0)
+    assert np.abs(got - want).max() <= 2e-5 + 1e-4 * np.abs(want).max()
+
+
+def test_attention_all_rows_equals_dense():
+    """Every position kept: sparse attention is dense attention (torch SDPA, fp64)."""
+    rng = np.random.default_rng(3)
+    d, n_q, n_kv, n = 128, 8, 2, 192
+    got, want = _attn_case(rng, 1, 1, n_q, n_kv, n, n, 0, None)
+    assert np.abs(got - want).max() <= 1e-4
