@@ -24,7 +24,7 @@ def workload(name="t", B=1, lens=(300,), H=256, n_q=8, n_kv=2, budget=64, n_laye
              cap=None, append=False, hot_frac=0.01, seed=0, n_sink=4, n_recent=64, rho=0.9,
              gpu_layers=None):
     lens = tuple(lens)
-    cap = cap if cap is not None else max(max(lens), 1) + (steps if append else 0)
+    cap = cap if cap is not None else max(max(lens), 1, budget) + (steps if append else 0)
     return Workload(name=name, B=B, lens=lens, H=H, n_q=n_q, n_kv=n_kv, d=128, budget=budget,
                     n_layers=n_layers, gpu_layers=tuple(gpu_layers or (0,) * B), steps=steps,
                     rho=(rho,) * B, hot=tuple(max(1, int(hot_frac * L)) for L in lens), seed=seed,
