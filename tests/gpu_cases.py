@@ -20,7 +20,7 @@ from sparse_kv_cache_retrieval_gb300.synth import make_inputs
 DEV = "cuda"
 
 
-def workload(name="t", B=1, lens=(300,), H=256, n_q=8, n_kv=2, budget=64, n_layers=1, steps=1,
+def workload(name="t", B=1, lens=(300,), H=256, n_q=8, n_kv=2, budget=96, n_layers=1, steps=1,
              cap=None, append=False, hot_frac=0.01, seed=0, n_sink=4, n_recent=64, rho=0.9,
              gpu_layers=None):
     lens = tuple(lens)

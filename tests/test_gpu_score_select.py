@@ -43,10 +43,11 @@ SMALL = [
     ("ragged_batch", dict(B=3, lens=(1500, 129, 700), n_q=8, n_kv=2, H=256, budget=96)),
     ("batch17_over_16", dict(B=17, lens=tuple(200 + 37 * i for i in range(17)), n_q=8, n_kv=2, H=256,
                              budget=80)),
-    ("len_le_budget_select_all", dict(lens=(50,), budget=64)),
-    ("len_eq_budget", dict(lens=(64,), budget=64)),
-    ("len_budget_plus_one", dict(lens=(65,), budget=64, cap=65)),
-    ("len_tiny", dict(lens=(3,), budget=64)),
+    ("len_le_budget_select_all", dict(lens=(50,), budget=96)),
+    ("len_eq_budget", dict(lens=(96,), budget=96)),
+    ("len_budget_plus_one", dict(lens=(97,), budget=96, cap=97)),
+    ("len_tiny", dict(lens=(3,), budget=96)),
+    ("len_zero", dict(lens=(0,), budget=96)),
     ("forced_only", dict(lens=(500,), budget=68)),
     ("no_forced", dict(lens=(500,), budget=50, n_sink=0, n_recent=0)),
     ("cap_multi_cta_cluster", dict(lens=(20000,), n_q=8, n_kv=2, H=256, budget=300, cap=20011)),
@@ -77,7 +78,7 @@ def test_score_select_append_grows_len_and_switches_from_select_all():
 
 
 def test_append_at_capacity_sets_overflow_and_keeps_len():
-    cfg = workload(name="full", lens=(100,), n_q=8, n_kv=2, H=256, budget=64, cap=100, append=True)
+    cfg = workload(name="full", lens=(100,), n_q=8, n_kv=2, H=256, budget=96, cap=100, append=True)
     run = ScoreRun(cfg)
     run.call(0, 1)
     assert int(run.len.item()) == 100
@@ -85,7 +86,7 @@ def test_append_at_capacity_sets_overflow_and_keeps_len():
 
 
 def test_all_equal_keys_ties_go_to_lower_positions():
-    cfg = workload(name="ties", lens=(400,), n_q=8, n_kv=2, H=256, budget=80)
+    cfg = workload(name="ties", lens=(400,), n_q=8, n_kv=2, H=256, budget=80, n_recent=64)
     run = ScoreRun(cfg)
     run.K[:, :, :400] = run.K[:, :, :1]   # every row equal -> every score equal
     gq, gs, gsel, glen, gK = run.call(0, 0)
