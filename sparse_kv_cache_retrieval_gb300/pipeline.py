@@ -201,11 +201,8 @@ class DecodePipeline:
 
     @staticmethod
     def _timing_event():
-        # inside a CUDA graph a timing event must become a record node
-        try:
-            return torch.cuda.Event(enable_timing=True, external=True)
-        except TypeError:
-            return torch.cuda.Event(enable_timing=True)
+        # timing runs eagerly only; graphs carry no timing events
+        return torch.cuda.Event(enable_timing=True)
 
     def _timed_call(self, kind, stream, fn):
         if not self.timing:
@@ -273,7 +270,12 @@ class DecodePipeline:
         self.join()
 
     def capture(self, t0: int, n: int) -> torch.cuda.CUDAGraph:
-        """A CUDA graph of steps [t0, t0+n) (both streams, forked and joined)."""
+        """A CUDA graph of steps [t0, t0+n) (both streams, forked and joined).
+
+        Replay it on stream A (``with torch.cuda.stream(pipe.sA): g.replay()``).
+        Timing must be off while capturing."""
+        if self.timing:
+            raise RuntimeError("disable timing before capturing a graph")
         g = torch.cuda.CUDAGraph()
         self.sA.wait_stream(self.sB)
         saved = list(self._gather_pending)
