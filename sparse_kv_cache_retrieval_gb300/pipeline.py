@@ -158,6 +158,8 @@ class DecodePipeline:
 
         # optional timing events: (stream, kind, start, end) per launch
         self._timed: List[tuple] = []
+        self._all_events: List[torch.cuda.Event] = []
+        self._capturing = False
         self._prologue_done = False
 
     def enable_host_io(self) -> None:
@@ -199,9 +201,13 @@ class DecodePipeline:
                                    l1 - l0, self.B, self.n_q, self.n_kv, self.d, self.K, self.scale,
                                    self.out[l0].data_ptr(), self.ws_attn, stream=stream)
 
-    @staticmethod
-    def _timing_event():
-        # timing runs eagerly only; graphs carry no timing events
+    def _timing_event(self):
+        # Inside a capture a timing event must be an external record node.
+        # Every event a graph records stays referenced in self._timed for the
+        # pipeline's lifetime: destroying an event a graph still records into
+        # is undefined behaviour at launch.
+        if self._capturing:
+            return torch.cuda.Event(enable_timing=True, external=True)
         return torch.cuda.Event(enable_timing=True)
 
     def _timed_call(self, kind, stream, fn):
@@ -209,6 +215,7 @@ class DecodePipeline:
             fn()
             return
         s, e = self._timing_event(), self._timing_event()
+        self._all_events.extend((s, e))
         s.record(stream)
         fn()
         e.record(stream)
@@ -273,18 +280,21 @@ class DecodePipeline:
         """A CUDA graph of steps [t0, t0+n) (both streams, forked and joined).
 
         Replay it on stream A (``with torch.cuda.stream(pipe.sA): g.replay()``).
-        Timing must be off while capturing."""
-        if self.timing:
-            raise RuntimeError("disable timing before capturing a graph")
+        With timing on, the graph records external timing events that the
+        pipeline keeps alive; read them after a replay."""
         g = torch.cuda.CUDAGraph()
         self.sA.wait_stream(self.sB)
         saved = list(self._gather_pending)
         self._gather_pending = [False] * len(self.chunks)
-        with torch.cuda.graph(g, stream=self.sA):
-            self.sB.wait_stream(self.sA)
-            for t in range(t0, t0 + n):
-                self.step(t)
-            self.sA.wait_stream(self.sB)
+        self._capturing = True
+        try:
+            with torch.cuda.graph(g, stream=self.sA):
+                self.sB.wait_stream(self.sA)
+                for t in range(t0, t0 + n):
+                    self.step(t)
+                self.sA.wait_stream(self.sB)
+        finally:
+            self._capturing = False
         self._gather_pending = [False] * len(self.chunks)
         del saved
         return g
@@ -301,6 +311,7 @@ class DecodePipeline:
         return res
 
     def reset_timing(self) -> None:
+        """Forget the recorded (kind, start, end) triples; the events stay alive."""
         self._timed = []
 
     # ------------------------------------------------------------------ accounting
