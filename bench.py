@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-sample-steps", type=int, default=2)
     ap.add_argument("--oracle-sample-layers", type=int, default=2)
+    ap.add_argument("--profile", action="store_true",
+                    help="hot path only for a profiler: prologue, then --steps eager steps")
     return ap.parse_args()
 
 
@@ -287,6 +289,13 @@ def our_arm(args, rank, world, local):
     log("allocating and filling the pinned host store")
     pipe = DecodePipeline(cfg, inp, layers_per_launch=args.layers_per_launch, timing=False)
     log("pipeline ready")
+    if args.profile:
+        pipe.prologue()
+        pipe.run(0, K)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_steps": K, "workload": cfg.name,
+                          "launches_per_step": 4 + 2 * len(pipe.chunks)}))
+        return
 
     # ---- every kernel runs once outside capture (first calls set kernel
     # attributes); then an eager pass reads each step's load counts
