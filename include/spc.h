@@ -233,6 +233,35 @@ int spc_sparse_decode_attn(const void* q, const spc_kv_view* views, const int32_
                            size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * spc_sparse_decode_attn without a caller workspace. The paper has no
+ * counterpart: this exists for callers that cannot allocate device memory --
+ * for example code running under another framework's memory manager, which
+ * reserves the device memory up front so a private cudaMalloc would fail or
+ * escape its accounting, or a decode loop that must not pay for cudaMalloc /
+ * cudaFree and the device-wide synchronisation they can bring.
+ *
+ * Same arguments, computation and limits as spc_sparse_decode_attn, minus the
+ * workspace. Its scratch (split partials and merge counters) lives in a fixed
+ * SPC_ATTN_NOALLOC_SCRATCH_BYTES area of the library's own device memory,
+ * which every GPU that loads the library holds until the process exits; the
+ * call itself allocates nothing. Shapes whose scratch would not fit return
+ * SPC_ERR_WORKSPACE before anything is launched (spc_sparse_decode_attn_
+ * workspace_size() tells the need). The first call on each device looks up the
+ * area's address with that device current; make that first call before any
+ * stream capture. Every call clears the counters it needs (one memset on
+ * `stream`) and then launches the kernel. All calls share the one area: calls
+ * whose work overlaps on the GPU (different streams, or different host
+ * threads without ordering) race on it and give wrong results; order them on
+ * one stream.
+ * ---------------------------------------------------------------------- */
+#define SPC_ATTN_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+int spc_sparse_decode_attn_noalloc(const void* q, const spc_kv_view* views,
+                                   const int32_t* selected, const int32_t* slot_pos, int n_layers,
+                                   int B, int n_q, int n_kv, int d, int budget, float scale,
+                                   float* out, void* stream);
+
+/* ------------------------------------------------------------------------
  * Helpers (no counterpart on the pages).
  * ---------------------------------------------------------------------- */
 

@@ -44,6 +44,8 @@ SIGNATURES = {
     "spc_sparse_decode_attn_workspace_size": (ctypes.c_size_t, [_I] * 6),
     "spc_sparse_decode_attn": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P,
                                     ctypes.c_size_t, _P]),
+    "spc_sparse_decode_attn_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float,
+                                            _P, _P]),
     "spc_host_device_pointer": (_I, [_P, ctypes.POINTER(ctypes.c_void_p)]),
     "spc_stream_read": (_I, [_P, ctypes.c_size_t, _P, _I, _P]),
 }
@@ -159,6 +161,18 @@ def spc_sparse_decode_attn(q, views, selected, slot_pos, n_layers, B, n_q, n_kv,
     _check("spc_sparse_decode_attn", lib().spc_sparse_decode_attn(
         _ptr(q), _ptr(views), _ptr(selected), _ptr(slot_pos), n_layers, B, n_q, n_kv, d, budget,
         float(scale), _ptr(out), _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+SPC_ATTN_NOALLOC_SCRATCH_BYTES = 8 << 20
+
+
+def spc_sparse_decode_attn_noalloc(q, views, selected, slot_pos, n_layers, B, n_q, n_kv, d, budget,
+                                   scale, out, stream=None) -> None:
+    """spc_sparse_decode_attn with the library's fixed scratch area instead of a
+    caller workspace (for callers that cannot allocate device memory)."""
+    _check("spc_sparse_decode_attn_noalloc", lib().spc_sparse_decode_attn_noalloc(
+        _ptr(q), _ptr(views), _ptr(selected), _ptr(slot_pos), n_layers, B, n_q, n_kv, d, budget,
+        float(scale), _ptr(out), _stream(stream)))
 
 
 def spc_host_device_pointer(host) -> int:

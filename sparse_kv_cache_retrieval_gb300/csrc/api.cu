@@ -175,6 +175,18 @@ int spc_sparse_decode_attn(const void* q, const spc_kv_view* views, const int32_
                      workspace, stream);
 }
 
+int spc_sparse_decode_attn_noalloc(const void* q, const spc_kv_view* views, const int32_t* selected,
+                                   const int32_t* slot_pos, int n_layers, int B, int n_q, int n_kv,
+                                   int d, int budget, float scale, float* out, void* stream) {
+  if (!q || !views || !selected || !slot_pos || !out) return SPC_ERR_INVALID_ARG;
+  if (d != SPC_HEAD_DIM || !group_ok(n_q, n_kv)) return SPC_ERR_SHAPE;
+  if (n_layers < 1 || B < 1 || B > SPC_MAX_BATCH || (long long)n_layers * B > 65535) return SPC_ERR_SHAPE;
+  if (n_kv > 65535 || budget < 1 || budget > SPC_MAX_BUDGET) return SPC_ERR_SHAPE;
+  if (!(scale > 0.f)) return SPC_ERR_INVALID_ARG;
+  return attn_noalloc_launch(q, views, selected, slot_pos, n_layers, B, n_q, n_kv, budget, scale, out,
+                             stream);
+}
+
 int spc_host_device_pointer(void* host_ptr, void** device_ptr) {
   if (!host_ptr || !device_ptr) return SPC_ERR_INVALID_ARG;
   void* p = nullptr;

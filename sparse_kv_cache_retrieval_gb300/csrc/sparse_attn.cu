@@ -354,3 +354,54 @@ int attn_launch(const void* q, const spc_kv_view* views, const int32_t* selected
 }
 
 }  // namespace spc
+
+// ============================================================== no-allocation variant
+// Scratch of spc_sparse_decode_attn_noalloc: a fixed area in the library's own
+// device memory, so callers that cannot allocate device memory need not pass a
+// workspace. Every device that loads the library holds these bytes until the
+// process exits. Only host code needs its address (cudaGetSymbolAddress); the
+// name itself is a host-side stand-in and must never be passed to a kernel.
+#include <mutex>
+
+namespace spc {
+
+static __device__ __align__(256) unsigned char g_attn_noalloc_scratch[SPC_ATTN_NOALLOC_SCRATCH_BYTES];
+
+// Device address of the scratch area on the current device, looked up once
+// per device (with that device current) and cached; nullptr on failure.
+static void* attn_noalloc_scratch_address() {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_attn_noalloc_scratch) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+int attn_noalloc_launch(const void* q, const spc_kv_view* views, const int32_t* selected,
+                        const int32_t* slot_pos, int n_layers, int B, int n_q, int n_kv, int budget,
+                        float scale, float* out, void* stream) {
+  if (attn_workspace(n_layers, B, n_q, n_kv, budget) > SPC_ATTN_NOALLOC_SCRATCH_BYTES)
+    return SPC_ERR_WORKSPACE;
+  void* scratch = attn_noalloc_scratch_address();
+  if (!scratch) return SPC_ERR_CUDA;
+  // the split-merge counters must start at zero; the partials are always
+  // written before they are read
+  const size_t nseg = (size_t)n_layers * B * n_kv;
+  if (cudaMemsetAsync(scratch, 0, nseg * sizeof(uint32_t), static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return SPC_ERR_CUDA;
+  return attn_launch(q, views, selected, slot_pos, n_layers, B, n_q, n_kv, budget, scale, out,
+                     scratch, stream);
+}
+
+}  // namespace spc

@@ -40,6 +40,10 @@ int attn_launch(const void* q, const spc_kv_view* views, const int32_t* selected
                 const int32_t* slot_pos, int n_layers, int B, int n_q, int n_kv, int budget,
                 float scale, float* out, void* workspace, void* stream);
 
+int attn_noalloc_launch(const void* q, const spc_kv_view* views, const int32_t* selected,
+                        const int32_t* slot_pos, int n_layers, int B, int n_q, int n_kv, int budget,
+                        float scale, float* out, void* stream);
+
 int stream_read_launch(const void* src, size_t bytes, uint32_t* sink, int n_blocks, void* stream);
 
 int device_sm_count();
