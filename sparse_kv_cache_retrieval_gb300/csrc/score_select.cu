@@ -22,20 +22,17 @@
 //    lane-rotated row order so that a half-warp reduce-scatter needs no
 //    selects; base-2 logits go to scratch and per-warp (max, sum 2^(l-max))
 //    partials give the logsumexp.
-//  * select_kernel: one thread-block cluster (up to 8 CTAs) per (request,
-//    KV head); keys live in shared memory; the logsumexp partials, the 4
-//    radix-select histograms (8-bit digits, warp-aggregated with match.any)
-//    and the compaction counts are combined across the cluster through
-//    distributed shared memory; the ordered compaction keeps positions
-//    ascending and resolves ties at the K-th key to the lower position.
-#include <cooperative_groups.h>
+//  * lse_kernel / score_kernel / topk_kernel: logsumexp per head, the group
+//    score and its order key for every position on the whole GPU with a
+//    per-(request, KV head) histogram of the key's top 11 bits, then one CTA
+//    per (request, KV head) that finds the threshold key (histogram bin, then
+//    two refinement passes over the bin's candidates) and writes the selection
+//    with an ordered compaction (ascending, ties to the lower position).
 #include <cuda_bf16.h>
 #include <math.h>
 
 #include "spc_device.cuh"
 #include "spc_internal.h"
-
-namespace cg = cooperative_groups;
 
 namespace spc {
 
@@ -320,9 +317,8 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
         for (int h = 0; h < S::HB; ++h) {
           const int hq = g * G + hb * S::HB + h;
           if (own) a.logits[((size_t)b * a.n_q + hq) * a.cap + row0 + rloc] = acc[0][h];
-          float mm = own ? acc[0][h] : -INFINITY;
-          float ss = own ? 1.f : 0.f;
-          warp_lse2(mm, ss);
+          const float mm = warp_max(own ? acc[0][h] : -INFINITY);
+          const float ss = warp_sum(own ? exp2f(acc[0][h] - mm) : 0.f);
           if (lane == h)
             a.part[((size_t)b * a.n_q + hq) * a.n_parts + (size_t)tile * S::PPT + warp * S::NB + bt] =
                 make_float2(mm, ss);
@@ -336,199 +332,214 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
   }
 }
 
-// ============================================================== select
+// ============================================================== group score + Top-K
+// Three small kernels replace one long-latency one:
+//  * lse_kernel: one CTA per query head folds the scan's (max, sum) partials
+//    into log2-sum-exp;
+//  * score_kernel: every position of every (request, KV head) in parallel:
+//    s = max_h (l_h - lse_h), the monotone uint32 order key, and a 2048-bin
+//    histogram of the key's top 11 bits (block histogram in shared memory,
+//    flushed to a per-segment global histogram);
+//  * topk_kernel: one CTA per (request, KV head) finds the bin holding the
+//    (K-|F|)-th largest key, refines the remaining 21 bits over the bin's
+//    candidates (gathered in shared memory; global fallback for huge ties),
+//    then writes the selection with an ordered two-pass compaction (ties at
+//    the threshold key to the lower positions). It leaves the global
+//    histogram zeroed for the next call.
+constexpr int kHistBins = 2048;
+constexpr int kScoreThreads = 256;
+constexpr int kScorePos = 2048;        // positions per score block
+constexpr int kTopkThreads = 1024;
+constexpr int kCandMax = 8192;
+
 struct SelArgs {
   const float* logits;
   const float2* part;
+  float* lse2;
+  uint32_t* keys;
+  uint32_t* ghist;
   int32_t* len;
   float* scores_out;
   int32_t* selected;
   uint32_t* done;
-  int B, n_q, n_kv, G, cap, K, n_sink, n_recent, append, P, n_parts, ppt;
+  int B, n_q, n_kv, G, cap, K, n_sink, n_recent, append, n_parts, ppt;
 };
-
-constexpr int kSelThreads = 512;
 
 __device__ __forceinline__ bool is_forced(int p, int L, int n_sink, int n_recent) {
   return p < n_sink || p >= L - n_recent;
 }
 
-__global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a) {
-  cg::cluster_group cluster = cg::this_cluster();
-  const int C = (int)cluster.num_blocks();
-  const int cr = (int)cluster.block_rank();
-  const int seg = blockIdx.x / C;
-  const int b = seg / a.n_kv, g = seg - b * a.n_kv;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-
-  extern __shared__ uint32_t keys[];          // [P]
-  __shared__ uint32_t hist[2][256];
-  __shared__ float lse_m[SPC_MAX_GROUP], lse_s[SPC_MAX_GROUP], lse2[SPC_MAX_GROUP];
-  __shared__ int scratch[33];
-  __shared__ int s_digit, s_rem, s_last;
-  __shared__ int s_counts[2];
-
+__global__ void __launch_bounds__(256) lse_kernel(SelArgs a) {
+  const int bh = blockIdx.x, b = bh / a.n_q;
   const int L = effective_len(a.len, b, a.append, a.cap);
-  const int lo = cr * a.P;
-  const int hi = min(lo + a.P, L);
-  int32_t* out = a.selected + (size_t)seg * a.K;
-
-  // ---- 1. logsumexp per query head of the group, partials split over the cluster
-  const int n_valid_parts = ((L + kScanRows - 1) / kScanRows) * a.ppt;
-  for (int h = warp; h < a.G; h += kSelThreads / 32) {
-    const float2* ph = a.part + ((size_t)b * a.n_q + (size_t)g * a.G + h) * a.n_parts;
-    float m = -INFINITY, s = 0.f;
-    for (int i = cr * 32 + lane; i < n_valid_parts; i += C * 32) {
-      const float2 v = __ldcg(ph + i);
-      lse2_combine(m, s, v.x, v.y);
-    }
-    warp_lse2(m, s);
-    if (lane == 0) { lse_m[h] = m; lse_s[h] = s; }
+  const int nv = ((L + kScanRows - 1) / kScanRows) * a.ppt;
+  const float2* ph = a.part + (size_t)bh * a.n_parts;
+  float m = -INFINITY, s = 0.f;
+  for (int i = threadIdx.x; i < nv; i += 256) {
+    const float2 v = __ldcg(ph + i);
+    lse2_combine(m, s, v.x, v.y);
   }
-  cluster.sync();
-  if (tid < a.G) {
-    float m = -INFINITY, s = 0.f;
-    for (int c = 0; c < C; ++c)
-      lse2_combine(m, s, *cluster.map_shared_rank(&lse_m[tid], c), *cluster.map_shared_rank(&lse_s[tid], c));
-    lse2[tid] = (s > 0.f) ? m + log2f(s) : INFINITY;
-  }
+  warp_lse2(m, s);
+  __shared__ float sm[8], ss[8];
+  if ((threadIdx.x & 31) == 0) { sm[threadIdx.x >> 5] = m; ss[threadIdx.x >> 5] = s; }
   __syncthreads();
+  if (threadIdx.x == 0) {
+    float M = -INFINITY, Sx = 0.f;
+    for (int w = 0; w < 8; ++w) lse2_combine(M, Sx, sm[w], ss[w]);
+    a.lse2[bh] = Sx > 0.f ? M + log2f(Sx) : INFINITY;
+  }
+}
 
-  // ---- 2. group score s = max_h (l_h - lse_h) (base 2) and order keys
+__global__ void __launch_bounds__(kScoreThreads) score_kernel(SelArgs a) {
+  const int seg = blockIdx.y, b = seg / a.n_kv, g = seg - b * a.n_kv;
+  const int L = effective_len(a.len, b, a.append, a.cap);
+  const int p0 = blockIdx.x * kScorePos;
+  if (p0 >= L) return;
+  __shared__ uint32_t hist[kHistBins];
+  __shared__ float lse[SPC_MAX_GROUP];
+  const int tid = threadIdx.x, lane = tid & 31;
+  for (int i = tid; i < kHistBins; i += kScoreThreads) hist[i] = 0u;
+  for (int h = tid; h < a.G; h += kScoreThreads) lse[h] = a.lse2[(size_t)b * a.n_q + (size_t)g * a.G + h];
+  __syncthreads();
   const float* lg = a.logits + ((size_t)b * a.n_q + (size_t)g * a.G) * a.cap;
-  for (int i = tid; i < a.P; i += kSelThreads) {
-    const int p = lo + i;
-    uint32_t key = 0;
+  constexpr int PER = kScorePos / kScoreThreads;  // 8
+  uint32_t key[PER];
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int p = p0 + k * kScoreThreads + tid;
+    key[k] = 0u;
     if (p < L) {
       float sc = -INFINITY;
-      for (int h = 0; h < a.G; ++h) sc = fmaxf(sc, __ldcg(lg + (size_t)h * a.cap + p) - lse2[h]);
+      for (int h = 0; h < a.G; ++h) sc = fmaxf(sc, __ldcg(lg + (size_t)h * a.cap + p) - lse[h]);
       if (a.scores_out) a.scores_out[(size_t)seg * a.cap + p] = exp2f(sc);
-      if (!is_forced(p, L, a.n_sink, a.n_recent)) key = order_key(sc);
+      if (!is_forced(p, L, a.n_sink, a.n_recent)) key[k] = order_key(sc);
+      a.keys[(size_t)seg * a.cap + p] = key[k];
     }
-    keys[i] = key;
   }
+  if (L > a.K) {
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      const int bin = key[k] ? int(key[k] >> 21) : kHistBins;
+      const unsigned peers = __match_any_sync(0xffffffffu, bin);
+      if (bin < kHistBins && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
+    }
+    __syncthreads();
+    uint32_t* gh = a.ghist + (size_t)seg * kHistBins;
+    for (int i = tid; i < kHistBins; i += kScoreThreads)
+      if (hist[i]) atomicAdd(&gh[i], hist[i]);
+  }
+}
+
+// Bin (scanning from the top) where the running count reaches `rem`, over
+// `nbins` counts held in shared memory; returns (bin, rem - count above it).
+// Every thread of the block calls it. nbins <= 2 * blockDim.x.
+__device__ __forceinline__ void find_bin(const uint32_t* cnt, int nbins, int rem, int* scratch,
+                                         int* s_bin, int* s_rem) {
+  const int t = threadIdx.x;
+  const int bA = nbins - 1 - 2 * t, bB = nbins - 2 - 2 * t;  // descending pair
+  const int cA = bA >= 0 ? (int)cnt[bA] : 0, cB = bB >= 0 ? (int)cnt[bB] : 0;
+  int tot;
+  const int before = block_excl_scan(cA + cB, scratch, &tot);
+  if (bA >= 0 && before < rem && before + cA >= rem) { *s_bin = bA; *s_rem = rem - before; }
+  if (bB >= 0 && before + cA < rem && before + cA + cB >= rem) { *s_bin = bB; *s_rem = rem - before - cA; }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kTopkThreads) topk_kernel(SelArgs a) {
+  const int seg = blockIdx.x, b = seg / a.n_kv;
+  const int L = effective_len(a.len, b, a.append, a.cap);
+  const int tid = threadIdx.x, lane = tid & 31;
+  int32_t* out = a.selected + (size_t)seg * a.K;
+  const uint32_t* keys = a.keys + (size_t)seg * a.cap;
+  uint32_t* gh = a.ghist + (size_t)seg * kHistBins;
+  __shared__ uint32_t hist[kHistBins];
+  __shared__ uint32_t cand[kCandMax];
+  __shared__ int scratch[33];
+  __shared__ int s_bin, s_rem, s_cnt, s_last;
 
   if (L <= a.K) {
-    // everything fits in the budget: keep [0, L), pad with -1
-    for (int p = lo + tid; p < hi; p += kSelThreads) out[p] = p;
-    if (cr == 0)
-      for (int i = L + tid; i < a.K; i += kSelThreads) out[i] = -1;
+    for (int p = tid; p < a.K; p += kTopkThreads) out[p] = p < L ? p : -1;
   } else {
-    __syncthreads();
-    // ---- 3. radix select of the (K - |F|)-th largest key, 8-bit digits
     const int Kp = a.K - (a.n_sink + a.n_recent);
-    uint32_t prefix = 0, mask = 0;
-    int rem = Kp;
+    uint32_t T = 0xffffffffu;
+    int need = 0;
+    // global histogram of the top 11 bits -> shared memory; leave it zeroed
+    for (int i = tid; i < kHistBins; i += kTopkThreads) { hist[i] = gh[i]; gh[i] = 0u; }
+    if (tid == 0) s_cnt = 0;
+    __syncthreads();
     if (Kp > 0) {
-      for (int pass = 0; pass < 4; ++pass) {
-        const int shift = 24 - 8 * pass;
-        uint32_t* hb = hist[pass & 1];
-        if (tid < 256) hb[tid] = 0;
-        __syncthreads();
-        for (int base = 0; base < a.P; base += kSelThreads) {
-          const int i = base + tid;
-          const uint32_t key = i < a.P ? keys[i] : 0u;
-          const int digit = (key != 0u && (key & mask) == prefix) ? int((key >> shift) & 255u) : 256;
-          const unsigned peers = __match_any_sync(0xffffffffu, digit);
-          if (digit < 256 && lane == __ffs(peers) - 1) atomicAdd(&hb[digit], (uint32_t)__popc(peers));
-        }
-        cluster.sync();
-        // suffix counts over digits 255..0; thread t handles digit 255 - t
-        int tot = 0;
-        if (tid < 256)
-          for (int c = 0; c < C; ++c) tot += (int)*cluster.map_shared_rank(&hb[255 - tid], c);
-        const int incl = warp_incl_scan(tot);
-        if (lane == 31 && warp < 8) scratch[warp] = incl;
-        __syncthreads();
-        if (tid < 256) {
-          int before = 0;
-          for (int w = 0; w < warp; ++w) before += scratch[w];
-          const int sfx = before + incl;  // keys with digit >= 255 - tid
-          if (sfx >= rem && sfx - tot < rem) {
-            s_digit = 255 - tid;
-            s_rem = rem - (sfx - tot);
+      find_bin(hist, kHistBins, Kp, scratch, &s_bin, &s_rem);
+      const uint32_t b1 = (uint32_t)s_bin;
+      int rem = s_rem;
+      const int n1 = (int)hist[b1];
+      const bool local = n1 <= kCandMax;
+      if (local) {
+        for (int p = tid; p < L; p += kTopkThreads) {
+          const uint32_t k = keys[p];
+          if (k && (k >> 21) == b1) {
+            const int j = atomicAdd(&s_cnt, 1);
+            if (j < kCandMax) cand[j] = k;
           }
         }
+      }
+      __syncthreads();
+      // two refinement passes: bits 20..10, then 9..0
+      uint32_t prefix = b1 << 21, mask = 0xffe00000u;
+      for (int pass = 0; pass < 2; ++pass) {
+        const int shift = pass == 0 ? 10 : 0;
+        const int nb = pass == 0 ? 2048 : 1024;
+        const uint32_t dmask = (uint32_t)nb - 1u;
+        for (int i = tid; i < kHistBins; i += kTopkThreads) hist[i] = 0u;
         __syncthreads();
-        prefix |= (uint32_t)s_digit << shift;
-        mask |= 255u << shift;
+        const int n = local ? min(s_cnt, kCandMax) : L;
+        for (int base = 0; base < n; base += kTopkThreads) {
+          const int i = base + tid;
+          uint32_t k = 0u;
+          if (i < n) k = local ? cand[i] : keys[i];
+          const int d = (k && (k & mask) == prefix) ? int((k >> shift) & dmask) : nb;
+          const unsigned peers = __match_any_sync(0xffffffffu, d);
+          if (d < nb && lane == __ffs(peers) - 1) atomicAdd(&hist[d], (uint32_t)__popc(peers));
+        }
+        __syncthreads();
+        find_bin(hist, nb, rem, scratch, &s_bin, &s_rem);
+        prefix |= (uint32_t)s_bin << shift;
+        mask |= dmask << shift;
         rem = s_rem;
         __syncthreads();
       }
-    } else {
-      prefix = 0xffffffffu;
-      rem = 0;
+      T = prefix;
+      need = rem;
     }
-    const uint32_t T = prefix;
-    const int need_eq = rem;
-
-    // ---- 4. per-CTA counts, exchanged across the cluster
-    int n_base = 0, n_eq = 0;
-    for (int i = tid; i < a.P; i += kSelThreads) {
-      const int p = lo + i;
-      if (p >= L) break;
-      const uint32_t key = keys[i];
-      if (is_forced(p, L, a.n_sink, a.n_recent) || (key != 0u && key > T)) ++n_base;
-      else if (Kp > 0 && key != 0u && key == T) ++n_eq;
+    // ordered compaction: thread t owns the contiguous positions [lo, hi)
+    const int chunk = (L + kTopkThreads - 1) / kTopkThreads;
+    const int lo = min(L, tid * chunk), hi = min(L, lo + chunk);
+    int nb_ = 0, ne_ = 0;
+    for (int p = lo; p < hi; ++p) {
+      const uint32_t k = keys[p];
+      if (is_forced(p, L, a.n_sink, a.n_recent) || (k && k > T)) ++nb_;
+      else if (Kp > 0 && k && k == T) ++ne_;
     }
-    int tb_total, te_total;
-    block_excl_scan(n_base, scratch, &tb_total);
-    block_excl_scan(n_eq, scratch, &te_total);
-    if (tid == 0) { s_counts[0] = tb_total; s_counts[1] = te_total; }
-    cluster.sync();
-    int out_base = 0, eq_before = 0;
-    for (int c = 0; c < cr; ++c) {
-      const int cb = *cluster.map_shared_rank(&s_counts[0], c);
-      const int ce = *cluster.map_shared_rank(&s_counts[1], c);
-      const int take_c = max(0, min(need_eq - eq_before, ce));
-      out_base += cb + take_c;
-      eq_before += ce;
-    }
-    const int take = max(0, min(need_eq - eq_before, te_total));
-
-    // ---- 5. ordered compaction, 4 consecutive positions per thread per round
-    int run_eq = 0, run_sel = 0;
-    for (int base = 0; base < a.P; base += kSelThreads * 4) {
-      const int i0 = base + tid * 4;
-      uint32_t kk[4];
-      bool forced[4];
-      int ecount = 0;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int i = i0 + k, p = lo + i;
-        const bool in = (i < a.P) && (p < L);
-        kk[k] = in ? keys[i] : 0u;
-        forced[k] = in && is_forced(p, L, a.n_sink, a.n_recent);
-        ecount += (Kp > 0 && kk[k] != 0u && kk[k] == T) ? 1 : 0;
+    int tb, te;
+    const int base_b = block_excl_scan(nb_, scratch, &tb);
+    const int base_e = block_excl_scan(ne_, scratch, &te);
+    int o = base_b + min(base_e, need);
+    int eq_seen = base_e;
+    for (int p = lo; p < hi; ++p) {
+      const uint32_t k = keys[p];
+      bool sel = is_forced(p, L, a.n_sink, a.n_recent) || (k && k > T);
+      if (!sel && Kp > 0 && k && k == T) {
+        sel = eq_seen < need;
+        ++eq_seen;
       }
-      int etot;
-      int erank = run_eq + block_excl_scan(ecount, scratch, &etot);
-      bool sel[4];
-      int scount = 0;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const bool eq = (Kp > 0 && kk[k] != 0u && kk[k] == T);
-        const bool gt = (kk[k] != 0u && kk[k] > T);
-        sel[k] = forced[k] || gt || (eq && erank < take);
-        if (eq) ++erank;
-        scount += sel[k] ? 1 : 0;
+      if (sel) {
+        if (o < a.K) out[o] = p;
+        ++o;
       }
-      int stot;
-      int srank = run_sel + block_excl_scan(scount, scratch, &stot);
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        if (sel[k]) {
-          if (out_base + srank < a.K) out[out_base + srank] = lo + i0 + k;
-          ++srank;
-        }
-      run_eq += etot;
-      run_sel += stot;
     }
   }
-  // keep this CTA's shared memory alive until every remote read is done
-  cluster.sync();
 
   if (a.append) {
+    __syncthreads();
     if (tid == 0) {
       __threadfence();
       s_last = (atomicAdd(a.done, 1u) == gridDim.x - 1);
@@ -536,7 +547,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a) {
     __syncthreads();
     if (s_last) {
       __threadfence();
-      for (int bb = tid; bb < a.B; bb += kSelThreads) {
+      for (int bb = tid; bb < a.B; bb += kTopkThreads) {
         const int L0 = a.len[bb];
         if (L0 >= 0 && L0 < a.cap) a.len[bb] = L0 + 1;
       }
@@ -547,7 +558,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a) {
 
 // ============================================================== host side
 struct ScoreLayout {
-  size_t status, done, counters, q, part_proj, logits, part_scan, total;
+  size_t status, done, counters, q, part_proj, logits, part_scan, lse, keys, hist, total;
   int S, Hc, n_col_tiles, bz, n_tiles, ppt, n_parts;
 };
 
@@ -577,6 +588,9 @@ static ScoreLayout score_layout(int B, int H, int n_q, int n_kv, int cap) {
   l.part_proj = take(sizeof(float) * (size_t)l.S * B * Ntot);
   l.logits = take(sizeof(float) * (size_t)B * n_q * cap);
   l.part_scan = take(sizeof(float2) * (size_t)B * n_q * l.n_parts);
+  l.lse = take(sizeof(float) * (size_t)B * n_q);
+  l.keys = take(sizeof(uint32_t) * (size_t)B * n_kv * cap);
+  l.hist = take(sizeof(uint32_t) * (size_t)B * n_kv * kHistBins);
   l.total = off;
   return l;
 }
@@ -675,11 +689,14 @@ int score_select_launch(const ScoreSelectCall& c) {
     if (e != cudaSuccess) return SPC_ERR_CUDA;
   }
 
-  // ---- group score + select (one cluster per (request, KV head))
+  // ---- logsumexp, group score + histogram, Top-K
   if (c.stages & SPC_STAGE_SELECT) {
     SelArgs sa{};
     sa.logits = reinterpret_cast<const float*>(ws + l.logits);
     sa.part = reinterpret_cast<const float2*>(ws + l.part_scan);
+    sa.lse2 = reinterpret_cast<float*>(ws + l.lse);
+    sa.keys = reinterpret_cast<uint32_t*>(ws + l.keys);
+    sa.ghist = reinterpret_cast<uint32_t*>(ws + l.hist);
     sa.len = c.len;
     sa.scores_out = c.scores_out;
     sa.selected = c.selected;
@@ -687,32 +704,13 @@ int score_select_launch(const ScoreSelectCall& c) {
     sa.B = c.B; sa.n_q = c.n_q; sa.n_kv = c.n_kv; sa.G = G; sa.cap = c.cap; sa.K = c.budget;
     sa.n_sink = c.n_sink; sa.n_recent = c.n_recent; sa.append = c.append;
     sa.n_parts = l.n_parts; sa.ppt = l.ppt;
-    int C = (c.cap + 8191) / 8192;
-    C = C < 1 ? 1 : (C > 8 ? 8 : C);
-    int P = (c.cap + C - 1) / C;
-    P = (P + 3) & ~3;
-    sa.P = P;
-    const size_t smem = sizeof(uint32_t) * (size_t)P;
-    static size_t attr = 0;
-    if (smem > attr) {
-      e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return SPC_ERR_CUDA;
-      attr = smem;
-    }
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(c.B * c.n_kv * C);
-    cfg.blockDim = dim3(kSelThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = C;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, select_kernel, sa);
-    if (e != cudaSuccess) return SPC_ERR_CUDA;
+    lse_kernel<<<c.B * c.n_q, 256, 0, st>>>(sa);
+    if (cudaGetLastError() != cudaSuccess) return SPC_ERR_CUDA;
+    const dim3 sg((c.cap + kScorePos - 1) / kScorePos, c.B * c.n_kv);
+    score_kernel<<<sg, kScoreThreads, 0, st>>>(sa);
+    if (cudaGetLastError() != cudaSuccess) return SPC_ERR_CUDA;
+    topk_kernel<<<c.B * c.n_kv, kTopkThreads, 0, st>>>(sa);
+    if (cudaGetLastError() != cudaSuccess) return SPC_ERR_CUDA;
   }
   return SPC_OK;
 }

@@ -7,32 +7,49 @@
 // Context Sparsity in LLMs" (paperlayer.ai summary) §4.3 (for GQA the selected
 // KV serves every query head of its group).
 //
-// GB300 design: the kept rows of one (layer, request, KV head) are split into
-// chunks of 64 rows; a CTA walks a contiguous range of chunks with a 2-stage
-// cp.async pipeline (16-byte copies; invalid rows are zero-filled), computes
-// the G heads' base-2 scores with the lane-rotated half-warp reduce-scatter
-// (one load of each K row serves the whole group), keeps an online softmax
-// per head, and accumulates P.V with every thread owning (head, 8 columns)
-// pairs so V rows are read once per row group. Split ranges are merged by the
-// last CTA of the (layer, request, KV head), in split order (deterministic).
+// GB300 design. Work item = a contiguous range of 64-row chunks of one
+// (layer, request, KV head). Persistent CTAs of 4 consumer warps + 1 producer
+// warp walk their items in a static round-robin:
+//  * the producer streams each chunk's K and V rows into a 3-stage shared-
+//    memory ring with cp.async.bulk (TMA engine, mbarrier byte counts): one
+//    16 KiB copy per tensor in slot mode (slots are contiguous), one 256-byte
+//    copy per kept row in position mode; it publishes a 64-bit mask of the
+//    chunk's valid rows and runs ahead across item boundaries;
+//  * consumers form the G heads' base-2 scores with a lane-rotated half-warp
+//    reduce-scatter (each K row is read from shared memory once for the whole
+//    group), update an online softmax per head (two named barriers per chunk),
+//    and accumulate P.V in registers that persist across chunks, each thread
+//    owning (heads, 8 columns) so a V row is read once per row group;
+//  * an item's (max, sum, unnormalised output) is either the result or a
+//    partial that the last CTA of its (layer, request, KV head) merges, in
+//    split order (deterministic).
 #include "spc_device.cuh"
 #include "spc_internal.h"
 
 namespace spc {
 
-constexpr int kAttnThreads = 256;
-constexpr int kAttnRows = 64;
-constexpr int kAttnTargetCtas = 608;  // split so one launch fills the GPU ~4 CTAs deep
-constexpr size_t kAttnStageBytes = (size_t)kAttnRows * kRowBytes;  // 16 KiB
+constexpr int kAttnRows = 64;                       // rows per chunk
+constexpr int kAttnCWarps = 4;                      // consumer warps
+constexpr int kAttnCThreads = kAttnCWarps * 32;     // 128
+constexpr int kAttnThreads = kAttnCThreads + 32;    // + producer warp
+constexpr int kAttnStages = 3;
+constexpr uint32_t kAttnTileBytes = kAttnRows * kRowBytes;  // 16 KiB (K or V)
+constexpr int kAttnItemsPerCta = 2;                 // split target: ~2 items per resident CTA
+constexpr long long kAttnWait = 4000000000ll;
 
 template <int G>
 struct AttnShape {
-  static constexpr int HB = G < 8 ? G : 8;
+  static constexpr int HB = G < 8 ? G : 8;          // heads per register block
   static constexpr int NHB = G / HB;
-  static constexpr int PAIRS = G * 16;
-  static constexpr int TPG = PAIRS < kAttnThreads ? PAIRS : kAttnThreads;
-  static constexpr int RG = kAttnThreads / TPG;
-  static constexpr int PPT = PAIRS / TPG;
+  static constexpr int R = HB <= 4 ? 8 : 4;         // rows per half-warp QK batch
+  static constexpr int NB = 8 / R;                  // batches (8 rows per half-warp per chunk)
+  static constexpr int PAIRS = NHB * 16;            // (head block, 8-column chunk) pairs
+  static constexpr int TPG = PAIRS < kAttnCThreads ? PAIRS : kAttnCThreads;
+  static constexpr int RG = kAttnCThreads / TPG;    // row groups in P.V
+  static constexpr int PPT = PAIRS / TPG;           // pairs per thread
+  // row-group partial sums left after folding lanes l and l^16 (TPG <= 16)
+  static constexpr int NRED = TPG <= 16 ? RG / 2 : RG;
+  static constexpr int CTAS_PER_SM = G <= 8 ? 2 : 1;
 };
 
 struct AttnArgs {
@@ -43,245 +60,360 @@ struct AttnArgs {
   float* out;
   float* part;
   uint32_t* counters;
-  int B, n_q, n_kv, K, n_split, cps, n_chunks;
+  int* status;
+  int B, n_q, n_kv, K, n_split, cps, n_chunks, n_items;
   float scale2;
 };
 
 template <int G>
+struct AttnSmem {
+  static constexpr size_t stages = (size_t)kAttnStages * 2 * kAttnTileBytes;
+  static constexpr size_t q = sizeof(float) * G * kD;
+  static constexpr size_t sc = sizeof(float) * G * kAttnRows;       // raw scores [G][64]
+  static constexpr size_t pt = sizeof(float) * kAttnRows * G;       // weights [64][G]
+  static constexpr size_t ored = sizeof(float) * AttnShape<G>::NRED * G * kD;
+  static constexpr size_t small = sizeof(float) * 4 * 64 + sizeof(uint64_t) * (3 * kAttnStages);
+  static constexpr size_t total = stages + q + sc + pt + ored + small;
+};
+
+__device__ __forceinline__ void cons_bar() { asm volatile("bar.sync 1, %0;" :: "n"(kAttnCThreads) : "memory"); }
+
+template <int G>
+__device__ __forceinline__ void item_coords(const AttnArgs& a, int item, int& lb, int& g, int& split) {
+  split = item % a.n_split;
+  const int rest = item / a.n_split;
+  g = rest % a.n_kv;
+  lb = rest / a.n_kv;
+}
+
+template <int G>
 __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
   using S = AttnShape<G>;
+  using M = AttnSmem<G>;
   extern __shared__ __align__(128) uint8_t asmem[];
-  uint4* Ks = reinterpret_cast<uint4*>(asmem);                          // [2][64][16]
-  uint4* Vs = reinterpret_cast<uint4*>(asmem + 2 * kAttnStageBytes);    // [2][64][16]
-  float* q_s = reinterpret_cast<float*>(asmem + 4 * kAttnStageBytes);   // [G][128]
-  float* sc = q_s + G * kD;                                             // [G][64]
-  float* m_s = sc + G * kAttnRows;                                      // [G]
-  float* l_s = m_s + G;                                                 // [G]
-  float* al_s = l_s + G;                                                // [G]
-  int* rowok = reinterpret_cast<int*>(al_s + G);                        // [2][64]
+  uint4* stage_kv = reinterpret_cast<uint4*>(asmem);                       // [stage][K|V][64][16]
+  float* q_s = reinterpret_cast<float*>(asmem + M::stages);                // [G][128]
+  float* sc = reinterpret_cast<float*>(asmem + M::stages + M::q);         // [G][64]
+  float* pT = reinterpret_cast<float*>(asmem + M::stages + M::q + M::sc); // [64][G]
+  float* ored = reinterpret_cast<float*>(asmem + M::stages + M::q + M::sc + M::pt);
+  float* m_s = reinterpret_cast<float*>(asmem + M::stages + M::q + M::sc + M::pt + M::ored);
+  float* l_s = m_s + 64;
+  float* al_s = l_s + 64;
+  uint64_t* okmask = reinterpret_cast<uint64_t*>(al_s + 128);
+  uint64_t* full = okmask + kAttnStages;
+  uint64_t* empty = full + kAttnStages;
   __shared__ int s_last;
 
-  const int split = blockIdx.x, g = blockIdx.y, lb = blockIdx.z;
-  const int b = lb % a.B;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, l16 = lane & 15;
-  const spc_kv_view vw = a.views[lb];
-  const size_t seg = (size_t)b * a.n_kv + g;
-  const int32_t* idx = (vw.use_slots ? a.slot_pos : a.selected) + seg * a.K;
-  const uint16_t* kbase = static_cast<const uint16_t*>(vw.k) + (size_t)g * vw.rows * kD;
-  const uint16_t* vbase = static_cast<const uint16_t*>(vw.v) + (size_t)g * vw.rows * kD;
-  const int c0 = split * a.cps;
-  const int c1 = min(c0 + a.cps, a.n_chunks);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < kAttnStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kAttnCWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
 
-  // q for the group, base-2 scaled
-  const uint16_t* qg = a.q + ((size_t)lb * a.n_q + (size_t)g * G) * kD;
-  for (int i = tid; i < G * kD; i += kAttnThreads)
-    q_s[i] = __uint_as_float(uint32_t(qg[i]) << 16) * a.scale2;
-  for (int h = tid; h < G; h += kAttnThreads) { m_s[h] = -INFINITY; l_s[h] = 0.f; }
-
-  auto issue = [&](int c, int st) {
+  if (warp == kAttnCWarps) {
+    // ================= producer warp
+    int it = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
+      int lb, g, split;
+      item_coords<G>(a, item, lb, g, split);
+      const spc_kv_view vw = a.views[lb];
+      const int b = lb % a.B;
+      const int32_t* idx = (vw.use_slots ? a.slot_pos : a.selected) + ((size_t)b * a.n_kv + g) * a.K;
+      const uint16_t* kb = static_cast<const uint16_t*>(vw.k) + (size_t)g * vw.rows * kD;
+      const uint16_t* vb = static_cast<const uint16_t*>(vw.v) + (size_t)g * vw.rows * kD;
+      const int c0 = split * a.cps, c1 = min(c0 + a.cps, a.n_chunks);
+      for (int c = c0; c < c1; ++c, ++it) {
+        const int s = it % kAttnStages;
+        const uint32_t ph = (it / kAttnStages) & 1;
+        if (!mbar_wait_bounded(&empty[s], ph ^ 1, kAttnWait)) {
+          if (lane == 0) set_status(a.status, SPC_ERR_TIMEOUT);
+          ok = false;
+          break;
+        }
+        // row validity and source row for this lane's two rows
+        int src[2];
+        bool val[2];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int id = tid + k * kAttnThreads;
-      const int r = id >> 5, part = id & 31, kv = part >> 4, ch = part & 15;
-      const int i = c * kAttnRows + r;
-      long long row = -1;
-      if (i < a.K) {
-        const int v = idx[i];
-        if (v >= 0) row = vw.use_slots ? i : v;
-        if (row >= vw.rows) row = -1;
+        for (int h = 0; h < 2; ++h) {
+          const int r = lane + 32 * h, i = c * kAttnRows + r;
+          long long row = -1;
+          if (i < a.K) {
+            const int v = idx[i];
+            if (v >= 0) row = vw.use_slots ? i : v;
+            if (row >= vw.rows) row = -1;
+          }
+          val[h] = row >= 0;
+          src[h] = (int)(row < 0 ? 0 : row);
+        }
+        const uint32_t lo = __ballot_sync(0xffffffffu, val[0]);
+        const uint32_t hi = __ballot_sync(0xffffffffu, val[1]);
+        uint4* kdst = stage_kv + (size_t)s * 2 * kAttnRows * 16;
+        uint4* vdst = kdst + kAttnRows * 16;
+        if (vw.use_slots) {
+          // contiguous slots [c*64, min(K, c*64+64)): one copy per tensor
+          const int n_in = min(kAttnRows, a.K - c * kAttnRows);
+          if (lane == 0) {
+            okmask[s] = ((uint64_t)hi << 32) | lo;
+            mbar_arrive_expect_tx(&full[s], 2u * n_in * kRowBytes);
+            bulk_g2s(kdst, kb + (size_t)c * kAttnRows * kD, n_in * kRowBytes, &full[s]);
+            bulk_g2s(vdst, vb + (size_t)c * kAttnRows * kD, n_in * kRowBytes, &full[s]);
+          }
+        } else {
+          const int nval = __popc(lo) + __popc(hi);
+          if (lane == 0) {
+            okmask[s] = ((uint64_t)hi << 32) | lo;
+            mbar_arrive_expect_tx(&full[s], 2u * nval * kRowBytes);
+          }
+          __syncwarp();
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            if (val[h]) {
+              const int r = lane + 32 * h;
+              bulk_g2s(kdst + r * 16, kb + (size_t)src[h] * kD, kRowBytes, &full[s]);
+              bulk_g2s(vdst + r * 16, vb + (size_t)src[h] * kD, kRowBytes, &full[s]);
+            }
+          }
+        }
+        __syncwarp();
       }
-      const uint16_t* src = (kv ? vbase : kbase) + (size_t)(row < 0 ? 0 : row) * kD + ch * 8;
-      uint4* dst = (kv ? Vs : Ks) + ((size_t)st * kAttnRows + r) * 16 + ch;
-      cp_async16(dst, src, row < 0 ? 0 : 16);
-      if (part == 0) rowok[st * kAttnRows + r] = row >= 0;
     }
-  };
-
-  // thread roles in P.V: (head, 8-column chunk) pairs, rows split over RG groups
-  const int rg = tid / S::TPG, tp = tid - rg * S::TPG;
-  const int cc = tp & 15, hbase = tp >> 4;
-  float acc[S::PPT][8];
-#pragma unroll
-  for (int k = 0; k < S::PPT; ++k)
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc[k][e] = 0.f;
-
-  float qr[S::HB][8];
-  const int hw = tid >> 4;  // half-warp 0..15 -> rows [hw*4, hw*4+4)
-
-  if (c0 < c1) {
-    issue(c0, 0);
-    cp_async_commit();
-  }
-  __syncthreads();  // q_s ready
-  if (S::NHB == 1) {
-#pragma unroll
-    for (int h = 0; h < S::HB; ++h)
-#pragma unroll
-      for (int e = 0; e < 8; ++e) qr[h][e] = q_s[h * kD + l16 * 8 + e];
+    // wait (bounded) for the copies still in flight before leaving
+    if (lane == 0)
+      for (int k = max(0, it - kAttnStages); k < it; ++k)
+        mbar_wait_bounded(&full[k % kAttnStages], (k / kAttnStages) & 1, kAttnWait);
+    return;
   }
 
-  for (int c = c0; c < c1; ++c) {
-    const int st = (c - c0) & 1;
-    if (c + 1 < c1) {
-      issue(c + 1, st ^ 1);
-      cp_async_commit();
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
+  // ================= consumers (128 threads)
+  const int ctid = tid;                        // 0..127
+  const int hw = ctid >> 4, l16 = ctid & 15;   // half-warp 0..7 -> rows [hw*8, hw*8+8)
+  const int rg = ctid / S::TPG, tp = ctid - rg * S::TPG;
+  const int cc = tp & 15, hbp = tp >> 4;       // column chunk, first head block of this thread
+  int it = 0;
+  bool dead = false;  // a wait gave up: keep the barrier sequence, skip further waits
+  for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
+    int lb, g, split;
+    item_coords<G>(a, item, lb, g, split);
+    const int c0 = split * a.cps, c1 = min(c0 + a.cps, a.n_chunks);
 
-    // ---- scores: 4 rows per half-warp, all heads of the group
-    const uint4* kt = Ks + (size_t)st * kAttnRows * 16;
+    // q of the group (base-2 scaled) and softmax state
+    cons_bar();  // previous item's readers of q_s / m_s are done
+    const uint16_t* qg = a.q + ((size_t)lb * a.n_q + (size_t)g * G) * kD;
+    for (int i = ctid; i < G * kD; i += kAttnCThreads) q_s[i] = __uint_as_float(uint32_t(qg[i]) << 16) * a.scale2;
+    for (int h = ctid; h < G; h += kAttnCThreads) { m_s[h] = -INFINITY; l_s[h] = 0.f; }
+    cons_bar();
+    float qr[S::HB][8];
+    if (S::NHB == 1) {
+#pragma unroll
+      for (int h = 0; h < S::HB; ++h)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) qr[h][e] = q_s[h * kD + l16 * 8 + e];
+    }
+    float acc[S::PPT][S::HB][8];
+#pragma unroll
+    for (int k = 0; k < S::PPT; ++k)
+#pragma unroll
+      for (int h = 0; h < S::HB; ++h)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[k][h][e] = 0.f;
+
+    for (int c = c0; c < c1; ++c, ++it) {
+      const int s = it % kAttnStages;
+      const uint32_t ph = (it / kAttnStages) & 1;
+      if (!dead && !mbar_wait_bounded(&full[s], ph, kAttnWait)) {
+        if (lane == 0) set_status(a.status, SPC_ERR_TIMEOUT);
+        dead = true;
+      }
+      const uint64_t okm = dead ? 0ull : okmask[s];
+      const uint4* kt = stage_kv + (size_t)s * 2 * kAttnRows * 16;
+      const uint4* vt = kt + kAttnRows * 16;
+
+      // ---- scores, 8 rows per half-warp
 #pragma unroll 1
-    for (int hb = 0; hb < S::NHB; ++hb) {
-      if (S::NHB > 1) {
+      for (int hb = 0; hb < S::NHB; ++hb) {
+        if (S::NHB > 1) {
 #pragma unroll
-        for (int h = 0; h < S::HB; ++h)
+          for (int h = 0; h < S::HB; ++h)
 #pragma unroll
-          for (int e = 0; e < 8; ++e) qr[h][e] = q_s[(hb * S::HB + h) * kD + l16 * 8 + e];
+            for (int e = 0; e < 8; ++e) qr[h][e] = q_s[(hb * S::HB + h) * kD + l16 * 8 + e];
+        }
+#pragma unroll
+        for (int bt = 0; bt < S::NB; ++bt) {
+          const int rbase = hw * 8 + bt * S::R;
+          float sacc[S::R][S::HB];
+#pragma unroll
+          for (int j = 0; j < S::R; ++j) {
+            const uint4 w = kt[(rbase + (j ^ (l16 & (S::R - 1)))) * 16 + l16];
+            float v[8];
+            unpack8(w, v);
+#pragma unroll
+            for (int h = 0; h < S::HB; ++h) {
+              float d0 = v[0] * qr[h][0];
+#pragma unroll
+              for (int e = 1; e < 8; ++e) d0 = fmaf(v[e], qr[h][e], d0);
+              sacc[j][h] = d0;
+            }
+          }
+#pragma unroll
+          for (int m = S::R / 2; m >= 1; m >>= 1)
+#pragma unroll
+            for (int j = 0; j < m; ++j)
+#pragma unroll
+              for (int h = 0; h < S::HB; ++h) sacc[j][h] += __shfl_xor_sync(0xffffffffu, sacc[j + m][h], m);
+#pragma unroll
+          for (int m = S::R; m < 16; m <<= 1)
+#pragma unroll
+            for (int h = 0; h < S::HB; ++h) sacc[0][h] += __shfl_xor_sync(0xffffffffu, sacc[0][h], m);
+          if (l16 < S::R) {
+            const int r = rbase + l16;
+            const bool ok = (okm >> r) & 1ull;
+#pragma unroll
+            for (int h = 0; h < S::HB; ++h) sc[(hb * S::HB + h) * kAttnRows + r] = ok ? sacc[0][h] : -INFINITY;
+          }
+        }
       }
-      float s4[4][S::HB];
+      cons_bar();
+
+      // ---- online softmax, heads spread over the 4 consumer warps
+      for (int h = warp; h < G; h += kAttnCWarps) {
+        const float x0 = sc[h * kAttnRows + lane], x1 = sc[h * kAttnRows + lane + 32];
+        const float mo = m_s[h];
+        const float mn = fmaxf(mo, warp_max(fmaxf(x0, x1)));
+        const float p0 = mn == -INFINITY ? 0.f : exp2f(x0 - mn);
+        const float p1 = mn == -INFINITY ? 0.f : exp2f(x1 - mn);
+        pT[lane * G + h] = p0;
+        pT[(lane + 32) * G + h] = p1;
+        const float ps = warp_sum(p0 + p1);
+        if (lane == 0) {
+          const float alpha = (mn == -INFINITY) ? 1.f : exp2f(mo - mn);
+          al_s[h] = alpha;
+          l_s[h] = l_s[h] * alpha + ps;
+          m_s[h] = mn;
+        }
+      }
+      cons_bar();
+
+      // ---- P.V over the valid rows of this thread's row group
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint4 w = kt[(hw * 4 + (j ^ (l16 & 3))) * 16 + l16];
+      for (int k = 0; k < S::PPT; ++k) {
+        const int h0 = (hbp + k * (S::TPG / 16)) * S::HB;
+#pragma unroll
+        for (int h = 0; h < S::HB; ++h) {
+          const float al = al_s[h0 + h];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[k][h][e] *= al;
+        }
+      }
+      for (int r = rg; r < kAttnRows; r += S::RG) {
+        if (!((okm >> r) & 1ull)) continue;
+        const uint4 w = vt[r * 16 + cc];
         float v[8];
         unpack8(w, v);
 #pragma unroll
-        for (int h = 0; h < S::HB; ++h) {
-          float d0 = v[0] * qr[h][0];
+        for (int k = 0; k < S::PPT; ++k) {
+          const int h0 = (hbp + k * (S::TPG / 16)) * S::HB;
+          float p[S::HB];
 #pragma unroll
-          for (int e = 1; e < 8; ++e) d0 = fmaf(v[e], qr[h][e], d0);
-          s4[j][h] = d0;
+          for (int h = 0; h < S::HB; ++h) p[h] = pT[r * G + h0 + h];
+#pragma unroll
+          for (int h = 0; h < S::HB; ++h)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[k][h][e] = fmaf(p[h], v[e], acc[k][h][e]);
         }
       }
-#pragma unroll
-      for (int m = 2; m >= 1; m >>= 1)
-#pragma unroll
-        for (int j = 0; j < m; ++j)
-#pragma unroll
-          for (int h = 0; h < S::HB; ++h) s4[j][h] += __shfl_xor_sync(0xffffffffu, s4[j + m][h], m);
-#pragma unroll
-      for (int m = 4; m < 16; m <<= 1)
-#pragma unroll
-        for (int h = 0; h < S::HB; ++h) s4[0][h] += __shfl_xor_sync(0xffffffffu, s4[0][h], m);
-      if (l16 < 4) {
-        const int r = hw * 4 + l16;
-        const bool ok = rowok[st * kAttnRows + r] != 0;
-#pragma unroll
-        for (int h = 0; h < S::HB; ++h) sc[(hb * S::HB + h) * kAttnRows + r] = ok ? s4[0][h] : -INFINITY;
-      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
     }
-    __syncthreads();
 
-    // ---- online softmax per head (one warp per head)
-    for (int h = warp; h < G; h += kAttnThreads / 32) {
-      float* sh = sc + h * kAttnRows;
-      const float x0 = sh[lane], x1 = sh[lane + 32];
-      const float mo = m_s[h];
-      const float mn = fmaxf(mo, warp_max(fmaxf(x0, x1)));
-      const float p0 = mn == -INFINITY ? 0.f : exp2f(x0 - mn);
-      const float p1 = mn == -INFINITY ? 0.f : exp2f(x1 - mn);
-      sh[lane] = p0;
-      sh[lane + 32] = p1;
-      const float ps = warp_sum(p0 + p1);
-      if (lane == 0) {
-        const float alpha = (mn == -INFINITY) ? 1.f : exp2f(mo - mn);
-        al_s[h] = alpha;
-        l_s[h] = l_s[h] * alpha + ps;
-        m_s[h] = mn;
-      }
-    }
-    __syncthreads();
-
-    // ---- P.V
-    const uint4* vt = Vs + (size_t)st * kAttnRows * 16;
+    // ---- fold row groups (lanes l, l^16 in the warp, then the warps in a
+    // fixed order); write the output or this split's partial
+    if (S::TPG <= 16) {
 #pragma unroll
-    for (int k = 0; k < S::PPT; ++k) {
-      const float al = al_s[hbase + k * (S::TPG / 16)];
+      for (int k = 0; k < S::PPT; ++k)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[k][e] *= al;
+        for (int h = 0; h < S::HB; ++h)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[k][h][e] += __shfl_xor_sync(0xffffffffu, acc[k][h][e], 16);
     }
-    for (int r = rg; r < kAttnRows; r += S::RG) {
-      const uint4 w = vt[r * 16 + cc];
-      float v[8];
-      unpack8(w, v);
+    if (S::TPG > 16 || lane < 16) {
+      const int slot = S::TPG <= 16 ? warp : rg;
 #pragma unroll
       for (int k = 0; k < S::PPT; ++k) {
-        const float p = sc[(hbase + k * (S::TPG / 16)) * kAttnRows + r];
+        const int h0 = (hbp + k * (S::TPG / 16)) * S::HB;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[k][e] = fmaf(p, v[e], acc[k][e]);
+        for (int h = 0; h < S::HB; ++h) {
+          float* dst = ored + ((size_t)slot * G + h0 + h) * kD + cc * 8;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) dst[e] = acc[k][h][e];
+        }
       }
     }
-    __syncthreads();
-  }
-
-  // ---- fold row groups, then write the output or this split's partial
-  float* o_s = reinterpret_cast<float*>(asmem);  // [RG][G][128], reuses the K/V stages
+    cons_bar();
+    const size_t lbg = (size_t)lb * a.n_kv + g;
+    float* outp = a.out + ((size_t)lb * a.n_q + (size_t)g * G) * kD;
+    if (a.n_split == 1) {
+      for (int i = ctid; i < G * kD; i += kAttnCThreads) {
+        float o = 0.f;
 #pragma unroll
-  for (int k = 0; k < S::PPT; ++k) {
-    float* dst = o_s + ((size_t)rg * G + hbase + k * (S::TPG / 16)) * kD + cc * 8;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) dst[e] = acc[k][e];
-  }
-  __syncthreads();
-  if (S::RG > 1) {
-    for (int i = tid; i < G * kD; i += kAttnThreads) {
+        for (int r = 0; r < S::NRED; ++r) o += ored[(size_t)r * G * kD + i];
+        const float l = l_s[i / kD];
+        outp[i] = l > 0.f ? o / l : 0.f;
+      }
+      continue;
+    }
+    float* pp = a.part + (lbg * a.n_split + split) * (size_t)G * (kD + 2);
+    for (int i = ctid; i < G * kD; i += kAttnCThreads) {
       float o = 0.f;
 #pragma unroll
-      for (int r = 0; r < S::RG; ++r) o += o_s[(size_t)r * G * kD + i];
-      o_s[i] = o;  // row-group 0 slot; each i is owned by one thread
+      for (int r = 0; r < S::NRED; ++r) o += ored[(size_t)r * G * kD + i];
+      pp[(i / kD) * (kD + 2) + 2 + (i % kD)] = o;
     }
-    __syncthreads();
-  }
-
-  const size_t lbg = (size_t)lb * a.n_kv + g;
-  float* outp = a.out + ((size_t)lb * a.n_q + (size_t)g * G) * kD;
-  if (a.n_split == 1) {
-    for (int i = tid; i < G * kD; i += kAttnThreads) {
-      const float l = l_s[i / kD];
-      outp[i] = l > 0.f ? o_s[i] / l : 0.f;
+    for (int h = ctid; h < G; h += kAttnCThreads) {
+      pp[h * (kD + 2)] = m_s[h];
+      pp[h * (kD + 2) + 1] = l_s[h];
     }
-    return;
-  }
-  float* pp = a.part + (lbg * a.n_split + split) * (size_t)G * (kD + 2);
-  for (int i = tid; i < G * kD; i += kAttnThreads) pp[(i / kD) * (kD + 2) + 2 + (i % kD)] = o_s[i];
-  for (int h = tid; h < G; h += kAttnThreads) {
-    pp[h * (kD + 2)] = m_s[h];
-    pp[h * (kD + 2) + 1] = l_s[h];
-  }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = (atomicAdd(&a.counters[lbg], 1u) == (uint32_t)(a.n_split - 1));
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  const float* pb = a.part + lbg * a.n_split * (size_t)G * (kD + 2);
-  for (int i = tid; i < G * kD; i += kAttnThreads) {
-    const int h = i / kD, c = i % kD;
-    float M = -INFINITY;
-    for (int s = 0; s < a.n_split; ++s) M = fmaxf(M, __ldcg(pb + ((size_t)s * G + h) * (kD + 2)));
-    float Ls = 0.f, O = 0.f;
-    if (M != -INFINITY) {
-      for (int s = 0; s < a.n_split; ++s) {
-        const float* ph = pb + ((size_t)s * G + h) * (kD + 2);
-        const float ms = __ldcg(ph);
-        const float w = ms == -INFINITY ? 0.f : exp2f(ms - M);
-        Ls += __ldcg(ph + 1) * w;
-        O += __ldcg(ph + 2 + c) * w;
+    __threadfence();
+    cons_bar();
+    if (ctid == 0) s_last = (atomicAdd(&a.counters[lbg], 1u) == (uint32_t)(a.n_split - 1));
+    cons_bar();
+    if (!s_last) continue;
+    __threadfence();
+    const float* pb = a.part + lbg * a.n_split * (size_t)G * (kD + 2);
+    for (int i = ctid; i < G * kD; i += kAttnCThreads) {
+      const int h = i / kD, c = i % kD;
+      float M = -INFINITY;
+      for (int sp = 0; sp < a.n_split; ++sp) M = fmaxf(M, __ldcg(pb + ((size_t)sp * G + h) * (kD + 2)));
+      float Ls = 0.f, O = 0.f;
+      if (M != -INFINITY) {
+        for (int sp = 0; sp < a.n_split; ++sp) {
+          const float* ph = pb + ((size_t)sp * G + h) * (kD + 2);
+          const float ms = __ldcg(ph);
+          const float w = ms == -INFINITY ? 0.f : exp2f(ms - M);
+          Ls += __ldcg(ph + 1) * w;
+          O += __ldcg(ph + 2 + c) * w;
+        }
       }
+      outp[i] = Ls > 0.f ? O / Ls : 0.f;
     }
-    outp[i] = Ls > 0.f ? O / Ls : 0.f;
+    if (ctid == 0) a.counters[lbg] = 0u;
   }
-  if (tid == 0) a.counters[lbg] = 0u;
 }
 
-static void attn_split(int n_layers, int B, int n_kv, int budget, int* n_split, int* cps,
+static int attn_ctas_per_sm(int G) { return G <= 8 ? 2 : 1; }
+
+static void attn_split(int n_layers, int B, int n_kv, int budget, int G, int* n_split, int* cps,
                        int* n_chunks) {
   const int nc = (budget + kAttnRows - 1) / kAttnRows;
   const long long base = (long long)n_layers * B * n_kv;
-  long long want = (kAttnTargetCtas + base - 1) / base;
+  // target items: ~2 per resident CTA on a 152-SM GB300 (a fixed count, so
+  // the workspace size does not depend on the device)
+  const long long target = (long long)kAttnItemsPerCta * attn_ctas_per_sm(G) * 152;
+  long long want = (target + base - 1) / base;
   if (want < 1) want = 1;
   if (want > nc) want = nc;
   const int c = (int)((nc + want - 1) / want);
@@ -290,19 +422,9 @@ static void attn_split(int n_layers, int B, int n_kv, int budget, int* n_split, 
   *n_chunks = nc;
 }
 
-template <int G>
-static size_t attn_smem_bytes() {
-  using S = AttnShape<G>;
-  const size_t b = 4 * kAttnStageBytes +
-                   sizeof(float) * ((size_t)G * kD + (size_t)G * kAttnRows + 3 * (size_t)G) +
-                   sizeof(int) * 2 * kAttnRows;
-  const size_t o = sizeof(float) * (size_t)S::RG * G * kD;
-  return b > o ? b : o;
-}
-
 size_t attn_workspace(int n_layers, int B, int n_q, int n_kv, int budget) {
   int ns, cps, nc;
-  attn_split(n_layers, B, n_kv, budget, &ns, &cps, &nc);
+  attn_split(n_layers, B, n_kv, budget, n_q / n_kv, &ns, &cps, &nc);
   const size_t nseg = (size_t)n_layers * B * n_kv;
   const size_t cnt = (nseg * sizeof(uint32_t) + 255) & ~size_t(255);
   const size_t part = ns > 1 ? nseg * ns * (size_t)(n_q / n_kv) * (kD + 2) * sizeof(float) : 0;
@@ -310,14 +432,17 @@ size_t attn_workspace(int n_layers, int B, int n_q, int n_kv, int budget) {
 }
 
 template <int G>
-static cudaError_t launch_attn(const AttnArgs& aa, dim3 grid, cudaStream_t st) {
-  const size_t smem = attn_smem_bytes<G>();
+static cudaError_t launch_attn(const AttnArgs& aa, cudaStream_t st) {
+  const size_t smem = AttnSmem<G>::total;
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(attn_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr = true;
   }
+  int grid = AttnShape<G>::CTAS_PER_SM * device_sm_count();
+  if (grid < 1) grid = 1;
+  if (grid > aa.n_items) grid = aa.n_items;
   attn_kernel<G><<<grid, kAttnThreads, smem, st>>>(aa);
   return cudaGetLastError();
 }
@@ -335,20 +460,21 @@ int attn_launch(const void* q, const spc_kv_view* views, const int32_t* selected
   aa.counters = static_cast<uint32_t*>(workspace);
   aa.part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
                                      ((nseg * sizeof(uint32_t) + 255) & ~size_t(255)));
+  aa.status = nullptr;
   aa.B = B; aa.n_q = n_q; aa.n_kv = n_kv; aa.K = budget;
-  attn_split(n_layers, B, n_kv, budget, &aa.n_split, &aa.cps, &aa.n_chunks);
+  attn_split(n_layers, B, n_kv, budget, n_q / n_kv, &aa.n_split, &aa.cps, &aa.n_chunks);
+  aa.n_items = (int)(nseg * aa.n_split);
   aa.scale2 = scale * kLog2e;
-  const dim3 grid(aa.n_split, n_kv, n_layers * B);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   switch (n_q / n_kv) {
-    case 1: e = launch_attn<1>(aa, grid, st); break;
-    case 2: e = launch_attn<2>(aa, grid, st); break;
-    case 4: e = launch_attn<4>(aa, grid, st); break;
-    case 8: e = launch_attn<8>(aa, grid, st); break;
-    case 16: e = launch_attn<16>(aa, grid, st); break;
-    case 32: e = launch_attn<32>(aa, grid, st); break;
-    default: e = launch_attn<64>(aa, grid, st); break;
+    case 1: e = launch_attn<1>(aa, st); break;
+    case 2: e = launch_attn<2>(aa, st); break;
+    case 4: e = launch_attn<4>(aa, st); break;
+    case 8: e = launch_attn<8>(aa, st); break;
+    case 16: e = launch_attn<16>(aa, st); break;
+    case 32: e = launch_attn<32>(aa, st); break;
+    default: e = launch_attn<64>(aa, st); break;
   }
   return e == cudaSuccess ? SPC_OK : SPC_ERR_CUDA;
 }
