@@ -150,8 +150,18 @@ __global__ void __launch_bounds__(kProjThreads) proj_kernel(ProjArgs a) {
   for (int i = threadIdx.x; i < BB * kProjTile; i += kProjThreads) {
     const int bb = i / kProjTile, c = i - bb * kProjTile, b = b0 + bb;
     if (b >= a.B) continue;
-    float s = 0.f;
-    for (int sp = 0; sp < a.S; ++sp) s += __ldcg(a.part + ((size_t)sp * a.B + b) * a.Ntot + col0 + c);
+    float s4[4] = {0.f, 0.f, 0.f, 0.f};
+    const float* pc = a.part + (size_t)b * a.Ntot + col0 + c;
+    const size_t st = (size_t)a.B * a.Ntot;
+    int sp = 0;
+    for (; sp + 4 <= a.S; sp += 4) {
+      s4[0] += __ldcg(pc + (sp + 0) * st);
+      s4[1] += __ldcg(pc + (sp + 1) * st);
+      s4[2] += __ldcg(pc + (sp + 2) * st);
+      s4[3] += __ldcg(pc + (sp + 3) * st);
+    }
+    for (; sp < a.S; ++sp) s4[0] += __ldcg(pc + sp * st);
+    const float s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
     if (!is_k) {
       a.q_ws[(size_t)b * a.Nq + col0 + c] = s;
       if (a.q_out) a.q_out[(size_t)b * a.Nq + col0 + c] = s;
@@ -362,7 +372,7 @@ struct SelArgs {
   float* scores_out;
   int32_t* selected;
   uint32_t* done;
-  int B, n_q, n_kv, G, cap, K, n_sink, n_recent, append, n_parts, ppt;
+  int B, n_q, n_kv, G, cap, K, n_sink, n_recent, append, n_parts, ppt, kstride;
 };
 
 __device__ __forceinline__ bool is_forced(int p, int L, int n_sink, int n_recent) {
@@ -413,7 +423,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(SelArgs a) {
       for (int h = 0; h < a.G; ++h) sc = fmaxf(sc, __ldcg(lg + (size_t)h * a.cap + p) - lse[h]);
       if (a.scores_out) a.scores_out[(size_t)seg * a.cap + p] = exp2f(sc);
       if (!is_forced(p, L, a.n_sink, a.n_recent)) key[k] = order_key(sc);
-      a.keys[(size_t)seg * a.cap + p] = key[k];
+      a.keys[(size_t)seg * a.kstride + p] = key[k];
     }
   }
   if (L > a.K) {
@@ -445,17 +455,28 @@ __device__ __forceinline__ void find_bin(const uint32_t* cnt, int nbins, int rem
   __syncthreads();
 }
 
+// Keys of positions [4*i4, 4*i4 + 4) with positions >= L zeroed.
+__device__ __forceinline__ void keys4(const uint4* k4, int i4, int L, uint32_t k[4]) {
+  const uint4 v = k4[i4];
+  const int p = 4 * i4;
+  k[0] = p + 0 < L ? v.x : 0u;
+  k[1] = p + 1 < L ? v.y : 0u;
+  k[2] = p + 2 < L ? v.z : 0u;
+  k[3] = p + 3 < L ? v.w : 0u;
+}
+
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(SelArgs a) {
   const int seg = blockIdx.x, b = seg / a.n_kv;
   const int L = effective_len(a.len, b, a.append, a.cap);
   const int tid = threadIdx.x, lane = tid & 31;
   int32_t* out = a.selected + (size_t)seg * a.K;
-  const uint32_t* keys = a.keys + (size_t)seg * a.cap;
+  const uint4* k4 = reinterpret_cast<const uint4*>(a.keys + (size_t)seg * a.kstride);
   uint32_t* gh = a.ghist + (size_t)seg * kHistBins;
   __shared__ uint32_t hist[kHistBins];
   __shared__ uint32_t cand[kCandMax];
   __shared__ int scratch[33];
   __shared__ int s_bin, s_rem, s_cnt, s_last;
+  const int n4 = (L + 3) / 4;
 
   if (L <= a.K) {
     for (int p = tid; p < a.K; p += kTopkThreads) out[p] = p < L ? p : -1;
@@ -471,15 +492,24 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(SelArgs a) {
       find_bin(hist, kHistBins, Kp, scratch, &s_bin, &s_rem);
       const uint32_t b1 = (uint32_t)s_bin;
       int rem = s_rem;
-      const int n1 = (int)hist[b1];
-      const bool local = n1 <= kCandMax;
+      const bool local = (int)hist[b1] <= kCandMax;
       if (local) {
-        for (int p = tid; p < L; p += kTopkThreads) {
-          const uint32_t k = keys[p];
-          if (k && (k >> 21) == b1) {
-            const int j = atomicAdd(&s_cnt, 1);
-            if (j < kCandMax) cand[j] = k;
+        for (int i0 = tid; i0 < n4; i0 += 4 * kTopkThreads) {
+          uint32_t kk[4][4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int i4 = i0 + u * kTopkThreads;
+            if (i4 < n4) keys4(k4, i4, L, kk[u]);
+            else kk[u][0] = kk[u][1] = kk[u][2] = kk[u][3] = 0u;
           }
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (kk[u][j] && (kk[u][j] >> 21) == b1) {
+                const int c = atomicAdd(&s_cnt, 1);
+                if (c < kCandMax) cand[c] = kk[u][j];
+              }
         }
       }
       __syncthreads();
@@ -491,14 +521,28 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(SelArgs a) {
         const uint32_t dmask = (uint32_t)nb - 1u;
         for (int i = tid; i < kHistBins; i += kTopkThreads) hist[i] = 0u;
         __syncthreads();
-        const int n = local ? min(s_cnt, kCandMax) : L;
-        for (int base = 0; base < n; base += kTopkThreads) {
-          const int i = base + tid;
-          uint32_t k = 0u;
-          if (i < n) k = local ? cand[i] : keys[i];
-          const int d = (k && (k & mask) == prefix) ? int((k >> shift) & dmask) : nb;
-          const unsigned peers = __match_any_sync(0xffffffffu, d);
-          if (d < nb && lane == __ffs(peers) - 1) atomicAdd(&hist[d], (uint32_t)__popc(peers));
+        if (local) {
+          const int n = min(s_cnt, kCandMax);
+          for (int base = 0; base < n; base += kTopkThreads) {
+            const int i = base + tid;
+            const uint32_t k = i < n ? cand[i] : 0u;
+            const int d = (k && (k & mask) == prefix) ? int((k >> shift) & dmask) : nb;
+            const unsigned peers = __match_any_sync(0xffffffffu, d);
+            if (d < nb && lane == __ffs(peers) - 1) atomicAdd(&hist[d], (uint32_t)__popc(peers));
+          }
+        } else {
+          for (int base = 0; base < n4; base += kTopkThreads) {
+            const int i4 = base + tid;
+            uint32_t kk[4] = {0u, 0u, 0u, 0u};
+            if (i4 < n4) keys4(k4, i4, L, kk);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t k = kk[j];
+              const int d = (k && (k & mask) == prefix) ? int((k >> shift) & dmask) : nb;
+              const unsigned peers = __match_any_sync(0xffffffffu, d);
+              if (d < nb && lane == __ffs(peers) - 1) atomicAdd(&hist[d], (uint32_t)__popc(peers));
+            }
+          }
         }
         __syncthreads();
         find_bin(hist, nb, rem, scratch, &s_bin, &s_rem);
@@ -510,31 +554,57 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(SelArgs a) {
       T = prefix;
       need = rem;
     }
-    // ordered compaction: thread t owns the contiguous positions [lo, hi)
-    const int chunk = (L + kTopkThreads - 1) / kTopkThreads;
-    const int lo = min(L, tid * chunk), hi = min(L, lo + chunk);
+    // ordered compaction: thread t owns the contiguous quads [q0, q1)
+    const int qpt = (n4 + kTopkThreads - 1) / kTopkThreads;
+    const int q0 = min(n4, tid * qpt), q1 = min(n4, q0 + qpt);
     int nb_ = 0, ne_ = 0;
-    for (int p = lo; p < hi; ++p) {
-      const uint32_t k = keys[p];
-      if (is_forced(p, L, a.n_sink, a.n_recent) || (k && k > T)) ++nb_;
-      else if (Kp > 0 && k && k == T) ++ne_;
+    for (int qb = q0; qb < q1; qb += 8) {
+      uint32_t kk[8][4];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (qb + u < q1) keys4(k4, qb + u, L, kk[u]);
+        else kk[u][0] = kk[u][1] = kk[u][2] = kk[u][3] = 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int p = 4 * (qb + u) + j;
+          if (qb + u >= q1 || p >= L) continue;
+          const uint32_t k = kk[u][j];
+          if (is_forced(p, L, a.n_sink, a.n_recent) || (k && k > T)) ++nb_;
+          else if (Kp > 0 && k && k == T) ++ne_;
+        }
     }
     int tb, te;
     const int base_b = block_excl_scan(nb_, scratch, &tb);
     const int base_e = block_excl_scan(ne_, scratch, &te);
     int o = base_b + min(base_e, need);
     int eq_seen = base_e;
-    for (int p = lo; p < hi; ++p) {
-      const uint32_t k = keys[p];
-      bool sel = is_forced(p, L, a.n_sink, a.n_recent) || (k && k > T);
-      if (!sel && Kp > 0 && k && k == T) {
-        sel = eq_seen < need;
-        ++eq_seen;
+    for (int qb = q0; qb < q1; qb += 8) {
+      uint32_t kk[8][4];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (qb + u < q1) keys4(k4, qb + u, L, kk[u]);
+        else kk[u][0] = kk[u][1] = kk[u][2] = kk[u][3] = 0u;
       }
-      if (sel) {
-        if (o < a.K) out[o] = p;
-        ++o;
-      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int p = 4 * (qb + u) + j;
+          if (qb + u >= q1 || p >= L) continue;
+          const uint32_t k = kk[u][j];
+          bool sel = is_forced(p, L, a.n_sink, a.n_recent) || (k && k > T);
+          if (!sel && Kp > 0 && k && k == T) {
+            sel = eq_seen < need;
+            ++eq_seen;
+          }
+          if (sel) {
+            if (o < a.K) out[o] = p;
+            ++o;
+          }
+        }
     }
   }
 
@@ -589,7 +659,7 @@ static ScoreLayout score_layout(int B, int H, int n_q, int n_kv, int cap) {
   l.logits = take(sizeof(float) * (size_t)B * n_q * cap);
   l.part_scan = take(sizeof(float2) * (size_t)B * n_q * l.n_parts);
   l.lse = take(sizeof(float) * (size_t)B * n_q);
-  l.keys = take(sizeof(uint32_t) * (size_t)B * n_kv * cap);
+  l.keys = take(sizeof(uint32_t) * (size_t)B * n_kv * ((cap + 3) & ~3));
   l.hist = take(sizeof(uint32_t) * (size_t)B * n_kv * kHistBins);
   l.total = off;
   return l;
@@ -703,7 +773,7 @@ int score_select_launch(const ScoreSelectCall& c) {
     sa.done = reinterpret_cast<uint32_t*>(ws + l.done);
     sa.B = c.B; sa.n_q = c.n_q; sa.n_kv = c.n_kv; sa.G = G; sa.cap = c.cap; sa.K = c.budget;
     sa.n_sink = c.n_sink; sa.n_recent = c.n_recent; sa.append = c.append;
-    sa.n_parts = l.n_parts; sa.ppt = l.ppt;
+    sa.n_parts = l.n_parts; sa.ppt = l.ppt; sa.kstride = (c.cap + 3) & ~3;
     lse_kernel<<<c.B * c.n_q, 256, 0, st>>>(sa);
     if (cudaGetLastError() != cudaSuccess) return SPC_ERR_CUDA;
     const dim3 sg((c.cap + kScorePos - 1) / kScorePos, c.B * c.n_kv);

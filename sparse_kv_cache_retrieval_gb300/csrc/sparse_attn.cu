@@ -36,6 +36,7 @@ constexpr int kAttnStages = 3;
 constexpr uint32_t kAttnTileBytes = kAttnRows * kRowBytes;  // 16 KiB (K or V)
 constexpr int kAttnItemsPerCta = 2;                 // split target: ~2 items per resident CTA
 constexpr long long kAttnWait = 4000000000ll;
+constexpr int kPartStride = kD + 4;                // (m, l, pad, pad, o[128])
 
 template <int G>
 struct AttnShape {
@@ -366,16 +367,16 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
       }
       continue;
     }
-    float* pp = a.part + (lbg * a.n_split + split) * (size_t)G * (kD + 2);
+    float* pp = a.part + (lbg * a.n_split + split) * (size_t)G * kPartStride;
     for (int i = ctid; i < G * kD; i += kAttnCThreads) {
       float o = 0.f;
 #pragma unroll
       for (int r = 0; r < S::NRED; ++r) o += ored[(size_t)r * G * kD + i];
-      pp[(i / kD) * (kD + 2) + 2 + (i % kD)] = o;
+      pp[(i / kD) * kPartStride + 4 + (i % kD)] = o;
     }
     for (int h = ctid; h < G; h += kAttnCThreads) {
-      pp[h * (kD + 2)] = m_s[h];
-      pp[h * (kD + 2) + 1] = l_s[h];
+      pp[h * kPartStride] = m_s[h];
+      pp[h * kPartStride + 1] = l_s[h];
     }
     __threadfence();
     cons_bar();
@@ -383,22 +384,37 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
     cons_bar();
     if (!s_last) continue;
     __threadfence();
-    const float* pb = a.part + lbg * a.n_split * (size_t)G * (kD + 2);
-    for (int i = ctid; i < G * kD; i += kAttnCThreads) {
-      const int h = i / kD, c = i % kD;
+    // merge the splits: stage every (max, sum) in shared memory (q_s is free
+    // now), per head the global max and the weights, then float4 sums
+    const float* pb = a.part + lbg * a.n_split * (size_t)G * kPartStride;
+    float* wsp = q_s;                                   // [n_split][G] weights
+    float* linv = q_s + a.n_split * G;                  // [G]
+    for (int i = ctid; i < a.n_split * G; i += kAttnCThreads) wsp[i] = __ldcg(pb + (size_t)i * kPartStride);
+    cons_bar();
+    for (int h = ctid; h < G; h += kAttnCThreads) {
       float M = -INFINITY;
-      for (int sp = 0; sp < a.n_split; ++sp) M = fmaxf(M, __ldcg(pb + ((size_t)sp * G + h) * (kD + 2)));
-      float Ls = 0.f, O = 0.f;
-      if (M != -INFINITY) {
-        for (int sp = 0; sp < a.n_split; ++sp) {
-          const float* ph = pb + ((size_t)sp * G + h) * (kD + 2);
-          const float ms = __ldcg(ph);
-          const float w = ms == -INFINITY ? 0.f : exp2f(ms - M);
-          Ls += __ldcg(ph + 1) * w;
-          O += __ldcg(ph + 2 + c) * w;
-        }
+      for (int sp = 0; sp < a.n_split; ++sp) M = fmaxf(M, wsp[sp * G + h]);
+      float Ls = 0.f;
+      for (int sp = 0; sp < a.n_split; ++sp) {
+        const float ms = wsp[sp * G + h];
+        const float w = (M == -INFINITY || ms == -INFINITY) ? 0.f : exp2f(ms - M);
+        Ls += __ldcg(pb + ((size_t)sp * G + h) * kPartStride + 1) * w;
+        wsp[sp * G + h] = w;
       }
-      outp[i] = Ls > 0.f ? O / Ls : 0.f;
+      linv[h] = Ls > 0.f ? 1.f / Ls : 0.f;
+    }
+    cons_bar();
+    for (int i4 = ctid; i4 < G * (kD / 4); i4 += kAttnCThreads) {
+      const int h = i4 / (kD / 4), c4 = i4 - h * (kD / 4);
+      float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+      for (int sp = 0; sp < a.n_split; ++sp) {
+        const float w = wsp[sp * G + h];
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(pb + ((size_t)sp * G + h) * kPartStride + 4) + c4);
+        O.x = fmaf(w, v.x, O.x); O.y = fmaf(w, v.y, O.y); O.z = fmaf(w, v.z, O.z); O.w = fmaf(w, v.w, O.w);
+      }
+      const float li = linv[h];
+      reinterpret_cast<float4*>(outp + (size_t)h * kD)[c4] = make_float4(O.x * li, O.y * li, O.z * li, O.w * li);
     }
     if (ctid == 0) a.counters[lbg] = 0u;
   }
@@ -427,7 +443,7 @@ size_t attn_workspace(int n_layers, int B, int n_q, int n_kv, int budget) {
   attn_split(n_layers, B, n_kv, budget, n_q / n_kv, &ns, &cps, &nc);
   const size_t nseg = (size_t)n_layers * B * n_kv;
   const size_t cnt = (nseg * sizeof(uint32_t) + 255) & ~size_t(255);
-  const size_t part = ns > 1 ? nseg * ns * (size_t)(n_q / n_kv) * (kD + 2) * sizeof(float) : 0;
+  const size_t part = ns > 1 ? nseg * ns * (size_t)(n_q / n_kv) * kPartStride * sizeof(float) : 0;
   return cnt + part;
 }
 
