@@ -400,29 +400,46 @@ __global__ void __launch_bounds__(256) lse_kernel(SelArgs a) {
   }
 }
 
+template <int G>
 __global__ void __launch_bounds__(kScoreThreads) score_kernel(SelArgs a) {
   const int seg = blockIdx.y, b = seg / a.n_kv, g = seg - b * a.n_kv;
   const int L = effective_len(a.len, b, a.append, a.cap);
   const int p0 = blockIdx.x * kScorePos;
   if (p0 >= L) return;
   __shared__ uint32_t hist[kHistBins];
-  __shared__ float lse[SPC_MAX_GROUP];
+  __shared__ float lse[G];
   const int tid = threadIdx.x, lane = tid & 31;
   for (int i = tid; i < kHistBins; i += kScoreThreads) hist[i] = 0u;
-  for (int h = tid; h < a.G; h += kScoreThreads) lse[h] = a.lse2[(size_t)b * a.n_q + (size_t)g * a.G + h];
+  for (int h = tid; h < G; h += kScoreThreads) lse[h] = a.lse2[(size_t)b * a.n_q + (size_t)g * G + h];
   __syncthreads();
-  const float* lg = a.logits + ((size_t)b * a.n_q + (size_t)g * a.G) * a.cap;
-  constexpr int PER = kScorePos / kScoreThreads;  // 8
+  const float* lg = a.logits + ((size_t)b * a.n_q + (size_t)g * G) * a.cap;
+  constexpr int PER = kScorePos / kScoreThreads;  // 8 positions per thread
+  constexpr int HC = G < 8 ? G : 8;               // heads per batch of loads in flight
+  float sc[PER];
+#pragma unroll
+  for (int k = 0; k < PER; ++k) sc[k] = -INFINITY;
+  for (int h0 = 0; h0 < G; h0 += HC) {
+    float v[HC][PER];
+#pragma unroll
+    for (int h = 0; h < HC; ++h)
+#pragma unroll
+      for (int k = 0; k < PER; ++k) {
+        const int p = p0 + k * kScoreThreads + tid;
+        v[h][k] = p < L ? __ldcg(lg + (size_t)(h0 + h) * a.cap + p) : -INFINITY;
+      }
+#pragma unroll
+    for (int h = 0; h < HC; ++h)
+#pragma unroll
+      for (int k = 0; k < PER; ++k) sc[k] = fmaxf(sc[k], v[h][k] - lse[h0 + h]);
+  }
   uint32_t key[PER];
 #pragma unroll
   for (int k = 0; k < PER; ++k) {
     const int p = p0 + k * kScoreThreads + tid;
     key[k] = 0u;
     if (p < L) {
-      float sc = -INFINITY;
-      for (int h = 0; h < a.G; ++h) sc = fmaxf(sc, __ldcg(lg + (size_t)h * a.cap + p) - lse[h]);
-      if (a.scores_out) a.scores_out[(size_t)seg * a.cap + p] = exp2f(sc);
-      if (!is_forced(p, L, a.n_sink, a.n_recent)) key[k] = order_key(sc);
+      if (a.scores_out) a.scores_out[(size_t)seg * a.cap + p] = exp2f(sc[k]);
+      if (!is_forced(p, L, a.n_sink, a.n_recent)) key[k] = order_key(sc[k]);
       a.keys[(size_t)seg * a.kstride + p] = key[k];
     }
   }
@@ -777,7 +794,15 @@ int score_select_launch(const ScoreSelectCall& c) {
     lse_kernel<<<c.B * c.n_q, 256, 0, st>>>(sa);
     if (cudaGetLastError() != cudaSuccess) return SPC_ERR_CUDA;
     const dim3 sg((c.cap + kScorePos - 1) / kScorePos, c.B * c.n_kv);
-    score_kernel<<<sg, kScoreThreads, 0, st>>>(sa);
+    switch (G) {
+      case 1: score_kernel<1><<<sg, kScoreThreads, 0, st>>>(sa); break;
+      case 2: score_kernel<2><<<sg, kScoreThreads, 0, st>>>(sa); break;
+      case 4: score_kernel<4><<<sg, kScoreThreads, 0, st>>>(sa); break;
+      case 8: score_kernel<8><<<sg, kScoreThreads, 0, st>>>(sa); break;
+      case 16: score_kernel<16><<<sg, kScoreThreads, 0, st>>>(sa); break;
+      case 32: score_kernel<32><<<sg, kScoreThreads, 0, st>>>(sa); break;
+      default: score_kernel<64><<<sg, kScoreThreads, 0, st>>>(sa); break;
+    }
     if (cudaGetLastError() != cudaSuccess) return SPC_ERR_CUDA;
     topk_kernel<<<c.B * c.n_kv, kTopkThreads, 0, st>>>(sa);
     if (cudaGetLastError() != cudaSuccess) return SPC_ERR_CUDA;
