@@ -150,6 +150,7 @@ int spc_gather_kv(const spc_gather_view* views, int layer_lo, int layer_hi, cons
   if (B < 1 || B > SPC_MAX_BATCH || n_kv < 1 || B * n_kv > 1024) return SPC_ERR_SHAPE;
   if (layer_lo < 0 || layer_hi < layer_lo) return SPC_ERR_SHAPE;
   if (budget < 1 || budget > SPC_MAX_BUDGET || cap < 1 || cap > SPC_MAX_CAP) return SPC_ERR_SHAPE;
+  if ((long long)(layer_hi - layer_lo) * 2 * B * n_kv * budget >= (1ll << 31)) return SPC_ERR_SHAPE;
   return gather_launch(views, layer_lo, layer_hi, load_slot, load_pos, n_load, B, n_kv, cap, budget,
                        stream);
 }

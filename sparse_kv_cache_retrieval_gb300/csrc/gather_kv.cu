@@ -48,23 +48,23 @@ gather_kernel(const spc_gather_view* __restrict__ views, int layer_lo, int layer
   __syncthreads();
 
   const int R = run;
-  const long long per_layer = 2ll * R;
-  const long long total = (long long)(layer_hi - layer_lo) * per_layer;
+  const int per_layer = 2 * R;
+  const int total = (layer_hi - layer_lo) * per_layer;   // host limits keep this < 2^31
   const int l16 = tid & 15;
-  const long long hw0 = ((long long)blockIdx.x * kGatherThreads + tid) >> 4;
-  const long long nhw = ((long long)gridDim.x * kGatherThreads) >> 4;
+  const int hw0 = (blockIdx.x * kGatherThreads + tid) >> 4;
+  const int nhw = (gridDim.x * kGatherThreads) >> 4;
 
-  for (long long item0 = hw0; item0 < total; item0 += nhw * kGatherUnroll) {
+  for (int item0 = hw0; item0 < total; item0 += nhw * kGatherUnroll) {
     uint4 v[kGatherUnroll];
     uint16_t* dst[kGatherUnroll];
 #pragma unroll
     for (int u = 0; u < kGatherUnroll; ++u) {
       dst[u] = nullptr;
-      const long long item = item0 + u * nhw;
+      const int item = item0 + u * nhw;
       if (item >= total) continue;
-      const long long lq = item / per_layer;
-      const int layer = layer_lo + (int)lq;
-      const int rem = (int)(item - lq * per_layer);
+      const int lq = item / per_layer;
+      const int layer = layer_lo + lq;
+      const int rem = item - lq * per_layer;
       const int kv = rem >= R ? 1 : 0;
       const int j = rem - kv * R;
       // largest seg with pre[seg] <= j (segments with no load have equal bounds)

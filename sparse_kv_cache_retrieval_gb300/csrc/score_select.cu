@@ -24,7 +24,7 @@
 //    partials give the logsumexp.
 //  * lse_kernel / score_kernel / topk_kernel: logsumexp per head, the group
 //    score and its order key for every position on the whole GPU with a
-//    per-(request, KV head) histogram of the key's top 11 bits, then one CTA
+//    per-(request, KV head) histogram of the key's bits 30..20, then one CTA
 //    per (request, KV head) that finds the threshold key (histogram bin, then
 //    two refinement passes over the bin's candidates) and writes the selection
 //    with an ordered compaction (ascending, ties to the lower position).
@@ -103,15 +103,12 @@ __global__ void __launch_bounds__(kProjThreads) proj_kernel(ProjArgs a) {
 
   const uint16_t* wp = W + (size_t)r_begin * ld + wcol0 + l16 * 8;
   int r = warp * 2 + (lane >> 4);
-  for (; r + 48 < nr; r += 64) {
-    const uint4 w0 = ldg_stream(wp + (size_t)r * ld);
-    const uint4 w1 = ldg_stream(wp + (size_t)(r + 16) * ld);
-    const uint4 w2 = ldg_stream(wp + (size_t)(r + 32) * ld);
-    const uint4 w3 = ldg_stream(wp + (size_t)(r + 48) * ld);
-    proj_fma<BB>(acc, w0, xs + r * BB);
-    proj_fma<BB>(acc, w1, xs + (r + 16) * BB);
-    proj_fma<BB>(acc, w2, xs + (r + 32) * BB);
-    proj_fma<BB>(acc, w3, xs + (r + 48) * BB);
+  for (; r + 112 < nr; r += 128) {
+    uint4 w[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) w[u] = ldg_stream(wp + (size_t)(r + 16 * u) * ld);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) proj_fma<BB>(acc, w[u], xs + (r + 16 * u) * BB);
   }
   for (; r < nr; r += 16) proj_fma<BB>(acc, ldg_stream(wp + (size_t)r * ld), xs + r * BB);
 
@@ -347,9 +344,9 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
 //  * lse_kernel: one CTA per query head folds the scan's (max, sum) partials
 //    into log2-sum-exp;
 //  * score_kernel: every position of every (request, KV head) in parallel:
-//    s = max_h (l_h - lse_h), the monotone uint32 order key, and a 2048-bin
-//    histogram of the key's top 11 bits (block histogram in shared memory,
-//    flushed to a per-segment global histogram);
+//    s = max_h (l_h - lse_h), p = 2^s, the monotone uint32 order key of p, and
+//    a 2048-bin histogram of the key's bits 30..20 (block histogram in shared
+//    memory, flushed to a per-segment global histogram);
 //  * topk_kernel: one CTA per (request, KV head) finds the bin holding the
 //    (K-|F|)-th largest key, refines the remaining 21 bits over the bin's
 //    candidates (gathered in shared memory; global fallback for huge ties),
@@ -432,21 +429,25 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(SelArgs a) {
 #pragma unroll
       for (int k = 0; k < PER; ++k) sc[k] = fmaxf(sc[k], v[h][k] - lse[h0 + h]);
   }
+  // order key of the group score p = 2^s in [0, 1]: its float bits + 1 (0 is
+  // reserved for forced / absent positions). Probabilities spread over many
+  // exponents, so the key's bits 30..20 make a fine first histogram.
   uint32_t key[PER];
 #pragma unroll
   for (int k = 0; k < PER; ++k) {
-    const int p = p0 + k * kScoreThreads + tid;
+    const int pos = p0 + k * kScoreThreads + tid;
     key[k] = 0u;
-    if (p < L) {
-      if (a.scores_out) a.scores_out[(size_t)seg * a.cap + p] = exp2f(sc[k]);
-      if (!is_forced(p, L, a.n_sink, a.n_recent)) key[k] = order_key(sc[k]);
-      a.keys[(size_t)seg * a.kstride + p] = key[k];
+    if (pos < L) {
+      const float pr = exp2f(sc[k]);
+      if (a.scores_out) a.scores_out[(size_t)seg * a.cap + pos] = pr;
+      if (!is_forced(pos, L, a.n_sink, a.n_recent)) key[k] = __float_as_uint(pr) + 1u;
+      a.keys[(size_t)seg * a.kstride + pos] = key[k];
     }
   }
   if (L > a.K) {
 #pragma unroll
     for (int k = 0; k < PER; ++k) {
-      const int bin = key[k] ? int(key[k] >> 21) : kHistBins;
+      const int bin = key[k] ? int(key[k] >> 20) : kHistBins;
       const unsigned peers = __match_any_sync(0xffffffffu, bin);
       if (bin < kHistBins && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
     }
@@ -523,18 +524,18 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(SelArgs a) {
           for (int u = 0; u < 4; ++u)
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-              if (kk[u][j] && (kk[u][j] >> 21) == b1) {
+              if (kk[u][j] && (kk[u][j] >> 20) == b1) {
                 const int c = atomicAdd(&s_cnt, 1);
                 if (c < kCandMax) cand[c] = kk[u][j];
               }
         }
       }
       __syncthreads();
-      // two refinement passes: bits 20..10, then 9..0
-      uint32_t prefix = b1 << 21, mask = 0xffe00000u;
+      // two refinement passes: bits 19..10, then 9..0
+      uint32_t prefix = b1 << 20, mask = 0xfff00000u;
       for (int pass = 0; pass < 2; ++pass) {
         const int shift = pass == 0 ? 10 : 0;
-        const int nb = pass == 0 ? 2048 : 1024;
+        const int nb = 1024;
         const uint32_t dmask = (uint32_t)nb - 1u;
         for (int i = tid; i < kHistBins; i += kTopkThreads) hist[i] = 0u;
         __syncthreads();
@@ -650,8 +651,8 @@ struct ScoreLayout {
 };
 
 static int proj_splits(int H) {
-  int S = H / 512;
-  return S < 1 ? 1 : (S > 16 ? 16 : S);
+  int S = H / 256;
+  return S < 1 ? 1 : (S > 32 ? 32 : S);
 }
 
 static int scan_ppt(int G) { return kScanCWarps * ((G < 8 ? G : 8) <= 4 ? 1 : 2); }
