@@ -7,50 +7,54 @@
 // Context Sparsity in LLMs" (paperlayer.ai summary) §4.3 (for GQA the selected
 // KV serves every query head of its group).
 //
-// GB300 design. Work item = a contiguous range of 64-row chunks of one
-// (layer, request, KV head). Persistent CTAs of 4 consumer warps + 1 producer
-// warp walk their items in a static round-robin:
-//  * the producer streams each chunk's K and V rows into a 3-stage shared-
-//    memory ring with cp.async.bulk (TMA engine, mbarrier byte counts): one
-//    16 KiB copy per tensor in slot mode (slots are contiguous), one 256-byte
-//    copy per kept row in position mode; it publishes a 64-bit mask of the
-//    chunk's valid rows and runs ahead across item boundaries;
-//  * consumers form the G heads' base-2 scores with a lane-rotated half-warp
-//    reduce-scatter (each K row is read from shared memory once for the whole
-//    group), update an online softmax per head (two named barriers per chunk),
-//    and accumulate P.V in registers that persist across chunks, each thread
-//    owning (heads, 8 columns) so a V row is read once per row group;
-//  * an item's (max, sum, unnormalised output) is either the result or a
-//    partial that the last CTA of its (layer, request, KV head) merges, in
-//    split order (deterministic).
+// GB300 design. Per (layer, request, KV head) the kept rows form a small dense
+// contraction: G query heads x 128 dims against up to `budget` rows. It is
+// HBM-bound, but on CUDA cores its instruction stream (unpacking, shuffles,
+// FMAs) held the SMs to ~1 instruction per cycle, well short of the memory
+// rate. Here both products run on the tensor cores with mma.sync m16n8k16
+// (bf16 in, fp32 accumulate; bf16 x bf16 products are exact in fp32):
+//  * work item = a contiguous range of 64-row chunks of one (layer, request,
+//    KV head); persistent CTAs of 4 consumer warps + 1 producer warp walk the
+//    items round-robin;
+//  * the producer copies each kept K and V row (256 bytes) with cp.async.bulk
+//    into a 2-stage shared-memory ring whose rows are padded to 272 bytes (so
+//    ldmatrix reads them without bank conflicts), counting bytes on an
+//    mbarrier, and publishes the chunk's 64-bit valid-row mask;
+//  * each consumer warp owns one 16-head tile of the group (zero-padded when
+//    G < 16) and a slice of the chunk's rows: S = Q K^T from ldmatrix'ed K
+//    fragments, masked online softmax in base 2 held per warp, then O += P V
+//    with P reused from the S accumulators as an A fragment, split into bf16
+//    high and low parts (two MMAs) so the weights keep ~16 bits, against
+//    ldmatrix.trans'ed V fragments;
+//  * warps sharing a head tile merge (max, sum, O) through shared memory at the
+//    end of an item; the item's result is the output or a partial that the last
+//    CTA of its (layer, request, KV head) merges in split order (deterministic).
+#include <cuda_bf16.h>
+
 #include "spc_device.cuh"
 #include "spc_internal.h"
 
 namespace spc {
 
 constexpr int kAttnRows = 64;                       // rows per chunk
-constexpr int kAttnCWarps = 4;                      // consumer warps
-constexpr int kAttnCThreads = kAttnCWarps * 32;     // 128
+constexpr int kAttnPitch = 272;                     // smem bytes per row (256 + 16)
+constexpr int kAttnCWarps = 4;
+constexpr int kAttnCThreads = kAttnCWarps * 32;
 constexpr int kAttnThreads = kAttnCThreads + 32;    // + producer warp
-constexpr int kAttnStages = 3;
-constexpr uint32_t kAttnTileBytes = kAttnRows * kRowBytes;  // 16 KiB (K or V)
+constexpr int kAttnStages = 2;
+constexpr int kAttnTile = kAttnRows * kAttnPitch;   // 17408 bytes (K or V)
+constexpr int kAttnCtasPerSm = 2;
 constexpr int kAttnItemsPerCta = 2;                 // split target: ~2 items per resident CTA
 constexpr long long kAttnWait = 4000000000ll;
-constexpr int kPartStride = kD + 4;                // (m, l, pad, pad, o[128])
+constexpr int kPartStride = kD + 4;                 // (m, l, pad, pad, o[128])
 
 template <int G>
 struct AttnShape {
-  static constexpr int HB = G < 8 ? G : 8;          // heads per register block
-  static constexpr int NHB = G / HB;
-  static constexpr int R = HB <= 4 ? 8 : 4;         // rows per half-warp QK batch
-  static constexpr int NB = 8 / R;                  // batches (8 rows per half-warp per chunk)
-  static constexpr int PAIRS = NHB * 16;            // (head block, 8-column chunk) pairs
-  static constexpr int TPG = PAIRS < kAttnCThreads ? PAIRS : kAttnCThreads;
-  static constexpr int RG = kAttnCThreads / TPG;    // row groups in P.V
-  static constexpr int PPT = PAIRS / TPG;           // pairs per thread
-  // row-group partial sums left after folding lanes l and l^16 (TPG <= 16)
-  static constexpr int NRED = TPG <= 16 ? RG / 2 : RG;
-  static constexpr int CTAS_PER_SM = G <= 8 ? 2 : 1;
+  static constexpr int NMT = G <= 16 ? 1 : G / 16;  // 16-head tiles
+  static constexpr int NRS = kAttnCWarps / NMT;     // warps sharing a tile (row split)
+  static constexpr int RW = kAttnRows / NRS;        // rows per warp per chunk
+  static constexpr int NT = RW / 8;                 // QK n-tiles (8 rows each)
+  static constexpr int KS = RW / 16;                // PV k-steps (16 rows each)
 };
 
 struct AttnArgs {
@@ -68,18 +72,37 @@ struct AttnArgs {
 
 template <int G>
 struct AttnSmem {
-  static constexpr size_t stages = (size_t)kAttnStages * 2 * kAttnTileBytes;
-  static constexpr size_t q = sizeof(float) * G * kD;
-  static constexpr size_t sc = sizeof(float) * G * kAttnRows;       // raw scores [G][64]
-  static constexpr size_t pt = sizeof(float) * kAttnRows * G;       // weights [64][G]
-  static constexpr size_t ored = sizeof(float) * AttnShape<G>::NRED * G * kD;
-  static constexpr size_t small = sizeof(float) * 4 * 64 + sizeof(uint64_t) * (3 * kAttnStages);
-  static constexpr size_t total = stages + q + sc + pt + ored + small;
+  using S = AttnShape<G>;
+  static constexpr size_t stages = (size_t)kAttnStages * 2 * kAttnTile;
+  static constexpr size_t mo = sizeof(float) * S::NRS * G * kD;       // per row-split O
+  static constexpr size_t ml = sizeof(float) * 2 * S::NRS * G;        // per row-split (m, l)
+  static constexpr size_t wsp = sizeof(float) * (S::NRS * G + 2 * G); // row-split weights, (M, L)
+  static constexpr size_t total = stages + mo + ml + wsp + sizeof(uint64_t) * 3 * kAttnStages;
 };
 
 __device__ __forceinline__ void cons_bar() { asm volatile("bar.sync 1, %0;" :: "n"(kAttnCThreads) : "memory"); }
 
-template <int G>
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+               "{%0,%1,%2,%3};"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+               : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// bf16x2 of (lo, hi): lo in the low half (the lower column index)
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+__device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
 __device__ __forceinline__ void item_coords(const AttnArgs& a, int item, int& lb, int& g, int& split) {
   split = item % a.n_split;
   const int rest = item / a.n_split;
@@ -92,15 +115,10 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
   using S = AttnShape<G>;
   using M = AttnSmem<G>;
   extern __shared__ __align__(128) uint8_t asmem[];
-  uint4* stage_kv = reinterpret_cast<uint4*>(asmem);                       // [stage][K|V][64][16]
-  float* q_s = reinterpret_cast<float*>(asmem + M::stages);                // [G][128]
-  float* sc = reinterpret_cast<float*>(asmem + M::stages + M::q);         // [G][64]
-  float* pT = reinterpret_cast<float*>(asmem + M::stages + M::q + M::sc); // [64][G]
-  float* ored = reinterpret_cast<float*>(asmem + M::stages + M::q + M::sc + M::pt);
-  float* m_s = reinterpret_cast<float*>(asmem + M::stages + M::q + M::sc + M::pt + M::ored);
-  float* l_s = m_s + 64;
-  float* al_s = l_s + 64;
-  uint64_t* okmask = reinterpret_cast<uint64_t*>(al_s + 128);
+  float* mo = reinterpret_cast<float*>(asmem + M::stages);                       // [NRS][G][128]
+  float* ml = reinterpret_cast<float*>(asmem + M::stages + M::mo);               // [NRS][G][2]
+  float* wsp = reinterpret_cast<float*>(asmem + M::stages + M::mo + M::ml);      // [NRS][G] + [G][2]
+  uint64_t* okmask = reinterpret_cast<uint64_t*>(asmem + M::stages + M::mo + M::ml + M::wsp);
   uint64_t* full = okmask + kAttnStages;
   uint64_t* empty = full + kAttnStages;
   __shared__ int s_last;
@@ -116,12 +134,12 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
   __syncthreads();
 
   if (warp == kAttnCWarps) {
-    // ================= producer warp
+    // ================= producer warp: per-row bulk copies into padded rows
     int it = 0;
     bool ok = true;
     for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
       int lb, g, split;
-      item_coords<G>(a, item, lb, g, split);
+      item_coords(a, item, lb, g, split);
       const spc_kv_view vw = a.views[lb];
       const int b = lb % a.B;
       const int32_t* idx = (vw.use_slots ? a.slot_pos : a.selected) + ((size_t)b * a.n_kv + g) * a.K;
@@ -136,8 +154,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
           ok = false;
           break;
         }
-        // row validity and source row for this lane's two rows
-        int src[2];
+        long long src[2];
         bool val[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -149,79 +166,64 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
             if (row >= vw.rows) row = -1;
           }
           val[h] = row >= 0;
-          src[h] = (int)(row < 0 ? 0 : row);
+          src[h] = row;
         }
         const uint32_t lo = __ballot_sync(0xffffffffu, val[0]);
         const uint32_t hi = __ballot_sync(0xffffffffu, val[1]);
-        uint4* kdst = stage_kv + (size_t)s * 2 * kAttnRows * 16;
-        uint4* vdst = kdst + kAttnRows * 16;
-        if (vw.use_slots) {
-          // contiguous slots [c*64, min(K, c*64+64)): one copy per tensor
-          const int n_in = min(kAttnRows, a.K - c * kAttnRows);
-          if (lane == 0) {
-            okmask[s] = ((uint64_t)hi << 32) | lo;
-            mbar_arrive_expect_tx(&full[s], 2u * n_in * kRowBytes);
-            bulk_g2s(kdst, kb + (size_t)c * kAttnRows * kD, n_in * kRowBytes, &full[s]);
-            bulk_g2s(vdst, vb + (size_t)c * kAttnRows * kD, n_in * kRowBytes, &full[s]);
-          }
-        } else {
-          const int nval = __popc(lo) + __popc(hi);
-          if (lane == 0) {
-            okmask[s] = ((uint64_t)hi << 32) | lo;
-            mbar_arrive_expect_tx(&full[s], 2u * nval * kRowBytes);
-          }
-          __syncwarp();
+        const int nval = __popc(lo) + __popc(hi);
+        uint8_t* kdst = asmem + (size_t)s * 2 * kAttnTile;
+        uint8_t* vdst = kdst + kAttnTile;
+        if (lane == 0) {
+          okmask[s] = ((uint64_t)hi << 32) | lo;
+          mbar_arrive_expect_tx(&full[s], 2u * nval * kRowBytes);
+        }
+        __syncwarp();
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            if (val[h]) {
-              const int r = lane + 32 * h;
-              bulk_g2s(kdst + r * 16, kb + (size_t)src[h] * kD, kRowBytes, &full[s]);
-              bulk_g2s(vdst + r * 16, vb + (size_t)src[h] * kD, kRowBytes, &full[s]);
-            }
+        for (int h = 0; h < 2; ++h) {
+          if (val[h]) {
+            const int r = lane + 32 * h;
+            bulk_g2s(kdst + r * kAttnPitch, kb + (size_t)src[h] * kD, kRowBytes, &full[s]);
+            bulk_g2s(vdst + r * kAttnPitch, vb + (size_t)src[h] * kD, kRowBytes, &full[s]);
           }
         }
         __syncwarp();
       }
     }
-    // wait (bounded) for the copies still in flight before leaving
     if (lane == 0)
       for (int k = max(0, it - kAttnStages); k < it; ++k)
         mbar_wait_bounded(&full[k % kAttnStages], (k / kAttnStages) & 1, kAttnWait);
     return;
   }
 
-  // ================= consumers (128 threads)
-  const int ctid = tid;                        // 0..127
-  const int hw = ctid >> 4, l16 = ctid & 15;   // half-warp 0..7 -> rows [hw*8, hw*8+8)
-  const int rg = ctid / S::TPG, tp = ctid - rg * S::TPG;
-  const int cc = tp & 15, hbp = tp >> 4;       // column chunk, first head block of this thread
+  // ================= consumers
+  const int gid = lane >> 2, tig = lane & 3;
+  const int mt = warp / S::NRS, rs = warp % S::NRS;
+  const int row0 = rs * S::RW;                      // this warp's rows in a chunk
+  const int h_lo = mt * 16 + gid, h_hi = h_lo + 8;  // heads of this thread's rows
+  const uint32_t smem0 = smem_u32(asmem);
+  const int lm = lane >> 3, lr = lane & 7;          // ldmatrix: matrix and row of this lane
   int it = 0;
-  bool dead = false;  // a wait gave up: keep the barrier sequence, skip further waits
+  bool dead = false;
   for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
     int lb, g, split;
-    item_coords<G>(a, item, lb, g, split);
+    item_coords(a, item, lb, g, split);
     const int c0 = split * a.cps, c1 = min(c0 + a.cps, a.n_chunks);
 
-    // q of the group (base-2 scaled) and softmax state
-    cons_bar();  // previous item's readers of q_s / m_s are done
+    // Q fragments of this warp's head tile (rows >= G are zero)
     const uint16_t* qg = a.q + ((size_t)lb * a.n_q + (size_t)g * G) * kD;
-    for (int i = ctid; i < G * kD; i += kAttnCThreads) q_s[i] = __uint_as_float(uint32_t(qg[i]) << 16) * a.scale2;
-    for (int h = ctid; h < G; h += kAttnCThreads) { m_s[h] = -INFINITY; l_s[h] = 0.f; }
-    cons_bar();
-    float qr[S::HB][8];
-    if (S::NHB == 1) {
+    uint32_t qf[8][4];
 #pragma unroll
-      for (int h = 0; h < S::HB; ++h)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) qr[h][e] = q_s[h * kD + l16 * 8 + e];
+    for (int ks = 0; ks < 8; ++ks) {
+      const int c = ks * 16 + tig * 2;
+      qf[ks][0] = h_lo < G ? *reinterpret_cast<const uint32_t*>(qg + (size_t)h_lo * kD + c) : 0u;
+      qf[ks][1] = h_hi < G ? *reinterpret_cast<const uint32_t*>(qg + (size_t)h_hi * kD + c) : 0u;
+      qf[ks][2] = h_lo < G ? *reinterpret_cast<const uint32_t*>(qg + (size_t)h_lo * kD + c + 8) : 0u;
+      qf[ks][3] = h_hi < G ? *reinterpret_cast<const uint32_t*>(qg + (size_t)h_hi * kD + c + 8) : 0u;
     }
-    float acc[S::PPT][S::HB][8];
+    float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
+    float o[16][4];
 #pragma unroll
-    for (int k = 0; k < S::PPT; ++k)
-#pragma unroll
-      for (int h = 0; h < S::HB; ++h)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[k][h][e] = 0.f;
+    for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
 
     for (int c = c0; c < c1; ++c, ++it) {
       const int s = it % kAttnStages;
@@ -231,204 +233,212 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
         dead = true;
       }
       const uint64_t okm = dead ? 0ull : okmask[s];
-      const uint4* kt = stage_kv + (size_t)s * 2 * kAttnRows * 16;
-      const uint4* vt = kt + kAttnRows * 16;
+      const uint32_t kbase = smem0 + (uint32_t)(s * 2 * kAttnTile);
+      const uint32_t vbase = kbase + kAttnTile;
 
-      // ---- scores, 8 rows per half-warp
-#pragma unroll 1
-      for (int hb = 0; hb < S::NHB; ++hb) {
-        if (S::NHB > 1) {
+      // ---- S = Q K^T over this warp's RW rows
+      float sacc[S::NT][4];
 #pragma unroll
-          for (int h = 0; h < S::HB; ++h)
+      for (int n = 0; n < S::NT; ++n) sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) qr[h][e] = q_s[(hb * S::HB + h) * kD + l16 * 8 + e];
-        }
+      for (int ks = 0; ks < 8; ++ks) {
 #pragma unroll
-        for (int bt = 0; bt < S::NB; ++bt) {
-          const int rbase = hw * 8 + bt * S::R;
-          float sacc[S::R][S::HB];
-#pragma unroll
-          for (int j = 0; j < S::R; ++j) {
-            const uint4 w = kt[(rbase + (j ^ (l16 & (S::R - 1)))) * 16 + l16];
-            float v[8];
-            unpack8(w, v);
-#pragma unroll
-            for (int h = 0; h < S::HB; ++h) {
-              float d0 = v[0] * qr[h][0];
-#pragma unroll
-              for (int e = 1; e < 8; ++e) d0 = fmaf(v[e], qr[h][e], d0);
-              sacc[j][h] = d0;
-            }
-          }
-#pragma unroll
-          for (int m = S::R / 2; m >= 1; m >>= 1)
-#pragma unroll
-            for (int j = 0; j < m; ++j)
-#pragma unroll
-              for (int h = 0; h < S::HB; ++h) sacc[j][h] += __shfl_xor_sync(0xffffffffu, sacc[j + m][h], m);
-#pragma unroll
-          for (int m = S::R; m < 16; m <<= 1)
-#pragma unroll
-            for (int h = 0; h < S::HB; ++h) sacc[0][h] += __shfl_xor_sync(0xffffffffu, sacc[0][h], m);
-          if (l16 < S::R) {
-            const int r = rbase + l16;
-            const bool ok = (okm >> r) & 1ull;
-#pragma unroll
-            for (int h = 0; h < S::HB; ++h) sc[(hb * S::HB + h) * kAttnRows + r] = ok ? sacc[0][h] : -INFINITY;
-          }
+        for (int np = 0; np < S::NT / 2; ++np) {
+          const int row = row0 + np * 16 + ((lm >> 1) << 3) + lr;
+          const uint32_t addr = kbase + row * kAttnPitch + (ks * 16 + (lm & 1) * 8) * 2;
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(addr, b0, b1, b2, b3);
+          mma_bf16(sacc[2 * np], qf[ks], b0, b1);
+          mma_bf16(sacc[2 * np + 1], qf[ks], b2, b3);
         }
       }
-      cons_bar();
-
-      // ---- online softmax, heads spread over the 4 consumer warps
-      for (int h = warp; h < G; h += kAttnCWarps) {
-        const float x0 = sc[h * kAttnRows + lane], x1 = sc[h * kAttnRows + lane + 32];
-        const float mo = m_s[h];
-        const float mn = fmaxf(mo, warp_max(fmaxf(x0, x1)));
-        const float p0 = mn == -INFINITY ? 0.f : exp2f(x0 - mn);
-        const float p1 = mn == -INFINITY ? 0.f : exp2f(x1 - mn);
-        pT[lane * G + h] = p0;
-        pT[(lane + 32) * G + h] = p1;
-        const float ps = warp_sum(p0 + p1);
-        if (lane == 0) {
-          const float alpha = (mn == -INFINITY) ? 1.f : exp2f(mo - mn);
-          al_s[h] = alpha;
-          l_s[h] = l_s[h] * alpha + ps;
-          m_s[h] = mn;
+      // ---- masked online softmax (base 2), per head row of the tile
+      float mx_lo = -INFINITY, mx_hi = -INFINITY;
+#pragma unroll
+      for (int n = 0; n < S::NT; ++n) {
+        const int r = row0 + n * 8 + tig * 2;
+        const bool v0 = (okm >> r) & 1ull, v1 = (okm >> (r + 1)) & 1ull;
+        sacc[n][0] = v0 ? sacc[n][0] * a.scale2 : -INFINITY;
+        sacc[n][1] = v1 ? sacc[n][1] * a.scale2 : -INFINITY;
+        sacc[n][2] = v0 ? sacc[n][2] * a.scale2 : -INFINITY;
+        sacc[n][3] = v1 ? sacc[n][3] * a.scale2 : -INFINITY;
+        mx_lo = fmaxf(mx_lo, fmaxf(sacc[n][0], sacc[n][1]));
+        mx_hi = fmaxf(mx_hi, fmaxf(sacc[n][2], sacc[n][3]));
+      }
+#pragma unroll
+      for (int off = 1; off <= 2; off <<= 1) {
+        mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, off));
+        mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, off));
+      }
+      const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
+      const float al_lo = mn_lo == -INFINITY ? 1.f : exp2f(m_lo - mn_lo);
+      const float al_hi = mn_hi == -INFINITY ? 1.f : exp2f(m_hi - mn_hi);
+      float sum_lo = 0.f, sum_hi = 0.f;
+#pragma unroll
+      for (int n = 0; n < S::NT; ++n) {
+        sacc[n][0] = mn_lo == -INFINITY ? 0.f : exp2f(sacc[n][0] - mn_lo);
+        sacc[n][1] = mn_lo == -INFINITY ? 0.f : exp2f(sacc[n][1] - mn_lo);
+        sacc[n][2] = mn_hi == -INFINITY ? 0.f : exp2f(sacc[n][2] - mn_hi);
+        sacc[n][3] = mn_hi == -INFINITY ? 0.f : exp2f(sacc[n][3] - mn_hi);
+        sum_lo += sacc[n][0] + sacc[n][1];
+        sum_hi += sacc[n][2] + sacc[n][3];
+      }
+#pragma unroll
+      for (int off = 1; off <= 2; off <<= 1) {
+        sum_lo += __shfl_xor_sync(0xffffffffu, sum_lo, off);
+        sum_hi += __shfl_xor_sync(0xffffffffu, sum_hi, off);
+      }
+      l_lo = l_lo * al_lo + sum_lo;
+      l_hi = l_hi * al_hi + sum_hi;
+      m_lo = mn_lo;
+      m_hi = mn_hi;
+      if (__any_sync(0xffffffffu, al_lo != 1.f || al_hi != 1.f)) {
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {
+          o[n][0] *= al_lo; o[n][1] *= al_lo;
+          o[n][2] *= al_hi; o[n][3] *= al_hi;
         }
       }
-      cons_bar();
-
-      // ---- P.V over the valid rows of this thread's row group
+      // ---- O += P V, P split into bf16 high + low parts
 #pragma unroll
-      for (int k = 0; k < S::PPT; ++k) {
-        const int h0 = (hbp + k * (S::TPG / 16)) * S::HB;
+      for (int ks = 0; ks < S::KS; ++ks) {
+        uint32_t ah[4], al[4];
+        const float* p0 = sacc[2 * ks];
+        const float* p1 = sacc[2 * ks + 1];
+        const float h00 = bf16_round(p0[0]), h01 = bf16_round(p0[1]), h02 = bf16_round(p0[2]),
+                    h03 = bf16_round(p0[3]);
+        const float h10 = bf16_round(p1[0]), h11 = bf16_round(p1[1]), h12 = bf16_round(p1[2]),
+                    h13 = bf16_round(p1[3]);
+        ah[0] = pack_bf16(h00, h01); ah[1] = pack_bf16(h02, h03);
+        ah[2] = pack_bf16(h10, h11); ah[3] = pack_bf16(h12, h13);
+        al[0] = pack_bf16(p0[0] - h00, p0[1] - h01); al[1] = pack_bf16(p0[2] - h02, p0[3] - h03);
+        al[2] = pack_bf16(p1[0] - h10, p1[1] - h11); al[3] = pack_bf16(p1[2] - h12, p1[3] - h13);
+        const int vrow = row0 + ks * 16 + ((lm & 1) << 3) + lr;
 #pragma unroll
-        for (int h = 0; h < S::HB; ++h) {
-          const float al = al_s[h0 + h];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) acc[k][h][e] *= al;
-        }
-      }
-      for (int r = rg; r < kAttnRows; r += S::RG) {
-        if (!((okm >> r) & 1ull)) continue;
-        const uint4 w = vt[r * 16 + cc];
-        float v[8];
-        unpack8(w, v);
-#pragma unroll
-        for (int k = 0; k < S::PPT; ++k) {
-          const int h0 = (hbp + k * (S::TPG / 16)) * S::HB;
-          float p[S::HB];
-#pragma unroll
-          for (int h = 0; h < S::HB; ++h) p[h] = pT[r * G + h0 + h];
-#pragma unroll
-          for (int h = 0; h < S::HB; ++h)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[k][h][e] = fmaf(p[h], v[e], acc[k][h][e]);
+        for (int dp = 0; dp < 8; ++dp) {
+          const uint32_t addr = vbase + vrow * kAttnPitch + (dp * 16 + (lm >> 1) * 8) * 2;
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(addr, b0, b1, b2, b3);
+          mma_bf16(o[2 * dp], ah, b0, b1);
+          mma_bf16(o[2 * dp], al, b0, b1);
+          mma_bf16(o[2 * dp + 1], ah, b2, b3);
+          mma_bf16(o[2 * dp + 1], al, b2, b3);
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
 
-    // ---- fold row groups (lanes l, l^16 in the warp, then the warps in a
-    // fixed order); write the output or this split's partial
-    if (S::TPG <= 16) {
-#pragma unroll
-      for (int k = 0; k < S::PPT; ++k)
-#pragma unroll
-        for (int h = 0; h < S::HB; ++h)
-#pragma unroll
-          for (int e = 0; e < 8; ++e) acc[k][h][e] += __shfl_xor_sync(0xffffffffu, acc[k][h][e], 16);
+    // ---- merge the row-split warps of each head tile, then output or partial
+    cons_bar();  // the previous item's readers of mo / ml / wsp are done
+    if (tig == 0) {
+      if (h_lo < G) { ml[(rs * G + h_lo) * 2] = m_lo; ml[(rs * G + h_lo) * 2 + 1] = l_lo; }
+      if (h_hi < G) { ml[(rs * G + h_hi) * 2] = m_hi; ml[(rs * G + h_hi) * 2 + 1] = l_hi; }
     }
-    if (S::TPG > 16 || lane < 16) {
-      const int slot = S::TPG <= 16 ? warp : rg;
 #pragma unroll
-      for (int k = 0; k < S::PPT; ++k) {
-        const int h0 = (hbp + k * (S::TPG / 16)) * S::HB;
-#pragma unroll
-        for (int h = 0; h < S::HB; ++h) {
-          float* dst = ored + ((size_t)slot * G + h0 + h) * kD + cc * 8;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) dst[e] = acc[k][h][e];
-        }
+    for (int n = 0; n < 16; ++n) {
+      const int d0 = n * 8 + tig * 2;
+      if (h_lo < G) {
+        mo[((size_t)rs * G + h_lo) * kD + d0] = o[n][0];
+        mo[((size_t)rs * G + h_lo) * kD + d0 + 1] = o[n][1];
       }
+      if (h_hi < G) {
+        mo[((size_t)rs * G + h_hi) * kD + d0] = o[n][2];
+        mo[((size_t)rs * G + h_hi) * kD + d0 + 1] = o[n][3];
+      }
+    }
+    cons_bar();
+    float* wr = wsp;                   // [NRS][G] row-split weights
+    float* mlg = wsp + S::NRS * G;     // [G][2]: (M, L)
+    for (int h = tid; h < G; h += kAttnCThreads) {
+      float Mx = -INFINITY;
+#pragma unroll
+      for (int r = 0; r < S::NRS; ++r) Mx = fmaxf(Mx, ml[(r * G + h) * 2]);
+      float Ls = 0.f;
+#pragma unroll
+      for (int r = 0; r < S::NRS; ++r) {
+        const float mr = ml[(r * G + h) * 2];
+        const float w = (Mx == -INFINITY || mr == -INFINITY) ? 0.f : exp2f(mr - Mx);
+        wr[r * G + h] = w;
+        Ls += ml[(r * G + h) * 2 + 1] * w;
+      }
+      mlg[2 * h] = Mx;
+      mlg[2 * h + 1] = Ls;
     }
     cons_bar();
     const size_t lbg = (size_t)lb * a.n_kv + g;
     float* outp = a.out + ((size_t)lb * a.n_q + (size_t)g * G) * kD;
     if (a.n_split == 1) {
-      for (int i = ctid; i < G * kD; i += kAttnCThreads) {
-        float o = 0.f;
+      for (int i = tid; i < G * kD; i += kAttnCThreads) {
+        const int h = i / kD;
+        float v = 0.f;
 #pragma unroll
-        for (int r = 0; r < S::NRED; ++r) o += ored[(size_t)r * G * kD + i];
-        const float l = l_s[i / kD];
-        outp[i] = l > 0.f ? o / l : 0.f;
+        for (int r = 0; r < S::NRS; ++r) v += mo[(size_t)r * G * kD + i] * wr[r * G + h];
+        const float L = mlg[2 * h + 1];
+        outp[i] = L > 0.f ? v / L : 0.f;
       }
       continue;
     }
     float* pp = a.part + (lbg * a.n_split + split) * (size_t)G * kPartStride;
-    for (int i = ctid; i < G * kD; i += kAttnCThreads) {
-      float o = 0.f;
+    for (int i = tid; i < G * kD; i += kAttnCThreads) {
+      const int h = i / kD;
+      float v = 0.f;
 #pragma unroll
-      for (int r = 0; r < S::NRED; ++r) o += ored[(size_t)r * G * kD + i];
-      pp[(i / kD) * kPartStride + 4 + (i % kD)] = o;
+      for (int r = 0; r < S::NRS; ++r) v += mo[(size_t)r * G * kD + i] * wr[r * G + h];
+      pp[h * kPartStride + 4 + (i % kD)] = v;
     }
-    for (int h = ctid; h < G; h += kAttnCThreads) {
-      pp[h * kPartStride] = m_s[h];
-      pp[h * kPartStride + 1] = l_s[h];
+    for (int h = tid; h < G; h += kAttnCThreads) {
+      pp[h * kPartStride] = mlg[2 * h];
+      pp[h * kPartStride + 1] = mlg[2 * h + 1];
     }
     __threadfence();
     cons_bar();
-    if (ctid == 0) s_last = (atomicAdd(&a.counters[lbg], 1u) == (uint32_t)(a.n_split - 1));
+    if (tid == 0) s_last = (atomicAdd(&a.counters[lbg], 1u) == (uint32_t)(a.n_split - 1));
     cons_bar();
     if (!s_last) continue;
     __threadfence();
-    // merge the splits: stage every (max, sum) in shared memory (q_s is free
-    // now), per head the global max and the weights, then float4 sums
+    // merge the splits: (max, sum) of every split staged in shared memory,
+    // then float4 sums with independent loads
     const float* pb = a.part + lbg * a.n_split * (size_t)G * kPartStride;
-    float* wsp = q_s;                                   // [n_split][G] weights
-    float* linv = q_s + a.n_split * G;                  // [G]
-    for (int i = ctid; i < a.n_split * G; i += kAttnCThreads) wsp[i] = __ldcg(pb + (size_t)i * kPartStride);
+    float* wsplit = mo;                                 // [n_split][G] (mo is free now)
+    float* linv = mo + a.n_split * G;                   // [G]
+    for (int i = tid; i < a.n_split * G; i += kAttnCThreads) wsplit[i] = __ldcg(pb + (size_t)i * kPartStride);
     cons_bar();
-    for (int h = ctid; h < G; h += kAttnCThreads) {
-      float M = -INFINITY;
-      for (int sp = 0; sp < a.n_split; ++sp) M = fmaxf(M, wsp[sp * G + h]);
+    for (int h = tid; h < G; h += kAttnCThreads) {
+      float Mx = -INFINITY;
+      for (int sp = 0; sp < a.n_split; ++sp) Mx = fmaxf(Mx, wsplit[sp * G + h]);
       float Ls = 0.f;
       for (int sp = 0; sp < a.n_split; ++sp) {
-        const float ms = wsp[sp * G + h];
-        const float w = (M == -INFINITY || ms == -INFINITY) ? 0.f : exp2f(ms - M);
+        const float ms = wsplit[sp * G + h];
+        const float w = (Mx == -INFINITY || ms == -INFINITY) ? 0.f : exp2f(ms - Mx);
         Ls += __ldcg(pb + ((size_t)sp * G + h) * kPartStride + 1) * w;
-        wsp[sp * G + h] = w;
+        wsplit[sp * G + h] = w;
       }
       linv[h] = Ls > 0.f ? 1.f / Ls : 0.f;
     }
     cons_bar();
-    for (int i4 = ctid; i4 < G * (kD / 4); i4 += kAttnCThreads) {
+    for (int i4 = tid; i4 < G * (kD / 4); i4 += kAttnCThreads) {
       const int h = i4 / (kD / 4), c4 = i4 - h * (kD / 4);
       float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
       for (int sp = 0; sp < a.n_split; ++sp) {
-        const float w = wsp[sp * G + h];
+        const float w = wsplit[sp * G + h];
         const float4 v = __ldcg(reinterpret_cast<const float4*>(pb + ((size_t)sp * G + h) * kPartStride + 4) + c4);
         O.x = fmaf(w, v.x, O.x); O.y = fmaf(w, v.y, O.y); O.z = fmaf(w, v.z, O.z); O.w = fmaf(w, v.w, O.w);
       }
       const float li = linv[h];
       reinterpret_cast<float4*>(outp + (size_t)h * kD)[c4] = make_float4(O.x * li, O.y * li, O.z * li, O.w * li);
     }
-    if (ctid == 0) a.counters[lbg] = 0u;
+    if (tid == 0) a.counters[lbg] = 0u;
   }
 }
 
-static int attn_ctas_per_sm(int G) { return G <= 8 ? 2 : 1; }
-
-static void attn_split(int n_layers, int B, int n_kv, int budget, int G, int* n_split, int* cps,
-                       int* n_chunks) {
+static void attn_split(int n_layers, int B, int n_kv, int budget, int* n_split, int* cps, int* n_chunks) {
   const int nc = (budget + kAttnRows - 1) / kAttnRows;
   const long long base = (long long)n_layers * B * n_kv;
   // target items: ~2 per resident CTA on a 152-SM GB300 (a fixed count, so
   // the workspace size does not depend on the device)
-  const long long target = (long long)kAttnItemsPerCta * attn_ctas_per_sm(G) * 152;
+  const long long target = (long long)kAttnItemsPerCta * kAttnCtasPerSm * 152;
   long long want = (target + base - 1) / base;
   if (want < 1) want = 1;
   if (want > nc) want = nc;
@@ -440,7 +450,7 @@ static void attn_split(int n_layers, int B, int n_kv, int budget, int G, int* n_
 
 size_t attn_workspace(int n_layers, int B, int n_q, int n_kv, int budget) {
   int ns, cps, nc;
-  attn_split(n_layers, B, n_kv, budget, n_q / n_kv, &ns, &cps, &nc);
+  attn_split(n_layers, B, n_kv, budget, &ns, &cps, &nc);
   const size_t nseg = (size_t)n_layers * B * n_kv;
   const size_t cnt = (nseg * sizeof(uint32_t) + 255) & ~size_t(255);
   const size_t part = ns > 1 ? nseg * ns * (size_t)(n_q / n_kv) * kPartStride * sizeof(float) : 0;
@@ -456,7 +466,7 @@ static cudaError_t launch_attn(const AttnArgs& aa, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  int grid = AttnShape<G>::CTAS_PER_SM * device_sm_count();
+  int grid = kAttnCtasPerSm * device_sm_count();
   if (grid < 1) grid = 1;
   if (grid > aa.n_items) grid = aa.n_items;
   attn_kernel<G><<<grid, kAttnThreads, smem, st>>>(aa);
@@ -478,7 +488,7 @@ int attn_launch(const void* q, const spc_kv_view* views, const int32_t* selected
                                      ((nseg * sizeof(uint32_t) + 255) & ~size_t(255)));
   aa.status = nullptr;
   aa.B = B; aa.n_q = n_q; aa.n_kv = n_kv; aa.K = budget;
-  attn_split(n_layers, B, n_kv, budget, n_q / n_kv, &aa.n_split, &aa.cps, &aa.n_chunks);
+  attn_split(n_layers, B, n_kv, budget, &aa.n_split, &aa.cps, &aa.n_chunks);
   aa.n_items = (int)(nseg * aa.n_split);
   aa.scale2 = scale * kLog2e;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
