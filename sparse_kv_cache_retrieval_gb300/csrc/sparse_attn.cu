@@ -173,6 +173,20 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
         const int nval = __popc(lo) + __popc(hi);
         uint8_t* kdst = asmem + (size_t)s * 2 * kAttnTile;
         uint8_t* vdst = kdst + kAttnTile;
+        // rows not copied: V is zeroed so that P = 0 times it stays 0 (the
+        // tensor cores multiply every row; K of such rows only feeds scores
+        // that are replaced by -inf)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (!val[h]) {
+            uint4* vr = reinterpret_cast<uint4*>(vdst + (lane + 32 * h) * kAttnPitch);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) vr[q] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        // order these writes before the stage's next bulk copies
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
         if (lane == 0) {
           okmask[s] = ((uint64_t)hi << 32) | lo;
           mbar_arrive_expect_tx(&full[s], 2u * nval * kRowBytes);
