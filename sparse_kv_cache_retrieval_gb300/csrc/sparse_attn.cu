@@ -13,9 +13,10 @@
 // FMAs) held the SMs to ~1 instruction per cycle, well short of the memory
 // rate. Here both products run on the tensor cores with mma.sync m16n8k16
 // (bf16 in, fp32 accumulate; bf16 x bf16 products are exact in fp32):
-//  * work item = a contiguous range of 64-row chunks of one (layer, request,
-//    KV head); persistent CTAs of 4 consumer warps + 1 producer warp walk the
-//    items round-robin;
+//  * each (layer, request, KV head) is served by a thread-block cluster of up
+//    to 8 CTAs (and, when a launch has too few of them to fill the GPU, by a
+//    few such clusters); each CTA (4 consumer warps + 1 producer warp) streams
+//    a contiguous range of 64-row chunks;
 //  * the producer copies each kept K and V row (256 bytes) with cp.async.bulk
 //    into a 2-stage shared-memory ring whose rows are padded to 272 bytes (so
 //    ldmatrix reads them without bank conflicts), counting bytes on an
@@ -26,9 +27,12 @@
 //    with P reused from the S accumulators as an A fragment, split into bf16
 //    high and low parts (two MMAs) so the weights keep ~16 bits, against
 //    ldmatrix.trans'ed V fragments;
-//  * warps sharing a head tile merge (max, sum, O) through shared memory at the
-//    end of an item; the item's result is the output or a partial that the last
-//    CTA of its (layer, request, KV head) merges in split order (deterministic).
+//  * warps sharing a head tile merge (max, sum, O) through shared memory; the
+//    CTAs of a cluster merge through distributed shared memory (rank 0 reads
+//    its peers); when several clusters share a (layer, request, KV head), each
+//    writes a partial to the workspace and the last one merges them in split
+//    order. Every merge is in a fixed order (deterministic).
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
 #include "spc_device.cuh"
@@ -43,8 +47,8 @@ constexpr int kAttnCThreads = kAttnCWarps * 32;
 constexpr int kAttnThreads = kAttnCThreads + 32;    // + producer warp
 constexpr int kAttnStages = 2;
 constexpr int kAttnTile = kAttnRows * kAttnPitch;   // 17408 bytes (K or V)
-constexpr int kAttnCtasPerSm = 2;
-constexpr int kAttnItemsPerCta = 2;                 // split target: ~2 items per resident CTA
+constexpr int kAttnMaxCluster = 8;
+constexpr int kAttnTargetCtas = 228;                // ~1.5 CTAs per SM of a 152-SM GB300
 constexpr long long kAttnWait = 4000000000ll;
 constexpr int kPartStride = kD + 4;                 // (m, l, pad, pad, o[128])
 
@@ -66,18 +70,22 @@ struct AttnArgs {
   float* part;
   uint32_t* counters;
   int* status;
-  int B, n_q, n_kv, K, n_split, cps, n_chunks, n_items;
+  int B, n_q, n_kv, K, n_split, C, cpc, n_chunks;
   float scale2;
 };
+
+constexpr size_t round16(size_t x) { return (x + 15) & ~size_t(15); }
 
 template <int G>
 struct AttnSmem {
   using S = AttnShape<G>;
   static constexpr size_t stages = (size_t)kAttnStages * 2 * kAttnTile;
-  static constexpr size_t mo = sizeof(float) * S::NRS * G * kD;       // per row-split O
-  static constexpr size_t ml = sizeof(float) * 2 * S::NRS * G;        // per row-split (m, l)
-  static constexpr size_t wsp = sizeof(float) * (S::NRS * G + 2 * G); // row-split weights, (M, L)
-  static constexpr size_t total = stages + mo + ml + wsp + sizeof(uint64_t) * 3 * kAttnStages;
+  static constexpr size_t mo = round16(sizeof(float) * S::NRS * G * kD);   // per row-split O
+  static constexpr size_t ml = round16(sizeof(float) * 2 * S::NRS * G);    // per row-split (m, l)
+  // row-split weights [NRS][G], later cluster weights [C][G] + sums [G]
+  static constexpr size_t wsp = round16(sizeof(float) * ((S::NRS > kAttnMaxCluster ? S::NRS : kAttnMaxCluster) + 1) * G);
+  static constexpr size_t cres = round16(sizeof(float) * G * kPartStride); // this CTA's (m, l, O)
+  static constexpr size_t total = stages + mo + ml + wsp + cres + sizeof(uint64_t) * 3 * kAttnStages;
 };
 
 __device__ __forceinline__ void cons_bar() { asm volatile("bar.sync 1, %0;" :: "n"(kAttnCThreads) : "memory"); }
@@ -103,27 +111,30 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 __device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 
-__device__ __forceinline__ void item_coords(const AttnArgs& a, int item, int& lb, int& g, int& split) {
-  split = item % a.n_split;
-  const int rest = item / a.n_split;
-  g = rest % a.n_kv;
-  lb = rest / a.n_kv;
-}
-
 template <int G>
 __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
   using S = AttnShape<G>;
   using M = AttnSmem<G>;
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ __align__(128) uint8_t asmem[];
   float* mo = reinterpret_cast<float*>(asmem + M::stages);                       // [NRS][G][128]
   float* ml = reinterpret_cast<float*>(asmem + M::stages + M::mo);               // [NRS][G][2]
   float* wsp = reinterpret_cast<float*>(asmem + M::stages + M::mo + M::ml);      // [NRS][G] + [G][2]
-  uint64_t* okmask = reinterpret_cast<uint64_t*>(asmem + M::stages + M::mo + M::ml + M::wsp);
+  float* cres = reinterpret_cast<float*>(asmem + M::stages + M::mo + M::ml + M::wsp);  // [G][132]
+  uint64_t* okmask = reinterpret_cast<uint64_t*>(asmem + M::stages + M::mo + M::ml + M::wsp + M::cres);
   uint64_t* full = okmask + kAttnStages;
   uint64_t* empty = full + kAttnStages;
   __shared__ int s_last;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rank = (int)cluster.block_rank();
+  const int cid = blockIdx.x / a.C;                 // cluster id
+  const int split = cid % a.n_split, seg = cid / a.n_split;
+  const int g = seg % a.n_kv, lb = seg / a.n_kv, b = lb % a.B;
+  const int c0 = min(a.n_chunks, (split * a.C + rank) * a.cpc);
+  const int c1 = min(a.n_chunks, c0 + a.cpc);
+
   if (tid == 0) {
     for (int s = 0; s < kAttnStages; ++s) {
       mbar_init(&full[s], 1);
@@ -135,93 +146,79 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
 
   if (warp == kAttnCWarps) {
     // ================= producer warp: per-row bulk copies into padded rows
+    const spc_kv_view vw = a.views[lb];
+    const int32_t* idx = (vw.use_slots ? a.slot_pos : a.selected) + ((size_t)b * a.n_kv + g) * a.K;
+    const uint16_t* kb = static_cast<const uint16_t*>(vw.k) + (size_t)g * vw.rows * kD;
+    const uint16_t* vb = static_cast<const uint16_t*>(vw.v) + (size_t)g * vw.rows * kD;
     int it = 0;
-    bool ok = true;
-    for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
-      int lb, g, split;
-      item_coords(a, item, lb, g, split);
-      const spc_kv_view vw = a.views[lb];
-      const int b = lb % a.B;
-      const int32_t* idx = (vw.use_slots ? a.slot_pos : a.selected) + ((size_t)b * a.n_kv + g) * a.K;
-      const uint16_t* kb = static_cast<const uint16_t*>(vw.k) + (size_t)g * vw.rows * kD;
-      const uint16_t* vb = static_cast<const uint16_t*>(vw.v) + (size_t)g * vw.rows * kD;
-      const int c0 = split * a.cps, c1 = min(c0 + a.cps, a.n_chunks);
-      for (int c = c0; c < c1; ++c, ++it) {
-        const int s = it % kAttnStages;
-        const uint32_t ph = (it / kAttnStages) & 1;
-        if (!mbar_wait_bounded(&empty[s], ph ^ 1, kAttnWait)) {
-          if (lane == 0) set_status(a.status, SPC_ERR_TIMEOUT);
-          ok = false;
-          break;
-        }
-        long long src[2];
-        bool val[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int r = lane + 32 * h, i = c * kAttnRows + r;
-          long long row = -1;
-          if (i < a.K) {
-            const int v = idx[i];
-            if (v >= 0) row = vw.use_slots ? i : v;
-            if (row >= vw.rows) row = -1;
-          }
-          val[h] = row >= 0;
-          src[h] = row;
-        }
-        const uint32_t lo = __ballot_sync(0xffffffffu, val[0]);
-        const uint32_t hi = __ballot_sync(0xffffffffu, val[1]);
-        const int nval = __popc(lo) + __popc(hi);
-        uint8_t* kdst = asmem + (size_t)s * 2 * kAttnTile;
-        uint8_t* vdst = kdst + kAttnTile;
-        // rows not copied: V is zeroed so that P = 0 times it stays 0 (the
-        // tensor cores multiply every row; K of such rows only feeds scores
-        // that are replaced by -inf)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          if (!val[h]) {
-            uint4* vr = reinterpret_cast<uint4*>(vdst + (lane + 32 * h) * kAttnPitch);
-#pragma unroll
-            for (int q = 0; q < 16; ++q) vr[q] = make_uint4(0u, 0u, 0u, 0u);
-          }
-        }
-        // order these writes before the stage's next bulk copies
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) {
-          okmask[s] = ((uint64_t)hi << 32) | lo;
-          mbar_arrive_expect_tx(&full[s], 2u * nval * kRowBytes);
-        }
-        __syncwarp();
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          if (val[h]) {
-            const int r = lane + 32 * h;
-            bulk_g2s(kdst + r * kAttnPitch, kb + (size_t)src[h] * kD, kRowBytes, &full[s]);
-            bulk_g2s(vdst + r * kAttnPitch, vb + (size_t)src[h] * kD, kRowBytes, &full[s]);
-          }
-        }
-        __syncwarp();
+    for (int c = c0; c < c1; ++c, ++it) {
+      const int s = it % kAttnStages;
+      const uint32_t ph = (it / kAttnStages) & 1;
+      if (!mbar_wait_bounded(&empty[s], ph ^ 1, kAttnWait)) {
+        if (lane == 0) set_status(a.status, SPC_ERR_TIMEOUT);
+        break;
       }
+      long long src[2];
+      bool val[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int r = lane + 32 * h, i = c * kAttnRows + r;
+        long long row = -1;
+        if (i < a.K) {
+          const int v = idx[i];
+          if (v >= 0) row = vw.use_slots ? i : v;
+          if (row >= vw.rows) row = -1;
+        }
+        val[h] = row >= 0;
+        src[h] = row;
+      }
+      const uint32_t lo = __ballot_sync(0xffffffffu, val[0]);
+      const uint32_t hi = __ballot_sync(0xffffffffu, val[1]);
+      const int nval = __popc(lo) + __popc(hi);
+      uint8_t* kdst = asmem + (size_t)s * 2 * kAttnTile;
+      uint8_t* vdst = kdst + kAttnTile;
+      // rows not copied: V is zeroed so that P = 0 times it stays 0 (the
+      // tensor cores multiply every row; K of such rows only feeds scores
+      // that are replaced by -inf)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (!val[h]) {
+          uint4* vr = reinterpret_cast<uint4*>(vdst + (lane + 32 * h) * kAttnPitch);
+#pragma unroll
+          for (int q = 0; q < 16; ++q) vr[q] = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      // order these writes before the stage's next bulk copies
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) {
+        okmask[s] = ((uint64_t)hi << 32) | lo;
+        mbar_arrive_expect_tx(&full[s], 2u * nval * kRowBytes);
+      }
+      __syncwarp();
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (val[h]) {
+          const int r = lane + 32 * h;
+          bulk_g2s(kdst + r * kAttnPitch, kb + (size_t)src[h] * kD, kRowBytes, &full[s]);
+          bulk_g2s(vdst + r * kAttnPitch, vb + (size_t)src[h] * kD, kRowBytes, &full[s]);
+        }
+      }
+      __syncwarp();
     }
     if (lane == 0)
       for (int k = max(0, it - kAttnStages); k < it; ++k)
         mbar_wait_bounded(&full[k % kAttnStages], (k / kAttnStages) & 1, kAttnWait);
-    return;
-  }
-
-  // ================= consumers
-  const int gid = lane >> 2, tig = lane & 3;
-  const int mt = warp / S::NRS, rs = warp % S::NRS;
-  const int row0 = rs * S::RW;                      // this warp's rows in a chunk
-  const int h_lo = mt * 16 + gid, h_hi = h_lo + 8;  // heads of this thread's rows
-  const uint32_t smem0 = smem_u32(asmem);
-  const int lm = lane >> 3, lr = lane & 7;          // ldmatrix: matrix and row of this lane
-  int it = 0;
-  bool dead = false;
-  for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
-    int lb, g, split;
-    item_coords(a, item, lb, g, split);
-    const int c0 = split * a.cps, c1 = min(c0 + a.cps, a.n_chunks);
+    __syncwarp();
+  } else {
+    // ================= consumers
+    const int gid = lane >> 2, tig = lane & 3;
+    const int mt = warp / S::NRS, rs = warp % S::NRS;
+    const int row0 = rs * S::RW;                      // this warp's rows in a chunk
+    const int h_lo = mt * 16 + gid, h_hi = h_lo + 8;  // heads of this thread's rows
+    const uint32_t smem0 = smem_u32(asmem);
+    const int lm = lane >> 3, lr = lane & 7;          // ldmatrix: matrix and row of this lane
+    bool dead = false;
 
     // Q fragments of this warp's head tile (rows >= G are zero)
     const uint16_t* qg = a.q + ((size_t)lb * a.n_q + (size_t)g * G) * kD;
@@ -239,6 +236,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
 #pragma unroll
     for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
 
+    int it = 0;
     for (int c = c0; c < c1; ++c, ++it) {
       const int s = it % kAttnStages;
       const uint32_t ph = (it / kAttnStages) & 1;
@@ -343,8 +341,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
       if (lane == 0) mbar_arrive(&empty[s]);
     }
 
-    // ---- merge the row-split warps of each head tile, then output or partial
-    cons_bar();  // the previous item's readers of mo / ml / wsp are done
+    // ---- merge the row-split warps of each head tile into this CTA's result
     if (tig == 0) {
       if (h_lo < G) { ml[(rs * G + h_lo) * 2] = m_lo; ml[(rs * G + h_lo) * 2 + 1] = l_lo; }
       if (h_hi < G) { ml[(rs * G + h_hi) * 2] = m_hi; ml[(rs * G + h_hi) * 2 + 1] = l_hi; }
@@ -363,7 +360,6 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
     }
     cons_bar();
     float* wr = wsp;                   // [NRS][G] row-split weights
-    float* mlg = wsp + S::NRS * G;     // [G][2]: (M, L)
     for (int h = tid; h < G; h += kAttnCThreads) {
       float Mx = -INFINITY;
 #pragma unroll
@@ -376,95 +372,124 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
         wr[r * G + h] = w;
         Ls += ml[(r * G + h) * 2 + 1] * w;
       }
-      mlg[2 * h] = Mx;
-      mlg[2 * h + 1] = Ls;
+      cres[h * kPartStride] = Mx;
+      cres[h * kPartStride + 1] = Ls;
     }
     cons_bar();
-    const size_t lbg = (size_t)lb * a.n_kv + g;
-    float* outp = a.out + ((size_t)lb * a.n_q + (size_t)g * G) * kD;
-    if (a.n_split == 1) {
-      for (int i = tid; i < G * kD; i += kAttnCThreads) {
-        const int h = i / kD;
-        float v = 0.f;
-#pragma unroll
-        for (int r = 0; r < S::NRS; ++r) v += mo[(size_t)r * G * kD + i] * wr[r * G + h];
-        const float L = mlg[2 * h + 1];
-        outp[i] = L > 0.f ? v / L : 0.f;
-      }
-      continue;
-    }
-    float* pp = a.part + (lbg * a.n_split + split) * (size_t)G * kPartStride;
     for (int i = tid; i < G * kD; i += kAttnCThreads) {
       const int h = i / kD;
       float v = 0.f;
 #pragma unroll
       for (int r = 0; r < S::NRS; ++r) v += mo[(size_t)r * G * kD + i] * wr[r * G + h];
-      pp[h * kPartStride + 4 + (i % kD)] = v;
+      cres[h * kPartStride + 4 + (i % kD)] = v;
     }
-    for (int h = tid; h < G; h += kAttnCThreads) {
-      pp[h * kPartStride] = mlg[2 * h];
-      pp[h * kPartStride + 1] = mlg[2 * h + 1];
-    }
-    __threadfence();
-    cons_bar();
-    if (tid == 0) s_last = (atomicAdd(&a.counters[lbg], 1u) == (uint32_t)(a.n_split - 1));
-    cons_bar();
-    if (!s_last) continue;
-    __threadfence();
-    // merge the splits: (max, sum) of every split staged in shared memory,
-    // then float4 sums with independent loads
-    const float* pb = a.part + lbg * a.n_split * (size_t)G * kPartStride;
-    float* wsplit = mo;                                 // [n_split][G] (mo is free now)
-    float* linv = mo + a.n_split * G;                   // [G]
-    for (int i = tid; i < a.n_split * G; i += kAttnCThreads) wsplit[i] = __ldcg(pb + (size_t)i * kPartStride);
-    cons_bar();
+  }
+
+  // ================= cluster merge (distributed shared memory), all threads
+  cluster.sync();
+  if (rank == 0 && warp < kAttnCWarps) {
+    float* outp = a.out + ((size_t)lb * a.n_q + (size_t)g * G) * kD;
+    const size_t lbg = (size_t)lb * a.n_kv + g;
+    float* res = (a.n_split == 1) ? nullptr : a.part + (lbg * a.n_split + split) * (size_t)G * kPartStride;
+    // per head: max and weights of the cluster's CTAs (wsp is free here)
+    float* wc = wsp;  // [C][G] then [G] sums
     for (int h = tid; h < G; h += kAttnCThreads) {
       float Mx = -INFINITY;
-      for (int sp = 0; sp < a.n_split; ++sp) Mx = fmaxf(Mx, wsplit[sp * G + h]);
+      for (int r = 0; r < a.C; ++r) Mx = fmaxf(Mx, *cluster.map_shared_rank(cres + h * kPartStride, r));
       float Ls = 0.f;
-      for (int sp = 0; sp < a.n_split; ++sp) {
-        const float ms = wsplit[sp * G + h];
-        const float w = (Mx == -INFINITY || ms == -INFINITY) ? 0.f : exp2f(ms - Mx);
-        Ls += __ldcg(pb + ((size_t)sp * G + h) * kPartStride + 1) * w;
-        wsplit[sp * G + h] = w;
+      for (int r = 0; r < a.C; ++r) {
+        const float mr = *cluster.map_shared_rank(cres + h * kPartStride, r);
+        const float w = (Mx == -INFINITY || mr == -INFINITY) ? 0.f : exp2f(mr - Mx);
+        wc[r * G + h] = w;
+        Ls += *cluster.map_shared_rank(cres + h * kPartStride + 1, r) * w;
       }
-      linv[h] = Ls > 0.f ? 1.f / Ls : 0.f;
+      wc[a.C * G + h] = Ls;
+      if (res) { res[h * kPartStride] = Mx; res[h * kPartStride + 1] = Ls; }
     }
     cons_bar();
     for (int i4 = tid; i4 < G * (kD / 4); i4 += kAttnCThreads) {
       const int h = i4 / (kD / 4), c4 = i4 - h * (kD / 4);
       float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-      for (int sp = 0; sp < a.n_split; ++sp) {
-        const float w = wsplit[sp * G + h];
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(pb + ((size_t)sp * G + h) * kPartStride + 4) + c4);
+      for (int r = 0; r < a.C; ++r) {
+        const float w = wc[r * G + h];
+        const float4 v = *reinterpret_cast<const float4*>(
+            cluster.map_shared_rank(cres + h * kPartStride + 4 + 4 * c4, r));
         O.x = fmaf(w, v.x, O.x); O.y = fmaf(w, v.y, O.y); O.z = fmaf(w, v.z, O.z); O.w = fmaf(w, v.w, O.w);
       }
-      const float li = linv[h];
-      reinterpret_cast<float4*>(outp + (size_t)h * kD)[c4] = make_float4(O.x * li, O.y * li, O.z * li, O.w * li);
+      if (res) {
+        reinterpret_cast<float4*>(res + h * kPartStride + 4)[c4] = O;
+      } else {
+        const float L = wc[a.C * G + h];
+        const float li = L > 0.f ? 1.f / L : 0.f;
+        reinterpret_cast<float4*>(outp + (size_t)h * kD)[c4] = make_float4(O.x * li, O.y * li, O.z * li, O.w * li);
+      }
     }
-    if (tid == 0) a.counters[lbg] = 0u;
+    if (res) {
+      // several clusters serve this (layer, request, KV head): the last merges
+      __threadfence();
+      cons_bar();
+      if (tid == 0) s_last = (atomicAdd(&a.counters[lbg], 1u) == (uint32_t)(a.n_split - 1));
+      cons_bar();
+      if (s_last) {
+        __threadfence();
+        const float* pb = a.part + lbg * a.n_split * (size_t)G * kPartStride;
+        float* wsplit = mo;                                 // [n_split][G]
+        float* linv = mo + a.n_split * G;                   // [G]
+        for (int i = tid; i < a.n_split * G; i += kAttnCThreads) wsplit[i] = __ldcg(pb + (size_t)i * kPartStride);
+        cons_bar();
+        for (int h = tid; h < G; h += kAttnCThreads) {
+          float Mx = -INFINITY;
+          for (int sp = 0; sp < a.n_split; ++sp) Mx = fmaxf(Mx, wsplit[sp * G + h]);
+          float Ls = 0.f;
+          for (int sp = 0; sp < a.n_split; ++sp) {
+            const float ms = wsplit[sp * G + h];
+            const float w = (Mx == -INFINITY || ms == -INFINITY) ? 0.f : exp2f(ms - Mx);
+            Ls += __ldcg(pb + ((size_t)sp * G + h) * kPartStride + 1) * w;
+            wsplit[sp * G + h] = w;
+          }
+          linv[h] = Ls > 0.f ? 1.f / Ls : 0.f;
+        }
+        cons_bar();
+        for (int i4 = tid; i4 < G * (kD / 4); i4 += kAttnCThreads) {
+          const int h = i4 / (kD / 4), c4 = i4 - h * (kD / 4);
+          float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+          for (int sp = 0; sp < a.n_split; ++sp) {
+            const float w = wsplit[sp * G + h];
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(pb + ((size_t)sp * G + h) * kPartStride + 4) + c4);
+            O.x = fmaf(w, v.x, O.x); O.y = fmaf(w, v.y, O.y); O.z = fmaf(w, v.z, O.z); O.w = fmaf(w, v.w, O.w);
+          }
+          const float li = linv[h];
+          reinterpret_cast<float4*>(outp + (size_t)h * kD)[c4] = make_float4(O.x * li, O.y * li, O.z * li, O.w * li);
+        }
+        if (tid == 0) a.counters[lbg] = 0u;
+      }
+    }
   }
+  // keep this CTA's shared memory alive until rank 0 has read it
+  cluster.sync();
 }
 
-static void attn_split(int n_layers, int B, int n_kv, int budget, int* n_split, int* cps, int* n_chunks) {
+static void attn_plan(int n_layers, int B, int n_kv, int budget, int* C, int* n_split, int* cpc,
+                      int* n_chunks) {
   const int nc = (budget + kAttnRows - 1) / kAttnRows;
-  const long long base = (long long)n_layers * B * n_kv;
-  // target items: ~2 per resident CTA on a 152-SM GB300 (a fixed count, so
-  // the workspace size does not depend on the device)
-  const long long target = (long long)kAttnItemsPerCta * kAttnCtasPerSm * 152;
-  long long want = (target + base - 1) / base;
-  if (want < 1) want = 1;
-  if (want > nc) want = nc;
-  const int c = (int)((nc + want - 1) / want);
-  *cps = c;
-  *n_split = (nc + c - 1) / c;
+  const long long nseg = (long long)n_layers * B * n_kv;
+  const int c = nc < kAttnMaxCluster ? nc : kAttnMaxCluster;
+  // a fixed CTA target (not the device's SM count) keeps the workspace size a
+  // function of the shapes alone
+  long long s = (kAttnTargetCtas + nseg * c - 1) / (nseg * c);
+  const int smax = (nc + c - 1) / c;
+  if (s < 1) s = 1;
+  if (s > smax) s = smax;
+  *C = c;
+  *n_split = (int)s;
+  *cpc = (nc + (int)s * c - 1) / ((int)s * c);
   *n_chunks = nc;
 }
 
 size_t attn_workspace(int n_layers, int B, int n_q, int n_kv, int budget) {
-  int ns, cps, nc;
-  attn_split(n_layers, B, n_kv, budget, &ns, &cps, &nc);
+  int C, ns, cpc, nc;
+  attn_plan(n_layers, B, n_kv, budget, &C, &ns, &cpc, &nc);
   const size_t nseg = (size_t)n_layers * B * n_kv;
   const size_t cnt = (nseg * sizeof(uint32_t) + 255) & ~size_t(255);
   const size_t part = ns > 1 ? nseg * ns * (size_t)(n_q / n_kv) * kPartStride * sizeof(float) : 0;
@@ -472,7 +497,7 @@ size_t attn_workspace(int n_layers, int B, int n_q, int n_kv, int budget) {
 }
 
 template <int G>
-static cudaError_t launch_attn(const AttnArgs& aa, cudaStream_t st) {
+static cudaError_t launch_attn(const AttnArgs& aa, int nseg, cudaStream_t st) {
   const size_t smem = AttnSmem<G>::total;
   static bool attr = false;
   if (!attr) {
@@ -480,11 +505,19 @@ static cudaError_t launch_attn(const AttnArgs& aa, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  int grid = kAttnCtasPerSm * device_sm_count();
-  if (grid < 1) grid = 1;
-  if (grid > aa.n_items) grid = aa.n_items;
-  attn_kernel<G><<<grid, kAttnThreads, smem, st>>>(aa);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)(nseg * aa.n_split * aa.C));
+  cfg.blockDim = dim3(kAttnThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = aa.C;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_kernel<G>, aa);
 }
 
 int attn_launch(const void* q, const spc_kv_view* views, const int32_t* selected,
@@ -502,19 +535,18 @@ int attn_launch(const void* q, const spc_kv_view* views, const int32_t* selected
                                      ((nseg * sizeof(uint32_t) + 255) & ~size_t(255)));
   aa.status = nullptr;
   aa.B = B; aa.n_q = n_q; aa.n_kv = n_kv; aa.K = budget;
-  attn_split(n_layers, B, n_kv, budget, &aa.n_split, &aa.cps, &aa.n_chunks);
-  aa.n_items = (int)(nseg * aa.n_split);
+  attn_plan(n_layers, B, n_kv, budget, &aa.C, &aa.n_split, &aa.cpc, &aa.n_chunks);
   aa.scale2 = scale * kLog2e;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   switch (n_q / n_kv) {
-    case 1: e = launch_attn<1>(aa, st); break;
-    case 2: e = launch_attn<2>(aa, st); break;
-    case 4: e = launch_attn<4>(aa, st); break;
-    case 8: e = launch_attn<8>(aa, st); break;
-    case 16: e = launch_attn<16>(aa, st); break;
-    case 32: e = launch_attn<32>(aa, st); break;
-    default: e = launch_attn<64>(aa, st); break;
+    case 1: e = launch_attn<1>(aa, (int)nseg, st); break;
+    case 2: e = launch_attn<2>(aa, (int)nseg, st); break;
+    case 4: e = launch_attn<4>(aa, (int)nseg, st); break;
+    case 8: e = launch_attn<8>(aa, (int)nseg, st); break;
+    case 16: e = launch_attn<16>(aa, (int)nseg, st); break;
+    case 32: e = launch_attn<32>(aa, (int)nseg, st); break;
+    default: e = launch_attn<64>(aa, (int)nseg, st); break;
   }
   return e == cudaSuccess ? SPC_OK : SPC_ERR_CUDA;
 }

@@ -66,7 +66,8 @@ def _without_workspace(case, L, B, n_q, n_kv, K):
 
 
 @pytest.mark.parametrize("L,B,n_q,n_kv,K,cap,use_slots", [
-    (4, 1, 32, 8, 2048, 4096, 1),     # the benchmark's shape: split over the budget, merged in scratch
+    (1, 1, 32, 8, 2048, 4096, 1),     # one layer: several clusters per KV head merge through the scratch
+    (4, 1, 32, 8, 2048, 4096, 1),     # the benchmark's launch shape
     (2, 2, 64, 8, 1000, 3000, 0),     # positions into a full cache
 ])
 def test_noalloc_matches_the_workspace_entry_point_on_two_calls(L, B, n_q, n_kv, K, cap, use_slots):
