@@ -87,9 +87,9 @@ def test_noalloc_matches_the_workspace_entry_point_on_two_calls(L, B, n_q, n_kv,
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
-    # 4 layers x 2 KV heads x 64-head groups x budget 4096 needs ~17 MB of
-    # split partials, more than the fixed area: refused before any launch
-    L, B, n_q, n_kv, K = 4, 1, 128, 2, 4096
+    # 1023 layers x 64 requests x 64 KV heads need ~16 MB of merge counters,
+    # more than the fixed area: refused before any launch
+    L, B, n_q, n_kv, K = 1023, 64, 64, 64, 64
     assert spc.spc_sparse_decode_attn_workspace_size(L, B, n_q, n_kv, 128, K) > \
         spc.SPC_ATTN_NOALLOC_SCRATCH_BYTES
     fake = 0x10000
