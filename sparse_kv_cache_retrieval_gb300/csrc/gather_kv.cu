@@ -12,16 +12,20 @@
 // NVLink-C2C / PCIe link by ordinary 16-byte loads. A work item is one
 // 256-byte row (one layer, K or V, one KV head, one position) copied by a
 // half-warp; items are laid out (layer, K/V, flattened load index) and spread
-// over a grid-stride loop with 4 rows in flight per half-warp, so the link
-// sees thousands of independent 256-byte reads at once. The flattened load
-// index j maps back to (request, KV head, i) through a prefix sum of n_load
-// kept in shared memory.
+// over a grid-stride loop with 4 rows in flight per half-warp. The link
+// saturates with about 0.5 MB in flight, which a small grid (one CTA of 512
+// threads per 8 SMs) already keeps: the rest of the GPU stays free for the
+// kernels that run beside the gather on the other stream (attention, key
+// scan). The flattened load index j maps back to (request, KV head, i)
+// through a prefix sum of n_load kept in shared memory.
 #include "spc_device.cuh"
 #include "spc_internal.h"
 
+#include <algorithm>
+
 namespace spc {
 
-constexpr int kGatherThreads = 256;
+constexpr int kGatherThreads = 512;
 constexpr int kGatherUnroll = 4;
 constexpr int kGatherMaxSeg = 1024;
 
@@ -99,7 +103,7 @@ int gather_launch(const spc_gather_view* views, int layer_lo, int layer_hi, cons
   const long long max_items = (long long)(layer_hi - layer_lo) * 2 * B * n_kv * budget;
   const long long per_block = (kGatherThreads / 16) * kGatherUnroll;
   long long grid = (max_items + per_block - 1) / per_block;
-  const long long cap_grid = 8ll * device_sm_count();
+  const long long cap_grid = std::max(8, device_sm_count() / 8);
   if (grid > cap_grid) grid = cap_grid;
   if (grid < 1) grid = 1;
   gather_kernel<<<(int)grid, kGatherThreads, 0, static_cast<cudaStream_t>(stream)>>>(

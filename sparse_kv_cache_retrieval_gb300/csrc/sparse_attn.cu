@@ -17,10 +17,12 @@
 //    to 8 CTAs (and, when a launch has too few of them to fill the GPU, by a
 //    few such clusters); each CTA (4 consumer warps + 1 producer warp) streams
 //    a contiguous range of 64-row chunks;
-//  * the producer copies each kept K and V row (256 bytes) with cp.async.bulk
-//    into a 2-stage shared-memory ring whose rows are padded to 272 bytes (so
-//    ldmatrix reads them without bank conflicts), counting bytes on an
-//    mbarrier, and publishes the chunk's 64-bit valid-row mask;
+//  * the producer warp prefetches the CTA's row indices once, then copies each
+//    chunk's K and V rows into a 3-stage shared-memory ring with 16-byte
+//    cp.async (rows not kept are zero-filled), the 16-byte pieces of row r
+//    placed at piece index ^ (r & 7) so that ldmatrix reads are free of bank
+//    conflicts; cp.async completion arrives on the stage's mbarrier, and the
+//    chunk's 64-bit valid-row mask is published with it;
 //  * each consumer warp owns one 16-head tile of the group (zero-padded when
 //    G < 16) and a slice of the chunk's rows: S = Q K^T from ldmatrix'ed K
 //    fragments, masked online softmax in base 2 held per warp, then O += P V
@@ -41,12 +43,13 @@
 namespace spc {
 
 constexpr int kAttnRows = 64;                       // rows per chunk
-constexpr int kAttnPitch = 272;                     // smem bytes per row (256 + 16)
+constexpr int kAttnPitch = 256;                     // smem bytes per row (16-byte chunks XOR-swizzled)
 constexpr int kAttnCWarps = 4;
 constexpr int kAttnCThreads = kAttnCWarps * 32;
 constexpr int kAttnThreads = kAttnCThreads + 32;    // + producer warp
-constexpr int kAttnStages = 2;
-constexpr int kAttnTile = kAttnRows * kAttnPitch;   // 17408 bytes (K or V)
+constexpr int kAttnStages = 3;
+constexpr int kAttnMaxCpc = 16;                     // chunks per CTA (row indices prefetched)
+constexpr int kAttnTile = kAttnRows * kAttnPitch;   // 16 KiB (K or V)
 constexpr int kAttnMaxCluster = 8;
 constexpr int kAttnTargetCtas = 228;                // ~1.5 CTAs per SM of a 152-SM GB300
 constexpr long long kAttnWait = 4000000000ll;
@@ -137,7 +140,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
 
   if (tid == 0) {
     for (int s = 0; s < kAttnStages; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], 32 + 1);   // 32 cp.async arrivals + the mask publisher
       mbar_init(&empty[s], kAttnCWarps);
     }
     fence_mbar_init();
@@ -145,12 +148,22 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
   __syncthreads();
 
   if (warp == kAttnCWarps) {
-    // ================= producer warp: per-row bulk copies into padded rows
+    // ================= producer warp: 16-byte cp.async into swizzled rows
     const spc_kv_view vw = a.views[lb];
     const int32_t* idx = (vw.use_slots ? a.slot_pos : a.selected) + ((size_t)b * a.n_kv + g) * a.K;
     const uint16_t* kb = static_cast<const uint16_t*>(vw.k) + (size_t)g * vw.rows * kD;
     const uint16_t* vb = static_cast<const uint16_t*>(vw.v) + (size_t)g * vw.rows * kD;
+    // row indices of every chunk of this CTA, two rows per lane per chunk
+    int srow[kAttnMaxCpc][2];
+#pragma unroll
+    for (int k = 0; k < kAttnMaxCpc; ++k)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int i = (c0 + k) * kAttnRows + lane + 32 * h;
+        srow[k][h] = (c0 + k < c1 && i < a.K) ? idx[i] : -1;
+      }
     int it = 0;
+#pragma unroll 1
     for (int c = c0; c < c1; ++c, ++it) {
       const int s = it % kAttnStages;
       const uint32_t ph = (it / kAttnStages) & 1;
@@ -158,57 +171,48 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
         if (lane == 0) set_status(a.status, SPC_ERR_TIMEOUT);
         break;
       }
-      long long src[2];
       bool val[2];
+      long long row[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const int r = lane + 32 * h, i = c * kAttnRows + r;
-        long long row = -1;
-        if (i < a.K) {
-          const int v = idx[i];
-          if (v >= 0) row = vw.use_slots ? i : v;
-          if (row >= vw.rows) row = -1;
-        }
-        val[h] = row >= 0;
-        src[h] = row;
+        int v = -1;
+#pragma unroll
+        for (int k = 0; k < kAttnMaxCpc; ++k)
+          if (k == it) v = srow[k][h];
+        const int i = c * kAttnRows + lane + 32 * h;
+        long long r = -1;
+        if (v >= 0) r = vw.use_slots ? i : v;
+        if (r >= vw.rows) r = -1;
+        val[h] = r >= 0;
+        row[h] = r < 0 ? 0 : r;
       }
       const uint32_t lo = __ballot_sync(0xffffffffu, val[0]);
       const uint32_t hi = __ballot_sync(0xffffffffu, val[1]);
-      const int nval = __popc(lo) + __popc(hi);
       uint8_t* kdst = asmem + (size_t)s * 2 * kAttnTile;
       uint8_t* vdst = kdst + kAttnTile;
-      // rows not copied: V is zeroed so that P = 0 times it stays 0 (the
-      // tensor cores multiply every row; K of such rows only feeds scores
-      // that are replaced by -inf)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        if (!val[h]) {
-          uint4* vr = reinterpret_cast<uint4*>(vdst + (lane + 32 * h) * kAttnPitch);
+        const int r = lane + 32 * h;
+        const int nb = val[h] ? 16 : 0;   // 0: zero-fill the row
+        const uint16_t* ks = kb + (size_t)row[h] * kD;
+        const uint16_t* vs = vb + (size_t)row[h] * kD;
 #pragma unroll
-          for (int q = 0; q < 16; ++q) vr[q] = make_uint4(0u, 0u, 0u, 0u);
+        for (int j = 0; j < 16; ++j) {
+          const int off = r * kAttnPitch + ((j ^ (r & 7)) << 4);
+          cp_async16(kdst + off, ks + j * 8, nb);
+          cp_async16(vdst + off, vs + j * 8, nb);
         }
       }
-      // order these writes before the stage's next bulk copies
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      __syncwarp();
       if (lane == 0) {
         okmask[s] = ((uint64_t)hi << 32) | lo;
-        mbar_arrive_expect_tx(&full[s], 2u * nval * kRowBytes);
+        mbar_arrive(&full[s]);
       }
-      __syncwarp();
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        if (val[h]) {
-          const int r = lane + 32 * h;
-          bulk_g2s(kdst + r * kAttnPitch, kb + (size_t)src[h] * kD, kRowBytes, &full[s]);
-          bulk_g2s(vdst + r * kAttnPitch, vb + (size_t)src[h] * kD, kRowBytes, &full[s]);
-        }
-      }
-      __syncwarp();
+      // arrives on full[s] once this lane's copies have landed
+      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(smem_u32(&full[s])) : "memory");
     }
-    if (lane == 0)
-      for (int k = max(0, it - kAttnStages); k < it; ++k)
-        mbar_wait_bounded(&full[k % kAttnStages], (k / kAttnStages) & 1, kAttnWait);
+    // wait (bounded) for the copies still in flight before leaving
+    for (int k = max(0, it - kAttnStages); k < it; ++k)
+      mbar_wait_bounded(&full[k % kAttnStages], (k / kAttnStages) & 1, kAttnWait);
     __syncwarp();
   } else {
     // ================= consumers
@@ -257,7 +261,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
 #pragma unroll
         for (int np = 0; np < S::NT / 2; ++np) {
           const int row = row0 + np * 16 + ((lm >> 1) << 3) + lr;
-          const uint32_t addr = kbase + row * kAttnPitch + (ks * 16 + (lm & 1) * 8) * 2;
+          const uint32_t addr = kbase + row * kAttnPitch + (((ks * 2 + (lm & 1)) ^ (row & 7)) << 4);
           uint32_t b0, b1, b2, b3;
           ldsm_x4(addr, b0, b1, b2, b3);
           mma_bf16(sacc[2 * np], qf[ks], b0, b1);
@@ -328,7 +332,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
         const int vrow = row0 + ks * 16 + ((lm & 1) << 3) + lr;
 #pragma unroll
         for (int dp = 0; dp < 8; ++dp) {
-          const uint32_t addr = vbase + vrow * kAttnPitch + (dp * 16 + (lm >> 1) * 8) * 2;
+          const uint32_t addr = vbase + vrow * kAttnPitch + (((dp * 2 + (lm >> 1)) ^ (vrow & 7)) << 4);
           uint32_t b0, b1, b2, b3;
           ldsm_x4_t(addr, b0, b1, b2, b3);
           mma_bf16(o[2 * dp], ah, b0, b1);
@@ -481,6 +485,8 @@ static void attn_plan(int n_layers, int B, int n_kv, int budget, int* C, int* n_
   const int smax = (nc + c - 1) / c;
   if (s < 1) s = 1;
   if (s > smax) s = smax;
+  // at most kAttnMaxCpc chunks per CTA (their row indices are prefetched)
+  while ((nc + s * c - 1) / (s * c) > kAttnMaxCpc) ++s;
   *C = c;
   *n_split = (int)s;
   *cpc = (nc + (int)s * c - 1) / ((int)s * c);
