@@ -22,12 +22,13 @@
 //    lane-rotated row order so that a half-warp reduce-scatter needs no
 //    selects; base-2 logits go to scratch and per-warp (max, sum 2^(l-max))
 //    partials give the logsumexp.
-//  * lse_kernel / score_kernel / topk_kernel: logsumexp per head, the group
-//    score and its order key for every position on the whole GPU with a
-//    per-(request, KV head) histogram of the key's bits 30..20, then one CTA
-//    per (request, KV head) that finds the threshold key (histogram bin, then
-//    two refinement passes over the bin's candidates) and writes the selection
-//    with an ordered compaction (ascending, ties to the lower position).
+//  * select_kernel: one thread-block cluster per (request, KV head) folds the
+//    logsumexp of each head, forms the group score and its order key for
+//    every position, finds the threshold key with a three-level radix select
+//    whose histograms are summed through distributed shared memory, and
+//    writes the selection with an ordered compaction (ascending, ties to the
+//    lower position).
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -184,7 +185,7 @@ struct ScanArgs {
   float* logits;
   float2* part;
   int* status;
-  int n_q, n_kv, cap, n_tiles, total_tiles, append, n_parts;
+  int n_q, n_kv, cap, lstride, n_tiles, total_tiles, append, n_parts;
   float qscale;
 };
 
@@ -323,7 +324,7 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
 #pragma unroll
         for (int h = 0; h < S::HB; ++h) {
           const int hq = g * G + hb * S::HB + h;
-          if (own) a.logits[((size_t)b * a.n_q + hq) * a.cap + row0 + rloc] = acc[0][h];
+          if (own) a.logits[((size_t)b * a.n_q + hq) * a.lstride + row0 + rloc] = acc[0][h];
           const float mm = warp_max(own ? acc[0][h] : -INFINITY);
           const float ss = warp_sum(own ? exp2f(acc[0][h] - mm) : 0.f);
           if (lane == h)
@@ -340,314 +341,255 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
 }
 
 // ============================================================== group score + Top-K
-// Three small kernels replace one long-latency one:
-//  * lse_kernel: one CTA per query head folds the scan's (max, sum) partials
-//    into log2-sum-exp;
-//  * score_kernel: every position of every (request, KV head) in parallel:
-//    s = max_h (l_h - lse_h), p = 2^s, the monotone uint32 order key of p, and
-//    a 2048-bin histogram of the key's bits 30..20 (block histogram in shared
-//    memory, flushed to a per-segment global histogram);
-//  * topk_kernel: one CTA per (request, KV head) finds the bin holding the
-//    (K-|F|)-th largest key, refines the remaining 21 bits over the bin's
-//    candidates (gathered in shared memory; global fallback for huge ties),
-//    then writes the selection with an ordered two-pass compaction (ties at
-//    the threshold key to the lower positions). It leaves the global
-//    histogram zeroed for the next call.
-constexpr int kHistBins = 2048;
-constexpr int kScoreThreads = 256;
-constexpr int kScorePos = 2048;        // positions per score block
-constexpr int kTopkThreads = 1024;
-constexpr int kCandMax = 8192;
+// One kernel, one thread-block cluster of C CTAs per (request, KV head); rank
+// r owns the contiguous positions [r*slice, (r+1)*slice):
+//  * logsumexp: rank r folds its share of the scan's (max, sum) partials of
+//    each head of the group; the C results meet through distributed shared
+//    memory;
+//  * group score s = max_h (l_h - lse_h), p = 2^s (written out on request)
+//    and the order key of p (its float bits + 1; 0 marks a forced or absent
+//    position), kept in shared memory (global spill for very long slices);
+//  * the (K - |F|)-th largest key by a three-level radix select over bits
+//    30..20, 19..10 and 9..0: each rank histograms its keys, rank r sums its
+//    share of the bins over the cluster, every rank then finds the bin that
+//    holds the threshold (a level whose bin is taken whole ends the search);
+//  * an ordered compaction: the cluster's prefix counts give each rank its
+//    output offset, keys equal to the threshold go to the lowest positions.
+constexpr int kSelThreads = 512;
+constexpr int kSelMaxCluster = 16;
+constexpr int kHistBins = 2048;       // level 1: key bits 30..20
+constexpr int kSubBins = 1024;        // levels 2 and 3: bits 19..10, 9..0
+constexpr int kSelSmemKeys = 8192;    // keys of a slice kept in shared memory up to this count
 
 struct SelArgs {
   const float* logits;
   const float2* part;
-  float* lse2;
-  uint32_t* keys;
-  uint32_t* ghist;
+  uint32_t* keys;        // global key spill, [segment][kstride]
   int32_t* len;
   float* scores_out;
   int32_t* selected;
   uint32_t* done;
-  int B, n_q, n_kv, G, cap, K, n_sink, n_recent, append, n_parts, ppt, kstride;
+  int B, n_q, n_kv, cap, lstride, K, n_sink, n_recent, append, n_parts, ppt, kstride, C, slice, cpt;
+};
+
+struct SelSmem {
+  uint32_t hist[kHistBins];           // this rank's histogram of the current level
+  uint32_t tot[kHistBins];            // this rank's share of the cluster-wide counts
+  uint32_t keys[kSelSmemKeys];
+  float pm[SPC_MAX_GROUP], ps[SPC_MAX_GROUP], lse[SPC_MAX_GROUP];
+  int scratch[33];
+  int cnt[2];                         // this rank's (above, equal) counts
+  int bin, rem, whole;
 };
 
 __device__ __forceinline__ bool is_forced(int p, int L, int n_sink, int n_recent) {
   return p < n_sink || p >= L - n_recent;
 }
 
-__global__ void __launch_bounds__(256) lse_kernel(SelArgs a) {
-  const int bh = blockIdx.x, b = bh / a.n_q;
-  const int L = effective_len(a.len, b, a.append, a.cap);
-  const int nv = ((L + kScanRows - 1) / kScanRows) * a.ppt;
-  const float2* ph = a.part + (size_t)bh * a.n_parts;
-  float m = -INFINITY, s = 0.f;
-  for (int i = threadIdx.x; i < nv; i += 256) {
-    const float2 v = __ldcg(ph + i);
-    lse2_combine(m, s, v.x, v.y);
+// Bin (scanning from the top) where the running count reaches `rem`, over
+// `nbins` counts in shared memory (nbins a multiple of the block size): writes
+// the bin, rem minus the count above it, and whether the bin is taken whole.
+__device__ __forceinline__ void find_bin(const uint32_t* cnt, int nbins, int rem, SelSmem& sm) {
+  const int per = nbins / kSelThreads;
+  const int d0 = threadIdx.x * per;   // descending rank of this thread's first bin
+  int local = 0;
+  for (int j = 0; j < per; ++j) local += (int)cnt[nbins - 1 - (d0 + j)];
+  int tot;
+  int before = block_excl_scan(local, sm.scratch, &tot);
+  for (int j = 0; j < per; ++j) {
+    const int bin = nbins - 1 - (d0 + j);
+    const int c = (int)cnt[bin];
+    if (before < rem && before + c >= rem) {
+      sm.bin = bin;
+      sm.rem = rem - before;
+      sm.whole = (before + c == rem);
+    }
+    before += c;
   }
-  warp_lse2(m, s);
-  __shared__ float sm[8], ss[8];
-  if ((threadIdx.x & 31) == 0) { sm[threadIdx.x >> 5] = m; ss[threadIdx.x >> 5] = s; }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    float M = -INFINITY, Sx = 0.f;
-    for (int w = 0; w < 8; ++w) lse2_combine(M, Sx, sm[w], ss[w]);
-    a.lse2[bh] = Sx > 0.f ? M + log2f(Sx) : INFINITY;
-  }
 }
 
 template <int G>
-__global__ void __launch_bounds__(kScoreThreads) score_kernel(SelArgs a) {
-  const int seg = blockIdx.y, b = seg / a.n_kv, g = seg - b * a.n_kv;
+__global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  extern __shared__ __align__(16) uint8_t sel_smem[];
+  SelSmem& sm = *reinterpret_cast<SelSmem*>(sel_smem);
+  const int C = a.C;
+  const int rank = (int)cluster.block_rank();
+  const int seg = blockIdx.x / C;
+  const int b = seg / a.n_kv, g = seg - b * a.n_kv;
   const int L = effective_len(a.len, b, a.append, a.cap);
-  const int p0 = blockIdx.x * kScorePos;
-  if (p0 >= L) return;
-  __shared__ uint32_t hist[kHistBins];
-  __shared__ float lse[G];
-  const int tid = threadIdx.x, lane = tid & 31;
-  for (int i = tid; i < kHistBins; i += kScoreThreads) hist[i] = 0u;
-  for (int h = tid; h < G; h += kScoreThreads) lse[h] = a.lse2[(size_t)b * a.n_q + (size_t)g * G + h];
-  __syncthreads();
-  const float* lg = a.logits + ((size_t)b * a.n_q + (size_t)g * G) * a.cap;
-  constexpr int PER = kScorePos / kScoreThreads;  // 8 positions per thread
-  constexpr int HC = G < 8 ? G : 8;               // heads per batch of loads in flight
-  float sc[PER];
-#pragma unroll
-  for (int k = 0; k < PER; ++k) sc[k] = -INFINITY;
-  for (int h0 = 0; h0 < G; h0 += HC) {
-    float v[HC][PER];
-#pragma unroll
-    for (int h = 0; h < HC; ++h)
-#pragma unroll
-      for (int k = 0; k < PER; ++k) {
-        const int p = p0 + k * kScoreThreads + tid;
-        v[h][k] = p < L ? __ldcg(lg + (size_t)(h0 + h) * a.cap + p) : -INFINITY;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int NW = kSelThreads / 32;
+  const bool topk = L > a.K;
+  const int Kp = a.K - (a.n_sink + a.n_recent);
+
+  // ---- logsumexp of each head: this rank's share of the partials
+  {
+    const int nv = ((L + kScanRows - 1) / kScanRows) * a.ppt;
+    const int v0 = (int)((long long)nv * rank / C), v1 = (int)((long long)nv * (rank + 1) / C);
+    for (int h = warp; h < G; h += NW) {
+      const float2* ph = a.part + ((size_t)b * a.n_q + (size_t)g * G + h) * a.n_parts;
+      float m = -INFINITY, s = 0.f;
+      for (int i = v0 + lane; i < v1; i += 32) {
+        const float2 v = __ldcg(ph + i);
+        lse2_combine(m, s, v.x, v.y);
       }
-#pragma unroll
-    for (int h = 0; h < HC; ++h)
-#pragma unroll
-      for (int k = 0; k < PER; ++k) sc[k] = fmaxf(sc[k], v[h][k] - lse[h0 + h]);
-  }
-  // order key of the group score p = 2^s in [0, 1]: its float bits + 1 (0 is
-  // reserved for forced / absent positions). Probabilities spread over many
-  // exponents, so the key's bits 30..20 make a fine first histogram.
-  uint32_t key[PER];
-#pragma unroll
-  for (int k = 0; k < PER; ++k) {
-    const int pos = p0 + k * kScoreThreads + tid;
-    key[k] = 0u;
-    if (pos < L) {
-      const float pr = exp2f(sc[k]);
-      if (a.scores_out) a.scores_out[(size_t)seg * a.cap + pos] = pr;
-      if (!is_forced(pos, L, a.n_sink, a.n_recent)) key[k] = __float_as_uint(pr) + 1u;
-      a.keys[(size_t)seg * a.kstride + pos] = key[k];
+      warp_lse2(m, s);
+      if (lane == 0) { sm.pm[h] = m; sm.ps[h] = s; }
     }
   }
-  if (L > a.K) {
+  for (int i = tid; i < kHistBins; i += kSelThreads) sm.hist[i] = 0u;
+  cluster.sync();
+  for (int h = tid; h < G; h += kSelThreads) {
+    float rm[kSelMaxCluster], rs[kSelMaxCluster];
 #pragma unroll
-    for (int k = 0; k < PER; ++k) {
-      const int bin = key[k] ? int(key[k] >> 20) : kHistBins;
-      const unsigned peers = __match_any_sync(0xffffffffu, bin);
-      if (bin < kHistBins && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
-    }
-    __syncthreads();
-    uint32_t* gh = a.ghist + (size_t)seg * kHistBins;
-    for (int i = tid; i < kHistBins; i += kScoreThreads)
-      if (hist[i]) atomicAdd(&gh[i], hist[i]);
+    for (int r = 0; r < kSelMaxCluster; ++r)
+      if (r < C) { rm[r] = *cluster.map_shared_rank(&sm.pm[h], r); rs[r] = *cluster.map_shared_rank(&sm.ps[h], r); }
+    float m = -INFINITY, s = 0.f;
+#pragma unroll
+    for (int r = 0; r < kSelMaxCluster; ++r)
+      if (r < C) lse2_combine(m, s, rm[r], rs[r]);
+    sm.lse[h] = s > 0.f ? m + log2f(s) : INFINITY;
   }
-}
-
-// Bin (scanning from the top) where the running count reaches `rem`, over
-// `nbins` counts held in shared memory; returns (bin, rem - count above it).
-// Every thread of the block calls it. nbins <= 2 * blockDim.x.
-__device__ __forceinline__ void find_bin(const uint32_t* cnt, int nbins, int rem, int* scratch,
-                                         int* s_bin, int* s_rem) {
-  const int t = threadIdx.x;
-  const int bA = nbins - 1 - 2 * t, bB = nbins - 2 - 2 * t;  // descending pair
-  const int cA = bA >= 0 ? (int)cnt[bA] : 0, cB = bB >= 0 ? (int)cnt[bB] : 0;
-  int tot;
-  const int before = block_excl_scan(cA + cB, scratch, &tot);
-  if (bA >= 0 && before < rem && before + cA >= rem) { *s_bin = bA; *s_rem = rem - before; }
-  if (bB >= 0 && before + cA < rem && before + cA + cB >= rem) { *s_bin = bB; *s_rem = rem - before - cA; }
   __syncthreads();
-}
 
-// Keys of positions [4*i4, 4*i4 + 4) with positions >= L zeroed.
-__device__ __forceinline__ void keys4(const uint4* k4, int i4, int L, uint32_t k[4]) {
-  const uint4 v = k4[i4];
-  const int p = 4 * i4;
-  k[0] = p + 0 < L ? v.x : 0u;
-  k[1] = p + 1 < L ? v.y : 0u;
-  k[2] = p + 2 < L ? v.z : 0u;
-  k[3] = p + 3 < L ? v.w : 0u;
-}
+  // ---- group score, its key, and the level-1 histogram of this rank's slice
+  const int p_lo = rank * a.slice;
+  const int p_end = min(L, p_lo + a.slice);
+  const int t0 = p_lo + tid * a.cpt;
+  const int t1 = min(p_end, t0 + a.cpt);
+  uint32_t* kb = a.slice <= kSelSmemKeys ? sm.keys : a.keys + (size_t)seg * a.kstride + p_lo;
+  const float* lg = a.logits + ((size_t)b * a.n_q + (size_t)g * G) * a.lstride;
+  constexpr int HC = G < 8 ? G : 8;   // heads whose loads are in flight together
+  for (int p = t0; p < t1; p += 4) {
+    float sc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    for (int h0 = 0; h0 < G; h0 += HC) {
+      float4 v[HC];
+#pragma unroll
+      for (int h = 0; h < HC; ++h) v[h] = __ldcg(reinterpret_cast<const float4*>(lg + (size_t)(h0 + h) * a.lstride + p));
+#pragma unroll
+      for (int h = 0; h < HC; ++h) {
+        const float l = sm.lse[h0 + h];
+        sc[0] = fmaxf(sc[0], v[h].x - l);
+        sc[1] = fmaxf(sc[1], v[h].y - l);
+        sc[2] = fmaxf(sc[2], v[h].z - l);
+        sc[3] = fmaxf(sc[3], v[h].w - l);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int pos = p + j;
+      if (pos >= t1) break;
+      const float pr = exp2f(sc[j]);
+      if (a.scores_out) a.scores_out[(size_t)seg * a.cap + pos] = pr;
+      const uint32_t key = is_forced(pos, L, a.n_sink, a.n_recent) ? 0u : __float_as_uint(pr) + 1u;
+      kb[pos - p_lo] = key;
+      if (topk && key) atomicAdd(&sm.hist[key >> 20], 1u);
+    }
+  }
 
-__global__ void __launch_bounds__(kTopkThreads) topk_kernel(SelArgs a) {
-  const int seg = blockIdx.x, b = seg / a.n_kv;
-  const int L = effective_len(a.len, b, a.append, a.cap);
-  const int tid = threadIdx.x, lane = tid & 31;
   int32_t* out = a.selected + (size_t)seg * a.K;
-  const uint4* k4 = reinterpret_cast<const uint4*>(a.keys + (size_t)seg * a.kstride);
-  uint32_t* gh = a.ghist + (size_t)seg * kHistBins;
-  __shared__ uint32_t hist[kHistBins];
-  __shared__ uint32_t cand[kCandMax];
-  __shared__ int scratch[33];
-  __shared__ int s_bin, s_rem, s_cnt, s_last;
-  const int n4 = (L + 3) / 4;
-
-  if (L <= a.K) {
-    for (int p = tid; p < a.K; p += kTopkThreads) out[p] = p < L ? p : -1;
+  if (!topk) {
+    // select all: positions 0..L-1, then -1
+    const int i0 = (int)((long long)a.K * rank / C), i1 = (int)((long long)a.K * (rank + 1) / C);
+    for (int i = i0 + tid; i < i1; i += kSelThreads) out[i] = i < L ? i : -1;
   } else {
-    const int Kp = a.K - (a.n_sink + a.n_recent);
+    // ---- threshold key T: the Kp-th largest non-forced key; `need` keys equal
+    // to T are taken (T = all-ones and need = 0 when nothing but F is taken)
     uint32_t T = 0xffffffffu;
     int need = 0;
-    // global histogram of the top 11 bits -> shared memory; leave it zeroed
-    for (int i = tid; i < kHistBins; i += kTopkThreads) { hist[i] = gh[i]; gh[i] = 0u; }
-    if (tid == 0) s_cnt = 0;
-    __syncthreads();
     if (Kp > 0) {
-      find_bin(hist, kHistBins, Kp, scratch, &s_bin, &s_rem);
-      const uint32_t b1 = (uint32_t)s_bin;
-      int rem = s_rem;
-      const bool local = (int)hist[b1] <= kCandMax;
-      if (local) {
-        for (int i0 = tid; i0 < n4; i0 += 4 * kTopkThreads) {
-          uint32_t kk[4][4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int i4 = i0 + u * kTopkThreads;
-            if (i4 < n4) keys4(k4, i4, L, kk[u]);
-            else kk[u][0] = kk[u][1] = kk[u][2] = kk[u][3] = 0u;
-          }
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              if (kk[u][j] && (kk[u][j] >> 20) == b1) {
-                const int c = atomicAdd(&s_cnt, 1);
-                if (c < kCandMax) cand[c] = kk[u][j];
-              }
-        }
-      }
-      __syncthreads();
-      // two refinement passes: bits 19..10, then 9..0
-      uint32_t prefix = b1 << 20, mask = 0xfff00000u;
-      for (int pass = 0; pass < 2; ++pass) {
-        const int shift = pass == 0 ? 10 : 0;
-        const int nb = 1024;
-        const uint32_t dmask = (uint32_t)nb - 1u;
-        for (int i = tid; i < kHistBins; i += kTopkThreads) hist[i] = 0u;
-        __syncthreads();
-        if (local) {
-          const int n = min(s_cnt, kCandMax);
-          for (int base = 0; base < n; base += kTopkThreads) {
-            const int i = base + tid;
-            const uint32_t k = i < n ? cand[i] : 0u;
-            const int d = (k && (k & mask) == prefix) ? int((k >> shift) & dmask) : nb;
-            const unsigned peers = __match_any_sync(0xffffffffu, d);
-            if (d < nb && lane == __ffs(peers) - 1) atomicAdd(&hist[d], (uint32_t)__popc(peers));
-          }
-        } else {
-          for (int base = 0; base < n4; base += kTopkThreads) {
-            const int i4 = base + tid;
-            uint32_t kk[4] = {0u, 0u, 0u, 0u};
-            if (i4 < n4) keys4(k4, i4, L, kk);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const uint32_t k = kk[j];
-              const int d = (k && (k & mask) == prefix) ? int((k >> shift) & dmask) : nb;
-              const unsigned peers = __match_any_sync(0xffffffffu, d);
-              if (d < nb && lane == __ffs(peers) - 1) atomicAdd(&hist[d], (uint32_t)__popc(peers));
-            }
+      uint32_t prefix = 0u, pmask = 0u;
+      int rem = Kp;
+      for (int lvl = 0; lvl < 3; ++lvl) {
+        const int shift = lvl == 0 ? 20 : (lvl == 1 ? 10 : 0);
+        const int nb = lvl == 0 ? kHistBins : kSubBins;
+        if (lvl > 0) {
+          for (int i = tid; i < nb; i += kSelThreads) sm.hist[i] = 0u;
+          __syncthreads();
+          for (int p = t0; p < t1; ++p) {
+            const uint32_t k = kb[p - p_lo];
+            if (k && (k & pmask) == prefix) atomicAdd(&sm.hist[(k >> shift) & (uint32_t)(nb - 1)], 1u);
           }
         }
+        cluster.sync();
+        const int share = nb / C;
+        for (int i = tid; i < share; i += kSelThreads) {
+          const int bin = rank * share + i;
+          uint32_t sum = 0u;
+#pragma unroll 4
+          for (int r = 0; r < C; ++r) sum += *cluster.map_shared_rank(&sm.hist[bin], r);
+          sm.tot[bin] = sum;
+        }
+        cluster.sync();
+        for (int i = tid; i < nb; i += kSelThreads) sm.hist[i] = *cluster.map_shared_rank(&sm.tot[i], i / share);
         __syncthreads();
-        find_bin(hist, nb, rem, scratch, &s_bin, &s_rem);
-        prefix |= (uint32_t)s_bin << shift;
-        mask |= dmask << shift;
-        rem = s_rem;
+        find_bin(sm.hist, nb, rem, sm);
+        const uint32_t lower = prefix | ((uint32_t)sm.bin << shift);
+        if (sm.whole || lvl == 2) {
+          if (sm.whole) { T = lower ? lower - 1u : 0u; need = 0; }
+          else { T = lower; need = sm.rem; }
+          break;
+        }
+        prefix = lower;
+        pmask |= (uint32_t)(nb - 1) << shift;
+        rem = sm.rem;
         __syncthreads();
       }
-      T = prefix;
-      need = rem;
     }
-    // ordered compaction: thread t owns the contiguous quads [q0, q1)
-    const int qpt = (n4 + kTopkThreads - 1) / kTopkThreads;
-    const int q0 = min(n4, tid * qpt), q1 = min(n4, q0 + qpt);
+    // ---- ordered compaction over the cluster
     int nb_ = 0, ne_ = 0;
-    for (int qb = q0; qb < q1; qb += 8) {
-      uint32_t kk[8][4];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        if (qb + u < q1) keys4(k4, qb + u, L, kk[u]);
-        else kk[u][0] = kk[u][1] = kk[u][2] = kk[u][3] = 0u;
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int p = 4 * (qb + u) + j;
-          if (qb + u >= q1 || p >= L) continue;
-          const uint32_t k = kk[u][j];
-          if (is_forced(p, L, a.n_sink, a.n_recent) || (k && k > T)) ++nb_;
-          else if (Kp > 0 && k && k == T) ++ne_;
-        }
+    for (int p = t0; p < t1; ++p) {
+      const uint32_t k = kb[p - p_lo];
+      if (is_forced(p, L, a.n_sink, a.n_recent) || (k && k > T)) ++nb_;
+      else if (need > 0 && k && k == T) ++ne_;
     }
     int tb, te;
-    const int base_b = block_excl_scan(nb_, scratch, &tb);
-    const int base_e = block_excl_scan(ne_, scratch, &te);
+    int base_b = block_excl_scan(nb_, sm.scratch, &tb);
+    int base_e = block_excl_scan(ne_, sm.scratch, &te);
+    if (tid == 0) { sm.cnt[0] = tb; sm.cnt[1] = te; }
+    cluster.sync();
+    for (int r = 0; r < rank; ++r) {
+      base_b += *cluster.map_shared_rank(&sm.cnt[0], r);
+      base_e += *cluster.map_shared_rank(&sm.cnt[1], r);
+    }
     int o = base_b + min(base_e, need);
     int eq_seen = base_e;
-    for (int qb = q0; qb < q1; qb += 8) {
-      uint32_t kk[8][4];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        if (qb + u < q1) keys4(k4, qb + u, L, kk[u]);
-        else kk[u][0] = kk[u][1] = kk[u][2] = kk[u][3] = 0u;
+    for (int p = t0; p < t1; ++p) {
+      const uint32_t k = kb[p - p_lo];
+      bool sel = is_forced(p, L, a.n_sink, a.n_recent) || (k && k > T);
+      if (!sel && need > 0 && k && k == T) {
+        sel = eq_seen < need;
+        ++eq_seen;
       }
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int p = 4 * (qb + u) + j;
-          if (qb + u >= q1 || p >= L) continue;
-          const uint32_t k = kk[u][j];
-          bool sel = is_forced(p, L, a.n_sink, a.n_recent) || (k && k > T);
-          if (!sel && Kp > 0 && k && k == T) {
-            sel = eq_seen < need;
-            ++eq_seen;
-          }
-          if (sel) {
-            if (o < a.K) out[o] = p;
-            ++o;
-          }
-        }
+      if (sel) {
+        if (o < a.K) out[o] = p;
+        ++o;
+      }
     }
   }
+  // no rank leaves while a peer may still read its shared memory
+  cluster.sync();
 
-  if (a.append) {
-    __syncthreads();
-    if (tid == 0) {
+  if (a.append && rank == 0 && tid == 0) {
+    __threadfence();
+    if (atomicAdd(a.done, 1u) == gridDim.x / C - 1) {
       __threadfence();
-      s_last = (atomicAdd(a.done, 1u) == gridDim.x - 1);
-    }
-    __syncthreads();
-    if (s_last) {
-      __threadfence();
-      for (int bb = tid; bb < a.B; bb += kTopkThreads) {
+      for (int bb = 0; bb < a.B; ++bb) {
         const int L0 = a.len[bb];
         if (L0 >= 0 && L0 < a.cap) a.len[bb] = L0 + 1;
       }
-      if (tid == 0) *a.done = 0u;
+      *a.done = 0u;
     }
   }
 }
 
 // ============================================================== host side
 struct ScoreLayout {
-  size_t status, done, counters, q, part_proj, logits, part_scan, lse, keys, hist, total;
-  int S, Hc, n_col_tiles, bz, n_tiles, ppt, n_parts;
+  size_t status, done, counters, q, part_proj, logits, part_scan, keys, total;
+  int S, Hc, n_col_tiles, bz, n_tiles, ppt, n_parts, lstride;
 };
 
 static int proj_splits(int H) {
@@ -667,6 +609,7 @@ static ScoreLayout score_layout(int B, int H, int n_q, int n_kv, int cap) {
   l.n_tiles = (cap + kScanRows - 1) / kScanRows;
   l.ppt = scan_ppt(n_q / n_kv);
   l.n_parts = l.n_tiles * l.ppt;
+  l.lstride = (cap + 3) & ~3;
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off = (off + bytes + 255) & ~size_t(255); return o; };
   l.status = take(2 * sizeof(int));
@@ -674,11 +617,9 @@ static ScoreLayout score_layout(int B, int H, int n_q, int n_kv, int cap) {
   l.counters = take(sizeof(uint32_t) * (size_t)l.n_col_tiles * 4 /* grid.z <= 4 */);
   l.q = take(sizeof(float) * (size_t)B * Nq);
   l.part_proj = take(sizeof(float) * (size_t)l.S * B * Ntot);
-  l.logits = take(sizeof(float) * (size_t)B * n_q * cap);
+  l.logits = take(sizeof(float) * (size_t)B * n_q * l.lstride);
   l.part_scan = take(sizeof(float2) * (size_t)B * n_q * l.n_parts);
-  l.lse = take(sizeof(float) * (size_t)B * n_q);
   l.keys = take(sizeof(uint32_t) * (size_t)B * n_kv * ((cap + 3) & ~3));
-  l.hist = take(sizeof(uint32_t) * (size_t)B * n_kv * kHistBins);
   l.total = off;
   return l;
 }
@@ -710,6 +651,47 @@ static cudaError_t launch_proj(const ProjArgs& pa, dim3 grid, size_t smem, cudaS
   }
   proj_kernel<BB><<<grid, kProjThreads, smem, st>>>(pa);
   return cudaGetLastError();
+}
+
+// Cluster size: about one CTA per SM over all segments, at most 16, and at
+// least 512 positions per CTA; a size the device cannot co-schedule is halved.
+template <int G>
+static int launch_select(SelArgs& sa, int nseg, cudaStream_t st) {
+  const size_t smem = sizeof(SelSmem);
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(select_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+        cudaFuncSetAttribute(select_kernel<G>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+      return SPC_ERR_CUDA;
+    attr = true;
+  }
+  int C = 1;
+  while (C < kSelMaxCluster && nseg * C * 2 <= device_sm_count() && sa.cap / (C * 2) >= 512) C *= 2;
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute at[1];
+  cfg.blockDim = dim3(kSelThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  for (;; C /= 2) {
+    cfg.gridDim = dim3(nseg * C, 1, 1);
+    at[0].val.clusterDim.x = C;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    int n_clusters = 0;
+    if (C == 1 || (cudaOccupancyMaxActiveClusters(&n_clusters, select_kernel<G>, &cfg) == cudaSuccess &&
+                   n_clusters > 0))
+      break;
+    cudaGetLastError();
+  }
+  const int per_rank = (sa.cap + C - 1) / C;
+  sa.C = C;
+  sa.cpt = (((per_rank + kSelThreads - 1) / kSelThreads) + 3) & ~3;
+  sa.slice = (per_rank + 3) & ~3;
+  if (cudaLaunchKernelEx(&cfg, select_kernel<G>, sa) != cudaSuccess) return SPC_ERR_CUDA;
+  return SPC_OK;
 }
 
 int score_select_launch(const ScoreSelectCall& c) {
@@ -759,7 +741,7 @@ int score_select_launch(const ScoreSelectCall& c) {
     sa.logits = reinterpret_cast<float*>(ws + l.logits);
     sa.part = reinterpret_cast<float2*>(ws + l.part_scan);
     sa.status = status;
-    sa.n_q = c.n_q; sa.n_kv = c.n_kv; sa.cap = c.cap; sa.n_tiles = l.n_tiles;
+    sa.n_q = c.n_q; sa.n_kv = c.n_kv; sa.cap = c.cap; sa.lstride = l.lstride; sa.n_tiles = l.n_tiles;
     sa.total_tiles = c.B * c.n_kv * l.n_tiles; sa.append = c.append; sa.n_parts = l.n_parts;
     sa.qscale = kLog2e / sqrtf((float)kD);
     int grid = 2 * device_sm_count();
@@ -777,36 +759,30 @@ int score_select_launch(const ScoreSelectCall& c) {
     if (e != cudaSuccess) return SPC_ERR_CUDA;
   }
 
-  // ---- logsumexp, group score + histogram, Top-K
+  // ---- logsumexp, group score, Top-K (one cluster per request and KV head)
   if (c.stages & SPC_STAGE_SELECT) {
     SelArgs sa{};
     sa.logits = reinterpret_cast<const float*>(ws + l.logits);
     sa.part = reinterpret_cast<const float2*>(ws + l.part_scan);
-    sa.lse2 = reinterpret_cast<float*>(ws + l.lse);
     sa.keys = reinterpret_cast<uint32_t*>(ws + l.keys);
-    sa.ghist = reinterpret_cast<uint32_t*>(ws + l.hist);
     sa.len = c.len;
     sa.scores_out = c.scores_out;
     sa.selected = c.selected;
     sa.done = reinterpret_cast<uint32_t*>(ws + l.done);
-    sa.B = c.B; sa.n_q = c.n_q; sa.n_kv = c.n_kv; sa.G = G; sa.cap = c.cap; sa.K = c.budget;
+    sa.B = c.B; sa.n_q = c.n_q; sa.n_kv = c.n_kv; sa.cap = c.cap; sa.lstride = l.lstride; sa.K = c.budget;
     sa.n_sink = c.n_sink; sa.n_recent = c.n_recent; sa.append = c.append;
     sa.n_parts = l.n_parts; sa.ppt = l.ppt; sa.kstride = (c.cap + 3) & ~3;
-    lse_kernel<<<c.B * c.n_q, 256, 0, st>>>(sa);
-    if (cudaGetLastError() != cudaSuccess) return SPC_ERR_CUDA;
-    const dim3 sg((c.cap + kScorePos - 1) / kScorePos, c.B * c.n_kv);
+    int rc;
     switch (G) {
-      case 1: score_kernel<1><<<sg, kScoreThreads, 0, st>>>(sa); break;
-      case 2: score_kernel<2><<<sg, kScoreThreads, 0, st>>>(sa); break;
-      case 4: score_kernel<4><<<sg, kScoreThreads, 0, st>>>(sa); break;
-      case 8: score_kernel<8><<<sg, kScoreThreads, 0, st>>>(sa); break;
-      case 16: score_kernel<16><<<sg, kScoreThreads, 0, st>>>(sa); break;
-      case 32: score_kernel<32><<<sg, kScoreThreads, 0, st>>>(sa); break;
-      default: score_kernel<64><<<sg, kScoreThreads, 0, st>>>(sa); break;
+      case 1: rc = launch_select<1>(sa, c.B * c.n_kv, st); break;
+      case 2: rc = launch_select<2>(sa, c.B * c.n_kv, st); break;
+      case 4: rc = launch_select<4>(sa, c.B * c.n_kv, st); break;
+      case 8: rc = launch_select<8>(sa, c.B * c.n_kv, st); break;
+      case 16: rc = launch_select<16>(sa, c.B * c.n_kv, st); break;
+      case 32: rc = launch_select<32>(sa, c.B * c.n_kv, st); break;
+      default: rc = launch_select<64>(sa, c.B * c.n_kv, st); break;
     }
-    if (cudaGetLastError() != cudaSuccess) return SPC_ERR_CUDA;
-    topk_kernel<<<c.B * c.n_kv, kTopkThreads, 0, st>>>(sa);
-    if (cudaGetLastError() != cudaSuccess) return SPC_ERR_CUDA;
+    if (rc != SPC_OK) return rc;
   }
   return SPC_OK;
 }
