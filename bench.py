@@ -46,7 +46,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="cfg2")
-    ap.add_argument("--layers-per-launch", type=int, default=4)
+    ap.add_argument("--layers-per-launch", type=int, default=16)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-sample-steps", type=int, default=2)
@@ -404,7 +404,9 @@ def our_arm(args, rank, world, local):
                              "frac": round(a / hbm_peak, 3) if hbm_peak else None,
                              "algorithmic_bytes": scan_bytes, "mean_us": round(kern["key_scan"]["mean_us"], 2)}
     if "gather" in kern:
-        per_launch = gathered / max(1, n_gather_launches)
+        # gathered bytes are counted over the n_eager steps whose load counts
+        # were read back; launches over the K timed steps
+        per_launch = gathered / max(1, n_eager * n_gather_launches // max(1, K))
         a = gbs(per_launch, kern["gather"]["mean_us"])
         kinfo["gather"] = {"bound": "host_link", "achieved": round(a, 1), "peak": round(zc_peak, 1),
                            "unit": "GB/s", "frac": round(a / zc_peak, 3) if zc_peak else None,

@@ -149,19 +149,26 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
 
   if (warp == kAttnCWarps) {
     // ================= producer warp: 16-byte cp.async into swizzled rows
+    // row indices of every chunk of this CTA, two rows per lane per chunk,
+    // fetched from both index arrays together with the view (one round trip)
     const spc_kv_view vw = a.views[lb];
-    const int32_t* idx = (vw.use_slots ? a.slot_pos : a.selected) + ((size_t)b * a.n_kv + g) * a.K;
-    const uint16_t* kb = static_cast<const uint16_t*>(vw.k) + (size_t)g * vw.rows * kD;
-    const uint16_t* vb = static_cast<const uint16_t*>(vw.v) + (size_t)g * vw.rows * kD;
-    // row indices of every chunk of this CTA, two rows per lane per chunk
-    int srow[kAttnMaxCpc][2];
+    const size_t ioff = ((size_t)b * a.n_kv + g) * a.K;
+    int srow[kAttnMaxCpc][2], ssel[kAttnMaxCpc][2];
 #pragma unroll
     for (int k = 0; k < kAttnMaxCpc; ++k)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int i = (c0 + k) * kAttnRows + lane + 32 * h;
-        srow[k][h] = (c0 + k < c1 && i < a.K) ? idx[i] : -1;
+        const bool in = c0 + k < c1 && i < a.K;
+        srow[k][h] = in ? a.slot_pos[ioff + i] : -1;
+        ssel[k][h] = in ? a.selected[ioff + i] : -1;
       }
+    if (!vw.use_slots) {
+#pragma unroll
+      for (int k = 0; k < kAttnMaxCpc; ++k) { srow[k][0] = ssel[k][0]; srow[k][1] = ssel[k][1]; }
+    }
+    const uint16_t* kb = static_cast<const uint16_t*>(vw.k) + (size_t)g * vw.rows * kD;
+    const uint16_t* vb = static_cast<const uint16_t*>(vw.v) + (size_t)g * vw.rows * kD;
     int it = 0;
 #pragma unroll 1
     for (int c = c0; c < c1; ++c, ++it) {
@@ -172,7 +179,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
         break;
       }
       bool val[2];
-      long long row[2];
+      int row[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         int v = -1;
@@ -180,7 +187,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
         for (int k = 0; k < kAttnMaxCpc; ++k)
           if (k == it) v = srow[k][h];
         const int i = c * kAttnRows + lane + 32 * h;
-        long long r = -1;
+        int r = -1;
         if (v >= 0) r = vw.use_slots ? i : v;
         if (r >= vw.rows) r = -1;
         val[h] = r >= 0;
@@ -190,18 +197,19 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
       const uint32_t hi = __ballot_sync(0xffffffffu, val[1]);
       uint8_t* kdst = asmem + (size_t)s * 2 * kAttnTile;
       uint8_t* vdst = kdst + kAttnTile;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int r = lane + 32 * h;
-        const int nb = val[h] ? 16 : 0;   // 0: zero-fill the row
-        const uint16_t* ks = kb + (size_t)row[h] * kD;
-        const uint16_t* vs = vb + (size_t)row[h] * kD;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int off = r * kAttnPitch + ((j ^ (r & 7)) << 4);
-          cp_async16(kdst + off, ks + j * 8, nb);
-          cp_async16(vdst + off, vs + j * 8, nb);
-        }
+      // one instruction copies two whole rows: lanes 0-15 row 2j, lanes 16-31
+      // row 2j + 1, lane l its 16-byte piece l & 15 (coalesced 256-byte reads)
+      const int piece = lane & 15, half = lane >> 4;
+#pragma unroll 8
+      for (int j = 0; j < kAttnRows / 2; ++j) {
+        const int r = 2 * j + half;
+        const int src_lane = r & 31;
+        const int rr = __shfl_sync(0xffffffffu, j < 16 ? row[0] : row[1], src_lane);
+        const uint32_t okw = j < 16 ? lo : hi;
+        const int nb = ((okw >> src_lane) & 1u) ? 16 : 0;   // 0: zero-fill the row
+        const int off = r * kAttnPitch + ((piece ^ (r & 7)) << 4);
+        cp_async16(kdst + off, kb + (size_t)rr * kD + piece * 8, nb);
+        cp_async16(vdst + off, vb + (size_t)rr * kD + piece * 8, nb);
       }
       if (lane == 0) {
         okmask[s] = ((uint64_t)hi << 32) | lo;
@@ -398,14 +406,21 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
     // per head: max and weights of the cluster's CTAs (wsp is free here)
     float* wc = wsp;  // [C][G] then [G] sums
     for (int h = tid; h < G; h += kAttnCThreads) {
+      // every peer's (max, sum) in flight at once
+      float2 ml_r[kAttnMaxCluster];
+#pragma unroll
+      for (int r = 0; r < kAttnMaxCluster; ++r)
+        ml_r[r] = r < a.C ? *reinterpret_cast<const float2*>(cluster.map_shared_rank(cres + h * kPartStride, r))
+                          : make_float2(-INFINITY, 0.f);
       float Mx = -INFINITY;
-      for (int r = 0; r < a.C; ++r) Mx = fmaxf(Mx, *cluster.map_shared_rank(cres + h * kPartStride, r));
+#pragma unroll
+      for (int r = 0; r < kAttnMaxCluster; ++r) Mx = fmaxf(Mx, ml_r[r].x);
       float Ls = 0.f;
-      for (int r = 0; r < a.C; ++r) {
-        const float mr = *cluster.map_shared_rank(cres + h * kPartStride, r);
-        const float w = (Mx == -INFINITY || mr == -INFINITY) ? 0.f : exp2f(mr - Mx);
-        wc[r * G + h] = w;
-        Ls += *cluster.map_shared_rank(cres + h * kPartStride + 1, r) * w;
+#pragma unroll
+      for (int r = 0; r < kAttnMaxCluster; ++r) {
+        const float w = (Mx == -INFINITY || ml_r[r].x == -INFINITY) ? 0.f : exp2f(ml_r[r].x - Mx);
+        if (r < a.C) wc[r * G + h] = w;
+        Ls += ml_r[r].y * w;
       }
       wc[a.C * G + h] = Ls;
       if (res) { res[h * kPartStride] = Mx; res[h * kPartStride + 1] = Ls; }
@@ -413,12 +428,17 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
     cons_bar();
     for (int i4 = tid; i4 < G * (kD / 4); i4 += kAttnCThreads) {
       const int h = i4 / (kD / 4), c4 = i4 - h * (kD / 4);
+      float4 v[kAttnMaxCluster];
+#pragma unroll
+      for (int r = 0; r < kAttnMaxCluster; ++r)
+        if (r < a.C)
+          v[r] = *reinterpret_cast<const float4*>(cluster.map_shared_rank(cres + h * kPartStride + 4 + 4 * c4, r));
       float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int r = 0; r < a.C; ++r) {
+#pragma unroll
+      for (int r = 0; r < kAttnMaxCluster; ++r) {
+        if (r >= a.C) break;
         const float w = wc[r * G + h];
-        const float4 v = *reinterpret_cast<const float4*>(
-            cluster.map_shared_rank(cres + h * kPartStride + 4 + 4 * c4, r));
-        O.x = fmaf(w, v.x, O.x); O.y = fmaf(w, v.y, O.y); O.z = fmaf(w, v.z, O.z); O.w = fmaf(w, v.w, O.w);
+        O.x = fmaf(w, v[r].x, O.x); O.y = fmaf(w, v[r].y, O.y); O.z = fmaf(w, v[r].z, O.z); O.w = fmaf(w, v[r].w, O.w);
       }
       if (res) {
         reinterpret_cast<float4*>(res + h * kPartStride + 4)[c4] = O;

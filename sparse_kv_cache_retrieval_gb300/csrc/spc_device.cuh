@@ -69,7 +69,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 }
 // A waiting thread is suspended until the phase completes or this many
 // nanoseconds pass, so a wait costs no issue slots while it sleeps.
-constexpr uint32_t kTryWaitHintNs = 10000000u;
+#ifndef SPC_TRY_WAIT_HINT_NS
+#define SPC_TRY_WAIT_HINT_NS 10000000u
+#endif
+constexpr uint32_t kTryWaitHintNs = SPC_TRY_WAIT_HINT_NS;
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;

@@ -53,7 +53,7 @@ class DecodePipeline:
     """
 
     def __init__(self, cfg: Workload, inputs: Inputs, *, device: str = "cuda",
-                 n_layers: Optional[int] = None, layers_per_launch: int = 4,
+                 n_layers: Optional[int] = None, layers_per_launch: int = 16,
                  host_io: bool = False, timing: bool = False, fill_threads: Optional[int] = None):
         self.cfg = cfg
         self.inp = inputs
@@ -146,6 +146,9 @@ class DecodePipeline:
                                    dtype=torch.uint8, device=dev)
         self.sA = torch.cuda.Stream(device=dev)
         self.sB = torch.cuda.Stream(device=dev)
+        # gathers of consecutive layer chunks alternate over two streams so
+        # that one launch's ramp-down overlaps the next one's ramp-up
+        self.sBs = [self.sB, torch.cuda.Stream(device=dev)]
         self.e_attn = [torch.cuda.Event() for _ in self.chunks]
         self.e_gath = [torch.cuda.Event() for _ in self.chunks]
         self._gather_pending = [False] * len(self.chunks)
@@ -259,9 +262,10 @@ class DecodePipeline:
                 sA.wait_event(self.e_gath[c])
             self._timed_call("attention", sA, lambda: self._attn(q_layers, p, l0, l1, sA))
             self.e_attn[c].record(sA)
-            sB.wait_event(self.e_attn[c])
-            self._timed_call("gather", sB, lambda: self._gather(pn, l0, l1, sB))
-            self.e_gath[c].record(sB)
+            sg = self.sBs[c % 2]
+            sg.wait_event(self.e_attn[c])
+            self._timed_call("gather", sg, lambda: self._gather(pn, l0, l1, sg))
+            self.e_gath[c].record(sg)
             self._gather_pending[c] = True
         if self.host_io:
             with torch.cuda.stream(sA):
@@ -269,7 +273,8 @@ class DecodePipeline:
                 self.sel_host[t].copy_(self.selected[pn], non_blocking=True)
 
     def join(self) -> None:
-        self.sA.wait_stream(self.sB)
+        for sg in self.sBs:
+            self.sA.wait_stream(sg)
 
     def run(self, t0: int, n: int) -> None:
         for t in range(t0, t0 + n):
@@ -283,16 +288,17 @@ class DecodePipeline:
         With timing on, the graph records external timing events that the
         pipeline keeps alive; read them after a replay."""
         g = torch.cuda.CUDAGraph()
-        self.sA.wait_stream(self.sB)
+        self.join()
         saved = list(self._gather_pending)
         self._gather_pending = [False] * len(self.chunks)
         self._capturing = True
         try:
             with torch.cuda.graph(g, stream=self.sA):
-                self.sB.wait_stream(self.sA)
+                for sg in self.sBs:
+                    sg.wait_stream(self.sA)
                 for t in range(t0, t0 + n):
                     self.step(t)
-                self.sA.wait_stream(self.sB)
+                self.join()
         finally:
             self._capturing = False
         self._gather_pending = [False] * len(self.chunks)
