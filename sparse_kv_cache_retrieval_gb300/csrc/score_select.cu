@@ -16,12 +16,12 @@
 //    split partials; the appended key row is rounded to bf16 and written in
 //    place.
 //  * scan_kernel: persistent CTAs; one producer warp streams 32 KiB tiles of
-//    128 consecutive key rows into a 3-stage shared-memory ring with
-//    cp.async.bulk (TMA engine, mbarrier completion); 4 consumer warps form
-//    the dot products on CUDA cores (q in registers, fp32 accumulate) with a
-//    lane-rotated row order so that a half-warp reduce-scatter needs no
-//    selects; base-2 logits go to scratch and per-warp (max, sum 2^(l-max))
-//    partials give the logsumexp.
+//    128 consecutive key rows into a 3-stage shared-memory ring with coalesced
+//    16-byte cp.async (XOR-swizzled rows, mbarrier completion); 4 consumer
+//    warps form S = Q K^T on tensor cores (mma.sync m16n8k16 bf16, fp32
+//    accumulate, q split into bf16 high + low parts) from ldmatrix fragments;
+//    base-2 logits go to scratch and per-warp (max, sum 2^(l-max)) partials
+//    give the logsumexp.
 //  * select_kernel: one thread-block cluster per (request, KV head) folds the
 //    logsumexp of each head, forms the group score and its order key for
 //    every position, finds the threshold key with a three-level radix select
@@ -196,27 +196,28 @@ constexpr int kScanStages = 3;
 constexpr uint32_t kScanTileBytes = kScanRows * kRowBytes;
 constexpr long long kWaitLimit = 4000000000ll;  // clock cycles (~2 s)
 
+// Warp roles of the tensor-core scan: NMT tiles of 16 query heads; the
+// NRS = 4 / NMT warps of a head tile split a key tile's rows (RW each); one
+// logsumexp partial per head per warp per key tile.
 template <int G>
 struct ScanShape {
-  static constexpr int HB = G < 8 ? G : 8;         // heads per register block
-  static constexpr int R = HB <= 4 ? 16 : 8;       // rows per half-warp batch
-  static constexpr int NB = 16 / R;                // batches per half-warp per tile
-  static constexpr int NHB = G / HB;
-  static constexpr int PPT = kScanCWarps * NB;     // lse partials per tile
+  static constexpr int NMT = G <= 16 ? 1 : G / 16;
+  static constexpr int NRS = kScanCWarps / NMT;
+  static constexpr int RW = kScanRows / NRS;
+  static constexpr int PPT = NRS;
 };
 
 template <int G>
 __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
   using S = ScanShape<G>;
   extern __shared__ __align__(128) uint8_t scan_smem[];
-  uint4* tiles = reinterpret_cast<uint4*>(scan_smem);
   uint64_t* full = reinterpret_cast<uint64_t*>(scan_smem + kScanStages * kScanTileBytes);
   uint64_t* empty = full + kScanStages;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kScanStages; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], 32);       // one cp.async arrival per producer lane
       mbar_init(&empty[s], kScanCWarps);
     }
     fence_mbar_init();
@@ -224,8 +225,10 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
   __syncthreads();
 
   if (warp == kScanCWarps) {
-    // ---------------- producer: one lane issues the bulk copies
-    if (lane != 0) return;
+    // ---------------- producer: 16-byte cp.async, two whole rows per
+    // instruction (lanes 0-15 row 2j, lanes 16-31 row 2j+1), the 16-byte
+    // pieces of row r stored at piece ^ (r & 7); rows past the end zero-filled
+    const int piece = lane & 15, half = lane >> 4;
     int it = 0;
     for (int t = blockIdx.x; t < a.total_tiles; t += gridDim.x) {
       const int seg = t / a.n_tiles, tile = t - seg * a.n_tiles;
@@ -237,12 +240,18 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
       const int s = it % kScanStages;
       const uint32_t ph = (it / kScanStages) & 1;
       if (!mbar_wait_bounded(&empty[s], ph ^ 1, kWaitLimit)) {
-        set_status(a.status, SPC_ERR_TIMEOUT);
+        if (lane == 0) set_status(a.status, SPC_ERR_TIMEOUT);
         break;
       }
-      mbar_arrive_expect_tx(&full[s], nrows * kRowBytes);
-      bulk_g2s(tiles + (size_t)s * kScanRows * 16, a.K + ((size_t)seg * a.cap + row0) * kD,
-               nrows * kRowBytes, &full[s]);
+      uint8_t* dst = scan_smem + (size_t)s * kScanTileBytes;
+      const uint16_t* src = a.K + ((size_t)seg * a.cap + row0) * kD + piece * 8;
+#pragma unroll 8
+      for (int j = 0; j < kScanRows / 2; ++j) {
+        const int r = 2 * j + half;
+        const bool ok = r < nrows;
+        cp_async16(dst + r * kRowBytes + ((piece ^ (r & 7)) << 4), src + (size_t)(ok ? r : 0) * kD, ok ? 16 : 0);
+      }
+      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(smem_u32(&full[s])) : "memory");
       ++it;
     }
     // wait (bounded) until every copy issued has landed before leaving
@@ -251,10 +260,12 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
     return;
   }
 
-  // ---------------- consumers
-  const int hwi = warp * 2 + (lane >> 4);  // half-warp 0..7 -> rows [hwi*16, hwi*16+16)
-  const int l16 = lane & 15;
-  float qr[S::HB][8];
+  // ---------------- consumers: S = Q K^T on tensor cores (q split into bf16
+  // high + low parts, so the logits keep fp32 accuracy)
+  const int mt = warp % S::NMT, rs = warp / S::NMT;
+  const int gid = lane >> 2, tig = lane & 3, lm = lane >> 3, lr = lane & 7;
+  const int h_lo = mt * 16 + gid, h_hi = h_lo + 8;
+  uint32_t qh[8][4], ql[8][4];
   int cur_seg = -1;
   int it = 0;
   for (int t = blockIdx.x; t < a.total_tiles; t += gridDim.x) {
@@ -266,76 +277,105 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
     const int nrows = min(kScanRows, L - row0);
     const int s = it % kScanStages;
     const uint32_t ph = (it / kScanStages) & 1;
-    if (!mbar_wait_bounded(&full[s], ph, kWaitLimit)) {
-      set_status(a.status, SPC_ERR_TIMEOUT);
-      break;
-    }
-    const uint4* tb = tiles + (size_t)s * kScanRows * 16;
-    const float* qg = a.q + ((size_t)b * a.n_q + (size_t)g * G) * kD + l16 * 8;
-
-    for (int bt = 0; bt < S::NB; ++bt) {
-#pragma unroll 1
-      for (int hb = 0; hb < S::NHB; ++hb) {
-        if (S::NHB > 1 || seg != cur_seg) {
+    if (seg != cur_seg) {
+      const float* qg = a.q + ((size_t)b * a.n_q + (size_t)g * G) * kD;
 #pragma unroll
-          for (int h = 0; h < S::HB; ++h) {
-            const float4 q0 = __ldg(reinterpret_cast<const float4*>(qg + (size_t)(hb * S::HB + h) * kD));
-            const float4 q1 = __ldg(reinterpret_cast<const float4*>(qg + (size_t)(hb * S::HB + h) * kD + 4));
-            qr[h][0] = q0.x * a.qscale; qr[h][1] = q0.y * a.qscale;
-            qr[h][2] = q0.z * a.qscale; qr[h][3] = q0.w * a.qscale;
-            qr[h][4] = q1.x * a.qscale; qr[h][5] = q1.y * a.qscale;
-            qr[h][6] = q1.z * a.qscale; qr[h][7] = q1.w * a.qscale;
-          }
-        }
-        float acc[S::R][S::HB];
-        const int rbase = hwi * 16 + bt * S::R;
+      for (int ks = 0; ks < 8; ++ks) {
 #pragma unroll
-        for (int j = 0; j < S::R; ++j) {
-          // lane l16 reads chunk l16 of row (j ^ l16): conflict-free, and the
-          // reduce-scatter below then needs compile-time indices only
-          const uint4 w = tb[(rbase + (j ^ (l16 & (S::R - 1)))) * 16 + l16];
-          float v[8];
-          unpack8(w, v);
-#pragma unroll
-          for (int h = 0; h < S::HB; ++h) {
-            float d0 = v[0] * qr[h][0];
-#pragma unroll
-            for (int e = 1; e < 8; ++e) d0 = fmaf(v[e], qr[h][e], d0);
-            acc[j][h] = d0;
-          }
-        }
-        // reduce-scatter over rows: lane keeps row (j ^ l16) for j < m
-#pragma unroll
-        for (int m = S::R / 2; m >= 1; m >>= 1) {
-#pragma unroll
-          for (int j = 0; j < m; ++j)
-#pragma unroll
-            for (int h = 0; h < S::HB; ++h)
-              acc[j][h] += __shfl_xor_sync(0xffffffffu, acc[j + m][h], m);
-        }
-        // lanes l16 and l16 ^ R.. hold the same row: finish over the rest
-#pragma unroll
-        for (int m = S::R; m < 16; m <<= 1)
-#pragma unroll
-          for (int h = 0; h < S::HB; ++h) acc[0][h] += __shfl_xor_sync(0xffffffffu, acc[0][h], m);
-
-        const int rloc = rbase + (l16 & (S::R - 1));
-        const bool own = (l16 < S::R) && (rloc < nrows);
-#pragma unroll
-        for (int h = 0; h < S::HB; ++h) {
-          const int hq = g * G + hb * S::HB + h;
-          if (own) a.logits[((size_t)b * a.n_q + hq) * a.lstride + row0 + rloc] = acc[0][h];
-          const float mm = warp_max(own ? acc[0][h] : -INFINITY);
-          const float ss = warp_sum(own ? exp2f(acc[0][h] - mm) : 0.f);
-          if (lane == h)
-            a.part[((size_t)b * a.n_q + hq) * a.n_parts + (size_t)tile * S::PPT + warp * S::NB + bt] =
-                make_float2(mm, ss);
+        for (int e = 0; e < 4; ++e) {
+          const int h = (e & 1) ? h_hi : h_lo;
+          const int c = ks * 16 + tig * 2 + ((e & 2) ? 8 : 0);
+          float2 v = make_float2(0.f, 0.f);
+          if (h < G) v = *reinterpret_cast<const float2*>(qg + (size_t)h * kD + c);
+          const float x = v.x * a.qscale, y = v.y * a.qscale;
+          const float xh = bf16_round(x), yh = bf16_round(y);
+          qh[ks][e] = pack_bf16(xh, yh);
+          ql[ks][e] = pack_bf16(x - xh, y - yh);
         }
       }
+      cur_seg = seg;
     }
-    cur_seg = seg;
+    if (!mbar_wait_bounded(&full[s], ph, kWaitLimit)) {
+      if (lane == 0) set_status(a.status, SPC_ERR_TIMEOUT);
+      break;
+    }
+    const uint32_t base = smem_u32(scan_smem + (size_t)s * kScanTileBytes);
+    float* lg_lo = a.logits + ((size_t)b * a.n_q + (size_t)g * G + h_lo) * a.lstride + row0;
+    float* lg_hi = a.logits + ((size_t)b * a.n_q + (size_t)g * G + h_hi) * a.lstride + row0;
+    float m_lo = -INFINITY, s_lo = 0.f, m_hi = -INFINITY, s_hi = 0.f;
+#pragma unroll 1
+    for (int sb = 0; sb < S::RW / 32; ++sb) {
+      const int r0 = rs * S::RW + sb * 32;
+      float acc[4][4];
+#pragma unroll
+      for (int n = 0; n < 4; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+      float acl[4][4];   // the q-low products: a second chain halves the MMA dependency depth
+#pragma unroll
+      for (int n = 0; n < 4; ++n) acl[n][0] = acl[n][1] = acl[n][2] = acl[n][3] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+#pragma unroll
+        for (int np = 0; np < 2; ++np) {
+          const int row = r0 + np * 16 + ((lm >> 1) << 3) + lr;
+          const uint32_t addr = base + row * kRowBytes + (((ks * 2 + (lm & 1)) ^ (row & 7)) << 4);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(addr, b0, b1, b2, b3);
+          mma_bf16(acc[2 * np], qh[ks], b0, b1);
+          mma_bf16(acl[2 * np], ql[ks], b0, b1);
+          mma_bf16(acc[2 * np + 1], qh[ks], b2, b3);
+          mma_bf16(acl[2 * np + 1], ql[ks], b2, b3);
+        }
+      }
+#pragma unroll
+      for (int n = 0; n < 4; ++n) { acc[n][0] += acl[n][0]; acc[n][1] += acl[n][1]; acc[n][2] += acl[n][2]; acc[n][3] += acl[n][3]; }
+      // logits out; block max and sum of 2^(l - max) per head row
+      float bm_lo = -INFINITY, bm_hi = -INFINITY;
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        const int key = r0 + n * 8 + tig * 2;
+        const bool v0 = key < nrows, v1 = key + 1 < nrows;
+        if (!v0) acc[n][0] = acc[n][2] = -INFINITY;
+        if (!v1) acc[n][1] = acc[n][3] = -INFINITY;
+        if (h_lo < G) {
+          if (v1) *reinterpret_cast<float2*>(lg_lo + key) = make_float2(acc[n][0], acc[n][1]);
+          else if (v0) lg_lo[key] = acc[n][0];
+        }
+        if (h_hi < G) {
+          if (v1) *reinterpret_cast<float2*>(lg_hi + key) = make_float2(acc[n][2], acc[n][3]);
+          else if (v0) lg_hi[key] = acc[n][2];
+        }
+        bm_lo = fmaxf(bm_lo, fmaxf(acc[n][0], acc[n][1]));
+        bm_hi = fmaxf(bm_hi, fmaxf(acc[n][2], acc[n][3]));
+      }
+#pragma unroll
+      for (int o = 1; o <= 2; o <<= 1) {
+        bm_lo = fmaxf(bm_lo, __shfl_xor_sync(0xffffffffu, bm_lo, o));
+        bm_hi = fmaxf(bm_hi, __shfl_xor_sync(0xffffffffu, bm_hi, o));
+      }
+      float bs_lo = 0.f, bs_hi = 0.f;
+      if (bm_lo != -INFINITY) {
+#pragma unroll
+        for (int n = 0; n < 4; ++n) bs_lo += exp2f(acc[n][0] - bm_lo) + exp2f(acc[n][1] - bm_lo);
+      }
+      if (bm_hi != -INFINITY) {
+#pragma unroll
+        for (int n = 0; n < 4; ++n) bs_hi += exp2f(acc[n][2] - bm_hi) + exp2f(acc[n][3] - bm_hi);
+      }
+#pragma unroll
+      for (int o = 1; o <= 2; o <<= 1) {
+        bs_lo += __shfl_xor_sync(0xffffffffu, bs_lo, o);
+        bs_hi += __shfl_xor_sync(0xffffffffu, bs_hi, o);
+      }
+      lse2_combine(m_lo, s_lo, bm_lo, bs_lo);
+      lse2_combine(m_hi, s_hi, bm_hi, bs_hi);
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
+    if (tig == 0) {
+      const size_t pi = (size_t)tile * S::PPT + rs;
+      if (h_lo < G) a.part[((size_t)b * a.n_q + (size_t)g * G + h_lo) * a.n_parts + pi] = make_float2(m_lo, s_lo);
+      if (h_hi < G) a.part[((size_t)b * a.n_q + (size_t)g * G + h_hi) * a.n_parts + pi] = make_float2(m_hi, s_hi);
+    }
     ++it;
   }
 }
@@ -597,7 +637,7 @@ static int proj_splits(int H) {
   return S < 1 ? 1 : (S > 32 ? 32 : S);
 }
 
-static int scan_ppt(int G) { return kScanCWarps * ((G < 8 ? G : 8) <= 4 ? 1 : 2); }
+static int scan_ppt(int G) { return kScanCWarps / (G <= 16 ? 1 : G / 16); }
 
 static ScoreLayout score_layout(int B, int H, int n_q, int n_kv, int cap) {
   ScoreLayout l{};

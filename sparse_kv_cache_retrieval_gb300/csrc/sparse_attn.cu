@@ -51,7 +51,8 @@ constexpr int kAttnStages = 3;
 constexpr int kAttnMaxCpc = 16;                     // chunks per CTA (row indices prefetched)
 constexpr int kAttnTile = kAttnRows * kAttnPitch;   // 16 KiB (K or V)
 constexpr int kAttnMaxCluster = 8;
-constexpr int kAttnTargetCtas = 228;                // ~1.5 CTAs per SM of a 152-SM GB300
+constexpr int kAttnTargetCtas = 228;               // ~1.5 CTAs per SM of a 152-SM GB300
+constexpr int kAttnWaveCtas = 304;                 // two CTAs per SM on 152 SMs
 constexpr long long kAttnWait = 4000000000ll;
 constexpr int kPartStride = kD + 4;                 // (m, l, pad, pad, o[128])
 
@@ -92,27 +93,6 @@ struct AttnSmem {
 };
 
 __device__ __forceinline__ void cons_bar() { asm volatile("bar.sync 1, %0;" :: "n"(kAttnCThreads) : "memory"); }
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
-}
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-               "{%0,%1,%2,%3};"
-               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-               : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-// bf16x2 of (lo, hi): lo in the low half (the lower column index)
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
-__device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 
 template <int G>
 __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
@@ -498,9 +478,12 @@ static void attn_plan(int n_layers, int B, int n_kv, int budget, int* C, int* n_
                       int* n_chunks) {
   const int nc = (budget + kAttnRows - 1) / kAttnRows;
   const long long nseg = (long long)n_layers * B * n_kv;
-  const int c = nc < kAttnMaxCluster ? nc : kAttnMaxCluster;
-  // a fixed CTA target (not the device's SM count) keeps the workspace size a
-  // function of the shapes alone
+  // cluster size: the largest power of two (up to 8) that keeps the launch
+  // within one wave of two CTAs per SM, so each CTA streams many chunks and
+  // pays its prologue and merge once; a fixed CTA target (not the device's SM
+  // count) keeps the workspace size a function of the shapes alone
+  int c = 1;
+  while (c < kAttnMaxCluster && c < nc && nseg * c * 2 <= kAttnWaveCtas) c *= 2;
   long long s = (kAttnTargetCtas + nseg * c - 1) / (nseg * c);
   const int smax = (nc + c - 1) / c;
   if (s < 1) s = 1;
