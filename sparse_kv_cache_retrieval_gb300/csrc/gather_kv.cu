@@ -28,6 +28,10 @@ namespace spc {
 constexpr int kGatherThreads = 512;
 constexpr int kGatherUnroll = 4;
 constexpr int kGatherMaxSeg = 1024;
+#ifndef SPC_GATHER_SMS_PER_CTA
+#define SPC_GATHER_SMS_PER_CTA 8
+#endif
+constexpr int kGatherSmsPerCta = SPC_GATHER_SMS_PER_CTA;   // one gather CTA per this many SMs
 
 __global__ void __launch_bounds__(kGatherThreads)
 gather_kernel(const spc_gather_view* __restrict__ views, int layer_lo, int layer_hi,
@@ -58,13 +62,21 @@ gather_kernel(const spc_gather_view* __restrict__ views, int layer_lo, int layer
   const int hw0 = (blockIdx.x * kGatherThreads + tid) >> 4;
   const int nhw = (gridDim.x * kGatherThreads) >> 4;
 
-  for (int item0 = hw0; item0 < total; item0 += nhw * kGatherUnroll) {
-    uint4 v[kGatherUnroll];
-    uint16_t* dst[kGatherUnroll];
+  // Three stages per batch of kGatherUnroll rows of this half-warp: (A) locate
+  // each row and load its (position, slot); (B) load the row from the host;
+  // (C) store it to its slot. A runs one batch ahead of B, so the load of the
+  // indices hides behind the previous batch's host round trip.
+  int pos_n[kGatherUnroll], slot_n[kGatherUnroll];
+  const uint16_t* hbase_n[kGatherUnroll];
+  uint16_t* sbase_n[kGatherUnroll];
+  auto stage_a = [&](int item0) {
 #pragma unroll
     for (int u = 0; u < kGatherUnroll; ++u) {
-      dst[u] = nullptr;
       const int item = item0 + u * nhw;
+      hbase_n[u] = nullptr;
+      sbase_n[u] = nullptr;
+      pos_n[u] = 0;
+      slot_n[u] = 0;
       if (item >= total) continue;
       const int lq = item / per_layer;
       const int layer = layer_lo + lq;
@@ -83,15 +95,29 @@ gather_kernel(const spc_gather_view* __restrict__ views, int layer_lo, int layer
       const int lrel = layer - vw.layer0;
       if (lrel < 0 || lrel >= vw.n_layers) continue;
       const size_t li = (size_t)seg * K + i;
-      const int pos = load_pos[li];
-      const int slot = load_slot[li];
-      const size_t hrow = (((size_t)lrel * 2 + kv) * n_kv + g) * cap + pos;
-      const size_t srow = (((size_t)lrel * 2 + kv) * n_kv + g) * K + slot;
-      v[u] = ldg_stream(static_cast<const uint16_t*>(vw.host) + hrow * kD + l16 * 8);
-      dst[u] = static_cast<uint16_t*>(vw.slots) + srow * kD + l16 * 8;
+      pos_n[u] = load_pos[li];
+      slot_n[u] = load_slot[li];
+      const size_t hseg = (((size_t)lrel * 2 + kv) * n_kv + g) * cap;
+      const size_t sseg = (((size_t)lrel * 2 + kv) * n_kv + g) * K;
+      hbase_n[u] = static_cast<const uint16_t*>(vw.host) + hseg * kD + l16 * 8;
+      sbase_n[u] = static_cast<uint16_t*>(vw.slots) + sseg * kD + l16 * 8;
     }
+  };
+
+  stage_a(hw0);
+  for (int item0 = hw0; item0 < total; item0 += nhw * kGatherUnroll) {
+    uint4 v[kGatherUnroll];
+    uint16_t* dst[kGatherUnroll];
 #pragma unroll
-    for (int u = 0; u < kGatherUnroll; ++u)
+    for (int u = 0; u < kGatherUnroll; ++u) {   // stage B of this batch
+      dst[u] = nullptr;
+      if (!hbase_n[u]) continue;
+      v[u] = ldg_stream(hbase_n[u] + (size_t)pos_n[u] * kD);
+      dst[u] = sbase_n[u] + (size_t)slot_n[u] * kD;
+    }
+    stage_a(item0 + nhw * kGatherUnroll);       // stage A of the next batch
+#pragma unroll
+    for (int u = 0; u < kGatherUnroll; ++u)     // stage C of this batch
       if (dst[u]) stg_v4(dst[u], v[u]);
   }
 }
@@ -103,7 +129,7 @@ int gather_launch(const spc_gather_view* views, int layer_lo, int layer_hi, cons
   const long long max_items = (long long)(layer_hi - layer_lo) * 2 * B * n_kv * budget;
   const long long per_block = (kGatherThreads / 16) * kGatherUnroll;
   long long grid = (max_items + per_block - 1) / per_block;
-  const long long cap_grid = std::max(8, device_sm_count() / 8);
+  const long long cap_grid = std::max(4, device_sm_count() / kGatherSmsPerCta);
   if (grid > cap_grid) grid = cap_grid;
   if (grid < 1) grid = 1;
   gather_kernel<<<(int)grid, kGatherThreads, 0, static_cast<cudaStream_t>(stream)>>>(

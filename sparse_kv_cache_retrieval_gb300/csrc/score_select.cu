@@ -15,7 +15,7 @@
 //    small batch), 16-byte loads, deterministic last-block reduction of the
 //    split partials; the appended key row is rounded to bf16 and written in
 //    place.
-//  * scan_kernel: persistent CTAs; one producer warp streams 32 KiB tiles of
+//  * scan_kernel: each CTA takes a few consecutive key tiles; one producer warp streams 32 KiB tiles of
 //    128 consecutive key rows into a 3-stage shared-memory ring with coalesced
 //    16-byte cp.async (XOR-swizzled rows, mbarrier completion); 4 consumer
 //    warps form S = Q K^T on tensor cores (mma.sync m16n8k16 bf16, fp32
@@ -185,7 +185,7 @@ struct ScanArgs {
   float* logits;
   float2* part;
   int* status;
-  int n_q, n_kv, cap, lstride, n_tiles, total_tiles, append, n_parts;
+  int n_q, n_kv, cap, lstride, n_tiles, total_tiles, append, n_parts, tpc;
   float qscale;
 };
 
@@ -193,6 +193,10 @@ constexpr int kScanRows = 128;
 constexpr int kScanCWarps = 4;
 constexpr int kScanThreads = (kScanCWarps + 1) * 32;
 constexpr int kScanStages = 3;
+#ifndef SPC_SCAN_TILES_PER_CTA
+#define SPC_SCAN_TILES_PER_CTA 8
+#endif
+constexpr int kScanTilesPerCta = SPC_SCAN_TILES_PER_CTA;
 constexpr uint32_t kScanTileBytes = kScanRows * kRowBytes;
 constexpr long long kWaitLimit = 4000000000ll;  // clock cycles (~2 s)
 
@@ -230,7 +234,8 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
     // pieces of row r stored at piece ^ (r & 7); rows past the end zero-filled
     const int piece = lane & 15, half = lane >> 4;
     int it = 0;
-    for (int t = blockIdx.x; t < a.total_tiles; t += gridDim.x) {
+    const int t_end = min(a.total_tiles, (blockIdx.x + 1) * a.tpc);
+    for (int t = blockIdx.x * a.tpc; t < t_end; ++t) {
       const int seg = t / a.n_tiles, tile = t - seg * a.n_tiles;
       const int b = seg / a.n_kv;
       const int L = effective_len(a.len, b, a.append, a.cap);
@@ -268,7 +273,8 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
   uint32_t qh[8][4], ql[8][4];
   int cur_seg = -1;
   int it = 0;
-  for (int t = blockIdx.x; t < a.total_tiles; t += gridDim.x) {
+  const int t_end = min(a.total_tiles, (blockIdx.x + 1) * a.tpc);
+  for (int t = blockIdx.x * a.tpc; t < t_end; ++t) {
     const int seg = t / a.n_tiles, tile = t - seg * a.n_tiles;
     const int b = seg / a.n_kv, g = seg - b * a.n_kv;
     const int L = effective_len(a.len, b, a.append, a.cap);
@@ -784,9 +790,10 @@ int score_select_launch(const ScoreSelectCall& c) {
     sa.n_q = c.n_q; sa.n_kv = c.n_kv; sa.cap = c.cap; sa.lstride = l.lstride; sa.n_tiles = l.n_tiles;
     sa.total_tiles = c.B * c.n_kv * l.n_tiles; sa.append = c.append; sa.n_parts = l.n_parts;
     sa.qscale = kLog2e / sqrtf((float)kD);
-    int grid = 2 * device_sm_count();
-    if (grid < 1) grid = 1;
-    if (grid > sa.total_tiles) grid = sa.total_tiles;
+    // each CTA takes kScanTilesPerCta consecutive tiles: the hardware block
+    // scheduler then balances the load when other kernels hold some SMs
+    sa.tpc = kScanTilesPerCta;
+    const int grid = (sa.total_tiles + sa.tpc - 1) / sa.tpc;
     switch (G) {
       case 1: e = launch_scan<1>(sa, grid, st); break;
       case 2: e = launch_scan<2>(sa, grid, st); break;
