@@ -58,6 +58,7 @@ typedef enum spc_status {
 #define SPC_MAX_BUDGET 4096     /* KV budget per KV head                       */
 #define SPC_MAX_BATCH 64
 #define SPC_MAX_GROUP 64        /* query heads per KV head (1,2,4,8,16,32,64) */
+#define SPC_MAX_HIDDEN 32768    /* retrieval-head input width H               */
 
 /* Human-readable name of a status code. Never NULL. */
 const char* spc_status_string(int status);
@@ -103,8 +104,8 @@ int spc_version(void);
  *            call leaves it ready for the next one. Its first int32 is the
  *            device status word: 0, or SPC_ERR_TIMEOUT / SPC_ERR_OVERFLOW set
  *            by a kernel; the caller reads and clears it.
- * Limits: d = 128; n_q % n_kv == 0 with G in {1,2,4,8,16,32,64}; H % 8 == 0;
- *         1 <= B <= 64; 1 <= budget <= min(cap, 4096); cap <= 262144;
+ * Limits: d = 128; n_q % n_kv == 0 with G in {1,2,4,8,16,32,64}; H % 8 == 0,
+ *         8 <= H <= 32768; 1 <= B <= 64; 1 <= budget <= min(cap, 4096); cap <= 262144;
  *         n_sink + n_recent <= budget.
  * Concurrent calls must use distinct workspaces.
  * ---------------------------------------------------------------------- */

@@ -107,7 +107,7 @@ int spc_score_select_stages(const void* x, const void* Wq, const void* Wk, void*
       (q_out && !aligned16(q_out)))
     return SPC_ERR_INVALID_ARG;
   if (d != SPC_HEAD_DIM || !group_ok(n_q, n_kv)) return SPC_ERR_SHAPE;
-  if (B < 1 || B > SPC_MAX_BATCH || H < 8 || H % 8) return SPC_ERR_SHAPE;
+  if (B < 1 || B > SPC_MAX_BATCH || H < 8 || H > SPC_MAX_HIDDEN || H % 8) return SPC_ERR_SHAPE;
   if (cap < 1 || cap > SPC_MAX_CAP) return SPC_ERR_SHAPE;
   if (budget < 1 || budget > SPC_MAX_BUDGET || budget > cap) return SPC_ERR_SHAPE;
   if (n_sink < 0 || n_recent < 0 || n_sink + n_recent > budget) return SPC_ERR_SHAPE;

@@ -12,9 +12,10 @@
 //
 // GB300 design:
 //  * proj_kernel: split-K GEMV over [W_q | W_k] (HBM-bound on the weights at
-//    small batch), 16-byte loads, deterministic last-block reduction of the
-//    split partials; the appended key row is rounded to bf16 and written in
-//    place.
+//    small batch), 16-byte loads, up to 16 in flight per thread; the splits
+//    of a column tile form one thread-block cluster and meet in rank 0's
+//    shared memory (fixed order, deterministic); the appended key row is
+//    rounded to bf16 and written in place.
 //  * scan_kernel: each CTA takes a few consecutive key tiles; one producer warp streams 32 KiB tiles of
 //    128 consecutive key rows into a 3-stage shared-memory ring with coalesced
 //    16-byte cp.async (XOR-swizzled rows, mbarrier completion); 4 consumer
@@ -24,10 +25,10 @@
 //    give the logsumexp.
 //  * select_kernel: one thread-block cluster per (request, KV head) folds the
 //    logsumexp of each head, forms the group score and its order key for
-//    every position, finds the threshold key with a three-level radix select
-//    whose histograms are summed through distributed shared memory, and
-//    writes the selection with an ordered compaction (ascending, ties to the
-//    lower position).
+//    every position, finds the threshold key with a radix select whose
+//    histograms meet through distributed shared memory, and writes the
+//    selection with an ordered compaction (ascending, ties to the lower
+//    position).
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <math.h>
@@ -52,15 +53,13 @@ struct ProjArgs {
   const int32_t* len;
   float* q_ws;
   float* q_out;
-  float* part;
-  uint32_t* counters;
   int* status;
   int B, H, Nq, Nk, Ntot, n_kv, cap, S, Hc;
 };
 
 constexpr int kProjThreads = 256;
 constexpr int kProjTile = 128;
-constexpr int kProjBB = 16;  // batch rows per block (grid.z covers B)
+constexpr int kProjMaxSplit = 16;
 
 template <int BB>
 __device__ __forceinline__ void proj_fma(float (&acc)[BB][8], const uint4& w, const float* xr) {
@@ -74,11 +73,17 @@ __device__ __forceinline__ void proj_fma(float (&acc)[BB][8], const uint4& w, co
   }
 }
 
+// One cluster of S CTAs per 128-column tile: rank r forms the partial product
+// over hidden rows [r*Hc, (r+1)*Hc); rank 0 sums the S partials through
+// distributed shared memory in rank order (deterministic) and writes the
+// result.
 template <int BB>
 __global__ void __launch_bounds__(kProjThreads) proj_kernel(ProjArgs a) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ float psm[];
-  __shared__ int s_last;
-  const int tile = blockIdx.x, split = blockIdx.y, b0 = blockIdx.z * BB;
+  const int split = (int)cluster.block_rank();
+  const int tile = blockIdx.x / a.S, b0 = blockIdx.z * BB;
   const int col0 = tile * kProjTile;
   const bool is_k = col0 >= a.Nq;
   const uint16_t* W = is_k ? a.Wk : a.Wq;
@@ -88,7 +93,7 @@ __global__ void __launch_bounds__(kProjThreads) proj_kernel(ProjArgs a) {
   const int nr = max(0, min(a.H, r_begin + a.Hc) - r_begin);
 
   float* xs = psm;                       // [Hc][BB]
-  float* red = psm + a.Hc * BB;          // [8 warps][BB][128]
+  float* red = psm + a.Hc * BB;          // [8 warps][BB][128]; [BB][128] partial after the fold
   for (int i = threadIdx.x; i < nr * BB; i += kProjThreads) {
     const int r = i / BB, bb = i - r * BB, b = b0 + bb;
     xs[i] = (b < a.B) ? __uint_as_float(uint32_t(a.x[(size_t)b * a.H + r_begin + r]) << 16) : 0.f;
@@ -102,18 +107,20 @@ __global__ void __launch_bounds__(kProjThreads) proj_kernel(ProjArgs a) {
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[bb][e] = 0.f;
 
+  // half-warp hw takes rows hw, hw + 16, ...; LD weight loads in flight
+  constexpr int LD = BB <= 2 ? 16 : 8;
   const uint16_t* wp = W + (size_t)r_begin * ld + wcol0 + l16 * 8;
   int r = warp * 2 + (lane >> 4);
-  for (; r + 112 < nr; r += 128) {
-    uint4 w[8];
+  for (; r + 16 * (LD - 1) < nr; r += 16 * LD) {
+    uint4 w[LD];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) w[u] = ldg_stream(wp + (size_t)(r + 16 * u) * ld);
+    for (int u = 0; u < LD; ++u) w[u] = ldg_stream(wp + (size_t)(r + 16 * u) * ld);
 #pragma unroll
-    for (int u = 0; u < 8; ++u) proj_fma<BB>(acc, w[u], xs + (r + 16 * u) * BB);
+    for (int u = 0; u < LD; ++u) proj_fma<BB>(acc, w[u], xs + (r + 16 * u) * BB);
   }
   for (; r < nr; r += 16) proj_fma<BB>(acc, ldg_stream(wp + (size_t)r * ld), xs + r * BB);
 
-  // the two half-warps hold the same 128 columns: fold them, then across warps
+  // the two half-warps hold the same 128 columns: fold them, then the warps
 #pragma unroll
   for (int bb = 0; bb < BB; ++bb)
 #pragma unroll
@@ -128,53 +135,40 @@ __global__ void __launch_bounds__(kProjThreads) proj_kernel(ProjArgs a) {
   }
   __syncthreads();
   for (int i = threadIdx.x; i < BB * kProjTile; i += kProjThreads) {
-    const int bb = i / kProjTile, c = i - bb * kProjTile;
-    if (b0 + bb >= a.B) continue;
-    float s = 0.f;
+    float sum = 0.f;
 #pragma unroll
-    for (int w = 0; w < kProjThreads / 32; ++w) s += red[(w * BB + bb) * kProjTile + c];
-    a.part[((size_t)split * a.B + b0 + bb) * a.Ntot + col0 + c] = s;
+    for (int w = 0; w < kProjThreads / 32; ++w) sum += red[w * BB * kProjTile + i];
+    red[i] = sum;   // only this thread reads element i of warp 0's slice
   }
+  cluster.sync();
 
-  // deterministic cross-block reduction: the last split block of this tile
-  // sums the partials in split order and writes the result
-  __threadfence();
-  __syncthreads();
-  const int ctr = tile * gridDim.z + blockIdx.z;
-  if (threadIdx.x == 0) s_last = (atomicAdd(&a.counters[ctr], 1u) == (uint32_t)(a.S - 1));
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  for (int i = threadIdx.x; i < BB * kProjTile; i += kProjThreads) {
-    const int bb = i / kProjTile, c = i - bb * kProjTile, b = b0 + bb;
-    if (b >= a.B) continue;
-    float s4[4] = {0.f, 0.f, 0.f, 0.f};
-    const float* pc = a.part + (size_t)b * a.Ntot + col0 + c;
-    const size_t st = (size_t)a.B * a.Ntot;
-    int sp = 0;
-    for (; sp + 4 <= a.S; sp += 4) {
-      s4[0] += __ldcg(pc + (sp + 0) * st);
-      s4[1] += __ldcg(pc + (sp + 1) * st);
-      s4[2] += __ldcg(pc + (sp + 2) * st);
-      s4[3] += __ldcg(pc + (sp + 3) * st);
-    }
-    for (; sp < a.S; ++sp) s4[0] += __ldcg(pc + sp * st);
-    const float s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
-    if (!is_k) {
-      a.q_ws[(size_t)b * a.Nq + col0 + c] = s;
-      if (a.q_out) a.q_out[(size_t)b * a.Nq + col0 + c] = s;
-    } else {
-      const int g = wcol0 / kD;
-      const int L = a.len[b];
-      if (L >= 0 && L < a.cap) {
-        const __nv_bfloat16 h = __float2bfloat16_rn(s);
-        a.K_dlm[(((size_t)b * a.n_kv + g) * a.cap + L) * kD + c] = __bfloat16_as_ushort(h);
-      } else if (c == 0) {
-        set_status(a.status, SPC_ERR_OVERFLOW);
+  if (split == 0) {
+    for (int i = threadIdx.x; i < BB * kProjTile; i += kProjThreads) {
+      const int bb = i / kProjTile, c = i - bb * kProjTile, b = b0 + bb;
+      if (b >= a.B) continue;
+      float v[kProjMaxSplit];
+#pragma unroll
+      for (int q = 0; q < kProjMaxSplit; ++q) v[q] = q < a.S ? *cluster.map_shared_rank(red + i, q) : 0.f;
+      float sum = 0.f;
+#pragma unroll
+      for (int q = 0; q < kProjMaxSplit; ++q) sum += v[q];
+      if (!is_k) {
+        a.q_ws[(size_t)b * a.Nq + col0 + c] = sum;
+        if (a.q_out) a.q_out[(size_t)b * a.Nq + col0 + c] = sum;
+      } else {
+        const int g = wcol0 / kD;
+        const int L = a.len[b];
+        if (L >= 0 && L < a.cap) {
+          const __nv_bfloat16 h = __float2bfloat16_rn(sum);
+          a.K_dlm[(((size_t)b * a.n_kv + g) * a.cap + L) * kD + c] = __bfloat16_as_ushort(h);
+        } else if (c == 0) {
+          set_status(a.status, SPC_ERR_OVERFLOW);
+        }
       }
     }
   }
-  if (threadIdx.x == 0) a.counters[ctr] = 0u;
+  // peers keep their shared memory until rank 0 has read it
+  cluster.sync();
 }
 
 // ============================================================== key scan
@@ -389,23 +383,28 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
 // ============================================================== group score + Top-K
 // One kernel, one thread-block cluster of C CTAs per (request, KV head); rank
 // r owns the contiguous positions [r*slice, (r+1)*slice):
-//  * logsumexp: rank r folds its share of the scan's (max, sum) partials of
-//    each head of the group; the C results meet through distributed shared
-//    memory;
+//  * logsumexp of each head of the group over the scan's (max, sum) partials:
+//    every rank folds all of them when they are few, else each folds a share
+//    and the C results meet through distributed shared memory;
 //  * group score s = max_h (l_h - lse_h), p = 2^s (written out on request)
 //    and the order key of p (its float bits + 1; 0 marks a forced or absent
-//    position), kept in shared memory (global spill for very long slices);
-//  * the (K - |F|)-th largest key by a three-level radix select over bits
-//    30..20, 19..10 and 9..0: each rank histograms its keys, rank r sums its
-//    share of the bins over the cluster, every rank then finds the bin that
-//    holds the threshold (a level whose bin is taken whole ends the search);
-//  * an ordered compaction: the cluster's prefix counts give each rank its
-//    output offset, keys equal to the threshold go to the lowest positions.
+//    position), kept in shared memory (global spill for very long slices),
+//    with this rank's histogram of the key's bits 30..20;
+//  * every rank sums the C histograms and finds the bin that holds the
+//    (K - |F|)-th largest key. Usually few keys fall in that bin: every rank
+//    then gathers all ranks' keys of the bin and finishes the select on them
+//    alone (bits 19..10, then 9..0), and the same gathered keys give each
+//    rank its output offset. When the bin holds very many equal-prefix keys
+//    the two finer levels are histogrammed over the cluster instead;
+//  * an ordered compaction of the rank's slice (ascending positions, keys
+//    equal to the threshold to the lowest positions).
 constexpr int kSelThreads = 512;
 constexpr int kSelMaxCluster = 16;
 constexpr int kHistBins = 2048;       // level 1: key bits 30..20
 constexpr int kSubBins = 1024;        // levels 2 and 3: bits 19..10, 9..0
 constexpr int kSelSmemKeys = 8192;    // keys of a slice kept in shared memory up to this count
+constexpr int kSelCandMax = 4096;     // threshold-bin keys finished per rank
+constexpr int kSelLseLocal = 8192;    // partials (all heads) a rank folds alone
 
 struct SelArgs {
   const float* logits;
@@ -420,11 +419,17 @@ struct SelArgs {
 
 struct SelSmem {
   uint32_t hist[kHistBins];           // this rank's histogram of the current level
-  uint32_t tot[kHistBins];            // this rank's share of the cluster-wide counts
+  uint32_t tot[kHistBins];            // the cluster's counts (or this rank's share of them)
   uint32_t keys[kSelSmemKeys];
+  uint32_t lc[kSelCandMax];           // this rank's keys in the threshold bin (any order)
+  uint32_t cand[kSelCandMax];         // every rank's, in rank order
   float pm[SPC_MAX_GROUP], ps[SPC_MAX_GROUP], lse[SPC_MAX_GROUP];
+  float wm[SPC_MAX_GROUP > kSelThreads / 32 ? SPC_MAX_GROUP : kSelThreads / 32];   // per-(head, warp) logsumexp partials
+  float ws[SPC_MAX_GROUP > kSelThreads / 32 ? SPC_MAX_GROUP : kSelThreads / 32];
   int scratch[33];
-  int cnt[2];                         // this rank's (above, equal) counts
+  int cnt[2];                         // published counts of this rank
+  int ncand;
+  int rb[kSelMaxCluster + 1];         // candidate offsets of the ranks
   int bin, rem, whole;
 };
 
@@ -455,6 +460,13 @@ __device__ __forceinline__ void find_bin(const uint32_t* cnt, int nbins, int rem
   __syncthreads();
 }
 
+// Sum over the block of one int per thread (contains __syncthreads).
+__device__ __forceinline__ int block_sum(int v, int* scratch) {
+  int tot;
+  block_excl_scan(v, scratch, &tot);
+  return tot;
+}
+
 template <int G>
 __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a) {
   namespace cg = cooperative_groups;
@@ -471,33 +483,54 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a) {
   const bool topk = L > a.K;
   const int Kp = a.K - (a.n_sink + a.n_recent);
 
-  // ---- logsumexp of each head: this rank's share of the partials
+  // ---- logsumexp of each head: NW / G warps per head (one when G >= NW),
+  // eight partial loads in flight per lane
+  const int nv = ((L + kScanRows - 1) / kScanRows) * a.ppt;
+  const bool lse_local = (long long)nv * G <= kSelLseLocal;
   {
-    const int nv = ((L + kScanRows - 1) / kScanRows) * a.ppt;
-    const int v0 = (int)((long long)nv * rank / C), v1 = (int)((long long)nv * (rank + 1) / C);
-    for (int h = warp; h < G; h += NW) {
+    constexpr int WPH = G >= NW ? 1 : NW / G;
+    const int sub = warp % WPH;
+    const int r0 = lse_local ? 0 : (int)((long long)nv * rank / C);
+    const int r1 = lse_local ? nv : (int)((long long)nv * (rank + 1) / C);
+    const int v0 = r0 + (int)((long long)(r1 - r0) * sub / WPH);
+    const int v1 = r0 + (int)((long long)(r1 - r0) * (sub + 1) / WPH);
+    for (int h = warp / WPH; h < G; h += NW / WPH) {
       const float2* ph = a.part + ((size_t)b * a.n_q + (size_t)g * G + h) * a.n_parts;
       float m = -INFINITY, s = 0.f;
-      for (int i = v0 + lane; i < v1; i += 32) {
-        const float2 v = __ldcg(ph + i);
-        lse2_combine(m, s, v.x, v.y);
+      for (int i0 = v0 + lane; i0 < v1; i0 += 32 * 8) {
+        float2 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = i0 + 32 * u < v1 ? __ldcg(ph + i0 + 32 * u) : make_float2(-INFINITY, 0.f);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) lse2_combine(m, s, v[u].x, v[u].y);
       }
       warp_lse2(m, s);
-      if (lane == 0) { sm.pm[h] = m; sm.ps[h] = s; }
+      if (lane == 0) { sm.wm[h * WPH + sub] = m; sm.ws[h * WPH + sub] = s; }
     }
   }
-  for (int i = tid; i < kHistBins; i += kSelThreads) sm.hist[i] = 0u;
-  cluster.sync();
+  __syncthreads();
   for (int h = tid; h < G; h += kSelThreads) {
-    float rm[kSelMaxCluster], rs[kSelMaxCluster];
-#pragma unroll
-    for (int r = 0; r < kSelMaxCluster; ++r)
-      if (r < C) { rm[r] = *cluster.map_shared_rank(&sm.pm[h], r); rs[r] = *cluster.map_shared_rank(&sm.ps[h], r); }
+    constexpr int WPH = G >= NW ? 1 : NW / G;
     float m = -INFINITY, s = 0.f;
-#pragma unroll
-    for (int r = 0; r < kSelMaxCluster; ++r)
-      if (r < C) lse2_combine(m, s, rm[r], rs[r]);
+    for (int w = 0; w < WPH; ++w) lse2_combine(m, s, sm.wm[h * WPH + w], sm.ws[h * WPH + w]);
+    sm.pm[h] = m;
+    sm.ps[h] = s;
     sm.lse[h] = s > 0.f ? m + log2f(s) : INFINITY;
+  }
+  for (int i = tid; i < kHistBins; i += kSelThreads) sm.hist[i] = 0u;
+  if (!lse_local) {
+    cluster.sync();
+    for (int h = tid; h < G; h += kSelThreads) {
+      float rm[kSelMaxCluster], rs[kSelMaxCluster];
+#pragma unroll
+      for (int r = 0; r < kSelMaxCluster; ++r)
+        if (r < C) { rm[r] = *cluster.map_shared_rank(&sm.pm[h], r); rs[r] = *cluster.map_shared_rank(&sm.ps[h], r); }
+      float m = -INFINITY, s = 0.f;
+#pragma unroll
+      for (int r = 0; r < kSelMaxCluster; ++r)
+        if (r < C) lse2_combine(m, s, rm[r], rs[r]);
+      sm.lse[h] = s > 0.f ? m + log2f(s) : INFINITY;
+    }
   }
   __syncthreads();
 
@@ -524,16 +557,18 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a) {
         sc[3] = fmaxf(sc[3], v[h].w - l);
       }
     }
+    uint32_t key[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int pos = p + j;
       if (pos >= t1) break;
       const float pr = exp2f(sc[j]);
       if (a.scores_out) a.scores_out[(size_t)seg * a.cap + pos] = pr;
-      const uint32_t key = is_forced(pos, L, a.n_sink, a.n_recent) ? 0u : __float_as_uint(pr) + 1u;
-      kb[pos - p_lo] = key;
-      if (topk && key) atomicAdd(&sm.hist[key >> 20], 1u);
+      key[j] = is_forced(pos, L, a.n_sink, a.n_recent) ? 0u : __float_as_uint(pr) + 1u;
+      if (topk && key[j]) atomicAdd(&sm.hist[key[j] >> 20], 1u);
     }
+    // positions past the end keep key 0: the 4-key groups below read them
+    *reinterpret_cast<uint4*>(kb + (p - p_lo)) = make_uint4(key[0], key[1], key[2], key[3]);
   }
 
   int32_t* out = a.selected + (size_t)seg * a.K;
@@ -542,80 +577,176 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a) {
     const int i0 = (int)((long long)a.K * rank / C), i1 = (int)((long long)a.K * (rank + 1) / C);
     for (int i = i0 + tid; i < i1; i += kSelThreads) out[i] = i < L ? i : -1;
   } else {
-    // ---- threshold key T: the Kp-th largest non-forced key; `need` keys equal
-    // to T are taken (T = all-ones and need = 0 when nothing but F is taken)
-    uint32_t T = 0xffffffffu;
-    int need = 0;
-    if (Kp > 0) {
-      uint32_t prefix = 0u, pmask = 0u;
-      int rem = Kp;
-      for (int lvl = 0; lvl < 3; ++lvl) {
-        const int shift = lvl == 0 ? 20 : (lvl == 1 ? 10 : 0);
-        const int nb = lvl == 0 ? kHistBins : kSubBins;
-        if (lvl > 0) {
-          for (int i = tid; i < nb; i += kSelThreads) sm.hist[i] = 0u;
-          __syncthreads();
-          for (int p = t0; p < t1; ++p) {
-            const uint32_t k = kb[p - p_lo];
-            if (k && (k & pmask) == prefix) atomicAdd(&sm.hist[(k >> shift) & (uint32_t)(nb - 1)], 1u);
-          }
-        }
-        cluster.sync();
-        const int share = nb / C;
-        for (int i = tid; i < share; i += kSelThreads) {
-          const int bin = rank * share + i;
-          uint32_t sum = 0u;
-#pragma unroll 4
-          for (int r = 0; r < C; ++r) sum += *cluster.map_shared_rank(&sm.hist[bin], r);
-          sm.tot[bin] = sum;
-        }
-        cluster.sync();
-        for (int i = tid; i < nb; i += kSelThreads) sm.hist[i] = *cluster.map_shared_rank(&sm.tot[i], i / share);
+  // ---- threshold key T: the Kp-th largest non-forced key; `need` keys equal
+  // to T are taken (T = all-ones and need = 0 when nothing but F is taken).
+  // base_b / base_e: selected keys above T / equal to T in lower ranks.
+  uint32_t T = 0xffffffffu;
+  int need = 0;
+  int base_b = -1, base_e = 0;        // base_b < 0: offsets still to exchange
+  if (Kp > 0) {
+    cluster.sync();                   // every rank's level-1 histogram is final
+    for (int i = tid; i < kHistBins; i += kSelThreads) {
+      uint32_t v[kSelMaxCluster];
+#pragma unroll
+      for (int r = 0; r < kSelMaxCluster; ++r) v[r] = r < C ? *cluster.map_shared_rank(&sm.hist[i], r) : 0u;
+      uint32_t sum = 0u;
+#pragma unroll
+      for (int r = 0; r < kSelMaxCluster; ++r) sum += v[r];
+      sm.tot[i] = sum;
+    }
+    __syncthreads();
+    find_bin(sm.tot, kHistBins, Kp, sm);
+    const uint32_t b1 = (uint32_t)sm.bin;
+    const int rem1 = sm.rem;
+    if (sm.whole) {
+      T = b1 ? (b1 << 20) - 1u : 0u;
+    } else if ((int)sm.tot[b1] <= kSelCandMax) {
+      // this rank's keys in bin b1, and its count of forced + above-bin keys
+      if (tid == 0) sm.ncand = 0;
+      __syncthreads();
+      int above = 0;
+      for (int p = t0; p < t1; ++p) {
+        const uint32_t k = kb[p - p_lo];
+        if (is_forced(p, L, a.n_sink, a.n_recent) || (k >> 20) > b1) ++above;
+        else if (k && (k >> 20) == b1) sm.lc[atomicAdd(&sm.ncand, 1)] = k;
+      }
+      above = block_sum(above, sm.scratch);
+      if (tid == 0) sm.cnt[0] = above;
+      cluster.sync();                 // candidates and counts of every rank published
+      // candidate counts of the ranks (one load each, in parallel), their
+      // offsets, then every candidate copied by its own thread
+      int nc_r = 0, ab_r = 0;
+      if (tid < C) {
+        nc_r = *cluster.map_shared_rank(&sm.ncand, tid);
+        if (tid < rank) ab_r = *cluster.map_shared_rank(&sm.cnt[0], tid);
+      }
+      if (tid < C) sm.rb[tid + 1] = nc_r;
+      const int ab_lower = block_sum(ab_r, sm.scratch);
+      if (tid == 0) {
+        sm.rb[0] = 0;
+        for (int r = 0; r < C; ++r) sm.rb[r + 1] += sm.rb[r];
+      }
+      __syncthreads();
+      for (int i = tid; i < sm.rb[C]; i += kSelThreads) {
+        int r = 0;
+        while (sm.rb[r + 1] <= i) ++r;
+        sm.cand[i] = *cluster.map_shared_rank(&sm.lc[i - sm.rb[r]], r);
+      }
+      __syncthreads();
+      const int ncand = sm.rb[C];
+      // levels 2 and 3 over the gathered keys
+      uint32_t prefix = b1 << 20, pmask = 0xfff00000u;
+      int rem = rem1;
+      for (int lvl = 1; lvl < 3; ++lvl) {
+        const int shift = lvl == 1 ? 10 : 0;
+        for (int i = tid; i < kSubBins; i += kSelThreads) sm.hist[i] = 0u;
         __syncthreads();
-        find_bin(sm.hist, nb, rem, sm);
-        const uint32_t lower = prefix | ((uint32_t)sm.bin << shift);
-        if (sm.whole || lvl == 2) {
-          if (sm.whole) { T = lower ? lower - 1u : 0u; need = 0; }
-          else { T = lower; need = sm.rem; }
-          break;
+        for (int i = tid; i < ncand; i += kSelThreads) {
+          const uint32_t k = sm.cand[i];
+          if ((k & pmask) == prefix) atomicAdd(&sm.hist[(k >> shift) & (kSubBins - 1)], 1u);
         }
+        __syncthreads();
+        find_bin(sm.hist, kSubBins, rem, sm);
+        const uint32_t lower = prefix | ((uint32_t)sm.bin << shift);
+        if (sm.whole) { T = lower ? lower - 1u : 0u; need = 0; break; }
+        if (lvl == 2) { T = lower; need = sm.rem; break; }
         prefix = lower;
-        pmask |= (uint32_t)(nb - 1) << shift;
+        pmask |= (uint32_t)(kSubBins - 1) << shift;
         rem = sm.rem;
         __syncthreads();
       }
+      // offsets of this rank: lower ranks' keys above T and equal to T
+      int gt = 0, eq = 0;
+      for (int i = tid; i < sm.rb[rank]; i += kSelThreads) {
+        const uint32_t k = sm.cand[i];
+        gt += k > T;
+        eq += k == T;
+      }
+      base_b = ab_lower + block_sum(gt, sm.scratch);
+      base_e = need > 0 ? block_sum(eq, sm.scratch) : 0;
+    } else {
+      // very many keys share the threshold bin's prefix: histogram the two
+      // finer levels over the cluster
+      uint32_t prefix = b1 << 20, pmask = 0xfff00000u;
+      int rem = rem1;
+      for (int lvl = 1; lvl < 3; ++lvl) {
+        const int shift = lvl == 1 ? 10 : 0;
+        cluster.sync();               // no peer still reads this rank's last histogram
+        for (int i = tid; i < kSubBins; i += kSelThreads) sm.hist[i] = 0u;
+        __syncthreads();
+        for (int p = t0; p < t1; ++p) {
+          const uint32_t k = kb[p - p_lo];
+          if (k && (k & pmask) == prefix) atomicAdd(&sm.hist[(k >> shift) & (kSubBins - 1)], 1u);
+        }
+        cluster.sync();
+        for (int i = tid; i < kSubBins; i += kSelThreads) {
+          uint32_t sum = 0u;
+          for (int r = 0; r < C; ++r) sum += *cluster.map_shared_rank(&sm.hist[i], r);
+          sm.tot[i] = sum;
+        }
+        __syncthreads();
+        find_bin(sm.tot, kSubBins, rem, sm);
+        const uint32_t lower = prefix | ((uint32_t)sm.bin << shift);
+        if (sm.whole) { T = lower ? lower - 1u : 0u; need = 0; break; }
+        if (lvl == 2) { T = lower; need = sm.rem; break; }
+        prefix = lower;
+        pmask |= (uint32_t)(kSubBins - 1) << shift;
+        rem = sm.rem;
+      }
     }
-    // ---- ordered compaction over the cluster
-    int nb_ = 0, ne_ = 0;
-    for (int p = t0; p < t1; ++p) {
-      const uint32_t k = kb[p - p_lo];
-      if (is_forced(p, L, a.n_sink, a.n_recent) || (k && k > T)) ++nb_;
-      else if (need > 0 && k && k == T) ++ne_;
+  }
+
+  // ---- ordered compaction of this rank's slice: thread t owns the 4-key
+  // groups [t0, t1) (one 16-byte read each)
+  int nb_ = 0, ne_ = 0;
+  for (int p = t0; p < t1; p += 4) {
+    const uint4 k4 = *reinterpret_cast<const uint4*>(kb + (p - p_lo));
+    const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int q = p + j;
+      if (q >= t1) break;
+      if (is_forced(q, L, a.n_sink, a.n_recent) || (kk[j] && kk[j] > T)) ++nb_;
+      else if (need > 0 && kk[j] && kk[j] == T) ++ne_;
     }
-    int tb, te;
-    int base_b = block_excl_scan(nb_, sm.scratch, &tb);
-    int base_e = block_excl_scan(ne_, sm.scratch, &te);
+  }
+  int tb, te;
+  int off_b = block_excl_scan(nb_, sm.scratch, &tb);
+  int off_e = block_excl_scan(ne_, sm.scratch, &te);
+  if (base_b < 0) {
+    // offsets from the lower ranks' published counts
     if (tid == 0) { sm.cnt[0] = tb; sm.cnt[1] = te; }
     cluster.sync();
+    base_b = 0;
+    base_e = 0;
     for (int r = 0; r < rank; ++r) {
       base_b += *cluster.map_shared_rank(&sm.cnt[0], r);
       base_e += *cluster.map_shared_rank(&sm.cnt[1], r);
     }
-    int o = base_b + min(base_e, need);
-    int eq_seen = base_e;
-    for (int p = t0; p < t1; ++p) {
-      const uint32_t k = kb[p - p_lo];
-      bool sel = is_forced(p, L, a.n_sink, a.n_recent) || (k && k > T);
-      if (!sel && need > 0 && k && k == T) {
+  }
+  off_b += base_b;
+  off_e += base_e;
+  int o = off_b + min(off_e, need);
+  int eq_seen = off_e;
+  for (int p = t0; p < t1; p += 4) {
+    const uint4 k4 = *reinterpret_cast<const uint4*>(kb + (p - p_lo));
+    const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int q = p + j;
+      if (q >= t1) break;
+      bool sel = is_forced(q, L, a.n_sink, a.n_recent) || (kk[j] && kk[j] > T);
+      if (!sel && need > 0 && kk[j] && kk[j] == T) {
         sel = eq_seen < need;
         ++eq_seen;
       }
       if (sel) {
-        if (o < a.K) out[o] = p;
+        if (o < a.K) out[o] = q;
         ++o;
       }
     }
   }
+  }  // topk
   // no rank leaves while a peer may still read its shared memory
   cluster.sync();
 
@@ -634,24 +765,16 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a) {
 
 // ============================================================== host side
 struct ScoreLayout {
-  size_t status, done, counters, q, part_proj, logits, part_scan, keys, total;
-  int S, Hc, n_col_tiles, bz, n_tiles, ppt, n_parts, lstride;
+  size_t status, done, q, logits, part_scan, keys, total;
+  int n_tiles, ppt, n_parts, lstride;
 };
-
-static int proj_splits(int H) {
-  int S = H / 256;
-  return S < 1 ? 1 : (S > 32 ? 32 : S);
-}
 
 static int scan_ppt(int G) { return kScanCWarps / (G <= 16 ? 1 : G / 16); }
 
 static ScoreLayout score_layout(int B, int H, int n_q, int n_kv, int cap) {
   ScoreLayout l{};
-  const int Nq = n_q * kD, Nk = n_kv * kD, Ntot = Nq + Nk;
-  l.S = proj_splits(H);
-  l.Hc = (H + l.S - 1) / l.S;
-  l.n_col_tiles = Ntot / kProjTile;
-  l.bz = (B + kProjBB - 1) / kProjBB;
+  const int Nq = n_q * kD;
+  (void)H;
   l.n_tiles = (cap + kScanRows - 1) / kScanRows;
   l.ppt = scan_ppt(n_q / n_kv);
   l.n_parts = l.n_tiles * l.ppt;
@@ -660,9 +783,7 @@ static ScoreLayout score_layout(int B, int H, int n_q, int n_kv, int cap) {
   auto take = [&](size_t bytes) { size_t o = off; off = (off + bytes + 255) & ~size_t(255); return o; };
   l.status = take(2 * sizeof(int));
   l.done = l.status + sizeof(int);
-  l.counters = take(sizeof(uint32_t) * (size_t)l.n_col_tiles * 4 /* grid.z <= 4 */);
   l.q = take(sizeof(float) * (size_t)B * Nq);
-  l.part_proj = take(sizeof(float) * (size_t)l.S * B * Ntot);
   l.logits = take(sizeof(float) * (size_t)B * n_q * l.lstride);
   l.part_scan = take(sizeof(float2) * (size_t)B * n_q * l.n_parts);
   l.keys = take(sizeof(uint32_t) * (size_t)B * n_kv * ((cap + 3) & ~3));
@@ -687,16 +808,47 @@ static cudaError_t launch_scan(const ScanArgs& sa, int grid, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// Splits per column tile (the cluster size): one per 256 hidden rows, at most
+// 16; a size the device cannot co-schedule is halved.
 template <int BB>
-static cudaError_t launch_proj(const ProjArgs& pa, dim3 grid, size_t smem, cudaStream_t st) {
-  static size_t attr = 0;
-  if (smem > attr) {
-    cudaError_t e = cudaFuncSetAttribute(proj_kernel<BB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr = smem;
+static int launch_proj(ProjArgs& pa, int n_tiles, int bz, cudaStream_t st) {
+  static bool cluster_attr = false;
+  static size_t smem_attr = 0;
+  if (!cluster_attr) {
+    if (cudaFuncSetAttribute(proj_kernel<BB>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+      return SPC_ERR_CUDA;
+    cluster_attr = true;
   }
-  proj_kernel<BB><<<grid, kProjThreads, smem, st>>>(pa);
-  return cudaGetLastError();
+  int S = pa.H / 256;
+  S = S < 1 ? 1 : (S > kProjMaxSplit ? kProjMaxSplit : S);
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute at[1];
+  cfg.blockDim = dim3(kProjThreads, 1, 1);
+  cfg.stream = st;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  for (;; S /= 2) {
+    pa.S = S;
+    pa.Hc = (pa.H + S - 1) / S;
+    const size_t smem = sizeof(float) * ((size_t)pa.Hc * BB + (kProjThreads / 32) * BB * kProjTile);
+    if (smem > smem_attr) {
+      if (cudaFuncSetAttribute(proj_kernel<BB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return SPC_ERR_CUDA;
+      smem_attr = smem;
+    }
+    cfg.gridDim = dim3(n_tiles * S, 1, bz);
+    cfg.dynamicSmemBytes = smem;
+    at[0].val.clusterDim.x = S;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    int n_clusters = 0;
+    if (S == 1 || (cudaOccupancyMaxActiveClusters(&n_clusters, proj_kernel<BB>, &cfg) == cudaSuccess &&
+                   n_clusters > 0))
+      break;
+    cudaGetLastError();
+  }
+  return cudaLaunchKernelEx(&cfg, proj_kernel<BB>, pa) == cudaSuccess ? SPC_OK : SPC_ERR_CUDA;
 }
 
 // Cluster size: about one CTA per SM over all segments, at most 16, and at
@@ -759,23 +911,21 @@ int score_select_launch(const ScoreSelectCall& c) {
     pa.len = c.len;
     pa.q_ws = reinterpret_cast<float*>(ws + l.q);
     pa.q_out = c.q_out;
-    pa.part = reinterpret_cast<float*>(ws + l.part_proj);
-    pa.counters = reinterpret_cast<uint32_t*>(ws + l.counters);
     pa.status = status;
     pa.B = c.B; pa.H = c.H; pa.Nq = Nq; pa.Nk = Nk; pa.Ntot = Nq + Nk; pa.n_kv = c.n_kv;
-    pa.cap = c.cap; pa.S = l.S; pa.Hc = l.Hc;
+    pa.cap = c.cap;
     const int n_tiles = (Nq + (c.append ? Nk : 0)) / kProjTile;
     const int bb = c.B <= 1 ? 1 : c.B <= 2 ? 2 : c.B <= 4 ? 4 : c.B <= 8 ? 8 : 16;
-    const dim3 grid(n_tiles, l.S, (c.B + bb - 1) / bb);
-    const size_t smem = sizeof(float) * ((size_t)l.Hc * bb + (kProjThreads / 32) * bb * kProjTile);
+    const int bz = (c.B + bb - 1) / bb;
+    int rc;
     switch (bb) {
-      case 1: e = launch_proj<1>(pa, grid, smem, st); break;
-      case 2: e = launch_proj<2>(pa, grid, smem, st); break;
-      case 4: e = launch_proj<4>(pa, grid, smem, st); break;
-      case 8: e = launch_proj<8>(pa, grid, smem, st); break;
-      default: e = launch_proj<16>(pa, grid, smem, st); break;
+      case 1: rc = launch_proj<1>(pa, n_tiles, bz, st); break;
+      case 2: rc = launch_proj<2>(pa, n_tiles, bz, st); break;
+      case 4: rc = launch_proj<4>(pa, n_tiles, bz, st); break;
+      case 8: rc = launch_proj<8>(pa, n_tiles, bz, st); break;
+      default: rc = launch_proj<16>(pa, n_tiles, bz, st); break;
     }
-    if (e != cudaSuccess) return SPC_ERR_CUDA;
+    if (rc != SPC_OK) return rc;
   }
 
   // ---- key scan

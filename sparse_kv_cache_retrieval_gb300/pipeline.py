@@ -1,6 +1,6 @@
-"""The decode step on two CUDA streams: select for the next step, diff, and
-per layer chunk attention (stream A) followed by the in-place gather of the
-next step's missing rows (stream B).
+"""The decode step on four CUDA streams: the retrieval head's projection and
+key scan (stream C), select, diff and per layer chunk attention (stream A),
+and the in-place gather of the next step's missing rows (streams B0, B1).
 
 Method ordering: "ASPLOS'26 | SpeContext 让小模型先圈出重要 KV Cache"
 (marsggbo blog) §4 -- the retrieval head predicts the positions of step t+1
@@ -13,12 +13,16 @@ prologue runs the head once on the last prompt token and loads its whole
 selection before the first decode step.
 
 Ordering (per layer chunk c, step t, parity p = t % 2):
-  A: score_select(x_{t+1}) -> selected[1-p]; diff(selected[1-p], slot_pos[p])
+  C: wait select(t-1); project + key scan of x_{t+1}          (the "front")
+  A: wait front(t); select -> selected[1-p]; diff(selected[1-p], slot_pos[p])
      -> slot_pos[1-p], loads[1-p]; for each chunk c: wait gather(c, t-1);
      attention(c, selected[p], slot_pos[p]); record attn(c, t)
   B: wait attn(c, t); gather(c, loads[1-p]) into the slots; record gather(c, t)
-The in-place overwrite of chunk c therefore always follows the attention that
-reads the old rows, and the next step's attention on c always follows it.
+Inside a run of steps, the front of step t+1 is issued right after select(t)
+(it only needs the scan scratch that select(t) has consumed and the length
+select(t) has advanced), so it overlaps diff(t) and attention(t). The
+in-place overwrite of chunk c always follows the attention that reads the
+old rows, and the next step's attention on c always follows it.
 
 PyTorch provides device memory, pinned host memory, streams, events and CUDA
 graphs; every step of the method runs in libspc's kernels.
@@ -144,11 +148,20 @@ class DecodePipeline:
         self.chunks = [(l0, min(L, l0 + lc)) for l0 in range(0, L, lc)]
         self.ws_attn = torch.zeros(spc.spc_sparse_decode_attn_workspace_size(lc, B, self.n_q, n_kv, d, K),
                                    dtype=torch.uint8, device=dev)
-        self.sA = torch.cuda.Stream(device=dev)
-        self.sB = torch.cuda.Stream(device=dev)
+        # stream priorities: select/diff/attention (A) and the link-bound
+        # gathers (B) are on the critical path; the front (C) has a whole
+        # step of slack, so its CTAs yield to theirs
+        hi, lo = self._priorities()
+        self.sA = torch.cuda.Stream(device=dev, priority=hi)
+        self.sB = torch.cuda.Stream(device=dev, priority=hi)
         # gathers of consecutive layer chunks alternate over two streams so
         # that one launch's ramp-down overlaps the next one's ramp-up
-        self.sBs = [self.sB, torch.cuda.Stream(device=dev)]
+        self.sBs = [self.sB, torch.cuda.Stream(device=dev, priority=hi)]
+        self.sC = torch.cuda.Stream(device=dev, priority=lo)
+        self.e_front = torch.cuda.Event()
+        self.e_sel = torch.cuda.Event()
+        self._front_issued = None      # step whose front is in flight on stream C
+        self._range_end = None         # end of the current run of steps (look-ahead bound)
         self.e_attn = [torch.cuda.Event() for _ in self.chunks]
         self.e_gath = [torch.cuda.Event() for _ in self.chunks]
         self._gather_pending = [False] * len(self.chunks)
@@ -165,10 +178,20 @@ class DecodePipeline:
         self._capturing = False
         self._prologue_done = False
 
+    @staticmethod
+    def _priorities():
+        """(highest, lowest) stream priority of the device (lower is higher)."""
+        try:
+            lo, hi = torch.cuda.Stream.priority_range()
+        except Exception:
+            return 0, 0
+        return hi, lo
+
     def enable_host_io(self) -> None:
         """Switch to end-to-end mode: every step copies its head input and LLM
         queries from pinned host memory and copies its attention output and
-        selection back to pinned host memory, all on stream A."""
+        selection back to pinned host memory (the head input on stream C, the
+        rest on stream A)."""
         if self.host_io:
             return
         inputs, B, L, d, dev = self.inp, self.B, self.L, self.d, self.dev
@@ -236,26 +259,52 @@ class DecodePipeline:
             self._gather(0, 0, self.L, sA)
         sA.synchronize()
         self._gather_pending = [False] * len(self.chunks)
+        self._front_issued = None
         self._prologue_done = True
+
+    def _front(self, t: int) -> None:
+        """Projection and key scan of step t (input x[t+1]) on stream C, after
+        the select of step t-1 issued in this run (none before the first)."""
+        sC = self.sC
+        append = 1 if self.cfg.append else 0
+        if self._front_issued is not None:
+            sC.wait_event(self.e_sel)
+        else:
+            sC.wait_stream(self.sA)
+        pn = (t + 1) % 2
+        if self.host_io:
+            with torch.cuda.stream(sC):
+                self.x_stage.copy_(self.x_host[t + 1], non_blocking=True)
+            x = self.x_stage
+        else:
+            x = self.x_dev[t + 1]
+        if self.timing:
+            self._timed_call("project", sC, lambda: self._score_select(x, self.selected[pn], append, sC, 1))
+            self._timed_call("key_scan", sC, lambda: self._score_select(x, self.selected[pn], append, sC, 2))
+        else:
+            self._score_select(x, self.selected[pn], append, sC, 3)
+        self.e_front.record(sC)
+        self._front_issued = t
 
     def step(self, t: int) -> None:
         """Issue decode step t (uses inputs x[t+1] and q_llm[t])."""
-        sA, sB = self.sA, self.sB
+        sA = self.sA
         p, pn = t % 2, (t + 1) % 2
         append = 1 if self.cfg.append else 0
+        if self._front_issued != t:
+            self._front(t)
+        sA.wait_event(self.e_front)
         if self.host_io:
             with torch.cuda.stream(sA):
-                self.x_stage.copy_(self.x_host[t + 1], non_blocking=True)
                 self.q_stage.copy_(self.q_host[t], non_blocking=True)
-            x, q_layers = self.x_stage, self.q_stage
+            q_layers = self.q_stage
         else:
-            x, q_layers = self.x_dev[t + 1], self.q_dev[t]
-        if self.timing:
-            self._timed_call("project", sA, lambda: self._score_select(x, self.selected[pn], append, sA, 1))
-            self._timed_call("key_scan", sA, lambda: self._score_select(x, self.selected[pn], append, sA, 2))
-            self._timed_call("select", sA, lambda: self._score_select(x, self.selected[pn], append, sA, 4))
-        else:
-            self._score_select(x, self.selected[pn], append, sA)
+            q_layers = self.q_dev[t]
+        # the select stage reads only the front's scratch; x is not used
+        self._timed_call("select", sA, lambda: self._score_select(self.x_dev[0], self.selected[pn], append, sA, 4))
+        self.e_sel.record(sA)
+        if self._range_end is not None and t + 1 < self._range_end and t + 2 < len(self.inp.x):
+            self._front(t + 1)
         self._timed_call("diff", sA, lambda: self._diff(pn, p, sA))
         for c, (l0, l1) in enumerate(self.chunks):
             if self._gather_pending[c]:
@@ -273,12 +322,17 @@ class DecodePipeline:
                 self.sel_host[t].copy_(self.selected[pn], non_blocking=True)
 
     def join(self) -> None:
-        for sg in self.sBs:
+        for sg in self.sBs + [self.sC]:
             self.sA.wait_stream(sg)
+        self._front_issued = None
 
     def run(self, t0: int, n: int) -> None:
-        for t in range(t0, t0 + n):
-            self.step(t)
+        self._range_end = t0 + n
+        try:
+            for t in range(t0, t0 + n):
+                self.step(t)
+        finally:
+            self._range_end = None
         self.join()
 
     def capture(self, t0: int, n: int) -> torch.cuda.CUDAGraph:
@@ -294,13 +348,16 @@ class DecodePipeline:
         self._capturing = True
         try:
             with torch.cuda.graph(g, stream=self.sA):
-                for sg in self.sBs:
+                for sg in self.sBs + [self.sC]:
                     sg.wait_stream(self.sA)
+                self._front_issued = None
+                self._range_end = t0 + n
                 for t in range(t0, t0 + n):
                     self.step(t)
                 self.join()
         finally:
             self._capturing = False
+            self._range_end = None
         self._gather_pending = [False] * len(self.chunks)
         del saved
         return g

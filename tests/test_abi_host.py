@@ -85,6 +85,7 @@ def test_score_select_rejects_bad_arguments(lib):
     assert _score(lib, n_sink=500, n_recent=64) == -2    # forced set > budget
     assert _score(lib, B=0) == -2
     assert _score(lib, H=4095) == -2
+    assert _score(lib, H=32776) == -2                   # H > max
     assert _score(lib) == -5                             # workspace too small
     assert lib.spc_score_select_stages(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 1, 4096, 32, 8, 128, 4096,
                                        512, 4, 64, None, None, FAKE, FAKE, 1 << 40, None, 0) == -1

@@ -60,6 +60,20 @@ def test_score_select_small(name, kw):
     _one_call(cfg)
 
 
+def test_all_equal_keys_over_a_long_context_ties_go_to_lower_positions():
+    # every one of 20000 keys ties: the threshold bin holds far more keys than
+    # one rank finishes alone, so the finer levels run over the whole cluster
+    cfg = workload(name="ties_long", lens=(20000,), n_q=8, n_kv=2, H=256, budget=300, n_recent=64,
+                   cap=20000)
+    run = ScoreRun(cfg)
+    run.K[:, :, :20000] = run.K[:, :, :1]
+    gq, gs, gsel, glen, gK = run.call(0, 0)
+    expect = list(range(4 + 232)) + list(range(20000 - 64, 20000))
+    for g in range(2):
+        assert gsel[0, g].tolist() == expect
+    assert run.status() == 0
+
+
 def test_score_select_append_grows_len_and_switches_from_select_all():
     # phase-A shape in miniature: len 120 -> 123 with budget 121
     cfg = workload(name="append", lens=(120, 118), B=2, n_q=8, n_kv=2, H=256, budget=121, steps=3,
