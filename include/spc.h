@@ -278,6 +278,17 @@ int spc_host_device_pointer(void* host_ptr, void** device_ptr);
  * sink: uint32 [n_blocks]. src 16-byte aligned. */
 int spc_stream_read(const void* src, size_t bytes, uint32_t* sink, int n_blocks, void* stream);
 
+/* Copies `bytes` from `src` to `dst` with a kernel (no copy engine): either
+ * address may be device memory or the device-visible address of mapped
+ * pinned host memory (spc_host_device_pointer). The pages have no
+ * counterpart; it is the host I/O of a decode loop captured in a CUDA graph,
+ * where a copy-engine transfer to or from host memory inside the graph stalled
+ * every step, while this kernel reads and writes the mapped memory directly.
+ * 16-byte aligned addresses move in 16-byte words; any other bytes move one
+ * at a time. Up to 16 CTAs of 256 threads, so it leaves the GPU to the other
+ * streams. src and dst must not overlap. */
+int spc_copy(void* dst, const void* src, size_t bytes, void* stream);
+
 /* Number of streaming multiprocessors of the current device (0 on error). */
 int spc_device_sm_count(void);
 

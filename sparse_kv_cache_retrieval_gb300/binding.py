@@ -48,6 +48,7 @@ SIGNATURES = {
                                             _P, _P]),
     "spc_host_device_pointer": (_I, [_P, ctypes.POINTER(ctypes.c_void_p)]),
     "spc_stream_read": (_I, [_P, ctypes.c_size_t, _P, _I, _P]),
+    "spc_copy": (_I, [_P, _P, ctypes.c_size_t, _P]),
 }
 
 
@@ -184,6 +185,11 @@ def spc_host_device_pointer(host) -> int:
 def spc_stream_read(src, nbytes, sink, n_blocks, stream=None) -> None:
     _check("spc_stream_read", lib().spc_stream_read(_ptr(src), nbytes, _ptr(sink), n_blocks,
                                                     _stream(stream)))
+
+
+def spc_copy(dst, src, nbytes, stream=None) -> None:
+    """Kernel copy between device memory and device-visible host addresses."""
+    _check("spc_copy", lib().spc_copy(_ptr(dst), _ptr(src), int(nbytes), _stream(stream)))
 
 
 def spc_device_sm_count() -> int:

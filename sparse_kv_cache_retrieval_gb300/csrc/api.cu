@@ -51,13 +51,47 @@ __global__ void __launch_bounds__(512) stream_read_kernel(const uint4* __restric
   }
 }
 
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Plain loads and stores (no read-only path): the host side of a mapped
+// buffer may change between launches.
+__global__ void __launch_bounds__(256) copy_kernel(uint8_t* __restrict__ dst, const uint8_t* __restrict__ src,
+                                                   size_t bytes, int vec) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  const size_t t = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  size_t done = 0;
+  if (vec) {
+    const size_t n16 = bytes / 16;
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+    size_t i = t;
+    for (; i + 3 * stride < n16; i += 4 * stride) {
+      const uint4 a = s4[i], b = s4[i + stride], c = s4[i + 2 * stride], d = s4[i + 3 * stride];
+      d4[i] = a; d4[i + stride] = b; d4[i + 2 * stride] = c; d4[i + 3 * stride] = d;
+    }
+    for (; i < n16; i += stride) d4[i] = s4[i];
+    done = n16 * 16;
+  }
+  for (size_t j = done + t; j < bytes; j += stride) dst[j] = src[j];
+}
+
+int copy_launch(void* dst, const void* src, size_t bytes, void* stream) {
+  const bool vec = aligned16(dst) && aligned16(src);
+  const size_t units = vec ? bytes / 16 : bytes;
+  size_t grid = (units + 256 * 4 - 1) / (256 * 4);
+  if (grid > 16) grid = 16;
+  if (grid < 1) grid = 1;
+  copy_kernel<<<(unsigned)grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<uint8_t*>(dst), static_cast<const uint8_t*>(src), bytes, vec ? 1 : 0);
+  return cudaGetLastError() == cudaSuccess ? SPC_OK : SPC_ERR_CUDA;
+}
+
 int stream_read_launch(const void* src, size_t bytes, uint32_t* sink, int n_blocks, void* stream) {
   stream_read_kernel<<<n_blocks, 512, 0, static_cast<cudaStream_t>(stream)>>>(
       static_cast<const uint4*>(src), bytes / 16, sink);
   return cudaGetLastError() == cudaSuccess ? SPC_OK : SPC_ERR_CUDA;
 }
 
-static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 static bool group_ok(int n_q, int n_kv) {
   if (n_q < 1 || n_kv < 1 || n_q % n_kv) return false;
   const int G = n_q / n_kv;
@@ -197,6 +231,12 @@ int spc_host_device_pointer(void* host_ptr, void** device_ptr) {
   }
   *device_ptr = p;
   return SPC_OK;
+}
+
+int spc_copy(void* dst, const void* src, size_t bytes, void* stream) {
+  if (bytes == 0) return SPC_OK;
+  if (!dst || !src) return SPC_ERR_INVALID_ARG;
+  return copy_launch(dst, src, bytes, stream);
 }
 
 int spc_stream_read(const void* src, size_t bytes, uint32_t* sink, int n_blocks, void* stream) {

@@ -93,7 +93,11 @@ class DecodePipeline:
         self.load_slot = i32(2, B, n_kv, K)
         self.load_pos = i32(2, B, n_kv, K)
         self.n_load = i32(2, B, n_kv)
-        self.out = torch.zeros(L, B, self.n_q, d, dtype=torch.float32, device=dev)
+        # attention output, double-buffered by step parity (the copy of step t's
+        # output to the host may still run while step t+1 writes); `out` is the
+        # buffer of the step issued last
+        self.out_buf = torch.zeros(2, L, B, self.n_q, d, dtype=torch.float32, device=dev)
+        self.out = self.out_buf[0]
 
         # LLM KV: HBM full caches, pinned host stores, HBM slots
         self.hbm: List[Optional[torch.Tensor]] = []
@@ -165,6 +169,14 @@ class DecodePipeline:
         self.e_attn = [torch.cuda.Event() for _ in self.chunks]
         self.e_gath = [torch.cuda.Event() for _ in self.chunks]
         self._gather_pending = [False] * len(self.chunks)
+        # host I/O: H2D of the LLM queries one step ahead (stream H), D2H of
+        # each step's output and selection (stream D), per parity events
+        self.sH = torch.cuda.Stream(device=dev, priority=hi)
+        self.sD = torch.cuda.Stream(device=dev, priority=lo)
+        self.e_q = [torch.cuda.Event(), torch.cuda.Event()]
+        self.e_attn_end = [torch.cuda.Event(), torch.cuda.Event()]
+        self.e_d2h = [torch.cuda.Event(), torch.cuda.Event()]
+        self._reset_io_state()
 
         self.host_io = False
         if host_io:
@@ -187,11 +199,17 @@ class DecodePipeline:
             return 0, 0
         return hi, lo
 
+    def _reset_io_state(self) -> None:
+        self._q_issued = None                 # step whose query copy is in flight
+        self._attn_end_rec = [False, False]   # e_attn_end[parity] recorded in this run
+        self._d2h_pending = [False, False]    # e_d2h[parity] recorded in this run
+
     def enable_host_io(self) -> None:
         """Switch to end-to-end mode: every step copies its head input and LLM
         queries from pinned host memory and copies its attention output and
-        selection back to pinned host memory (the head input on stream C, the
-        rest on stream A)."""
+        selection back to pinned host memory. The head input goes with the
+        front (stream C); the queries of step t+1 are copied while step t runs
+        (stream H, double-buffered); outputs go back on stream D."""
         if self.host_io:
             return
         inputs, B, L, d, dev = self.inp, self.B, self.L, self.d, self.dev
@@ -199,9 +217,20 @@ class DecodePipeline:
         self.x_host = torch.from_numpy(inputs.x.view(np.int16).copy()).pin_memory()
         self.q_host = torch.from_numpy(np.ascontiguousarray(inputs.q_llm[:, :L]).view(np.int16)).pin_memory()
         self.x_stage = torch.empty(B, self.H, dtype=torch.int16, device=dev)
-        self.q_stage = torch.empty(L, B, self.n_q, d, dtype=torch.int16, device=dev)
+        self.q_stage = torch.empty(2, L, B, self.n_q, d, dtype=torch.int16, device=dev)
         self.out_host = torch.empty((n_steps, L, B, self.n_q, d), dtype=torch.float32).pin_memory()
         self.sel_host = torch.empty((n_steps, B, self.n_kv, self.K), dtype=torch.int32).pin_memory()
+        # transfers run as libspc copy kernels on the device-visible addresses
+        # of the pinned buffers (a copy-engine transfer to or from host memory
+        # inside a CUDA graph stalled every step)
+        self._x_bytes = B * self.H * 2
+        self._q_bytes = L * B * self.n_q * d * 2
+        self._out_bytes = L * B * self.n_q * d * 4
+        self._sel_bytes = B * self.n_kv * self.K * 4
+        self._x_dev_host = spc.spc_host_device_pointer(self.x_host)
+        self._q_dev_host = spc.spc_host_device_pointer(self.q_host)
+        self._out_dev_host = spc.spc_host_device_pointer(self.out_host)
+        self._sel_dev_host = spc.spc_host_device_pointer(self.sel_host)
         self.host_io = True
 
     # ------------------------------------------------------------------ pieces
@@ -221,11 +250,11 @@ class DecodePipeline:
         spc.spc_gather_kv(self.gviews, l0, l1, self.load_slot[pn], self.load_pos[pn], self.n_load[pn],
                           self.B, self.n_kv, self.d, self.cap, self.K, stream=stream)
 
-    def _attn(self, q_layers, p, l0, l1, stream):
+    def _attn(self, q_layers, out, p, l0, l1, stream):
         views = self.aviews.data_ptr() + l0 * self.aview_stride
         spc.spc_sparse_decode_attn(q_layers[l0].data_ptr(), views, self.selected[p], self.slot_pos[p],
                                    l1 - l0, self.B, self.n_q, self.n_kv, self.d, self.K, self.scale,
-                                   self.out[l0].data_ptr(), self.ws_attn, stream=stream)
+                                   out[l0].data_ptr(), self.ws_attn, stream=stream)
 
     def _timing_event(self):
         # Inside a capture a timing event must be an external record node.
@@ -273,8 +302,7 @@ class DecodePipeline:
             sC.wait_stream(self.sA)
         pn = (t + 1) % 2
         if self.host_io:
-            with torch.cuda.stream(sC):
-                self.x_stage.copy_(self.x_host[t + 1], non_blocking=True)
+            spc.spc_copy(self.x_stage, self._x_dev_host + (t + 1) * self._x_bytes, self._x_bytes, stream=sC)
             x = self.x_stage
         else:
             x = self.x_dev[t + 1]
@@ -286,45 +314,75 @@ class DecodePipeline:
         self.e_front.record(sC)
         self._front_issued = t
 
+    def _q_copy(self, t: int) -> None:
+        """H2D copy of the LLM queries of step t into q_stage[t % 2] on stream
+        H, after the attention of step t-2 (the buffer's last reader)."""
+        sH, par = self.sH, t % 2
+        if self._attn_end_rec[par]:
+            sH.wait_event(self.e_attn_end[par])
+        else:
+            sH.wait_stream(self.sA)
+        spc.spc_copy(self.q_stage[par], self._q_dev_host + t * self._q_bytes, self._q_bytes, stream=sH)
+        self.e_q[par].record(sH)
+        self._q_issued = t
+
     def step(self, t: int) -> None:
         """Issue decode step t (uses inputs x[t+1] and q_llm[t])."""
         sA = self.sA
         p, pn = t % 2, (t + 1) % 2
         append = 1 if self.cfg.append else 0
+        lookahead = self._range_end is not None and t + 1 < self._range_end
         if self._front_issued != t:
             self._front(t)
+        if self.host_io and self._q_issued != t:
+            self._q_copy(t)
         sA.wait_event(self.e_front)
         if self.host_io:
-            with torch.cuda.stream(sA):
-                self.q_stage.copy_(self.q_host[t], non_blocking=True)
-            q_layers = self.q_stage
+            if self._d2h_pending[p]:
+                # step t-2's copies still read selected[pn] and out_buf[p]
+                sA.wait_event(self.e_d2h[p])
+            sA.wait_event(self.e_q[p])
+            q_layers = self.q_stage[p]
         else:
             q_layers = self.q_dev[t]
+        out_t = self.out_buf[p]
+        self.out = out_t
         # the select stage reads only the front's scratch; x is not used
         self._timed_call("select", sA, lambda: self._score_select(self.x_dev[0], self.selected[pn], append, sA, 4))
         self.e_sel.record(sA)
-        if self._range_end is not None and t + 1 < self._range_end and t + 2 < len(self.inp.x):
+        if lookahead and t + 2 < len(self.inp.x):
             self._front(t + 1)
         self._timed_call("diff", sA, lambda: self._diff(pn, p, sA))
         for c, (l0, l1) in enumerate(self.chunks):
             if self._gather_pending[c]:
                 sA.wait_event(self.e_gath[c])
-            self._timed_call("attention", sA, lambda: self._attn(q_layers, p, l0, l1, sA))
+            self._timed_call("attention", sA, lambda: self._attn(q_layers, out_t, p, l0, l1, sA))
             self.e_attn[c].record(sA)
             sg = self.sBs[c % 2]
             sg.wait_event(self.e_attn[c])
             self._timed_call("gather", sg, lambda: self._gather(pn, l0, l1, sg))
             self.e_gath[c].record(sg)
             self._gather_pending[c] = True
+        self.e_attn_end[p].record(sA)
+        self._attn_end_rec[p] = True
         if self.host_io:
-            with torch.cuda.stream(sA):
-                self.out_host[t].copy_(self.out, non_blocking=True)
-                self.sel_host[t].copy_(self.selected[pn], non_blocking=True)
+            if lookahead and t + 1 < self.n_steps:
+                self._q_copy(t + 1)
+            sD = self.sD
+            sD.wait_event(self.e_attn_end[p])
+            spc.spc_copy(self._out_dev_host + t * self._out_bytes, out_t, self._out_bytes, stream=sD)
+            spc.spc_copy(self._sel_dev_host + t * self._sel_bytes, self.selected[pn], self._sel_bytes, stream=sD)
+            self.e_d2h[p].record(sD)
+            self._d2h_pending[p] = True
+
+    def _side_streams(self):
+        return self.sBs + [self.sC, self.sH, self.sD]
 
     def join(self) -> None:
-        for sg in self.sBs + [self.sC]:
+        for sg in self._side_streams():
             self.sA.wait_stream(sg)
         self._front_issued = None
+        self._reset_io_state()
 
     def run(self, t0: int, n: int) -> None:
         self._range_end = t0 + n
@@ -348,9 +406,10 @@ class DecodePipeline:
         self._capturing = True
         try:
             with torch.cuda.graph(g, stream=self.sA):
-                for sg in self.sBs + [self.sC]:
+                for sg in self._side_streams():
                     sg.wait_stream(self.sA)
                 self._front_issued = None
+                self._reset_io_state()
                 self._range_end = t0 + n
                 for t in range(t0, t0 + n):
                     self.step(t)
