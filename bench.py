@@ -47,6 +47,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="cfg2")
     ap.add_argument("--layers-per-launch", type=int, default=16)
+    ap.add_argument("--gather-streams", type=int, default=2, choices=[1, 2])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-sample-steps", type=int, default=2)
@@ -175,6 +176,64 @@ def host_link_peak(pipe, spc, torch):
     return best_zc, best_ce
 
 
+def isolated_times(pipe, spc, torch, t_last: int, reps: int = 20) -> dict:
+    """Each kernel of one step timed alone, in the launch configuration the
+    step uses: a CUDA graph of `reps` (L2 flush, kernel) pairs on stream A,
+    minus a graph of the flushes alone, divided by `reps`. The flush streams a
+    256 MiB device buffer (twice the L2), so every launch reads from DRAM or
+    over the host link. Repeats the calls of the last decode step issued
+    (t_last) on the state it left, so the selection, slot map and load lists
+    are those of a steady-state step and every timed call is idempotent."""
+    sA = pipe.sA
+    flush = torch.ones(256 << 20, dtype=torch.uint8, device=pipe.dev)
+    n_sink = spc.spc_device_sm_count() * 2
+    fsink = torch.zeros(n_sink, dtype=torch.int32, device=pipe.dev)
+    p, pn = t_last % 2, (t_last + 1) % 2
+    x = pipe.x_dev[t_last + 1]
+    l0, l1 = pipe.chunks[0]
+    calls = {
+        "project": lambda: pipe._score_select(x, pipe.selected[pn], 0, sA, 1),
+        "key_scan": lambda: pipe._score_select(x, pipe.selected[pn], 0, sA, 2),
+        "select": lambda: pipe._score_select(x, pipe.selected[pn], 0, sA, 4),
+        "diff": lambda: pipe._diff(pn, p, sA),
+        "attention": lambda: pipe._attn(pipe.q_dev[t_last], pipe.out_buf[p], p, l0, l1, sA),
+        "gather": lambda: pipe._gather(pn, l0, l1, sA),
+    }
+
+    def graph(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=sA):
+            for _ in range(reps):
+                spc.spc_stream_read(flush, flush.numel(), fsink, n_sink, stream=sA)
+                if fn is not None:
+                    fn()
+        return g
+
+    def replay(g, n=5):
+        ts = []
+        for _ in range(n):
+            torch.cuda.synchronize()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(sA):
+                s.record(sA)
+                g.replay()
+                e.record(sA)
+            torch.cuda.synchronize()
+            ts.append(s.elapsed_time(e) * 1e3)
+        return statistics.median(ts[1:])
+
+    t_flush = replay(graph(None))
+    out = {}
+    for name, fn in calls.items():
+        with torch.cuda.stream(sA):
+            fn()
+        torch.cuda.synchronize()
+        out[name] = max(0.0, (replay(graph(fn)) - t_flush) / reps)
+    n_rows = int(pipe.n_load[pn].sum().item())
+    del flush
+    return {"us": out, "gather_rows": n_rows, "gather_layers": l1 - l0, "attn_layers": l1 - l0}
+
+
 def hbm_read_peak(spc, torch):
     """Streaming read of a 2 GiB device buffer with the same 16-byte load kernel."""
     n = 2 << 30
@@ -287,14 +346,26 @@ def our_arm(args, rank, world, local):
     log("generating inputs")
     inp = make_inputs(cfg, steps=W + K + 1)
     log("allocating and filling the pinned host store")
-    pipe = DecodePipeline(cfg, inp, layers_per_launch=args.layers_per_launch, timing=False)
+    pipe = DecodePipeline(cfg, inp, layers_per_launch=args.layers_per_launch, timing=False,
+                          gather_streams=args.gather_streams)
     log("pipeline ready")
     if args.profile:
+        # the launch sequence a profiler sees: the prologue (one whole-selection
+        # gather), then per step proj, scan, select, diff and per layer chunk
+        # attention + gather; the rows each step's gathers move are read back
+        # with plain copies (no kernel), so the units of a captured launch are known
         pipe.prologue()
-        pipe.run(0, K)
+        rows = []
+        for t in range(K):
+            pipe.step(t)
+            pipe.join()
+            torch.cuda.synchronize()
+            rows.append(int(pipe.n_load[(t + 1) % 2].cpu().numpy().astype(np.int64).sum()))
         torch.cuda.synchronize()
         print(json.dumps({"profile_steps": K, "workload": cfg.name,
-                          "launches_per_step": 4 + 2 * len(pipe.chunks)}))
+                          "launches_per_step": 4 + 2 * len(pipe.chunks),
+                          "chunks": pipe.chunks, "gathered_rows_per_kv_per_layer": rows,
+                          "scan_positions": [int(v) for v in pipe.len.cpu().numpy()]}))
         return
 
     # ---- every kernel runs once outside capture (first calls set kernel
@@ -420,6 +491,22 @@ def our_arm(args, rank, world, local):
     for k in ("project", "select", "diff"):
         if k in kern:
             kinfo[k] = {"mean_us": round(kern[k]["mean_us"], 2), "launches": kern[k]["launches"]}
+    # every kernel alone (L2 flushed before each launch), same launch shapes
+    log("isolated kernel timing")
+    iso = isolated_times(pipe, spc, torch, t_last=W + K - 1)
+    iso_bytes = {"key_scan": (scan_bytes, hbm_peak),
+                 "attention": (attn_bytes_per_layer * iso["attn_layers"], hbm_peak),
+                 "gather": (iso["gather_rows"] * iso["gather_layers"] * 2 * 256, zc_peak)}
+    for k, us in iso["us"].items():
+        r = kinfo.setdefault(k, {})
+        r["isolated_us"] = round(us, 2)
+        if k in iso_bytes:
+            nb, pk = iso_bytes[k]
+            a = gbs(nb, us)
+            r["isolated_achieved"] = round(a, 1)
+            r["isolated_frac"] = round(a / pk, 3) if pk else None
+            r["isolated_bytes"] = int(nb)
+    log("isolated: " + ", ".join(f"{k} {v:.1f} us" for k, v in iso["us"].items()))
     dominant = max(kern, key=lambda k: kern[k]["total_ms"]) if kern else None
     roof = None
     if dominant in ("gather", "key_scan", "attention"):
@@ -471,7 +558,7 @@ def our_arm(args, rank, world, local):
     if rank != 0:
         return
     config = describe(cfg)
-    config.update({"layers_per_launch": args.layers_per_launch,
+    config.update({"layers_per_launch": args.layers_per_launch, "gather_streams": args.gather_streams,
                    "l2": "inputs larger than L2: each step reads the 64 MiB key cache, 256 MiB of "
                          "slots and writes the gathered rows (> 129 MB L2)",
                    "graph": "CUDA graph per step range, two streams", "kernel_timing": timing_src})

@@ -26,7 +26,10 @@
 namespace spc {
 
 constexpr int kGatherThreads = 512;
-constexpr int kGatherUnroll = 4;
+#ifndef SPC_GATHER_UNROLL
+#define SPC_GATHER_UNROLL 4
+#endif
+constexpr int kGatherUnroll = SPC_GATHER_UNROLL;
 constexpr int kGatherMaxSeg = 1024;
 #ifndef SPC_GATHER_SMS_PER_CTA
 #define SPC_GATHER_SMS_PER_CTA 8

@@ -300,8 +300,8 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
       break;
     }
     const uint32_t base = smem_u32(scan_smem + (size_t)s * kScanTileBytes);
-    float* lg_lo = a.logits + ((size_t)b * a.n_q + (size_t)g * G + h_lo) * a.lstride + row0;
-    float* lg_hi = a.logits + ((size_t)b * a.n_q + (size_t)g * G + h_hi) * a.lstride + row0;
+    // logits are position-major: [segment][position][G]
+    float* lg = a.logits + ((size_t)seg * a.lstride + row0) * G;
     float m_lo = -INFINITY, s_lo = 0.f, m_hi = -INFINITY, s_hi = 0.f;
 #pragma unroll 1
     for (int sb = 0; sb < S::RW / 32; ++sb) {
@@ -337,12 +337,12 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
         if (!v0) acc[n][0] = acc[n][2] = -INFINITY;
         if (!v1) acc[n][1] = acc[n][3] = -INFINITY;
         if (h_lo < G) {
-          if (v1) *reinterpret_cast<float2*>(lg_lo + key) = make_float2(acc[n][0], acc[n][1]);
-          else if (v0) lg_lo[key] = acc[n][0];
+          if (v0) lg[(size_t)key * G + h_lo] = acc[n][0];
+          if (v1) lg[(size_t)(key + 1) * G + h_lo] = acc[n][1];
         }
         if (h_hi < G) {
-          if (v1) *reinterpret_cast<float2*>(lg_hi + key) = make_float2(acc[n][2], acc[n][3]);
-          else if (v0) lg_hi[key] = acc[n][2];
+          if (v0) lg[(size_t)key * G + h_hi] = acc[n][2];
+          if (v1) lg[(size_t)(key + 1) * G + h_hi] = acc[n][3];
         }
         bm_lo = fmaxf(bm_lo, fmaxf(acc[n][0], acc[n][1]));
         bm_hi = fmaxf(bm_hi, fmaxf(acc[n][2], acc[n][3]));
@@ -375,6 +375,186 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
       const size_t pi = (size_t)tile * S::PPT + rs;
       if (h_lo < G) a.part[((size_t)b * a.n_q + (size_t)g * G + h_lo) * a.n_parts + pi] = make_float2(m_lo, s_lo);
       if (h_hi < G) a.part[((size_t)b * a.n_q + (size_t)g * G + h_hi) * a.n_parts + pi] = make_float2(m_hi, s_hi);
+    }
+    ++it;
+  }
+}
+
+// Key-major tensor-core scan for groups of up to 8 query heads. The key rows
+// are the M side of m16n8k16 (16 keys x 16 dims per ldmatrix.x4 from the
+// swizzled tile); the N side holds the group's queries twice, the bf16 high
+// parts in columns [0, HALF) and the low parts in [HALF, 2*HALF), HALF =
+// max(4, G), so one product yields both halves and their sum is q.K with
+// about 16 significant bits in q. Per 128-key tile each of 8 consumer warps
+// takes 16 keys: 8 (G <= 4) or 16 (G = 8) MMAs, two accumulator chains over
+// the halves of the head dimension. The tile's stage is released as soon as
+// its last fragment is in registers.
+constexpr int kScanKmWarps = 8;
+constexpr int kScanKmThreads = (kScanKmWarps + 1) * 32;
+
+template <int G>
+struct ScanKmShape {
+  static constexpr int HALF = G < 4 ? 4 : G;   // columns per half (high / low)
+  static constexpr int NT = 2 * HALF / 8;      // n-tiles of 8 columns
+  static constexpr int PPT = kScanKmWarps;     // logsumexp partials per tile per head
+};
+
+template <int G>
+__global__ void __launch_bounds__(kScanKmThreads) scan_kernel_km(ScanArgs a) {
+  static_assert(G <= 8, "key-major scan serves groups of at most 8 heads");
+  using S = ScanKmShape<G>;
+  extern __shared__ __align__(128) uint8_t scan_smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(scan_smem + kScanStages * kScanTileBytes);
+  uint64_t* empty = full + kScanStages;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kScanStages; ++s) {
+      mbar_init(&full[s], 32);       // one cp.async arrival per producer lane
+      mbar_init(&empty[s], kScanKmWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int t_end = min(a.total_tiles, (blockIdx.x + 1) * a.tpc);
+
+  if (warp == kScanKmWarps) {
+    // ---------------- producer: as in scan_kernel (two rows per cp.async
+    // instruction, piece p of row r stored at p ^ (r & 7), tail zero-filled)
+    const int piece = lane & 15, half = lane >> 4;
+    int it = 0;
+    for (int t = blockIdx.x * a.tpc; t < t_end; ++t) {
+      const int seg = t / a.n_tiles, tile = t - seg * a.n_tiles;
+      const int b = seg / a.n_kv;
+      const int L = effective_len(a.len, b, a.append, a.cap);
+      const int row0 = tile * kScanRows;
+      if (row0 >= L) continue;
+      const int nrows = min(kScanRows, L - row0);
+      const int s = it % kScanStages;
+      const uint32_t ph = (it / kScanStages) & 1;
+      if (!mbar_wait_bounded(&empty[s], ph ^ 1, kWaitLimit)) {
+        if (lane == 0) set_status(a.status, SPC_ERR_TIMEOUT);
+        break;
+      }
+      uint8_t* dst = scan_smem + (size_t)s * kScanTileBytes;
+      const uint16_t* src = a.K + ((size_t)seg * a.cap + row0) * kD + piece * 8;
+#pragma unroll 8
+      for (int j = 0; j < kScanRows / 2; ++j) {
+        const int r = 2 * j + half;
+        const bool ok = r < nrows;
+        cp_async16(dst + r * kRowBytes + ((piece ^ (r & 7)) << 4), src + (size_t)(ok ? r : 0) * kD, ok ? 16 : 0);
+      }
+      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(smem_u32(&full[s])) : "memory");
+      ++it;
+    }
+    for (int k = max(0, it - kScanStages); k < it; ++k)
+      mbar_wait_bounded(&full[k % kScanStages], (k / kScanStages) & 1, kWaitLimit);
+    return;
+  }
+
+  // ---------------- consumers
+  const int gid = lane >> 2, tig = lane & 3, mi = lane >> 3, ri = lane & 7;
+  const int r0 = warp * 16;                       // this warp's 16 keys of a tile
+  const int hA = 2 * tig, hB = hA + 1;            // heads of this lane's C columns
+  uint32_t qb[8][S::NT][2];                       // B fragments: q high / low, per k-step
+  int cur_seg = -1;
+  int it = 0;
+  for (int t = blockIdx.x * a.tpc; t < t_end; ++t) {
+    const int seg = t / a.n_tiles, tile = t - seg * a.n_tiles;
+    const int b = seg / a.n_kv, g = seg - b * a.n_kv;
+    const int L = effective_len(a.len, b, a.append, a.cap);
+    const int row0 = tile * kScanRows;
+    if (row0 >= L) continue;
+    const int nrows = min(kScanRows, L - row0);
+    const int s = it % kScanStages;
+    const uint32_t ph = (it / kScanStages) & 1;
+    if (seg != cur_seg) {
+      const float* qg = a.q + ((size_t)b * a.n_q + (size_t)g * G) * kD;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+#pragma unroll
+        for (int nt = 0; nt < S::NT; ++nt) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int col = nt * 8 + gid;
+            const bool low = col >= S::HALF;
+            const int h = low ? col - S::HALF : col;
+            const int k = ks * 16 + tig * 2 + e * 8;
+            float2 v = make_float2(0.f, 0.f);
+            if (h < G) v = *reinterpret_cast<const float2*>(qg + (size_t)h * kD + k);
+            const float x = v.x * a.qscale, y = v.y * a.qscale;
+            const float xh = bf16_round(x), yh = bf16_round(y);
+            qb[ks][nt][e] = low ? pack_bf16(x - xh, y - yh) : pack_bf16(xh, yh);
+          }
+        }
+      }
+      cur_seg = seg;
+    }
+    if (!mbar_wait_bounded(&full[s], ph, kWaitLimit)) {
+      if (lane == 0) set_status(a.status, SPC_ERR_TIMEOUT);
+      break;
+    }
+    const uint32_t base = smem_u32(scan_smem + (size_t)s * kScanTileBytes);
+    float acc[2][S::NT][4];
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+#pragma unroll
+      for (int nt = 0; nt < S::NT; ++nt) acc[c][nt][0] = acc[c][nt][1] = acc[c][nt][2] = acc[c][nt][3] = 0.f;
+    const int row = r0 + ri + ((mi & 1) << 3);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const int piece = ks * 2 + (mi >> 1);
+      uint32_t af[4];
+      ldsm_x4(base + row * kRowBytes + ((piece ^ (row & 7)) << 4), af[0], af[1], af[2], af[3]);
+#pragma unroll
+      for (int nt = 0; nt < S::NT; ++nt) mma_bf16(acc[ks & 1][nt], af, qb[ks][nt][0], qb[ks][nt][1]);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+
+    // high + low halves: l[0], l[1] = key r0+gid, heads hA, hB; l[2], l[3] = key r0+gid+8
+    float l[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float v[S::NT];
+#pragma unroll
+      for (int nt = 0; nt < S::NT; ++nt) v[nt] = acc[0][nt][e] + acc[1][nt][e];
+      if constexpr (S::NT == 1) l[e] = v[0] + __shfl_xor_sync(0xffffffffu, v[0], 2);
+      else l[e] = v[0] + v[1];
+    }
+    const int k0 = r0 + gid, k1 = k0 + 8;
+    const bool v0 = k0 < nrows, v1 = k1 < nrows;
+    if (!v0) l[0] = l[1] = -INFINITY;
+    if (!v1) l[2] = l[3] = -INFINITY;
+    float* lg = a.logits + ((size_t)seg * a.lstride + row0) * G;   // [position][G]
+    if (hA < G) {
+      if constexpr (G == 1) {
+        if (v0) lg[k0] = l[0];
+        if (v1) lg[k1] = l[2];
+      } else {
+        if (v0) *reinterpret_cast<float2*>(lg + (size_t)k0 * G + hA) = make_float2(l[0], l[1]);
+        if (v1) *reinterpret_cast<float2*>(lg + (size_t)k1 * G + hA) = make_float2(l[2], l[3]);
+      }
+    }
+    // per-head (max, sum 2^(l - max)) over this warp's 16 keys
+    float mA = fmaxf(l[0], l[2]), mB = fmaxf(l[1], l[3]);
+#pragma unroll
+    for (int o = 4; o <= 16; o <<= 1) {
+      mA = fmaxf(mA, __shfl_xor_sync(0xffffffffu, mA, o));
+      mB = fmaxf(mB, __shfl_xor_sync(0xffffffffu, mB, o));
+    }
+    float sA = mA == -INFINITY ? 0.f : exp2f(l[0] - mA) + exp2f(l[2] - mA);
+    float sB = mB == -INFINITY ? 0.f : exp2f(l[1] - mB) + exp2f(l[3] - mB);
+#pragma unroll
+    for (int o = 4; o <= 16; o <<= 1) {
+      sA += __shfl_xor_sync(0xffffffffu, sA, o);
+      sB += __shfl_xor_sync(0xffffffffu, sB, o);
+    }
+    if (gid == 0) {
+      const size_t pi = (size_t)tile * S::PPT + warp;
+      float2* pp = a.part + ((size_t)b * a.n_q + (size_t)g * G) * a.n_parts + pi;
+      if (hA < G) pp[(size_t)hA * a.n_parts] = make_float2(mA, sA);
+      if (hB < G) pp[(size_t)hB * a.n_parts] = make_float2(mB, sB);
     }
     ++it;
   }
@@ -540,21 +720,27 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a) {
   const int t0 = p_lo + tid * a.cpt;
   const int t1 = min(p_end, t0 + a.cpt);
   uint32_t* kb = a.slice <= kSelSmemKeys ? sm.keys : a.keys + (size_t)seg * a.kstride + p_lo;
-  const float* lg = a.logits + ((size_t)b * a.n_q + (size_t)g * G) * a.lstride;
-  constexpr int HC = G < 8 ? G : 8;   // heads whose loads are in flight together
+  // logits are position-major ([position][G]): 4 positions are 4*G
+  // consecutive floats, read as G float4 loads
+  const float* lg = a.logits + (size_t)seg * a.lstride * G;
+  constexpr int HC = G < 8 ? G : 8;   // float4 loads in flight together
   for (int p = t0; p < t1; p += 4) {
     float sc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-    for (int h0 = 0; h0 < G; h0 += HC) {
+    const float4* l4 = reinterpret_cast<const float4*>(lg + (size_t)p * G);
+#pragma unroll
+    for (int c0 = 0; c0 < G; c0 += HC) {
       float4 v[HC];
 #pragma unroll
-      for (int h = 0; h < HC; ++h) v[h] = __ldcg(reinterpret_cast<const float4*>(lg + (size_t)(h0 + h) * a.lstride + p));
+      for (int c = 0; c < HC; ++c) v[c] = __ldcg(l4 + c0 + c);
 #pragma unroll
-      for (int h = 0; h < HC; ++h) {
-        const float l = sm.lse[h0 + h];
-        sc[0] = fmaxf(sc[0], v[h].x - l);
-        sc[1] = fmaxf(sc[1], v[h].y - l);
-        sc[2] = fmaxf(sc[2], v[h].z - l);
-        sc[3] = fmaxf(sc[3], v[h].w - l);
+      for (int c = 0; c < HC; ++c) {
+        const float f[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int flat = (c0 + c) * 4 + e;      // position p + flat / G, head flat % G
+          const int j = flat / G, h = flat - j * G;
+          sc[j] = fmaxf(sc[j], f[e] - sm.lse[h]);
+        }
       }
     }
     uint32_t key[4] = {0u, 0u, 0u, 0u};
@@ -769,7 +955,9 @@ struct ScoreLayout {
   int n_tiles, ppt, n_parts, lstride;
 };
 
-static int scan_ppt(int G) { return kScanCWarps / (G <= 16 ? 1 : G / 16); }
+static int scan_ppt(int G) {
+  return G <= 8 ? kScanKmWarps : kScanCWarps / (G <= 16 ? 1 : G / 16);
+}
 
 static ScoreLayout score_layout(int B, int H, int n_q, int n_kv, int cap) {
   ScoreLayout l{};
@@ -795,16 +983,27 @@ size_t score_select_workspace(int B, int H, int n_q, int n_kv, int cap) {
   return score_layout(B, H, n_q, n_kv, cap).total;
 }
 
+// Groups of up to 8 heads take the key-major kernel, larger ones the
+// head-major one.
 template <int G>
 static cudaError_t launch_scan(const ScanArgs& sa, int grid, cudaStream_t st) {
   const size_t smem = kScanStages * kScanTileBytes + 2 * kScanStages * sizeof(uint64_t);
   static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(scan_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr = true;
+  if constexpr (G <= 8) {
+    if (!attr) {
+      cudaError_t e = cudaFuncSetAttribute(scan_kernel_km<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      attr = true;
+    }
+    scan_kernel_km<G><<<grid, kScanKmThreads, smem, st>>>(sa);
+  } else {
+    if (!attr) {
+      cudaError_t e = cudaFuncSetAttribute(scan_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      attr = true;
+    }
+    scan_kernel<G><<<grid, kScanThreads, smem, st>>>(sa);
   }
-  scan_kernel<G><<<grid, kScanThreads, smem, st>>>(sa);
   return cudaGetLastError();
 }
 

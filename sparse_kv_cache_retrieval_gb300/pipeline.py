@@ -58,7 +58,8 @@ class DecodePipeline:
 
     def __init__(self, cfg: Workload, inputs: Inputs, *, device: str = "cuda",
                  n_layers: Optional[int] = None, layers_per_launch: int = 16,
-                 host_io: bool = False, timing: bool = False, fill_threads: Optional[int] = None):
+                 host_io: bool = False, timing: bool = False, fill_threads: Optional[int] = None,
+                 gather_streams: int = 2):
         self.cfg = cfg
         self.inp = inputs
         self.dev = torch.device(device)
@@ -158,9 +159,14 @@ class DecodePipeline:
         hi, lo = self._priorities()
         self.sA = torch.cuda.Stream(device=dev, priority=hi)
         self.sB = torch.cuda.Stream(device=dev, priority=hi)
-        # gathers of consecutive layer chunks alternate over two streams so
-        # that one launch's ramp-down overlaps the next one's ramp-up
-        self.sBs = [self.sB, torch.cuda.Stream(device=dev, priority=hi)]
+        # gathers of consecutive layer chunks alternate over `gather_streams`
+        # streams: with two, one launch's ramp-down overlaps the next one's
+        # ramp-up; with one, the gathers never share the host link, so each
+        # chunk's rows land as early as the link allows
+        if gather_streams not in (1, 2):
+            raise ValueError("gather_streams must be 1 or 2")
+        self.sBs = [self.sB] + [torch.cuda.Stream(device=dev, priority=hi)
+                                for _ in range(gather_streams - 1)]
         self.sC = torch.cuda.Stream(device=dev, priority=lo)
         self.e_front = torch.cuda.Event()
         self.e_sel = torch.cuda.Event()
@@ -358,7 +364,7 @@ class DecodePipeline:
                 sA.wait_event(self.e_gath[c])
             self._timed_call("attention", sA, lambda: self._attn(q_layers, out_t, p, l0, l1, sA))
             self.e_attn[c].record(sA)
-            sg = self.sBs[c % 2]
+            sg = self.sBs[c % len(self.sBs)]
             sg.wait_event(self.e_attn[c])
             self._timed_call("gather", sg, lambda: self._gather(pn, l0, l1, sg))
             self.e_gath[c].record(sg)

@@ -39,6 +39,8 @@ SMALL = [
     ("g2", dict(lens=(640,), n_q=8, n_kv=4, H=256, budget=80)),
     ("g8", dict(lens=(900,), n_q=16, n_kv=2, H=512, budget=100)),
     ("g16", dict(lens=(513,), n_q=16, n_kv=1, H=256, budget=72)),
+    ("g32", dict(lens=(1100,), n_q=32, n_kv=1, H=256, budget=90)),
+    ("g8_two_groups_ragged_tiles", dict(B=2, lens=(1025, 255), n_q=16, n_kv=2, H=256, budget=120)),
     ("mqa_g64", dict(lens=(1300,), n_q=64, n_kv=1, H=1024, budget=200)),
     ("ragged_batch", dict(B=3, lens=(1500, 129, 700), n_q=8, n_kv=2, H=256, budget=96)),
     ("batch17_over_16", dict(B=17, lens=tuple(200 + 37 * i for i in range(17)), n_q=8, n_kv=2, H=256,
