@@ -57,6 +57,10 @@ struct ProjArgs {
   int B, H, Nq, Nk, Ntot, n_kv, cap, S, Hc;
 };
 
+#ifndef SPC_PROJ_TC_MIN_BATCH
+#define SPC_PROJ_TC_MIN_BATCH 4   // batches of at least this many requests project on tensor cores
+#endif
+constexpr long long kWaitLimit = 4000000000ll;  // bounded mbarrier waits: clock cycles (~2 s)
 constexpr int kProjThreads = 256;
 constexpr int kProjTile = 128;
 constexpr int kProjMaxSplit = 16;
@@ -171,6 +175,161 @@ __global__ void __launch_bounds__(kProjThreads) proj_kernel(ProjArgs a) {
   cluster.sync();
 }
 
+// Tensor-core projection for batched head inputs: [x_b; ...] (16 requests,
+// zero-padded) times a 128-column tile of [W_q | W_k] on mma.sync m16n8k16
+// (bf16 operands, exact products, fp32 accumulation). A producer warp streams
+// 64-row slices of the weight tile (16 KiB) and the matching 64 columns of x
+// (2 KiB) into a 4-stage ring with cp.async, both XOR-swizzled by 16-byte
+// piece so ldmatrix reads are conflict-free; each of 4 consumer warps owns 32
+// columns. The splits over H of one column tile form a thread-block cluster
+// and meet in rank 0's shared memory in rank order, as in proj_kernel.
+constexpr int kPtcRows = 64;                          // hidden rows per stage
+constexpr int kPtcStages = 4;
+constexpr int kPtcWarps = 4;
+constexpr int kPtcThreads = (kPtcWarps + 1) * 32;
+constexpr uint32_t kPtcWBytes = kPtcRows * kProjTile * 2;   // 16 KiB of weights
+constexpr uint32_t kPtcXBytes = 16 * kPtcRows * 2;          // 2 KiB of x (16 rows x 128 B)
+constexpr uint32_t kPtcStageBytes = kPtcWBytes + kPtcXBytes;
+constexpr size_t kPtcSmem = (size_t)kPtcStages * kPtcStageBytes + sizeof(float) * 16 * kProjTile +
+                            2 * kPtcStages * sizeof(uint64_t);
+
+__global__ void __launch_bounds__(kPtcThreads) proj_tc_kernel(ProjArgs a) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  extern __shared__ __align__(128) uint8_t ptc_smem[];
+  const int split = (int)cluster.block_rank();
+  const int tile = blockIdx.x / a.S, b0 = blockIdx.z * 16;
+  const int col0 = tile * kProjTile;
+  const bool is_k = col0 >= a.Nq;
+  const uint16_t* W = is_k ? a.Wk : a.Wq;
+  const int ld = is_k ? a.Nk : a.Nq;
+  const int wcol0 = is_k ? col0 - a.Nq : col0;
+  const int r_begin = split * a.Hc;                       // a multiple of 8
+  const int nr = max(0, min(a.H, r_begin + a.Hc) - r_begin);   // a multiple of 8
+  const int n_chunks = (nr + kPtcRows - 1) / kPtcRows;
+
+  uint8_t* ring = ptc_smem;
+  float* red = reinterpret_cast<float*>(ring + kPtcStages * kPtcStageBytes);   // [16][128] partial
+  uint64_t* full = reinterpret_cast<uint64_t*>(red + 16 * kProjTile);
+  uint64_t* empty = full + kPtcStages;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPtcStages; ++s) {
+      mbar_init(&full[s], 32);
+      mbar_init(&empty[s], kPtcWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kPtcWarps) {
+    // ---------------- producer: per stage 64 weight rows of 256 bytes (two
+    // rows per cp.async instruction, piece p of row r at p ^ (r & 7)) and 16 x
+    // rows of 128 bytes (piece p of row r at p ^ (r & 7)); rows past the
+    // slice or the batch are zero-filled
+    const int piece = lane & 15, half = lane >> 4;
+    const uint16_t* src0 = W + (size_t)r_begin * ld + wcol0 + piece * 8;
+    for (int c = 0; c < n_chunks; ++c) {
+      const int s = c % kPtcStages;
+      const uint32_t ph = (c / kPtcStages) & 1;
+      if (!mbar_wait_bounded(&empty[s], ph ^ 1, kWaitLimit)) {
+        if (lane == 0) set_status(a.status, SPC_ERR_TIMEOUT);
+        break;
+      }
+      uint8_t* dst = ring + (size_t)s * kPtcStageBytes;
+#pragma unroll 8
+      for (int j = 0; j < kPtcRows / 2; ++j) {
+        const int r = 2 * j + half, rg = c * kPtcRows + r;
+        const bool ok = rg < nr;
+        cp_async16(dst + r * kRowBytes + ((piece ^ (r & 7)) << 4), src0 + (size_t)(ok ? rg : 0) * ld, ok ? 16 : 0);
+      }
+      uint8_t* xdst = dst + kPtcWBytes;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int idx = lane + 32 * i, xr = idx >> 3, xpc = idx & 7;
+        const int k = c * kPtcRows + xpc * 8;
+        const bool ok = b0 + xr < a.B && k < nr;
+        const uint16_t* xs = ok ? a.x + (size_t)(b0 + xr) * a.H + r_begin + k : a.x;
+        cp_async16(xdst + xr * (kPtcRows * 2) + ((xpc ^ (xr & 7)) << 4), xs, ok ? 16 : 0);
+      }
+      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(smem_u32(&full[s])) : "memory");
+    }
+    for (int c = max(0, n_chunks - kPtcStages); c < n_chunks; ++c)
+      mbar_wait_bounded(&full[c % kPtcStages], (c / kPtcStages) & 1, kWaitLimit);
+  } else {
+    // ---------------- consumers: warp w owns columns [32w, 32w + 32)
+    float acc[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    const int xr = lane & 15, xhi = lane >> 4;                 // A: x row and k-half this lane addresses
+    const int krow = (lane & 7) + (((lane >> 3) & 1) << 3);    // B: weight row within a 16-row k-step
+    const int npc = warp * 4 + (lane >> 4);                    // B: first 16-byte column piece
+    for (int c = 0; c < n_chunks; ++c) {
+      const int s = c % kPtcStages;
+      const uint32_t ph = (c / kPtcStages) & 1;
+      if (!mbar_wait_bounded(&full[s], ph, kWaitLimit)) {
+        if (lane == 0) set_status(a.status, SPC_ERR_TIMEOUT);
+        break;
+      }
+      const uint32_t wbase = smem_u32(ring + (size_t)s * kPtcStageBytes);
+      const uint32_t xbase = wbase + kPtcWBytes + xr * (kPtcRows * 2);
+#pragma unroll
+      for (int ks = 0; ks < kPtcRows / 16; ++ks) {
+        uint32_t af[4];
+        ldsm_x4(xbase + (((ks * 2 + xhi) ^ (xr & 7)) << 4), af[0], af[1], af[2], af[3]);
+        const int r = ks * 16 + krow;
+#pragma unroll
+        for (int pr = 0; pr < 2; ++pr) {
+          const int pc = npc + pr * 2;
+          uint32_t b00, b01, b10, b11;
+          ldsm_x4_t(wbase + r * kRowBytes + ((pc ^ (r & 7)) << 4), b00, b01, b10, b11);
+          mma_bf16(acc[2 * pr], af, b00, b01);
+          mma_bf16(acc[2 * pr + 1], af, b10, b11);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    // this split's partial: rows gid / gid + 8, columns 32w + 8nt + 2tig (+1)
+    const int gid = lane >> 2, tig = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      const int cc = warp * 32 + nt * 8 + tig * 2;
+      *reinterpret_cast<float2*>(red + gid * kProjTile + cc) = make_float2(acc[nt][0], acc[nt][1]);
+      *reinterpret_cast<float2*>(red + (gid + 8) * kProjTile + cc) = make_float2(acc[nt][2], acc[nt][3]);
+    }
+  }
+  cluster.sync();
+
+  if (split == 0) {
+    for (int i = threadIdx.x; i < 16 * kProjTile; i += kPtcThreads) {
+      const int bb = i / kProjTile, c = i - bb * kProjTile, b = b0 + bb;
+      if (b >= a.B) continue;
+      float v[kProjMaxSplit];
+#pragma unroll
+      for (int q = 0; q < kProjMaxSplit; ++q) v[q] = q < a.S ? *cluster.map_shared_rank(red + i, q) : 0.f;
+      float sum = 0.f;
+#pragma unroll
+      for (int q = 0; q < kProjMaxSplit; ++q) sum += v[q];
+      if (!is_k) {
+        a.q_ws[(size_t)b * a.Nq + col0 + c] = sum;
+        if (a.q_out) a.q_out[(size_t)b * a.Nq + col0 + c] = sum;
+      } else {
+        const int g = wcol0 / kD;
+        const int L = a.len[b];
+        if (L >= 0 && L < a.cap) {
+          const __nv_bfloat16 h = __float2bfloat16_rn(sum);
+          a.K_dlm[(((size_t)b * a.n_kv + g) * a.cap + L) * kD + c] = __bfloat16_as_ushort(h);
+        } else if (c == 0) {
+          set_status(a.status, SPC_ERR_OVERFLOW);
+        }
+      }
+    }
+  }
+  cluster.sync();
+}
+
 // ============================================================== key scan
 struct ScanArgs {
   const uint16_t* K;
@@ -187,12 +346,15 @@ constexpr int kScanRows = 128;
 constexpr int kScanCWarps = 4;
 constexpr int kScanThreads = (kScanCWarps + 1) * 32;
 constexpr int kScanStages = 3;
+// Tiles per CTA: 0 sizes the grid to one wave of kScanCtasPerSm CTAs per SM
+// (each CTA streams a run of consecutive tiles, so the kernel lasts as long
+// as its longest run); a positive value fixes the run length.
 #ifndef SPC_SCAN_TILES_PER_CTA
-#define SPC_SCAN_TILES_PER_CTA 8
+#define SPC_SCAN_TILES_PER_CTA 0
 #endif
 constexpr int kScanTilesPerCta = SPC_SCAN_TILES_PER_CTA;
+constexpr int kScanCtasPerSm = 2;   // the 3-stage ring (98 KB) allows two per SM
 constexpr uint32_t kScanTileBytes = kScanRows * kRowBytes;
-constexpr long long kWaitLimit = 4000000000ll;  // clock cycles (~2 s)
 
 // Warp roles of the tensor-core scan: NMT tiles of 16 query heads; the
 // NRS = 4 / NMT warps of a head tile split a key tile's rows (RW each); one
@@ -720,26 +882,54 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a) {
   const int t0 = p_lo + tid * a.cpt;
   const int t1 = min(p_end, t0 + a.cpt);
   uint32_t* kb = a.slice <= kSelSmemKeys ? sm.keys : a.keys + (size_t)seg * a.kstride + p_lo;
-  // logits are position-major ([position][G]): 4 positions are 4*G
-  // consecutive floats, read as G float4 loads
+  // logits are position-major ([position][G]): a group of 4 positions is 4*G
+  // consecutive floats, read as G float4 loads. Groups are dealt to threads
+  // round robin (a warp reads 32 consecutive groups), every thread runs the
+  // same number of rounds, and the histogram increments are aggregated over
+  // the lanes of a warp that hit the same bin (the keys of one context crowd
+  // into few bins).
   const float* lg = a.logits + (size_t)seg * a.lstride * G;
   constexpr int HC = G < 8 ? G : 8;   // float4 loads in flight together
-  for (int p = t0; p < t1; p += 4) {
+  const int n_grp = p_end > p_lo ? (p_end - p_lo + 3) >> 2 : 0;
+  const int n_rounds = (n_grp + kSelThreads - 1) / kSelThreads;
+  // groups of up to 8 heads: the next round's loads are issued before the
+  // current ones are used
+  constexpr int NPF = G <= 8 ? G : 1;
+  float4 pf[NPF];
+  if (G <= 8 && tid < n_grp) {
+#pragma unroll
+    for (int c = 0; c < NPF; ++c) pf[c] = __ldcg(reinterpret_cast<const float4*>(lg + (size_t)(p_lo + 4 * tid) * G) + c);
+  }
+  for (int rd = 0; rd < n_rounds; ++rd) {
+    const int gi = rd * kSelThreads + tid;
+    const bool gv = gi < n_grp;
+    const int p = p_lo + 4 * gi;
     float sc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-    const float4* l4 = reinterpret_cast<const float4*>(lg + (size_t)p * G);
+    if (gv) {
+      const float4* l4 = reinterpret_cast<const float4*>(lg + (size_t)p * G);
 #pragma unroll
-    for (int c0 = 0; c0 < G; c0 += HC) {
-      float4 v[HC];
+      for (int c0 = 0; c0 < G; c0 += HC) {
+        float4 v[HC];
+        if constexpr (G <= 8) {
 #pragma unroll
-      for (int c = 0; c < HC; ++c) v[c] = __ldcg(l4 + c0 + c);
+          for (int c = 0; c < HC; ++c) v[c] = pf[c];
+          if (gi + kSelThreads < n_grp) {
 #pragma unroll
-      for (int c = 0; c < HC; ++c) {
-        const float f[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+            for (int c = 0; c < NPF; ++c) pf[c] = __ldcg(l4 + (size_t)kSelThreads * G + c);
+          }
+        } else {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int flat = (c0 + c) * 4 + e;      // position p + flat / G, head flat % G
-          const int j = flat / G, h = flat - j * G;
-          sc[j] = fmaxf(sc[j], f[e] - sm.lse[h]);
+          for (int c = 0; c < HC; ++c) v[c] = __ldcg(l4 + c0 + c);
+        }
+#pragma unroll
+        for (int c = 0; c < HC; ++c) {
+          const float f[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int flat = (c0 + c) * 4 + e;      // position p + flat / G, head flat % G
+            const int j = flat / G, h = flat - j * G;
+            sc[j] = fmaxf(sc[j], f[e] - sm.lse[h]);
+          }
         }
       }
     }
@@ -747,15 +937,21 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int pos = p + j;
-      if (pos >= t1) break;
-      const float pr = exp2f(sc[j]);
-      if (a.scores_out) a.scores_out[(size_t)seg * a.cap + pos] = pr;
-      key[j] = is_forced(pos, L, a.n_sink, a.n_recent) ? 0u : __float_as_uint(pr) + 1u;
-      if (topk && key[j]) atomicAdd(&sm.hist[key[j] >> 20], 1u);
+      if (gv && pos < p_end) {
+        const float pr = exp2f(sc[j]);
+        if (a.scores_out) a.scores_out[(size_t)seg * a.cap + pos] = pr;
+        key[j] = is_forced(pos, L, a.n_sink, a.n_recent) ? 0u : __float_as_uint(pr) + 1u;
+      }
+      if (topk) {
+        const uint32_t bin = key[j] ? key[j] >> 20 : 0xffffffffu;
+        const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+        if (bin != 0xffffffffu && lane == __ffs(peers) - 1) atomicAdd(&sm.hist[bin], (uint32_t)__popc(peers));
+      }
     }
     // positions past the end keep key 0: the 4-key groups below read them
-    *reinterpret_cast<uint4*>(kb + (p - p_lo)) = make_uint4(key[0], key[1], key[2], key[3]);
+    if (gv) *reinterpret_cast<uint4*>(kb + (p - p_lo)) = make_uint4(key[0], key[1], key[2], key[3]);
   }
+  __syncthreads();   // the passes below read keys other threads wrote
 
   int32_t* out = a.selected + (size_t)seg * a.K;
   if (!topk) {
@@ -1050,8 +1246,55 @@ static int launch_proj(ProjArgs& pa, int n_tiles, int bz, cudaStream_t st) {
   return cudaLaunchKernelEx(&cfg, proj_kernel<BB>, pa) == cudaSuccess ? SPC_OK : SPC_ERR_CUDA;
 }
 
-// Cluster size: about one CTA per SM over all segments, at most 16, and at
-// least 512 positions per CTA; a size the device cannot co-schedule is halved.
+// The tensor-core projection: the splits per column tile (the cluster size)
+// are the largest power of two that keeps the grid within one wave of two
+// CTAs per SM, at most 16 and at most one per 256 hidden rows, so every CTA
+// streams a long run of weight rows; split boundaries fall on multiples of 8
+// hidden rows.
+static int launch_proj_tc(ProjArgs& pa, int n_tiles, int bz, cudaStream_t st) {
+  static bool cluster_attr = false;
+  static size_t smem_attr = 0;
+  if (!cluster_attr) {
+    if (cudaFuncSetAttribute(proj_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+      return SPC_ERR_CUDA;
+    cluster_attr = true;
+  }
+  const long long slots = 2LL * (device_sm_count() > 0 ? device_sm_count() : 1);
+  int S = 1;
+  while (S < kProjMaxSplit && 2 * S * 256 <= pa.H && (long long)n_tiles * bz * 2 * S <= slots) S *= 2;
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute at[1];
+  cfg.blockDim = dim3(kPtcThreads, 1, 1);
+  cfg.stream = st;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  for (;; S /= 2) {
+    pa.S = S;
+    pa.Hc = ((pa.H + S - 1) / S + 7) / 8 * 8;
+    const size_t smem = kPtcSmem;
+    if (smem > smem_attr) {
+      if (cudaFuncSetAttribute(proj_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return SPC_ERR_CUDA;
+      smem_attr = smem;
+    }
+    cfg.gridDim = dim3(n_tiles * S, 1, bz);
+    cfg.dynamicSmemBytes = smem;
+    at[0].val.clusterDim.x = S;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    int n_clusters = 0;
+    if (S == 1 || (cudaOccupancyMaxActiveClusters(&n_clusters, proj_tc_kernel, &cfg) == cudaSuccess &&
+                   n_clusters > 0))
+      break;
+    cudaGetLastError();
+  }
+  return cudaLaunchKernelEx(&cfg, proj_tc_kernel, pa) == cudaSuccess ? SPC_OK : SPC_ERR_CUDA;
+}
+
+// Cluster size: at most two CTAs per SM over all segments, at most 16, and
+// at least 512 positions per CTA; a size the device cannot co-schedule is
+// halved.
 template <int G>
 static int launch_select(SelArgs& sa, int nseg, cudaStream_t st) {
   const size_t smem = sizeof(SelSmem);
@@ -1063,7 +1306,7 @@ static int launch_select(SelArgs& sa, int nseg, cudaStream_t st) {
     attr = true;
   }
   int C = 1;
-  while (C < kSelMaxCluster && nseg * C * 2 <= device_sm_count() && sa.cap / (C * 2) >= 512) C *= 2;
+  while (C < kSelMaxCluster && nseg * C * 2 <= 2 * device_sm_count() && sa.cap / (C * 2) >= 512) C *= 2;
   cudaLaunchConfig_t cfg{};
   cudaLaunchAttribute at[1];
   cfg.blockDim = dim3(kSelThreads, 1, 1);
@@ -1117,7 +1360,10 @@ int score_select_launch(const ScoreSelectCall& c) {
     const int bb = c.B <= 1 ? 1 : c.B <= 2 ? 2 : c.B <= 4 ? 4 : c.B <= 8 ? 8 : 16;
     const int bz = (c.B + bb - 1) / bb;
     int rc;
-    switch (bb) {
+    if (c.B >= SPC_PROJ_TC_MIN_BATCH) {
+      rc = launch_proj_tc(pa, n_tiles, (c.B + 15) / 16, st);
+      if (rc != SPC_OK) return rc;
+    } else switch (bb) {
       case 1: rc = launch_proj<1>(pa, n_tiles, bz, st); break;
       case 2: rc = launch_proj<2>(pa, n_tiles, bz, st); break;
       case 4: rc = launch_proj<4>(pa, n_tiles, bz, st); break;
@@ -1139,9 +1385,14 @@ int score_select_launch(const ScoreSelectCall& c) {
     sa.n_q = c.n_q; sa.n_kv = c.n_kv; sa.cap = c.cap; sa.lstride = l.lstride; sa.n_tiles = l.n_tiles;
     sa.total_tiles = c.B * c.n_kv * l.n_tiles; sa.append = c.append; sa.n_parts = l.n_parts;
     sa.qscale = kLog2e / sqrtf((float)kD);
-    // each CTA takes kScanTilesPerCta consecutive tiles: the hardware block
-    // scheduler then balances the load when other kernels hold some SMs
-    sa.tpc = kScanTilesPerCta;
+    // each CTA takes a run of consecutive tiles
+    if (kScanTilesPerCta > 0) {
+      sa.tpc = kScanTilesPerCta;
+    } else {
+      const long long slots = (long long)kScanCtasPerSm * (device_sm_count() > 0 ? device_sm_count() : 1);
+      sa.tpc = (int)((sa.total_tiles + slots - 1) / slots);
+      if (sa.tpc < 1) sa.tpc = 1;
+    }
     const int grid = (sa.total_tiles + sa.tpc - 1) / sa.tpc;
     switch (G) {
       case 1: e = launch_scan<1>(sa, grid, st); break;

@@ -117,6 +117,29 @@ def test_chain_cfg2_shape_two_layers():
     run_chain(cfg, 3, 3, layers_per_launch=2)
 
 
+def test_chain_cfg4b_128k_context_append_full_shape():
+    # full cfg4b shapes (4 requests at 131072 positions, capacity 131328,
+    # budget 2048, appending) on two host layers and two steps
+    cfg = scaled(CONFIGS["cfg4b"], n_layers=2, steps=2)
+    assert cfg.cap == 131072 + 256
+    swaps, pipe = run_chain(cfg, 2, 2, layers_per_launch=2)
+    assert pipe.len.cpu().tolist() == [131074] * 4
+
+
+def test_chain_cfg5_70b_shape_hbm_and_host_layers():
+    # full cfg5 shapes (8 requests x 65536 positions, 64/8 heads, H 8192,
+    # budget 4096): layer 0 resident in HBM (attention by position), layer 1
+    # through the host slots
+    cfg = scaled(CONFIGS["cfg5"], n_layers=2, steps=1)
+    assert cfg.gpu_layers == (1,) * 8
+    run_chain(cfg, 1, 2, layers_per_launch=2)
+
+
+def test_chain_cfg5_mqa_full_shape():
+    cfg = scaled(CONFIGS["cfg5mqa"], n_layers=2, steps=1)
+    run_chain(cfg, 1, 2, layers_per_launch=2)
+
+
 def _state(pipe):
     return [pipe.out.cpu(), pipe.selected.cpu(), pipe.slot_pos.cpu(), pipe.len.cpu()] + \
         [s.cpu() for s in pipe.slots if s is not None]

@@ -45,6 +45,11 @@ SMALL = [
     ("ragged_batch", dict(B=3, lens=(1500, 129, 700), n_q=8, n_kv=2, H=256, budget=96)),
     ("batch17_over_16", dict(B=17, lens=tuple(200 + 37 * i for i in range(17)), n_q=8, n_kv=2, H=256,
                              budget=80)),
+    ("batch5_hidden520_partial_stage", dict(B=5, lens=(300, 200, 450, 129, 260), n_q=8, n_kv=2, H=520,
+                                            budget=96)),
+    ("batch4_hidden8", dict(B=4, lens=(200, 150, 100, 250), n_q=8, n_kv=2, H=8, budget=96)),
+    ("batch16_hidden8192_split16", dict(B=16, lens=tuple(150 + 11 * i for i in range(16)), n_q=8, n_kv=2,
+                                        H=8192, budget=96)),
     ("len_le_budget_select_all", dict(lens=(50,), budget=96)),
     ("len_eq_budget", dict(lens=(96,), budget=96)),
     ("len_budget_plus_one", dict(lens=(97,), budget=96, cap=97)),
@@ -76,10 +81,12 @@ def test_all_equal_keys_over_a_long_context_ties_go_to_lower_positions():
     assert run.status() == 0
 
 
-def test_score_select_append_grows_len_and_switches_from_select_all():
-    # phase-A shape in miniature: len 120 -> 123 with budget 121
-    cfg = workload(name="append", lens=(120, 118), B=2, n_q=8, n_kv=2, H=256, budget=121, steps=3,
-                   append=True)
+@pytest.mark.parametrize("B", [2, 6])
+def test_score_select_append_grows_len_and_switches_from_select_all(B):
+    # phase-A shape in miniature: len 120 -> 123 with budget 121 (B = 6 takes
+    # the tensor-core projection, B = 2 the CUDA-core one)
+    cfg = workload(name="append", lens=tuple(120 - 2 * (b % 2) for b in range(B)), B=B, n_q=8, n_kv=2,
+                   H=256, budget=121, steps=3, append=True)
     run = ScoreRun(cfg)
     oK = run.inp.K_dlm.copy()
     olens = [int(v) for v in run.inp.lens]
