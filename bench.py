@@ -54,6 +54,9 @@ def parse():
     ap.add_argument("--oracle-sample-layers", type=int, default=2)
     ap.add_argument("--profile", action="store_true",
                     help="hot path only for a profiler: prologue, then --steps eager steps")
+    ap.add_argument("--c3", action="store_true",
+                    help="adaptive memory management on a growing context: per-step latency of the "
+                         "progressive per-layer offload vs offloading every layer at once")
     return ap.parse_args()
 
 
@@ -141,7 +144,22 @@ class ClockSampler:
 # hot-path kernels, from one `ncu --set full` capture of each on the cfg2
 # workload (the summary and its command are in profiles/). A figure is used
 # only while the kernel's source file still hashes to the one captured.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # gather of decode step 0, layers 16-31: 1550 loads per KV head x 16 layers x K/V
+    # = 49 600 rows; 396 800 system-memory sectors (12 697 600 B) read over the
+    # host link + 46 592 B DRAM read + 1 024 B DRAM write
+    "gather": {"source": "sparse_kv_cache_retrieval_gb300/csrc/gather_kv.cu",
+               "sha256": "04dab5b41b342fe03b3889fbeddba4406b5510aaaf6ef23eadd4d265a318c548",
+               "bytes_per_unit": (12697600 + 46592 + 1024) / 49600, "unit": "moved 256-byte row"},
+    # key scan over 32 768 positions x 8 KV heads: 67 141 376 B DRAM read + 291 584 B write
+    "key_scan": {"source": "sparse_kv_cache_retrieval_gb300/csrc/score_select.cu",
+                 "sha256": "a9f6f12e8f667d2c959d33ee2632990b1b4e2acfe77b8e5fd69580f08f1960c1",
+                 "bytes_per_unit": (67141376 + 291584) / 262144, "unit": "256-byte key row"},
+    # attention over 16 layers x 8 KV heads x 2048 kept rows: 134 536 192 B read + 3 158 272 B write
+    "attention": {"source": "sparse_kv_cache_retrieval_gb300/csrc/sparse_attn.cu",
+                  "sha256": "d9112f28e3e3d682b5752e0855a30680955cbc2f3a4731c432777b503ebe64ae",
+                  "bytes_per_unit": (134536192 + 3158272) / 262144, "unit": "512-byte K+V row"},
+}
 
 
 def _sha256(rel: str) -> str:
@@ -517,6 +535,9 @@ def our_arm(args, rank, world, local):
     for k in ("project", "select", "diff"):
         if k in kern:
             kinfo[k] = {"mean_us": round(kern[k]["mean_us"], 2), "launches": kern[k]["launches"]}
+    for k, ub in (("gather", 256), ("key_scan", 256), ("attention", 512)):
+        if k in kinfo:
+            kinfo[k]["traffic"] = ncu_traffic(k, kinfo[k]["algorithmic_bytes"] / ub)
     # every kernel alone (L2 flushed before each launch), same launch shapes
     log("isolated kernel timing")
     iso = isolated_times(pipe, spc, torch, t_last=W + K - 1)
@@ -610,11 +631,108 @@ def our_arm(args, rank, world, local):
     print(json.dumps(line))
 
 
+# ---------------------------------------------------------------- C3 arm
+def _next_offload_step(pipe, t0: int, K: int) -> int:
+    """First step after t0 at which the memory model moves another layer."""
+    for t in range(t0, K):
+        for b in range(pipe.B):
+            n_off = pipe.L - pipe.gpu_layers[b]
+            if pipe._offload_count(pipe._kv_length(b, t), n_off) > n_off:
+                return t
+    return K
+
+
+def c3_arm(args, rank, world, local):
+    """Per-step decode latency while the context grows across the memory
+    model's thresholds: the progressive policy ([Blog] §7, one more layer to
+    the host per threshold) against a static one (everything to the host at
+    the first threshold). The steps between two offloads are captured in one
+    CUDA graph with an event on stream A at every step boundary and replayed
+    once; each offload runs eagerly between graphs (it drains the GPU, copies
+    the layer to the host store, fills its workspace and repoints the view
+    tables) and is timed on its own, GPU time and wall time."""
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from sparse_kv_cache_retrieval_gb300.configs import CONFIGS, describe
+    from sparse_kv_cache_retrieval_gb300.pipeline import DecodePipeline
+    from sparse_kv_cache_retrieval_gb300.synth import make_inputs
+
+    torch.cuda.set_device(local)
+    cfg = CONFIGS["c3"]
+    K = cfg.steps
+    inp = make_inputs(cfg, steps=K + 1)
+    warm = DecodePipeline(cfg, inp, kv_bytes=cfg.kv_bytes)    # first calls set kernel attributes
+    warm.prologue()
+    for t in range(2):
+        warm.step(t)
+    warm.join()
+    torch.cuda.synchronize()
+    del warm
+    res = {}
+    for policy in ("progressive", "static"):
+        log(f"c3: {policy}")
+        pipe = DecodePipeline(cfg, inp, kv_bytes=cfg.kv_bytes, offload_policy=policy)
+        pipe.prologue()
+        torch.cuda.synchronize()
+        step_us, offloads, t = [], [], 0
+        while t < K:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            w0 = time.perf_counter()
+            e0.record(pipe.sA)
+            moved = pipe.maybe_offload(t)
+            e1.record(pipe.sA)
+            torch.cuda.synchronize()
+            if moved:
+                offloads.append({"step": t, "layers_moved": moved,
+                                 "gpu_us": round(e0.elapsed_time(e1) * 1e3, 1),
+                                 "wall_us": round((time.perf_counter() - w0) * 1e6, 1)})
+            t_next = _next_offload_step(pipe, t + 1, K)
+            g, evs = pipe.capture_timed(t, t_next - t)
+            with torch.cuda.stream(pipe.sA):
+                g.replay()
+            torch.cuda.synchronize()
+            step_us += [evs[i].elapsed_time(evs[i + 1]) * 1e3 for i in range(len(evs) - 1)]
+            t = t_next
+        us = np.array(step_us)
+        first = offloads[0]["step"] if offloads else K
+        res[policy] = {
+            "us_per_step_mean": round(float(us.mean()), 1),
+            "us_per_step_before_first_offload": round(float(us[:first].mean()), 1) if first > 0 else None,
+            "us_per_step_last_64": round(float(us[-64:].mean()), 1),
+            "offloads": offloads,
+            "layers_offloaded_at_end": cfg.n_layers - pipe.gpu_layers[0],
+            "window_means_us": [round(float(us[i:i + 32].mean()), 1) for i in range(0, K, 32)],
+        }
+        del pipe, g
+        torch.cuda.empty_cache()
+    if rank != 0:
+        return
+    p, st = res["progressive"], res["static"]
+    line = {"metric": "c3 growing-context decode us/step, progressive vs static offload", "unit": "us/step",
+            "value": p["us_per_step_last_64"], "higher_is_better": False, "n_gpus": world, "steps": K,
+            "data": "synthetic", "config": dict(describe(cfg), kv_bytes=cfg.kv_bytes,
+                                                 thresholds=c3_thresholds(cfg)),
+            "progressive": p, "static": st,
+            "max_offload_wall_us": {k: max([o["wall_us"] for o in v["offloads"]] or [0]) for k, v in res.items()}}
+    print(json.dumps(line))
+
+
+def c3_thresholds(cfg):
+    from sparse_kv_cache_retrieval_gb300 import binding as spc
+    thr = spc.spc_offload_thresholds(cfg.n_layers, cfg.n_kv, cfg.d, cfg.B, cfg.budget, cfg.kv_bytes)
+    return [t for t in thr[:-1] if t <= cfg.cap]
+
+
 def main():
     faulthandler.dump_traceback_later(240, repeat=True, file=sys.stderr)
     args = parse()
     rank, world, local = dist_setup(args.gpus)
-    if args.impl == "reference":
+    if args.c3:
+        c3_arm(args, rank, world, local)
+    elif args.impl == "reference":
         reference_arm(args, rank, world)
     else:
         our_arm(args, rank, world, local)

@@ -194,6 +194,44 @@ int spc_gather_kv(const spc_gather_view* views, int layer_lo, int layer_hi,
                   int B, int n_kv, int d, int cap, int budget, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Adaptive memory management (C3). [Blog] §7: thresholds on the sequence
+ * length are computed ahead of time from the model's layer count, KV heads and
+ * head dimension, the GPU memory available and the number of concurrent
+ * requests and the KV budget; each time the context reaches the next
+ * threshold the last layer still on the GPU moves its KV to CPU memory and
+ * keeps only a budget-sized workspace on the GPU, so GPU memory stays used
+ * without a cliff. [Summary] §6.2, §6.2.1 (same, "progressively offloads").
+ *
+ * spc_offload_thresholds (host only, no GPU needed). With R = 2 * n_kv * d * 2
+ * bytes per position and layer (K and V, bf16) and B requests, k offloaded
+ * layers at context length s cost B * ((n_layers - k) * s + k * budget) * R
+ * bytes of GPU KV memory. For k = 0 .. n_layers-1:
+ *   thresholds[k] = floor((kv_bytes / (B * R) - k * budget) / (n_layers - k)) + 1,
+ * the shortest length at which k offloaded layers no longer fit, so that at
+ * s >= thresholds[k] a (k+1)-th layer must go; thresholds[n_layers] =
+ * INT64_MAX. The runtime rule: while s >= thresholds[n_off], offload layer
+ * n_layers - 1 - n_off and increment n_off (last layers first).
+ * thresholds  host array of n_layers + 1 int64, written on success.
+ * Returns SPC_ERR_WORKSPACE when even every layer offloaded (n_layers budget
+ * workspaces per request) does not fit in kv_bytes.
+ *
+ * spc_fill_slots: the workspace of a layer entering CPU memory starts out with
+ * the rows the request keeps resident. For layers l in [layer_lo, layer_hi)
+ * held by request b's view (view.layer0 <= l < view.layer0 + view.n_layers),
+ * kv in {K, V}, KV head g and slot s with 0 <= p = slot_pos[b,g,s] < cap:
+ *   view.slots[l', kv, g, s, :] = view.host[l', kv, g, p, :],  l' = l - view.layer0
+ * view.host may be device memory (the layer's HBM cache, the usual source) or
+ * a device-visible host address; both bf16 [n_layers][2][n_kv][cap or budget][d],
+ * 16-byte aligned. slot_pos int32 [B][n_kv][budget]. Rows are copied bit-exact.
+ * Limits as spc_gather_kv.
+ * ---------------------------------------------------------------------- */
+int spc_offload_thresholds(int n_layers, int n_kv, int d, int B, int budget, int64_t kv_bytes,
+                           int64_t* thresholds);
+
+int spc_fill_slots(const spc_gather_view* views, int layer_lo, int layer_hi, const int32_t* slot_pos,
+                   int B, int n_kv, int d, int cap, int budget, void* stream);
+
+/* ------------------------------------------------------------------------
  * Sparse GQA decode attention over the resident budget. [Blog] §2 formula
  * over the kept rows; §4: the LLM forward uses the sparse KV prepared in the
  * previous iteration; [Summary] §4.3: for GQA the selected KV serves every

@@ -216,6 +216,55 @@ def sparse_attention(q_bits: np.ndarray, K_bits: np.ndarray, V_bits: np.ndarray,
 
 
 # --------------------------------------------------------------------------
+# C3: adaptive memory management ([Blog] §7: sequence-length thresholds from
+#     the model's layers, KV heads and head dimension, the free GPU memory,
+#     the concurrent requests and the KV budget; past each threshold the last
+#     layer still on the GPU moves to CPU memory and keeps a budget-sized
+#     workspace; [Summary] §6.2 and §6.2.1)
+# --------------------------------------------------------------------------
+def kv_row_bytes(n_kv: int, d: int, elem_bytes: int = 2) -> int:
+    """GPU bytes one position costs in one layer: K and V, every KV head."""
+    return 2 * n_kv * d * elem_bytes
+
+
+def gpu_kv_bytes(length: int, n_offloaded: int, n_layers: int, n_kv: int, d: int, B: int,
+                 budget: int) -> int:
+    """GPU KV bytes of B requests of `length` positions when the last
+    `n_offloaded` layers live in CPU memory: every layer still on the GPU holds
+    all `length` rows, every offloaded layer a `budget`-row workspace."""
+    rows = (n_layers - n_offloaded) * length + n_offloaded * budget
+    return B * rows * kv_row_bytes(n_kv, d)
+
+
+def offload_thresholds(n_layers: int, n_kv: int, d: int, B: int, budget: int,
+                       kv_bytes: int) -> List[int]:
+    """threshold[k] (k = 0..n_layers-1): the shortest context at which k
+    offloaded layers no longer fit in `kv_bytes`, so the (k+1)-th must go.
+    threshold[n_layers] is None (nothing left to offload). Written from the
+    definition: the largest length that fits with k offloaded layers, plus one.
+    Raises ValueError when even every layer offloaded does not fit."""
+    per_req_rows = kv_bytes // (B * kv_row_bytes(n_kv, d))   # rows one request may hold
+    if per_req_rows < n_layers * budget:
+        raise ValueError("the budget workspaces of all layers exceed the KV memory")
+    out: List[int] = []
+    for k in range(n_layers):
+        fit = (per_req_rows - k * budget) // (n_layers - k)   # longest length that fits
+        out.append(int(fit) + 1)
+    out.append(None)
+    return out
+
+
+def layers_to_offload(length: int, thresholds: Sequence[Optional[int]], n_offloaded: int) -> int:
+    """The runtime rule of [Blog] §7: while the length has reached the
+    threshold for the current number of offloaded layers, offload one more.
+    Returns the new number of offloaded layers (never fewer than before)."""
+    n = n_offloaded
+    while thresholds[n] is not None and length >= thresholds[n]:
+        n += 1
+    return n
+
+
+# --------------------------------------------------------------------------
 # the decode step ([Blog] §4 loop: select for the next step, load only the
 # difference, run the LLM on the previously prepared sparse KV)
 # --------------------------------------------------------------------------
@@ -291,4 +340,5 @@ class DecodeState:
 
 
 __all__ = ["bf16_to_f64", "round_to_bf16", "project", "head_probabilities", "group_scores",
-           "forced_positions", "select", "elastic_diff", "gather", "sparse_attention", "DecodeState"]
+           "forced_positions", "select", "elastic_diff", "gather", "sparse_attention", "kv_row_bytes",
+           "gpu_kv_bytes", "offload_thresholds", "layers_to_offload", "DecodeState"]

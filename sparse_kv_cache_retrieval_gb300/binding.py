@@ -49,6 +49,8 @@ SIGNATURES = {
     "spc_host_device_pointer": (_I, [_P, ctypes.POINTER(ctypes.c_void_p)]),
     "spc_stream_read": (_I, [_P, ctypes.c_size_t, _P, _I, _P]),
     "spc_copy": (_I, [_P, _P, ctypes.c_size_t, _P]),
+    "spc_fill_slots": (_I, [_P, _I, _I, _P, _I, _I, _I, _I, _I, _P]),
+    "spc_offload_thresholds": (_I, [_I, _I, _I, _I, _I, ctypes.c_int64, ctypes.POINTER(ctypes.c_int64)]),
 }
 
 
@@ -190,6 +192,20 @@ def spc_stream_read(src, nbytes, sink, n_blocks, stream=None) -> None:
 def spc_copy(dst, src, nbytes, stream=None) -> None:
     """Kernel copy between device memory and device-visible host addresses."""
     _check("spc_copy", lib().spc_copy(_ptr(dst), _ptr(src), int(nbytes), _stream(stream)))
+
+
+def spc_fill_slots(views, layer_lo, layer_hi, slot_pos, B, n_kv, d, cap, budget, stream=None) -> None:
+    _check("spc_fill_slots", lib().spc_fill_slots(_ptr(views), layer_lo, layer_hi, _ptr(slot_pos), B,
+                                                  n_kv, d, cap, budget, _stream(stream)))
+
+
+def spc_offload_thresholds(n_layers, n_kv, d, B, budget, kv_bytes) -> list:
+    """Host-side memory model: n_layers + 1 context-length thresholds (the
+    last one is INT64_MAX)."""
+    out = (ctypes.c_int64 * (n_layers + 1))()
+    _check("spc_offload_thresholds", lib().spc_offload_thresholds(n_layers, n_kv, d, B, budget,
+                                                                  int(kv_bytes), out))
+    return [int(v) for v in out]
 
 
 def spc_device_sm_count() -> int:

@@ -45,6 +45,7 @@ class Workload:
     n_sink: int = 4
     n_recent: int = 64
     gamma: float = 8.0     # planted hot keys get + gamma*sqrt(G) along the group's query direction
+    kv_bytes: Optional[int] = None   # GPU memory for the LLM KV: set = adaptive layer offload
     note: str = ""
 
     @property
@@ -131,6 +132,17 @@ def _build() -> dict:
     cfgs["cfg5mqa"] = dataclasses.replace(
         cfgs["cfg5"], name="cfg5mqa_b8_ctx65536_mqa64x1_budget4096_80layers", n_kv=1,
         note="MQA variant of cfg5: all 64 query heads form one group")
+    # adaptive memory management on a growing context: 4 requests from 4096
+    # positions, one token per step, GPU KV memory for 4127 positions of all
+    # 32 layers per request, so the first threshold falls 32 steps in and a
+    # further layer leaves every ~70-100 steps
+    row4 = 2 * 8 * 128 * 2
+    cfgs["c3"] = Workload(
+        name="c3_b4_ctx4096+512_append_gqa32x8_budget2048_32layers_adaptive",
+        B=4, lens=(4096,) * 4, H=4096, n_q=32, n_kv=8, d=128, budget=2048, n_layers=32,
+        gpu_layers=(32,) * 4, steps=512, rho=(0.9,) * 4, hot=(41,) * 4, seed=5, append=True,
+        cap=4096 + 512, kv_bytes=4 * 32 * 4127 * row4,
+        note="progressive per-layer offload driven by the memory model's thresholds")
     return cfgs
 
 

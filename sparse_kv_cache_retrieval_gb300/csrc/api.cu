@@ -194,6 +194,29 @@ size_t spc_sparse_decode_attn_workspace_size(int n_layers, int B, int n_q, int n
   return attn_workspace(n_layers, B, n_q, n_kv, budget);
 }
 
+int spc_fill_slots(const spc_gather_view* views, int layer_lo, int layer_hi, const int32_t* slot_pos,
+                   int B, int n_kv, int d, int cap, int budget, void* stream) {
+  if (!views || !slot_pos) return SPC_ERR_INVALID_ARG;
+  if (d != SPC_HEAD_DIM) return SPC_ERR_SHAPE;
+  if (B < 1 || B > SPC_MAX_BATCH || n_kv < 1 || B * n_kv > 1024) return SPC_ERR_SHAPE;
+  if (layer_lo < 0 || layer_hi < layer_lo) return SPC_ERR_SHAPE;
+  if (budget < 1 || budget > SPC_MAX_BUDGET || cap < 1 || cap > SPC_MAX_CAP) return SPC_ERR_SHAPE;
+  return fill_slots_launch(views, layer_lo, layer_hi, slot_pos, B, n_kv, cap, budget, stream);
+}
+
+int spc_offload_thresholds(int n_layers, int n_kv, int d, int B, int budget, int64_t kv_bytes,
+                           int64_t* thresholds) {
+  if (!thresholds) return SPC_ERR_INVALID_ARG;
+  if (n_layers < 1 || n_kv < 1 || d < 1 || B < 1 || budget < 1 || kv_bytes < 0) return SPC_ERR_SHAPE;
+  const long long row = 2LL * n_kv * d * 2;                       // K and V, every KV head, bf16
+  const long long per_req_rows = kv_bytes / (row * B);            // rows one request may hold
+  if (per_req_rows < (long long)n_layers * budget) return SPC_ERR_WORKSPACE;
+  for (int k = 0; k < n_layers; ++k)
+    thresholds[k] = (per_req_rows - (long long)k * budget) / (n_layers - k) + 1;
+  thresholds[n_layers] = INT64_MAX;
+  return SPC_OK;
+}
+
 int spc_sparse_decode_attn(const void* q, const spc_kv_view* views, const int32_t* selected,
                            const int32_t* slot_pos, int n_layers, int B, int n_q, int n_kv, int d,
                            int budget, float scale, float* out, void* workspace,

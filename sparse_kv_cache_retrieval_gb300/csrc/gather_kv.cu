@@ -125,6 +125,53 @@ gather_kernel(const spc_gather_view* __restrict__ views, int layer_lo, int layer
   }
 }
 
+// Slot fill of layers entering the host ([Blog] §7: an offloaded layer keeps a
+// budget-sized workspace on the GPU; it starts out holding the resident rows).
+// One 256-byte row per half-warp, grid-stride over (layer, K/V, request, KV
+// head, slot); slots whose position is empty or outside [0, cap) are left
+// untouched. The source may be device memory (the layer's HBM cache) or a
+// device-visible host address.
+constexpr int kFillThreads = 256;
+
+__global__ void __launch_bounds__(kFillThreads)
+fill_slots_kernel(const spc_gather_view* __restrict__ views, int layer_lo, int layer_hi,
+                  const int32_t* __restrict__ slot_pos, int B, int n_kv, int cap, int K) {
+  const int l16 = threadIdx.x & 15;
+  const long long per_layer = 2LL * B * n_kv * K;
+  const long long total = (long long)(layer_hi - layer_lo) * per_layer;
+  const long long nhw = (long long)gridDim.x * (kFillThreads / 16);
+  for (long long item = ((long long)blockIdx.x * kFillThreads + threadIdx.x) >> 4; item < total; item += nhw) {
+    const int lq = (int)(item / per_layer);
+    long long rem = item - lq * per_layer;
+    const int kv = (int)(rem / ((long long)B * n_kv * K));
+    rem -= (long long)kv * B * n_kv * K;
+    const int seg = (int)(rem / K), slot = (int)(rem - (long long)seg * K);
+    const int b = seg / n_kv, g = seg - b * n_kv;
+    const spc_gather_view vw = views[b];
+    const int lrel = layer_lo + lq - vw.layer0;
+    if (lrel < 0 || lrel >= vw.n_layers) continue;
+    const int pos = slot_pos[(size_t)seg * K + slot];
+    if (pos < 0 || pos >= cap) continue;
+    const size_t hrow = ((((size_t)lrel * 2 + kv) * n_kv + g) * cap + pos) * kD + l16 * 8;
+    const size_t srow = ((((size_t)lrel * 2 + kv) * n_kv + g) * K + slot) * kD + l16 * 8;
+    const uint4 v = ldg_stream(static_cast<const uint16_t*>(vw.host) + hrow);
+    stg_v4(static_cast<uint16_t*>(vw.slots) + srow, v);
+  }
+}
+
+int fill_slots_launch(const spc_gather_view* views, int layer_lo, int layer_hi, const int32_t* slot_pos,
+                      int B, int n_kv, int cap, int budget, void* stream) {
+  if (layer_hi <= layer_lo) return SPC_OK;
+  const long long items = (long long)(layer_hi - layer_lo) * 2 * B * n_kv * budget;
+  long long grid = (items + (kFillThreads / 16) - 1) / (kFillThreads / 16);
+  const long long cap_grid = 4LL * std::max(1, device_sm_count());
+  if (grid > cap_grid) grid = cap_grid;
+  if (grid < 1) grid = 1;
+  fill_slots_kernel<<<(int)grid, kFillThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      views, layer_lo, layer_hi, slot_pos, B, n_kv, cap, budget);
+  return cudaGetLastError() == cudaSuccess ? SPC_OK : SPC_ERR_CUDA;
+}
+
 int gather_launch(const spc_gather_view* views, int layer_lo, int layer_hi, const int32_t* load_slot,
                   const int32_t* load_pos, const int32_t* n_load, int B, int n_kv, int cap,
                   int budget, void* stream) {

@@ -944,8 +944,12 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a) {
       }
       if (topk) {
         const uint32_t bin = key[j] ? key[j] >> 20 : 0xffffffffu;
-        const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-        if (bin != 0xffffffffu && lane == __ffs(peers) - 1) atomicAdd(&sm.hist[bin], (uint32_t)__popc(peers));
+        if (n_rounds > 1) {   // long slices: aggregate equal bins over the warp first
+          const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+          if (bin != 0xffffffffu && lane == __ffs(peers) - 1) atomicAdd(&sm.hist[bin], (uint32_t)__popc(peers));
+        } else if (bin != 0xffffffffu) {
+          atomicAdd(&sm.hist[bin], 1u);
+        }
       }
     }
     // positions past the end keep key 0: the 4-key groups below read them

@@ -59,7 +59,8 @@ class DecodePipeline:
     def __init__(self, cfg: Workload, inputs: Inputs, *, device: str = "cuda",
                  n_layers: Optional[int] = None, layers_per_launch: int = 16,
                  host_io: bool = False, timing: bool = False, fill_threads: Optional[int] = None,
-                 gather_streams: int = 2):
+                 gather_streams: int = 2, kv_bytes: Optional[int] = None,
+                 offload_policy: str = "progressive"):
         self.cfg = cfg
         self.inp = inputs
         self.dev = torch.device(device)
@@ -100,52 +101,60 @@ class DecodePipeline:
         self.out_buf = torch.zeros(2, L, B, self.n_q, d, dtype=torch.float32, device=dev)
         self.out = self.out_buf[0]
 
-        # LLM KV: HBM full caches, pinned host stores, HBM slots
-        self.hbm: List[Optional[torch.Tensor]] = []
+        # adaptive memory management (C3, "ASPLOS'26 | SpeContext ..." §7):
+        # context-length thresholds from the memory model; each request starts
+        # with as many trailing layers offloaded as its context requires, and
+        # maybe_offload() moves further layers as the context grows
+        if offload_policy not in ("progressive", "static"):
+            raise ValueError("offload_policy is 'progressive' or 'static'")
+        self.adaptive = kv_bytes is not None
+        self.kv_bytes = kv_bytes
+        self.offload_policy = offload_policy
+        self.thresholds = None
+        self.offload_log: List[tuple] = []        # (step, request, layer) of every offload
+        self._pending_free: List[torch.Tensor] = []
+        if self.adaptive:
+            self.thresholds = spc.spc_offload_thresholds(L, n_kv, d, B, K, int(kv_bytes))
+            self.gpu_layers = [L - self._offload_count(self._kv_length(b, -1), 0) for b in range(B)]
+
+        # LLM KV: per-layer HBM full caches, pinned host stores and HBM slots.
+        # A request's host store and slots cover layers [store_base[b], L): its
+        # host layers in the static split, every layer in the adaptive one (so
+        # a layer can move without reallocating)
+        self.hbm: List[List[Optional[torch.Tensor]]] = []
         self.host_stores: List[Optional[torch.Tensor]] = []
         self.slots: List[Optional[torch.Tensor]] = []
-        host_dev_ptrs, slot_ptrs, layer0, n_host = [], [], [], []
+        self.store_base: List[int] = []
+        self._store_dev: List[int] = []
         for b in range(B):
             ng = self.gpu_layers[b]
-            nh = L - ng
-            if ng > 0:
-                buf = np.empty((ng, 2, n_kv, cap, d), np.uint16)
-                fill_llm_kv(cfg, b, 0, buf, threads=fill_threads)
-                self.hbm.append(_dev_u16(buf, dev))
+            s0 = 0 if self.adaptive else ng
+            layers = []
+            for l in range(ng):
+                buf = np.empty((1, 2, n_kv, cap, d), np.uint16)
+                fill_llm_kv(cfg, b, l, buf, threads=fill_threads)
+                layers.append(_dev_u16(buf[0], dev))
                 del buf
-            else:
-                self.hbm.append(None)
-            if nh > 0:
-                hs = torch.empty((nh, 2, n_kv, cap, d), dtype=torch.int16, pin_memory=True)
-                fill_llm_kv(cfg, b, ng, hs.numpy().view(np.uint16), threads=fill_threads)
+            self.hbm.append(layers)
+            if L - s0 > 0:
+                hs = torch.empty((L - s0, 2, n_kv, cap, d), dtype=torch.int16, pin_memory=True)
+                if L - ng > 0:
+                    fill_llm_kv(cfg, b, ng, hs.numpy().view(np.uint16)[ng - s0:], threads=fill_threads)
                 self.host_stores.append(hs)
-                sl = torch.zeros((nh, 2, n_kv, K, d), dtype=torch.int16, device=dev)
-                self.slots.append(sl)
-                host_dev_ptrs.append(spc.spc_host_device_pointer(hs))
-                slot_ptrs.append(sl.data_ptr())
+                self.slots.append(torch.zeros((L - s0, 2, n_kv, K, d), dtype=torch.int16, device=dev))
+                self._store_dev.append(spc.spc_host_device_pointer(hs))
             else:
                 self.host_stores.append(None)
                 self.slots.append(None)
-                host_dev_ptrs.append(0)
-                slot_ptrs.append(0)
-            layer0.append(ng)
-            n_host.append(nh)
-        self.gviews = spc.to_device_bytes(spc.gather_views(host_dev_ptrs, slot_ptrs, layer0, n_host), dev)
+                self._store_dev.append(0)
+            self.store_base.append(s0)
+        self._layer_bytes = 2 * n_kv * cap * d * 2
+        self._slot_layer_bytes = 2 * n_kv * K * d * 2
+        self.gviews = spc.to_device_bytes(self._gather_view_table(), dev)
 
         # attention views [L][B]
-        kp, vp, rows, use = [], [], [], []
-        for l in range(L):
-            for b in range(B):
-                ng = self.gpu_layers[b]
-                if l < ng:
-                    base = self.hbm[b][l]
-                    kp.append(base[0].data_ptr()); vp.append(base[1].data_ptr())
-                    rows.append(cap); use.append(0)
-                else:
-                    base = self.slots[b][l - ng]
-                    kp.append(base[0].data_ptr()); vp.append(base[1].data_ptr())
-                    rows.append(K); use.append(1)
-        self.aviews = spc.to_device_bytes(spc.kv_views(kp, vp, rows, use), dev)
+        table = np.concatenate([self._attn_view_row(l, b) for l in range(L) for b in range(B)])
+        self.aviews = spc.to_device_bytes(table, dev)
         self.aview_stride = 32 * B
 
         # layer chunks, streams, events
@@ -195,6 +204,114 @@ class DecodePipeline:
         self._all_events: List[torch.cuda.Event] = []
         self._capturing = False
         self._prologue_done = False
+        self._step_events: Optional[List[torch.cuda.Event]] = None
+
+    # ------------------------------------------------------------------ layout
+    def _gather_view_table(self) -> np.ndarray:
+        host, slots, layer0, n_host = [], [], [], []
+        for b in range(self.B):
+            ng, s0 = self.gpu_layers[b], self.store_base[b]
+            if self.slots[b] is not None and ng < self.L:
+                host.append(self._store_dev[b] + (ng - s0) * self._layer_bytes)
+                slots.append(self.slots[b].data_ptr() + (ng - s0) * self._slot_layer_bytes)
+            else:
+                host.append(0)
+                slots.append(0)
+            layer0.append(ng)
+            n_host.append(self.L - ng)
+        return spc.gather_views(host, slots, layer0, n_host)
+
+    def _attn_view_row(self, l: int, b: int) -> np.ndarray:
+        if l < self.gpu_layers[b]:
+            base, rows, use = self.hbm[b][l], self.cap, 0
+        else:
+            base, rows, use = self.slots[b][l - self.store_base[b]], self.K, 1
+        return spc.kv_views([base[0].data_ptr()], [base[1].data_ptr()], [rows], [use])
+
+    def host_slots(self, b: int) -> Optional[torch.Tensor]:
+        """Slots of request b's host layers, [L - gpu_layers[b]][2][n_kv][K][d]."""
+        if self.slots[b] is None or self.gpu_layers[b] >= self.L:
+            return None
+        return self.slots[b][self.gpu_layers[b] - self.store_base[b]:]
+
+    # ------------------------------------------------------------------ C3
+    def _kv_length(self, b: int, t: int) -> int:
+        """Context length of request b while step t runs (t = -1: the prompt):
+        an appending workload adds one row per step."""
+        n = int(self.inp.lens[b]) + (t + 1 if self.cfg.append and t >= 0 else 0)
+        return min(n, self.cap)
+
+    def _offload_count(self, length: int, n_off: int) -> int:
+        """Offloaded layers a request of `length` positions needs. progressive:
+        the rule of [Blog] §7 (while the length has reached the threshold of
+        the current count, offload one more layer); static: nothing until the
+        first threshold, then every layer at once."""
+        thr = self.thresholds
+        if self.offload_policy == "static":
+            return self.L if length >= thr[0] else n_off
+        while n_off < self.L and length >= thr[n_off]:
+            n_off += 1
+        return n_off
+
+    def maybe_offload(self, t: int) -> int:
+        """Before issuing step t: offload the layers the memory model asks for.
+        Returns the number of layers moved. Each move waits for the GPU to
+        drain (the view tables change), copies the layer's cache to the
+        pinned host store, fills its budget workspace from the HBM cache
+        with the slot map step t attends with, and repoints the views."""
+        if not self.adaptive:
+            return 0
+        moved = 0
+        for b in range(self.B):
+            length = self._kv_length(b, t)
+            target = self._offload_count(length, self.L - self.gpu_layers[b])
+            while self.L - self.gpu_layers[b] < target:
+                if self._capturing:
+                    raise RuntimeError("an offload cannot be captured in a CUDA graph")
+                if moved == 0:
+                    torch.cuda.synchronize()
+                    self._pending_free.clear()
+                self._offload_layer(b, t % 2)
+                self.offload_log.append((t, b, self.gpu_layers[b]))
+                moved += 1
+        return moved
+
+    def _offload_layer(self, b: int, p: int) -> None:
+        l = self.gpu_layers[b] - 1
+        s0, sA = self.store_base[b], self.sA
+        src = self.hbm[b][l]
+        with torch.cuda.stream(sA):
+            # the whole layer, [2][n_kv][cap][d]: rows past the current length
+            # stand for the K/V rows the LLM writes as the context grows (the
+            # workloads prefill them), so the store is complete from here on
+            spc.spc_copy(self._store_dev[b] + (l - s0) * self._layer_bytes, src.data_ptr(), self._layer_bytes,
+                         stream=sA)
+            host = [0] * self.B
+            slots = [0] * self.B
+            n_layers = [0] * self.B
+            host[b] = src.data_ptr()
+            slots[b] = self.slots[b][l - s0].data_ptr()
+            n_layers[b] = 1
+            fill_views = spc.to_device_bytes(spc.gather_views(host, slots, [l] * self.B, n_layers), self.dev)
+            spc.spc_fill_slots(fill_views, l, l + 1, self.slot_pos[p], self.B, self.n_kv, self.d, self.cap,
+                               self.K, stream=sA)
+            self.gpu_layers[b] = l
+            self.hbm[b][l] = None
+            row = torch.from_numpy(self._attn_view_row(l, b).view(np.uint8).copy()).to(self.dev)
+            off = l * self.aview_stride + b * 32
+            self.aviews[off:off + 32].copy_(row)
+            self.gviews.copy_(torch.from_numpy(self._gather_view_table().view(np.uint8).copy()).to(self.dev))
+        # the copy and the fill read the old cache: keep it until the next drain
+        self._pending_free.extend([src, fill_views])
+
+    def kv_hbm_bytes(self) -> int:
+        """GPU KV bytes the memory model charges now: full caches of HBM layers
+        at the current length plus one budget workspace per offloaded layer."""
+        tot = 0
+        for b in range(self.B):
+            n_off = self.L - self.gpu_layers[b]
+            tot += ((self.L - n_off) * self._kv_length(b, -1) + n_off * self.K) * 2 * self.n_kv * self.d * 2
+        return tot
 
     @staticmethod
     def _priorities():
@@ -338,6 +455,13 @@ class DecodePipeline:
         p, pn = t % 2, (t + 1) % 2
         append = 1 if self.cfg.append else 0
         lookahead = self._range_end is not None and t + 1 < self._range_end
+        if self.adaptive:
+            self.maybe_offload(t)
+        if self._step_events is not None:
+            ev = self._timing_event()
+            self._all_events.append(ev)
+            ev.record(sA)
+            self._step_events.append(ev)
         if self._front_issued != t:
             self._front(t)
         if self.host_io and self._q_issued != t:
@@ -399,7 +523,18 @@ class DecodePipeline:
             self._range_end = None
         self.join()
 
-    def capture(self, t0: int, n: int) -> torch.cuda.CUDAGraph:
+    def capture_timed(self, t0: int, n: int):
+        """capture() with a timing event recorded on stream A at the start of
+        every step and after the last one; returns (graph, events). The
+        pipeline keeps the events alive."""
+        self._step_events = []
+        try:
+            g = self.capture(t0, n, _final_event=True)
+        finally:
+            evs, self._step_events = self._step_events, None
+        return g, evs
+
+    def capture(self, t0: int, n: int, _final_event: bool = False) -> torch.cuda.CUDAGraph:
         """A CUDA graph of steps [t0, t0+n) (both streams, forked and joined).
 
         Replay it on stream A (``with torch.cuda.stream(pipe.sA): g.replay()``).
@@ -420,6 +555,11 @@ class DecodePipeline:
                 for t in range(t0, t0 + n):
                     self.step(t)
                 self.join()
+                if _final_event and self._step_events is not None:
+                    ev = self._timing_event()
+                    self._all_events.append(ev)
+                    ev.record(self.sA)
+                    self._step_events.append(ev)
         finally:
             self._capturing = False
             self._range_end = None

@@ -132,3 +132,38 @@ def test_product_path_does_not_import_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")) and f != "smoke.py":
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
+
+
+def test_offload_thresholds_through_the_abi_match_the_oracle(lib):
+    # host-only entry point: the memory model of adaptive offloading, checked
+    # against the oracle's definition on random shapes and on the workloads
+    import numpy as np
+    import oracle.spc_oracle as O
+    rng = np.random.default_rng(5)
+    cases = [(32, 8, 128, 4, 2048, 12 << 30), (32, 8, 128, 16, 1024, 12 << 30),
+             (80, 8, 128, 8, 4096, 60 << 30), (80, 1, 128, 8, 4096, 20 << 30)]
+    for _ in range(200):
+        L, n_kv, B_, K = int(rng.integers(1, 90)), int(rng.integers(1, 9)), int(rng.integers(1, 17)), \
+            int(rng.integers(1, 4097))
+        row = 2 * n_kv * 128 * 2
+        cases.append((L, n_kv, 128, B_, K, int(B_ * row * L * K * rng.uniform(1.0, 40.0))))
+    for L, n_kv, d, B_, K, kv in cases:
+        got = B.spc_offload_thresholds(L, n_kv, d, B_, K, kv)
+        want = O.offload_thresholds(L, n_kv, d, B_, K, kv)
+        assert got[:L] == want[:L]
+        assert got[L] == 2 ** 63 - 1
+
+
+def test_offload_thresholds_reject_memory_below_the_workspaces(lib):
+    with pytest.raises(B.SpcError) as e:
+        B.spc_offload_thresholds(32, 8, 128, 2, 2048, 2 * 32 * 2048 * 4096 - 1)
+    assert e.value.status == -5
+    assert lib.spc_offload_thresholds(32, 8, 128, 2, 2048, 1 << 40, None) == -1
+    assert lib.spc_offload_thresholds(0, 8, 128, 2, 2048, 1 << 40, None) in (-1, -2)
+
+
+def test_fill_slots_validates_before_launch(lib):
+    assert lib.spc_fill_slots(None, 0, 1, FAKE, 1, 8, 128, 100, 64, None) == -1
+    assert lib.spc_fill_slots(FAKE, 0, 1, FAKE, 1, 8, 64, 100, 64, None) == -2
+    assert lib.spc_fill_slots(FAKE, 2, 1, FAKE, 1, 8, 128, 100, 64, None) == -2
+    assert lib.spc_fill_slots(FAKE, 0, 1, FAKE, 1, 8, 128, 100, 5000, None) == -2

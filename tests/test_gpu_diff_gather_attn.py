@@ -135,6 +135,50 @@ def test_gather_bit_exact_over_layers_and_requests():
         assert np.array_equal(got, want)
 
 
+@pytest.mark.parametrize("source", ["device", "host"])
+def test_fill_slots_bit_exact(source):
+    # the workspace of a layer entering CPU memory starts with the resident
+    # rows: slots[s] = cache[slot_pos[s]] for every slot holding a position
+    # (empty slots and out-of-range positions untouched), per request, K and V,
+    # KV head; layers outside a request's view are skipped
+    rng = np.random.default_rng(17)
+    B, n_kv, K, cap, L = 3, 2, 100, 400, 4
+    layer0 = [1, 3, 4]                  # request 2 has no layer in the view
+    caches, slots, hptr, sptr = [], [], [], []
+    for b in range(B):
+        n = max(1, L - layer0[b])
+        bits = rng.integers(-32768, 32767, (n, 2, n_kv, cap, 128), dtype=np.int16)
+        if source == "device":
+            c = torch.from_numpy(bits).to(DEV)
+            hptr.append(c.data_ptr())
+        else:
+            c = torch.from_numpy(bits).pin_memory()
+            hptr.append(spc.spc_host_device_pointer(c))
+        sl = torch.full((n, 2, n_kv, K, 128), 7, dtype=torch.int16, device=DEV)
+        caches.append((bits, c)); slots.append(sl); sptr.append(sl.data_ptr())
+    views = spc.to_device_bytes(spc.gather_views(hptr, sptr, layer0, [L - v for v in layer0]), DEV)
+    slot_pos = np.full((B, n_kv, K), -1, np.int64)
+    for b in range(B):
+        for g in range(n_kv):
+            m = int(rng.integers(K // 2, K + 1))
+            slot_pos[b, g, rng.choice(K, size=m, replace=False)] = rng.choice(cap, size=m, replace=False)
+    slot_pos[0, 0, 0] = cap + 5                     # out of range: left untouched
+    spc.spc_fill_slots(views, 2, 4, i32(slot_pos), B, n_kv, 128, cap, K)   # layers 2 and 3 only
+    torch.cuda.synchronize()
+    for b in range(B):
+        got = slots[b].cpu().numpy()
+        want = np.full_like(got, 7)
+        bits = caches[b][0]
+        for l in range(max(2, layer0[b]), 4):
+            lr = l - layer0[b]
+            for g in range(n_kv):
+                for s_ in range(K):
+                    p_ = slot_pos[b, g, s_]
+                    if 0 <= p_ < cap:
+                        want[lr, :, g, s_] = bits[lr, :, g, p_]
+        assert np.array_equal(got, want), f"request {b}"
+
+
 def _attn_case(rng, L, B, n_q, n_kv, K, cap, use_slots, n_valid=None, empty_group=False):
     """Returns GPU output and oracle output for one attention launch."""
     d = 128

@@ -31,9 +31,9 @@ def oracle_stores(cfg, L):
     return stores
 
 
-def run_chain(cfg, steps, L, layers_per_launch=1):
+def run_chain(cfg, steps, L, layers_per_launch=1, on_step=None, **pipe_kw):
     inp = make_inputs(cfg, steps=steps, n_layers=L)
-    pipe = DecodePipeline(cfg, inp, n_layers=L, layers_per_launch=layers_per_launch)
+    pipe = DecodePipeline(cfg, inp, n_layers=L, layers_per_launch=layers_per_launch, **pipe_kw)
     stores = oracle_stores(cfg, L)
     ost = O.DecodeState(inp.K_dlm, inp.lens, stores, pipe.gpu_layers, cfg.budget, cfg.n_sink,
                         cfg.n_recent)
@@ -42,6 +42,16 @@ def run_chain(cfg, steps, L, layers_per_launch=1):
     pipe.prologue()
     diverged = np.zeros((cfg.B, cfg.n_kv), bool)
     swaps_total = 0
+    # the prologue's selection S_0 is held to the same tie band; a head whose
+    # S_0 swapped a tie attends over a (validly) different set from step 0 on
+    gsel0 = pipe.selected[0].cpu().numpy()
+    for b in range(cfg.B):
+        for g in range(cfg.n_kv):
+            ok, sw, msg = selection_within_tie_band(gsel0[b, g], osel[b][g], oss[b][g], cfg.budget,
+                                                    cfg.n_sink, cfg.n_recent)
+            assert ok, f"prologue b={b} g={g}: {msg}"
+            swaps_total += sw
+            diverged[b, g] |= sw > 0
     scale = 1 / math.sqrt(cfg.d)
     for t in range(steps):
         p, pn = t % 2, (t + 1) % 2
@@ -49,6 +59,8 @@ def run_chain(cfg, steps, L, layers_per_launch=1):
         pipe.step(t)
         pipe.join()
         torch.cuda.synchronize()
+        if on_step is not None:
+            on_step(t, pipe)
         _, _, _, oss, osel = ost.score_select(inp.x[t + 1], inp.Wq, inp.Wk, cfg.n_q, append=cfg.append)
         oout = ost.attention(inp.q_llm[t, :L], scale)
         loads = ost.diff_and_gather(osel)
@@ -83,9 +95,9 @@ def run_chain(cfg, steps, L, layers_per_launch=1):
                 assert set(gslot[b, g][gslot[b, g] >= 0].tolist()) == set(gsel[b, g][gsel[b, g] >= 0].tolist())
         # slots hold the rows their slot map names, byte for byte (host layers)
         for b in range(cfg.B):
-            if pipe.slots[b] is None:
+            if pipe.host_slots(b) is None:
                 continue
-            sl = pipe.slots[b].cpu().numpy().view(np.uint16)
+            sl = pipe.host_slots(b).cpu().numpy().view(np.uint16)
             h0 = pipe.gpu_layers[b]
             for g in range(cfg.n_kv):
                 held = gslot[b, g]
@@ -138,6 +150,47 @@ def test_chain_cfg5_70b_shape_hbm_and_host_layers():
 def test_chain_cfg5_mqa_full_shape():
     cfg = scaled(CONFIGS["cfg5mqa"], n_layers=2, steps=1)
     run_chain(cfg, 1, 2, layers_per_launch=2)
+
+
+def _growing_small(steps=8):
+    from tests.gpu_cases import workload
+    return workload(name="c3_small", B=2, lens=(100, 98), H=256, n_q=8, n_kv=2, budget=96, n_layers=4,
+                    steps=steps, append=True)
+
+
+@pytest.mark.parametrize("policy", ["progressive", "static"])
+def test_chain_adaptive_offload_crosses_thresholds(policy):
+    # adaptive memory management: a growing context crosses the memory model's
+    # thresholds during the run; every step still matches the oracle (selections,
+    # load lists, slot maps and contents, attention), the number of offloaded
+    # layers follows the rule at every step, and the last layers go first
+    cfg = _growing_small()
+    L, B = 4, cfg.B
+    row = 2 * cfg.n_kv * 128 * 2
+    kv_bytes = B * 408 * row
+    thr = O.offload_thresholds(L, cfg.n_kv, 128, B, cfg.budget, kv_bytes)
+    assert thr[:3] == [103, 105, 109]
+    seen = []
+
+    def on_step(t, pipe):
+        for b in range(B):
+            length = int(cfg.lens[b]) + t + 1
+            n_off = L - pipe.gpu_layers[b]
+            if policy == "progressive":
+                assert n_off == O.layers_to_offload(length, thr, 0)
+                assert O.gpu_kv_bytes(length, n_off, L, cfg.n_kv, 128, B, cfg.budget) <= kv_bytes
+            else:
+                assert n_off == (L if length >= thr[0] else 0)
+        seen.append([L - g for g in pipe.gpu_layers])
+
+    swaps, pipe = run_chain(cfg, 8, L, layers_per_launch=2, on_step=on_step, kv_bytes=kv_bytes,
+                            offload_policy=policy)
+    moved = [(b, l) for (_, b, l) in pipe.offload_log]
+    for b in range(B):
+        layers = [l for (bb, l) in moved if bb == b]
+        assert layers == sorted(layers, reverse=True)          # last layers first
+        assert layers == list(range(L - 1, L - 1 - len(layers), -1))
+    assert seen[-1] != seen[0]                                  # something moved during the run
 
 
 def _state(pipe):

@@ -330,6 +330,95 @@ def check_attention_special(attn_fn):
 
 
 # ----------------------------------------------------------------- the pins
+# ---------------------------------------------------------------- C3 memory model
+def _offload_cases():
+    rng = np.random.default_rng(21)
+    for _ in range(40):
+        L = int(rng.integers(1, 9))
+        n_kv = int(rng.integers(1, 4))
+        d = int(rng.choice([2, 4, 8]))
+        B = int(rng.integers(1, 4))
+        K = int(rng.integers(1, 12))
+        row = 2 * n_kv * d * 2
+        # between "all workspaces just fit" and "the whole context fits 3x over"
+        kv = int(B * row * rng.integers(L * K, L * K * 6 + 2))
+        yield L, n_kv, d, B, K, kv
+
+
+def check_offload_bruteforce(thr_fn):
+    """For every length, the rule applied from the thresholds gives the fewest
+    offloaded (last) layers whose GPU footprint fits the memory, found by trying
+    every count."""
+    for L, n_kv, d, B, K, kv in _offload_cases():
+        thr = thr_fn(L, n_kv, d, B, K, kv)
+        n = 0
+        for length in range(1, 40 * K + 40):
+            n = O.layers_to_offload(length, thr, n)
+            best = next(k for k in range(L + 1) if O.gpu_kv_bytes(length, k, L, n_kv, d, B, K) <= kv)
+            if n != best:
+                return False
+    return True
+
+
+def check_offload_boundaries(thr_fn):
+    """At threshold[k] - 1 the footprint with k offloaded layers fits; at
+    threshold[k] it does not; thresholds never decrease."""
+    for L, n_kv, d, B, K, kv in _offload_cases():
+        thr = thr_fn(L, n_kv, d, B, K, kv)
+        if thr[L] is not None or any(thr[k] > thr[k + 1] for k in range(L - 1)):
+            return False
+        for k in range(L):
+            if O.gpu_kv_bytes(thr[k] - 1, k, L, n_kv, d, B, K) > kv:
+                return False
+            if thr[k] > K and O.gpu_kv_bytes(thr[k], k, L, n_kv, d, B, K) <= kv:
+                return False
+    return True
+
+
+def check_offload_pages_example(thr_fn):
+    """[Blog] §7 / [Summary] §6.2.1 narrative on a Llama3-8B-shaped model (32
+    layers, 8 KV heads, d 128): below the first threshold every layer keeps its
+    full KV on the GPU; past it the last layer (index 31) goes to the CPU;
+    between the second and the third thresholds the last two are on the CPU."""
+    L = 32
+    thr = thr_fn(L, 8, 128, 1, 2048, 8 << 30)
+    offl = lambda length: O.layers_to_offload(length, thr, 0)
+    if offl(thr[0] - 1) != 0 or offl(thr[0]) != 1:
+        return False
+    if list(range(L - offl(thr[0]), L)) != [31]:
+        return False
+    mid = (thr[1] + thr[2]) // 2
+    return offl(mid) == 2 and list(range(L - offl(mid), L)) == [30, 31]
+
+
+def test_offload_thresholds_bruteforce():
+    assert check_offload_bruteforce(O.offload_thresholds)
+
+
+def test_offload_thresholds_boundaries():
+    assert check_offload_boundaries(O.offload_thresholds)
+
+
+def test_offload_follows_the_pages_example():
+    assert check_offload_pages_example(O.offload_thresholds)
+
+
+def test_offload_infeasible_memory_is_rejected():
+    with pytest.raises(ValueError):
+        O.offload_thresholds(32, 8, 128, 2, 2048, 2 * 32 * 2048 * 4096 - 1)
+    O.offload_thresholds(32, 8, 128, 2, 2048, 2 * 32 * 2048 * 4096)
+
+
+def test_offload_rule_is_monotone_along_a_growing_context():
+    thr = O.offload_thresholds(8, 2, 16, 3, 50, 3 * 2 * 2 * 16 * 2 * 900)
+    n, prev = 0, 0
+    for length in range(1, 2000):
+        n = O.layers_to_offload(length, thr, n)
+        assert n >= prev
+        assert O.gpu_kv_bytes(length, n, 8, 2, 16, 3, 50) <= 3 * 2 * 2 * 16 * 2 * 900
+        prev = n
+
+
 def test_bf16_decode_known_values():
     assert O.bf16_to_f64(np.array([0x3F80, 0xC000, 0x4049, 0x0000, 0x8000], np.uint16)).tolist() == \
         [1.0, -2.0, 3.140625, 0.0, -0.0]
@@ -555,6 +644,18 @@ def _mut_attn_k_for_v(q_bits, K_bits, V_bits, rows, scale):
     return O.sparse_attention(q_bits, K_bits, K_bits, rows, scale)
 
 
+def _mut_offload_last_fit(L, n_kv, d, B, K, kv):
+    """Threshold at the longest length that still fits (off by one)."""
+    thr = O.offload_thresholds(L, n_kv, d, B, K, kv)
+    return [t - 1 if t is not None else None for t in thr]
+
+
+def _mut_offload_no_workspace(L, n_kv, d, B, K, kv):
+    """Offloaded layers counted as free (the budget workspace dropped)."""
+    per_req = kv // (B * O.kv_row_bytes(n_kv, d))
+    return [per_req // (L - k) + 1 for k in range(L)] + [None]
+
+
 MUTANTS = [
     ("round truncates", [check_bf16_golden, check_bf16_bruteforce], _mut_round_truncate),
     ("round half up", [check_bf16_golden, check_bf16_bruteforce], _mut_round_half_up),
@@ -569,6 +670,9 @@ MUTANTS = [
     ("reload everything", [check_diff_invariants, check_diff_worked_example], _mut_diff_reload_all),
     ("attention without normaliser", [check_attention_vs_sdpa, check_attention_special], _mut_attn_no_softmax_norm),
     ("K used as V", [check_attention_vs_sdpa, check_attention_subset_vs_sdpa], _mut_attn_k_for_v),
+    ("offload threshold off by one", [check_offload_bruteforce, check_offload_boundaries], _mut_offload_last_fit),
+    ("offloaded layer keeps no workspace", [check_offload_bruteforce, check_offload_boundaries],
+     _mut_offload_no_workspace),
 ]
 
 
