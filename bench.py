@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="cfg2")
     ap.add_argument("--layers-per-launch", type=int, default=16)
+    ap.add_argument("--layers", type=int, default=None,
+                    help="LLM layers to run (default: the workload's); the JSON line states it")
     ap.add_argument("--gather-streams", type=int, default=2, choices=[1, 2])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -388,9 +390,10 @@ def our_arm(args, rank, world, local):
     cfg = CONFIGS[args.config]
     W, K = max(3, args.warmup), args.steps
     log("generating inputs")
-    inp = make_inputs(cfg, steps=W + K + 1)
+    n_layers = cfg.n_layers if args.layers is None else max(1, min(args.layers, cfg.n_layers))
+    inp = make_inputs(cfg, steps=W + K + 1, n_layers=n_layers)
     log("allocating and filling the pinned host store")
-    pipe = DecodePipeline(cfg, inp, layers_per_launch=args.layers_per_launch, timing=False,
+    pipe = DecodePipeline(cfg, inp, n_layers=n_layers, layers_per_launch=args.layers_per_launch, timing=False,
                           gather_streams=args.gather_streams)
     log("pipeline ready")
     if args.profile:
@@ -493,7 +496,7 @@ def our_arm(args, rank, world, local):
 
     # algorithmic bytes
     nl = np.stack(nl_steps)                                        # [n_eager][B][n_kv]
-    host_layers = np.array([cfg.n_layers - pipe.gpu_layers[b] for b in range(cfg.B)])
+    host_layers = np.array([pipe.L - pipe.gpu_layers[b] for b in range(cfg.B)])
     gathered = int((nl.sum(axis=2) * host_layers[None, :]).sum() * 2 * 256)
     full_reload = int(n_eager * cfg.B * cfg.n_kv * cfg.budget * host_layers.mean() * 2 * 256)
     overlap = 1.0 - nl.sum() / (n_eager * cfg.B * cfg.n_kv * min(cfg.budget, min(cfg.lens)))
@@ -527,7 +530,7 @@ def our_arm(args, rank, world, local):
                            "unit": "GB/s", "frac": round(a / zc_peak, 3) if zc_peak else None,
                            "algorithmic_bytes": int(per_launch), "mean_us": round(kern["gather"]["mean_us"], 2)}
     if "attention" in kern:
-        per_launch = attn_bytes_per_layer * args.layers_per_launch
+        per_launch = attn_bytes_per_layer * (pipe.chunks[0][1] - pipe.chunks[0][0])
         a = gbs(per_launch, kern["attention"]["mean_us"])
         kinfo["attention"] = {"bound": "hbm", "achieved": round(a, 1), "peak": hbm_peak, "unit": "GB/s",
                               "frac": round(a / hbm_peak, 3) if hbm_peak else None,
@@ -607,9 +610,13 @@ def our_arm(args, rank, world, local):
     if rank != 0:
         return
     config = describe(cfg)
+    if n_layers != cfg.n_layers:
+        config["layers"] = n_layers
+        config["layers_note"] = f"{n_layers} of the workload's {cfg.n_layers} layers"
     config.update({"layers_per_launch": args.layers_per_launch, "gather_streams": args.gather_streams,
-                   "l2": "inputs larger than L2: each step reads the 64 MiB key cache, 256 MiB of "
-                         "slots and writes the gathered rows (> 129 MB L2)",
+                   "l2": (f"inputs larger than L2: each step reads the {scan_bytes / 2**20:.0f} MiB key cache "
+                          f"and {attn_bytes_per_layer * n_layers / 2**20:.0f} MiB of K/V rows and writes the "
+                          f"gathered rows (> 129 MB L2)"),
                    "graph": "CUDA graph per step range, two streams", "kernel_timing": timing_src})
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
