@@ -275,9 +275,11 @@ def isolated_times(pipe, spc, torch, t_last: int, reps: int = 20) -> dict:
             fn()
         torch.cuda.synchronize()
         out[name] = max(0.0, (replay(graph(fn)) - t_flush) / reps)
-    n_rows = int(pipe.n_load[pn].sum().item())
+    # rows the timed gather moved: each request's loads times its host layers in the chunk
+    nl_b = pipe.n_load[pn].sum(dim=1).cpu().tolist()
+    moved = sum(int(n) * max(0, l1 - max(l0, pipe.gpu_layers[b])) * 2 for b, n in enumerate(nl_b))
     del flush
-    return {"us": out, "gather_rows": n_rows, "gather_layers": l1 - l0, "attn_layers": l1 - l0}
+    return {"us": out, "gather_moved_rows": moved, "attn_layers": l1 - l0}
 
 
 def hbm_read_peak(spc, torch):
@@ -546,7 +548,7 @@ def our_arm(args, rank, world, local):
     iso = isolated_times(pipe, spc, torch, t_last=W + K - 1)
     iso_bytes = {"key_scan": (scan_bytes, hbm_peak),
                  "attention": (attn_bytes_per_layer * iso["attn_layers"], hbm_peak),
-                 "gather": (iso["gather_rows"] * iso["gather_layers"] * 2 * 256, zc_peak)}
+                 "gather": (iso["gather_moved_rows"] * 256, zc_peak)}
     for k, us in iso["us"].items():
         r = kinfo.setdefault(k, {})
         r["isolated_us"] = round(us, 2)

@@ -168,25 +168,36 @@ int spc_elastic_diff(const int32_t* selected, const int32_t* slot_pos_prev,
  *
  * For model layers l in [layer_lo, layer_hi) held in host memory by request b
  * (view.layer0 <= l < view.layer0 + view.n_layers), for kv in {K, V}, KV head
- * g and i < n_load[b,g]:
- *   slots[l', kv, g, load_slot[b,g,i], :] = host[l', kv, g, load_pos[b,g,i], :]
- * with l' = l - view.layer0. Each row is d bf16 (256 bytes), copied bit-exact.
+ * g and i < n_load[b,g], with p = load_pos[b,g,i] and s = load_slot[b,g,i]:
+ *   slots[l - view.layer0, kv, g, s, :] = host[p, g, l - view.store_layer0, kv, :]
+ * Each row is d bf16 (256 bytes), copied bit-exact.
  *
  * views      device array [B] of spc_gather_view.
  * host       device-visible address of mapped pinned host memory (see
- *            spc_host_device_pointer), bf16 [n_layers][2][n_kv][cap][d],
- *            16-byte aligned.
- * slots      device memory bf16 [n_layers][2][n_kv][budget][d], 16-byte aligned.
+ *            spc_host_device_pointer), POSITION-MAJOR:
+ *            bf16 [cap][n_kv][view.store_layers][2][d], 16-byte aligned. One
+ *            (position, KV head) holds every stored layer's K and V row
+ *            contiguously, so a load reads one run of 512 bytes per layer
+ *            from a single host page: the GPU translates host addresses page
+ *            by page over the link, and a layer-major store made every
+ *            scattered row a separate page (measured: 13-22 GB/s once a step
+ *            touched ~100 000 pages of a 64 GiB store, against ~180 GB/s).
+ *            store_layer0 is the model layer of the store's layer 0.
+ * slots      device memory bf16 [view.n_layers][2][n_kv][budget][d] for layers
+ *            [view.layer0, view.layer0 + view.n_layers), 16-byte aligned.
  * The slots being overwritten must not be read concurrently: order this call
  * after the attention that reads the previous contents (an event).
- * Limits: B * n_kv <= 1024, budget <= 4096.
+ * Limits: B * n_kv <= 1024, budget <= 4096; the view's host layers must lie
+ * inside the store (store_layer0 <= layer0 and layer0 + n_layers <=
+ * store_layer0 + store_layers), else the layer is skipped.
  * ---------------------------------------------------------------------- */
 typedef struct spc_gather_view {
   const void* host;
   void* slots;
   int32_t layer0;
   int32_t n_layers;
-  int64_t reserved;
+  int32_t store_layer0;
+  int32_t store_layers;
 } spc_gather_view;
 
 int spc_gather_kv(const spc_gather_view* views, int layer_lo, int layer_hi,
@@ -220,16 +231,27 @@ int spc_gather_kv(const spc_gather_view* views, int layer_lo, int layer_hi,
  * held by request b's view (view.layer0 <= l < view.layer0 + view.n_layers),
  * kv in {K, V}, KV head g and slot s with 0 <= p = slot_pos[b,g,s] < cap:
  *   view.slots[l', kv, g, s, :] = view.host[l', kv, g, p, :],  l' = l - view.layer0
- * view.host may be device memory (the layer's HBM cache, the usual source) or
- * a device-visible host address; both bf16 [n_layers][2][n_kv][cap or budget][d],
- * 16-byte aligned. slot_pos int32 [B][n_kv][budget]. Rows are copied bit-exact.
- * Limits as spc_gather_kv.
+ * Here view.host is a LAYER-MAJOR cache bf16 [n_layers][2][n_kv][cap][d] (the
+ * layer's HBM cache, the usual source; a device-visible host address also
+ * works); store_layer0 / store_layers are not used. slots bf16
+ * [n_layers][2][n_kv][budget][d]; slot_pos int32 [B][n_kv][budget]. Rows are
+ * copied bit-exact. Limits as spc_gather_kv.
+ *
+ * spc_store_layer: writes one layer's layer-major cache into a position-major
+ * host store (the copy half of an offload):
+ *   store[p, g, layer, kv, :] = src[kv, g, p, :]   for p < rows, every g, kv,
+ * src bf16 [2][n_kv][cap][d] (device memory), store the device-visible address
+ * of bf16 [cap][n_kv][store_layers][2][d]; 0 <= layer < store_layers,
+ * rows <= cap. A kernel copy (no copy engine), 16-byte aligned addresses.
  * ---------------------------------------------------------------------- */
 int spc_offload_thresholds(int n_layers, int n_kv, int d, int B, int budget, int64_t kv_bytes,
                            int64_t* thresholds);
 
 int spc_fill_slots(const spc_gather_view* views, int layer_lo, int layer_hi, const int32_t* slot_pos,
                    int B, int n_kv, int d, int cap, int budget, void* stream);
+
+int spc_store_layer(void* store, const void* src, int n_kv, int d, int cap, int rows, int store_layers,
+                    int layer, void* stream);
 
 /* ------------------------------------------------------------------------
  * Sparse GQA decode attention over the resident budget. [Blog] §2 formula

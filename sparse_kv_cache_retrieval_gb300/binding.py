@@ -22,7 +22,7 @@ STATUS_NAMES = {0: "SPC_OK", -1: "SPC_ERR_INVALID_ARG", -2: "SPC_ERR_SHAPE", -3:
 
 # struct layouts of include/spc.h (32 bytes each)
 GATHER_VIEW_DTYPE = np.dtype([("host", "<u8"), ("slots", "<u8"), ("layer0", "<i4"),
-                              ("n_layers", "<i4"), ("reserved", "<i8")])
+                              ("n_layers", "<i4"), ("store_layer0", "<i4"), ("store_layers", "<i4")])
 KV_VIEW_DTYPE = np.dtype([("k", "<u8"), ("v", "<u8"), ("rows", "<i8"), ("use_slots", "<i4"),
                           ("reserved", "<i4")])
 
@@ -50,6 +50,7 @@ SIGNATURES = {
     "spc_stream_read": (_I, [_P, ctypes.c_size_t, _P, _I, _P]),
     "spc_copy": (_I, [_P, _P, ctypes.c_size_t, _P]),
     "spc_fill_slots": (_I, [_P, _I, _I, _P, _I, _I, _I, _I, _I, _P]),
+    "spc_store_layer": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "spc_offload_thresholds": (_I, [_I, _I, _I, _I, _I, ctypes.c_int64, ctypes.POINTER(ctypes.c_int64)]),
 }
 
@@ -199,6 +200,11 @@ def spc_fill_slots(views, layer_lo, layer_hi, slot_pos, B, n_kv, d, cap, budget,
                                                   n_kv, d, cap, budget, _stream(stream)))
 
 
+def spc_store_layer(store, src, n_kv, d, cap, rows, store_layers, layer, stream=None) -> None:
+    _check("spc_store_layer", lib().spc_store_layer(_ptr(store), _ptr(src), n_kv, d, cap, rows, store_layers,
+                                                    layer, _stream(stream)))
+
+
 def spc_offload_thresholds(n_layers, n_kv, d, B, budget, kv_bytes) -> list:
     """Host-side memory model: n_layers + 1 context-length thresholds (the
     last one is INT64_MAX)."""
@@ -214,9 +220,14 @@ def spc_device_sm_count() -> int:
 
 # ------------------------------------------------------------------ view tables
 def gather_views(host_ptrs: Sequence[int], slot_ptrs: Sequence[int], layer0: Sequence[int],
-                 n_layers: Sequence[int]) -> np.ndarray:
+                 n_layers: Sequence[int], store_layer0: Optional[Sequence[int]] = None,
+                 store_layers: Optional[Sequence[int]] = None) -> np.ndarray:
+    """spc_gather_view table. By default a request's store holds exactly its
+    host layers (store_layer0 = layer0, store_layers = n_layers)."""
     v = np.zeros(len(host_ptrs), GATHER_VIEW_DTYPE)
     v["host"], v["slots"], v["layer0"], v["n_layers"] = host_ptrs, slot_ptrs, layer0, n_layers
+    v["store_layer0"] = layer0 if store_layer0 is None else store_layer0
+    v["store_layers"] = n_layers if store_layers is None else store_layers
     return v
 
 

@@ -204,6 +204,16 @@ int spc_fill_slots(const spc_gather_view* views, int layer_lo, int layer_hi, con
   return fill_slots_launch(views, layer_lo, layer_hi, slot_pos, B, n_kv, cap, budget, stream);
 }
 
+int spc_store_layer(void* store, const void* src, int n_kv, int d, int cap, int rows, int store_layers,
+                    int layer, void* stream) {
+  if (!store || !src) return SPC_ERR_INVALID_ARG;
+  if (!aligned16(store) || !aligned16(src)) return SPC_ERR_INVALID_ARG;
+  if (d != SPC_HEAD_DIM) return SPC_ERR_SHAPE;
+  if (n_kv < 1 || n_kv > 1024 || cap < 1 || cap > SPC_MAX_CAP || rows < 0 || rows > cap) return SPC_ERR_SHAPE;
+  if (store_layers < 1 || layer < 0 || layer >= store_layers) return SPC_ERR_SHAPE;
+  return store_layer_launch(store, src, n_kv, cap, rows, store_layers, layer, stream);
+}
+
 int spc_offload_thresholds(int n_layers, int n_kv, int d, int B, int budget, int64_t kv_bytes,
                            int64_t* thresholds) {
   if (!thresholds) return SPC_ERR_INVALID_ARG;

@@ -9,15 +9,19 @@
 // (paperlayer.ai summary) §5.1, §5.4 (loads performed in place).
 //
 // GB300 design: the host store is mapped pinned memory read over the
-// NVLink-C2C / PCIe link by ordinary 16-byte loads. A work item is one
-// 256-byte row (one layer, K or V, one KV head, one position) copied by a
-// half-warp; items are laid out (layer, K/V, flattened load index) and spread
-// over a grid-stride loop with 4 rows in flight per half-warp. The link
-// saturates with about 0.5 MB in flight, which a small grid (one CTA of 512
-// threads per 8 SMs) already keeps: the rest of the GPU stays free for the
-// kernels that run beside the gather on the other stream (attention, key
-// scan). The flattened load index j maps back to (request, KV head, i)
-// through a prefix sum of n_load kept in shared memory.
+// NVLink-C2C link by ordinary 16-byte loads, laid out position-major
+// ([cap][n_kv][layers][2][d]): the GPU translates host addresses page by page
+// across the link, and a load of position p for KV head g reads the K and V
+// rows of every layer of the launch as one contiguous run from one page. A
+// work item is one 256-byte row (one load, one layer, K or V) copied by a
+// half-warp; items are ordered (load, layer, K/V), so consecutive half-warps
+// stream consecutive bytes of the host store, and spread over a grid-stride
+// loop with 4 rows in flight per half-warp. The link saturates with about
+// 0.5 MB in flight, which a small grid (one CTA of 512 threads per 8 SMs)
+// already keeps: the rest of the GPU stays free for the kernels that run
+// beside the gather on the other stream (attention, key scan). The flattened
+// load index maps back to (request, KV head, i) through a prefix sum of
+// n_load kept in shared memory.
 #include "spc_device.cuh"
 #include "spc_internal.h"
 
@@ -59,8 +63,9 @@ gather_kernel(const spc_gather_view* __restrict__ views, int layer_lo, int layer
   __syncthreads();
 
   const int R = run;
-  const int per_layer = 2 * R;
-  const int total = (layer_hi - layer_lo) * per_layer;   // host limits keep this < 2^31
+  const int NL = layer_hi - layer_lo;
+  const int per_load = 2 * NL;                           // rows of one load: every layer, K and V
+  const int total = R * per_load;                        // host limits keep this < 2^31
   const int l16 = tid & 15;
   const int hw0 = (blockIdx.x * kGatherThreads + tid) >> 4;
   const int nhw = (gridDim.x * kGatherThreads) >> 4;
@@ -70,6 +75,7 @@ gather_kernel(const spc_gather_view* __restrict__ views, int layer_lo, int layer
   // (C) store it to its slot. A runs one batch ahead of B, so the load of the
   // indices hides behind the previous batch's host round trip.
   int pos_n[kGatherUnroll], slot_n[kGatherUnroll];
+  uint32_t hstride_n[kGatherUnroll];
   const uint16_t* hbase_n[kGatherUnroll];
   uint16_t* sbase_n[kGatherUnroll];
   auto stage_a = [&](int item0) {
@@ -81,11 +87,10 @@ gather_kernel(const spc_gather_view* __restrict__ views, int layer_lo, int layer
       pos_n[u] = 0;
       slot_n[u] = 0;
       if (item >= total) continue;
-      const int lq = item / per_layer;
-      const int layer = layer_lo + lq;
-      const int rem = item - lq * per_layer;
-      const int kv = rem >= R ? 1 : 0;
-      const int j = rem - kv * R;
+      const int j = item / per_load;
+      const int rem = item - j * per_load;
+      const int layer = layer_lo + (rem >> 1);
+      const int kv = rem & 1;
       // largest seg with pre[seg] <= j (segments with no load have equal bounds)
       int lo = 0, hi = nseg - 1;
       while (lo < hi) {
@@ -96,14 +101,16 @@ gather_kernel(const spc_gather_view* __restrict__ views, int layer_lo, int layer
       const int b = seg / n_kv, g = seg - b * n_kv;
       const spc_gather_view vw = sv[b];
       const int lrel = layer - vw.layer0;
-      if (lrel < 0 || lrel >= vw.n_layers) continue;
+      const int lst = layer - vw.store_layer0;
+      if (lrel < 0 || lrel >= vw.n_layers || lst < 0 || lst >= vw.store_layers) continue;
       const size_t li = (size_t)seg * K + i;
       pos_n[u] = load_pos[li];
       slot_n[u] = load_slot[li];
-      const size_t hseg = (((size_t)lrel * 2 + kv) * n_kv + g) * cap;
-      const size_t sseg = (((size_t)lrel * 2 + kv) * n_kv + g) * K;
-      hbase_n[u] = static_cast<const uint16_t*>(vw.host) + hseg * kD + l16 * 8;
-      sbase_n[u] = static_cast<uint16_t*>(vw.slots) + sseg * kD + l16 * 8;
+      // host row (p, g, lst, kv) = ((p * n_kv + g) * store_layers + lst) * 2 + kv
+      hbase_n[u] = static_cast<const uint16_t*>(vw.host) +
+                   (((size_t)g * vw.store_layers + lst) * 2 + kv) * kD + l16 * 8;
+      sbase_n[u] = static_cast<uint16_t*>(vw.slots) + ((((size_t)lrel * 2 + kv) * n_kv + g) * K) * kD + l16 * 8;
+      hstride_n[u] = (uint32_t)n_kv * (uint32_t)vw.store_layers * 2u * kD;   // elements per position
     }
   };
 
@@ -115,7 +122,7 @@ gather_kernel(const spc_gather_view* __restrict__ views, int layer_lo, int layer
     for (int u = 0; u < kGatherUnroll; ++u) {   // stage B of this batch
       dst[u] = nullptr;
       if (!hbase_n[u]) continue;
-      v[u] = ldg_stream(hbase_n[u] + (size_t)pos_n[u] * kD);
+      v[u] = ldg_stream(hbase_n[u] + (size_t)pos_n[u] * hstride_n[u]);
       dst[u] = sbase_n[u] + (size_t)slot_n[u] * kD;
     }
     stage_a(item0 + nhw * kGatherUnroll);       // stage A of the next batch
@@ -169,6 +176,37 @@ int fill_slots_launch(const spc_gather_view* views, int layer_lo, int layer_hi, 
   if (grid < 1) grid = 1;
   fill_slots_kernel<<<(int)grid, kFillThreads, 0, static_cast<cudaStream_t>(stream)>>>(
       views, layer_lo, layer_hi, slot_pos, B, n_kv, cap, budget);
+  return cudaGetLastError() == cudaSuccess ? SPC_OK : SPC_ERR_CUDA;
+}
+
+// One layer of a layer-major cache ([2][n_kv][cap][d], device memory) into a
+// position-major host store ([cap][n_kv][store_layers][2][d]): one 256-byte
+// row per half-warp, items in store order (position, KV head, K/V) so each
+// (position, head) pair is written as one 512-byte run.
+__global__ void __launch_bounds__(kFillThreads)
+store_layer_kernel(uint16_t* __restrict__ store, const uint16_t* __restrict__ src, int n_kv, int cap, int rows,
+                   int store_layers, int layer) {
+  const int l16 = threadIdx.x & 15;
+  const long long total = (long long)rows * n_kv * 2;
+  const long long nhw = (long long)gridDim.x * (kFillThreads / 16);
+  for (long long item = ((long long)blockIdx.x * kFillThreads + threadIdx.x) >> 4; item < total; item += nhw) {
+    const long long p = item / (2 * n_kv);
+    const int rem = (int)(item - p * 2 * n_kv);
+    const int g = rem >> 1, kv = rem & 1;
+    const uint4 v = ldg_stream(src + (((size_t)kv * n_kv + g) * cap + p) * kD + l16 * 8);
+    stg_v4(store + ((((size_t)p * n_kv + g) * store_layers + layer) * 2 + kv) * kD + l16 * 8, v);
+  }
+}
+
+int store_layer_launch(void* store, const void* src, int n_kv, int cap, int rows, int store_layers, int layer,
+                       void* stream) {
+  if (rows <= 0) return SPC_OK;
+  const long long items = (long long)rows * n_kv * 2;
+  long long grid = (items + (kFillThreads / 16) - 1) / (kFillThreads / 16);
+  const long long cap_grid = 2LL * std::max(1, device_sm_count());
+  if (grid > cap_grid) grid = cap_grid;
+  store_layer_kernel<<<(int)grid, kFillThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<uint16_t*>(store), static_cast<const uint16_t*>(src), n_kv, cap, rows, store_layers, layer);
   return cudaGetLastError() == cudaSuccess ? SPC_OK : SPC_ERR_CUDA;
 }
 

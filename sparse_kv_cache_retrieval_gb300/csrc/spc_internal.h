@@ -38,6 +38,9 @@ int gather_launch(const spc_gather_view* views, int layer_lo, int layer_hi, cons
 int fill_slots_launch(const spc_gather_view* views, int layer_lo, int layer_hi, const int32_t* slot_pos,
                       int B, int n_kv, int cap, int budget, void* stream);
 
+int store_layer_launch(void* store, const void* src, int n_kv, int cap, int rows, int store_layers, int layer,
+                       void* stream);
+
 size_t attn_workspace(int n_layers, int B, int n_q, int n_kv, int budget);
 int attn_launch(const void* q, const spc_kv_view* views, const int32_t* selected,
                 const int32_t* slot_pos, int n_layers, int B, int n_q, int n_kv, int budget,

@@ -37,7 +37,7 @@ import torch
 
 from . import binding as spc
 from .configs import Workload
-from .synth import Inputs, fill_llm_kv
+from .synth import Inputs, fill_llm_kv, fill_llm_kv_store
 
 _BF16_ROW = 256  # bytes of one K or V row at d = 128
 
@@ -137,9 +137,11 @@ class DecodePipeline:
                 del buf
             self.hbm.append(layers)
             if L - s0 > 0:
-                hs = torch.empty((L - s0, 2, n_kv, cap, d), dtype=torch.int16, pin_memory=True)
+                # position-major [cap][n_kv][layers][2][d]: one (position, head)
+                # holds every stored layer's K and V row in one host page
+                hs = torch.empty((cap, n_kv, L - s0, 2, d), dtype=torch.int16, pin_memory=True)
                 if L - ng > 0:
-                    fill_llm_kv(cfg, b, ng, hs.numpy().view(np.uint16)[ng - s0:], threads=fill_threads)
+                    fill_llm_kv_store(cfg, b, ng, L, hs.numpy().view(np.uint16), s0, threads=fill_threads)
                 self.host_stores.append(hs)
                 self.slots.append(torch.zeros((L - s0, 2, n_kv, K, d), dtype=torch.int16, device=dev))
                 self._store_dev.append(spc.spc_host_device_pointer(hs))
@@ -148,7 +150,6 @@ class DecodePipeline:
                 self.slots.append(None)
                 self._store_dev.append(0)
             self.store_base.append(s0)
-        self._layer_bytes = 2 * n_kv * cap * d * 2
         self._slot_layer_bytes = 2 * n_kv * K * d * 2
         self.gviews = spc.to_device_bytes(self._gather_view_table(), dev)
 
@@ -208,18 +209,20 @@ class DecodePipeline:
 
     # ------------------------------------------------------------------ layout
     def _gather_view_table(self) -> np.ndarray:
-        host, slots, layer0, n_host = [], [], [], []
+        host, slots, layer0, n_host, st0, stn = [], [], [], [], [], []
         for b in range(self.B):
             ng, s0 = self.gpu_layers[b], self.store_base[b]
             if self.slots[b] is not None and ng < self.L:
-                host.append(self._store_dev[b] + (ng - s0) * self._layer_bytes)
+                host.append(self._store_dev[b])
                 slots.append(self.slots[b].data_ptr() + (ng - s0) * self._slot_layer_bytes)
             else:
                 host.append(0)
                 slots.append(0)
             layer0.append(ng)
             n_host.append(self.L - ng)
-        return spc.gather_views(host, slots, layer0, n_host)
+            st0.append(s0)
+            stn.append(self.L - s0)
+        return spc.gather_views(host, slots, layer0, n_host, st0, stn)
 
     def _attn_view_row(self, l: int, b: int) -> np.ndarray:
         if l < self.gpu_layers[b]:
@@ -281,11 +284,11 @@ class DecodePipeline:
         s0, sA = self.store_base[b], self.sA
         src = self.hbm[b][l]
         with torch.cuda.stream(sA):
-            # the whole layer, [2][n_kv][cap][d]: rows past the current length
-            # stand for the K/V rows the LLM writes as the context grows (the
-            # workloads prefill them), so the store is complete from here on
-            spc.spc_copy(self._store_dev[b] + (l - s0) * self._layer_bytes, src.data_ptr(), self._layer_bytes,
-                         stream=sA)
+            # every row of the layer up to the capacity: rows past the current
+            # length stand for the K/V rows the LLM writes as the context grows
+            # (the workloads prefill them), so the store is complete from here on
+            spc.spc_store_layer(self._store_dev[b], src, self.n_kv, self.d, self.cap, self.cap, self.L - s0, l - s0,
+                                stream=sA)
             host = [0] * self.B
             slots = [0] * self.B
             n_layers = [0] * self.B

@@ -171,4 +171,29 @@ def fill_llm_kv(cfg: Workload, b: int, layer0: int, out: np.ndarray, threads: Op
         list(ex.map(work, jobs))
 
 
-__all__ = ["Inputs", "make_inputs", "fill_llm_kv", "to_bf16_bits", "bf16_bits_to_f32", "rng_for"]
+def fill_llm_kv_store(cfg: Workload, b: int, layer_lo: int, layer_hi: int, store: np.ndarray,
+                      store_layer0: int, threads: Optional[int] = None) -> None:
+    """The rows of ``fill_llm_kv`` for layers [layer_lo, layer_hi) written into a
+    position-major store, u16 [rows][n_kv][store_layers][2][d] (row p, head g,
+    layer l, K or V at store[p, g, l - store_layer0, kv]); same values as
+    ``fill_llm_kv`` gives the layer-major layout."""
+    rows = store.shape[0]
+    jobs = [(l, kv, g) for l in range(layer_lo, layer_hi) for kv in range(2) for g in range(cfg.n_kv)]
+
+    def work(job):
+        l, kv, g = job
+        tmp = np.empty((rows, cfg.d), np.uint16)
+        _normal_bf16_into(tmp, rng_for(cfg.seed, _TAG_KV, b, l, kv, g))
+        store[:, g, l - store_layer0, kv, :] = tmp
+
+    threads = threads or min(16, os.cpu_count() or 1)
+    if threads <= 1 or len(jobs) <= 1:
+        for j in jobs:
+            work(j)
+        return
+    with cf.ThreadPoolExecutor(threads) as ex:
+        list(ex.map(work, jobs))
+
+
+__all__ = ["Inputs", "make_inputs", "fill_llm_kv", "fill_llm_kv_store", "to_bf16_bits", "bf16_bits_to_f32",
+           "rng_for"]

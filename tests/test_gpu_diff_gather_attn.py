@@ -95,22 +95,29 @@ def test_elastic_diff_partial_selection():
             assert np.array_equal(lp[b, g, :nl[b, g]], olp) and np.array_equal(nxt[b, g], onxt)
 
 
-def test_gather_bit_exact_over_layers_and_requests():
+@pytest.mark.parametrize("whole_store", [False, True])
+def test_gather_bit_exact_over_layers_and_requests(whole_store):
+    # host stores are position-major [cap][n_kv][store_layers][2][d]; with
+    # whole_store every request's store holds all L layers (the adaptive
+    # layout) while only layers >= layer0 are host-resident
     rng = np.random.default_rng(11)
     B, n_kv, K, cap, L = 3, 4, 96, 700, 5
     layer0 = [0, 2, 5]                      # request 2 keeps every layer in HBM
-    stores, slots, hptr, sptr = [], [], [], []
+    stores, slots, hptr, sptr, s0s, sns = [], [], [], [], [], []
     for b in range(B):
         nh = L - layer0[b]
+        s0 = 0 if whole_store else layer0[b]
         if nh == 0:
             stores.append(None); slots.append(None); hptr.append(0); sptr.append(0)
+            s0s.append(s0); sns.append(L - s0)
             continue
-        hs = torch.empty((nh, 2, n_kv, cap, 128), dtype=torch.int16, pin_memory=True)
-        hs.numpy()[:] = rng.integers(-32768, 32767, hs.shape, dtype=np.int16)
+        bits = rng.integers(-32768, 32767, (L - s0, 2, n_kv, cap, 128), dtype=np.int16)   # layer-major
+        hs = torch.from_numpy(np.ascontiguousarray(bits.transpose(3, 2, 0, 1, 4))).pin_memory()
         sl = torch.zeros((nh, 2, n_kv, K, 128), dtype=torch.int16, device=DEV)
-        stores.append(hs); slots.append(sl)
+        stores.append((bits, hs)); slots.append(sl)
         hptr.append(spc.spc_host_device_pointer(hs)); sptr.append(sl.data_ptr())
-    views = spc.to_device_bytes(spc.gather_views(hptr, sptr, layer0, [L - v for v in layer0]), DEV)
+        s0s.append(s0); sns.append(L - s0)
+    views = spc.to_device_bytes(spc.gather_views(hptr, sptr, layer0, [L - v for v in layer0], s0s, sns), DEV)
     sel, prev = random_state(rng, B, n_kv, K, cap, 0.5)
     loads = [[O.elastic_diff(sel[b, g], prev[b, g]) for g in range(n_kv)] for b in range(B)]
     ls = np.zeros((B, n_kv, K), np.int32)
@@ -130,9 +137,25 @@ def test_gather_bit_exact_over_layers_and_requests():
             continue
         got = slots[b].cpu().numpy().view(np.uint16)
         want = np.zeros_like(got)
-        O.gather(stores[b].numpy().view(np.uint16), want, [x[0] for x in loads[b]],
-                 [x[1] for x in loads[b]])
+        bits = stores[b][0].view(np.uint16)[layer0[b] - s0s[b]:]
+        O.gather(bits, want, [x[0] for x in loads[b]], [x[1] for x in loads[b]])
         assert np.array_equal(got, want)
+
+
+def test_store_layer_writes_one_layer_position_major():
+    # the copy half of an offload: a layer-major HBM cache into its layer of a
+    # position-major pinned store, bit-exact, other layers untouched
+    rng = np.random.default_rng(23)
+    n_kv, cap, SL, layer, rows = 4, 300, 5, 3, 260
+    src_bits = rng.integers(-32768, 32767, (2, n_kv, cap, 128), dtype=np.int16)
+    src = torch.from_numpy(src_bits).to(DEV)
+    store = torch.full((cap, n_kv, SL, 2, 128), 5, dtype=torch.int16).pin_memory()
+    spc.spc_store_layer(spc.spc_host_device_pointer(store), src, n_kv, 128, cap, rows, SL, layer)
+    torch.cuda.synchronize()
+    got = store.numpy()
+    want = np.full_like(got, 5)
+    want[:rows, :, layer] = src_bits[:, :, :rows].transpose(2, 1, 0, 3)
+    assert np.array_equal(got, want)
 
 
 @pytest.mark.parametrize("source", ["device", "host"])
