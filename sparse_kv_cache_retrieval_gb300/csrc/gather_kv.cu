@@ -11,17 +11,16 @@
 // GB300 design: the host store is mapped pinned memory read over the
 // NVLink-C2C link by ordinary 16-byte loads, laid out position-major
 // ([cap][n_kv][layers][2][d]): the GPU translates host addresses page by page
-// across the link, and a load of position p for KV head g reads the K and V
-// rows of every layer of the launch as one contiguous run from one page. A
-// work item is one 256-byte row (one load, one layer, K or V) copied by a
-// half-warp; items are ordered (load, layer, K/V), so consecutive half-warps
-// stream consecutive bytes of the host store, and spread over a grid-stride
-// loop with 4 rows in flight per half-warp. The link saturates with about
-// 0.5 MB in flight, which a small grid (one CTA of 512 threads per 8 SMs)
-// already keeps: the rest of the GPU stays free for the kernels that run
-// beside the gather on the other stream (attention, key scan). The flattened
-// load index maps back to (request, KV head, i) through a prefix sum of
-// n_load kept in shared memory.
+// across the link, and one load (position p, KV head g) is a single
+// contiguous run holding the K and V rows of every layer of the launch. One
+// warp streams one load's run: each instruction moves one layer's K row
+// (lanes 0-15) and V row (lanes 16-31), 512 contiguous bytes, with up to 8
+// layers in flight; the (position, slot) pair and the segment search are done
+// once per load. A small grid (one CTA of 512 threads per 8 SMs) keeps about
+// 1 MB in flight, enough for the link, and leaves the rest of the GPU to the
+// kernels that run beside the gather on the other streams (attention, key
+// scan). The flattened load index maps back to (request, KV head, i) through
+// a prefix sum of n_load kept in shared memory.
 #include "spc_device.cuh"
 #include "spc_internal.h"
 
@@ -31,7 +30,7 @@ namespace spc {
 
 constexpr int kGatherThreads = 512;
 #ifndef SPC_GATHER_UNROLL
-#define SPC_GATHER_UNROLL 4
+#define SPC_GATHER_UNROLL 8    // layers of one run in flight per warp
 #endif
 constexpr int kGatherUnroll = SPC_GATHER_UNROLL;
 constexpr int kGatherMaxSeg = 1024;
@@ -63,74 +62,45 @@ gather_kernel(const spc_gather_view* __restrict__ views, int layer_lo, int layer
   __syncthreads();
 
   const int R = run;
-  const int NL = layer_hi - layer_lo;
-  const int per_load = 2 * NL;                           // rows of one load: every layer, K and V
-  const int total = R * per_load;                        // host limits keep this < 2^31
-  const int l16 = tid & 15;
-  const int hw0 = (blockIdx.x * kGatherThreads + tid) >> 4;
-  const int nhw = (gridDim.x * kGatherThreads) >> 4;
-
-  // Three stages per batch of kGatherUnroll rows of this half-warp: (A) locate
-  // each row and load its (position, slot); (B) load the row from the host;
-  // (C) store it to its slot. A runs one batch ahead of B, so the load of the
-  // indices hides behind the previous batch's host round trip.
-  int pos_n[kGatherUnroll], slot_n[kGatherUnroll];
-  uint32_t hstride_n[kGatherUnroll];
-  const uint16_t* hbase_n[kGatherUnroll];
-  uint16_t* sbase_n[kGatherUnroll];
-  auto stage_a = [&](int item0) {
-#pragma unroll
-    for (int u = 0; u < kGatherUnroll; ++u) {
-      const int item = item0 + u * nhw;
-      hbase_n[u] = nullptr;
-      sbase_n[u] = nullptr;
-      pos_n[u] = 0;
-      slot_n[u] = 0;
-      if (item >= total) continue;
-      const int j = item / per_load;
-      const int rem = item - j * per_load;
-      const int layer = layer_lo + (rem >> 1);
-      const int kv = rem & 1;
-      // largest seg with pre[seg] <= j (segments with no load have equal bounds)
-      int lo = 0, hi = nseg - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (pre[mid] <= j) lo = mid; else hi = mid - 1;
-      }
-      const int seg = lo, i = j - pre[seg];
-      const int b = seg / n_kv, g = seg - b * n_kv;
-      const spc_gather_view vw = sv[b];
-      const int lrel = layer - vw.layer0;
-      const int lst = layer - vw.store_layer0;
-      if (lrel < 0 || lrel >= vw.n_layers || lst < 0 || lst >= vw.store_layers) continue;
-      const size_t li = (size_t)seg * K + i;
-      pos_n[u] = load_pos[li];
-      slot_n[u] = load_slot[li];
-      // host row (p, g, lst, kv) = ((p * n_kv + g) * store_layers + lst) * 2 + kv
-      hbase_n[u] = static_cast<const uint16_t*>(vw.host) +
-                   (((size_t)g * vw.store_layers + lst) * 2 + kv) * kD + l16 * 8;
-      sbase_n[u] = static_cast<uint16_t*>(vw.slots) + ((((size_t)lrel * 2 + kv) * n_kv + g) * K) * kD + l16 * 8;
-      hstride_n[u] = (uint32_t)n_kv * (uint32_t)vw.store_layers * 2u * kD;   // elements per position
+  const int lane = tid & 31, piece = lane & 15, kv = lane >> 4;
+  const int w0 = (blockIdx.x * kGatherThreads + tid) >> 5;
+  const int nw = (gridDim.x * kGatherThreads) >> 5;
+  for (int j = w0; j < R; j += nw) {
+    // largest seg with pre[seg] <= j (segments with no load have equal bounds)
+    int lo = 0, hi = nseg - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pre[mid] <= j) lo = mid; else hi = mid - 1;
     }
-  };
-
-  stage_a(hw0);
-  for (int item0 = hw0; item0 < total; item0 += nhw * kGatherUnroll) {
-    uint4 v[kGatherUnroll];
-    uint16_t* dst[kGatherUnroll];
+    const int seg = lo, i = j - pre[seg];
+    const int b = seg / n_kv, g = seg - b * n_kv;
+    const spc_gather_view vw = sv[b];
+    // layers of this launch the request holds in host memory and in its store
+    const int l_begin = max(layer_lo, max(vw.layer0, vw.store_layer0));
+    const int l_end = min(layer_hi, min(vw.layer0 + vw.n_layers, vw.store_layer0 + vw.store_layers));
+    if (l_begin >= l_end) continue;
+    const size_t li = (size_t)seg * K + i;
+    const int pos = __ldg(load_pos + li);
+    const int slot = __ldg(load_slot + li);
+    // the run: store[pos, g, l - store_layer0, kv, :] for l in [l_begin, l_end)
+    const uint16_t* run = static_cast<const uint16_t*>(vw.host) +
+                          (((size_t)pos * n_kv + g) * vw.store_layers + (l_begin - vw.store_layer0)) * 2 * kD +
+                          kv * kD + piece * 8;
+    uint16_t* dst0 = static_cast<uint16_t*>(vw.slots) +
+                     ((((size_t)(l_begin - vw.layer0) * 2 + kv) * n_kv + g) * K + slot) * kD + piece * 8;
+    const size_t dst_layer = (size_t)2 * n_kv * K * kD;     // elements between two layers' slots
+    for (int l0 = 0; l0 < l_end - l_begin; l0 += kGatherUnroll) {
+      uint4 v[kGatherUnroll];
 #pragma unroll
-    for (int u = 0; u < kGatherUnroll; ++u) {   // stage B of this batch
-      dst[u] = nullptr;
-      if (!hbase_n[u]) continue;
-      v[u] = ldg_stream(hbase_n[u] + (size_t)pos_n[u] * hstride_n[u]);
-      dst[u] = sbase_n[u] + (size_t)slot_n[u] * kD;
+      for (int u = 0; u < kGatherUnroll; ++u)
+        if (l0 + u < l_end - l_begin) v[u] = ldg_stream(run + (size_t)(l0 + u) * 2 * kD);
+#pragma unroll
+      for (int u = 0; u < kGatherUnroll; ++u)
+        if (l0 + u < l_end - l_begin) stg_v4(dst0 + (size_t)(l0 + u) * dst_layer, v[u]);
     }
-    stage_a(item0 + nhw * kGatherUnroll);       // stage A of the next batch
-#pragma unroll
-    for (int u = 0; u < kGatherUnroll; ++u)     // stage C of this batch
-      if (dst[u]) stg_v4(dst[u], v[u]);
   }
 }
+
 
 // Slot fill of layers entering the host ([Blog] §7: an offloaded layer keeps a
 // budget-sized workspace on the GPU; it starts out holding the resident rows).
@@ -214,9 +184,9 @@ int gather_launch(const spc_gather_view* views, int layer_lo, int layer_hi, cons
                   const int32_t* load_pos, const int32_t* n_load, int B, int n_kv, int cap,
                   int budget, void* stream) {
   if (layer_hi <= layer_lo) return SPC_OK;
-  const long long max_items = (long long)(layer_hi - layer_lo) * 2 * B * n_kv * budget;
-  const long long per_block = (kGatherThreads / 16) * kGatherUnroll;
-  long long grid = (max_items + per_block - 1) / per_block;
+  const long long max_loads = (long long)B * n_kv * budget;          // one warp per load at a time
+  const long long per_block = kGatherThreads / 32;
+  long long grid = (max_loads + per_block - 1) / per_block;
   const long long cap_grid = std::max(4, device_sm_count() / kGatherSmsPerCta);
   if (grid > cap_grid) grid = cap_grid;
   if (grid < 1) grid = 1;
