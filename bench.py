@@ -147,20 +147,20 @@ class ClockSampler:
 # workload (the summary and its command are in profiles/). A figure is used
 # only while the kernel's source file still hashes to the one captured.
 NCU_TRAFFIC = {
-    # gather of decode step 0, layers 16-31: 1550 loads per KV head x 16 layers x K/V
-    # = 49 600 rows; 396 800 system-memory sectors (12 697 600 B) read over the
-    # host link + 46 592 B DRAM read + 1 024 B DRAM write
+    # gather of decode step 0, layers 16-31: 1550 loads x 16 layers x K/V = 49 600
+    # rows; 396 800 system-memory sectors (12 697 600 B) read over the host link
+    # + 27 136 B DRAM read + 512 B DRAM write
     "gather": {"source": "sparse_kv_cache_retrieval_gb300/csrc/gather_kv.cu",
-               "sha256": "04dab5b41b342fe03b3889fbeddba4406b5510aaaf6ef23eadd4d265a318c548",
-               "bytes_per_unit": (12697600 + 46592 + 1024) / 49600, "unit": "moved 256-byte row"},
-    # key scan over 32 768 positions x 8 KV heads: 67 141 376 B DRAM read + 291 584 B write
+               "sha256": "698bd9e4683f695f1ac27d5225eced8534439a61e22a43b1cf2f692bf1277bfb",
+               "bytes_per_unit": (12697600 + 27136 + 512) / 49600, "unit": "moved 256-byte row"},
+    # key scan over 32 768 positions x 8 KV heads: 67 141 120 B DRAM read + 285 440 B write
     "key_scan": {"source": "sparse_kv_cache_retrieval_gb300/csrc/score_select.cu",
-                 "sha256": "a9f6f12e8f667d2c959d33ee2632990b1b4e2acfe77b8e5fd69580f08f1960c1",
-                 "bytes_per_unit": (67141376 + 291584) / 262144, "unit": "256-byte key row"},
-    # attention over 16 layers x 8 KV heads x 2048 kept rows: 134 536 192 B read + 3 158 272 B write
+                 "sha256": "df251f8d23bde64a3e27365d8152cde3d8b761720b263eafd1a216ffed577fdb",
+                 "bytes_per_unit": (67141120 + 285440) / 262144, "unit": "256-byte key row"},
+    # attention over 16 layers x 8 KV heads x 2048 kept rows: 134 535 680 B read + 3 283 456 B write
     "attention": {"source": "sparse_kv_cache_retrieval_gb300/csrc/sparse_attn.cu",
                   "sha256": "d9112f28e3e3d682b5752e0855a30680955cbc2f3a4731c432777b503ebe64ae",
-                  "bytes_per_unit": (134536192 + 3158272) / 262144, "unit": "512-byte K+V row"},
+                  "bytes_per_unit": (134535680 + 3283456) / 262144, "unit": "512-byte K+V row"},
 }
 
 
