@@ -224,9 +224,22 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
       qf[ks][3] = h_hi < G ? *reinterpret_cast<const uint32_t*>(qg + (size_t)h_hi * kD + c + 8) : 0u;
     }
     float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
-    float o[16][4];
+    // P V layout. G <= 8 (kDM): O^T = V^T P^T with the 128 output dims on the
+    // M side (8 m-tiles from ldmatrix.trans of the V rows) and P's bf16 high
+    // and low parts packed on the N side (columns [0, HALF) high, [HALF,
+    // 2 HALF) low, HALF = max(4, G)): 8 (G <= 4) or 16 (G = 8) MMAs per 16
+    // keys. Larger groups keep heads on the M side (32 MMAs per 16 keys).
+    constexpr bool kDM = G <= 8;
+    constexpr int HALF = G < 4 ? 4 : G;
+    constexpr int PNT = kDM ? (2 * HALF) / 8 : 1;
+    float o[kDM ? 1 : 16][4];
+    float oT[kDM ? 8 : 1][PNT][4];
 #pragma unroll
-    for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    for (int n = 0; n < (kDM ? 1 : 16); ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < (kDM ? 8 : 1); ++mt)
+#pragma unroll
+      for (int nt = 0; nt < PNT; ++nt) oT[mt][nt][0] = oT[mt][nt][1] = oT[mt][nt][2] = oT[mt][nt][3] = 0.f;
 
     int it = 0;
     for (int c = c0; c < c1; ++c, ++it) {
@@ -297,12 +310,65 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
       m_lo = mn_lo;
       m_hi = mn_hi;
       if (__any_sync(0xffffffffu, al_lo != 1.f || al_hi != 1.f)) {
+        if constexpr (kDM) {
+          // this lane's O^T columns 2tig, 2tig+1 belong to heads (2tig + e) mod HALF,
+          // whose rescale factor sits in the lanes of row gid = head
+          const float a0 = __shfl_sync(0xffffffffu, al_lo, ((2 * tig) & (HALF - 1)) * 4);
+          const float a1 = __shfl_sync(0xffffffffu, al_lo, ((2 * tig + 1) & (HALF - 1)) * 4);
 #pragma unroll
-        for (int n = 0; n < 16; ++n) {
-          o[n][0] *= al_lo; o[n][1] *= al_lo;
-          o[n][2] *= al_hi; o[n][3] *= al_hi;
+          for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < PNT; ++nt) {
+              oT[mt][nt][0] *= a0; oT[mt][nt][1] *= a1;
+              oT[mt][nt][2] *= a0; oT[mt][nt][3] *= a1;
+            }
+        } else {
+#pragma unroll
+          for (int n = 0; n < 16; ++n) {
+            o[n][0] *= al_lo; o[n][1] *= al_lo;
+            o[n][2] *= al_hi; o[n][3] *= al_hi;
+          }
         }
       }
+      if constexpr (kDM) {
+        // ---- O^T += V^T P^T. B fragment of column n = gid: keys (2tig, 2tig+1)
+        // and (2tig+8, 2tig+9) of P's row for that column's head, which this
+        // lane holds (row gid) for a high column; a low column of G <= 4 takes
+        // the row of lane gid - 4 (lane ^ 16)
+#pragma unroll
+        for (int ks = 0; ks < S::KS; ++ks) {
+          const float* p0 = sacc[2 * ks];
+          const float* p1 = sacc[2 * ks + 1];
+          uint32_t bh[2][PNT];
+          if constexpr (PNT == 1) {
+            const float y00 = __shfl_xor_sync(0xffffffffu, p0[0], 16), y01 = __shfl_xor_sync(0xffffffffu, p0[1], 16);
+            const float y10 = __shfl_xor_sync(0xffffffffu, p1[0], 16), y11 = __shfl_xor_sync(0xffffffffu, p1[1], 16);
+            if (gid < 4) {
+              bh[0][0] = pack_bf16(bf16_round(p0[0]), bf16_round(p0[1]));
+              bh[1][0] = pack_bf16(bf16_round(p1[0]), bf16_round(p1[1]));
+            } else {
+              bh[0][0] = pack_bf16(y00 - bf16_round(y00), y01 - bf16_round(y01));
+              bh[1][0] = pack_bf16(y10 - bf16_round(y10), y11 - bf16_round(y11));
+            }
+          } else {
+            const float h00 = bf16_round(p0[0]), h01 = bf16_round(p0[1]);
+            const float h10 = bf16_round(p1[0]), h11 = bf16_round(p1[1]);
+            bh[0][0] = pack_bf16(h00, h01);
+            bh[1][0] = pack_bf16(h10, h11);
+            bh[0][1] = pack_bf16(p0[0] - h00, p0[1] - h01);
+            bh[1][1] = pack_bf16(p1[0] - h10, p1[1] - h11);
+          }
+          const int krow = row0 + ks * 16 + (lane & 7) + (((lane >> 4) & 1) << 3);
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            const int piece = mt * 2 + ((lane >> 3) & 1);
+            uint32_t af[4];
+            ldsm_x4_t(vbase + krow * kAttnPitch + ((piece ^ (krow & 7)) << 4), af[0], af[1], af[2], af[3]);
+#pragma unroll
+            for (int nt = 0; nt < PNT; ++nt) mma_bf16(oT[mt][nt], af, bh[0][nt], bh[1][nt]);
+          }
+        }
+      } else {
       // ---- O += P V, P split into bf16 high + low parts
 #pragma unroll
       for (int ks = 0; ks < S::KS; ++ks) {
@@ -329,6 +395,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
           mma_bf16(o[2 * dp + 1], al, b2, b3);
         }
       }
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
@@ -338,6 +405,21 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
       if (h_lo < G) { ml[(rs * G + h_lo) * 2] = m_lo; ml[(rs * G + h_lo) * 2 + 1] = l_lo; }
       if (h_hi < G) { ml[(rs * G + h_hi) * 2] = m_hi; ml[(rs * G + h_hi) * 2 + 1] = l_hi; }
     }
+    if constexpr (kDM) {
+      // O[h][dim] = O^T[dim][high column of h] + O^T[dim][low column of h]
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float v;
+          if constexpr (PNT == 1) v = oT[mt][0][j] + __shfl_xor_sync(0xffffffffu, oT[mt][0][j], 2);
+          else v = oT[mt][0][j] + oT[mt][1][j];
+          const int head = 2 * tig + (j & 1);
+          const int dim = mt * 16 + gid + ((j >> 1) << 3);
+          if (head < G) mo[((size_t)rs * G + head) * kD + dim] = v;
+        }
+      }
+    } else
 #pragma unroll
     for (int n = 0; n < 16; ++n) {
       const int d0 = n * 8 + tig * 2;

@@ -357,6 +357,20 @@ class DecodePipeline:
         self._q_dev_host = spc.spc_host_device_pointer(self.q_host)
         self._out_dev_host = spc.spc_host_device_pointer(self.out_host)
         self._sel_dev_host = spc.spc_host_device_pointer(self.sel_host)
+        # the GPU's first write to each page of a pinned buffer pays for the
+        # page's address translation over the link: touch the output buffers
+        # once here, so the steps write to translated pages
+        with torch.cuda.stream(self.sD):
+            z = torch.zeros(max(self._out_bytes, self._sel_bytes, self._q_bytes, self._x_bytes) // 4 + 1,
+                            dtype=torch.float32, device=dev)
+            for t in range(n_steps):
+                spc.spc_copy(self._out_dev_host + t * self._out_bytes, z, self._out_bytes, stream=self.sD)
+                spc.spc_copy(self._sel_dev_host + t * self._sel_bytes, z, self._sel_bytes, stream=self.sD)
+                spc.spc_copy(z, self._q_dev_host + t * self._q_bytes, self._q_bytes, stream=self.sD)
+            for t in range(n_steps + 1):
+                spc.spc_copy(z, self._x_dev_host + t * self._x_bytes, self._x_bytes, stream=self.sD)
+        self.sD.synchronize()
+        del z
         self.host_io = True
 
     # ------------------------------------------------------------------ pieces
