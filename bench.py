@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--layers", type=int, default=None,
                     help="LLM layers to run (default: the workload's); the JSON line states it")
     ap.add_argument("--gather-streams", type=int, default=2, choices=[1, 2])
+    ap.add_argument("--no-elastic", action="store_true",
+                    help="reload every step's whole selection (the baseline elastic loading is measured against)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-sample-steps", type=int, default=2)
@@ -396,7 +398,7 @@ def our_arm(args, rank, world, local):
     inp = make_inputs(cfg, steps=W + K + 1, n_layers=n_layers)
     log("allocating and filling the pinned host store")
     pipe = DecodePipeline(cfg, inp, n_layers=n_layers, layers_per_launch=args.layers_per_launch, timing=False,
-                          gather_streams=args.gather_streams)
+                          gather_streams=args.gather_streams, elastic=not args.no_elastic)
     log("pipeline ready")
     if args.profile:
         # the launch sequence a profiler sees: the prologue (one whole-selection
@@ -501,7 +503,7 @@ def our_arm(args, rank, world, local):
     host_layers = np.array([pipe.L - pipe.gpu_layers[b] for b in range(cfg.B)])
     gathered = int((nl.sum(axis=2) * host_layers[None, :]).sum() * 2 * 256)
     full_reload = int(n_eager * cfg.B * cfg.n_kv * cfg.budget * host_layers.mean() * 2 * 256)
-    overlap = 1.0 - nl.sum() / (n_eager * cfg.B * cfg.n_kv * min(cfg.budget, min(cfg.lens)))
+    overlap = (1.0 - nl.sum() / (n_eager * cfg.B * cfg.n_kv * min(cfg.budget, min(cfg.lens)))) if pipe.elastic else None
     lens_now = pipe.len.cpu().numpy()
     scan_bytes = int(sum(int(L) for L in lens_now) * cfg.n_kv * 256)   # fixed-length workloads
     n_gather_launches = kern.get("gather", {}).get("launches", 1)
@@ -615,6 +617,8 @@ def our_arm(args, rank, world, local):
     if n_layers != cfg.n_layers:
         config["layers"] = n_layers
         config["layers_note"] = f"{n_layers} of the workload's {cfg.n_layers} layers"
+    if args.no_elastic:
+        config["elastic"] = "off: every step reloads its whole selection"
     config.update({"layers_per_launch": args.layers_per_launch, "gather_streams": args.gather_streams,
                    "l2": (f"inputs larger than L2: each step reads the {scan_bytes / 2**20:.0f} MiB key cache "
                           f"and {attn_bytes_per_layer * n_layers / 2**20:.0f} MiB of K/V rows and writes the "
@@ -634,7 +638,7 @@ def our_arm(args, rank, world, local):
         "elastic": {"gathered_bytes_per_step": gathered // n_eager,
                     "full_reload_bytes_per_step": full_reload // n_eager,
                     "transfer_saved": round(1 - gathered / max(1, full_reload), 3),
-                    "adjacent_overlap": round(float(overlap), 3)},
+                    "adjacent_overlap": round(float(overlap), 3) if overlap is not None else None},
         "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
     }
     print(json.dumps(line))

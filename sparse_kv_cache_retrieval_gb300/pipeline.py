@@ -60,7 +60,7 @@ class DecodePipeline:
                  n_layers: Optional[int] = None, layers_per_launch: int = 16,
                  host_io: bool = False, timing: bool = False, fill_threads: Optional[int] = None,
                  gather_streams: int = 2, kv_bytes: Optional[int] = None,
-                 offload_policy: str = "progressive"):
+                 offload_policy: str = "progressive", elastic: bool = True):
         self.cfg = cfg
         self.inp = inputs
         self.dev = torch.device(device)
@@ -95,6 +95,7 @@ class DecodePipeline:
         self.load_slot = i32(2, B, n_kv, K)
         self.load_pos = i32(2, B, n_kv, K)
         self.n_load = i32(2, B, n_kv)
+        self.no_resident = i32(B, n_kv, K, fill=-1)
         # attention output, double-buffered by step parity (the copy of step t's
         # output to the host may still run while step t+1 writes); `out` is the
         # buffer of the step issued last
@@ -107,6 +108,10 @@ class DecodePipeline:
         # maybe_offload() moves further layers as the context grows
         if offload_policy not in ("progressive", "static"):
             raise ValueError("offload_policy is 'progressive' or 'static'")
+        # elastic=False is the comparison the pages measure elastic loading
+        # against: every step reloads its whole selection (the diff sees no
+        # resident slot)
+        self.elastic = elastic
         self.adaptive = kv_bytes is not None
         self.kv_bytes = kv_bytes
         self.offload_policy = offload_policy
@@ -382,7 +387,8 @@ class DecodePipeline:
                                     stages=stages)
 
     def _diff(self, pn, p, stream):
-        spc.spc_elastic_diff(self.selected[pn], self.slot_pos[p], self.slot_pos[pn], self.load_slot[pn],
+        prev = self.slot_pos[p] if self.elastic else self.no_resident
+        spc.spc_elastic_diff(self.selected[pn], prev, self.slot_pos[pn], self.load_slot[pn],
                              self.load_pos[pn], self.n_load[pn], self.B, self.n_kv, self.K, self.cap,
                              stream=stream)
 

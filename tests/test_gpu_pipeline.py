@@ -193,6 +193,29 @@ def test_chain_adaptive_offload_crosses_thresholds(policy):
     assert seen[-1] != seen[0]                                  # something moved during the run
 
 
+def test_full_reload_mode_loads_every_selected_row_and_matches_elastic():
+    # the baseline elastic loading is measured against: each step reloads its
+    # whole selection; selections and attention outputs are those of the
+    # elastic path, only the traffic differs
+    cfg = scaled(CONFIGS["cfg1"], steps=4)
+    inp = make_inputs(cfg, steps=4)
+    a = DecodePipeline(cfg, inp, layers_per_launch=1)
+    b = DecodePipeline(cfg, inp, layers_per_launch=1, elastic=False)
+    a.prologue()
+    b.prologue()
+    for t in range(4):
+        for p_ in (a, b):
+            p_.step(t)
+            p_.join()
+        torch.cuda.synchronize()
+        pn = (t + 1) % 2
+        assert torch.equal(a.selected[pn], b.selected[pn])
+        n_sel = (b.selected[pn] >= 0).sum(dim=2)
+        assert torch.equal(b.n_load[pn], n_sel.to(torch.int32))
+        assert int(a.n_load[pn].sum()) < int(b.n_load[pn].sum())
+        assert (a.out - b.out).abs().max().item() <= 2e-5
+
+
 def _state(pipe):
     return [pipe.out.cpu(), pipe.selected.cpu(), pipe.slot_pos.cpu(), pipe.len.cpu()] + \
         [s.cpu() for s in pipe.slots if s is not None]
