@@ -49,7 +49,7 @@ def parse():
     ap.add_argument("--layers-per-launch", type=int, default=16)
     ap.add_argument("--layers", type=int, default=None,
                     help="LLM layers to run (default: the workload's); the JSON line states it")
-    ap.add_argument("--gather-streams", type=int, default=2, choices=[1, 2])
+    ap.add_argument("--gather-streams", type=int, default=1, choices=[1, 2])
     ap.add_argument("--no-elastic", action="store_true",
                     help="reload every step's whole selection (the baseline elastic loading is measured against)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -305,15 +305,17 @@ def hbm_read_peak(spc, torch):
 
 
 # ---------------------------------------------------------------- oracle (CPU) leg
-def oracle_sample(cfg_key: str, steps: int, layers: int) -> dict:
-    """Time the oracle on a bounded sample of the workload, single-threaded.
+def oracle_sample(cfg_key: str, steps: int, layers: int, threads: int = 1) -> dict:
+    """Time the oracle on a bounded sample of the workload.
 
-    Runs in a child process with one BLAS/OpenMP thread. The sample is the
-    full retrieval head (all positions, all heads) plus diff, gather and
-    attention for `layers` of the workload's layers; the per-layer part is
-    scaled to all layers to give us/step.
+    Runs in a child process with `threads` BLAS/OpenMP threads (the oracle's
+    matrix products use them). The sample is the full retrieval head (all
+    positions, all heads) plus diff, gather and attention for `layers` of the
+    workload's layers; the per-layer part is scaled to all layers to give
+    us/step.
     """
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+    n = str(max(1, threads))
+    env = dict(os.environ, OMP_NUM_THREADS=n, OPENBLAS_NUM_THREADS=n, MKL_NUM_THREADS=n,
                CUDA_VISIBLE_DEVICES="")
     code = f"""
 import json, math, sys, time
@@ -352,7 +354,8 @@ print(json.dumps({{"us_per_step": per_step_us, "head_s": t_head, "layers_s": t_l
     res = json.loads(r.stdout.strip().splitlines()[-1])
     res["sample"] = (f"{steps} decode steps of the full workload's retrieval head (all positions and "
                      f"heads) + diff/gather/attention on {layers} of the layers, per-layer time scaled "
-                     f"to all layers; float64 numpy, 1 thread")
+                     f"to all layers; float64 numpy, {n} BLAS thread(s)")
+    res["threads"] = int(n)
     return res
 
 
@@ -363,14 +366,15 @@ def reference_arm(args, rank, world):
     cfg = CONFIGS[args.config]
     runs = max(1, args.steps // 32) if args.steps > 0 else 1
     t0 = time.time()
-    res = oracle_sample(args.config, args.oracle_sample_steps, args.oracle_sample_layers)
+    res = oracle_sample(args.config, args.oracle_sample_steps, args.oracle_sample_layers,
+                        threads=os.cpu_count() or 1)
     value = res["us_per_step"]
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.oracle_sample_steps, "warmup": 0,
             "ms_per_step": round(value / 1e3, 3), "higher_is_better": False, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": describe(cfg),
-            "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": res["threads"], "kind": "oracle",
                              "sample": res["sample"]},
             "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "wall_s": round(time.time() - t0, 1)}
@@ -605,9 +609,12 @@ def our_arm(args, rank, world, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         log("oracle CPU sample")
         try:
-            res = oracle_sample(args.config, args.oracle_sample_steps, args.oracle_sample_layers)
-            cpu = {"value": round(res["us_per_step"], 1), "unit": UNIT, "cores": 1, "kind": "oracle",
-                   "sample": res["sample"]}
+            res = oracle_sample(args.config, args.oracle_sample_steps, args.oracle_sample_layers,
+                                threads=os.cpu_count() or 1)
+            one = oracle_sample(args.config, args.oracle_sample_steps, args.oracle_sample_layers, threads=1)
+            cpu = {"value": round(res["us_per_step"], 1), "unit": UNIT, "cores": res["threads"], "kind": "oracle",
+                   "sample": res["sample"],
+                   "single_thread": {"value": round(one["us_per_step"], 1), "cores": 1}}
         except Exception as ex:  # reported, never fatal for the GPU number
             cpu = {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": f"failed: {ex}"[:300]}
 

@@ -28,7 +28,10 @@
 
 namespace spc {
 
-constexpr int kGatherThreads = 512;
+#ifndef SPC_GATHER_THREADS
+#define SPC_GATHER_THREADS 512
+#endif
+constexpr int kGatherThreads = SPC_GATHER_THREADS;
 #ifndef SPC_GATHER_UNROLL
 #define SPC_GATHER_UNROLL 8    // layers of one run in flight per warp
 #endif

@@ -59,7 +59,7 @@ class DecodePipeline:
     def __init__(self, cfg: Workload, inputs: Inputs, *, device: str = "cuda",
                  n_layers: Optional[int] = None, layers_per_launch: int = 16,
                  host_io: bool = False, timing: bool = False, fill_threads: Optional[int] = None,
-                 gather_streams: int = 2, kv_bytes: Optional[int] = None,
+                 gather_streams: int = 1, kv_bytes: Optional[int] = None,
                  offload_policy: str = "progressive", elastic: bool = True):
         self.cfg = cfg
         self.inp = inputs
