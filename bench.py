@@ -151,18 +151,19 @@ class ClockSampler:
 NCU_TRAFFIC = {
     # gather of decode step 0, layers 16-31: 1550 loads x 16 layers x K/V = 49 600
     # rows; 396 800 system-memory sectors (12 697 600 B) read over the host link
-    # + 27 136 B DRAM read + 512 B DRAM write
+    # + 26 624 B DRAM read + 1 280 B DRAM write
     "gather": {"source": "sparse_kv_cache_retrieval_gb300/csrc/gather_kv.cu",
-               "sha256": "698bd9e4683f695f1ac27d5225eced8534439a61e22a43b1cf2f692bf1277bfb",
-               "bytes_per_unit": (12697600 + 27136 + 512) / 49600, "unit": "moved 256-byte row"},
-    # key scan over 32 768 positions x 8 KV heads: 67 141 120 B DRAM read + 285 440 B write
+               "sha256": "d81e9b9166c899f4c820d594fb21af5f6bb7b23790e98c209bf5423dd8677dad",
+               "bytes_per_unit": (12697600 + 26624 + 1280) / 49600, "unit": "moved 256-byte row"},
+    # key scan over 32 768 positions x 8 KV heads: 67 141 376 B DRAM read + 335 616 B write
     "key_scan": {"source": "sparse_kv_cache_retrieval_gb300/csrc/score_select.cu",
                  "sha256": "df251f8d23bde64a3e27365d8152cde3d8b761720b263eafd1a216ffed577fdb",
-                 "bytes_per_unit": (67141120 + 285440) / 262144, "unit": "256-byte key row"},
-    # attention over 16 layers x 8 KV heads x 2048 kept rows: 134 535 680 B read + 3 283 456 B write
+                 "bytes_per_unit": (67141376 + 335616) / 262144, "unit": "256-byte key row"},
+    # attention over 16 layers x 8 KV heads x 2048 kept rows, mean of two launches:
+    # 134 537 984 B read + 3 164 800 B write
     "attention": {"source": "sparse_kv_cache_retrieval_gb300/csrc/sparse_attn.cu",
-                  "sha256": "d9112f28e3e3d682b5752e0855a30680955cbc2f3a4731c432777b503ebe64ae",
-                  "bytes_per_unit": (134535680 + 3283456) / 262144, "unit": "512-byte K+V row"},
+                  "sha256": "01e645590c4b04bc2ebf3b3ffe7de26745c170c8cca195e315e23f35760f7f86",
+                  "bytes_per_unit": (134537984 + 3164800) / 262144, "unit": "512-byte K+V row"},
 }
 
 
