@@ -323,6 +323,99 @@ int spc_sparse_decode_attn_noalloc(const void* q, const spc_kv_view* views,
                                    float* out, void* stream);
 
 /* ------------------------------------------------------------------------
+ * MLA variant. [Blog] §5: for DeepSeek's MLA the retrieval picks entries of
+ * the low-dimensional latent cache and only the selected entries are
+ * up-projected; [Summary] §4.3: retrieval stays head-level and only the
+ * selected latent entries are expanded for attention.
+ *
+ * Shapes (DeepSeek-V2 style MLA): each position caches ONE latent row of
+ * SPC_MLA_LATENT + SPC_MLA_ROPE = 576 bf16 -- a 512-value latent c shared by
+ * every head, then a 64-value decoupled rope key. Head h expands c into the
+ * key [W_uk[h] c ; c_rope] (128 + 64 values) and the value W_uv[h] c (128);
+ * queries carry 128 "nope" values then 64 rope values per head. No RoPE
+ * rotation is applied (as in the GQA path). SPC_MLA_HEADS = 16 query heads
+ * (DeepSeek-V2-Lite, or one tensor-parallel shard of 8 of DeepSeek-V3's 128).
+ * The latent row is shared by all heads, so the 16 heads form one group (as
+ * for MQA): one selection per request, n_kv = 1 in the diff and slot maps.
+ * ---------------------------------------------------------------------- */
+#define SPC_MLA_LATENT 512
+#define SPC_MLA_ROPE 64
+#define SPC_MLA_NOPE 128
+#define SPC_MLA_V 128
+#define SPC_MLA_HEADS 16
+
+/* Retrieval head over the latent cache. For every request b:
+ *   q[b,h,:]  = x_b . Wq[:, h*192:(h+1)*192]                     (fp32)
+ *   if append and len[b] < cap:
+ *     C_dlm[b, len[b], :] = bf16_rne(x_b . Wdkv);  len[b] += 1
+ *   key_h(p)  = [Wuk[h] C_dlm[b,p,:512] ; C_dlm[b,p,512:]]
+ *   P_h[p]    = softmax_p(q[b,h] . key_h(p) / sqrt(192)),  p < len[b]
+ *   s[p]      = max_h P_h[p]
+ *   selected[b,:] = as spc_score_select with one group (forced sinks and
+ *               recent window, Top-K, ties to the lower position, -1 padded).
+ * Computed with the query absorbed into the latent space,
+ * [Wuk[h]^T q_nope ; q_rope] . C_dlm[b,p], the same quantity.
+ *
+ * x          bf16 [B][H].
+ * Wq         bf16 [H][16*192].
+ * Wuk        bf16 [16][128][512]: row j of head h maps the latent to key value j.
+ * Wdkv       bf16 [H][576] latent down-projection (may be NULL if !append).
+ * C_dlm      bf16 [B][cap][576] latent cache of the retrieval head, 16-byte
+ *            aligned; row len[b] is written when appending.
+ * len, scores_out ([B][cap]), selected ([B][budget]), workspace, status word
+ *            and stages: as spc_score_select_stages (the workspace size from
+ *            spc_mla_score_select_workspace_size). The projection stage also
+ *            absorbs the queries.
+ * Limits: H % 8 == 0, 8 <= H <= 32768; 1 <= B <= 64; 1 <= budget <=
+ *         min(cap, 4096); cap <= 262144; n_sink + n_recent <= budget.
+ * ---------------------------------------------------------------------- */
+size_t spc_mla_score_select_workspace_size(int B, int H, int cap, int budget);
+
+int spc_mla_score_select(const void* x, const void* Wq, const void* Wuk, const void* Wdkv, void* C_dlm,
+                         int32_t* len, int append, int B, int H, int cap, int budget, int n_sink,
+                         int n_recent, float* scores_out, int32_t* selected, void* workspace,
+                         size_t workspace_bytes, void* stream, int stages);
+
+/* Gather of missing latent rows from pinned host memory (spc_gather_kv with
+ * one KV head and 576-value rows, no K/V pair). For host layers l of request
+ * b and load i < n_load[b], p = load_pos[b,i], s = load_slot[b,i]:
+ *   slots[l - view.layer0, s, :] = host[p, l - view.store_layer0, :]
+ * host   POSITION-MAJOR bf16 [cap][view.store_layers][576] (one position's
+ *        latent rows of every stored layer are contiguous), device-visible
+ *        address of mapped pinned memory, 16-byte aligned.
+ * slots  bf16 [view.n_layers][budget][576] device memory, 16-byte aligned.
+ * load_slot, load_pos int32 [B][budget], n_load int32 [B] (spc_elastic_diff
+ * with n_kv = 1). Order after the attention that reads the old slot rows.
+ * Limits: budget <= 4096. */
+int spc_mla_gather(const spc_gather_view* views, int layer_lo, int layer_hi, const int32_t* load_slot,
+                   const int32_t* load_pos, const int32_t* n_load, int B, int cap, int budget,
+                   void* stream);
+
+/* Sparse MLA decode attention over the selected latent rows, for n_layers
+ * layers x B requests (unit u = layer * B + b):
+ *   out[u,h,:] = sum_r softmax_r(q[u,h] . key_{l,h}(C_r) * scale) W_uv[l,h] C_r[:512]
+ * over the rows r the view keeps (as spc_sparse_decode_attn: positions of
+ * `selected` into a full cache, or slots with slot_pos >= 0), with
+ * key_{l,h}(c) = [W_uk[l,h] c[:512] ; c[512:]]. Computed with the query
+ * absorbed and W_uv applied once to the softmax-weighted latent sum (the same
+ * quantity as up-projecting every selected row).
+ * q          bf16 [n_layers][B][16][192] LLM queries (nope, then rope values).
+ * Wuk, Wuv   bf16 [n_layers][16][128][512].
+ * views      device array [n_layers][B] of spc_kv_view: k = latent rows bf16
+ *            [rows][576] (16-byte aligned), v unused (NULL), rows, use_slots.
+ * selected, slot_pos int32 [B][budget] (shared by all layers).
+ * out        fp32 [n_layers][B][16][128].
+ * workspace  device scratch of spc_mla_decode_attn_workspace_size() bytes,
+ *            256-byte aligned; its first int32 is a status word (0, or
+ *            SPC_ERR_TIMEOUT set by a kernel), ZERO-FILLED BEFORE FIRST USE.
+ * Limits: budget <= 4096; n_layers * B <= 65535. */
+size_t spc_mla_decode_attn_workspace_size(int n_layers, int B, int budget);
+
+int spc_mla_decode_attn(const void* q, const void* Wuk, const void* Wuv, const spc_kv_view* views,
+                        const int32_t* selected, const int32_t* slot_pos, int n_layers, int B, int budget,
+                        float scale, float* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * Helpers (no counterpart on the pages).
  * ---------------------------------------------------------------------- */
 

@@ -52,6 +52,13 @@ SIGNATURES = {
     "spc_fill_slots": (_I, [_P, _I, _I, _P, _I, _I, _I, _I, _I, _P]),
     "spc_store_layer": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "spc_offload_thresholds": (_I, [_I, _I, _I, _I, _I, ctypes.c_int64, ctypes.POINTER(ctypes.c_int64)]),
+    "spc_mla_score_select_workspace_size": (ctypes.c_size_t, [_I] * 4),
+    "spc_mla_score_select": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P,
+                                  ctypes.c_size_t, _P, _I]),
+    "spc_mla_gather": (_I, [_P, _I, _I, _P, _P, _P, _I, _I, _I, _P]),
+    "spc_mla_decode_attn_workspace_size": (ctypes.c_size_t, [_I] * 3),
+    "spc_mla_decode_attn": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, ctypes.c_float, _P, _P, ctypes.c_size_t,
+                                 _P]),
 }
 
 
@@ -212,6 +219,43 @@ def spc_offload_thresholds(n_layers, n_kv, d, B, budget, kv_bytes) -> list:
     _check("spc_offload_thresholds", lib().spc_offload_thresholds(n_layers, n_kv, d, B, budget,
                                                                   int(kv_bytes), out))
     return [int(v) for v in out]
+
+
+# ------------------------------------------------------------------ MLA variant
+SPC_MLA_LATENT, SPC_MLA_ROPE, SPC_MLA_NOPE, SPC_MLA_V, SPC_MLA_HEADS = 512, 64, 128, 128, 16
+
+
+def spc_mla_score_select_workspace_size(B, H, cap, budget) -> int:
+    return int(lib().spc_mla_score_select_workspace_size(B, H, cap, budget))
+
+
+def spc_mla_score_select(x, Wq, Wuk, Wdkv, C_dlm, len, append, B, H, cap, budget, n_sink, n_recent,
+                         scores_out, selected, workspace, workspace_bytes=None, stream=None, stages=7) -> None:
+    if workspace_bytes is None:
+        workspace_bytes = _nbytes(workspace)
+    _check("spc_mla_score_select", lib().spc_mla_score_select(
+        _ptr(x), _ptr(Wq), _ptr(Wuk), _ptr(Wdkv), _ptr(C_dlm), _ptr(len), int(append), B, H, cap, budget,
+        n_sink, n_recent, _ptr(scores_out), _ptr(selected), _ptr(workspace), workspace_bytes, _stream(stream),
+        int(stages)))
+
+
+def spc_mla_gather(views, layer_lo, layer_hi, load_slot, load_pos, n_load, B, cap, budget, stream=None) -> None:
+    _check("spc_mla_gather", lib().spc_mla_gather(
+        _ptr(views), layer_lo, layer_hi, _ptr(load_slot), _ptr(load_pos), _ptr(n_load), B, cap, budget,
+        _stream(stream)))
+
+
+def spc_mla_decode_attn_workspace_size(n_layers, B, budget) -> int:
+    return int(lib().spc_mla_decode_attn_workspace_size(n_layers, B, budget))
+
+
+def spc_mla_decode_attn(q, Wuk, Wuv, views, selected, slot_pos, n_layers, B, budget, scale, out, workspace,
+                        workspace_bytes=None, stream=None) -> None:
+    if workspace_bytes is None:
+        workspace_bytes = _nbytes(workspace)
+    _check("spc_mla_decode_attn", lib().spc_mla_decode_attn(
+        _ptr(q), _ptr(Wuk), _ptr(Wuv), _ptr(views), _ptr(selected), _ptr(slot_pos), n_layers, B, budget,
+        float(scale), _ptr(out), _ptr(workspace), workspace_bytes, _stream(stream)))
 
 
 def spc_device_sm_count() -> int:

@@ -22,6 +22,8 @@ import math
 from typing import List, Optional
 
 GiB = 1 << 30
+MLA_LATENT_ROW = 512 + 64      # latent + decoupled rope key, per position and layer
+MLA_QK = 128 + 64              # per-head query: nope + rope values
 
 
 @dataclasses.dataclass(frozen=True)
@@ -46,6 +48,7 @@ class Workload:
     n_recent: int = 64
     gamma: float = 8.0     # planted hot keys get + gamma*sqrt(G) along the group's query direction
     kv_bytes: Optional[int] = None   # GPU memory for the LLM KV: set = adaptive layer offload
+    mla: bool = False      # MLA attention: one 576-value latent row per position (n_kv = 1, d = 128)
     note: str = ""
 
     @property
@@ -55,9 +58,15 @@ class Workload:
     def host_layers(self, b: int) -> int:
         return self.n_layers - self.gpu_layers[b]
 
+    @property
+    def row_elems(self) -> int:
+        """bf16 values one position holds in one layer: K and V of every KV
+        head, or one MLA latent row (512 latent + 64 rope values)."""
+        return MLA_LATENT_ROW if self.mla else self.n_kv * 2 * self.d
+
     def kv_layer_bytes(self, length: int) -> int:
-        """Bytes of one layer's K and V for one request at the given length (bf16)."""
-        return length * self.n_kv * 2 * self.d * 2
+        """Bytes of one layer's KV for one request at the given length (bf16)."""
+        return length * self.row_elems * 2
 
     def host_store_bytes(self) -> int:
         return sum(self.host_layers(b) * self.kv_layer_bytes(self.cap) for b in range(self.B))
@@ -132,6 +141,15 @@ def _build() -> dict:
     cfgs["cfg5mqa"] = dataclasses.replace(
         cfgs["cfg5"], name="cfg5mqa_b8_ctx65536_mqa64x1_budget4096_80layers", n_kv=1,
         note="MQA variant of cfg5: all 64 query heads form one group")
+    # MLA (DeepSeek-V2-Lite shapes: hidden 2048, 16 heads, latent 512 + rope
+    # 64, 27 layers): the cfg2 setting (32K context, budget 2048, every layer's
+    # latent cache in pinned host memory) on a latent cache
+    cfgs["mla"] = Workload(
+        name="mla_b1_ctx32768_mla16_latent512_budget2048_27layers_host",
+        B=1, lens=(32768,), H=2048, n_q=16, n_kv=1, d=128, budget=2048, n_layers=27,
+        gpu_layers=(0,), steps=64, rho=(0.9,), hot=(328,), seed=6, cap=32768, mla=True,
+        note="MLA variant: head-level selection over the latent cache, only selected latent rows "
+             "loaded and up-projected; latent cache (27 layers, 0.95 GiB) in pinned host")
     # adaptive memory management on a growing context: 4 requests from 4096
     # positions, one token per step, GPU KV memory for 4127 positions of all
     # 32 layers per request, so the first threshold falls 32 steps in and a
@@ -180,7 +198,8 @@ def describe(cfg: Workload) -> dict:
         "host_layers": [cfg.host_layers(b) for b in range(cfg.B)] if cfg.B <= 4 else
         sum(cfg.host_layers(b) for b in range(cfg.B)),
         "sinks": cfg.n_sink, "recent": cfg.n_recent, "seed": cfg.seed,
+        **({"attention": "mla", "latent_row": MLA_LATENT_ROW} if cfg.mla else {}),
     }
 
 
-__all__ = ["Workload", "CONFIGS", "scaled", "describe", "GiB"]
+__all__ = ["Workload", "CONFIGS", "scaled", "describe", "GiB", "MLA_LATENT_ROW", "MLA_QK"]

@@ -255,6 +255,67 @@ int spc_sparse_decode_attn_noalloc(const void* q, const spc_kv_view* views, cons
                              stream);
 }
 
+size_t spc_mla_score_select_workspace_size(int B, int H, int cap, int budget) {
+  (void)budget;
+  if (B < 1 || B > SPC_MAX_BATCH || H < 1 || cap < 1) return 0;
+  return mla_score_select_workspace(B, cap);
+}
+
+int spc_mla_score_select(const void* x, const void* Wq, const void* Wuk, const void* Wdkv, void* C_dlm,
+                         int32_t* len, int append, int B, int H, int cap, int budget, int n_sink,
+                         int n_recent, float* scores_out, int32_t* selected, void* workspace,
+                         size_t workspace_bytes, void* stream, int stages) {
+  if (!x || !Wq || !Wuk || !C_dlm || !len || !selected) return SPC_ERR_INVALID_ARG;
+  if (append != 0 && append != 1) return SPC_ERR_INVALID_ARG;
+  if (stages < 1 || stages > 7) return SPC_ERR_INVALID_ARG;
+  if (append && !Wdkv) return SPC_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(Wq) || !aligned16(Wuk) || (Wdkv && !aligned16(Wdkv)) || !aligned16(C_dlm))
+    return SPC_ERR_INVALID_ARG;
+  if (B < 1 || B > SPC_MAX_BATCH || H < 8 || H > SPC_MAX_HIDDEN || H % 8) return SPC_ERR_SHAPE;
+  if (cap < 1 || cap > SPC_MAX_CAP) return SPC_ERR_SHAPE;
+  if (budget < 1 || budget > SPC_MAX_BUDGET || budget > cap) return SPC_ERR_SHAPE;
+  if (n_sink < 0 || n_recent < 0 || n_sink + n_recent > budget) return SPC_ERR_SHAPE;
+  const size_t need = mla_score_select_workspace(B, cap);
+  if (!workspace || workspace_bytes < need) return SPC_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SPC_ERR_INVALID_ARG;
+  MlaScoreSelectCall c{};
+  c.x = x; c.Wq = Wq; c.Wuk = Wuk; c.Wdkv = Wdkv; c.C_dlm = C_dlm; c.len = len; c.append = append;
+  c.B = B; c.H = H; c.cap = cap; c.budget = budget; c.n_sink = n_sink; c.n_recent = n_recent;
+  c.scores_out = scores_out; c.selected = selected; c.workspace = workspace; c.stream = stream;
+  c.stages = stages;
+  return mla_score_select_launch(c);
+}
+
+int spc_mla_gather(const spc_gather_view* views, int layer_lo, int layer_hi, const int32_t* load_slot,
+                   const int32_t* load_pos, const int32_t* n_load, int B, int cap, int budget,
+                   void* stream) {
+  if (!views || !load_slot || !load_pos || !n_load) return SPC_ERR_INVALID_ARG;
+  if (B < 1 || B > SPC_MAX_BATCH) return SPC_ERR_SHAPE;
+  if (layer_lo < 0 || layer_hi < layer_lo) return SPC_ERR_SHAPE;
+  if (budget < 1 || budget > SPC_MAX_BUDGET || cap < 1 || cap > SPC_MAX_CAP) return SPC_ERR_SHAPE;
+  return mla_gather_launch(views, layer_lo, layer_hi, load_slot, load_pos, n_load, B, budget, stream);
+}
+
+size_t spc_mla_decode_attn_workspace_size(int n_layers, int B, int budget) {
+  if (n_layers < 1 || B < 1 || budget < 1 || budget > SPC_MAX_BUDGET) return 0;
+  return mla_attn_workspace(n_layers, B, budget);
+}
+
+int spc_mla_decode_attn(const void* q, const void* Wuk, const void* Wuv, const spc_kv_view* views,
+                        const int32_t* selected, const int32_t* slot_pos, int n_layers, int B, int budget,
+                        float scale, float* out, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !Wuk || !Wuv || !views || !selected || !slot_pos || !out) return SPC_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(Wuk) || !aligned16(Wuv) || !aligned16(out)) return SPC_ERR_INVALID_ARG;
+  if (n_layers < 1 || B < 1 || B > SPC_MAX_BATCH || (long long)n_layers * B > 65535) return SPC_ERR_SHAPE;
+  if (budget < 1 || budget > SPC_MAX_BUDGET) return SPC_ERR_SHAPE;
+  if (!(scale > 0.f)) return SPC_ERR_INVALID_ARG;
+  const size_t need = mla_attn_workspace(n_layers, B, budget);
+  if (!workspace || workspace_bytes < need) return SPC_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SPC_ERR_INVALID_ARG;
+  return mla_attn_launch(q, Wuk, Wuv, views, selected, slot_pos, n_layers, B, budget, scale, out, workspace,
+                         stream);
+}
+
 int spc_host_device_pointer(void* host_ptr, void** device_ptr) {
   if (!host_ptr || !device_ptr) return SPC_ERR_INVALID_ARG;
   void* p = nullptr;

@@ -55,6 +55,7 @@ struct ProjArgs {
   float* q_out;
   int* status;
   int B, H, Nq, Nk, Ntot, n_kv, cap, S, Hc;
+  int latent;   // 1: the appended row is one MLA latent row [B][cap][Nk] (Nk = 576)
 };
 
 #ifndef SPC_PROJ_TC_MIN_BATCH
@@ -93,6 +94,10 @@ __global__ void __launch_bounds__(kProjThreads) proj_kernel(ProjArgs a) {
   const uint16_t* W = is_k ? a.Wk : a.Wq;
   const int ld = is_k ? a.Nk : a.Nq;
   const int wcol0 = is_k ? col0 - a.Nq : col0;
+  // a tile may reach past the last weight column (the 576-column MLA latent
+  // row: the fifth tile has 64 columns); lanes past it read the tile's first
+  // columns, and their sums are not stored
+  const int ncol = min(kProjTile, ld - wcol0);
   const int r_begin = split * a.Hc;
   const int nr = max(0, min(a.H, r_begin + a.Hc) - r_begin);
 
@@ -113,7 +118,7 @@ __global__ void __launch_bounds__(kProjThreads) proj_kernel(ProjArgs a) {
 
   // half-warp hw takes rows hw, hw + 16, ...; LD weight loads in flight
   constexpr int LD = BB <= 2 ? 16 : 8;
-  const uint16_t* wp = W + (size_t)r_begin * ld + wcol0 + l16 * 8;
+  const uint16_t* wp = W + (size_t)r_begin * ld + wcol0 + (l16 * 8 < ncol ? l16 * 8 : 0);
   int r = warp * 2 + (lane >> 4);
   for (; r + 16 * (LD - 1) < nr; r += 16 * LD) {
     uint4 w[LD];
@@ -149,7 +154,7 @@ __global__ void __launch_bounds__(kProjThreads) proj_kernel(ProjArgs a) {
   if (split == 0) {
     for (int i = threadIdx.x; i < BB * kProjTile; i += kProjThreads) {
       const int bb = i / kProjTile, c = i - bb * kProjTile, b = b0 + bb;
-      if (b >= a.B) continue;
+      if (b >= a.B || c >= ncol) continue;
       float v[kProjMaxSplit];
 #pragma unroll
       for (int q = 0; q < kProjMaxSplit; ++q) v[q] = q < a.S ? *cluster.map_shared_rank(red + i, q) : 0.f;
@@ -164,7 +169,9 @@ __global__ void __launch_bounds__(kProjThreads) proj_kernel(ProjArgs a) {
         const int L = a.len[b];
         if (L >= 0 && L < a.cap) {
           const __nv_bfloat16 h = __float2bfloat16_rn(sum);
-          a.K_dlm[(((size_t)b * a.n_kv + g) * a.cap + L) * kD + c] = __bfloat16_as_ushort(h);
+          const size_t at = a.latent ? ((size_t)b * a.cap + L) * a.Nk + wcol0 + c
+                                     : (((size_t)b * a.n_kv + g) * a.cap + L) * kD + c;
+          a.K_dlm[at] = __bfloat16_as_ushort(h);
         } else if (c == 0) {
           set_status(a.status, SPC_ERR_OVERFLOW);
         }
@@ -1433,6 +1440,321 @@ int score_select_launch(const ScoreSelectCall& c) {
       case 32: rc = launch_select<32>(sa, c.B * c.n_kv, st); break;
       default: rc = launch_select<64>(sa, c.B * c.n_kv, st); break;
     }
+    if (rc != SPC_OK) return rc;
+  }
+  return SPC_OK;
+}
+
+
+// ============================================================== MLA retrieval head
+// "ASPLOS'26 | SpeContext ..." (marsggbo blog) §5 and "SpeContext: ..."
+// (paperlayer.ai summary) §4.3: with MLA the head scores the latent cache,
+// head-level; the latent row is shared by all query heads, so (as for MQA)
+// the 16 heads form one group and each request gets one selection.
+//
+// Latent scan: logits l[b, p, h] = qa[b, h] . C[b, p] * log2(e) / sqrt(192)
+// for the absorbed queries qa (576 values: W_uk[h]^T q_nope ; q_rope) over
+// the 576-value latent rows. One CTA per SM: a producer warp streams 32-row
+// tiles (36 KiB) into a 4-stage ring with 16-byte cp.async (pieces XOR-
+// swizzled by row); two groups of four consumer warps take alternate tiles.
+// Within a group the four warps split the 576 dims (9 k-steps of mma.sync
+// m16n8k16 each, the 16 heads on the M side, the query in bf16 high and low
+// parts so the logits keep fp32 accuracy), sum their partial tiles through
+// shared memory, and each finishes 8 of the 32 rows: logits out, one
+// logsumexp partial per head per 8 rows (16 per 128 positions).
+constexpr int kMsLat = SPC_MLA_LATENT + SPC_MLA_ROPE;   // 576
+constexpr int kMsLatBytes = kMsLat * 2;
+constexpr int kMsPieces = kMsLatBytes / 16;             // 72
+constexpr int kMsH = SPC_MLA_HEADS;                     // 16
+constexpr int kMsQk = SPC_MLA_NOPE + SPC_MLA_ROPE;      // 192
+constexpr int kMsRows = 32;
+constexpr int kMsStages = 4;
+constexpr int kMsGroups = 2;
+constexpr int kMsKw = 4;
+constexpr int kMsThreads = (kMsGroups * kMsKw + 1) * 32;
+constexpr int kMsKs = kMsLat / 16 / kMsKw;              // 9
+constexpr uint32_t kMsTile = kMsRows * kMsLatBytes;     // 36 KiB
+constexpr int kMsPpt = (kScanRows / kMsRows) * kMsKw;   // 16 partials per 128 positions
+constexpr size_t kMsRed = (size_t)kMsGroups * kMsKw * 4 * 32 * 16;
+constexpr size_t kMsSmem = kMsStages * (size_t)kMsTile + kMsRed + 2 * kMsStages * sizeof(uint64_t);
+
+struct MlaScanArgs {
+  const uint16_t* C;
+  const float* qa;
+  const int32_t* len;
+  float* logits;
+  float2* part;
+  int* status;
+  int cap, lstride, n_tiles, total_tiles, append, n_parts, tpc;
+  float qscale;
+};
+
+__device__ __forceinline__ void ms_bar(int grp) {
+  asm volatile("bar.sync %0, %1;" :: "r"(1 + grp), "n"(kMsKw * 32) : "memory");
+}
+
+// one CTA per SM: 224 registers for each of the 288 threads
+__global__ void __maxnreg__(224) mla_scan_kernel(MlaScanArgs a) {
+  extern __shared__ __align__(128) uint8_t mss[];
+  float4* red = reinterpret_cast<float4*>(mss + kMsStages * (size_t)kMsTile);
+  uint64_t* full = reinterpret_cast<uint64_t*>(mss + kMsStages * (size_t)kMsTile + kMsRed);
+  uint64_t* empty = full + kMsStages;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kMsStages; ++s) {
+      mbar_init(&full[s], 32);
+      mbar_init(&empty[s], kMsKw);   // the group that owns the stage
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int t_begin = blockIdx.x * a.tpc, t_end = min(a.total_tiles, t_begin + a.tpc);
+
+  if (warp == kMsGroups * kMsKw) {
+    // ---------------- producer
+    int it = 0;
+    for (int t = t_begin; t < t_end; ++t) {
+      const int b = t / a.n_tiles, tile = t - b * a.n_tiles;
+      const int L = effective_len(a.len, b, a.append, a.cap);
+      const int row0 = tile * kMsRows;
+      if (row0 >= L) continue;
+      const int nrows = min(kMsRows, L - row0);
+      const int s = it % kMsStages;
+      const uint32_t ph = (it / kMsStages) & 1;
+      if (!mbar_wait_bounded(&empty[s], ph ^ 1, kWaitLimit)) {
+        if (lane == 0) set_status(a.status, SPC_ERR_TIMEOUT);
+        break;
+      }
+      uint8_t* dst = mss + (size_t)s * kMsTile;
+      const uint16_t* src = a.C + ((size_t)b * a.cap + row0) * kMsLat;
+#pragma unroll 8
+      for (int k = 0; k < kMsRows * kMsPieces / 32; ++k) {
+        const int idx = lane + 32 * k;
+        const int r = idx / kMsPieces, piece = idx - r * kMsPieces;
+        const bool ok = r < nrows;
+        cp_async16(dst + r * kMsLatBytes + ((piece ^ (r & 7)) << 4), src + (size_t)(ok ? r : 0) * kMsLat + piece * 8,
+                   ok ? 16 : 0);
+      }
+      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(smem_u32(&full[s])) : "memory");
+      ++it;
+    }
+    for (int k = max(0, it - kMsStages); k < it; ++k)
+      mbar_wait_bounded(&full[k % kMsStages], (k / kMsStages) & 1, kWaitLimit);
+    return;
+  }
+
+  // ---------------- consumers
+  const int grp = warp / kMsKw, kw = warp - grp * kMsKw;
+  const int gid = lane >> 2, tig = lane & 3, lm = lane >> 3, lr = lane & 7;
+  const uint32_t smem0 = smem_u32(mss);
+  float4* rg = red + (size_t)grp * kMsKw * 4 * 32;
+  uint32_t qh[kMsKs][4], ql[kMsKs][4];
+  int cur_b = -1;
+  bool dead = false;
+  int it = 0;
+  for (int t = t_begin; t < t_end; ++t) {
+    const int b = t / a.n_tiles, tile = t - b * a.n_tiles;
+    const int L = effective_len(a.len, b, a.append, a.cap);
+    const int row0 = tile * kMsRows;
+    if (row0 >= L) {
+      // a tile past the end inside the last 128-position tile still owes
+      // its (empty) logsumexp partials
+      if (grp == 0 && (row0 & ~(kScanRows - 1)) < L && lane < kMsH)
+        a.part[((size_t)b * kMsH + lane) * a.n_parts + (size_t)tile * kMsKw + kw] = make_float2(-INFINITY, 0.f);
+      continue;
+    }
+    const int my = it++;
+    if (my % kMsGroups != grp) continue;
+    const int s = my % kMsStages;
+    const uint32_t ph = (my / kMsStages) & 1;
+    const int nrows = min(kMsRows, L - row0);
+    if (b != cur_b) {
+      const float* qp = a.qa + (size_t)b * kMsH * kMsLat;
+#pragma unroll
+      for (int ks = 0; ks < kMsKs; ++ks) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int h = gid + ((e & 1) ? 8 : 0);
+          const int c = (kw * kMsKs + ks) * 16 + tig * 2 + ((e & 2) ? 8 : 0);
+          const float2 v = *reinterpret_cast<const float2*>(qp + (size_t)h * kMsLat + c);
+          const float x = v.x * a.qscale, y = v.y * a.qscale;
+          const float xh = bf16_round(x), yh = bf16_round(y);
+          qh[ks][e] = pack_bf16(xh, yh);
+          ql[ks][e] = pack_bf16(x - xh, y - yh);
+        }
+      }
+      cur_b = b;
+    }
+    if (!dead && !mbar_wait_bounded(&full[s], ph, kWaitLimit)) {
+      if (lane == 0) set_status(a.status, SPC_ERR_TIMEOUT);
+      dead = true;
+    }
+    const uint32_t tb = smem0 + (uint32_t)(s * kMsTile);
+    float acc[4][4], acl[4][4];
+#pragma unroll
+    for (int n = 0; n < 4; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[n][e] = acl[n][e] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < kMsKs; ++ks) {
+      const int kg = kw * kMsKs + ks;
+#pragma unroll
+      for (int np = 0; np < 2; ++np) {
+        const int row = np * 16 + ((lm >> 1) << 3) + lr;
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(tb + row * kMsLatBytes + (((kg * 2 + (lm & 1)) ^ (row & 7)) << 4), b0, b1, b2, b3);
+        mma_bf16(acc[2 * np], qh[ks], b0, b1);
+        mma_bf16(acl[2 * np], ql[ks], b0, b1);
+        mma_bf16(acc[2 * np + 1], qh[ks], b2, b3);
+        mma_bf16(acl[2 * np + 1], ql[ks], b2, b3);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+#pragma unroll
+    for (int n = 0; n < 4; ++n)
+      rg[(kw * 4 + n) * 32 + lane] =
+          make_float4(acc[n][0] + acl[n][0], acc[n][1] + acl[n][1], acc[n][2] + acl[n][2], acc[n][3] + acl[n][3]);
+    ms_bar(grp);
+    float4 v = rg[kw * 32 + lane];
+#pragma unroll
+    for (int w = 1; w < kMsKw; ++w) {
+      const float4 u = rg[(w * 4 + kw) * 32 + lane];
+      v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
+    }
+    ms_bar(grp);
+    // rows kw*8 + 2 tig, +1 of the tile; heads gid (x, y) and gid + 8 (z, w)
+    const int key = kw * 8 + tig * 2;
+    const bool v0 = key < nrows, v1 = key + 1 < nrows;
+    float* lg = a.logits + ((size_t)b * a.lstride + row0) * kMsH;
+    if (v0) { lg[key * kMsH + gid] = v.x; lg[key * kMsH + gid + 8] = v.z; }
+    if (v1) { lg[(key + 1) * kMsH + gid] = v.y; lg[(key + 1) * kMsH + gid + 8] = v.w; }
+    if (!v0) v.x = v.z = -INFINITY;
+    if (!v1) v.y = v.w = -INFINITY;
+    float m_lo = fmaxf(v.x, v.y), m_hi = fmaxf(v.z, v.w);
+#pragma unroll
+    for (int o = 1; o <= 2; o <<= 1) {
+      m_lo = fmaxf(m_lo, __shfl_xor_sync(0xffffffffu, m_lo, o));
+      m_hi = fmaxf(m_hi, __shfl_xor_sync(0xffffffffu, m_hi, o));
+    }
+    float s_lo = m_lo == -INFINITY ? 0.f : exp2f(v.x - m_lo) + exp2f(v.y - m_lo);
+    float s_hi = m_hi == -INFINITY ? 0.f : exp2f(v.z - m_hi) + exp2f(v.w - m_hi);
+#pragma unroll
+    for (int o = 1; o <= 2; o <<= 1) {
+      s_lo += __shfl_xor_sync(0xffffffffu, s_lo, o);
+      s_hi += __shfl_xor_sync(0xffffffffu, s_hi, o);
+    }
+    if (tig == 0) {
+      const size_t pi = (size_t)tile * kMsKw + kw;
+      a.part[((size_t)b * kMsH + gid) * a.n_parts + pi] = make_float2(m_lo, s_lo);
+      a.part[((size_t)b * kMsH + gid + 8) * a.n_parts + pi] = make_float2(m_hi, s_hi);
+    }
+  }
+}
+
+struct MlaLayout {
+  size_t status, done, q, qa, logits, part, keys, total;
+  int n_tiles, n_parts, lstride;
+};
+
+static MlaLayout mla_layout(int B, int cap) {
+  MlaLayout l{};
+  l.n_tiles = (cap + kMsRows - 1) / kMsRows;
+  l.n_parts = ((cap + kScanRows - 1) / kScanRows) * kMsPpt;
+  l.lstride = (cap + 3) & ~3;
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off = (off + bytes + 255) & ~size_t(255); return o; };
+  l.status = take(2 * sizeof(int));
+  l.done = l.status + sizeof(int);
+  l.q = take(sizeof(float) * (size_t)B * kMsH * kMsQk);
+  l.qa = take(sizeof(float) * (size_t)B * kMsH * kMsLat);
+  l.logits = take(sizeof(float) * (size_t)B * kMsH * l.lstride);
+  l.part = take(sizeof(float2) * (size_t)B * kMsH * l.n_parts);
+  l.keys = take(sizeof(uint32_t) * (size_t)B * ((cap + 3) & ~3));
+  l.total = off;
+  return l;
+}
+
+size_t mla_score_select_workspace(int B, int cap) { return mla_layout(B, cap).total; }
+
+int mla_score_select_launch(const MlaScoreSelectCall& c) {
+  const MlaLayout l = mla_layout(c.B, c.cap);
+  uint8_t* ws = static_cast<uint8_t*>(c.workspace);
+  cudaStream_t st = static_cast<cudaStream_t>(c.stream);
+  int* status = reinterpret_cast<int*>(ws + l.status);
+  float* qws = reinterpret_cast<float*>(ws + l.q);
+  float* qa = reinterpret_cast<float*>(ws + l.qa);
+
+  // ---- projection (CUDA cores; the latent row's last tile is partial), absorption
+  if (c.stages & SPC_STAGE_PROJECT) {
+    ProjArgs pa{};
+    pa.x = static_cast<const uint16_t*>(c.x);
+    pa.Wq = static_cast<const uint16_t*>(c.Wq);
+    pa.Wk = static_cast<const uint16_t*>(c.Wdkv);
+    pa.K_dlm = static_cast<uint16_t*>(c.C_dlm);
+    pa.len = c.len;
+    pa.q_ws = qws;
+    pa.q_out = nullptr;
+    pa.status = status;
+    pa.B = c.B; pa.H = c.H; pa.Nq = kMsH * kMsQk; pa.Nk = kMsLat; pa.Ntot = pa.Nq + pa.Nk; pa.n_kv = 1;
+    pa.cap = c.cap; pa.latent = 1;
+    const int n_tiles = (pa.Nq + (c.append ? pa.Nk : 0) + kProjTile - 1) / kProjTile;
+    const int bb = c.B <= 1 ? 1 : c.B <= 2 ? 2 : c.B <= 4 ? 4 : c.B <= 8 ? 8 : 16;
+    const int bz = (c.B + bb - 1) / bb;
+    int rc;
+    switch (bb) {
+      case 1: rc = launch_proj<1>(pa, n_tiles, bz, st); break;
+      case 2: rc = launch_proj<2>(pa, n_tiles, bz, st); break;
+      case 4: rc = launch_proj<4>(pa, n_tiles, bz, st); break;
+      case 8: rc = launch_proj<8>(pa, n_tiles, bz, st); break;
+      default: rc = launch_proj<16>(pa, n_tiles, bz, st); break;
+    }
+    if (rc != SPC_OK) return rc;
+    rc = mla_absorb_launch(qws, 0, c.Wuk, c.B, c.B, qa, c.stream);
+    if (rc != SPC_OK) return rc;
+  }
+
+  // ---- latent scan
+  if (c.stages & SPC_STAGE_SCAN) {
+    MlaScanArgs sa{};
+    sa.C = static_cast<const uint16_t*>(c.C_dlm);
+    sa.qa = qa;
+    sa.len = c.len;
+    sa.logits = reinterpret_cast<float*>(ws + l.logits);
+    sa.part = reinterpret_cast<float2*>(ws + l.part);
+    sa.status = status;
+    sa.cap = c.cap; sa.lstride = l.lstride; sa.n_tiles = l.n_tiles; sa.total_tiles = c.B * l.n_tiles;
+    sa.append = c.append; sa.n_parts = l.n_parts;
+    sa.qscale = kLog2e / sqrtf((float)kMsQk);
+    const int sms = device_sm_count() > 0 ? device_sm_count() : 1;
+    sa.tpc = (sa.total_tiles + sms - 1) / sms;
+    if (sa.tpc < 1) sa.tpc = 1;
+    const int grid = (sa.total_tiles + sa.tpc - 1) / sa.tpc;
+    static bool attr = false;
+    if (!attr) {
+      if (cudaFuncSetAttribute(mla_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMsSmem) !=
+          cudaSuccess)
+        return SPC_ERR_CUDA;
+      attr = true;
+    }
+    mla_scan_kernel<<<grid, kMsThreads, kMsSmem, st>>>(sa);
+    if (cudaGetLastError() != cudaSuccess) return SPC_ERR_CUDA;
+  }
+
+  // ---- logsumexp, group score over all 16 heads, Top-K (one per request)
+  if (c.stages & SPC_STAGE_SELECT) {
+    SelArgs sa{};
+    sa.logits = reinterpret_cast<const float*>(ws + l.logits);
+    sa.part = reinterpret_cast<const float2*>(ws + l.part);
+    sa.keys = reinterpret_cast<uint32_t*>(ws + l.keys);
+    sa.len = c.len;
+    sa.scores_out = c.scores_out;
+    sa.selected = c.selected;
+    sa.done = reinterpret_cast<uint32_t*>(ws + l.done);
+    sa.B = c.B; sa.n_q = kMsH; sa.n_kv = 1; sa.cap = c.cap; sa.lstride = l.lstride; sa.K = c.budget;
+    sa.n_sink = c.n_sink; sa.n_recent = c.n_recent; sa.append = c.append;
+    sa.n_parts = l.n_parts; sa.ppt = kMsPpt; sa.kstride = (c.cap + 3) & ~3;
+    const int rc = launch_select<kMsH>(sa, c.B, st);
     if (rc != SPC_OK) return rc;
   }
   return SPC_OK;

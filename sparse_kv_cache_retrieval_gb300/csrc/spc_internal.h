@@ -50,6 +50,33 @@ int attn_noalloc_launch(const void* q, const spc_kv_view* views, const int32_t* 
                         const int32_t* slot_pos, int n_layers, int B, int n_q, int n_kv, int budget,
                         float scale, float* out, void* stream);
 
+struct MlaScoreSelectCall {
+  const void* x;
+  const void* Wq;
+  const void* Wuk;
+  const void* Wdkv;
+  void* C_dlm;
+  int32_t* len;
+  int append;
+  int B, H, cap, budget, n_sink, n_recent;
+  float* scores_out;
+  int32_t* selected;
+  void* workspace;
+  void* stream;
+  int stages;
+};
+
+size_t mla_score_select_workspace(int B, int cap);
+int mla_score_select_launch(const MlaScoreSelectCall& c);
+int mla_absorb_launch(const void* q, int q_bf16, const void* Wuk, int n_items, int items_per_w, float* qa,
+                      void* stream);
+size_t mla_attn_workspace(int n_layers, int B, int budget);
+int mla_attn_launch(const void* q, const void* Wuk, const void* Wuv, const spc_kv_view* views,
+                    const int32_t* selected, const int32_t* slot_pos, int n_layers, int B, int budget,
+                    float scale, float* out, void* workspace, void* stream);
+int mla_gather_launch(const spc_gather_view* views, int layer_lo, int layer_hi, const int32_t* load_slot,
+                      const int32_t* load_pos, const int32_t* n_load, int B, int budget, void* stream);
+
 int stream_read_launch(const void* src, size_t bytes, uint32_t* sink, int n_blocks, void* stream);
 
 int device_sm_count();

@@ -38,6 +38,7 @@ from .configs import Workload
 # Stream tags: each tensor draws from its own SeedSequence child, so changing
 # the number of steps or layers never changes any other tensor.
 _TAG_WQ, _TAG_WK, _TAG_KDLM, _TAG_HOT, _TAG_X, _TAG_QLLM, _TAG_KV = 1, 2, 3, 4, 5, 6, 7
+_TAG_WUK, _TAG_WDKV, _TAG_WUK_L, _TAG_WUV_L = 8, 9, 10, 11
 
 
 def rng_for(seed: int, *tags: int) -> np.random.Generator:
@@ -195,5 +196,120 @@ def fill_llm_kv_store(cfg: Workload, b: int, layer_lo: int, layer_hi: int, store
         list(ex.map(work, jobs))
 
 
+# ------------------------------------------------------------------ MLA
+# Recipe of the MLA workloads (DeepSeek-V2-style latent attention, 16 heads):
+#   * retrieval head: W_q [H][16*192] ~ N(0, 1/H) (per head 128 nope then 64
+#     rope columns), W_uk [16][128][512] ~ N(0, 1/512), W_dkv [H][576] ~ N(0, 1/H);
+#   * the head's latent cache C_dlm[b][p] ~ N(0, I_576) for p < len_b, zero
+#     above; planted hot positions get C += gamma * sqrt(16) * u, u the unit
+#     direction of the sum over heads of the heads' initial queries expressed
+#     in latent coordinates, [W_uk[h]^T q_nope ; q_rope] (data shaping only),
+#     so planted logits start about gamma standard deviations up;
+#   * LLM: latent rows ~ N(0, I_576) per layer and position; W_uk, W_uv per
+#     layer [16][128][512] ~ N(0, 1/512); queries [16][192] per layer drift as
+#     for GQA with norm sqrt(192).
+MLA_LAT, MLA_DC, MLA_NOPE, MLA_QK = 576, 512, 128, 192
+
+
+@dataclasses.dataclass
+class MlaInputs:
+    cfg: Workload
+    Wq: np.ndarray                  # u16 [H][16*192]
+    Wuk: np.ndarray                 # u16 [16][128][512] (retrieval head)
+    Wdkv: np.ndarray                # u16 [H][576]
+    C_dlm: np.ndarray               # u16 [B][cap][576]
+    hot: List[np.ndarray]           # per request: int64 [1][hot_b]
+    x: np.ndarray                   # u16 [steps+1][B][H]
+    q_llm: np.ndarray               # u16 [steps][n_layers][B][16][192]
+    Wuk_llm: np.ndarray             # u16 [n_layers][16][128][512]
+    Wuv_llm: np.ndarray             # u16 [n_layers][16][128][512]
+    lens: np.ndarray
+
+
+def make_mla_inputs(cfg: Workload, steps: Optional[int] = None, n_layers: Optional[int] = None) -> MlaInputs:
+    """Everything of an MLA workload except the LLM latent stores."""
+    steps = cfg.steps if steps is None else steps
+    L = cfg.n_layers if n_layers is None else n_layers
+    B, H, n_q, cap = cfg.B, cfg.H, cfg.n_q, cfg.cap
+    Wq = np.empty((H, n_q * MLA_QK), np.uint16)
+    _normal_bf16_into(Wq, rng_for(cfg.seed, _TAG_WQ), 1.0 / np.sqrt(H))
+    Wuk = np.empty((n_q, MLA_NOPE, MLA_DC), np.uint16)
+    _normal_bf16_into(Wuk, rng_for(cfg.seed, _TAG_WUK), 1.0 / np.sqrt(MLA_DC))
+    Wdkv = np.empty((H, MLA_LAT), np.uint16)
+    _normal_bf16_into(Wdkv, rng_for(cfg.seed, _TAG_WDKV), 1.0 / np.sqrt(H))
+    Wuk_l = np.empty((L, n_q, MLA_NOPE, MLA_DC), np.uint16)
+    Wuv_l = np.empty((L, n_q, MLA_NOPE, MLA_DC), np.uint16)
+    for l in range(L):
+        _normal_bf16_into(Wuk_l[l], rng_for(cfg.seed, _TAG_WUK_L, l), 1.0 / np.sqrt(MLA_DC))
+        _normal_bf16_into(Wuv_l[l], rng_for(cfg.seed, _TAG_WUV_L, l), 1.0 / np.sqrt(MLA_DC))
+
+    xs = np.empty((steps + 1, B, H), np.uint16)
+    for b in range(B):
+        r = rng_for(cfg.seed, _TAG_X, b)
+        x = r.standard_normal(H)
+        for t in range(steps + 1):
+            if t > 0:
+                x = _drift(x, r.standard_normal(H), cfg.rho[b], np.sqrt(H))
+            xs[t, b] = to_bf16_bits(x.astype(np.float32))
+
+    q_llm = np.empty((steps, L, B, n_q, MLA_QK), np.uint16)
+    for b in range(B):
+        r = rng_for(cfg.seed, _TAG_QLLM, b)
+        q = r.standard_normal((L, n_q, MLA_QK))
+        q *= np.sqrt(MLA_QK) / np.linalg.norm(q, axis=-1, keepdims=True)
+        for t in range(steps):
+            if t > 0:
+                q = _drift(q, r.standard_normal((L, n_q, MLA_QK)), cfg.rho[b], np.sqrt(MLA_QK))
+            q_llm[t, :, b] = to_bf16_bits(q.astype(np.float32))
+
+    C = np.zeros((B, cap, MLA_LAT), np.uint16)
+    Wq_f = bf16_bits_to_f32(Wq)
+    Wuk_f = bf16_bits_to_f32(Wuk)
+    hot = []
+    for b in range(B):
+        Lb = int(cfg.lens[b])
+        _normal_bf16_into(C[b, :Lb], rng_for(cfg.seed, _TAG_KDLM, b))
+        q0 = (bf16_bits_to_f32(xs[0, b]) @ Wq_f).reshape(n_q, MLA_QK)
+        lat = np.einsum("hjc,hj->hc", Wuk_f, q0[:, :MLA_NOPE])
+        u = np.concatenate([lat, q0[:, MLA_NOPE:]], axis=1).sum(axis=0)
+        u /= np.linalg.norm(u)
+        r = rng_for(cfg.seed, _TAG_HOT, b)
+        lo, hi = cfg.n_sink, max(cfg.n_sink, Lb - cfg.n_recent)
+        n_hot = min(int(cfg.hot[b]), hi - lo)
+        pos = np.sort(r.choice(np.arange(lo, hi), size=n_hot, replace=False))
+        rows = bf16_bits_to_f32(C[b, pos]) + np.float32(cfg.gamma * np.sqrt(n_q)) * u.astype(np.float32)
+        C[b, pos] = to_bf16_bits(rows)
+        hot.append(pos[None, :].astype(np.int64))
+    return MlaInputs(cfg=cfg, Wq=Wq, Wuk=Wuk, Wdkv=Wdkv, C_dlm=C, hot=hot, x=xs, q_llm=q_llm, Wuk_llm=Wuk_l,
+                     Wuv_llm=Wuv_l, lens=np.asarray(cfg.lens, np.int32))
+
+
+def fill_mla_layer(cfg: Workload, b: int, layer: int, out: np.ndarray) -> None:
+    """LLM latent rows of request b, one layer: u16 [rows][576] (the first
+    rows of the layer's sequence, so any prefix agrees)."""
+    _normal_bf16_into(out, rng_for(cfg.seed, _TAG_KV, b, layer))
+
+
+def fill_mla_store(cfg: Workload, b: int, layer_lo: int, layer_hi: int, store: np.ndarray, store_layer0: int,
+                   threads: Optional[int] = None) -> None:
+    """``fill_mla_layer`` rows of layers [layer_lo, layer_hi) written into a
+    position-major store u16 [rows][store_layers][576]."""
+    rows = store.shape[0]
+
+    def work(l):
+        tmp = np.empty((rows, MLA_LAT), np.uint16)
+        fill_mla_layer(cfg, b, l, tmp)
+        store[:, l - store_layer0, :] = tmp
+
+    layers = list(range(layer_lo, layer_hi))
+    threads = threads or min(16, os.cpu_count() or 1)
+    if threads <= 1 or len(layers) <= 1:
+        for l in layers:
+            work(l)
+        return
+    with cf.ThreadPoolExecutor(threads) as ex:
+        list(ex.map(work, layers))
+
+
 __all__ = ["Inputs", "make_inputs", "fill_llm_kv", "fill_llm_kv_store", "to_bf16_bits", "bf16_bits_to_f32",
-           "rng_for"]
+           "rng_for", "MlaInputs", "make_mla_inputs", "fill_mla_layer", "fill_mla_store"]

@@ -167,3 +167,45 @@ def test_fill_slots_validates_before_launch(lib):
     assert lib.spc_fill_slots(FAKE, 0, 1, FAKE, 1, 8, 64, 100, 64, None) == -2
     assert lib.spc_fill_slots(FAKE, 2, 1, FAKE, 1, 8, 128, 100, 64, None) == -2
     assert lib.spc_fill_slots(FAKE, 0, 1, FAKE, 1, 8, 128, 100, 5000, None) == -2
+
+
+def _mla_score(lib, **kw):
+    a = dict(x=FAKE, Wq=FAKE, Wuk=FAKE, Wd=FAKE, C=FAKE, len=FAKE, append=0, B=1, H=2048, cap=4096,
+             budget=512, n_sink=4, n_recent=64, scores=None, sel=FAKE, ws=FAKE, ws_bytes=0, stream=None,
+             stages=7)
+    a.update(kw)
+    return lib.spc_mla_score_select(a["x"], a["Wq"], a["Wuk"], a["Wd"], a["C"], a["len"], a["append"], a["B"],
+                                    a["H"], a["cap"], a["budget"], a["n_sink"], a["n_recent"], a["scores"],
+                                    a["sel"], a["ws"], a["ws_bytes"], a["stream"], a["stages"])
+
+
+def test_mla_calls_validate_before_launch(lib):
+    assert _mla_score(lib, x=None) == -1
+    assert _mla_score(lib, Wuk=None) == -1
+    assert _mla_score(lib, append=1, Wd=None) == -1
+    assert _mla_score(lib, C=FAKE + 8) == -1             # misaligned latent cache
+    assert _mla_score(lib, stages=0) == -1
+    assert _mla_score(lib, H=2047) == -2
+    assert _mla_score(lib, budget=8192) == -2
+    assert _mla_score(lib, budget=600, cap=512) == -2
+    assert _mla_score(lib, n_sink=500) == -2
+    assert _mla_score(lib) == -5                         # workspace too small
+    ws = B.spc_mla_score_select_workspace_size(1, 2048, 32768, 2048)
+    assert ws >= 16 * 32768 * 4                          # fp32 logits of 16 heads
+    assert lib.spc_mla_gather(None, 0, 1, FAKE, FAKE, FAKE, 1, 4096, 512, None) == -1
+    assert lib.spc_mla_gather(FAKE, 2, 1, FAKE, FAKE, FAKE, 1, 4096, 512, None) == -2
+    assert lib.spc_mla_gather(FAKE, 0, 1, FAKE, FAKE, FAKE, 65, 4096, 512, None) == -2
+    assert lib.spc_mla_gather(FAKE, 0, 1, FAKE, FAKE, FAKE, 1, 4096, 5000, None) == -2
+    wa = B.spc_mla_decode_attn_workspace_size(16, 1, 2048)
+    assert wa >= 16 * 16 * 576 * 4                       # the absorbed queries at least
+    assert B.spc_mla_decode_attn_workspace_size(16, 1, 5000) == 0
+    args = [FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, 1, 2048, 0.07, FAKE, FAKE, wa, None]
+    assert lib.spc_mla_decode_attn(None, *args[1:]) == -1
+    bad = list(args); bad[9] = 0.0
+    assert lib.spc_mla_decode_attn(*bad) == -1
+    bad = list(args); bad[12] = wa - 1
+    assert lib.spc_mla_decode_attn(*bad) == -5
+    bad = list(args); bad[8] = 0
+    assert lib.spc_mla_decode_attn(*bad) == -2
+    bad = list(args); bad[11] = FAKE + 64
+    assert lib.spc_mla_decode_attn(*bad) == -1           # workspace not 256-byte aligned
