@@ -171,8 +171,9 @@ struct MlaAttnArgs {
 
 __device__ __forceinline__ void ma_bar() { asm volatile("bar.sync 1, %0;" :: "n"(kMaCThreads) : "memory"); }
 
-// two CTAs per SM: 200 registers for each of the 160 threads
-__global__ void __maxnreg__(200) mla_attn_kernel(MlaAttnArgs a) {
+// two CTAs per SM: ten warps over four sub-partitions of 16K registers leave
+// 168 registers per thread
+__global__ void __launch_bounds__(kMaThreads, 2) mla_attn_kernel(MlaAttnArgs a) {
   extern __shared__ __align__(128) uint8_t msm[];
   float4* red = reinterpret_cast<float4*>(msm + MaSmem::stages);
   uint16_t* pbuf = reinterpret_cast<uint16_t*>(msm + MaSmem::stages + MaSmem::red);       // [2][16][40]

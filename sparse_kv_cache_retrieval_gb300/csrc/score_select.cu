@@ -1456,8 +1456,9 @@ int score_select_launch(const ScoreSelectCall& c) {
 // for the absorbed queries qa (576 values: W_uk[h]^T q_nope ; q_rope) over
 // the 576-value latent rows. One CTA per SM: a producer warp streams 32-row
 // tiles (36 KiB) into a 4-stage ring with 16-byte cp.async (pieces XOR-
-// swizzled by row); two groups of four consumer warps take alternate tiles.
-// Within a group the four warps split the 576 dims (9 k-steps of mma.sync
+// swizzled by row) for four consumer warps (a second group of four would
+// leave each warp 168 registers, and the query fragments alone take 72).
+// The four warps split the 576 dims (9 k-steps of mma.sync
 // m16n8k16 each, the 16 heads on the M side, the query in bf16 high and low
 // parts so the logits keep fp32 accuracy), sum their partial tiles through
 // shared memory, and each finishes 8 of the 32 rows: logits out, one
@@ -1469,7 +1470,7 @@ constexpr int kMsH = SPC_MLA_HEADS;                     // 16
 constexpr int kMsQk = SPC_MLA_NOPE + SPC_MLA_ROPE;      // 192
 constexpr int kMsRows = 32;
 constexpr int kMsStages = 4;
-constexpr int kMsGroups = 2;
+constexpr int kMsGroups = 1;   // nine warps would cap registers at 168 (16K per SM sub-partition)
 constexpr int kMsKw = 4;
 constexpr int kMsThreads = (kMsGroups * kMsKw + 1) * 32;
 constexpr int kMsKs = kMsLat / 16 / kMsKw;              // 9
@@ -1493,8 +1494,7 @@ __device__ __forceinline__ void ms_bar(int grp) {
   asm volatile("bar.sync %0, %1;" :: "r"(1 + grp), "n"(kMsKw * 32) : "memory");
 }
 
-// one CTA per SM: 224 registers for each of the 288 threads
-__global__ void __maxnreg__(224) mla_scan_kernel(MlaScanArgs a) {
+__global__ void __launch_bounds__(kMsThreads, 1) mla_scan_kernel(MlaScanArgs a) {
   extern __shared__ __align__(128) uint8_t mss[];
   float4* red = reinterpret_cast<float4*>(mss + kMsStages * (size_t)kMsTile);
   uint64_t* full = reinterpret_cast<uint64_t*>(mss + kMsStages * (size_t)kMsTile + kMsRed);

@@ -36,8 +36,8 @@ import numpy as np
 import torch
 
 from . import binding as spc
-from .configs import Workload
-from .synth import Inputs, fill_llm_kv, fill_llm_kv_store
+from .configs import MLA_LATENT_ROW, MLA_QK, Workload
+from .synth import Inputs, fill_llm_kv, fill_llm_kv_store, fill_mla_layer, fill_mla_store
 
 _BF16_ROW = 256  # bytes of one K or V row at d = 128
 
@@ -49,11 +49,13 @@ def _dev_u16(a: np.ndarray, device) -> torch.Tensor:
 class DecodePipeline:
     """Device-resident state and the pipelined decode step for one workload.
 
-    ``inputs`` comes from ``synth.make_inputs``; ``n_layers`` may be smaller
-    than the workload's to keep tests small. LLM K/V of layers
-    [0, gpu_layers[b]) lives in HBM (attention reads it by position); the
-    other layers live in pinned host memory (``host_stores``) and are reached
-    through budget-sized HBM slots.
+    ``inputs`` comes from ``synth.make_inputs`` (``synth.make_mla_inputs`` for
+    an MLA workload); ``n_layers`` may be smaller than the workload's to keep
+    tests small. LLM KV of layers [0, gpu_layers[b]) lives in HBM (attention
+    reads it by position); the other layers live in pinned host memory
+    (``host_stores``) and are reached through budget-sized HBM slots. A
+    position of one layer holds K and V rows of every KV head ([2][n_kv][d],
+    GQA) or one 576-value latent row (MLA, n_kv = 1).
     """
 
     def __init__(self, cfg: Workload, inputs: Inputs, *, device: str = "cuda",
@@ -68,23 +70,36 @@ class DecodePipeline:
         self.B, self.H, self.n_q, self.n_kv, self.d = cfg.B, cfg.H, cfg.n_q, cfg.n_kv, cfg.d
         self.K, self.cap = cfg.budget, cfg.cap
         self.G = cfg.G
-        self.scale = 1.0 / math.sqrt(self.d)
+        self.mla = cfg.mla
+        self.qdim = MLA_QK if self.mla else self.d           # per-head LLM query width
+        self.scale = 1.0 / math.sqrt(self.qdim)
         self.gpu_layers = [min(int(g), self.L) for g in cfg.gpu_layers]
         self.host_io = host_io
         self.timing = timing
         dev = self.dev
         B, L, K, n_kv, d, cap = self.B, self.L, self.K, self.n_kv, self.d, self.cap
 
-        # retrieval head
+        # retrieval head (MLA: W_uk of the head, the latent down-projection
+        # for appends and the head's latent cache in place of W_k / K_dlm)
         self.Wq = _dev_u16(inputs.Wq, dev)
-        self.Wk = _dev_u16(inputs.Wk, dev)
-        self.K_dlm = _dev_u16(inputs.K_dlm, dev)
         self.len = torch.from_numpy(inputs.lens.astype(np.int32)).to(dev)
-        self.ws_score = torch.zeros(spc.spc_score_select_workspace_size(B, self.H, self.n_q, n_kv, d, cap, K),
-                                    dtype=torch.uint8, device=dev)
+        if self.mla:
+            if kv_bytes is not None:
+                raise ValueError("adaptive layer offload is implemented for GQA caches only")
+            self.Wuk = _dev_u16(inputs.Wuk, dev)
+            self.Wk = _dev_u16(inputs.Wdkv, dev)
+            self.K_dlm = _dev_u16(inputs.C_dlm, dev)
+            self.Wuk_llm = _dev_u16(inputs.Wuk_llm[:self.L], dev)
+            self.Wuv_llm = _dev_u16(inputs.Wuv_llm[:self.L], dev)
+            ws_bytes = spc.spc_mla_score_select_workspace_size(B, self.H, cap, K)
+        else:
+            self.Wk = _dev_u16(inputs.Wk, dev)
+            self.K_dlm = _dev_u16(inputs.K_dlm, dev)
+            ws_bytes = spc.spc_score_select_workspace_size(B, self.H, self.n_q, n_kv, d, cap, K)
+        self.ws_score = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
         n_steps = inputs.q_llm.shape[0]
         self.x_dev = _dev_u16(inputs.x, dev)                                  # [steps+1][B][H]
-        self.q_dev = _dev_u16(inputs.q_llm[:, :L], dev)                       # [steps][L][B][n_q][d]
+        self.q_dev = _dev_u16(inputs.q_llm[:, :L], dev)                       # [steps][L][B][n_q][qdim]
         self.n_steps = n_steps
 
         # selection state, double-buffered by step parity
@@ -136,26 +151,38 @@ class DecodePipeline:
             s0 = 0 if self.adaptive else ng
             layers = []
             for l in range(ng):
-                buf = np.empty((1, 2, n_kv, cap, d), np.uint16)
-                fill_llm_kv(cfg, b, l, buf, threads=fill_threads)
-                layers.append(_dev_u16(buf[0], dev))
+                if self.mla:
+                    buf = np.empty((cap, MLA_LATENT_ROW), np.uint16)
+                    fill_mla_layer(cfg, b, l, buf)
+                    layers.append(_dev_u16(buf, dev))
+                else:
+                    buf = np.empty((1, 2, n_kv, cap, d), np.uint16)
+                    fill_llm_kv(cfg, b, l, buf, threads=fill_threads)
+                    layers.append(_dev_u16(buf[0], dev))
                 del buf
             self.hbm.append(layers)
             if L - s0 > 0:
-                # position-major [cap][n_kv][layers][2][d]: one (position, head)
-                # holds every stored layer's K and V row in one host page
-                hs = torch.empty((cap, n_kv, L - s0, 2, d), dtype=torch.int16, pin_memory=True)
-                if L - ng > 0:
-                    fill_llm_kv_store(cfg, b, ng, L, hs.numpy().view(np.uint16), s0, threads=fill_threads)
+                # position-major [cap][n_kv][layers][2][d] (MLA: [cap][layers][576]):
+                # one (position, head) holds every stored layer's row(s) in one host page
+                if self.mla:
+                    hs = torch.empty((cap, L - s0, MLA_LATENT_ROW), dtype=torch.int16, pin_memory=True)
+                    if L - ng > 0:
+                        fill_mla_store(cfg, b, ng, L, hs.numpy().view(np.uint16), s0, threads=fill_threads)
+                    sl = torch.zeros((L - s0, K, MLA_LATENT_ROW), dtype=torch.int16, device=dev)
+                else:
+                    hs = torch.empty((cap, n_kv, L - s0, 2, d), dtype=torch.int16, pin_memory=True)
+                    if L - ng > 0:
+                        fill_llm_kv_store(cfg, b, ng, L, hs.numpy().view(np.uint16), s0, threads=fill_threads)
+                    sl = torch.zeros((L - s0, 2, n_kv, K, d), dtype=torch.int16, device=dev)
                 self.host_stores.append(hs)
-                self.slots.append(torch.zeros((L - s0, 2, n_kv, K, d), dtype=torch.int16, device=dev))
+                self.slots.append(sl)
                 self._store_dev.append(spc.spc_host_device_pointer(hs))
             else:
                 self.host_stores.append(None)
                 self.slots.append(None)
                 self._store_dev.append(0)
             self.store_base.append(s0)
-        self._slot_layer_bytes = 2 * n_kv * K * d * 2
+        self._slot_layer_bytes = K * cfg.row_elems * 2
         self.gviews = spc.to_device_bytes(self._gather_view_table(), dev)
 
         # attention views [L][B]
@@ -166,8 +193,9 @@ class DecodePipeline:
         # layer chunks, streams, events
         lc = max(1, min(layers_per_launch, L))
         self.chunks = [(l0, min(L, l0 + lc)) for l0 in range(0, L, lc)]
-        self.ws_attn = torch.zeros(spc.spc_sparse_decode_attn_workspace_size(lc, B, self.n_q, n_kv, d, K),
-                                   dtype=torch.uint8, device=dev)
+        ws_attn = (spc.spc_mla_decode_attn_workspace_size(lc, B, K) if self.mla else
+                   spc.spc_sparse_decode_attn_workspace_size(lc, B, self.n_q, n_kv, d, K))
+        self.ws_attn = torch.zeros(ws_attn, dtype=torch.uint8, device=dev)
         # stream priorities: select/diff/attention (A) and the link-bound
         # gathers (B) are on the critical path; the front (C) has a whole
         # step of slack, so its CTAs yield to theirs
@@ -202,7 +230,7 @@ class DecodePipeline:
         self.host_io = False
         if host_io:
             self.enable_host_io()
-        self.h2d_bytes_per_step = (B * self.H + L * B * self.n_q * d) * 2
+        self.h2d_bytes_per_step = (B * self.H + L * B * self.n_q * self.qdim) * 2
         self.d2h_bytes_per_step = L * B * self.n_q * d * 4 + B * n_kv * K * 4
 
         # optional timing events: (stream, kind, start, end) per launch
@@ -234,6 +262,8 @@ class DecodePipeline:
             base, rows, use = self.hbm[b][l], self.cap, 0
         else:
             base, rows, use = self.slots[b][l - self.store_base[b]], self.K, 1
+        if self.mla:
+            return spc.kv_views([base.data_ptr()], [0], [rows], [use])
         return spc.kv_views([base[0].data_ptr()], [base[1].data_ptr()], [rows], [use])
 
     def host_slots(self, b: int) -> Optional[torch.Tensor]:
@@ -348,14 +378,14 @@ class DecodePipeline:
         self.x_host = torch.from_numpy(inputs.x.view(np.int16).copy()).pin_memory()
         self.q_host = torch.from_numpy(np.ascontiguousarray(inputs.q_llm[:, :L]).view(np.int16)).pin_memory()
         self.x_stage = torch.empty(B, self.H, dtype=torch.int16, device=dev)
-        self.q_stage = torch.empty(2, L, B, self.n_q, d, dtype=torch.int16, device=dev)
+        self.q_stage = torch.empty(2, L, B, self.n_q, self.qdim, dtype=torch.int16, device=dev)
         self.out_host = torch.empty((n_steps, L, B, self.n_q, d), dtype=torch.float32).pin_memory()
         self.sel_host = torch.empty((n_steps, B, self.n_kv, self.K), dtype=torch.int32).pin_memory()
         # transfers run as libspc copy kernels on the device-visible addresses
         # of the pinned buffers (a copy-engine transfer to or from host memory
         # inside a CUDA graph stalled every step)
         self._x_bytes = B * self.H * 2
-        self._q_bytes = L * B * self.n_q * d * 2
+        self._q_bytes = L * B * self.n_q * self.qdim * 2
         self._out_bytes = L * B * self.n_q * d * 4
         self._sel_bytes = B * self.n_kv * self.K * 4
         self._x_dev_host = spc.spc_host_device_pointer(self.x_host)
@@ -381,6 +411,11 @@ class DecodePipeline:
     # ------------------------------------------------------------------ pieces
     def _score_select(self, x, out_sel, append: int, stream, stages: int = 7, q_out=None, scores_out=None):
         c = self.cfg
+        if self.mla:
+            spc.spc_mla_score_select(x, self.Wq, self.Wuk, self.Wk, self.K_dlm, self.len, append, self.B, self.H,
+                                     self.cap, self.K, c.n_sink, c.n_recent, scores_out, out_sel, self.ws_score,
+                                     stream=stream, stages=stages)
+            return
         spc.spc_score_select_stages(x, self.Wq, self.Wk, self.K_dlm, self.len, append, self.B, self.H,
                                     self.n_q, self.n_kv, self.d, self.cap, self.K, c.n_sink, c.n_recent,
                                     q_out, scores_out, out_sel, self.ws_score, stream=stream,
@@ -393,11 +428,20 @@ class DecodePipeline:
                              stream=stream)
 
     def _gather(self, pn, l0, l1, stream):
+        if self.mla:
+            spc.spc_mla_gather(self.gviews, l0, l1, self.load_slot[pn], self.load_pos[pn], self.n_load[pn], self.B,
+                               self.cap, self.K, stream=stream)
+            return
         spc.spc_gather_kv(self.gviews, l0, l1, self.load_slot[pn], self.load_pos[pn], self.n_load[pn],
                           self.B, self.n_kv, self.d, self.cap, self.K, stream=stream)
 
     def _attn(self, q_layers, out, p, l0, l1, stream):
         views = self.aviews.data_ptr() + l0 * self.aview_stride
+        if self.mla:
+            spc.spc_mla_decode_attn(q_layers[l0].data_ptr(), self.Wuk_llm[l0].data_ptr(),
+                                    self.Wuv_llm[l0].data_ptr(), views, self.selected[p], self.slot_pos[p], l1 - l0,
+                                    self.B, self.K, self.scale, out[l0].data_ptr(), self.ws_attn, stream=stream)
+            return
         spc.spc_sparse_decode_attn(q_layers[l0].data_ptr(), views, self.selected[p], self.slot_pos[p],
                                    l1 - l0, self.B, self.n_q, self.n_kv, self.d, self.K, self.scale,
                                    out[l0].data_ptr(), self.ws_attn, stream=stream)
@@ -610,7 +654,8 @@ class DecodePipeline:
         return self.n_load[parity].cpu().numpy()
 
     def key_scan_bytes(self, lens) -> int:
-        return int(sum(int(L) for L in lens) * self.n_kv * self.d * 2)
+        row = MLA_LATENT_ROW if self.mla else self.n_kv * self.d
+        return int(sum(int(L) for L in lens) * row * 2)
 
 
 __all__ = ["DecodePipeline"]

@@ -8,6 +8,7 @@ the 2e-3 tie band of the K-th score; the appended latent row within 1 bf16
 ulp; gathered rows bit-exact; attention within 1e-2 absolute (the bar of the
 GQA path).
 """
+import dataclasses
 import math
 
 import numpy as np
@@ -205,3 +206,111 @@ def test_mla_attention_many_splits():
     # one (layer, request) and the largest budget: 128 tiles of 32 rows over
     # 64 CTAs of two tiles each
     _attn_case(B=1, n_layers=1, budget=4096, hbm_layers=0, seed=79, cap=5000)
+
+
+# ------------------------------------------------------------------ the decode step
+def run_mla_chain(cfg, steps, L, layers_per_launch=1):
+    """The pipelined MLA decode step against the oracle's own chain: while the
+    GPU and oracle selections agree, load lists and slot maps match bit for
+    bit and attention is within the bar; a tie-band swap makes that request's
+    later steps comparable on sets only (band, slot contents)."""
+    from sparse_kv_cache_retrieval_gb300.pipeline import DecodePipeline
+    from sparse_kv_cache_retrieval_gb300.synth import fill_mla_layer
+    inp = make_mla_inputs(cfg, steps=steps, n_layers=L)
+    pipe = DecodePipeline(cfg, inp, n_layers=L, layers_per_launch=layers_per_launch)
+    stores = []
+    for b in range(cfg.B):
+        st = np.empty((L, cfg.cap, M.D_LAT), np.uint16)
+        for l in range(L):
+            fill_mla_layer(cfg, b, l, st[l])
+        stores.append(st)
+    ost = M.MlaDecodeState(inp.C_dlm, inp.lens, stores, pipe.gpu_layers, cfg.budget, cfg.n_sink, cfg.n_recent)
+    _, _, _, oss, osel = ost.score_select(inp.x[0], inp.Wq, inp.Wuk, inp.Wdkv, cfg.n_q, append=False)
+    ost.diff_and_gather(osel)
+    pipe.prologue()
+    diverged = np.zeros(cfg.B, bool)
+    swaps = 0
+    g0 = pipe.selected[0].cpu().numpy()
+    for b in range(cfg.B):
+        ok, sw, msg = selection_within_tie_band(g0[b, 0], osel[b][0], oss[b][0], cfg.budget, cfg.n_sink,
+                                                cfg.n_recent)
+        assert ok, f"prologue b={b}: {msg}"
+        swaps += sw
+        diverged[b] |= sw > 0
+    scale = 1 / math.sqrt(M.D_QK)
+    worst = 0.0
+    for t in range(steps):
+        pn = (t + 1) % 2
+        pipe.step(t)
+        pipe.join()
+        torch.cuda.synchronize()
+        _, _, _, oss, osel = ost.score_select(inp.x[t + 1], inp.Wq, inp.Wuk, inp.Wdkv, cfg.n_q, append=cfg.append)
+        oout = ost.attention(inp.q_llm[t, :L], inp.Wuk_llm[:L], inp.Wuv_llm[:L], scale)
+        loads = ost.diff_and_gather(osel)
+        gsel, gslot = pipe.selected[pn].cpu().numpy(), pipe.slot_pos[pn].cpu().numpy()
+        gnl, gls, glp = pipe.n_load[pn].cpu().numpy(), pipe.load_slot[pn].cpu().numpy(), pipe.load_pos[pn].cpu().numpy()
+        gout = pipe.out.cpu().numpy()
+        assert pipe.len.cpu().numpy().tolist() == ost.lens
+        for b in range(cfg.B):
+            ok, sw, msg = selection_within_tie_band(gsel[b, 0], osel[b][0], oss[b][0], cfg.budget, cfg.n_sink,
+                                                    cfg.n_recent)
+            assert ok, f"t={t} b={b}: {msg}"
+            swaps += sw
+            if not diverged[b]:
+                e = float(np.abs(gout[:, b] - oout[:, b]).max())
+                worst = max(worst, e)
+                assert e <= ATTN_ATOL, f"t={t} b={b}: attention error {e:.3g}"
+            diverged[b] |= sw > 0
+            if not diverged[b]:
+                ls, lp = loads[b][0]
+                assert gnl[b, 0] == lp.size
+                assert np.array_equal(glp[b, 0, :lp.size], lp) and np.array_equal(gls[b, 0, :ls.size], ls)
+                assert np.array_equal(gslot[b, 0], ost.slot_pos[b, 0])
+            assert set(gslot[b, 0][gslot[b, 0] >= 0].tolist()) == set(gsel[b, 0][gsel[b, 0] >= 0].tolist())
+            if pipe.host_slots(b) is not None:
+                sl = pipe.host_slots(b).cpu().numpy().view(np.uint16)
+                h0 = pipe.gpu_layers[b]
+                idx = np.nonzero(gslot[b, 0] >= 0)[0]
+                assert np.array_equal(sl[:, idx], stores[b][h0:, gslot[b, 0][idx]])
+    return swaps, worst, pipe
+
+
+def test_mla_chain_small_host_layers():
+    from sparse_kv_cache_retrieval_gb300.configs import CONFIGS, scaled
+    cfg = scaled(CONFIGS["mla"], lens=(3000,), n_layers=3, steps=3, budget=512)
+    _, worst, _ = run_mla_chain(cfg, 3, 3, layers_per_launch=2)
+    assert worst <= 3e-3
+
+
+def test_mla_chain_ragged_batch_hbm_host_split_append():
+    cfg = dataclasses.replace(mla_workload(name="chain", B=2, lens=(510, 900), H=256, budget=512, steps=3,
+                                           append=True), n_layers=2, gpu_layers=(1, 0))
+    _, _, pipe = run_mla_chain(cfg, 3, 2, layers_per_launch=2)
+    assert pipe.len.cpu().tolist() == [513, 903]
+
+
+def test_mla_chain_full_shape():
+    """The benchmark workload's shapes (32K context, budget 2048, 16 heads) on
+    two of its 27 host layers, two steps."""
+    from sparse_kv_cache_retrieval_gb300.configs import CONFIGS, scaled
+    cfg = scaled(CONFIGS["mla"], n_layers=2, steps=2)
+    assert cfg.cap == 32768 and cfg.budget == 2048
+    run_mla_chain(cfg, 2, 2, layers_per_launch=2)
+
+
+def test_mla_graph_replay_equals_eager():
+    from sparse_kv_cache_retrieval_gb300.configs import CONFIGS, scaled
+    from sparse_kv_cache_retrieval_gb300.pipeline import DecodePipeline
+    cfg = scaled(CONFIGS["mla"], lens=(2000,), n_layers=2, steps=3, budget=256)
+    inp = make_mla_inputs(cfg, steps=3, n_layers=2)
+    a = DecodePipeline(cfg, inp, n_layers=2, layers_per_launch=1)
+    a.prologue()
+    a.run(0, 3)
+    torch.cuda.synchronize()
+    b = DecodePipeline(cfg, inp, n_layers=2, layers_per_launch=1)
+    b.prologue()
+    g = b.capture(0, 3)
+    g.replay()
+    torch.cuda.synchronize()
+    for u, v in ((a.out, b.out), (a.selected, b.selected), (a.slot_pos, b.slot_pos), (a.slots[0], b.slots[0])):
+        assert torch.equal(u.cpu(), v.cpu())
