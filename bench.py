@@ -176,6 +176,13 @@ def _sha256(rel: str) -> str:
         return ""
 
 
+def traffic_units(cfg) -> dict:
+    """Per timed kind: (NCU_TRAFFIC key, algorithmic bytes of one unit)."""
+    if cfg.mla:
+        return {"gather": ("mla_gather", 1152), "key_scan": ("mla_scan", 1152), "attention": ("mla_attention", 1152)}
+    return {"gather": ("gather", 256), "key_scan": ("key_scan", 256), "attention": ("attention", 512)}
+
+
 def ncu_traffic(kind: str, units: float):
     """Traffic of one launch of `kind` moving `units` units, or None when no
     capture matches the current source."""
@@ -278,11 +285,38 @@ def isolated_times(pipe, spc, torch, t_last: int, reps: int = 20) -> dict:
             fn()
         torch.cuda.synchronize()
         out[name] = max(0.0, (replay(graph(fn)) - t_flush) / reps)
-    # rows the timed gather moved: each request's loads times its host layers in the chunk
+    # bytes the timed gather moved: each request's loads times its host layers in the chunk
     nl_b = pipe.n_load[pn].sum(dim=1).cpu().tolist()
-    moved = sum(int(n) * max(0, l1 - max(l0, pipe.gpu_layers[b])) * 2 for b, n in enumerate(nl_b))
+    moved = sum(int(n) * max(0, l1 - max(l0, pipe.gpu_layers[b])) for b, n in enumerate(nl_b))
     del flush
-    return {"us": out, "gather_moved_rows": moved, "attn_layers": l1 - l0}
+    return {"us": out, "gather_moved_bytes": moved * load_bytes(pipe.cfg), "attn_layers": l1 - l0}
+
+
+def load_bytes(cfg) -> int:
+    """Bytes one load moves per layer: the K and V rows of one KV head (GQA)
+    or one latent row (MLA)."""
+    return cfg.row_elems * 2 // cfg.n_kv
+
+
+def scan_row_bytes(cfg) -> int:
+    """Bytes of the retrieval head's cache per position and KV head."""
+    return (cfg.row_elems if cfg.mla else cfg.d) * 2
+
+
+def attn_bytes_per_layer(cfg, rows_kept: int) -> int:
+    """What one layer's attention must move: the kept rows, the queries and
+    the fp32 outputs; MLA adds the layer's W_uk and W_uv (applied once per
+    head to the query and to the weighted latent sum)."""
+    if cfg.mla:
+        return rows_kept * cfg.row_elems * 2 + cfg.n_q * 2 * 128 * 512 * 2 + cfg.B * cfg.n_q * (192 * 2 + 128 * 4)
+    return rows_kept * 2 * cfg.d * 2 + cfg.B * cfg.n_q * cfg.d * (2 + 4)
+
+
+# kernels one timed call launches
+def kernels_per_call(cfg) -> dict:
+    if cfg.mla:
+        return {"project": 2, "key_scan": 1, "select": 1, "diff": 1, "attention": 3, "gather": 1}
+    return {"project": 1, "key_scan": 1, "select": 1, "diff": 1, "attention": 1, "gather": 1}
 
 
 def hbm_read_peak(spc, torch):
@@ -318,14 +352,30 @@ def oracle_sample(cfg_key: str, steps: int, layers: int, threads: int = 1) -> di
     n = str(max(1, threads))
     env = dict(os.environ, OMP_NUM_THREADS=n, OPENBLAS_NUM_THREADS=n, MKL_NUM_THREADS=n,
                CUDA_VISIBLE_DEVICES="")
-    code = f"""
+    from sparse_kv_cache_retrieval_gb300.configs import CONFIGS
+    if CONFIGS[cfg_key].mla:
+        code = _ORACLE_MLA.format(root=ROOT, key=cfg_key, steps=steps, layers=layers)
+    else:
+        code = _ORACLE_GQA.format(root=ROOT, key=cfg_key, steps=steps, layers=layers)
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=900)
+    if r.returncode != 0:
+        raise RuntimeError("oracle sample failed:\n" + r.stderr[-2000:])
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    res["sample"] = (f"{steps} decode steps of the full workload's retrieval head (all positions and "
+                     f"heads) + diff/gather/attention on {layers} of the layers, per-layer time scaled "
+                     f"to all layers; float64 numpy, {n} BLAS thread(s)")
+    res["threads"] = int(n)
+    return res
+
+
+_ORACLE_GQA = """
 import json, math, sys, time
-sys.path.insert(0, {ROOT!r})
+sys.path.insert(0, {root!r})
 import numpy as np
 import oracle.spc_oracle as O
 from sparse_kv_cache_retrieval_gb300.configs import CONFIGS
 from sparse_kv_cache_retrieval_gb300.synth import make_inputs, fill_llm_kv
-cfg = CONFIGS[{cfg_key!r}]
+cfg = CONFIGS[{key!r}]
 S, Ls = {steps}, {layers}
 inp = make_inputs(cfg, steps=S, n_layers=Ls)
 stores = []
@@ -349,15 +399,39 @@ for t in range(S):
 per_step_us = (t_head + t_layers * cfg.n_layers / Ls) / S * 1e6
 print(json.dumps({{"us_per_step": per_step_us, "head_s": t_head, "layers_s": t_layers}}))
 """
-    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=900)
-    if r.returncode != 0:
-        raise RuntimeError("oracle sample failed:\n" + r.stderr[-2000:])
-    res = json.loads(r.stdout.strip().splitlines()[-1])
-    res["sample"] = (f"{steps} decode steps of the full workload's retrieval head (all positions and "
-                     f"heads) + diff/gather/attention on {layers} of the layers, per-layer time scaled "
-                     f"to all layers; float64 numpy, {n} BLAS thread(s)")
-    res["threads"] = int(n)
-    return res
+
+_ORACLE_MLA = """
+import json, math, sys, time
+sys.path.insert(0, {root!r})
+import numpy as np
+import oracle.mla_oracle as M
+from sparse_kv_cache_retrieval_gb300.configs import CONFIGS
+from sparse_kv_cache_retrieval_gb300.synth import make_mla_inputs, fill_mla_layer
+cfg = CONFIGS[{key!r}]
+S, Ls = {steps}, {layers}
+inp = make_mla_inputs(cfg, steps=S, n_layers=Ls)
+stores = []
+for b in range(cfg.B):
+    st = np.empty((Ls, cfg.cap, M.D_LAT), np.uint16)
+    for l in range(Ls):
+        fill_mla_layer(cfg, b, l, st[l])
+    stores.append(st)
+ost = M.MlaDecodeState(inp.C_dlm, inp.lens, stores, [min(g, Ls) for g in cfg.gpu_layers], cfg.budget,
+                       cfg.n_sink, cfg.n_recent)
+ost.diff_and_gather(ost.score_select(inp.x[0], inp.Wq, inp.Wuk, inp.Wdkv, cfg.n_q, False)[4])
+t_head = t_layers = 0.0
+for t in range(S):
+    t0 = time.perf_counter()
+    sel = ost.score_select(inp.x[t + 1], inp.Wq, inp.Wuk, inp.Wdkv, cfg.n_q, cfg.append)[4]
+    t1 = time.perf_counter()
+    ost.attention(inp.q_llm[t, :Ls], inp.Wuk_llm[:Ls], inp.Wuv_llm[:Ls], 1 / math.sqrt(M.D_QK))
+    ost.diff_and_gather(sel)
+    t2 = time.perf_counter()
+    t_head += t1 - t0
+    t_layers += t2 - t1
+per_step_us = (t_head + t_layers * cfg.n_layers / Ls) / S * 1e6
+print(json.dumps({{"us_per_step": per_step_us, "head_s": t_head, "layers_s": t_layers}}))
+"""
 
 
 def reference_arm(args, rank, world):
@@ -393,14 +467,14 @@ def our_arm(args, rank, world, local):
     from sparse_kv_cache_retrieval_gb300 import binding as spc
     from sparse_kv_cache_retrieval_gb300.configs import CONFIGS, describe
     from sparse_kv_cache_retrieval_gb300.pipeline import DecodePipeline
-    from sparse_kv_cache_retrieval_gb300.synth import make_inputs
+    from sparse_kv_cache_retrieval_gb300.synth import make_inputs, make_mla_inputs
 
     torch.cuda.set_device(local)
     cfg = CONFIGS[args.config]
     W, K = max(3, args.warmup), args.steps
     log("generating inputs")
     n_layers = cfg.n_layers if args.layers is None else max(1, min(args.layers, cfg.n_layers))
-    inp = make_inputs(cfg, steps=W + K + 1, n_layers=n_layers)
+    inp = (make_mla_inputs if cfg.mla else make_inputs)(cfg, steps=W + K + 1, n_layers=n_layers)
     log("allocating and filling the pinned host store")
     pipe = DecodePipeline(cfg, inp, n_layers=n_layers, layers_per_launch=args.layers_per_launch, timing=False,
                           gather_streams=args.gather_streams, elastic=not args.no_elastic)
@@ -419,7 +493,9 @@ def our_arm(args, rank, world, local):
             rows.append(int(pipe.n_load[(t + 1) % 2].cpu().numpy().astype(np.int64).sum()))
         torch.cuda.synchronize()
         print(json.dumps({"profile_steps": K, "workload": cfg.name,
-                          "launches_per_step": 4 + 2 * len(pipe.chunks),
+                          "launches_per_step": sum(kernels_per_call(cfg)[k] for k in ("project", "key_scan", "select",
+                                                                                       "diff")) +
+                          len(pipe.chunks) * (kernels_per_call(cfg)["attention"] + 1),
                           "chunks": pipe.chunks, "gathered_rows_per_kv_per_layer": rows,
                           "scan_positions": [int(v) for v in pipe.len.cpu().numpy()]}))
         return
@@ -500,20 +576,22 @@ def our_arm(args, rank, world, local):
         r["mean_us"] = r["total_ms"] * 1e3 / max(1, r["launches"])
     timing_src = ("CUDA event pair around every launch on its stream, in a second replay of the "
                   "same steps from the same state")
-    launches_per_step = sum(r["launches"] for r in kern.values()) // max(1, K)
+    kpc = kernels_per_call(cfg)
+    launches_per_step = sum(r["launches"] * kpc.get(k, 1) for k, r in kern.items()) // max(1, K)
 
 
     # algorithmic bytes
     nl = np.stack(nl_steps)                                        # [n_eager][B][n_kv]
     host_layers = np.array([pipe.L - pipe.gpu_layers[b] for b in range(cfg.B)])
-    gathered = int((nl.sum(axis=2) * host_layers[None, :]).sum() * 2 * 256)
-    full_reload = int(n_eager * cfg.B * cfg.n_kv * cfg.budget * host_layers.mean() * 2 * 256)
+    lb = load_bytes(cfg)
+    gathered = int((nl.sum(axis=2) * host_layers[None, :]).sum() * lb)
+    full_reload = int(n_eager * cfg.B * cfg.n_kv * cfg.budget * host_layers.mean() * lb)
     overlap = (1.0 - nl.sum() / (n_eager * cfg.B * cfg.n_kv * min(cfg.budget, min(cfg.lens)))) if pipe.elastic else None
     lens_now = pipe.len.cpu().numpy()
-    scan_bytes = int(sum(int(L) for L in lens_now) * cfg.n_kv * 256)   # fixed-length workloads
+    scan_bytes = int(sum(int(L) for L in lens_now) * cfg.n_kv * scan_row_bytes(cfg))   # fixed-length workloads
     n_gather_launches = kern.get("gather", {}).get("launches", 1)
     rows_kept = cfg.B * cfg.n_kv * min(cfg.budget, int(min(lens_now)))
-    attn_bytes_per_layer = rows_kept * 512 + cfg.B * cfg.n_q * 128 * (2 + 4)
+    attn_layer_bytes = attn_bytes_per_layer(cfg, rows_kept)
     peaks = measured_peaks()
     hbm_peak = peaks.get("hbm_gbs")
     log("measuring link and HBM read peaks")
@@ -539,7 +617,7 @@ def our_arm(args, rank, world, local):
                            "unit": "GB/s", "frac": round(a / zc_peak, 3) if zc_peak else None,
                            "algorithmic_bytes": int(per_launch), "mean_us": round(kern["gather"]["mean_us"], 2)}
     if "attention" in kern:
-        per_launch = attn_bytes_per_layer * (pipe.chunks[0][1] - pipe.chunks[0][0])
+        per_launch = attn_layer_bytes * (pipe.chunks[0][1] - pipe.chunks[0][0])
         a = gbs(per_launch, kern["attention"]["mean_us"])
         kinfo["attention"] = {"bound": "hbm", "achieved": round(a, 1), "peak": hbm_peak, "unit": "GB/s",
                               "frac": round(a / hbm_peak, 3) if hbm_peak else None,
@@ -547,15 +625,16 @@ def our_arm(args, rank, world, local):
     for k in ("project", "select", "diff"):
         if k in kern:
             kinfo[k] = {"mean_us": round(kern[k]["mean_us"], 2), "launches": kern[k]["launches"]}
-    for k, ub in (("gather", 256), ("key_scan", 256), ("attention", 512)):
+    units = traffic_units(cfg)
+    for k, (tk, ub) in units.items():
         if k in kinfo:
-            kinfo[k]["traffic"] = ncu_traffic(k, kinfo[k]["algorithmic_bytes"] / ub)
+            kinfo[k]["traffic"] = ncu_traffic(tk, kinfo[k]["algorithmic_bytes"] / ub)
     # every kernel alone (L2 flushed before each launch), same launch shapes
     log("isolated kernel timing")
     iso = isolated_times(pipe, spc, torch, t_last=W + K - 1)
     iso_bytes = {"key_scan": (scan_bytes, hbm_peak),
-                 "attention": (attn_bytes_per_layer * iso["attn_layers"], hbm_peak),
-                 "gather": (iso["gather_moved_rows"] * 256, zc_peak)}
+                 "attention": (attn_layer_bytes * iso["attn_layers"], hbm_peak),
+                 "gather": (iso["gather_moved_bytes"], zc_peak)}
     for k, us in iso["us"].items():
         r = kinfo.setdefault(k, {})
         r["isolated_us"] = round(us, 2)
@@ -570,8 +649,8 @@ def our_arm(args, rank, world, local):
     roof = None
     if dominant in ("gather", "key_scan", "attention"):
         r = kinfo[dominant]
-        unit_bytes = {"gather": 256, "key_scan": 256, "attention": 512}[dominant]
-        traffic = ncu_traffic(dominant, r["algorithmic_bytes"] / unit_bytes)
+        tk, unit_bytes = units[dominant]
+        traffic = ncu_traffic(tk, r["algorithmic_bytes"] / unit_bytes)
         roof = {"kernel": dominant, "bound": r["bound"], "achieved": r["achieved"], "peak": r["peak"],
                 "unit": "GB/s", "frac": r["frac"], "traffic": traffic,
                 "peak_source": "measured in this run (zero-copy read of pinned host memory)"
@@ -628,9 +707,10 @@ def our_arm(args, rank, world, local):
     if args.no_elastic:
         config["elastic"] = "off: every step reloads its whole selection"
     config.update({"layers_per_launch": args.layers_per_launch, "gather_streams": args.gather_streams,
-                   "l2": (f"inputs larger than L2: each step reads the {scan_bytes / 2**20:.0f} MiB key cache "
-                          f"and {attn_bytes_per_layer * n_layers / 2**20:.0f} MiB of K/V rows and writes the "
-                          f"gathered rows (> 129 MB L2)"),
+                   "l2": (f"inputs larger than L2: each step reads the {scan_bytes / 2**20:.0f} MiB "
+                          f"{'latent' if cfg.mla else 'key'} cache and {attn_layer_bytes * n_layers / 2**20:.0f} "
+                          f"MiB of {'latent rows and up-projection weights' if cfg.mla else 'K/V rows'} and "
+                          f"writes the gathered rows (> 129 MB L2)"),
                    "graph": "CUDA graph per step range, two streams", "kernel_timing": timing_src})
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
