@@ -24,9 +24,10 @@
 //    (128 x 512 bf16, 128 KiB) once and absorbs every query that uses it;
 //  * mla_attn_kernel: per (layer, request) the kept rows are split into runs
 //    of 32-row tiles, one CTA per run (two CTAs per SM). A producer warp copies
-//    each tile's rows with 16-byte cp.async into a 2-stage ring (rows XOR-
-//    swizzled by 16-byte piece, not-kept rows zero-filled, a 32-bit valid mask
-//    published with the stage). Four consumer warps split S = Q C^T over the
+//    each tile's rows into a 2-stage ring with one bulk copy (cp.async.bulk)
+//    per row, completion counted in bytes on the stage's mbarrier; rows sit
+//    1168 bytes apart (16 bytes of padding) so ldmatrix is conflict-free, and
+//    a 32-bit valid mask is published with the stage. Four consumer warps split S = Q C^T over the
 //    576 dims (9 k-steps of mma.sync m16n8k16 each; the 16 heads are the M
 //    side, the absorbed query rounded to bf16), sum the four partial S tiles
 //    through shared memory, run the online softmax in base 2, and compute
@@ -59,8 +60,9 @@ constexpr int kMH = SPC_MLA_HEADS;                    // 16
 constexpr long long kMlaWait = 4000000000ll;          // bounded mbarrier waits (clock cycles, ~2 s)
 
 // ============================================================== absorption
-constexpr int kAbsThreads = 256;   // two latent coordinates per thread
-constexpr int kAbsItems = 16;      // queries absorbed together
+constexpr int kAbsThreads = 256;   // 16 row groups x 16 lanes of 8 latent coordinates
+constexpr int kAbsRg = 16;
+constexpr int kAbsChunk = 128;     // latent coordinates per CTA (4 CTAs per head)
 
 template <typename QT>
 __device__ __forceinline__ float load_q(const QT* p);
@@ -70,69 +72,92 @@ template <>
 __device__ __forceinline__ float load_q<uint16_t>(const uint16_t* p) { return __uint_as_float(uint32_t(*p) << 16); }
 
 // qa[i, h] = [W_uk[w(i), h]^T q[i, h, :128] ; q[i, h, 128:192]] for items i
-// of weight matrix w(i) = i / items_per_w; grid (heads, weight matrices,
-// item chunks of 16).
-template <typename QT>
+// of weight matrix w(i) = i / items_per_w. Grid (heads, weight matrices,
+// 4 coordinate chunks x item chunks of NI): a CTA reads a 128-coordinate
+// column block of W_uk[w, h] (32 KiB, 16-byte loads, 8 rows in flight per
+// thread), each of 16 row groups sums 8 of the 128 nope rows, and the row
+// groups are added through shared memory.
+template <typename QT, int NI>
 __global__ void __launch_bounds__(kAbsThreads)
 mla_absorb_kernel(const QT* __restrict__ q, const uint16_t* __restrict__ Wuk, int n_items, int items_per_w,
                   float* __restrict__ qa) {
-  __shared__ float qs[kNope][kAbsItems];
-  const int h = blockIdx.x, w = blockIdx.y, tid = threadIdx.x;
-  const int i0 = w * items_per_w + blockIdx.z * kAbsItems;
-  const int i1 = min(min(n_items, (w + 1) * items_per_w), i0 + kAbsItems);
+  __shared__ float qs[kNope][NI];
+  __shared__ __align__(16) float red[kAbsRg * NI * kAbsChunk];
+  const int h = blockIdx.x, w = blockIdx.y, chunk = blockIdx.z & 3, zi = blockIdx.z >> 2, tid = threadIdx.x;
+  const int i0 = w * items_per_w + zi * NI;
+  const int i1 = min(min(n_items, (w + 1) * items_per_w), i0 + NI);
   const int ni = i1 - i0;
   if (ni <= 0) return;
-  for (int idx = tid; idx < kNope * kAbsItems; idx += kAbsThreads) {
-    const int j = idx / kAbsItems, it = idx - j * kAbsItems;
+  for (int idx = tid; idx < kNope * NI; idx += kAbsThreads) {
+    const int j = idx / NI, it = idx - j * NI;
     qs[j][it] = it < ni ? load_q<QT>(q + ((size_t)(i0 + it) * kMH + h) * kQk + j) : 0.f;
   }
-  for (int idx = tid; idx < ni * SPC_MLA_ROPE; idx += kAbsThreads) {
-    const int it = idx / SPC_MLA_ROPE, k = idx - it * SPC_MLA_ROPE;
-    qa[((size_t)(i0 + it) * kMH + h) * kLat + kDc + k] =
-        load_q<QT>(q + ((size_t)(i0 + it) * kMH + h) * kQk + kNope + k);
+  if (chunk == 0) {
+    for (int idx = tid; idx < ni * SPC_MLA_ROPE; idx += kAbsThreads) {
+      const int it = idx / SPC_MLA_ROPE, k = idx - it * SPC_MLA_ROPE;
+      qa[((size_t)(i0 + it) * kMH + h) * kLat + kDc + k] =
+          load_q<QT>(q + ((size_t)(i0 + it) * kMH + h) * kQk + kNope + k);
+    }
   }
   __syncthreads();
-  // W_uk[w, h] is [128][512]: row j holds the weights of nope value j; this
-  // thread owns latent coordinates 2 tid and 2 tid + 1 (one bf16 pair per row)
-  const uint32_t* W = reinterpret_cast<const uint32_t*>(Wuk + ((size_t)w * kMH + h) * kNope * kDc) + tid;
-  float a0[kAbsItems], a1[kAbsItems];
+  const int rg = tid >> 4, cl = tid & 15;
+  // W_uk[w, h] is [128][512]: row j holds the weights of nope value j
+  const uint16_t* W = Wuk + ((size_t)w * kMH + h) * kNope * kDc + chunk * kAbsChunk + cl * 8;
+  uint4 wv[kNope / kAbsRg];
 #pragma unroll
-  for (int it = 0; it < kAbsItems; ++it) a0[it] = a1[it] = 0.f;
-#pragma unroll 2
-  for (int j = 0; j < kNope; j += 8) {
-    uint32_t wv[8];
+  for (int k = 0; k < kNope / kAbsRg; ++k) wv[k] = ldg_stream(W + (size_t)(rg + kAbsRg * k) * kDc);
+  float acc[NI][8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) wv[u] = __ldg(W + (size_t)(j + u) * (kDc / 2));
+  for (int it = 0; it < NI; ++it)
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const float w0 = bf_lo(wv[u]), w1 = bf_hi(wv[u]);
+    for (int e = 0; e < 8; ++e) acc[it][e] = 0.f;
 #pragma unroll
-      for (int it = 0; it < kAbsItems; ++it) {
-        a0[it] = fmaf(w0, qs[j + u][it], a0[it]);
-        a1[it] = fmaf(w1, qs[j + u][it], a1[it]);
-      }
+  for (int k = 0; k < kNope / kAbsRg; ++k) {
+    float f[8];
+    unpack8(wv[k], f);
+    const int j = rg + kAbsRg * k;
+#pragma unroll
+    for (int it = 0; it < NI; ++it) {
+      const float qv = qs[j][it];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[it][e] = fmaf(f[e], qv, acc[it][e]);
     }
   }
 #pragma unroll
-  for (int it = 0; it < kAbsItems; ++it)
-    if (it < ni)
-      *reinterpret_cast<float2*>(qa + ((size_t)(i0 + it) * kMH + h) * kLat + 2 * tid) = make_float2(a0[it], a1[it]);
+  for (int it = 0; it < NI; ++it) {
+    float4* dst = reinterpret_cast<float4*>(red + ((size_t)(rg * NI + it) * kAbsChunk + cl * 8));
+    dst[0] = make_float4(acc[it][0], acc[it][1], acc[it][2], acc[it][3]);
+    dst[1] = make_float4(acc[it][4], acc[it][5], acc[it][6], acc[it][7]);
+  }
+  __syncthreads();
+  for (int o = tid; o < ni * kAbsChunk; o += kAbsThreads) {
+    const int it = o / kAbsChunk, c = o - it * kAbsChunk;
+    float sum = 0.f;
+#pragma unroll
+    for (int g = 0; g < kAbsRg; ++g) sum += red[(g * NI + it) * kAbsChunk + c];
+    qa[((size_t)(i0 + it) * kMH + h) * kLat + chunk * kAbsChunk + c] = sum;
+  }
+}
+
+template <typename QT>
+static void absorb_launch_t(const QT* q, const uint16_t* Wuk, int n_items, int items_per_w, float* qa,
+                            cudaStream_t st) {
+  const int n_w = (n_items + items_per_w - 1) / items_per_w;
+  const int ni = items_per_w <= 1 ? 1 : items_per_w <= 2 ? 2 : 4;
+  const dim3 grid(kMH, n_w, 4 * ((items_per_w + ni - 1) / ni));
+  if (ni == 1) mla_absorb_kernel<QT, 1><<<grid, kAbsThreads, 0, st>>>(q, Wuk, n_items, items_per_w, qa);
+  else if (ni == 2) mla_absorb_kernel<QT, 2><<<grid, kAbsThreads, 0, st>>>(q, Wuk, n_items, items_per_w, qa);
+  else mla_absorb_kernel<QT, 4><<<grid, kAbsThreads, 0, st>>>(q, Wuk, n_items, items_per_w, qa);
 }
 
 int mla_absorb_launch(const void* q, int q_bf16, const void* Wuk, int n_items, int items_per_w, float* qa,
                       void* stream) {
   if (n_items <= 0) return SPC_OK;
-  const int n_w = (n_items + items_per_w - 1) / items_per_w;
-  const dim3 grid(kMH, n_w, (items_per_w + kAbsItems - 1) / kAbsItems);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (q_bf16)
-    mla_absorb_kernel<uint16_t><<<grid, kAbsThreads, 0, st>>>(static_cast<const uint16_t*>(q),
-                                                              static_cast<const uint16_t*>(Wuk), n_items,
-                                                              items_per_w, qa);
+    absorb_launch_t(static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(Wuk), n_items, items_per_w, qa, st);
   else
-    mla_absorb_kernel<float><<<grid, kAbsThreads, 0, st>>>(static_cast<const float*>(q),
-                                                           static_cast<const uint16_t*>(Wuk), n_items,
-                                                           items_per_w, qa);
+    absorb_launch_t(static_cast<const float*>(q), static_cast<const uint16_t*>(Wuk), n_items, items_per_w, qa, st);
   return cudaGetLastError() == cudaSuccess ? SPC_OK : SPC_ERR_CUDA;
 }
 
@@ -142,7 +167,9 @@ constexpr int kMaStages = 2;
 constexpr int kMaCWarps = 4;
 constexpr int kMaCThreads = kMaCWarps * 32;
 constexpr int kMaThreads = kMaCThreads + 32;         // + producer warp
-constexpr uint32_t kMaTile = kMaRows * kLatBytes;    // 36 KiB
+constexpr int kMaPitch = kLatBytes + 16;             // 1168: rows 16 bytes apart in bank groups, so
+                                                     // ldmatrix over 8 rows is conflict-free
+constexpr uint32_t kMaTile = kMaRows * kMaPitch;     // 36.5 KiB
 constexpr int kMaKs = kLat / 16 / kMaCWarps;         // 9 k-steps of S per warp
 constexpr int kMaPStride = 40;                       // bf16 per P row (32 + 8: conflict-free ldmatrix)
 constexpr int kMaTargetCtas = 304;                   // two CTAs per SM of a 152-SM GB300
@@ -191,7 +218,7 @@ __global__ void __launch_bounds__(kMaThreads, 2) mla_attn_kernel(MlaAttnArgs a) 
 
   if (tid == 0) {
     for (int s = 0; s < kMaStages; ++s) {
-      mbar_init(&full[s], 32 + 1);   // 32 cp.async arrivals + the mask publisher
+      mbar_init(&full[s], 1);        // lane 0: mask published, 32 row copies expected
       mbar_init(&empty[s], kMaCWarps);
     }
     fence_mbar_init();
@@ -220,22 +247,16 @@ __global__ void __launch_bounds__(kMaThreads, 2) mla_attn_kernel(MlaAttnArgs a) 
         if (lane == 0) set_status(a.status, SPC_ERR_TIMEOUT);
         break;
       }
-      uint8_t* dst = msm + (size_t)s * kMaTile;
-      // 32 rows x 72 pieces: lane takes pieces lane, lane + 32, ... of the tile
-#pragma unroll 8
-      for (int k = 0; k < kMaRows * kLatPieces / 32; ++k) {
-        const int idx = lane + 32 * k;
-        const int rr = idx / kLatPieces, piece = idx - rr * kLatPieces;
-        const int row = __shfl_sync(0xffffffffu, r, rr);
-        const bool v = (ok >> rr) & 1u;
-        cp_async16(dst + rr * kLatBytes + ((piece ^ (rr & 7)) << 4),
-                   base + (size_t)(v ? row : 0) * kLat + piece * 8, v ? 16 : 0);
-      }
+      // one bulk copy per row, lane r copying row r of the tile; a row not
+      // kept copies the view's row 0 instead (finite values: its logits are
+      // masked, so its weight is exactly 0)
       if (lane == 0) {
         vmask[s] = ok;
-        mbar_arrive(&full[s]);
+        mbar_arrive_expect_tx(&full[s], kMaRows * kLatBytes);
       }
-      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(smem_u32(&full[s])) : "memory");
+      __syncwarp();
+      bulk_g2s(msm + (size_t)s * kMaTile + lane * kMaPitch, base + (size_t)(r < 0 ? 0 : r) * kLat, kLatBytes,
+               &full[s]);
     }
     for (int k = max(0, it - kMaStages); k < it; ++k)
       mbar_wait_bounded(&full[k % kMaStages], (k / kMaStages) & 1, kMlaWait);
@@ -293,7 +314,7 @@ __global__ void __launch_bounds__(kMaThreads, 2) mla_attn_kernel(MlaAttnArgs a) 
       for (int np = 0; np < 2; ++np) {
         const int row = np * 16 + ((lm >> 1) << 3) + lr;
         uint32_t b0, b1, b2, b3;
-        ldsm_x4(tb + row * kLatBytes + (((kg * 2 + (lm & 1)) ^ (row & 7)) << 4), b0, b1, b2, b3);
+        ldsm_x4(tb + row * kMaPitch + ((kg * 2 + (lm & 1)) << 4), b0, b1, b2, b3);
         mma_bf16(acc[2 * np], qh[ks], b0, b1);
         mma_bf16(acc[2 * np + 1], qh[ks], b2, b3);
       }
@@ -376,7 +397,7 @@ __global__ void __launch_bounds__(kMaThreads, 2) mla_attn_kernel(MlaAttnArgs a) 
       for (int np = 0; np < 8; ++np) {
         const int piece = kw * 16 + np * 2 + (lm >> 1);
         uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(tb + row * kLatBytes + ((piece ^ (row & 7)) << 4), b0, b1, b2, b3);
+        ldsm_x4_t(tb + row * kMaPitch + (piece << 4), b0, b1, b2, b3);
         mma_bf16(o[2 * np], ah, b0, b1);
         mma_bf16(o[2 * np], alw, b0, b1);
         mma_bf16(o[2 * np + 1], ah, b2, b3);
@@ -411,18 +432,23 @@ __global__ void __launch_bounds__(kMaThreads, 2) mla_attn_kernel(MlaAttnArgs a) 
 }
 
 // ============================================================== merge + W_uv
-constexpr int kMoThreads = 128;
+constexpr int kMoThreads = 256;
+constexpr int kMoChunk = 32;       // output values per CTA (4 CTAs per head)
 
+// Grid (units, heads, 4 chunks of 32 output values): merge the head's split
+// partials in split order (every CTA of the head the same way), then 8 warps
+// x 4 values each dot W_uv[l, h][v, :] with the merged latent sum, two
+// 16-byte loads per value and lane, all 8 in flight.
 __global__ void __launch_bounds__(kMoThreads)
 mla_out_kernel(const float* __restrict__ part, const uint16_t* __restrict__ Wuv, int B, int n_split,
                float* __restrict__ out) {
   __shared__ __align__(16) float lat[kDc];
   __shared__ float wgt[64];
-  const int unit = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  const int unit = blockIdx.x, h = blockIdx.y, v0 = blockIdx.z * kMoChunk, tid = threadIdx.x;
   const int l = unit / B;
   const float* pp = part + (size_t)unit * n_split * kMH * kMaPart + (size_t)h * kMaPart;
   const size_t sstride = (size_t)kMH * kMaPart;
-  // split weights exp2(m_s - M) / sum_s exp2(m_s - M) l_s, in split order
+  // split weights exp2(m_s - M) / sum_s exp2(m_s - M) l_s
   if (tid == 0) {
     float M = -INFINITY;
     for (int s = 0; s < n_split; ++s) M = fmaxf(M, pp[s * sstride]);
@@ -436,7 +462,7 @@ mla_out_kernel(const float* __restrict__ part, const uint16_t* __restrict__ Wuv,
     for (int s = 0; s < n_split; ++s) wgt[s] *= inv;
   }
   __syncthreads();
-  {
+  if (tid < kDc / 4) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s = 0; s < n_split; ++s) {
       const float w = wgt[s];
@@ -447,31 +473,31 @@ mla_out_kernel(const float* __restrict__ part, const uint16_t* __restrict__ Wuv,
     *reinterpret_cast<float4*>(lat + 4 * tid) = acc;
   }
   __syncthreads();
-  // out[v] = W_uv[l, h][v, :] . lat, one warp per 32 output values, 4 in flight
   const int warp = tid >> 5, lane = tid & 31;
   const uint16_t* W = Wuv + ((size_t)l * kMH + h) * kDv * kDc;
+  const int vb = v0 + warp * 4;
+  uint4 w0[4], w1[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    w0[u] = ldg_stream(W + (size_t)(vb + u) * kDc + lane * 8);
+    w1[u] = ldg_stream(W + (size_t)(vb + u) * kDc + 256 + lane * 8);
+  }
   float lv[16];
 #pragma unroll
   for (int e = 0; e < 8; ++e) { lv[e] = lat[lane * 8 + e]; lv[8 + e] = lat[256 + lane * 8 + e]; }
-  float* o = out + ((size_t)unit * kMH + h) * kDv;
-  for (int v0 = warp * 32; v0 < warp * 32 + 32; v0 += 4) {
-    float sum[4];
+  float sum[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const uint4 w0 = ldg_stream(W + (size_t)(v0 + u) * kDc + lane * 8);
-      const uint4 w1 = ldg_stream(W + (size_t)(v0 + u) * kDc + 256 + lane * 8);
-      float f0[8], f1[8];
-      unpack8(w0, f0);
-      unpack8(w1, f1);
-      float s = 0.f;
+  for (int u = 0; u < 4; ++u) {
+    float f0[8], f1[8];
+    unpack8(w0[u], f0);
+    unpack8(w1[u], f1);
+    float sacc = 0.f;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) s = fmaf(f0[e], lv[e], fmaf(f1[e], lv[8 + e], s));
-      sum[u] = s;
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) sum[u] = warp_sum(sum[u]);
-    if (lane < 4) o[v0 + lane] = sum[lane];
+    for (int e = 0; e < 8; ++e) sacc = fmaf(f0[e], lv[e], fmaf(f1[e], lv[8 + e], sacc));
+    sum[u] = warp_sum(sacc);
   }
+  const float r = lane == 0 ? sum[0] : lane == 1 ? sum[1] : lane == 2 ? sum[2] : sum[3];
+  if (lane < 4) out[((size_t)unit * kMH + h) * kDv + vb + lane] = r;
 }
 
 static void mla_attn_plan(int units, int budget, int* n_split, int* tpc) {
@@ -520,8 +546,8 @@ int mla_attn_launch(const void* q, const void* Wuk, const void* Wuv, const spc_k
   }
   mla_attn_kernel<<<units * aa.n_split, kMaThreads, MaSmem::total, st>>>(aa);
   if (cudaGetLastError() != cudaSuccess) return SPC_ERR_CUDA;
-  mla_out_kernel<<<dim3(units, kMH), kMoThreads, 0, st>>>(part, static_cast<const uint16_t*>(Wuv), B,
-                                                         aa.n_split, out);
+  mla_out_kernel<<<dim3(units, kMH, kDv / kMoChunk), kMoThreads, 0, st>>>(part, static_cast<const uint16_t*>(Wuv), B,
+                                                                         aa.n_split, out);
   return cudaGetLastError() == cudaSuccess ? SPC_OK : SPC_ERR_CUDA;
 }
 

@@ -1455,8 +1455,9 @@ int score_select_launch(const ScoreSelectCall& c) {
 // Latent scan: logits l[b, p, h] = qa[b, h] . C[b, p] * log2(e) / sqrt(192)
 // for the absorbed queries qa (576 values: W_uk[h]^T q_nope ; q_rope) over
 // the 576-value latent rows. One CTA per SM: a producer warp streams 32-row
-// tiles (36 KiB) into a 4-stage ring with 16-byte cp.async (pieces XOR-
-// swizzled by row) for four consumer warps (a second group of four would
+// tiles into a 4-stage ring, one bulk copy (cp.async.bulk) per row at a
+// 1168-byte pitch (16 bytes of padding keep ldmatrix conflict-free), for
+// four consumer warps (a second group of four would
 // leave each warp 168 registers, and the query fragments alone take 72).
 // The four warps split the 576 dims (9 k-steps of mma.sync
 // m16n8k16 each, the 16 heads on the M side, the query in bf16 high and low
@@ -1465,7 +1466,6 @@ int score_select_launch(const ScoreSelectCall& c) {
 // logsumexp partial per head per 8 rows (16 per 128 positions).
 constexpr int kMsLat = SPC_MLA_LATENT + SPC_MLA_ROPE;   // 576
 constexpr int kMsLatBytes = kMsLat * 2;
-constexpr int kMsPieces = kMsLatBytes / 16;             // 72
 constexpr int kMsH = SPC_MLA_HEADS;                     // 16
 constexpr int kMsQk = SPC_MLA_NOPE + SPC_MLA_ROPE;      // 192
 constexpr int kMsRows = 32;
@@ -1474,7 +1474,8 @@ constexpr int kMsGroups = 1;   // nine warps would cap registers at 168 (16K per
 constexpr int kMsKw = 4;
 constexpr int kMsThreads = (kMsGroups * kMsKw + 1) * 32;
 constexpr int kMsKs = kMsLat / 16 / kMsKw;              // 9
-constexpr uint32_t kMsTile = kMsRows * kMsLatBytes;     // 36 KiB
+constexpr int kMsPitch = kMsLatBytes + 16;              // 1168: conflict-free ldmatrix over 8 rows
+constexpr uint32_t kMsTile = kMsRows * kMsPitch;        // 36.5 KiB
 constexpr int kMsPpt = (kScanRows / kMsRows) * kMsKw;   // 16 partials per 128 positions
 constexpr size_t kMsRed = (size_t)kMsGroups * kMsKw * 4 * 32 * 16;
 constexpr size_t kMsSmem = kMsStages * (size_t)kMsTile + kMsRed + 2 * kMsStages * sizeof(uint64_t);
@@ -1502,7 +1503,7 @@ __global__ void __launch_bounds__(kMsThreads, 1) mla_scan_kernel(MlaScanArgs a) 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kMsStages; ++s) {
-      mbar_init(&full[s], 32);
+      mbar_init(&full[s], 1);        // lane 0, 32 row copies expected
       mbar_init(&empty[s], kMsKw);   // the group that owns the stage
     }
     fence_mbar_init();
@@ -1525,17 +1526,12 @@ __global__ void __launch_bounds__(kMsThreads, 1) mla_scan_kernel(MlaScanArgs a) 
         if (lane == 0) set_status(a.status, SPC_ERR_TIMEOUT);
         break;
       }
-      uint8_t* dst = mss + (size_t)s * kMsTile;
-      const uint16_t* src = a.C + ((size_t)b * a.cap + row0) * kMsLat;
-#pragma unroll 8
-      for (int k = 0; k < kMsRows * kMsPieces / 32; ++k) {
-        const int idx = lane + 32 * k;
-        const int r = idx / kMsPieces, piece = idx - r * kMsPieces;
-        const bool ok = r < nrows;
-        cp_async16(dst + r * kMsLatBytes + ((piece ^ (r & 7)) << 4), src + (size_t)(ok ? r : 0) * kMsLat + piece * 8,
-                   ok ? 16 : 0);
-      }
-      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(smem_u32(&full[s])) : "memory");
+      // one bulk copy per row (lane r: row r); rows past the end copy the
+      // tile's first row again (their logits are never written or summed)
+      if (lane == 0) mbar_arrive_expect_tx(&full[s], kMsRows * kMsLatBytes);
+      __syncwarp();
+      bulk_g2s(mss + (size_t)s * kMsTile + lane * kMsPitch,
+               a.C + ((size_t)b * a.cap + row0 + (lane < nrows ? lane : 0)) * kMsLat, kMsLatBytes, &full[s]);
       ++it;
     }
     for (int k = max(0, it - kMsStages); k < it; ++k)
@@ -1602,7 +1598,7 @@ __global__ void __launch_bounds__(kMsThreads, 1) mla_scan_kernel(MlaScanArgs a) 
       for (int np = 0; np < 2; ++np) {
         const int row = np * 16 + ((lm >> 1) << 3) + lr;
         uint32_t b0, b1, b2, b3;
-        ldsm_x4(tb + row * kMsLatBytes + (((kg * 2 + (lm & 1)) ^ (row & 7)) << 4), b0, b1, b2, b3);
+        ldsm_x4(tb + row * kMsPitch + ((kg * 2 + (lm & 1)) << 4), b0, b1, b2, b3);
         mma_bf16(acc[2 * np], qh[ks], b0, b1);
         mma_bf16(acl[2 * np], ql[ks], b0, b1);
         mma_bf16(acc[2 * np + 1], qh[ks], b2, b3);
