@@ -46,7 +46,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="cfg2")
-    ap.add_argument("--layers-per-launch", type=int, default=16)
+    ap.add_argument("--layers-per-launch", type=int, default=None,
+                    help="attention/gather layer chunk (default: the workload's, 16 for GQA, all layers for MLA)")
     ap.add_argument("--layers", type=int, default=None,
                     help="LLM layers to run (default: the workload's); the JSON line states it")
     ap.add_argument("--gather-streams", type=int, default=1, choices=[1, 2])
@@ -476,6 +477,8 @@ def our_arm(args, rank, world, local):
     n_layers = cfg.n_layers if args.layers is None else max(1, min(args.layers, cfg.n_layers))
     inp = (make_mla_inputs if cfg.mla else make_inputs)(cfg, steps=W + K + 1, n_layers=n_layers)
     log("allocating and filling the pinned host store")
+    if args.layers_per_launch is None:
+        args.layers_per_launch = cfg.layers_per_launch
     pipe = DecodePipeline(cfg, inp, n_layers=n_layers, layers_per_launch=args.layers_per_launch, timing=False,
                           gather_streams=args.gather_streams, elastic=not args.no_elastic)
     log("pipeline ready")

@@ -35,8 +35,9 @@
 //    with each warp owning 128 of the 512 latent dims (P in bf16 high + low
 //    parts from shared memory, the rows as ldmatrix.trans B fragments). Each
 //    CTA writes its (max, sum, O) partial to the workspace;
-//  * mla_out_kernel: per (layer, request, head) merges the partials in split
-//    order (deterministic) and applies W_uv[h] (128 x 512 bf16).
+//  * mla_out_kernel: per (layer, request, head, 32 output values) merges the
+//    partials in a fixed order (deterministic) and applies those 32 rows of
+//    W_uv[h] (128 x 512 bf16).
 //  * mla_gather_kernel: one warp per load streams the load's run of the
 //    position-major host store (every stored layer's latent row of that
 //    position, contiguous) into the layer slots.
@@ -436,7 +437,7 @@ constexpr int kMoThreads = 256;
 constexpr int kMoChunk = 32;       // output values per CTA (4 CTAs per head)
 
 // Grid (units, heads, 4 chunks of 32 output values): merge the head's split
-// partials in split order (every CTA of the head the same way), then 8 warps
+// partials in a fixed order (every CTA of the head the same way), then 8 warps
 // x 4 values each dot W_uv[l, h][v, :] with the merged latent sum, two
 // 16-byte loads per value and lane, all 8 in flight.
 __global__ void __launch_bounds__(kMoThreads)
@@ -448,18 +449,19 @@ mla_out_kernel(const float* __restrict__ part, const uint16_t* __restrict__ Wuv,
   const int l = unit / B;
   const float* pp = part + (size_t)unit * n_split * kMH * kMaPart + (size_t)h * kMaPart;
   const size_t sstride = (size_t)kMH * kMaPart;
-  // split weights exp2(m_s - M) / sum_s exp2(m_s - M) l_s
-  if (tid == 0) {
-    float M = -INFINITY;
-    for (int s = 0; s < n_split; ++s) M = fmaxf(M, pp[s * sstride]);
-    float den = 0.f;
-    for (int s = 0; s < n_split; ++s) {
-      const float e = M == -INFINITY ? 0.f : exp2f(pp[s * sstride] - M);
-      wgt[s] = e;
-      den += e * pp[s * sstride + 1];
-    }
+  // split weights exp2(m_s - M) / sum_s exp2(m_s - M) l_s, by warp 0 (two
+  // splits per lane, all loads in flight together; n_split <= 64)
+  if (tid < 32) {
+    const bool h0 = tid < n_split, h1 = tid + 32 < n_split;
+    const float2 a0 = h0 ? *reinterpret_cast<const float2*>(pp + tid * sstride) : make_float2(-INFINITY, 0.f);
+    const float2 a1 = h1 ? *reinterpret_cast<const float2*>(pp + (tid + 32) * sstride) : make_float2(-INFINITY, 0.f);
+    const float M = warp_max(fmaxf(a0.x, a1.x));
+    const float e0 = M == -INFINITY || !h0 ? 0.f : exp2f(a0.x - M);
+    const float e1 = M == -INFINITY || !h1 ? 0.f : exp2f(a1.x - M);
+    const float den = warp_sum(e0 * a0.y + e1 * a1.y);
     const float inv = den > 0.f ? 1.f / den : 0.f;
-    for (int s = 0; s < n_split; ++s) wgt[s] *= inv;
+    if (h0) wgt[tid] = e0 * inv;
+    if (h1) wgt[tid + 32] = e1 * inv;
   }
   __syncthreads();
   if (tid < kDc / 4) {
