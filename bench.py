@@ -152,19 +152,35 @@ class ClockSampler:
 NCU_TRAFFIC = {
     # gather of decode step 0, layers 16-31: 1550 loads x 16 layers x K/V = 49 600
     # rows; 396 800 system-memory sectors (12 697 600 B) read over the host link
-    # + 26 624 B DRAM read + 1 280 B DRAM write
+    # + 27 136 B DRAM read + 768 B DRAM write
     "gather": {"source": "sparse_kv_cache_retrieval_gb300/csrc/gather_kv.cu",
                "sha256": "d81e9b9166c899f4c820d594fb21af5f6bb7b23790e98c209bf5423dd8677dad",
-               "bytes_per_unit": (12697600 + 26624 + 1280) / 49600, "unit": "moved 256-byte row"},
-    # key scan over 32 768 positions x 8 KV heads: 67 141 376 B DRAM read + 335 616 B write
+               "bytes_per_unit": (12697600 + 27136 + 768) / 49600, "unit": "moved 256-byte row"},
+    # key scan over 32 768 positions x 8 KV heads: 67 140 864 B DRAM read + 373 760 B write
     "key_scan": {"source": "sparse_kv_cache_retrieval_gb300/csrc/score_select.cu",
-                 "sha256": "df251f8d23bde64a3e27365d8152cde3d8b761720b263eafd1a216ffed577fdb",
-                 "bytes_per_unit": (67141376 + 335616) / 262144, "unit": "256-byte key row"},
+                 "sha256": "4a191748e9f2cebc43c36e86a84a4aacf8a7af7ba6581cd6c75433f62852d15e",
+                 "bytes_per_unit": (67140864 + 373760) / 262144, "unit": "256-byte key row"},
     # attention over 16 layers x 8 KV heads x 2048 kept rows, mean of two launches:
-    # 134 537 984 B read + 3 164 800 B write
+    # 134 537 600 B read + 3 222 656 B write
     "attention": {"source": "sparse_kv_cache_retrieval_gb300/csrc/sparse_attn.cu",
                   "sha256": "01e645590c4b04bc2ebf3b3ffe7de26745c170c8cca195e315e23f35760f7f86",
-                  "bytes_per_unit": (134537984 + 3164800) / 262144, "unit": "512-byte K+V row"},
+                  "bytes_per_unit": (134537600 + 3222656) / 262144, "unit": "512-byte K+V row"},
+    # MLA: gather of decode step 0, 221 loads x 27 layers = 5 967 latent rows;
+    # 214 812 system-memory sectors (6 873 984 B) over the host link + 12 288 B DRAM read
+    "mla_gather": {"source": "sparse_kv_cache_retrieval_gb300/csrc/mla.cu",
+                   "sha256": "1407adb684fb8fd8d8b399abb07c577d59ad093bebb69169f9240d4bec35dbfe",
+                   "bytes_per_unit": (6873984 + 12288) / 5967, "unit": "moved 1152-byte latent row"},
+    # MLA latent scan over 32 768 positions: 37 803 776 B DRAM read
+    "mla_scan": {"source": "sparse_kv_cache_retrieval_gb300/csrc/score_select.cu",
+                 "sha256": "4a191748e9f2cebc43c36e86a84a4aacf8a7af7ba6581cd6c75433f62852d15e",
+                 "bytes_per_unit": 37803776 / 32768, "unit": "1152-byte latent row"},
+    # MLA attention call over 27 layers x 2048 kept rows (absorption + attention
+    # + merge/W_uv kernels): (56 800 512 + 64 724 992 + 66 444 288) B read
+    # + (36 608 + 1 076 224 + 377 088) B written
+    "mla_attention": {"source": "sparse_kv_cache_retrieval_gb300/csrc/mla.cu",
+                      "sha256": "1407adb684fb8fd8d8b399abb07c577d59ad093bebb69169f9240d4bec35dbfe",
+                      "bytes_per_unit": (56800512 + 64724992 + 66444288 + 36608 + 1076224 + 377088) / 55296,
+                      "unit": "1152-byte kept latent row"},
 }
 
 
@@ -178,7 +194,8 @@ def _sha256(rel: str) -> str:
 
 
 def traffic_units(cfg) -> dict:
-    """Per timed kind: (NCU_TRAFFIC key, algorithmic bytes of one unit)."""
+    """Per timed kind: (NCU_TRAFFIC key, bytes of one unit: a key row, a
+    moved row, a kept row)."""
     if cfg.mla:
         return {"gather": ("mla_gather", 1152), "key_scan": ("mla_scan", 1152), "attention": ("mla_attention", 1152)}
     return {"gather": ("gather", 256), "key_scan": ("key_scan", 256), "attention": ("attention", 512)}
@@ -628,10 +645,16 @@ def our_arm(args, rank, world, local):
     for k in ("project", "select", "diff"):
         if k in kern:
             kinfo[k] = {"mean_us": round(kern[k]["mean_us"], 2), "launches": kern[k]["launches"]}
+    # ncu traffic per launch: the captured bytes per unit times this launch's
+    # units (key rows, moved rows, kept rows)
     units = traffic_units(cfg)
+    n_units = {"key_scan": sum(int(L) for L in lens_now) * (1 if cfg.mla else cfg.n_kv),
+               "attention": rows_kept * (pipe.chunks[0][1] - pipe.chunks[0][0])}
+    if "gather" in kinfo:
+        n_units["gather"] = kinfo["gather"]["algorithmic_bytes"] / units["gather"][1]
     for k, (tk, ub) in units.items():
-        if k in kinfo:
-            kinfo[k]["traffic"] = ncu_traffic(tk, kinfo[k]["algorithmic_bytes"] / ub)
+        if k in kinfo and k in n_units:
+            kinfo[k]["traffic"] = ncu_traffic(tk, n_units[k])
     # every kernel alone (L2 flushed before each launch), same launch shapes
     log("isolated kernel timing")
     iso = isolated_times(pipe, spc, torch, t_last=W + K - 1)
@@ -652,8 +675,7 @@ def our_arm(args, rank, world, local):
     roof = None
     if dominant in ("gather", "key_scan", "attention"):
         r = kinfo[dominant]
-        tk, unit_bytes = units[dominant]
-        traffic = ncu_traffic(tk, r["algorithmic_bytes"] / unit_bytes)
+        traffic = r.get("traffic")
         roof = {"kernel": dominant, "bound": r["bound"], "achieved": r["achieved"], "peak": r["peak"],
                 "unit": "GB/s", "frac": r["frac"], "traffic": traffic,
                 "peak_source": "measured in this run (zero-copy read of pinned host memory)"
