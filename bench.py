@@ -51,6 +51,9 @@ def parse():
     ap.add_argument("--layers", type=int, default=None,
                     help="LLM layers to run (default: the workload's); the JSON line states it")
     ap.add_argument("--gather-streams", type=int, default=1, choices=[1, 2])
+    ap.add_argument("--front-after", choices=("select", "attention"), default=None,
+                    help="issue the next step's projection and key scan after this step's select or after its "
+                         "last attention (default: the workload's)")
     ap.add_argument("--no-elastic", action="store_true",
                     help="reload every step's whole selection (the baseline elastic loading is measured against)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -496,8 +499,11 @@ def our_arm(args, rank, world, local):
     log("allocating and filling the pinned host store")
     if args.layers_per_launch is None:
         args.layers_per_launch = cfg.layers_per_launch
+    if args.front_after is None:
+        args.front_after = cfg.front_after
     pipe = DecodePipeline(cfg, inp, n_layers=n_layers, layers_per_launch=args.layers_per_launch, timing=False,
-                          gather_streams=args.gather_streams, elastic=not args.no_elastic)
+                          gather_streams=args.gather_streams, elastic=not args.no_elastic,
+                          front_after=args.front_after)
     log("pipeline ready")
     if args.profile:
         # the launch sequence a profiler sees: the prologue (one whole-selection
@@ -732,6 +738,7 @@ def our_arm(args, rank, world, local):
     if args.no_elastic:
         config["elastic"] = "off: every step reloads its whole selection"
     config.update({"layers_per_launch": args.layers_per_launch, "gather_streams": args.gather_streams,
+                   "front_after": args.front_after,
                    "l2": (f"inputs larger than L2: each step reads the {scan_bytes / 2**20:.0f} MiB "
                           f"{'latent' if cfg.mla else 'key'} cache and {attn_layer_bytes * n_layers / 2**20:.0f} "
                           f"MiB of {'latent rows and up-projection weights' if cfg.mla else 'K/V rows'} and "

@@ -50,6 +50,8 @@ class Workload:
     kv_bytes: Optional[int] = None   # GPU memory for the LLM KV: set = adaptive layer offload
     mla: bool = False      # MLA attention: one 576-value latent row per position (n_kv = 1, d = 128)
     layers_per_launch: int = 16   # attention/gather layer chunk of the step schedule
+    front_after: str = "select"   # the next step's projection + key scan start after this step's
+                                  # select, or after its last attention ("attention")
     note: str = ""
 
     @property
@@ -105,6 +107,12 @@ def _cfg3_lens(seed: int, B: int):
 
 
 def _build() -> dict:
+    # Schedules: the link-bound workloads whose select/diff/attention chain is
+    # slowed by the next step's key scan running beside it (cfg2, cfg3) start
+    # that scan after the step's last attention (measured on one GB300:
+    # cfg2 135.1 vs 138.4 us/step, cfg3 1435 vs 1455); where the chain itself
+    # is the bound (cfg1, cfg4b, MLA) the scan overlaps it (cfg1 27.4 vs 34.0,
+    # cfg4b 521 vs 651, MLA 95.3 vs 106.8); cfg5 is indifferent (2781 vs 2779).
     cfgs = {}
     cfgs["cfg1"] = Workload(
         name="cfg1_b1_ctx4096_gqa32x8_budget512_2layers",
@@ -114,7 +122,7 @@ def _build() -> dict:
     cfgs["cfg2"] = Workload(
         name="cfg2_b1_ctx32768_gqa32x8_budget2048_32layers_host",
         B=1, lens=(32768,), H=4096, n_q=32, n_kv=8, d=128, budget=2048, n_layers=32,
-        gpu_layers=(0,), steps=64, rho=(0.9,), hot=(328,), seed=1, cap=32768,
+        gpu_layers=(0,), steps=64, rho=(0.9,), hot=(328,), seed=1, cap=32768, front_after="attention",
         note="Llama3.1-8B-shaped GQA; 32-layer KV (4 GiB) in pinned host; hot set 1%")
     lens3, rho3 = _cfg3_lens(2, 16)
     cap3 = max(lens3)
@@ -122,7 +130,7 @@ def _build() -> dict:
         name="cfg3_b16_ragged8k-16k_gqa32x8_budget1024_32layers_split",
         B=16, lens=lens3, H=4096, n_q=32, n_kv=8, d=128, budget=1024, n_layers=32,
         gpu_layers=_split_by_threshold(lens3, 32, 8, 128, 1024, 12 * GiB),
-        steps=32, rho=rho3, hot=tuple(max(1, L // 100) for L in lens3), seed=2, cap=cap3,
+        steps=32, rho=rho3, hot=tuple(max(1, L // 100) for L in lens3), seed=2, cap=cap3, front_after="attention",
         note="ragged batch; HBM/host split per request from a 12 GiB HBM allowance")
     cfgs["cfg4a"] = Workload(
         name="cfg4a_b4_ctx2048+256_append_gqa32x8_budget2048_32layers_host",

@@ -62,7 +62,7 @@ class DecodePipeline:
                  n_layers: Optional[int] = None, layers_per_launch: int = 16,
                  host_io: bool = False, timing: bool = False, fill_threads: Optional[int] = None,
                  gather_streams: int = 1, kv_bytes: Optional[int] = None,
-                 offload_policy: str = "progressive", elastic: bool = True):
+                 offload_policy: str = "progressive", elastic: bool = True, front_after: Optional[str] = None):
         self.cfg = cfg
         self.inp = inputs
         self.dev = torch.device(device)
@@ -127,6 +127,14 @@ class DecodePipeline:
         # against: every step reloads its whole selection (the diff sees no
         # resident slot)
         self.elastic = elastic
+        # where the next step's projection and key scan (the front) start
+        # inside a run of steps: right after this step's select ("select"),
+        # or after its last attention ("attention"), so that they do not
+        # compete with this step's diff and attention for the SMs and HBM
+        front_after = cfg.front_after if front_after is None else front_after
+        if front_after not in ("select", "attention"):
+            raise ValueError("front_after is 'select' or 'attention'")
+        self.front_after = front_after
         self.adaptive = kv_bytes is not None
         self.kv_bytes = kv_bytes
         self.offload_policy = offload_policy
@@ -481,15 +489,18 @@ class DecodePipeline:
         self._front_issued = None
         self._prologue_done = True
 
-    def _front(self, t: int) -> None:
+    def _front(self, t: int, after: Optional[torch.cuda.Event] = None) -> None:
         """Projection and key scan of step t (input x[t+1]) on stream C, after
-        the select of step t-1 issued in this run (none before the first)."""
+        the select of step t-1 issued in this run (none before the first), and
+        after `after` when given."""
         sC = self.sC
         append = 1 if self.cfg.append else 0
         if self._front_issued is not None:
             sC.wait_event(self.e_sel)
         else:
             sC.wait_stream(self.sA)
+        if after is not None:
+            sC.wait_event(after)
         pn = (t + 1) % 2
         if self.host_io:
             spc.spc_copy(self.x_stage, self._x_dev_host + (t + 1) * self._x_bytes, self._x_bytes, stream=sC)
@@ -547,7 +558,7 @@ class DecodePipeline:
         # the select stage reads only the front's scratch; x is not used
         self._timed_call("select", sA, lambda: self._score_select(self.x_dev[0], self.selected[pn], append, sA, 4))
         self.e_sel.record(sA)
-        if lookahead and t + 2 < len(self.inp.x):
+        if lookahead and t + 2 < len(self.inp.x) and self.front_after == "select":
             self._front(t + 1)
         self._timed_call("diff", sA, lambda: self._diff(pn, p, sA))
         for c, (l0, l1) in enumerate(self.chunks):
@@ -562,6 +573,8 @@ class DecodePipeline:
             self._gather_pending[c] = True
         self.e_attn_end[p].record(sA)
         self._attn_end_rec[p] = True
+        if lookahead and t + 2 < len(self.inp.x) and self.front_after == "attention":
+            self._front(t + 1, after=self.e_attn_end[p])
         if self.host_io:
             if lookahead and t + 1 < self.n_steps:
                 self._q_copy(t + 1)

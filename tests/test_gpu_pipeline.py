@@ -254,3 +254,21 @@ def test_host_io_matches_device_resident():
     torch.cuda.synchronize()
     for t in range(3):
         assert torch.equal(b.out_host[t], outs[t])
+
+
+def test_front_after_attention_gives_the_same_steps():
+    """Issuing the next step's projection and key scan after the last
+    attention instead of after the select changes only the schedule."""
+    cfg = scaled(CONFIGS["cfg2"], n_layers=4, steps=4)
+    inp = make_inputs(cfg, steps=4, n_layers=4)
+    a = DecodePipeline(cfg, inp, n_layers=4, layers_per_launch=2)
+    a.prologue()
+    a.run(0, 4)
+    torch.cuda.synchronize()
+    b = DecodePipeline(cfg, inp, n_layers=4, layers_per_launch=2, front_after="attention")
+    b.prologue()
+    g = b.capture(0, 4)
+    g.replay()
+    torch.cuda.synchronize()
+    for u, v in zip(_state(a), _state(b)):
+        assert torch.equal(u, v)
