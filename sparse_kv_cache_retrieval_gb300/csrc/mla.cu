@@ -89,6 +89,13 @@ mla_absorb_kernel(const QT* __restrict__ q, const uint16_t* __restrict__ Wuk, in
   const int i1 = min(min(n_items, (w + 1) * items_per_w), i0 + NI);
   const int ni = i1 - i0;
   if (ni <= 0) return;
+  const int rg = tid >> 4, cl = tid & 15;
+  // W_uk[w, h] is [128][512]: row j holds the weights of nope value j; this
+  // thread's 8 rows are requested before the queries are staged
+  const uint16_t* W = Wuk + ((size_t)w * kMH + h) * kNope * kDc + chunk * kAbsChunk + cl * 8;
+  uint4 wv[kNope / kAbsRg];
+#pragma unroll
+  for (int k = 0; k < kNope / kAbsRg; ++k) wv[k] = ldg_stream(W + (size_t)(rg + kAbsRg * k) * kDc);
   for (int idx = tid; idx < kNope * NI; idx += kAbsThreads) {
     const int j = idx / NI, it = idx - j * NI;
     qs[j][it] = it < ni ? load_q<QT>(q + ((size_t)(i0 + it) * kMH + h) * kQk + j) : 0.f;
@@ -101,12 +108,6 @@ mla_absorb_kernel(const QT* __restrict__ q, const uint16_t* __restrict__ Wuk, in
     }
   }
   __syncthreads();
-  const int rg = tid >> 4, cl = tid & 15;
-  // W_uk[w, h] is [128][512]: row j holds the weights of nope value j
-  const uint16_t* W = Wuk + ((size_t)w * kMH + h) * kNope * kDc + chunk * kAbsChunk + cl * 8;
-  uint4 wv[kNope / kAbsRg];
-#pragma unroll
-  for (int k = 0; k < kNope / kAbsRg; ++k) wv[k] = ldg_stream(W + (size_t)(rg + kAbsRg * k) * kDc);
   float acc[NI][8];
 #pragma unroll
   for (int it = 0; it < NI; ++it)
@@ -447,6 +448,17 @@ mla_out_kernel(const float* __restrict__ part, const uint16_t* __restrict__ Wuv,
   __shared__ float wgt[64];
   const int unit = blockIdx.x, h = blockIdx.y, v0 = blockIdx.z * kMoChunk, tid = threadIdx.x;
   const int l = unit / B;
+  const int warp = tid >> 5, lane = tid & 31;
+  // this warp's 4 rows of W_uv[l, h] are requested first: they do not depend
+  // on the merge, so their DRAM latency overlaps it
+  const uint16_t* W = Wuv + ((size_t)l * kMH + h) * kDv * kDc;
+  const int vb = v0 + warp * 4;
+  uint4 w0[4], w1[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    w0[u] = ldg_stream(W + (size_t)(vb + u) * kDc + lane * 8);
+    w1[u] = ldg_stream(W + (size_t)(vb + u) * kDc + 256 + lane * 8);
+  }
   const float* pp = part + (size_t)unit * n_split * kMH * kMaPart + (size_t)h * kMaPart;
   const size_t sstride = (size_t)kMH * kMaPart;
   // split weights exp2(m_s - M) / sum_s exp2(m_s - M) l_s, by warp 0 (two
@@ -475,15 +487,6 @@ mla_out_kernel(const float* __restrict__ part, const uint16_t* __restrict__ Wuv,
     *reinterpret_cast<float4*>(lat + 4 * tid) = acc;
   }
   __syncthreads();
-  const int warp = tid >> 5, lane = tid & 31;
-  const uint16_t* W = Wuv + ((size_t)l * kMH + h) * kDv * kDc;
-  const int vb = v0 + warp * 4;
-  uint4 w0[4], w1[4];
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    w0[u] = ldg_stream(W + (size_t)(vb + u) * kDc + lane * 8);
-    w1[u] = ldg_stream(W + (size_t)(vb + u) * kDc + 256 + lane * 8);
-  }
   float lv[16];
 #pragma unroll
   for (int e = 0; e < 8; ++e) { lv[e] = lat[lane * 8 + e]; lv[8 + e] = lat[256 + lane * 8 + e]; }

@@ -769,6 +769,7 @@ struct SelArgs {
 struct SelSmem {
   uint32_t hist[kHistBins];           // this rank's histogram of the current level
   uint32_t tot[kHistBins];            // the cluster's counts (or this rank's share of them)
+  uint32_t coarse[kHistBins / 32];    // this rank's level-1 counts per 32 bins
   uint32_t keys[kSelSmemKeys];
   uint32_t lc[kSelCandMax];           // this rank's keys in the threshold bin (any order)
   uint32_t cand[kSelCandMax];         // every rank's, in rank order
@@ -977,18 +978,67 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a) {
   int need = 0;
   int base_b = -1, base_e = 0;        // base_b < 0: offsets still to exchange
   if (Kp > 0) {
-    cluster.sync();                   // every rank's level-1 histogram is final
-    for (int i = tid; i < kHistBins; i += kSelThreads) {
-      uint32_t v[kSelMaxCluster];
+    // the threshold bin in two levels: this rank's counts per 32 bins first,
+    // then (one warp) the cluster's sums of those 64 coarse counts and of the
+    // 32 bins of the coarse bin that holds the Kp-th key; each rank reads
+    // 1 536 remote counts instead of all 2 048 bins of every rank
+    for (int j = warp; j < kHistBins / 32; j += NW) {
+      const uint32_t v = __reduce_add_sync(0xffffffffu, sm.hist[j * 32 + lane]);
+      if (lane == 0) sm.coarse[j] = v;
+    }
+    cluster.sync();                   // every rank's level-1 histograms are final
+    if (warp == 0) {
+      const uint32_t kp = (uint32_t)Kp;
+      // coarse bins from the top: lane l takes 63 - 2l and 62 - 2l
+      const int ja = kHistBins / 32 - 1 - 2 * lane, jb = ja - 1;
+      uint32_t va[kSelMaxCluster], vb[kSelMaxCluster];
 #pragma unroll
-      for (int r = 0; r < kSelMaxCluster; ++r) v[r] = r < C ? *cluster.map_shared_rank(&sm.hist[i], r) : 0u;
-      uint32_t sum = 0u;
+      for (int r = 0; r < kSelMaxCluster; ++r) {
+        va[r] = r < C ? *cluster.map_shared_rank(&sm.coarse[ja], r) : 0u;
+        vb[r] = r < C ? *cluster.map_shared_rank(&sm.coarse[jb], r) : 0u;
+      }
+      uint32_t c0 = 0u, c1 = 0u;
 #pragma unroll
-      for (int r = 0; r < kSelMaxCluster; ++r) sum += v[r];
-      sm.tot[i] = sum;
+      for (int r = 0; r < kSelMaxCluster; ++r) { c0 += va[r]; c1 += vb[r]; }
+      uint32_t incl = c0 + c1;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const uint32_t before = incl - (c0 + c1);
+      int J = -1;
+      uint32_t remJ = 0u;
+      if (before < kp && kp <= before + c0) { J = ja; remJ = kp - before; }
+      else if (before + c0 < kp && kp <= before + c0 + c1) { J = jb; remJ = kp - before - c0; }
+      const uint32_t found = __ballot_sync(0xffffffffu, J >= 0);
+      const int src = found ? __ffs(found) - 1 : 0;
+      J = __shfl_sync(0xffffffffu, J, src);
+      remJ = __shfl_sync(0xffffffffu, remJ, src);
+      if (J < 0) J = 0;
+      // the 32 bins of coarse bin J from the top: lane k takes bin 32 J + 31 - k
+      const int bi = J * 32 + 31 - lane;
+      uint32_t vf[kSelMaxCluster];
+#pragma unroll
+      for (int r = 0; r < kSelMaxCluster; ++r) vf[r] = r < C ? *cluster.map_shared_rank(&sm.hist[bi], r) : 0u;
+      uint32_t fc = 0u;
+#pragma unroll
+      for (int r = 0; r < kSelMaxCluster; ++r) fc += vf[r];
+      sm.tot[bi] = fc;
+      uint32_t fin = fc;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, fin, o);
+        if (lane >= o) fin += t;
+      }
+      const uint32_t fb = fin - fc;
+      if (fb < remJ && remJ <= fb + fc) {
+        sm.bin = bi;
+        sm.rem = (int)(remJ - fb);
+        sm.whole = (fb + fc == remJ);
+      }
     }
     __syncthreads();
-    find_bin(sm.tot, kHistBins, Kp, sm);
     const uint32_t b1 = (uint32_t)sm.bin;
     const int rem1 = sm.rem;
     if (sm.whole) {
