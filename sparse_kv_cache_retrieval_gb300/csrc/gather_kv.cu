@@ -14,10 +14,10 @@
 // across the link, and one load (position p, KV head g) is a single
 // contiguous run holding the K and V rows of every layer of the launch. One
 // warp streams one load's run: each instruction moves one layer's K row
-// (lanes 0-15) and V row (lanes 16-31), 512 contiguous bytes, with up to 8
-// layers in flight; the (position, slot) pair and the segment search are done
-// once per load. A small grid (one CTA of 512 threads per 8 SMs) keeps about
-// 1 MB in flight, enough for the link, and leaves the rest of the GPU to the
+// (lanes 0-15) and V row (lanes 16-31), 512 contiguous bytes, with up to 16
+// layers in flight (a whole 16-layer chunk's run in one round trip); the
+// (position, slot) pair and the segment search are done once per load. A small grid (one CTA of 512 threads per 8 SMs) keeps about
+// 2.5 MB in flight, enough for the link, and leaves the rest of the GPU to the
 // kernels that run beside the gather on the other streams (attention, key
 // scan). The flattened load index maps back to (request, KV head, i) through
 // a prefix sum of n_load kept in shared memory.
@@ -33,7 +33,7 @@ namespace spc {
 #endif
 constexpr int kGatherThreads = SPC_GATHER_THREADS;
 #ifndef SPC_GATHER_UNROLL
-#define SPC_GATHER_UNROLL 8    // layers of one run in flight per warp
+#define SPC_GATHER_UNROLL 16   // layers of one run in flight per warp (a 16-layer chunk in one round trip)
 #endif
 constexpr int kGatherUnroll = SPC_GATHER_UNROLL;
 constexpr int kGatherMaxSeg = 1024;
