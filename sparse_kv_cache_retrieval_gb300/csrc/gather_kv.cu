@@ -16,8 +16,9 @@
 // warp streams one load's run: each instruction moves one layer's K row
 // (lanes 0-15) and V row (lanes 16-31), 512 contiguous bytes, with up to 16
 // layers in flight (a whole 16-layer chunk's run in one round trip); the
-// (position, slot) pair and the segment search are done once per load. A small grid (one CTA of 512 threads per 8 SMs) keeps about
-// 2.5 MB in flight, enough for the link, and leaves the rest of the GPU to the
+// (position, slot) pair and the segment search are done once per load. A
+// small grid (one CTA of 512 threads per 8 SMs) keeps about 2.5 MB in
+// flight, enough for the link, and leaves the rest of the GPU to the
 // kernels that run beside the gather on the other streams (attention, key
 // scan). The flattened load index maps back to (request, KV head, i) through
 // a prefix sum of n_load kept in shared memory.
