@@ -145,6 +145,14 @@ def select(s: np.ndarray, budget: int, n_sink: int, n_recent: int) -> np.ndarray
     return np.sort(np.concatenate([F, taken]))
 
 
+def batch_level_select(s_groups: np.ndarray, budget: int, n_sink: int, n_recent: int) -> np.ndarray:
+    """The batch-level alternative the pages compare head-level retrieval
+    with ([Blog] §5: every head's weights merged into one Top-K): one selection
+    for the whole request from the element-wise max over ALL groups' scores,
+    shared by every KV head. s_groups: float64 [n_kv][len]."""
+    return select(np.asarray(s_groups, np.float64).max(axis=0), budget, n_sink, n_recent)
+
+
 # --------------------------------------------------------------------------
 # a5: elastic loading ([Blog] §6: to_load = S_now - S_last, worked example
 #     S_last={1,8,21,35}, S_now={1,8,21,50} -> {50}; [Summary] §5.4: reuse the
@@ -340,5 +348,5 @@ class DecodeState:
 
 
 __all__ = ["bf16_to_f64", "round_to_bf16", "project", "head_probabilities", "group_scores",
-           "forced_positions", "select", "elastic_diff", "gather", "sparse_attention", "kv_row_bytes",
+           "forced_positions", "select", "batch_level_select", "elastic_diff", "gather", "sparse_attention", "kv_row_bytes",
            "gpu_kv_bytes", "offload_thresholds", "layers_to_offload", "DecodeState"]
