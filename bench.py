@@ -54,6 +54,9 @@ def parse():
     ap.add_argument("--front-after", choices=("select", "attention"), default=None,
                     help="issue the next step's projection and key scan after this step's select or after its "
                          "last attention (default: the workload's)")
+    ap.add_argument("--retrieval", choices=("head", "batch"), default="head",
+                    help="head-level selection (the method) or the batch-level alternative the pages compare it "
+                         "with: one Top-K per request shared by every KV head")
     ap.add_argument("--no-elastic", action="store_true",
                     help="reload every step's whole selection (the baseline elastic loading is measured against)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -271,7 +274,7 @@ def isolated_times(pipe, spc, torch, t_last: int, reps: int = 20) -> dict:
     calls = {
         "project": lambda: pipe._score_select(x, pipe.selected[pn], 0, sA, 1),
         "key_scan": lambda: pipe._score_select(x, pipe.selected[pn], 0, sA, 2),
-        "select": lambda: pipe._score_select(x, pipe.selected[pn], 0, sA, 4),
+        "select": lambda: pipe._select(pn, 0, sA),
         "diff": lambda: pipe._diff(pn, p, sA),
         "attention": lambda: pipe._attn(pipe.q_dev[t_last], pipe.out_buf[p], p, l0, l1, sA),
         "gather": lambda: pipe._gather(pn, l0, l1, sA),
@@ -334,10 +337,11 @@ def attn_bytes_per_layer(cfg, rows_kept: int) -> int:
 
 
 # kernels one timed call launches
-def kernels_per_call(cfg) -> dict:
+def kernels_per_call(cfg, retrieval: str = "head") -> dict:
+    sel = 4 if retrieval == "batch" else 1     # batch-level: + merge, request select, copy to the KV heads
     if cfg.mla:
-        return {"project": 2, "key_scan": 1, "select": 1, "diff": 1, "attention": 3, "gather": 1}
-    return {"project": 1, "key_scan": 1, "select": 1, "diff": 1, "attention": 1, "gather": 1}
+        return {"project": 2, "key_scan": 1, "select": sel, "diff": 1, "attention": 3, "gather": 1}
+    return {"project": 1, "key_scan": 1, "select": sel, "diff": 1, "attention": 1, "gather": 1}
 
 
 def hbm_read_peak(spc, torch):
@@ -503,7 +507,7 @@ def our_arm(args, rank, world, local):
         args.front_after = cfg.front_after
     pipe = DecodePipeline(cfg, inp, n_layers=n_layers, layers_per_launch=args.layers_per_launch, timing=False,
                           gather_streams=args.gather_streams, elastic=not args.no_elastic,
-                          front_after=args.front_after)
+                          front_after=args.front_after, retrieval=args.retrieval)
     log("pipeline ready")
     if args.profile:
         # the launch sequence a profiler sees: the prologue (one whole-selection
@@ -519,9 +523,9 @@ def our_arm(args, rank, world, local):
             rows.append(int(pipe.n_load[(t + 1) % 2].cpu().numpy().astype(np.int64).sum()))
         torch.cuda.synchronize()
         print(json.dumps({"profile_steps": K, "workload": cfg.name,
-                          "launches_per_step": sum(kernels_per_call(cfg)[k] for k in ("project", "key_scan", "select",
-                                                                                       "diff")) +
-                          len(pipe.chunks) * (kernels_per_call(cfg)["attention"] + 1),
+                          "launches_per_step": sum(kernels_per_call(cfg, args.retrieval)[k]
+                                                   for k in ("project", "key_scan", "select", "diff")) +
+                          len(pipe.chunks) * (kernels_per_call(cfg, args.retrieval)["attention"] + 1),
                           "chunks": pipe.chunks, "gathered_rows_per_kv_per_layer": rows,
                           "scan_positions": [int(v) for v in pipe.len.cpu().numpy()]}))
         return
@@ -534,11 +538,33 @@ def our_arm(args, rank, world, local):
     torch.cuda.synchronize()
     pipe.prologue()
     nl_steps = []
+    # the eager pass also keeps the group scores, so the fraction of each
+    # group's score mass its resident set holds can be reported (head-level,
+    # and batch-level when that is the mode, with the overlap of the two sets)
+    pipe.record_scores = True
+    cover_used, cover_head, overlap = [], [], []
     for t in range(n_eager):
         pipe.step(t)
         pipe.join()
         torch.cuda.synchronize()
-        nl_steps.append(pipe.n_load[(t + 1) % 2].cpu().numpy().astype(np.int64))
+        pn = (t + 1) % 2
+        nl_steps.append(pipe.n_load[pn].cpu().numpy().astype(np.int64))
+        sc = pipe.group_scores.cpu().numpy()
+        used = pipe.selected[pn].cpu().numpy()
+        head = pipe.selected_head[pn].cpu().numpy() if pipe.retrieval == "batch" else used
+        lens_t = pipe.len.cpu().numpy()
+        for b in range(cfg.B):
+            Lb = int(lens_t[b])
+            for g in range(cfg.n_kv):
+                tot = float(sc[b, g, :Lb].sum())
+                if tot <= 0:
+                    continue
+                su = used[b, g][used[b, g] >= 0]
+                sh = head[b, g][head[b, g] >= 0]
+                cover_used.append(float(sc[b, g, su].sum()) / tot)
+                cover_head.append(float(sc[b, g, sh].sum()) / tot)
+                overlap.append(len(np.intersect1d(su, sh)) / max(1, len(sh)))
+    pipe.record_scores = False
     log("eager pass done; capturing graphs")
 
     # ---- graph-timed region: the headline number. The timed graph also
@@ -602,7 +628,7 @@ def our_arm(args, rank, world, local):
         r["mean_us"] = r["total_ms"] * 1e3 / max(1, r["launches"])
     timing_src = ("CUDA event pair around every launch on its stream, in a second replay of the "
                   "same steps from the same state")
-    kpc = kernels_per_call(cfg)
+    kpc = kernels_per_call(cfg, args.retrieval)
     launches_per_step = sum(r["launches"] * kpc.get(k, 1) for k, r in kern.items()) // max(1, K)
 
 
@@ -737,6 +763,8 @@ def our_arm(args, rank, world, local):
         config["layers_note"] = f"{n_layers} of the workload's {cfg.n_layers} layers"
     if args.no_elastic:
         config["elastic"] = "off: every step reloads its whole selection"
+    if args.retrieval == "batch":
+        config["retrieval"] = "batch-level: one Top-K per request shared by every KV head"
     config.update({"layers_per_launch": args.layers_per_launch, "gather_streams": args.gather_streams,
                    "front_after": args.front_after,
                    "l2": (f"inputs larger than L2: each step reads the {scan_bytes / 2**20:.0f} MiB "
@@ -760,6 +788,13 @@ def our_arm(args, rank, world, local):
                     "transfer_saved": round(1 - gathered / max(1, full_reload), 3),
                     "adjacent_overlap": round(float(overlap), 3) if overlap is not None else None},
         "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
+        "retrieval": {"mode": args.retrieval,
+                      "score_mass_kept": round(float(np.mean(cover_used)), 4) if cover_used else None,
+                      "score_mass_kept_head_level": round(float(np.mean(cover_head)), 4) if cover_head else None,
+                      "overlap_with_head_level": round(float(np.mean(overlap)), 4) if overlap else None,
+                      "note": "fraction of each KV-head group's retrieval score mass (max over its query heads of "
+                              "the softmax weights) that its resident set holds, mean over groups and the "
+                              f"{n_eager} eager steps"},
     }
     print(json.dumps(line))
 

@@ -323,6 +323,28 @@ int spc_sparse_decode_attn_noalloc(const void* q, const spc_kv_view* views,
                                    float* out, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Batch-level selection: the alternative the pages compare head-level
+ * retrieval with ([Blog] §5: merging every head's weights into one Top-K is
+ * too coarse; head-level keeps a set per head). For every request b:
+ *   s_b[p] = max_g scores[b,g,p],  p < len[b]
+ *   selected[b,g,:] = the spc_score_select rule (forced sinks and recent
+ *                     window, Top-K of s_b, ties to the lower position,
+ *                     ascending, -1 padded), the SAME set for every KV head g.
+ * scores     fp32 [B][n_kv][cap]: the group scores spc_score_select writes to
+ *            scores_out in the same step (entries p >= len are not read).
+ * len        int32 [B] current lengths (read only).
+ * selected   int32 [B][n_kv][budget] output.
+ * workspace  spc_batch_select_workspace_size() bytes, 256-byte aligned,
+ *            ZERO-FILLED BEFORE ITS FIRST USE (calls leave it ready).
+ * Limits: as spc_score_select (B <= 64, budget <= min(cap, 4096), cap <=
+ *         262144, n_sink + n_recent <= budget), n_kv <= 64.
+ * ---------------------------------------------------------------------- */
+size_t spc_batch_select_workspace_size(int B, int cap, int budget);
+
+int spc_batch_select(const float* scores, int32_t* len, int B, int n_kv, int cap, int budget, int n_sink,
+                     int n_recent, int32_t* selected, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * MLA variant. [Blog] §5: for DeepSeek's MLA the retrieval picks entries of
  * the low-dimensional latent cache and only the selected entries are
  * up-projected; [Summary] §4.3: retrieval stays head-level and only the

@@ -52,6 +52,8 @@ SIGNATURES = {
     "spc_fill_slots": (_I, [_P, _I, _I, _P, _I, _I, _I, _I, _I, _P]),
     "spc_store_layer": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "spc_offload_thresholds": (_I, [_I, _I, _I, _I, _I, ctypes.c_int64, ctypes.POINTER(ctypes.c_int64)]),
+    "spc_batch_select_workspace_size": (ctypes.c_size_t, [_I] * 3),
+    "spc_batch_select": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P, ctypes.c_size_t, _P]),
     "spc_mla_score_select_workspace_size": (ctypes.c_size_t, [_I] * 4),
     "spc_mla_score_select": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P,
                                   ctypes.c_size_t, _P, _I]),
@@ -219,6 +221,21 @@ def spc_offload_thresholds(n_layers, n_kv, d, B, budget, kv_bytes) -> list:
     _check("spc_offload_thresholds", lib().spc_offload_thresholds(n_layers, n_kv, d, B, budget,
                                                                   int(kv_bytes), out))
     return [int(v) for v in out]
+
+
+def spc_batch_select_workspace_size(B, cap, budget) -> int:
+    return int(lib().spc_batch_select_workspace_size(B, cap, budget))
+
+
+def spc_batch_select(scores, len, B, n_kv, cap, budget, n_sink, n_recent, selected, workspace, workspace_bytes=None,
+                     stream=None) -> None:
+    """Batch-level selection: one Top-K per request from the max over groups,
+    copied to every KV head."""
+    if workspace_bytes is None:
+        workspace_bytes = _nbytes(workspace)
+    _check("spc_batch_select", lib().spc_batch_select(
+        _ptr(scores), _ptr(len), B, n_kv, cap, budget, n_sink, n_recent, _ptr(selected), _ptr(workspace),
+        workspace_bytes, _stream(stream)))
 
 
 # ------------------------------------------------------------------ MLA variant

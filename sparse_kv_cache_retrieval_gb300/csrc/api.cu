@@ -255,6 +255,24 @@ int spc_sparse_decode_attn_noalloc(const void* q, const spc_kv_view* views, cons
                              stream);
 }
 
+size_t spc_batch_select_workspace_size(int B, int cap, int budget) {
+  if (B < 1 || B > SPC_MAX_BATCH || cap < 1 || cap > SPC_MAX_CAP || budget < 1 || budget > SPC_MAX_BUDGET) return 0;
+  return batch_select_workspace(B, cap, budget);
+}
+
+int spc_batch_select(const float* scores, int32_t* len, int B, int n_kv, int cap, int budget, int n_sink,
+                     int n_recent, int32_t* selected, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!scores || !len || !selected) return SPC_ERR_INVALID_ARG;
+  if (B < 1 || B > SPC_MAX_BATCH || n_kv < 1 || n_kv > SPC_MAX_GROUP) return SPC_ERR_SHAPE;
+  if (cap < 1 || cap > SPC_MAX_CAP) return SPC_ERR_SHAPE;
+  if (budget < 1 || budget > SPC_MAX_BUDGET || budget > cap) return SPC_ERR_SHAPE;
+  if (n_sink < 0 || n_recent < 0 || n_sink + n_recent > budget) return SPC_ERR_SHAPE;
+  const size_t need = batch_select_workspace(B, cap, budget);
+  if (!workspace || workspace_bytes < need) return SPC_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SPC_ERR_INVALID_ARG;
+  return batch_select_launch(scores, len, B, n_kv, cap, budget, n_sink, n_recent, selected, workspace, stream);
+}
+
 size_t spc_mla_score_select_workspace_size(int B, int H, int cap, int budget) {
   (void)budget;
   if (B < 1 || B > SPC_MAX_BATCH || H < 1 || cap < 1) return 0;

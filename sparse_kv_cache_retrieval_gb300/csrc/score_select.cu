@@ -36,6 +36,8 @@
 #include "spc_device.cuh"
 #include "spc_internal.h"
 
+#include <algorithm>
+
 namespace spc {
 
 __device__ __forceinline__ int effective_len(const int32_t* len, int b, int append, int cap) {
@@ -1804,6 +1806,95 @@ int mla_score_select_launch(const MlaScoreSelectCall& c) {
     if (rc != SPC_OK) return rc;
   }
   return SPC_OK;
+}
+
+
+// ============================================================== batch-level selection
+// "ASPLOS'26 | SpeContext ..." (marsggbo blog) §5 compares head-level
+// retrieval with a batch-level one that merges every head's weights into one
+// Top-K. Here: per request, the element-wise max over all groups' scores (the
+// group probabilities spc_score_select writes to scores_out) is written as a
+// base-2 logit with a zero log-normaliser, and the head-level select kernel
+// (one group of one head per request) takes the Top-K; the selection is then
+// copied to every KV head.
+struct BatchLayout {
+  size_t status, done, logits, part, keys, sel, total;
+  int lstride, n_parts;
+};
+
+static BatchLayout batch_layout(int B, int cap, int budget) {
+  BatchLayout l{};
+  l.lstride = (cap + 3) & ~3;
+  l.n_parts = (cap + kScanRows - 1) / kScanRows;
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off = (off + bytes + 255) & ~size_t(255); return o; };
+  l.status = take(2 * sizeof(int));
+  l.done = l.status + sizeof(int);
+  l.logits = take(sizeof(float) * (size_t)B * l.lstride);
+  l.part = take(sizeof(float2) * (size_t)B * l.n_parts);
+  l.keys = take(sizeof(uint32_t) * (size_t)B * l.lstride);
+  l.sel = take(sizeof(int32_t) * (size_t)B * budget);
+  l.total = off;
+  return l;
+}
+
+size_t batch_select_workspace(int B, int cap, int budget) { return batch_layout(B, cap, budget).total; }
+
+constexpr int kBcThreads = 256;
+
+__global__ void __launch_bounds__(kBcThreads)
+batch_combine_kernel(const float* __restrict__ scores, const int32_t* __restrict__ len, int n_kv, int cap,
+                     int lstride, int n_parts, float* __restrict__ logits, float2* __restrict__ part) {
+  const int b = blockIdx.y, p = blockIdx.x * kBcThreads + threadIdx.x;
+  int L = len[b];
+  L = L < 0 ? 0 : (L > cap ? cap : L);
+  if (p < L) {
+    float m = 0.f;
+    for (int g = 0; g < n_kv; ++g) m = fmaxf(m, scores[((size_t)b * n_kv + g) * cap + p]);
+    logits[(size_t)b * lstride + p] = m > 0.f ? log2f(m) : -INFINITY;
+  }
+  // one logsumexp partial per 128 positions: the first is (0, 1), so the
+  // select's normaliser is 0 and its probabilities are the merged scores
+  if (p < n_parts) part[(size_t)b * n_parts + p] = p == 0 ? make_float2(0.f, 1.f) : make_float2(-INFINITY, 0.f);
+}
+
+__global__ void __launch_bounds__(kBcThreads)
+batch_broadcast_kernel(const int32_t* __restrict__ sel, int n_kv, int K, long long total, int32_t* __restrict__ out) {
+  for (long long i = (long long)blockIdx.x * kBcThreads + threadIdx.x; i < total; i += (long long)gridDim.x * kBcThreads) {
+    const long long k = i % K, bg = i / K, b = bg / n_kv;
+    out[i] = sel[b * K + k];
+  }
+}
+
+int batch_select_launch(const float* scores, int32_t* len, int B, int n_kv, int cap, int budget, int n_sink,
+                        int n_recent, int32_t* selected, void* workspace, void* stream) {
+  const BatchLayout l = batch_layout(B, cap, budget);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int n_blk = (std::max(cap, l.n_parts) + kBcThreads - 1) / kBcThreads;
+  batch_combine_kernel<<<dim3(n_blk, B), kBcThreads, 0, st>>>(scores, len, n_kv, cap, l.lstride, l.n_parts,
+                                                              reinterpret_cast<float*>(ws + l.logits),
+                                                              reinterpret_cast<float2*>(ws + l.part));
+  if (cudaGetLastError() != cudaSuccess) return SPC_ERR_CUDA;
+  SelArgs sa{};
+  sa.logits = reinterpret_cast<const float*>(ws + l.logits);
+  sa.part = reinterpret_cast<const float2*>(ws + l.part);
+  sa.keys = reinterpret_cast<uint32_t*>(ws + l.keys);
+  sa.len = len;
+  sa.scores_out = nullptr;
+  sa.selected = reinterpret_cast<int32_t*>(ws + l.sel);
+  sa.done = reinterpret_cast<uint32_t*>(ws + l.done);
+  sa.B = B; sa.n_q = 1; sa.n_kv = 1; sa.cap = cap; sa.lstride = l.lstride; sa.K = budget;
+  sa.n_sink = n_sink; sa.n_recent = n_recent; sa.append = 0;
+  sa.n_parts = l.n_parts; sa.ppt = 1; sa.kstride = l.lstride;
+  const int rc = launch_select<1>(sa, B, st);
+  if (rc != SPC_OK) return rc;
+  const long long total = (long long)B * n_kv * budget;
+  long long grid = (total + kBcThreads - 1) / kBcThreads;
+  if (grid > 1024) grid = 1024;
+  batch_broadcast_kernel<<<(int)grid, kBcThreads, 0, st>>>(reinterpret_cast<const int32_t*>(ws + l.sel), n_kv,
+                                                          budget, total, selected);
+  return cudaGetLastError() == cudaSuccess ? SPC_OK : SPC_ERR_CUDA;
 }
 
 }  // namespace spc

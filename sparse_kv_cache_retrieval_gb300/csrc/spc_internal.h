@@ -77,6 +77,10 @@ int mla_attn_launch(const void* q, const void* Wuk, const void* Wuv, const spc_k
 int mla_gather_launch(const spc_gather_view* views, int layer_lo, int layer_hi, const int32_t* load_slot,
                       const int32_t* load_pos, const int32_t* n_load, int B, int budget, void* stream);
 
+size_t batch_select_workspace(int B, int cap, int budget);
+int batch_select_launch(const float* scores, int32_t* len, int B, int n_kv, int cap, int budget, int n_sink,
+                        int n_recent, int32_t* selected, void* workspace, void* stream);
+
 int stream_read_launch(const void* src, size_t bytes, uint32_t* sink, int n_blocks, void* stream);
 
 int device_sm_count();

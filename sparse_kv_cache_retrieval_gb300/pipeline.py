@@ -62,7 +62,8 @@ class DecodePipeline:
                  n_layers: Optional[int] = None, layers_per_launch: int = 16,
                  host_io: bool = False, timing: bool = False, fill_threads: Optional[int] = None,
                  gather_streams: int = 1, kv_bytes: Optional[int] = None,
-                 offload_policy: str = "progressive", elastic: bool = True, front_after: Optional[str] = None):
+                 offload_policy: str = "progressive", elastic: bool = True, front_after: Optional[str] = None,
+                 retrieval: str = "head"):
         self.cfg = cfg
         self.inp = inputs
         self.dev = torch.device(device)
@@ -111,6 +112,10 @@ class DecodePipeline:
         self.load_pos = i32(2, B, n_kv, K)
         self.n_load = i32(2, B, n_kv)
         self.no_resident = i32(B, n_kv, K, fill=-1)
+        self.group_scores = torch.zeros(B, n_kv, cap, dtype=torch.float32, device=dev)
+        self.selected_head = i32(2, B, n_kv, K, fill=-1)
+        self.ws_batch = (torch.zeros(spc.spc_batch_select_workspace_size(B, cap, K), dtype=torch.uint8, device=dev)
+                         if retrieval == "batch" else None)
         # attention output, double-buffered by step parity (the copy of step t's
         # output to the host may still run while step t+1 writes); `out` is the
         # buffer of the step issued last
@@ -135,6 +140,15 @@ class DecodePipeline:
         if front_after not in ("select", "attention"):
             raise ValueError("front_after is 'select' or 'attention'")
         self.front_after = front_after
+        # retrieval="batch" is the alternative the pages compare head-level
+        # retrieval with ([Blog] §5): one Top-K per request from the max over
+        # all groups' scores, shared by every KV head. The head-level
+        # selection of the same step is kept in selected_head for comparison;
+        # record_scores keeps the group scores in head-level mode too
+        if retrieval not in ("head", "batch"):
+            raise ValueError("retrieval is 'head' or 'batch'")
+        self.retrieval = retrieval
+        self.record_scores = False
         self.adaptive = kv_bytes is not None
         self.kv_bytes = kv_bytes
         self.offload_policy = offload_policy
@@ -429,6 +443,19 @@ class DecodePipeline:
                                     q_out, scores_out, out_sel, self.ws_score, stream=stream,
                                     stages=stages)
 
+    def _select(self, pn, append: int, stream):
+        """The select stage into selected[pn]: head-level, or (retrieval =
+        "batch") head-level into selected_head[pn] and the batch-level
+        selection from its group scores into selected[pn]."""
+        if self.retrieval == "batch":
+            self._score_select(self.x_dev[0], self.selected_head[pn], append, stream, 4, scores_out=self.group_scores)
+            c = self.cfg
+            spc.spc_batch_select(self.group_scores, self.len, self.B, self.n_kv, self.cap, self.K, c.n_sink,
+                                 c.n_recent, self.selected[pn], self.ws_batch, stream=stream)
+        else:
+            self._score_select(self.x_dev[0], self.selected[pn], append, stream, 4,
+                               scores_out=self.group_scores if self.record_scores else None)
+
     def _diff(self, pn, p, stream):
         prev = self.slot_pos[p] if self.elastic else self.no_resident
         spc.spc_elastic_diff(self.selected[pn], prev, self.slot_pos[pn], self.load_slot[pn],
@@ -481,7 +508,8 @@ class DecodePipeline:
         with torch.cuda.stream(sA):
             self.len.copy_(torch.from_numpy(self.inp.lens.astype(np.int32)))
             self.slot_pos[1].fill_(-1)
-            self._score_select(self.x_dev[0], self.selected[0], 0, sA)
+            self._score_select(self.x_dev[0], self.selected[0], 0, sA, 3)
+            self._select(0, 0, sA)
             self._diff(0, 1, sA)
             self._gather(0, 0, self.L, sA)
         sA.synchronize()
@@ -556,7 +584,7 @@ class DecodePipeline:
         out_t = self.out_buf[p]
         self.out = out_t
         # the select stage reads only the front's scratch; x is not used
-        self._timed_call("select", sA, lambda: self._score_select(self.x_dev[0], self.selected[pn], append, sA, 4))
+        self._timed_call("select", sA, lambda: self._select(pn, append, sA))
         self.e_sel.record(sA)
         if lookahead and t + 2 < len(self.inp.x) and self.front_after == "select":
             self._front(t + 1)

@@ -209,3 +209,19 @@ def test_mla_calls_validate_before_launch(lib):
     assert lib.spc_mla_decode_attn(*bad) == -2
     bad = list(args); bad[11] = FAKE + 64
     assert lib.spc_mla_decode_attn(*bad) == -1           # workspace not 256-byte aligned
+
+
+def test_batch_select_validates_before_launch(lib):
+    args = [FAKE, FAKE, 2, 8, 4096, 512, 4, 64, FAKE, FAKE, 1 << 30, None]
+    assert lib.spc_batch_select(None, *args[1:]) == -1
+    bad = list(args); bad[3] = 0
+    assert lib.spc_batch_select(*bad) == -2               # no KV head
+    bad = list(args); bad[5] = 5000
+    assert lib.spc_batch_select(*bad) == -2               # budget > cap
+    bad = list(args); bad[6] = 500
+    assert lib.spc_batch_select(*bad) == -2               # forced set > budget
+    bad = list(args); bad[10] = 16
+    assert lib.spc_batch_select(*bad) == -5               # workspace too small
+    bad = list(args); bad[9] = FAKE + 64
+    assert lib.spc_batch_select(*bad) == -1               # workspace misaligned
+    assert B.spc_batch_select_workspace_size(2, 4096, 512) >= 2 * 4096 * 4
