@@ -542,7 +542,7 @@ def our_arm(args, rank, world, local):
     # group's score mass its resident set holds can be reported (head-level,
     # and batch-level when that is the mode, with the overlap of the two sets)
     pipe.record_scores = True
-    cover_used, cover_head, overlap = [], [], []
+    cover_used, cover_head, overlap_sets = [], [], []
     for t in range(n_eager):
         pipe.step(t)
         pipe.join()
@@ -563,7 +563,7 @@ def our_arm(args, rank, world, local):
                 sh = head[b, g][head[b, g] >= 0]
                 cover_used.append(float(sc[b, g, su].sum()) / tot)
                 cover_head.append(float(sc[b, g, sh].sum()) / tot)
-                overlap.append(len(np.intersect1d(su, sh)) / max(1, len(sh)))
+                overlap_sets.append(len(np.intersect1d(su, sh)) / max(1, len(sh)))
     pipe.record_scores = False
     log("eager pass done; capturing graphs")
 
@@ -791,7 +791,7 @@ def our_arm(args, rank, world, local):
         "retrieval": {"mode": args.retrieval,
                       "score_mass_kept": round(float(np.mean(cover_used)), 4) if cover_used else None,
                       "score_mass_kept_head_level": round(float(np.mean(cover_head)), 4) if cover_head else None,
-                      "overlap_with_head_level": round(float(np.mean(overlap)), 4) if overlap else None,
+                      "overlap_with_head_level": round(float(np.mean(overlap_sets)), 4) if overlap_sets else None,
                       "note": "fraction of each KV-head group's retrieval score mass (max over its query heads of "
                               "the softmax weights) that its resident set holds, mean over groups and the "
                               f"{n_eager} eager steps"},
