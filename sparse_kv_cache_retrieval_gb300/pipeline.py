@@ -206,6 +206,17 @@ class DecodePipeline:
             self.store_base.append(s0)
         self._slot_layer_bytes = K * cfg.row_elems * 2
         self.gviews = spc.to_device_bytes(self._gather_view_table(), dev)
+        if self.adaptive:
+            # the GPU's first access to each page of a pinned buffer pays for the
+            # page's address translation over the link; an adaptive pipeline
+            # writes its stores only when a layer moves, so read every page once
+            # here (setup) instead of inside the first offload
+            sink = torch.zeros(spc.spc_device_sm_count() * 4, dtype=torch.int32, device=dev)
+            for b, hs in enumerate(self.host_stores):
+                if hs is not None:
+                    spc.spc_stream_read(self._store_dev[b], hs.numel() * 2 // 16 * 16, sink, sink.numel())
+            torch.cuda.synchronize()
+            del sink
 
         # attention views [L][B]
         table = np.concatenate([self._attn_view_row(l, b) for l in range(L) for b in range(B)])
