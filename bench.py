@@ -158,34 +158,34 @@ class ClockSampler:
 NCU_TRAFFIC = {
     # gather of decode step 0, layers 16-31: 1550 loads x 16 layers x K/V = 49 600
     # rows; 396 800 system-memory sectors (12 697 600 B) read over the host link
-    # + 27 136 B DRAM read + 768 B DRAM write
+    # + 29 440 B DRAM read + 512 B DRAM write
     "gather": {"source": "sparse_kv_cache_retrieval_gb300/csrc/gather_kv.cu",
-               "sha256": "d81e9b9166c899f4c820d594fb21af5f6bb7b23790e98c209bf5423dd8677dad",
-               "bytes_per_unit": (12697600 + 27136 + 768) / 49600, "unit": "moved 256-byte row"},
-    # key scan over 32 768 positions x 8 KV heads: 67 140 864 B DRAM read + 373 760 B write
+               "sha256": "64d94964969b6f26d0a9bcea0c5bd87912d644381332e95ddf493098441c6a6e",
+               "bytes_per_unit": (12697600 + 29440 + 512) / 49600, "unit": "moved 256-byte row"},
+    # key scan over 32 768 positions x 8 KV heads: 67 140 864 B DRAM read + 322 048 B write
     "key_scan": {"source": "sparse_kv_cache_retrieval_gb300/csrc/score_select.cu",
-                 "sha256": "4a191748e9f2cebc43c36e86a84a4aacf8a7af7ba6581cd6c75433f62852d15e",
-                 "bytes_per_unit": (67140864 + 373760) / 262144, "unit": "256-byte key row"},
+                 "sha256": "435af35b2dce2aca1b6918dd31cd0060a4e5b12aeac4683078bfa0e0b724bf14",
+                 "bytes_per_unit": (67140864 + 322048) / 262144, "unit": "256-byte key row"},
     # attention over 16 layers x 8 KV heads x 2048 kept rows, mean of two launches:
-    # 134 537 600 B read + 3 222 656 B write
+    # 134 537 728 B read + 3 063 680 B write
     "attention": {"source": "sparse_kv_cache_retrieval_gb300/csrc/sparse_attn.cu",
                   "sha256": "01e645590c4b04bc2ebf3b3ffe7de26745c170c8cca195e315e23f35760f7f86",
-                  "bytes_per_unit": (134537600 + 3222656) / 262144, "unit": "512-byte K+V row"},
+                  "bytes_per_unit": (134537728 + 3063680) / 262144, "unit": "512-byte K+V row"},
     # MLA: gather of decode step 0, 221 loads x 27 layers = 5 967 latent rows;
-    # 214 812 system-memory sectors (6 873 984 B) over the host link + 12 288 B DRAM read
+    # 214 812 system-memory sectors (6 873 984 B) over the host link + 12 032 B DRAM read
     "mla_gather": {"source": "sparse_kv_cache_retrieval_gb300/csrc/mla.cu",
-                   "sha256": "1407adb684fb8fd8d8b399abb07c577d59ad093bebb69169f9240d4bec35dbfe",
-                   "bytes_per_unit": (6873984 + 12288) / 5967, "unit": "moved 1152-byte latent row"},
-    # MLA latent scan over 32 768 positions: 37 803 776 B DRAM read
+                   "sha256": "be0983a4f8178692b7710bf687bcae1a143b6d3766c367f5420994e4a979335a",
+                   "bytes_per_unit": (6873984 + 12032) / 5967, "unit": "moved 1152-byte latent row"},
+    # MLA latent scan over 32 768 positions: 37 804 032 B DRAM read
     "mla_scan": {"source": "sparse_kv_cache_retrieval_gb300/csrc/score_select.cu",
-                 "sha256": "4a191748e9f2cebc43c36e86a84a4aacf8a7af7ba6581cd6c75433f62852d15e",
-                 "bytes_per_unit": 37803776 / 32768, "unit": "1152-byte latent row"},
+                 "sha256": "435af35b2dce2aca1b6918dd31cd0060a4e5b12aeac4683078bfa0e0b724bf14",
+                 "bytes_per_unit": 37804032 / 32768, "unit": "1152-byte latent row"},
     # MLA attention call over 27 layers x 2048 kept rows (absorption + attention
-    # + merge/W_uv kernels): (56 800 512 + 64 724 992 + 66 444 288) B read
-    # + (36 608 + 1 076 224 + 377 088) B written
+    # + merge/W_uv kernels): (56 800 768 + 64 725 248 + 66 445 056) B read
+    # + (80 896 + 1 136 384 + 615 168) B written
     "mla_attention": {"source": "sparse_kv_cache_retrieval_gb300/csrc/mla.cu",
-                      "sha256": "1407adb684fb8fd8d8b399abb07c577d59ad093bebb69169f9240d4bec35dbfe",
-                      "bytes_per_unit": (56800512 + 64724992 + 66444288 + 36608 + 1076224 + 377088) / 55296,
+                      "sha256": "be0983a4f8178692b7710bf687bcae1a143b6d3766c367f5420994e4a979335a",
+                      "bytes_per_unit": (56800768 + 64725248 + 66445056 + 80896 + 1136384 + 615168) / 55296,
                       "unit": "1152-byte kept latent row"},
 }
 
