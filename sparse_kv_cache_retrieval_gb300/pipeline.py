@@ -77,6 +77,7 @@ class DecodePipeline:
         self.gpu_layers = [min(int(g), self.L) for g in cfg.gpu_layers]
         self.host_io = host_io
         self.timing = timing
+        self.timing_kinds = None        # with timing on: the kinds that get event pairs (None: all)
         dev = self.dev
         B, L, K, n_kv, d, cap = self.B, self.L, self.K, self.n_kv, self.d, self.cap
 
@@ -501,8 +502,11 @@ class DecodePipeline:
             return torch.cuda.Event(enable_timing=True, external=True)
         return torch.cuda.Event(enable_timing=True)
 
+    def _is_timed(self, kind) -> bool:
+        return self.timing and (self.timing_kinds is None or kind in self.timing_kinds)
+
     def _timed_call(self, kind, stream, fn):
-        if not self.timing:
+        if not self._is_timed(kind):
             fn()
             return
         s, e = self._timing_event(), self._timing_event()
@@ -546,7 +550,7 @@ class DecodePipeline:
             x = self.x_stage
         else:
             x = self.x_dev[t + 1]
-        if self.timing:
+        if self._is_timed("project") or self._is_timed("key_scan"):
             self._timed_call("project", sC, lambda: self._score_select(x, self.selected[pn], append, sC, 1))
             self._timed_call("key_scan", sC, lambda: self._score_select(x, self.selected[pn], append, sC, 2))
         else:
