@@ -18,7 +18,6 @@ module computes any step of the method.
 from __future__ import annotations
 
 import dataclasses
-import math
 from typing import List, Optional
 
 GiB = 1 << 30

@@ -1,6 +1,8 @@
-"""The decode step on four CUDA streams: the retrieval head's projection and
-key scan (stream C), select, diff and per layer chunk attention (stream A),
-and the in-place gather of the next step's missing rows (streams B0, B1).
+"""The decode step on CUDA streams: the retrieval head's projection and key
+scan (stream C), select, diff and per layer chunk attention (stream A), and
+the in-place gather of the next step's missing rows (stream B; two
+alternating streams with gather_streams=2), for GQA caches or an MLA latent
+cache, with head-level (the method) or batch-level selection.
 
 Method ordering: "ASPLOS'26 | SpeContext 让小模型先圈出重要 KV Cache"
 (marsggbo blog) §4 -- the retrieval head predicts the positions of step t+1
@@ -20,9 +22,10 @@ Ordering (per layer chunk c, step t, parity p = t % 2):
   B: wait attn(c, t); gather(c, loads[1-p]) into the slots; record gather(c, t)
 Inside a run of steps, the front of step t+1 is issued right after select(t)
 (it only needs the scan scratch that select(t) has consumed and the length
-select(t) has advanced), so it overlaps diff(t) and attention(t). The
-in-place overwrite of chunk c always follows the attention that reads the
-old rows, and the next step's attention on c always follows it.
+select(t) has advanced), so it overlaps diff(t) and attention(t), or, with
+front_after="attention", after step t's last attention. The in-place
+overwrite of chunk c always follows the attention that reads the old rows,
+and the next step's attention on c always follows it.
 
 PyTorch provides device memory, pinned host memory, streams, events and CUDA
 graphs; every step of the method runs in libspc's kernels.
@@ -30,16 +33,14 @@ graphs; every step of the method runs in libspc's kernels.
 from __future__ import annotations
 
 import math
-from typing import Dict, List, Optional
+from typing import Dict, List, Optional, Union
 
 import numpy as np
 import torch
 
 from . import binding as spc
 from .configs import MLA_LATENT_ROW, MLA_QK, Workload
-from .synth import Inputs, fill_llm_kv, fill_llm_kv_store, fill_mla_layer, fill_mla_store
-
-_BF16_ROW = 256  # bytes of one K or V row at d = 128
+from .synth import Inputs, MlaInputs, fill_llm_kv, fill_llm_kv_store, fill_mla_layer, fill_mla_store
 
 
 def _dev_u16(a: np.ndarray, device) -> torch.Tensor:
@@ -58,7 +59,7 @@ class DecodePipeline:
     GQA) or one 576-value latent row (MLA, n_kv = 1).
     """
 
-    def __init__(self, cfg: Workload, inputs: Inputs, *, device: str = "cuda",
+    def __init__(self, cfg: Workload, inputs: Union[Inputs, MlaInputs], *, device: str = "cuda",
                  n_layers: Optional[int] = None, layers_per_launch: int = 16,
                  host_io: bool = False, timing: bool = False, fill_threads: Optional[int] = None,
                  gather_streams: int = 1, kv_bytes: Optional[int] = None,
