@@ -215,6 +215,24 @@ def test_mla_decode_state_chain_small():
     assert st.lens == [32, 11]
 
 
+def test_mla_planted_latent_rows_are_selected():
+    """Latent rows shifted along the heads' summed absorbed query direction
+    (8 standard deviations up) are the Top-K when they fit, for the one group
+    of 16 heads; written out here from the query, not through the generator."""
+    rng = np.random.default_rng(71)
+    n_q, n, n_hot = 16, 1500, 30
+    Wuk = O.round_to_bf16(rng.standard_normal((n_q, M.D_NOPE, M.D_C)) / math.sqrt(M.D_C))
+    q = rng.standard_normal((n_q, M.D_QK))
+    qa = np.concatenate([np.einsum("hjc,hj->hc", O.bf16_to_f64(Wuk), q[:, :M.D_NOPE]), q[:, M.D_NOPE:]], axis=1)
+    u = qa.sum(0) / np.linalg.norm(qa.sum(0))
+    C = rng.standard_normal((n, M.D_LAT))
+    hot = np.sort(rng.choice(np.arange(4, n - 64), n_hot, replace=False))
+    C[hot] += 8.0 * math.sqrt(n_q) * u
+    P = M.mla_head_probabilities(q, O.round_to_bf16(C), Wuk, n)
+    sel = O.select(O.group_scores(P, 1)[0], n_hot + 68, 4, 64)
+    assert set(hot.tolist()) <= set(sel.tolist())
+
+
 # ----------------------------------------------------------------- mutations
 def _mut_probs_no_rope(q, C_bits, Wuk_bits, length):
     C = np.array(C_bits, copy=True)
@@ -245,6 +263,12 @@ def _mut_attn_head0_uv(q_bits, C_bits, Wuk_bits, Wuv_bits, rows, scale):
                                   rows, scale)
 
 
+def _mut_probs_rope_from_latent(q, C_bits, Wuk_bits, length):
+    C = np.array(C_bits, copy=True)
+    C[:, M.D_C:] = C[:, M.D_C - M.D_ROPE:M.D_C]      # rope key read from the latent's last 64 values
+    return M.mla_head_probabilities(q, C, Wuk_bits, length)
+
+
 def _mut_project_rope_first(x_bits, Wq_bits, Wdkv_bits, n_q):
     q, c = M.mla_project(x_bits, Wq_bits, Wdkv_bits, n_q)
     return np.concatenate([q[..., M.D_NOPE:], q[..., :M.D_NOPE]], axis=-1), c
@@ -261,6 +285,8 @@ MUTANTS = [
     ("every head's values use head 0's W_uv", [check_mla_attention_vs_sdpa, check_mla_attention_special],
      _mut_attn_head0_uv),
     ("query split rope-first", [check_mla_projection_exact], _mut_project_rope_first),
+    ("rope key read from the latent's last values", [check_mla_probs_vs_sdpa, check_mla_probs_rope_closed_form],
+     _mut_probs_rope_from_latent),
 ]
 
 
