@@ -225,3 +225,24 @@ def test_batch_select_validates_before_launch(lib):
     bad = list(args); bad[9] = FAKE + 64
     assert lib.spc_batch_select(*bad) == -1               # workspace misaligned
     assert B.spc_batch_select_workspace_size(2, 4096, 512) >= 2 * 4096 * 4
+
+
+def test_header_is_plain_c99_and_links_against_the_library(lib, tmp_path):
+    """include/spc.h is a C ABI: a C99 program that includes it compiles with
+    warnings as errors and links against libspc.so."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_spc.c"
+    src.write_text('#include "spc.h"\n#include <stdio.h>\n'
+                   'int main(void) { printf("%s\\n", spc_status_string(SPC_ERR_SHAPE)); '
+                   'return spc_version() > 0 ? 0 : 1; }\n')
+    exe = tmp_path / "use_spc"
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        str(src), "-o", str(exe), B.LIB_PATH, "-Wl,-rpath," + os.path.dirname(B.LIB_PATH)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert run.returncode == 0 and "sizes" in run.stdout
