@@ -275,7 +275,8 @@ int spc_store_layer(void* store, const void* src, int n_kv, int d, int cap, int 
  * workspace  device scratch of spc_sparse_decode_attn_workspace_size() bytes,
  *            256-byte aligned, ZERO-FILLED BEFORE ITS FIRST USE (calls leave
  *            it ready).
- * Limits: d = 128, G in {1,2,4,8,16,32,64}, budget <= 4096.
+ * Limits: d = 128, G in {1,2,4,8,16,32,64}, 1 <= B <= 64, n_layers * B <=
+ * 65535, budget <= 4096, scale > 0.
  * ---------------------------------------------------------------------- */
 typedef struct spc_kv_view {
   const void* k;
@@ -408,7 +409,8 @@ int spc_mla_score_select(const void* x, const void* Wq, const void* Wuk, const v
  * slots  bf16 [view.n_layers][budget][576] device memory, 16-byte aligned.
  * load_slot, load_pos int32 [B][budget], n_load int32 [B] (spc_elastic_diff
  * with n_kv = 1). Order after the attention that reads the old slot rows.
- * Limits: budget <= 4096. */
+ * Limits: 1 <= B <= 64, budget <= 4096, cap <= 262144; the view's host
+ * layers must lie inside the store, else the layer is skipped. */
 int spc_mla_gather(const spc_gather_view* views, int layer_lo, int layer_hi, const int32_t* load_slot,
                    const int32_t* load_pos, const int32_t* n_load, int B, int cap, int budget,
                    void* stream);
@@ -430,7 +432,8 @@ int spc_mla_gather(const spc_gather_view* views, int layer_lo, int layer_hi, con
  * workspace  device scratch of spc_mla_decode_attn_workspace_size() bytes,
  *            256-byte aligned; its first int32 is a status word (0, or
  *            SPC_ERR_TIMEOUT set by a kernel), ZERO-FILLED BEFORE FIRST USE.
- * Limits: budget <= 4096; n_layers * B <= 65535. */
+ * Limits: 1 <= B <= 64, budget <= 4096, n_layers * B <= 65535, scale > 0;
+ * q, Wuk, Wuv and out 16-byte aligned. */
 size_t spc_mla_decode_attn_workspace_size(int n_layers, int B, int budget);
 
 int spc_mla_decode_attn(const void* q, const void* Wuk, const void* Wuv, const spc_kv_view* views,
