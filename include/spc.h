@@ -27,7 +27,10 @@
  *     launched; a rejected call launches nothing and returns a negative code.
  *   - Returns SPC_OK or a negative spc_status. An error raised by a kernel
  *     after launch surfaces at the caller's next synchronisation (CUDA error)
- *     or in the workspace status word (spc_score_select).
+ *     or in the workspace status word (spc_score_select, spc_sparse_decode_attn,
+ *     spc_mla_decode_attn): every bounded device-side wait that gives up
+ *     records SPC_ERR_TIMEOUT there, lets its copies in flight land and
+ *     returns, so the context stays usable.
  *   - Calls on the same stream may be captured into a CUDA graph once each
  *     entry point has been called once outside capture (the first call sets
  *     kernel attributes).
@@ -274,7 +277,10 @@ int spc_store_layer(void* store, const void* src, int n_kv, int d, int cap, int 
  * out        fp32 [n_layers][B][n_q][d].
  * workspace  device scratch of spc_sparse_decode_attn_workspace_size() bytes,
  *            256-byte aligned, ZERO-FILLED BEFORE ITS FIRST USE (calls leave
- *            it ready).
+ *            it ready). Its first int32 is the device status word: 0, or
+ *            SPC_ERR_TIMEOUT when a bounded wait of the kernel gave up (the
+ *            output of that call is then incomplete); the caller reads and
+ *            clears it.
  * Limits: d = 128, G in {1,2,4,8,16,32,64}, 1 <= B <= 64, n_layers * B <=
  * 65535, budget <= 4096, scale > 0.
  * ---------------------------------------------------------------------- */
@@ -310,8 +316,12 @@ int spc_sparse_decode_attn(const void* q, const spc_kv_view* views, const int32_
  * SPC_ERR_WORKSPACE before anything is launched (spc_sparse_decode_attn_
  * workspace_size() tells the need). The first call on each device looks up the
  * area's address with that device current; make that first call before any
- * stream capture. Every call clears the counters it needs (one memset on
- * `stream`) and then launches the kernel. All calls share the one area: calls
+ * stream capture. Every call clears the status word and the counters it needs
+ * (one memset on `stream`) and then launches the kernel. The status word lives
+ * in the library's area, which the caller cannot read: a bounded wait that
+ * gives up still ends the kernel (the output is then incomplete), but this
+ * variant does not report it -- use spc_sparse_decode_attn where that must be
+ * observed. All calls share the one area: calls
  * whose work overlaps on the GPU (different streams, or different host
  * threads without ordering) race on it and give wrong results; order them on
  * one stream.

@@ -51,6 +51,11 @@ class Workload:
     layers_per_launch: int = 16   # attention/gather layer chunk of the step schedule
     front_after: str = "select"   # the next step's projection + key scan start after this step's
                                   # select, or after its last attention ("attention")
+    host_store_copies: int = 0    # distinct LLM K/V contents in the batch: request b holds the K/V of
+                                  # request b % copies (0: every request its own). Lets a batch whose
+                                  # host stores would not fit in the box's memory share one pinned
+                                  # store per distinct content; selections, loads and bytes moved
+                                  # stay per request
     note: str = ""
 
     @property
@@ -59,6 +64,10 @@ class Workload:
 
     def host_layers(self, b: int) -> int:
         return self.n_layers - self.gpu_layers[b]
+
+    def kv_source(self, b: int) -> int:
+        """The request whose LLM K/V contents request b holds."""
+        return b % self.host_store_copies if self.host_store_copies else b
 
     @property
     def row_elems(self) -> int:
@@ -141,13 +150,21 @@ def _build() -> dict:
         B=4, lens=(131072,) * 4, H=4096, n_q=32, n_kv=8, d=128, budget=2048, n_layers=32,
         gpu_layers=(0,) * 4, steps=256, rho=(0.9,) * 4, hot=(1310,) * 4, seed=3, append=True,
         cap=131072 + 256, note="long reasoning phase B: continued from a 128K prefilled state")
+    # cfg5's 8 x 79 host layers are 158 GiB of K/V, more than the GPU machine's
+    # host memory holds pinned beside everything else: requests b and b + 2
+    # share their K/V contents, so two pinned stores of 19.75 GiB serve the
+    # batch. Every request still selects, diffs and gathers its own positions
+    # into its own slots, so the bytes moved per step are unchanged.
     cfgs["cfg5"] = Workload(
         name="cfg5_b8_ctx65536_gqa64x8_budget4096_80layers",
         B=8, lens=(65536,) * 8, H=8192, n_q=64, n_kv=8, d=128, budget=4096, n_layers=80,
         gpu_layers=(1,) * 8, steps=64, rho=(0.85,) * 8, hot=(327,) * 8, seed=4, cap=65536,
-        note="70B-shaped GQA; layer 0 in HBM, 79 layers in pinned host; hot set 0.5%")
+        host_store_copies=2,
+        note="70B-shaped GQA; layer 0 in HBM, 79 layers in pinned host; hot set 0.5%; "
+             "two distinct K/V contents (request b holds request b % 2's)")
+    # (one KV head: 8 x 79 host layers are 20 GiB, every request keeps its own)
     cfgs["cfg5mqa"] = dataclasses.replace(
-        cfgs["cfg5"], name="cfg5mqa_b8_ctx65536_mqa64x1_budget4096_80layers", n_kv=1,
+        cfgs["cfg5"], name="cfg5mqa_b8_ctx65536_mqa64x1_budget4096_80layers", n_kv=1, host_store_copies=0,
         note="MQA variant of cfg5: all 64 query heads form one group")
     # MLA (DeepSeek-V2-Lite shapes: hidden 2048, 16 heads, latent 512 + rope
     # 64, 27 layers): the cfg2 setting (32K context, budget 2048, every layer's
@@ -210,6 +227,10 @@ def describe(cfg: Workload) -> dict:
         sum(cfg.host_layers(b) for b in range(cfg.B)),
         "sinks": cfg.n_sink, "recent": cfg.n_recent, "seed": cfg.seed,
         **({"attention": "mla", "latent_row": MLA_LATENT_ROW} if cfg.mla else {}),
+        **({"host_store_copies": cfg.host_store_copies,
+            "host_store_note": f"request b holds the LLM K/V contents of request b % {cfg.host_store_copies} "
+                               "(shared pinned stores); selections, loads and bytes moved are per request"}
+           if cfg.host_store_copies else {}),
     }
 
 

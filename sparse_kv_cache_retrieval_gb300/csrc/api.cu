@@ -3,7 +3,11 @@
 // neither the device nor the stream.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include "spc.h"
 #include "spc_device.cuh"
@@ -11,17 +15,39 @@
 
 namespace spc {
 
+constexpr int kMaxDevices = 64;
+
 int device_sm_count() {
-  static int cached_dev = -1, cached = 0;
+  static std::atomic<int> cached[kMaxDevices];   // 0 = not looked up yet
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (dev != cached_dev) {
+  if (dev < 0 || dev >= kMaxDevices) {
     int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    cached = n;
-    cached_dev = dev;
+    return cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess ? n : 0;
   }
-  return cached;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
+
+cudaError_t set_func_attr(const void* fn, cudaFuncAttribute attr, int value) {
+  // kernel attributes belong to a device's context: remember, per (kernel,
+  // attribute, device), the largest value set so far
+  static std::mutex mu;
+  static std::map<std::tuple<const void*, int, int>, int> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  const auto key = std::make_tuple(fn, (int)attr, dev);
+  auto it = done.find(key);
+  if (it != done.end() && it->second >= value) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, attr, value);
+  if (e == cudaSuccess) done[key] = value;
+  return e;
 }
 
 // ---------------------------------------------------------------- stream read

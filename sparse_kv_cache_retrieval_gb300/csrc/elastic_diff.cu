@@ -114,13 +114,9 @@ int elastic_diff_launch(const int32_t* selected, const int32_t* prev, int32_t* n
                         int32_t* load_slot, int32_t* load_pos, int32_t* n_load, int B, int n_kv,
                         int budget, int cap, void* stream) {
   const size_t smem = sizeof(uint32_t) * (size_t)((cap + 31) / 32) + sizeof(int) * (size_t)budget;
-  static size_t attr = 0;
-  if (smem > attr) {
-    if (cudaFuncSetAttribute(diff_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-      return SPC_ERR_CUDA;
-    attr = smem;
-  }
+  if (set_func_attr((const void*)diff_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
+    return SPC_ERR_CUDA;
   diff_kernel<<<B * n_kv, kDiffThreads, smem, static_cast<cudaStream_t>(stream)>>>(
       selected, prev, next, load_slot, load_pos, n_load, budget, cap);
   return cudaGetLastError() == cudaSuccess ? SPC_OK : SPC_ERR_CUDA;

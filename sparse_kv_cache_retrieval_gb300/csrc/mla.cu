@@ -542,13 +542,9 @@ int mla_attn_launch(const void* q, const void* Wuk, const void* Wuv, const spc_k
   aa.status = status; aa.B = B; aa.K = budget;
   mla_attn_plan(units, budget, &aa.n_split, &aa.tpc);
   aa.scale2 = scale * kLog2e;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(mla_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)MaSmem::total) !=
-        cudaSuccess)
-      return SPC_ERR_CUDA;
-    attr = true;
-  }
+  if (set_func_attr((const void*)mla_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                    (int)MaSmem::total) != cudaSuccess)
+    return SPC_ERR_CUDA;
   mla_attn_kernel<<<units * aa.n_split, kMaThreads, MaSmem::total, st>>>(aa);
   if (cudaGetLastError() != cudaSuccess) return SPC_ERR_CUDA;
   mla_out_kernel<<<dim3(units, kMH, kDv / kMoChunk), kMoThreads, 0, st>>>(part, static_cast<const uint16_t*>(Wuv), B,

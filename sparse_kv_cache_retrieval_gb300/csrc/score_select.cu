@@ -1247,20 +1247,13 @@ size_t score_select_workspace(int B, int H, int n_q, int n_kv, int cap) {
 template <int G>
 static cudaError_t launch_scan(const ScanArgs& sa, int grid, cudaStream_t st) {
   const size_t smem = kScanStages * kScanTileBytes + 2 * kScanStages * sizeof(uint64_t);
-  static bool attr = false;
   if constexpr (G <= 8) {
-    if (!attr) {
-      cudaError_t e = cudaFuncSetAttribute(scan_kernel_km<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return e;
-      attr = true;
-    }
+    cudaError_t e = set_func_attr((const void*)scan_kernel_km<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
     scan_kernel_km<G><<<grid, kScanKmThreads, smem, st>>>(sa);
   } else {
-    if (!attr) {
-      cudaError_t e = cudaFuncSetAttribute(scan_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return e;
-      attr = true;
-    }
+    cudaError_t e = set_func_attr((const void*)scan_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
     scan_kernel<G><<<grid, kScanThreads, smem, st>>>(sa);
   }
   return cudaGetLastError();
@@ -1270,13 +1263,8 @@ static cudaError_t launch_scan(const ScanArgs& sa, int grid, cudaStream_t st) {
 // 16; a size the device cannot co-schedule is halved.
 template <int BB>
 static int launch_proj(ProjArgs& pa, int n_tiles, int bz, cudaStream_t st) {
-  static bool cluster_attr = false;
-  static size_t smem_attr = 0;
-  if (!cluster_attr) {
-    if (cudaFuncSetAttribute(proj_kernel<BB>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-      return SPC_ERR_CUDA;
-    cluster_attr = true;
-  }
+  if (set_func_attr((const void*)proj_kernel<BB>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+    return SPC_ERR_CUDA;
   int S = pa.H / 256;
   S = S < 1 ? 1 : (S > kProjMaxSplit ? kProjMaxSplit : S);
   cudaLaunchConfig_t cfg{};
@@ -1290,11 +1278,8 @@ static int launch_proj(ProjArgs& pa, int n_tiles, int bz, cudaStream_t st) {
     pa.S = S;
     pa.Hc = (pa.H + S - 1) / S;
     const size_t smem = sizeof(float) * ((size_t)pa.Hc * BB + (kProjThreads / 32) * BB * kProjTile);
-    if (smem > smem_attr) {
-      if (cudaFuncSetAttribute(proj_kernel<BB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-        return SPC_ERR_CUDA;
-      smem_attr = smem;
-    }
+    if (set_func_attr((const void*)proj_kernel<BB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return SPC_ERR_CUDA;
     cfg.gridDim = dim3(n_tiles * S, 1, bz);
     cfg.dynamicSmemBytes = smem;
     at[0].val.clusterDim.x = S;
@@ -1315,13 +1300,8 @@ static int launch_proj(ProjArgs& pa, int n_tiles, int bz, cudaStream_t st) {
 // streams a long run of weight rows; split boundaries fall on multiples of 8
 // hidden rows.
 static int launch_proj_tc(ProjArgs& pa, int n_tiles, int bz, cudaStream_t st) {
-  static bool cluster_attr = false;
-  static size_t smem_attr = 0;
-  if (!cluster_attr) {
-    if (cudaFuncSetAttribute(proj_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-      return SPC_ERR_CUDA;
-    cluster_attr = true;
-  }
+  if (set_func_attr((const void*)proj_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+    return SPC_ERR_CUDA;
   const long long slots = 2LL * (device_sm_count() > 0 ? device_sm_count() : 1);
   int S = 1;
   while (S < kProjMaxSplit && 2 * S * 256 <= pa.H && (long long)n_tiles * bz * 2 * S <= slots) S *= 2;
@@ -1336,11 +1316,8 @@ static int launch_proj_tc(ProjArgs& pa, int n_tiles, int bz, cudaStream_t st) {
     pa.S = S;
     pa.Hc = ((pa.H + S - 1) / S + 7) / 8 * 8;
     const size_t smem = kPtcSmem;
-    if (smem > smem_attr) {
-      if (cudaFuncSetAttribute(proj_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-        return SPC_ERR_CUDA;
-      smem_attr = smem;
-    }
+    if (set_func_attr((const void*)proj_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return SPC_ERR_CUDA;
     cfg.gridDim = dim3(n_tiles * S, 1, bz);
     cfg.dynamicSmemBytes = smem;
     at[0].val.clusterDim.x = S;
@@ -1361,13 +1338,10 @@ static int launch_proj_tc(ProjArgs& pa, int n_tiles, int bz, cudaStream_t st) {
 template <int G>
 static int launch_select(SelArgs& sa, int nseg, cudaStream_t st) {
   const size_t smem = sizeof(SelSmem);
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(select_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
-        cudaFuncSetAttribute(select_kernel<G>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-      return SPC_ERR_CUDA;
-    attr = true;
-  }
+  if (set_func_attr((const void*)select_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+          cudaSuccess ||
+      set_func_attr((const void*)select_kernel<G>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+    return SPC_ERR_CUDA;
   int C = 1;
   while (C < kSelMaxCluster && nseg * C * 2 <= 2 * device_sm_count() && sa.cap / (C * 2) >= 512) C *= 2;
   cudaLaunchConfig_t cfg{};
@@ -1778,13 +1752,9 @@ int mla_score_select_launch(const MlaScoreSelectCall& c) {
     sa.tpc = (sa.total_tiles + sms - 1) / sms;
     if (sa.tpc < 1) sa.tpc = 1;
     const int grid = (sa.total_tiles + sa.tpc - 1) / sa.tpc;
-    static bool attr = false;
-    if (!attr) {
-      if (cudaFuncSetAttribute(mla_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMsSmem) !=
-          cudaSuccess)
-        return SPC_ERR_CUDA;
-      attr = true;
-    }
+    if (set_func_attr((const void*)mla_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMsSmem) !=
+        cudaSuccess)
+      return SPC_ERR_CUDA;
     mla_scan_kernel<<<grid, kMsThreads, kMsSmem, st>>>(sa);
     if (cudaGetLastError() != cudaSuccess) return SPC_ERR_CUDA;
   }

@@ -37,6 +37,8 @@
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include "spc_device.cuh"
 #include "spc_internal.h"
 
@@ -76,7 +78,13 @@ struct AttnArgs {
   int* status;
   int B, n_q, n_kv, K, n_split, C, cpc, n_chunks;
   float scale2;
+  long long wait_limit;   // clock cycles a bounded wait spends before it gives up
+  int starve;             // test builds only: the producer issues no copies
 };
+
+// Workspace layout: a 256-byte status area (its first int32 is the status
+// word), the per-(layer, request, KV head) merge counters, the split partials.
+constexpr size_t kAttnStatusBytes = 256;
 
 constexpr size_t round16(size_t x) { return (x + 15) & ~size_t(15); }
 
@@ -150,11 +158,18 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
     const uint16_t* kb = static_cast<const uint16_t*>(vw.k) + (size_t)g * vw.rows * kD;
     const uint16_t* vb = static_cast<const uint16_t*>(vw.v) + (size_t)g * vw.rows * kD;
     int it = 0;
+#ifdef SPC_TEST_HOOKS
+    // a starved launch: no copy is issued and no stage is published, so every
+    // consumer's first wait runs out (the path a lost copy would take)
+    const int c_end = a.starve ? c0 : c1;
+#else
+    const int c_end = c1;
+#endif
 #pragma unroll 1
-    for (int c = c0; c < c1; ++c, ++it) {
+    for (int c = c0; c < c_end; ++c, ++it) {
       const int s = it % kAttnStages;
       const uint32_t ph = (it / kAttnStages) & 1;
-      if (!mbar_wait_bounded(&empty[s], ph ^ 1, kAttnWait)) {
+      if (!mbar_wait_bounded(&empty[s], ph ^ 1, a.wait_limit)) {
         if (lane == 0) set_status(a.status, SPC_ERR_TIMEOUT);
         break;
       }
@@ -200,7 +215,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
     }
     // wait (bounded) for the copies still in flight before leaving
     for (int k = max(0, it - kAttnStages); k < it; ++k)
-      mbar_wait_bounded(&full[k % kAttnStages], (k / kAttnStages) & 1, kAttnWait);
+      mbar_wait_bounded(&full[k % kAttnStages], (k / kAttnStages) & 1, a.wait_limit);
     __syncwarp();
   } else {
     // ================= consumers
@@ -245,7 +260,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
     for (int c = c0; c < c1; ++c, ++it) {
       const int s = it % kAttnStages;
       const uint32_t ph = (it / kAttnStages) & 1;
-      if (!dead && !mbar_wait_bounded(&full[s], ph, kAttnWait)) {
+      if (!dead && !mbar_wait_bounded(&full[s], ph, a.wait_limit)) {
         if (lane == 0) set_status(a.status, SPC_ERR_TIMEOUT);
         dead = true;
       }
@@ -584,18 +599,21 @@ size_t attn_workspace(int n_layers, int B, int n_q, int n_kv, int budget) {
   const size_t nseg = (size_t)n_layers * B * n_kv;
   const size_t cnt = (nseg * sizeof(uint32_t) + 255) & ~size_t(255);
   const size_t part = ns > 1 ? nseg * ns * (size_t)(n_q / n_kv) * kPartStride * sizeof(float) : 0;
-  return cnt + part;
+  return kAttnStatusBytes + cnt + part;
 }
+
+#ifdef SPC_TEST_HOOKS
+// Test builds only: the next `g_starve_calls` launches run starved, with a
+// wait limit of `g_starve_wait` clock cycles.
+static std::atomic<int> g_starve_calls{0};
+static std::atomic<long long> g_starve_wait{0};
+#endif
 
 template <int G>
 static cudaError_t launch_attn(const AttnArgs& aa, int nseg, cudaStream_t st) {
   const size_t smem = AttnSmem<G>::total;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  cudaError_t e = set_func_attr((const void*)attn_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)(nseg * aa.n_split * aa.C));
   cfg.blockDim = dim3(kAttnThreads);
@@ -621,10 +639,23 @@ int attn_launch(const void* q, const spc_kv_view* views, const int32_t* selected
   aa.slot_pos = slot_pos;
   aa.out = out;
   const size_t nseg = (size_t)n_layers * B * n_kv;
-  aa.counters = static_cast<uint32_t*>(workspace);
-  aa.part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                     ((nseg * sizeof(uint32_t) + 255) & ~size_t(255)));
-  aa.status = nullptr;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  aa.status = reinterpret_cast<int*>(ws);
+  aa.counters = reinterpret_cast<uint32_t*>(ws + kAttnStatusBytes);
+  aa.part = reinterpret_cast<float*>(ws + kAttnStatusBytes + ((nseg * sizeof(uint32_t) + 255) & ~size_t(255)));
+  aa.wait_limit = kAttnWait;
+  aa.starve = 0;
+#ifdef SPC_TEST_HOOKS
+  {
+    int n = g_starve_calls.load();
+    while (n > 0 && !g_starve_calls.compare_exchange_weak(n, n - 1)) {
+    }
+    if (n > 0) {
+      aa.starve = 1;
+      aa.wait_limit = g_starve_wait.load();
+    }
+  }
+#endif
   aa.B = B; aa.n_q = n_q; aa.n_kv = n_kv; aa.K = budget;
   attn_plan(n_layers, B, n_kv, budget, &aa.C, &aa.n_split, &aa.cpc, &aa.n_chunks);
   aa.scale2 = scale * kLog2e;
@@ -683,10 +714,10 @@ int attn_noalloc_launch(const void* q, const spc_kv_view* views, const int32_t* 
     return SPC_ERR_WORKSPACE;
   void* scratch = attn_noalloc_scratch_address();
   if (!scratch) return SPC_ERR_CUDA;
-  // the split-merge counters must start at zero; the partials are always
-  // written before they are read
+  // the status word and the split-merge counters must start at zero; the
+  // partials are always written before they are read
   const size_t nseg = (size_t)n_layers * B * n_kv;
-  if (cudaMemsetAsync(scratch, 0, nseg * sizeof(uint32_t), static_cast<cudaStream_t>(stream)) !=
+  if (cudaMemsetAsync(scratch, 0, kAttnStatusBytes + nseg * sizeof(uint32_t), static_cast<cudaStream_t>(stream)) !=
       cudaSuccess)
     return SPC_ERR_CUDA;
   return attn_launch(q, views, selected, slot_pos, n_layers, B, n_q, n_kv, budget, scale, out,
@@ -694,3 +725,17 @@ int attn_noalloc_launch(const void* q, const spc_kv_view* views, const int32_t* 
 }
 
 }  // namespace spc
+
+#ifdef SPC_TEST_HOOKS
+// Test builds only (compiled with -DSPC_TEST_HOOKS into a separate library,
+// never into libspc.so): the next `calls` launches of the GQA attention kernel
+// run starved -- the producer issues no copies -- and their bounded waits give
+// up after `wait_cycles` clock cycles, so a test can check that a wait that
+// runs out records SPC_ERR_TIMEOUT in the status word and returns.
+extern "C" int spc_test_starve_attention(int calls, long long wait_cycles) {
+  if (calls < 0 || wait_cycles < 1) return SPC_ERR_INVALID_ARG;
+  spc::g_starve_wait.store(wait_cycles);
+  spc::g_starve_calls.store(calls);
+  return SPC_OK;
+}
+#endif

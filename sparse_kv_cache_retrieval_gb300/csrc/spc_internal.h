@@ -1,12 +1,20 @@
 // Host-side declarations shared by the translation units of libspc.
 #pragma once
 
+#include <cuda_runtime.h>
+
 #include <cstddef>
 #include <cstdint>
 
 #include "spc.h"
 
 namespace spc {
+
+// Sets a kernel attribute on the current device unless a value at least as
+// large is already set there (dynamic shared memory size, or a 0/1 flag).
+// Kernel attributes belong to a device's context, so the record is kept per
+// (kernel, attribute, device); safe to call from several host threads.
+cudaError_t set_func_attr(const void* fn, cudaFuncAttribute attr, int value);
 
 struct ScoreSelectCall {
   const void* x;

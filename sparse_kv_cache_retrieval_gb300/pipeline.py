@@ -185,7 +185,15 @@ class DecodePipeline:
                     layers.append(_dev_u16(buf[0], dev))
                 del buf
             self.hbm.append(layers)
-            if L - s0 > 0:
+            src = cfg.kv_source(b)
+            if L - s0 > 0 and src != b and not self.adaptive and not self.mla and \
+                    self.store_base[src] == s0 and self.gpu_layers[src] == ng:
+                # request b holds request src's K/V contents: share its pinned
+                # store (the gather still reads b's own positions into b's slots)
+                self.host_stores.append(self.host_stores[src])
+                self.slots.append(torch.zeros((L - s0, 2, n_kv, K, d), dtype=torch.int16, device=dev))
+                self._store_dev.append(self._store_dev[src])
+            elif L - s0 > 0:
                 # position-major [cap][n_kv][layers][2][d] (MLA: [cap][layers][576]):
                 # one (position, head) holds every stored layer's row(s) in one host page
                 if self.mla:

@@ -21,6 +21,8 @@ are not available here):
     cosine ~1/sqrt(G) with that sum, so the planted logits start about gamma
     (= 8) standard deviations above the rest for every group size;
   * LLM K/V rows ~ N(0, I_d) for every layer and position up to the capacity;
+    a workload with ``host_store_copies`` = c > 0 draws c distinct contents
+    and request b holds those of request b % c (``Workload.kv_source``);
   * LLM query per layer q'_{l,0} ~ N(0, I_d) rescaled to norm sqrt(d), then the
     same drift as the head input.
 """
@@ -48,8 +50,12 @@ def rng_for(seed: int, *tags: int) -> np.random.Generator:
 def to_bf16_bits(a: np.ndarray) -> np.ndarray:
     """fp32 -> bf16 bit pattern, round to nearest even (finite inputs)."""
     u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
-    bias = ((u >> np.uint32(16)) & np.uint32(1)) + np.uint32(0x7FFF)
-    return ((u + bias) >> np.uint32(16)).astype(np.uint16)
+    w = u >> np.uint32(16)
+    w &= np.uint32(1)
+    w += np.uint32(0x7FFF)
+    w += u
+    w >>= np.uint32(16)
+    return w.astype(np.uint16)
 
 
 def bf16_bits_to_f32(u: np.ndarray) -> np.ndarray:
@@ -68,6 +74,18 @@ def _normal_bf16_into(out: np.ndarray, rng: np.random.Generator, scale: float = 
         if scale != 1.0:
             v *= np.float32(scale)
         flat[s:s + n] = to_bf16_bits(v)
+
+
+def _parallel(jobs, work, threads: Optional[int] = None) -> None:
+    """Run work(job) for every job on a thread pool (numpy's generators and
+    array operations release the GIL); jobs write disjoint outputs."""
+    threads = threads or min(16, os.cpu_count() or 1)
+    if threads <= 1 or len(jobs) <= 1:
+        for j in jobs:
+            work(j)
+        return
+    with cf.ThreadPoolExecutor(threads) as ex:
+        list(ex.map(work, jobs))
 
 
 def _drift(prev: np.ndarray, eps: np.ndarray, rho: float, norm: float) -> np.ndarray:
@@ -121,14 +139,16 @@ def make_inputs(cfg: Workload, steps: Optional[int] = None, n_layers: Optional[i
                 q = _drift(q, r.standard_normal((L, n_q, d)), cfg.rho[b], np.sqrt(d))
             q_llm[t, :, b] = to_bf16_bits(q.astype(np.float32))
 
-    # distilled-model key cache with planted hot positions
+    # distilled-model key cache with planted hot positions (every (b, g) has
+    # its own stream, so drawing them on several threads gives the same bits)
     K = np.zeros((B, n_kv, cap, d), np.uint16)
+    _parallel([(b, g) for b in range(B) for g in range(n_kv)],
+              lambda j: _normal_bf16_into(K[j[0], j[1], :int(cfg.lens[j[0]])],
+                                          rng_for(cfg.seed, _TAG_KDLM, j[0], j[1])))
     Wq_f = bf16_bits_to_f32(Wq)
     hot = []
     for b in range(B):
         Lb = int(cfg.lens[b])
-        for g in range(n_kv):
-            _normal_bf16_into(K[b, g, :Lb], rng_for(cfg.seed, _TAG_KDLM, b, g))
         # initial query direction of every group, only to aim the planted keys
         xq = bf16_bits_to_f32(xs[0, b]) @ Wq_f                       # [n_q*d]
         u = xq.reshape(n_kv, G, d).sum(axis=1)
@@ -157,19 +177,14 @@ def fill_llm_kv(cfg: Workload, b: int, layer0: int, out: np.ndarray, threads: Op
     whichever store (HBM or pinned host) it lands in.
     """
     nl = out.shape[0]
+    src = cfg.kv_source(b)
     jobs = [(l, kv, g) for l in range(nl) for kv in range(2) for g in range(cfg.n_kv)]
 
     def work(job):
         l, kv, g = job
-        _normal_bf16_into(out[l, kv, g], rng_for(cfg.seed, _TAG_KV, b, layer0 + l, kv, g))
+        _normal_bf16_into(out[l, kv, g], rng_for(cfg.seed, _TAG_KV, src, layer0 + l, kv, g))
 
-    threads = threads or min(16, os.cpu_count() or 1)
-    if threads <= 1 or len(jobs) == 1:
-        for j in jobs:
-            work(j)
-        return
-    with cf.ThreadPoolExecutor(threads) as ex:
-        list(ex.map(work, jobs))
+    _parallel(jobs, work, threads)
 
 
 def fill_llm_kv_store(cfg: Workload, b: int, layer_lo: int, layer_hi: int, store: np.ndarray,
@@ -179,21 +194,16 @@ def fill_llm_kv_store(cfg: Workload, b: int, layer_lo: int, layer_hi: int, store
     layer l, K or V at store[p, g, l - store_layer0, kv]); same values as
     ``fill_llm_kv`` gives the layer-major layout."""
     rows = store.shape[0]
+    src = cfg.kv_source(b)
     jobs = [(l, kv, g) for l in range(layer_lo, layer_hi) for kv in range(2) for g in range(cfg.n_kv)]
 
     def work(job):
         l, kv, g = job
         tmp = np.empty((rows, cfg.d), np.uint16)
-        _normal_bf16_into(tmp, rng_for(cfg.seed, _TAG_KV, b, l, kv, g))
+        _normal_bf16_into(tmp, rng_for(cfg.seed, _TAG_KV, src, l, kv, g))
         store[:, g, l - store_layer0, kv, :] = tmp
 
-    threads = threads or min(16, os.cpu_count() or 1)
-    if threads <= 1 or len(jobs) <= 1:
-        for j in jobs:
-            work(j)
-        return
-    with cf.ThreadPoolExecutor(threads) as ex:
-        list(ex.map(work, jobs))
+    _parallel(jobs, work, threads)
 
 
 # ------------------------------------------------------------------ MLA

@@ -25,3 +25,12 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    from tests import swap_log
+    if not swap_log.COUNTS:
+        return
+    terminalreporter.write_sep("-", "tie-band swaps (GPU vs oracle selections; allowed within 2e-3 of the K-th score)")
+    for tid, (sw, checked, heads) in sorted(swap_log.COUNTS.items()):
+        terminalreporter.write_line(f"{tid}: {sw} swapped positions, {heads} of {checked} selections with a swap")

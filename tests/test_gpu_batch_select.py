@@ -13,6 +13,8 @@ import oracle.spc_oracle as O
 from oracle.checks import selection_within_tie_band
 from sparse_kv_cache_retrieval_gb300 import binding as spc
 
+from tests import swap_log  # noqa: E402
+
 pytestmark = pytest.mark.gpu
 
 
@@ -61,9 +63,10 @@ def test_batch_select_one_group_equals_the_head_level_rule():
 def test_batch_level_pipeline_chain():
     """The decode step with batch-level retrieval against the oracle's own
     chain using the batch-level rule: the same set for every KV head, within
-    the tie band of the oracle's merged scores; while the sets agree, slot maps
-    match and attention is within the bar; the head-level selection of the
-    same step is kept beside it and matches the head-level rule."""
+    the tie band of the oracle's merged scores; the chain continues from the
+    GPU's set, so slot maps match and attention is within the bar at every
+    step; the head-level selection of the same step is kept beside it and
+    matches the head-level rule."""
     import math
     from oracle.checks import ATTN_ATOL
     from sparse_kv_cache_retrieval_gb300.configs import CONFIGS, scaled
@@ -84,10 +87,26 @@ def test_batch_level_pipeline_chain():
         return [[O.batch_level_select(ss[b], cfg.budget, cfg.n_sink, cfg.n_recent)] * cfg.n_kv
                 for b in range(cfg.B)]
 
+    tid = "batch-level chain"
+
+    def adopt(g, osel, oss, where):
+        # the GPU's batch-level set, within the tie band of the oracle's merged
+        # scores, is the one the chain continues from
+        out = []
+        for b in range(cfg.B):
+            merged = np.max(np.stack(oss[b]), axis=0)
+            ok, sw, msg = selection_within_tie_band(g[b, 0], osel[b][0], merged, cfg.budget, cfg.n_sink,
+                                                    cfg.n_recent)
+            assert ok, f"{where}: {msg}"
+            swap_log.record(tid, sw, 1, 1 if sw else 0)
+            for kv in range(cfg.n_kv):
+                assert np.array_equal(g[b, kv], g[b, 0])
+            out.append([g[b, 0][g[b, 0] >= 0].astype(np.int64)] * cfg.n_kv)
+        return out
+
     _, _, _, oss, ohead = ost.score_select(inp.x[0], inp.Wq, inp.Wk, cfg.n_q, False)
-    ost.diff_and_gather(batch_sel(oss))
     pipe.prologue()
-    diverged = False
+    ost.diff_and_gather(adopt(pipe.selected[0].cpu().numpy(), batch_sel(oss), oss, "prologue"))
     for t in range(3):
         pn = (t + 1) % 2
         pipe.step(t)
@@ -95,20 +114,13 @@ def test_batch_level_pipeline_chain():
         torch.cuda.synchronize()
         _, _, _, oss, ohead = ost.score_select(inp.x[t + 1], inp.Wq, inp.Wk, cfg.n_q, False)
         oout = ost.attention(inp.q_llm[t, :L], 1 / math.sqrt(cfg.d))
-        osel = batch_sel(oss)
-        ost.diff_and_gather(osel)
         g = pipe.selected[pn].cpu().numpy()
         gh = pipe.selected_head[pn].cpu().numpy()
+        ost.diff_and_gather(adopt(g, batch_sel(oss), oss, f"t={t}"))
         for b in range(cfg.B):
-            merged = np.max(np.stack(oss[b]), axis=0)
-            ok, sw, msg = selection_within_tie_band(g[b, 0], osel[b][0], merged, cfg.budget, cfg.n_sink, cfg.n_recent)
-            assert ok, f"t={t}: {msg}"
             for kv in range(cfg.n_kv):
-                assert np.array_equal(g[b, kv], g[b, 0])
                 okh, _, msgh = selection_within_tie_band(gh[b, kv], ohead[b][kv], oss[b][kv], cfg.budget,
                                                          cfg.n_sink, cfg.n_recent)
                 assert okh, f"t={t} head-level kv={kv}: {msgh}"
-            if not diverged:
-                assert float(np.abs(pipe.out.cpu().numpy()[:, b] - oout[:, b]).max()) <= ATTN_ATOL
-                assert np.array_equal(pipe.slot_pos[pn].cpu().numpy()[b], ost.slot_pos[b])
-            diverged |= sw > 0
+            assert float(np.abs(pipe.out.cpu().numpy()[:, b] - oout[:, b]).max()) <= ATTN_ATOL
+            assert np.array_equal(pipe.slot_pos[pn].cpu().numpy()[b], ost.slot_pos[b])

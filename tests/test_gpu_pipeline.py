@@ -1,11 +1,14 @@
 """GPU parity of the whole decode step (two streams, all four calls) against
-the oracle's own chain, plus graph-vs-eager and host-I/O equivalence.
+the oracle, plus graph-vs-eager and host-I/O equivalence.
 
-The oracle runs its own selections; while the GPU and oracle selections are
-identical, load lists and slot maps must match bit for bit and attention
-within tolerance. A tie-band swap (allowed, counted) makes the two slot maps
-diverge for that KV head from then on; its later steps are checked on sets
-(selection band, slot contents, attention) only.
+Every step the oracle computes its own selection, and the GPU's must equal
+it up to tie-band swaps (positions whose oracle scores lie within 2e-3 of the
+oracle's K-th score; counted and reported in the terminal summary). Several
+selections are then correct, so the chain continues from the one the GPU
+made: the oracle's diff, gather and attention take it as their input, and the
+GPU's load lists, slot maps and slot contents must match the oracle's bit for
+bit and its attention within tolerance, for every KV head at every step (a
+swap never switches a check off).
 """
 import math
 
@@ -14,10 +17,11 @@ import pytest
 import torch
 
 import oracle.spc_oracle as O
-from oracle.checks import ATTN_ATOL, selection_within_tie_band
+from oracle.checks import ATTN_ATOL
 from sparse_kv_cache_retrieval_gb300.configs import CONFIGS, scaled
 from sparse_kv_cache_retrieval_gb300.pipeline import DecodePipeline
 from sparse_kv_cache_retrieval_gb300.synth import fill_llm_kv, make_inputs
+from tests import swap_log
 
 pytestmark = pytest.mark.gpu
 
@@ -31,68 +35,52 @@ def oracle_stores(cfg, L):
     return stores
 
 
-def run_chain(cfg, steps, L, layers_per_launch=1, on_step=None, **pipe_kw):
+def run_chain(cfg, steps, L, layers_per_launch=1, on_step=None, test_id=None, **pipe_kw):
+    tid = test_id or cfg.name
     inp = make_inputs(cfg, steps=steps, n_layers=L)
     pipe = DecodePipeline(cfg, inp, n_layers=L, layers_per_launch=layers_per_launch, **pipe_kw)
     stores = oracle_stores(cfg, L)
     ost = O.DecodeState(inp.K_dlm, inp.lens, stores, pipe.gpu_layers, cfg.budget, cfg.n_sink,
                         cfg.n_recent)
     _, _, _, oss, osel = ost.score_select(inp.x[0], inp.Wq, inp.Wk, cfg.n_q, append=False)
-    ost.diff_and_gather(osel)
     pipe.prologue()
-    diverged = np.zeros((cfg.B, cfg.n_kv), bool)
     swaps_total = 0
-    # the prologue's selection S_0 is held to the same tie band; a head whose
-    # S_0 swapped a tie attends over a (validly) different set from step 0 on
-    gsel0 = pipe.selected[0].cpu().numpy()
-    for b in range(cfg.B):
-        for g in range(cfg.n_kv):
-            ok, sw, msg = selection_within_tie_band(gsel0[b, g], osel[b][g], oss[b][g], cfg.budget,
-                                                    cfg.n_sink, cfg.n_recent)
-            assert ok, f"prologue b={b} g={g}: {msg}"
-            swaps_total += sw
-            diverged[b, g] |= sw > 0
+    # the prologue's selection S_0 is held to the same tie band; the chain
+    # continues from the GPU's (valid) choice
+    sel, sw = swap_log.check_selection(tid, pipe.selected[0].cpu().numpy(), osel, oss, cfg.budget, cfg.n_sink,
+                                       cfg.n_recent, "prologue")
+    swaps_total += sw
+    ost.diff_and_gather(sel)
     scale = 1 / math.sqrt(cfg.d)
     for t in range(steps):
         p, pn = t % 2, (t + 1) % 2
-        S_t = [[s.copy() for s in row] for row in ost.S]
         pipe.step(t)
         pipe.join()
         torch.cuda.synchronize()
         if on_step is not None:
             on_step(t, pipe)
         _, _, _, oss, osel = ost.score_select(inp.x[t + 1], inp.Wq, inp.Wk, cfg.n_q, append=cfg.append)
+        # attention of step t runs over S_t, the selection the previous step adopted
         oout = ost.attention(inp.q_llm[t, :L], scale)
-        loads = ost.diff_and_gather(osel)
         gsel = pipe.selected[pn].cpu().numpy()
+        sel, sw = swap_log.check_selection(tid, gsel, osel, oss, cfg.budget, cfg.n_sink, cfg.n_recent, f"t={t}")
+        swaps_total += sw
+        loads = ost.diff_and_gather(sel)
         gslot = pipe.slot_pos[pn].cpu().numpy()
         gnl = pipe.n_load[pn].cpu().numpy()
         gls = pipe.load_slot[pn].cpu().numpy()
         glp = pipe.load_pos[pn].cpu().numpy()
         gout = pipe.out.cpu().numpy()
         assert pipe.len.cpu().numpy().tolist() == ost.lens
+        e = np.abs(gout - oout)
+        assert e.max() <= ATTN_ATOL, f"t={t}: attention max err {e.max():.3g}"
+        assert np.all(e <= 2e-5 + 1e-4 * np.abs(oout)), f"t={t}: attention"
         for b in range(cfg.B):
             for g in range(cfg.n_kv):
-                ok, sw, msg = selection_within_tie_band(gsel[b, g], osel[b][g], oss[b][g], cfg.budget,
-                                                        cfg.n_sink, cfg.n_recent)
-                assert ok, f"t={t} b={b} g={g}: {msg}"
-                swaps_total += sw
-                if sw:
-                    diverged[b, g] = True
-                # attention of step t used S_t: compare where the sets agree
-                G = cfg.G
-                if not diverged[b, g] or sw == 0:
-                    for l in range(L):
-                        e = np.abs(gout[l, b, g * G:(g + 1) * G] - oout[l, b, g * G:(g + 1) * G])
-                        if not diverged[b, g]:
-                            assert e.max() <= ATTN_ATOL
-                            assert np.all(e <= 2e-5 + 1e-4 * np.abs(oout[l, b, g * G:(g + 1) * G]))
-                if not diverged[b, g]:
-                    ls, lp = loads[b][g]
-                    assert gnl[b, g] == lp.size, f"t={t} n_load"
-                    assert np.array_equal(glp[b, g, :lp.size], lp) and np.array_equal(gls[b, g, :ls.size], ls)
-                    assert np.array_equal(gslot[b, g], ost.slot_pos[b, g])
-                assert set(gslot[b, g][gslot[b, g] >= 0].tolist()) == set(gsel[b, g][gsel[b, g] >= 0].tolist())
+                ls, lp = loads[b][g]
+                assert gnl[b, g] == lp.size, f"t={t} b={b} g={g} n_load"
+                assert np.array_equal(glp[b, g, :lp.size], lp) and np.array_equal(gls[b, g, :ls.size], ls)
+                assert np.array_equal(gslot[b, g], ost.slot_pos[b, g]), f"t={t} b={b} g={g} slot map"
         # slots hold the rows their slot map names, byte for byte (host layers)
         for b in range(cfg.B):
             if pipe.host_slots(b) is None:
@@ -102,14 +90,14 @@ def run_chain(cfg, steps, L, layers_per_launch=1, on_step=None, **pipe_kw):
             for g in range(cfg.n_kv):
                 held = gslot[b, g]
                 idx = np.nonzero(held >= 0)[0]
-                assert np.array_equal(sl[:, :, g, idx], stores[b][h0:, :, g, held[idx]])
+                assert np.array_equal(sl[:, :, g, idx], stores[b][h0:, :, g, held[idx]]), \
+                    f"t={t} b={b} g={g} slot contents"
     return swaps_total, pipe
 
 
 def test_chain_cfg1_full_size():
     cfg = CONFIGS["cfg1"]
-    swaps, _ = run_chain(cfg, cfg.steps, cfg.n_layers)
-    print("cfg1 tie-band swaps:", swaps)
+    run_chain(cfg, cfg.steps, cfg.n_layers)
 
 
 def test_chain_cfg4a_append_select_all_then_topk():
@@ -145,6 +133,18 @@ def test_chain_cfg5_70b_shape_hbm_and_host_layers():
     cfg = scaled(CONFIGS["cfg5"], n_layers=2, steps=1)
     assert cfg.gpu_layers == (1,) * 8
     run_chain(cfg, 1, 2, layers_per_launch=2)
+
+
+def test_chain_shared_host_stores():
+    # cfg5's layout on a small context: requests b and b + 2 hold the same
+    # K/V contents and share one pinned store, yet each selects, diffs and
+    # gathers its own positions into its own slots
+    cfg = scaled(CONFIGS["cfg5"], B=4, lens=(3000, 2900, 3000, 2800), n_layers=3, steps=2, budget=512, H=1024)
+    assert cfg.host_store_copies == 2 and cfg.kv_source(2) == 0 and cfg.kv_source(3) == 1
+    swaps, pipe = run_chain(cfg, 2, 3, layers_per_launch=2)
+    assert pipe.host_stores[2] is pipe.host_stores[0] and pipe.host_stores[3] is pipe.host_stores[1]
+    assert pipe.host_stores[1] is not pipe.host_stores[0]
+    assert pipe.slots[2] is not pipe.slots[0]
 
 
 def test_chain_cfg5_mqa_full_shape():

@@ -12,6 +12,7 @@ import torch
 
 from oracle.checks import bf16_ulp_distance
 from sparse_kv_cache_retrieval_gb300.configs import CONFIGS
+from tests import swap_log
 from tests.gpu_cases import ScoreRun, check_score_call, oracle_score, workload
 
 pytestmark = pytest.mark.gpu
@@ -127,7 +128,7 @@ def test_score_select_full_size_configs(key):
         cfg = cfg.__class__(**{**cfg.__dict__, "B": 2, "lens": cfg.lens[:2], "rho": cfg.rho[:2],
                                "hot": cfg.hot[:2], "gpu_layers": cfg.gpu_layers[:2]})
     swaps = _one_call(cfg, t=1 if cfg.append else 0, append=cfg.append)
-    print(f"{key}: tie-band swaps {swaps}")
+    swap_log.record(f"score_select full size {key}", swaps, cfg.B * cfg.n_kv, 0)
 
 
 def test_stages_one_by_one_equal_the_fused_call():

@@ -8,7 +8,8 @@ from a fixed scratch area inside the library. These checks call it through
 the C ABI twice in a row, on different inputs, and compare each result with
 the regular entry point's (same kernel, caller workspace), within the
 attention tolerance the other tests use. A second call must not be disturbed
-by what the first one left in the shared area.
+by what the first one left in the shared area. Both results are also held
+to the CPU oracle's attention on the same rows.
 
 This file is named to be collected last.
 """
@@ -18,6 +19,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle.spc_oracle as O
 from oracle.checks import ATTN_ATOL
 from sparse_kv_cache_retrieval_gb300 import binding as spc
 
@@ -47,6 +49,22 @@ def _case(seed, L, B, n_q, n_kv, K, cap, use_slots):
             sel[b, g, :m] = pos
             slot[b, g, rng.choice(K, size=m, replace=False)] = pos
     return keep, views, q, torch.from_numpy(sel).to(DEV), torch.from_numpy(slot).to(DEV)
+
+
+def _oracle(case, L, B, n_q, n_kv, use_slots):
+    """The oracle's attention on the case's bits: the rows a view keeps are
+    the slots holding a position (use_slots) or the selected positions."""
+    keep, views, q, sel, slot = case
+    qb = q.cpu().numpy().view(np.uint16)
+    sel_h, slot_h = sel.cpu().numpy(), slot.cpu().numpy()
+    want = np.zeros((L, B, n_q, 128), np.float64)
+    for l in range(L):
+        for b in range(B):
+            kv = keep[l * B + b].cpu().numpy().view(np.uint16)
+            rows = [np.nonzero(slot_h[b, g] >= 0)[0] if use_slots else sel_h[b, g][sel_h[b, g] >= 0]
+                    for g in range(n_kv)]
+            want[l, b] = O.sparse_attention(qb[l, b], kv[0], kv[1], rows, 1 / math.sqrt(128))
+    return want
 
 
 def _with_workspace(case, L, B, n_q, n_kv, K):
@@ -84,6 +102,10 @@ def test_noalloc_matches_the_workspace_entry_point_on_two_calls(L, B, n_q, n_kv,
         err = (got - ref).abs()
         assert float(err.max()) <= ATTN_ATOL
         assert bool(torch.all(err <= 2e-5 + 1e-4 * ref.abs()))
+        want = _oracle(case, L, B, n_q, n_kv, use_slots)
+        e = np.abs(got.cpu().numpy() - want)
+        assert e.max() <= ATTN_ATOL
+        assert np.all(e <= 2e-5 + 1e-4 * np.abs(want)), f"max err vs oracle {e.max():.3g}"
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
