@@ -57,6 +57,9 @@ def parse():
                     help="attention/gather layer chunk (default: the workload's, 16 for GQA, all layers for MLA)")
     ap.add_argument("--layers", type=int, default=None,
                     help="LLM layers to run (default: the workload's); the JSON line states it")
+    ap.add_argument("--context", type=int, default=None,
+                    help="context length of every request (default: the workload's), e.g. a smaller case of "
+                         "the same kernels for a profiler; the JSON line states it")
     ap.add_argument("--gather-streams", type=int, default=1, choices=[1, 2])
     ap.add_argument("--front-after", choices=("select", "attention"), default=None,
                     help="issue the next step's projection and key scan after this step's select or after its "
@@ -71,7 +74,10 @@ def parse():
     ap.add_argument("--oracle-sample-steps", type=int, default=2)
     ap.add_argument("--oracle-sample-layers", type=int, default=2)
     ap.add_argument("--profile", action="store_true",
-                    help="hot path only for a profiler: prologue, then --steps eager steps")
+                    help="hot path only for a profiler: prologue, then --steps eager steps (an adaptive workload "
+                         "such as c3 offloads layers as its context crosses the thresholds)")
+    ap.add_argument("--host-io", action="store_true",
+                    help="with --profile: every step copies its inputs from and its outputs to pinned host memory")
     ap.add_argument("--c3", action="store_true",
                     help="adaptive memory management on a growing context: per-step latency of the "
                          "progressive per-layer offload vs offloading every layer at once")
@@ -632,6 +638,10 @@ def our_arm(args, rank, world, local):
 
     torch.cuda.set_device(local)
     cfg = CONFIGS[args.config]
+    if args.context is not None:
+        from sparse_kv_cache_retrieval_gb300.configs import scaled
+        cfg = scaled(cfg, lens=(args.context,) * cfg.B, name_suffix=f"_ctx{args.context}")
+        args.no_cpu_baseline = True     # the oracle leg times the named workloads only
     W, K = max(3, args.warmup), args.steps
     log("generating inputs")
     n_layers = cfg.n_layers if args.layers is None else max(1, min(args.layers, cfg.n_layers))
@@ -641,9 +651,11 @@ def our_arm(args, rank, world, local):
         args.layers_per_launch = cfg.layers_per_launch
     if args.front_after is None:
         args.front_after = cfg.front_after
+    adaptive = args.profile and cfg.kv_bytes is not None
     pipe = DecodePipeline(cfg, inp, n_layers=n_layers, layers_per_launch=args.layers_per_launch, timing=False,
                           gather_streams=args.gather_streams, elastic=not args.no_elastic,
-                          front_after=args.front_after, retrieval=args.retrieval)
+                          front_after=args.front_after, retrieval=args.retrieval,
+                          kv_bytes=cfg.kv_bytes if adaptive else None, host_io=args.profile and args.host_io)
     log("pipeline ready")
     if args.profile:
         # the launch sequence a profiler sees: the prologue (one whole-selection
@@ -658,7 +670,7 @@ def our_arm(args, rank, world, local):
             torch.cuda.synchronize()
             rows.append(int(pipe.n_load[(t + 1) % 2].cpu().numpy().astype(np.int64).sum()))
         torch.cuda.synchronize()
-        print(json.dumps({"profile_steps": K, "workload": cfg.name,
+        print(json.dumps({"profile_steps": K, "workload": cfg.name, "offloads": pipe.offload_log,
                           "launches_per_step": sum(kernels_per_call(cfg, args.retrieval)[k]
                                                    for k in ("project", "key_scan", "select", "diff")) +
                           len(pipe.chunks) * (kernels_per_call(cfg, args.retrieval)["attention"] + 1),

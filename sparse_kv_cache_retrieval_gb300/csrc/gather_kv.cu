@@ -17,7 +17,7 @@
 // (lanes 0-15) and V row (lanes 16-31), 512 contiguous bytes, with up to 16
 // layers in flight (a whole 16-layer chunk's run in one round trip); the
 // (position, slot) pair and the segment search are done once per load. A
-// small grid (one CTA of 512 threads per 8 SMs) keeps about 2.5 MB in
+// small grid (two warps per SM on average, in CTAs of 4 warps) keeps about 2.5 MB in
 // flight, enough for the link, and leaves the rest of the GPU to the
 // kernels that run beside the gather on the other streams (attention, key
 // scan). The flattened load index maps back to (request, KV head, i) through
@@ -29,8 +29,15 @@
 
 namespace spc {
 
+// CTAs of 4 warps (16K registers), two warps per SM on average, i.e. one CTA
+// on every other SM. Measured on GB300 (70B-shaped workload, 80 layers, gathers
+// of ~380 MB beside the attention kernel; 32K-context workload, gathers of
+// ~12 MB beside the key scan): 512-thread CTAs, each needing a whole register
+// file and so waiting for an SM to drain, gave 10.8-10.9 ms/step and 130 us/step;
+// 128-thread CTAs 9.4-9.6 ms and 150 us; 64-thread CTAs on every SM 9.7-10.1 ms
+// and 210 us (host-link loads on every SM slowed the key scan beside them).
 #ifndef SPC_GATHER_THREADS
-#define SPC_GATHER_THREADS 512
+#define SPC_GATHER_THREADS 128
 #endif
 constexpr int kGatherThreads = SPC_GATHER_THREADS;
 #ifndef SPC_GATHER_UNROLL
@@ -38,10 +45,10 @@ constexpr int kGatherThreads = SPC_GATHER_THREADS;
 #endif
 constexpr int kGatherUnroll = SPC_GATHER_UNROLL;
 constexpr int kGatherMaxSeg = 1024;
-#ifndef SPC_GATHER_SMS_PER_CTA
-#define SPC_GATHER_SMS_PER_CTA 8
+#ifndef SPC_GATHER_WARPS_PER_SM
+#define SPC_GATHER_WARPS_PER_SM 2   // ~2.5 MB in flight on 152 SMs, enough for the host link
 #endif
-constexpr int kGatherSmsPerCta = SPC_GATHER_SMS_PER_CTA;   // one gather CTA per this many SMs
+constexpr int kGatherWarpsPerSm = SPC_GATHER_WARPS_PER_SM;
 
 __global__ void __launch_bounds__(kGatherThreads)
 gather_kernel(const spc_gather_view* __restrict__ views, int layer_lo, int layer_hi,
@@ -191,7 +198,8 @@ int gather_launch(const spc_gather_view* views, int layer_lo, int layer_hi, cons
   const long long max_loads = (long long)B * n_kv * budget;          // one warp per load at a time
   const long long per_block = kGatherThreads / 32;
   long long grid = (max_loads + per_block - 1) / per_block;
-  const long long cap_grid = std::max(4, device_sm_count() / kGatherSmsPerCta);
+  const long long cap_grid =
+      std::max(4LL, ((long long)std::max(1, device_sm_count()) * kGatherWarpsPerSm + per_block - 1) / per_block);
   if (grid > cap_grid) grid = cap_grid;
   if (grid < 1) grid = 1;
   gather_kernel<<<(int)grid, kGatherThreads, 0, static_cast<cudaStream_t>(stream)>>>(

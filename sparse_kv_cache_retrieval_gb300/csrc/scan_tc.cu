@@ -1,0 +1,473 @@
+// Key scan of the retrieval head for large query-head groups (G = 16, 32, 64;
+// the MQA shape is G = 64) on the 5th-generation tensor cores.
+//
+// Method: "ASPLOS'26 | SpeContext 让小模型先圈出重要 KV Cache" (marsggbo blog)
+// §2 (attention weights softmax(q K^T / sqrt(d)) of the retrieval head over
+// the whole context) and §5 (for GQA/MQA the weights of a group's query heads
+// are combined, so every head of the group scores every position of its KV
+// head); "SpeContext: Enabling Efficient Long-context Reasoning with
+// Speculative Context Sparsity in LLMs" (paperlayer.ai summary) §3.1 (the
+// per-step cost is this scan over the context) and §4.3.
+//
+// Computes the same outputs as the head-major mma.sync scan it replaces for
+// these group sizes: position-major base-2 logits l[seg][p][h] =
+// (q_h . K[p]) * log2(e) / sqrt(d) and per-(head, tile, part) logsumexp
+// partials (max, sum 2^(l - max)).
+//
+// GB300 design, one CTA per SM, warp-specialised:
+//  * warp 0, one lane: TMA producer. Each 128-position key tile (32 KiB) comes
+//    in as two 64-dimension boxes of a 3-D tensor map ([segment][position]
+//    [dim]) with the 128-byte swizzle, into a 4-stage ring; completion is
+//    counted in bytes on the stage's mbarrier. Positions past the capacity
+//    are zero-filled by the copy and masked below.
+//  * warp 1: allocates the tensor memory (two accumulators of 2G fp32
+//    columns), builds the B operand of the current segment in shared memory
+//    (the group's queries scaled by log2(e)/sqrt(d) and split into a bf16
+//    high part, rows [0, G), and a bf16 low part, rows [G, 2G), so that q.K
+//    keeps ~16 significant bits of q), and one lane issues the MMAs:
+//    D[128 positions][2G] += K_tile[128][128] x Q[2G][128]^T, K = 16 per
+//    instruction, 8 instructions per tile, both operands K-major with the
+//    128-byte swizzle; tcgen05.commit frees the key stage and publishes the
+//    accumulator.
+//  * warps 2 .. 2 + 4 CG - 1: epilogue, CG = 2 column groups for G >= 32 (two
+//    epilogue warps per SM sub-partition). Warp w reads TMEM lanes
+//    32 (w % 4) .. +31, i.e. one position per thread, for its group's G / CG
+//    heads with tcgen05.ld; logit = high + low; the tile's logits go through a
+//    padded shared-memory tile to coalesced 16-byte global stores, and each
+//    thread folds a block of positions of one head into a partial.
+// Every mbarrier wait is bounded: a wait that gives up records
+// SPC_ERR_TIMEOUT, the warp stops waiting (it keeps its loop so every
+// barrier is still reached), in-flight copies and MMAs are waited for
+// (bounded) before the tensor memory is released.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "spc_device.cuh"
+#include "spc_internal.h"
+
+namespace spc {
+
+constexpr int kTcRows = 128;                 // positions per tile (the MMA's M)
+constexpr int kTcStages = 4;
+constexpr uint32_t kTcTileBytes = kTcRows * kRowBytes;      // 32 KiB
+constexpr uint32_t kTcHalfBytes = kTcTileBytes / 2;         // one 64-dim box
+constexpr long long kTcWait = 4000000000ll;  // clock cycles (~2 s)
+
+template <int G>
+struct TcShape {
+  static constexpr int N = 2 * G;                                   // MMA N: q high | q low
+  // epilogue: CG column groups of 4 warps (each group covers all 128 TMEM
+  // lanes = positions, for G / CG of the heads), so each SM sub-partition
+  // runs CG epilogue warps
+  static constexpr int CG = G >= 32 ? 2 : 1;
+  static constexpr int HPT = G / CG;                                // heads per epilogue thread
+  static constexpr int kEpi = 128 * CG;                             // epilogue threads
+  static constexpr int kThreads = 64 + kEpi;
+  // logsumexp partials: thread e folds PB positions of head e % G
+  static constexpr int NB = kEpi / G;                               // position blocks per tile
+  static constexpr int PB = kTcRows / NB;
+  static constexpr int kPpt = G == 16 ? NB / 2 : NB;                // G = 16 folds block pairs in-warp
+  static constexpr uint32_t kQBytes = (uint32_t)N * kRowBytes;      // [N][128] bf16, two swizzled halves
+  static constexpr int kPitch = G + 4;                              // staging row pitch (floats)
+  static constexpr uint32_t kStageOut = kTcRows * kPitch * 4;
+  static constexpr int kTmemCols = 2 * N < 32 ? 32 : 2 * N;        // two accumulators
+  static constexpr size_t kSmem = 1024 /* alignment slack */ + (size_t)kTcStages * kTcTileBytes + kQBytes +
+                                  kStageOut + 16 * sizeof(uint64_t) + 16;
+  // instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major,
+  // N >> 3 at bit 17, M >> 4 at bit 24
+  static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+                                     ((uint32_t)(kTcRows >> 4) << 24);
+};
+
+int scan_tc_ppt(int G) {
+  return G == 16 ? TcShape<16>::kPpt : G == 32 ? TcShape<32>::kPpt : TcShape<64>::kPpt;
+}
+
+// ---------------------------------------------------------------- PTX wrappers
+// Shared-memory matrix descriptor of a K-major operand with the 128-byte
+// swizzle: start address >> 4, leading byte offset 16 (unused for this
+// layout), stride between 8-row groups 1024 bytes, descriptor version 1,
+// layout type 2 (128-byte swizzle).
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(16 >> 4) << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         (1ull << 46) | (2ull << 61);
+}
+
+__device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+               :: "r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+// arrives once on `bar` when every tcgen05 operation this thread issued before has completed
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+               :: "r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 consecutive fp32 columns of this warp's 32 TMEM lanes (one lane per thread)
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+// 16 consecutive fp32 columns
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+  asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+               :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+               : "memory");
+}
+
+template <int NT>
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, %0;" :: "n"(NT) : "memory"); }
+
+__device__ __forceinline__ int tc_len(const int32_t* len, int b, int append, int cap) {
+  int L = len[b];
+  L = L < 0 ? 0 : (L > cap ? cap : L);
+  return (append && L < cap) ? L + 1 : L;
+}
+
+template <int G>
+__global__ void __launch_bounds__(TcShape<G>::kThreads, 1) scan_tc_kernel(const __grid_constant__ CUtensorMap kmap,
+                                                                          ScanTcCall a) {
+  using S = TcShape<G>;
+  extern __shared__ uint8_t tc_raw[];
+  // 1024-byte aligned base (the 128-byte swizzle repeats every 8 rows of 128 B)
+  const uint32_t raw_addr = smem_u32(tc_raw);
+  uint8_t* base = tc_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  uint8_t* stages = base;
+  uint8_t* qsm = stages + (size_t)kTcStages * kTcTileBytes;
+  float* stg = reinterpret_cast<float*>(qsm + S::kQBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(stg) + S::kStageOut);
+  uint64_t* empty = full + kTcStages;
+  uint64_t* acc_full = empty + kTcStages;     // [2]
+  uint64_t* acc_empty = acc_full + 2;         // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kTcStages; ++s) {
+      mbar_init(&full[s], 1);        // the producer's expect_tx arrival (+ the copies' bytes)
+      mbar_init(&empty[s], 1);       // one tcgen05.commit
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);    // one tcgen05.commit
+      mbar_init(&acc_empty[i], S::kEpi / 32);   // one arrival per epilogue warp
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 :: "r"(smem_u32(tmem_slot)), "n"(S::kTmemCols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int t0 = blockIdx.x * a.tpc;
+  const int t_end = min(a.total_tiles, t0 + a.tpc);
+
+  if (warp == 0) {
+    // ================= TMA producer (one lane)
+    if (lane == 0) {
+      int it = 0;
+      bool dead = false;
+      for (int t = t0; t < t_end && !dead; ++t) {
+        const int seg = t / a.n_tiles, tile = t - seg * a.n_tiles;
+        const int b = seg / a.n_kv;
+        if (tile * kTcRows >= tc_len(a.len, b, a.append, a.cap)) continue;
+        const int s = it % kTcStages;
+        const uint32_t ph = (it / kTcStages) & 1;
+        if (!mbar_wait_bounded(&empty[s], ph ^ 1, kTcWait)) {
+          set_status(a.status, SPC_ERR_TIMEOUT);
+          dead = true;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[s], kTcTileBytes);
+        const uint32_t dst = smem_u32(stages + (size_t)s * kTcTileBytes);
+        tma_load_3d(dst, &kmap, 0, tile * kTcRows, seg, &full[s]);
+        tma_load_3d(dst + kTcHalfBytes, &kmap, 64, tile * kTcRows, seg, &full[s]);
+        ++it;
+      }
+      // the copies still in flight land before the CTA may exit
+      for (int k = max(0, it - kTcStages); k < it; ++k)
+        mbar_wait_bounded(&full[k % kTcStages], (k / kTcStages) & 1, kTcWait);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ================= B operand (queries) and MMA issue
+    int it = 0, cur_seg = -1, last_it = -1;
+    bool dead = false;
+    const uint32_t q0 = smem_u32(qsm);
+    for (int t = t0; t < t_end; ++t) {
+      const int seg = t / a.n_tiles, tile = t - seg * a.n_tiles;
+      const int b = seg / a.n_kv, g = seg - b * a.n_kv;
+      if (tile * kTcRows >= tc_len(a.len, b, a.append, a.cap)) continue;
+      if (seg != cur_seg) {
+        // the MMAs that read the previous segment's queries must be done
+        if (last_it >= 0 && !dead) {
+          bool ok = true;
+          if (lane == 0) ok = mbar_wait_bounded(&acc_full[last_it & 1], (last_it >> 1) & 1, kTcWait);
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!ok) {
+            if (lane == 0) set_status(a.status, SPC_ERR_TIMEOUT);
+            dead = true;
+          }
+        }
+        // rows [0, G): bf16(q * scale); rows [G, 2G): bf16 of the remainder.
+        // Element (row n, dim k) sits in half k / 64 at byte
+        // n * 128 + (((k % 64) / 8) ^ (n % 8)) * 16 + (k % 8) * 2
+        const float* qg = a.q + ((size_t)b * a.n_q + (size_t)g * G) * kD;
+        for (int item = lane; item < G * 16; item += 32) {
+          const int h = item >> 4, u16 = item & 15;         // 16 units of 8 dims per head
+          const float4 x0 = *reinterpret_cast<const float4*>(qg + (size_t)h * kD + u16 * 8);
+          const float4 x1 = *reinterpret_cast<const float4*>(qg + (size_t)h * kD + u16 * 8 + 4);
+          float v[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float p0 = v[2 * e] * a.qscale, p1 = v[2 * e + 1] * a.qscale;
+            const float h0 = bf16_round(p0), h1 = bf16_round(p1);
+            hi[e] = pack_bf16(h0, h1);
+            lo[e] = pack_bf16(p0 - h0, p1 - h1);
+          }
+          const int half = u16 >> 3, u = u16 & 7;
+          const uint32_t hrow = q0 + (uint32_t)half * (S::N * 128) + (uint32_t)h * 128 + (uint32_t)((u ^ (h & 7)) << 4);
+          const int hl = h + G;
+          const uint32_t lrow = q0 + (uint32_t)half * (S::N * 128) + (uint32_t)hl * 128 + (uint32_t)((u ^ (hl & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" :: "r"(hrow), "r"(hi[0]), "r"(hi[1]), "r"(hi[2]),
+                       "r"(hi[3]) : "memory");
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" :: "r"(lrow), "r"(lo[0]), "r"(lo[1]), "r"(lo[2]),
+                       "r"(lo[3]) : "memory");
+        }
+        // generic-proxy writes made visible to the tensor core's async proxy
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        cur_seg = seg;
+      }
+      const int s = it % kTcStages;
+      const uint32_t ph = (it / kTcStages) & 1;
+      const int acc = it & 1;
+      if (lane == 0 && !dead) {
+        if (!mbar_wait_bounded(&full[s], ph, kTcWait) ||
+            !mbar_wait_bounded(&acc_empty[acc], ((it >> 1) & 1) ^ 1, kTcWait)) {
+          set_status(a.status, SPC_ERR_TIMEOUT);
+          dead = true;
+        } else {
+          tc_fence_after();
+          const uint32_t kst = smem_u32(stages + (size_t)s * kTcTileBytes);
+          const uint32_t dcol = tmem + (uint32_t)(acc * S::N);
+#pragma unroll
+          for (int half = 0; half < 2; ++half)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t ad = umma_desc_sw128(kst + (uint32_t)half * kTcHalfBytes + (uint32_t)k * 32);
+              const uint64_t bd = umma_desc_sw128(q0 + (uint32_t)half * (S::N * 128) + (uint32_t)k * 32);
+              umma_f16(dcol, ad, bd, S::kIdesc, (half | k) ? 1u : 0u);
+            }
+          umma_commit(&empty[s]);          // the key stage may be refilled once these MMAs are done
+          umma_commit(&acc_full[acc]);     // the accumulator is ready for the epilogue
+          last_it = it;
+        }
+      }
+      dead = __shfl_sync(0xffffffffu, dead ? 1 : 0, 0) != 0;
+      last_it = __shfl_sync(0xffffffffu, last_it, 0);
+      ++it;
+    }
+    // every MMA issued has completed before the tensor memory is released
+    if (lane == 0 && last_it >= 0)
+      mbar_wait_bounded(&acc_full[last_it & 1], (last_it >> 1) & 1, kTcWait);
+    __syncwarp();
+  } else {
+    // ================= epilogue: one position per thread, HPT of its heads
+    const int e = threadIdx.x - 64;                 // 0 .. kEpi - 1
+    const int quad = warp & 3;                      // TMEM lanes 32 quad .. 32 quad + 31
+    const int cg = (warp - 2) >> 2;                 // column group: heads [cg HPT, (cg + 1) HPT)
+    const int p = quad * 32 + lane;                 // this thread's position in the tile
+    const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
+    const int h_red = e % G, j_red = e / G;         // reduction: head and position block
+    bool dead = false;
+    int it = 0;
+    for (int t = t0; t < t_end; ++t) {
+      const int seg = t / a.n_tiles, tile = t - seg * a.n_tiles;
+      const int b = seg / a.n_kv, g = seg - b * a.n_kv;
+      const int L = tc_len(a.len, b, a.append, a.cap);
+      const int row0 = tile * kTcRows;
+      if (row0 >= L) continue;
+      const int nrows = min(kTcRows, L - row0);
+      const int acc = it & 1;
+      if (!dead && !mbar_wait_bounded(&acc_full[acc], (it >> 1) & 1, kTcWait)) {
+        if (lane == 0) set_status(a.status, SPC_ERR_TIMEOUT);
+        dead = true;
+      }
+      tc_fence_after();
+      const bool valid = p < nrows && !dead;
+      float* srow = stg + (size_t)p * S::kPitch + cg * S::HPT;
+      if (!dead) {
+        const uint32_t hc = trow + (uint32_t)(acc * S::N + cg * S::HPT);
+        float hi[S::HPT], lo[S::HPT];
+        if constexpr (S::HPT == 32) {
+          tmem_ld32(hc, hi);
+          tmem_ld32(hc + G, lo);
+        } else {
+          tmem_ld16(hc, hi);
+          tmem_ld16(hc + G, lo);
+        }
+        tmem_ld_wait();
+#pragma unroll
+        for (int h = 0; h < S::HPT; h += 4) {
+          float4 o;
+          o.x = valid ? hi[h] + lo[h] : -INFINITY;
+          o.y = valid ? hi[h + 1] + lo[h + 1] : -INFINITY;
+          o.z = valid ? hi[h + 2] + lo[h + 2] : -INFINITY;
+          o.w = valid ? hi[h + 3] + lo[h + 3] : -INFINITY;
+          *reinterpret_cast<float4*>(srow + h) = o;
+        }
+      } else {
+#pragma unroll
+        for (int h = 0; h < S::HPT; h += 4)
+          *reinterpret_cast<float4*>(srow + h) = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      }
+      // this warp is done with the accumulator
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      epi_bar<S::kEpi>();
+      // ---- logsumexp partial of head h_red over positions [j_red PB, (j_red + 1) PB)
+      float x[S::PB];
+#pragma unroll
+      for (int i = 0; i < S::PB; ++i) x[i] = stg[(size_t)(j_red * S::PB + i) * S::kPitch + h_red];
+      float m = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < S::PB; ++i) m = fmaxf(m, x[i]);
+      float sm = 0.f;
+      if (m != -INFINITY) {
+#pragma unroll
+        for (int i = 0; i < S::PB; ++i) sm += exp2f(x[i] - m);
+      }
+      int slot = j_red;
+      if constexpr (G == 16) {
+        // lanes e and e + 16 hold the same head: fold the warp's two blocks
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, 16), s2 = __shfl_xor_sync(0xffffffffu, sm, 16);
+        lse2_combine(m, sm, m2, s2);
+        slot = e >> 5;
+      }
+      if (G != 16 || lane < 16) {
+        const size_t pi = (size_t)tile * S::kPpt + slot;
+        a.part[((size_t)b * a.n_q + (size_t)g * G + h_red) * a.n_parts + pi] = make_float2(m, sm);
+      }
+      // ---- the tile's logits, coalesced: [seg][row0 + r][h]
+      if (!dead) {
+        float* lg = a.logits + ((size_t)seg * a.lstride + row0) * G;
+        const int n4 = nrows * (G / 4);
+        for (int f = e; f < n4; f += S::kEpi) {
+          const int r = f / (G / 4), c4 = f - r * (G / 4);
+          const float4 v = *reinterpret_cast<const float4*>(stg + (size_t)r * S::kPitch + c4 * 4);
+          *reinterpret_cast<float4*>(lg + (size_t)r * G + c4 * 4) = v;
+        }
+      }
+      epi_bar<S::kEpi>();
+      ++it;
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "n"(S::kTmemCols)
+                 : "memory");
+  }
+}
+
+// ---------------------------------------------------------------- host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_tiled() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+template <int G>
+static cudaError_t launch_tc(const CUtensorMap& map, const ScanTcCall& c, int grid, cudaStream_t st) {
+  const size_t smem = TcShape<G>::kSmem;
+  cudaError_t e = set_func_attr((const void*)scan_tc_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  scan_tc_kernel<G><<<grid, TcShape<G>::kThreads, smem, st>>>(map, c);
+  return cudaGetLastError();
+}
+
+int scan_tc_launch(ScanTcCall c, int G, void* stream) {
+  EncodeTiledFn enc = encode_tiled();
+  if (!enc) return SPC_ERR_CUDA;
+  // K_dlm as [segment = b * n_kv + g][position][dim], boxes of 128 positions x 64 dims
+  CUtensorMap map;
+  const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)c.cap, (cuuint64_t)c.B * c.n_kv};
+  const cuuint64_t strides[2] = {(cuuint64_t)kRowBytes, (cuuint64_t)c.cap * kRowBytes};
+  const cuuint32_t box[3] = {64, (cuuint32_t)kTcRows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(c.K), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return SPC_ERR_CUDA;
+  // one wave: one CTA per SM, each a run of consecutive tiles
+  const int sms = device_sm_count() > 0 ? device_sm_count() : 1;
+  c.tpc = (c.total_tiles + sms - 1) / sms;
+  if (c.tpc < 1) c.tpc = 1;
+  const int grid = (c.total_tiles + c.tpc - 1) / c.tpc;
+  if (grid < 1) return SPC_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  switch (G) {
+    case 16: e = launch_tc<16>(map, c, grid, st); break;
+    case 32: e = launch_tc<32>(map, c, grid, st); break;
+    case 64: e = launch_tc<64>(map, c, grid, st); break;
+    default: return SPC_ERR_SHAPE;
+  }
+  return e == cudaSuccess ? SPC_OK : SPC_ERR_CUDA;
+}
+
+}  // namespace spc

@@ -1214,8 +1214,13 @@ struct ScoreLayout {
   int n_tiles, ppt, n_parts, lstride;
 };
 
+#ifndef SPC_SCAN_TC
+#define SPC_SCAN_TC 1   // groups of 16+ heads: the tcgen05 scan (0: the mma.sync head-major scan)
+#endif
+
 static int scan_ppt(int G) {
-  return G <= 8 ? kScanKmWarps : kScanCWarps / (G <= 16 ? 1 : G / 16);
+  if (G <= 8) return kScanKmWarps;
+  return SPC_SCAN_TC ? scan_tc_ppt(G) : kScanCWarps / (G <= 16 ? 1 : G / 16);
 }
 
 static ScoreLayout score_layout(int B, int H, int n_q, int n_kv, int cap) {
@@ -1422,6 +1427,15 @@ int score_select_launch(const ScoreSelectCall& c) {
     sa.n_q = c.n_q; sa.n_kv = c.n_kv; sa.cap = c.cap; sa.lstride = l.lstride; sa.n_tiles = l.n_tiles;
     sa.total_tiles = c.B * c.n_kv * l.n_tiles; sa.append = c.append; sa.n_parts = l.n_parts;
     sa.qscale = kLog2e / sqrtf((float)kD);
+    if (SPC_SCAN_TC && G >= 16) {
+      ScanTcCall tc{};
+      tc.K = sa.K; tc.q = sa.q; tc.len = sa.len; tc.logits = sa.logits; tc.part = sa.part; tc.status = status;
+      tc.B = c.B; tc.n_q = c.n_q; tc.n_kv = c.n_kv; tc.cap = c.cap; tc.lstride = l.lstride;
+      tc.n_tiles = l.n_tiles; tc.total_tiles = sa.total_tiles; tc.append = c.append; tc.n_parts = l.n_parts;
+      tc.qscale = sa.qscale;
+      const int rc = scan_tc_launch(tc, G, c.stream);
+      if (rc != SPC_OK) return rc;
+    } else {
     // each CTA takes a run of consecutive tiles
     if (kScanTilesPerCta > 0) {
       sa.tpc = kScanTilesPerCta;
@@ -1441,6 +1455,7 @@ int score_select_launch(const ScoreSelectCall& c) {
       default: e = launch_scan<64>(sa, grid, st); break;
     }
     if (e != cudaSuccess) return SPC_ERR_CUDA;
+    }
   }
 
   // ---- logsumexp, group score, Top-K (one cluster per request and KV head)

@@ -33,6 +33,22 @@ struct ScoreSelectCall {
 };
 
 size_t score_select_workspace(int B, int H, int n_q, int n_kv, int cap);
+
+// Key scan on the 5th-generation tensor cores for groups of 16, 32 or 64
+// query heads (scan_tc.cu): base-2 logits [segment][position][G] and
+// scan_tc_ppt(G) logsumexp partials per (head, 128-position tile).
+struct ScanTcCall {
+  const uint16_t* K;
+  const float* q;
+  const int32_t* len;
+  float* logits;
+  float2* part;
+  int* status;
+  int B, n_q, n_kv, cap, lstride, n_tiles, total_tiles, append, n_parts, tpc;
+  float qscale;
+};
+int scan_tc_ppt(int G);
+int scan_tc_launch(ScanTcCall c, int G, void* stream);
 int score_select_launch(const ScoreSelectCall& c);
 
 int elastic_diff_launch(const int32_t* selected, const int32_t* prev, int32_t* next,
