@@ -164,26 +164,34 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- ncu traffic
-# DRAM (and, for the gather, host-link) bytes per algorithmic unit of the
-# hot-path kernels, from one `ncu --set full` capture of each on the cfg2
-# workload (the summary and its command are in profiles/). A figure is used
-# only while the kernel's source file still hashes to the one captured.
+# DRAM bytes (host-link bytes for the gather) per algorithmic unit of the
+# hot-path kernels, from one ncu capture of each (the summaries and their
+# commands are in profiles/). A figure is used only while the kernel's source
+# file still hashes to the one captured.
 NCU_TRAFFIC = {
-    # gather of decode step 0, layers 16-31: 1550 loads x 16 layers x K/V = 49 600
-    # rows; 396 800 system-memory sectors (12 697 600 B) read over the host link
-    # + 29 440 B DRAM read + 512 B DRAM write
+    # gather of decode step 0, layers 1-15 (chunk 0) of the 70B-shaped workload at a 16K
+    # context: 35 554 loads x 15 layers x K/V = 1 066 620 rows; 8 532 960 system-memory
+    # sectors (273 054 720 B) read over the host link, i.e. 256.0 B per 256-byte row (the
+    # slot writes, 256 B per row into HBM, are the other half of the copy and are not
+    # host-link traffic; 211.7 MB of them had reached DRAM when the kernel ended)
     "gather": {"source": "sparse_kv_cache_retrieval_gb300/csrc/gather_kv.cu",
-               "sha256": "64d94964969b6f26d0a9bcea0c5bd87912d644381332e95ddf493098441c6a6e",
-               "bytes_per_unit": (12697600 + 29440 + 512) / 49600, "unit": "moved 256-byte row"},
-    # key scan over 32 768 positions x 8 KV heads: 67 140 864 B DRAM read + 322 048 B write
+               "sha256": "4840cb43e2a9779e4a4b7c33986b7fade82263e0181e55f173485d38404431ee",
+               "bytes_per_unit": 273054720 / 1066620, "unit": "moved 256-byte row (host-link bytes)"},
+    # key scan over 32 768 positions x 8 KV heads (second of two launches):
+    # 67 141 120 B DRAM read + 768 B write
     "key_scan": {"source": "sparse_kv_cache_retrieval_gb300/csrc/score_select.cu",
-                 "sha256": "435af35b2dce2aca1b6918dd31cd0060a4e5b12aeac4683078bfa0e0b724bf14",
-                 "bytes_per_unit": (67140864 + 322048) / 262144, "unit": "256-byte key row"},
-    # attention over 16 layers x 8 KV heads x 2048 kept rows, mean of two launches:
-    # 134 537 728 B read + 3 063 680 B write
+                 "sha256": "e933ecb3c598448f359b57bd3cd412e49d15a37f17859c100eaf23e9e2de7aae",
+                 "bytes_per_unit": (67141120 + 768) / 262144, "unit": "256-byte key row"},
+    # tcgen05 key scan, MQA (64 heads, one KV head), 8 requests x 16 384 positions:
+    # 33 847 040 B DRAM read + 321 536 B write (the logits stayed in L2)
+    "key_scan_tc": {"source": "sparse_kv_cache_retrieval_gb300/csrc/scan_tc.cu",
+                    "sha256": "899ff4ad1ab3a6322b10d0ae365cb9e7a5e4b5128fc56a690329ab92a2e6ac77",
+                    "bytes_per_unit": (33847040 + 321536) / 131072, "unit": "256-byte key row"},
+    # attention, 70B shape: 2 layers x 8 requests x 8 KV heads x 4096 kept rows:
+    # 272 741 888 B read + 4 417 280 B written
     "attention": {"source": "sparse_kv_cache_retrieval_gb300/csrc/sparse_attn.cu",
-                  "sha256": "01e645590c4b04bc2ebf3b3ffe7de26745c170c8cca195e315e23f35760f7f86",
-                  "bytes_per_unit": (134537728 + 3063680) / 262144, "unit": "512-byte K+V row"},
+                  "sha256": "683d9635124b692bf486c0c1b6e497acc135ba475d6c22e67bce765f4a6e9d18",
+                  "bytes_per_unit": (272741888 + 4417280) / 524288, "unit": "512-byte K+V row"},
     # MLA: gather of decode step 0, 221 loads x 27 layers = 5 967 latent rows;
     # 214 812 system-memory sectors (6 873 984 B) over the host link + 12 032 B DRAM read
     "mla_gather": {"source": "sparse_kv_cache_retrieval_gb300/csrc/mla.cu",
@@ -217,7 +225,8 @@ def traffic_units(cfg) -> dict:
     moved row, a kept row)."""
     if cfg.mla:
         return {"gather": ("mla_gather", 1152), "key_scan": ("mla_scan", 1152), "attention": ("mla_attention", 1152)}
-    return {"gather": ("gather", 256), "key_scan": ("key_scan", 256), "attention": ("attention", 512)}
+    return {"gather": ("gather", 256), "key_scan": ("key_scan_tc" if cfg.G >= 16 else "key_scan", 256),
+            "attention": ("attention", 512)}
 
 
 def ncu_traffic(kind: str, units: float):
