@@ -9,17 +9,23 @@
 // Speculative Context Sparsity in LLMs" (paperlayer.ai summary) §3.1 (the
 // per-step cost is this scan over the context) and §4.3.
 //
-// Computes the same outputs as the head-major mma.sync scan it replaces for
-// these group sizes: position-major base-2 logits l[seg][p][h] =
-// (q_h . K[p]) * log2(e) / sqrt(d) and per-(head, tile, part) logsumexp
-// partials (max, sum 2^(l - max)).
+// Two passes over the key cache (both HBM-bound, neither writes the logits):
+//  * pass 1 (SCAN stage) folds every head's logits into logsumexp partials
+//    (max, sum 2^(l - max)) per (head, 128-position tile, TMEM lane quadrant);
+//  * a fold kernel turns them into each head's normaliser lse_h (base 2);
+//  * pass 2 (SELECT stage) recomputes the logits and writes one value per
+//    position, the log2 of the group score max_h 2^(l_h - lse_h), which the
+//    radix select then ranks as a group of one head with a zero normaliser.
+// Logits are (q_h . K[p]) * log2(e) / sqrt(d). Reading the keys twice moves
+// 2 x 256 B per position, where writing position-major logits for G = 64
+// and reading them back in the select would move 256 + 256 + 256 B.
 //
 // GB300 design, one CTA per SM, warp-specialised:
 //  * warp 0, one lane: TMA producer. Each 128-position key tile (32 KiB) comes
 //    in as two 64-dimension boxes of a 3-D tensor map ([segment][position]
-//    [dim]) with the 128-byte swizzle, into a 4-stage ring; completion is
-//    counted in bytes on the stage's mbarrier. Positions past the capacity
-//    are zero-filled by the copy and masked below.
+//    [dim]) with the 128-byte swizzle, into a 6-stage ring (192 KiB in flight
+//    per SM); completion is counted in bytes on the stage's mbarrier.
+//    Positions past the capacity are zero-filled by the copy and masked.
 //  * warp 1: allocates the tensor memory (two accumulators of 2G fp32
 //    columns), builds the B operand of the current segment in shared memory
 //    (the group's queries scaled by log2(e)/sqrt(d) and split into a bf16
@@ -29,15 +35,16 @@
 //    instruction, 8 instructions per tile, both operands K-major with the
 //    128-byte swizzle; tcgen05.commit frees the key stage and publishes the
 //    accumulator.
-//  * warps 2 .. 2 + 4 CG - 1: epilogue, CG = 2 column groups for G >= 32 (two
-//    epilogue warps per SM sub-partition). Warp w reads TMEM lanes
-//    32 (w % 4) .. +31, i.e. one position per thread, for its group's G / CG
-//    heads with tcgen05.ld; logit = high + low; the tile's logits go through a
-//    padded shared-memory tile to coalesced 16-byte global stores, and each
-//    thread folds a block of positions of one head into a partial.
+//  * epilogue warps (CG column groups of 4, CG = 2 for G = 64): warp w reads
+//    TMEM lanes 32 (w % 4) .. +31 (one position per thread) for G / CG of the
+//    heads with tcgen05.ld and adds the high and low products. Pass 1 folds
+//    each head over the warp's 32 positions with a shuffle butterfly that
+//    leaves lane l holding head l's (max, sum); pass 2 takes the maximum over
+//    the thread's heads of l_h - lse_h, combines the column groups through
+//    shared memory and writes 128 consecutive floats per tile.
 // Every mbarrier wait is bounded: a wait that gives up records
 // SPC_ERR_TIMEOUT, the warp stops waiting (it keeps its loop so every
-// barrier is still reached), in-flight copies and MMAs are waited for
+// barrier is still reached), and in-flight copies and MMAs are waited for
 // (bounded) before the tensor memory is released.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -50,31 +57,29 @@
 namespace spc {
 
 constexpr int kTcRows = 128;                 // positions per tile (the MMA's M)
-constexpr int kTcStages = 4;
+constexpr int kTcStages = 6;
 constexpr uint32_t kTcTileBytes = kTcRows * kRowBytes;      // 32 KiB
 constexpr uint32_t kTcHalfBytes = kTcTileBytes / 2;         // one 64-dim box
 constexpr long long kTcWait = 4000000000ll;  // clock cycles (~2 s)
+constexpr int kTcPpt = 4;                    // partials per (head, tile): one per TMEM lane quadrant
+
+enum { kPassLse = 0, kPassScore = 1 };
 
 template <int G>
 struct TcShape {
   static constexpr int N = 2 * G;                                   // MMA N: q high | q low
   // epilogue: CG column groups of 4 warps (each group covers all 128 TMEM
-  // lanes = positions, for G / CG of the heads), so each SM sub-partition
-  // runs CG epilogue warps
-  static constexpr int CG = G >= 32 ? 2 : 1;
-  static constexpr int HPT = G / CG;                                // heads per epilogue thread
-  static constexpr int kEpi = 128 * CG;                             // epilogue threads
+  // lanes = positions, for HPT of the heads)
+  static constexpr int CG = G >= 64 ? 2 : 1;
+  static constexpr int HPT = G / CG;                                // 32 (G = 32, 64) or 16
+  static constexpr int LOG_HPT = HPT == 32 ? 5 : 4;
+  static constexpr int kEpi = 128 * CG;
   static constexpr int kThreads = 64 + kEpi;
-  // logsumexp partials: thread e folds PB positions of head e % G
-  static constexpr int NB = kEpi / G;                               // position blocks per tile
-  static constexpr int PB = kTcRows / NB;
-  static constexpr int kPpt = G == 16 ? NB / 2 : NB;                // G = 16 folds block pairs in-warp
   static constexpr uint32_t kQBytes = (uint32_t)N * kRowBytes;      // [N][128] bf16, two swizzled halves
-  static constexpr int kPitch = G + 4;                              // staging row pitch (floats)
-  static constexpr uint32_t kStageOut = kTcRows * kPitch * 4;
+  static constexpr uint32_t kXch = 2 * kTcRows * 4;                 // pass 2: column-group maxima, 2 buffers
   static constexpr int kTmemCols = 2 * N < 32 ? 32 : 2 * N;        // two accumulators
   static constexpr size_t kSmem = 1024 /* alignment slack */ + (size_t)kTcStages * kTcTileBytes + kQBytes +
-                                  kStageOut + 16 * sizeof(uint64_t) + 16;
+                                  kXch + 16 * sizeof(uint64_t) + 16;
   // instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major,
   // N >> 3 at bit 17, M >> 4 at bit 24
   static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
@@ -82,7 +87,8 @@ struct TcShape {
 };
 
 int scan_tc_ppt(int G) {
-  return G == 16 ? TcShape<16>::kPpt : G == 32 ? TcShape<32>::kPpt : TcShape<64>::kPpt;
+  (void)G;
+  return kTcPpt;
 }
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -155,7 +161,17 @@ __device__ __forceinline__ int tc_len(const int32_t* len, int b, int append, int
   return (append && L < cap) ? L + 1 : L;
 }
 
-template <int G>
+// (max, sum of 2^(x - max)) merge with one exp2: the smaller maximum's sum is
+// scaled; an empty side is (-inf, 0)
+__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
+  const bool keep = m >= m2;
+  const float M = keep ? m : m2, mn = keep ? m2 : m;
+  const float sb = keep ? s : s2, ss = keep ? s2 : s;
+  s = mn == -INFINITY ? sb : sb + ss * exp2f(mn - M);
+  m = M;
+}
+
+template <int G, int PASS>
 __global__ void __launch_bounds__(TcShape<G>::kThreads, 1) scan_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                                                                           ScanTcCall a) {
   using S = TcShape<G>;
@@ -165,8 +181,8 @@ __global__ void __launch_bounds__(TcShape<G>::kThreads, 1) scan_tc_kernel(const 
   uint8_t* base = tc_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   uint8_t* stages = base;
   uint8_t* qsm = stages + (size_t)kTcStages * kTcTileBytes;
-  float* stg = reinterpret_cast<float*>(qsm + S::kQBytes);
-  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(stg) + S::kStageOut);
+  float* xch = reinterpret_cast<float*>(qsm + S::kQBytes);           // [2][128]
+  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(xch) + S::kXch);
   uint64_t* empty = full + kTcStages;
   uint64_t* acc_full = empty + kTcStages;     // [2]
   uint64_t* acc_empty = acc_full + 2;         // [2]
@@ -310,12 +326,12 @@ __global__ void __launch_bounds__(TcShape<G>::kThreads, 1) scan_tc_kernel(const 
     __syncwarp();
   } else {
     // ================= epilogue: one position per thread, HPT of its heads
-    const int e = threadIdx.x - 64;                 // 0 .. kEpi - 1
     const int quad = warp & 3;                      // TMEM lanes 32 quad .. 32 quad + 31
     const int cg = (warp - 2) >> 2;                 // column group: heads [cg HPT, (cg + 1) HPT)
     const int p = quad * 32 + lane;                 // this thread's position in the tile
     const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
-    const int h_red = e % G, j_red = e / G;         // reduction: head and position block
+    float lse_r[S::HPT];                            // pass 2: this thread's heads' normalisers
+    int cur_seg = -1;
     bool dead = false;
     int it = 0;
     for (int t = t0; t < t_end; ++t) {
@@ -325,6 +341,12 @@ __global__ void __launch_bounds__(TcShape<G>::kThreads, 1) scan_tc_kernel(const 
       const int row0 = tile * kTcRows;
       if (row0 >= L) continue;
       const int nrows = min(kTcRows, L - row0);
+      if (PASS == kPassScore && seg != cur_seg) {
+        const float* lg = a.lse + (size_t)b * a.n_q + (size_t)g * G + cg * S::HPT;
+#pragma unroll
+        for (int h = 0; h < S::HPT; ++h) lse_r[h] = lg[h];
+        cur_seg = seg;
+      }
       const int acc = it & 1;
       if (!dead && !mbar_wait_bounded(&acc_full[acc], (it >> 1) & 1, kTcWait)) {
         if (lane == 0) set_status(a.status, SPC_ERR_TIMEOUT);
@@ -332,71 +354,79 @@ __global__ void __launch_bounds__(TcShape<G>::kThreads, 1) scan_tc_kernel(const 
       }
       tc_fence_after();
       const bool valid = p < nrows && !dead;
-      float* srow = stg + (size_t)p * S::kPitch + cg * S::HPT;
-      if (!dead) {
+      float v[S::HPT];
+      {
         const uint32_t hc = trow + (uint32_t)(acc * S::N + cg * S::HPT);
         float hi[S::HPT], lo[S::HPT];
-        if constexpr (S::HPT == 32) {
-          tmem_ld32(hc, hi);
-          tmem_ld32(hc + G, lo);
-        } else {
-          tmem_ld16(hc, hi);
-          tmem_ld16(hc + G, lo);
+        if (!dead) {
+          if constexpr (S::HPT == 32) {
+            tmem_ld32(hc, hi);
+            tmem_ld32(hc + G, lo);
+          } else {
+            tmem_ld16(hc, hi);
+            tmem_ld16(hc + G, lo);
+          }
+          tmem_ld_wait();
         }
-        tmem_ld_wait();
 #pragma unroll
-        for (int h = 0; h < S::HPT; h += 4) {
-          float4 o;
-          o.x = valid ? hi[h] + lo[h] : -INFINITY;
-          o.y = valid ? hi[h + 1] + lo[h + 1] : -INFINITY;
-          o.z = valid ? hi[h + 2] + lo[h + 2] : -INFINITY;
-          o.w = valid ? hi[h + 3] + lo[h + 3] : -INFINITY;
-          *reinterpret_cast<float4*>(srow + h) = o;
-        }
-      } else {
-#pragma unroll
-        for (int h = 0; h < S::HPT; h += 4)
-          *reinterpret_cast<float4*>(srow + h) = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        for (int h = 0; h < S::HPT; ++h) v[h] = valid ? hi[h] + lo[h] : -INFINITY;
       }
       // this warp is done with the accumulator
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[acc]);
-      epi_bar<S::kEpi>();
-      // ---- logsumexp partial of head h_red over positions [j_red PB, (j_red + 1) PB)
-      float x[S::PB];
+
+      if constexpr (PASS == kPassLse) {
+        // ---- (max, sum 2^(l - max)) of every head over this warp's 32
+        // positions: a butterfly that halves the heads a lane keeps at each
+        // step, so lane l ends with head l (16 heads: lanes 2j and 2j + 1
+        // with head j, merged at the end)
+        float m[S::HPT], sm[S::HPT];
 #pragma unroll
-      for (int i = 0; i < S::PB; ++i) x[i] = stg[(size_t)(j_red * S::PB + i) * S::kPitch + h_red];
-      float m = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < S::PB; ++i) m = fmaxf(m, x[i]);
-      float sm = 0.f;
-      if (m != -INFINITY) {
-#pragma unroll
-        for (int i = 0; i < S::PB; ++i) sm += exp2f(x[i] - m);
-      }
-      int slot = j_red;
-      if constexpr (G == 16) {
-        // lanes e and e + 16 hold the same head: fold the warp's two blocks
-        const float m2 = __shfl_xor_sync(0xffffffffu, m, 16), s2 = __shfl_xor_sync(0xffffffffu, sm, 16);
-        lse2_combine(m, sm, m2, s2);
-        slot = e >> 5;
-      }
-      if (G != 16 || lane < 16) {
-        const size_t pi = (size_t)tile * S::kPpt + slot;
-        a.part[((size_t)b * a.n_q + (size_t)g * G + h_red) * a.n_parts + pi] = make_float2(m, sm);
-      }
-      // ---- the tile's logits, coalesced: [seg][row0 + r][h]
-      if (!dead) {
-        float* lg = a.logits + ((size_t)seg * a.lstride + row0) * G;
-        const int n4 = nrows * (G / 4);
-        for (int f = e; f < n4; f += S::kEpi) {
-          const int r = f / (G / 4), c4 = f - r * (G / 4);
-          const float4 v = *reinterpret_cast<const float4*>(stg + (size_t)r * S::kPitch + c4 * 4);
-          *reinterpret_cast<float4*>(lg + (size_t)r * G + c4 * 4) = v;
+        for (int h = 0; h < S::HPT; ++h) {
+          m[h] = v[h];
+          sm[h] = v[h] == -INFINITY ? 0.f : 1.f;
         }
+#pragma unroll
+        for (int st = 0; st < S::LOG_HPT; ++st) {
+          const int k = 16 >> st;                      // lane bit of this step
+          const int n = S::HPT >> (st + 1);            // heads kept after it
+          const bool up = (lane & k) != 0;
+#pragma unroll
+          for (int i = 0; i < n; ++i) {
+            const float gm = up ? m[i] : m[i + n], gs = up ? sm[i] : sm[i + n];
+            float km = up ? m[i + n] : m[i], ks = up ? sm[i + n] : sm[i];
+            const float rm = __shfl_xor_sync(0xffffffffu, gm, k);
+            const float rs = __shfl_xor_sync(0xffffffffu, gs, k);
+            lse_merge(km, ks, rm, rs);
+            m[i] = km;
+            sm[i] = ks;
+          }
+        }
+        int head = lane;
+        if constexpr (S::HPT == 16) {
+          const float rm = __shfl_xor_sync(0xffffffffu, m[0], 1), rs = __shfl_xor_sync(0xffffffffu, sm[0], 1);
+          lse_merge(m[0], sm[0], rm, rs);
+          head = lane >> 1;
+        }
+        if (S::HPT == 32 || (lane & 1) == 0) {
+          const int h = cg * S::HPT + head;
+          a.part[((size_t)b * a.n_q + (size_t)g * G + h) * a.n_parts + (size_t)tile * kTcPpt + quad] =
+              make_float2(m[0], sm[0]);
+        }
+      } else {
+        // ---- log2 of the group score: max over heads of l_h - lse_h
+        float gs = -INFINITY;
+#pragma unroll
+        for (int h = 0; h < S::HPT; ++h) gs = fmaxf(gs, v[h] - lse_r[h]);
+        if constexpr (S::CG == 2) {
+          float* x = xch + (it & 1) * kTcRows;
+          if (cg == 1) x[p] = gs;
+          epi_bar<S::kEpi>();
+          if (cg == 0) gs = fmaxf(gs, x[p]);
+        }
+        if (cg == 0 && valid) a.gscore[(size_t)seg * a.lstride + row0 + p] = gs;
       }
-      epi_bar<S::kEpi>();
       ++it;
     }
     tc_fence_before();
@@ -408,6 +438,43 @@ __global__ void __launch_bounds__(TcShape<G>::kThreads, 1) scan_tc_kernel(const 
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "n"(S::kTmemCols)
                  : "memory");
   }
+}
+
+// Normalisers from the pass-1 partials, one warp per (request, query head),
+// eight partials in flight per lane: lse[b][h] = log2 sum_p 2^(l_h(p)) over
+// p < len (INFINITY for an empty context). The first CTA of every (request,
+// KV head) also writes the partials of a zero normaliser for the radix
+// select that ranks the group scores (one partial per tile: (0, 1) first).
+constexpr int kFoldThreads = 256;
+constexpr int kFoldHeads = kFoldThreads / 32;     // heads per CTA
+__global__ void __launch_bounds__(kFoldThreads) lse_fold_kernel(ScanTcCall a, int G, float2* part1, int n_parts1) {
+  const int per_seg = (G + kFoldHeads - 1) / kFoldHeads;
+  const int seg = blockIdx.x / per_seg, hblk = blockIdx.x - seg * per_seg;
+  const int b = seg / a.n_kv, g = seg - b * a.n_kv;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int L = tc_len(a.len, b, a.append, a.cap);
+  const int nv = ((L + kTcRows - 1) / kTcRows) * kTcPpt;
+  const int h = hblk * kFoldHeads + warp;
+  if (h < G) {
+    const float2* ph = a.part + ((size_t)b * a.n_q + (size_t)g * G + h) * a.n_parts;
+    float m = -INFINITY, s = 0.f;
+    for (int i0 = lane; i0 < nv; i0 += 32 * 8) {
+      float2 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = i0 + 32 * u < nv ? __ldcg(ph + i0 + 32 * u) : make_float2(-INFINITY, 0.f);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) lse_merge(m, s, v[u].x, v[u].y);
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
+      lse_merge(m, s, m2, s2);
+    }
+    if (lane == 0) a.lse[(size_t)b * a.n_q + (size_t)g * G + h] = s > 0.f ? m + log2f(s) : INFINITY;
+  }
+  if (hblk == 0)
+    for (int t = threadIdx.x; t < n_parts1; t += kFoldThreads)
+      part1[(size_t)seg * n_parts1 + t] = t == 0 ? make_float2(0.f, 1.f) : make_float2(-INFINITY, 0.f);
 }
 
 // ---------------------------------------------------------------- host side
@@ -431,16 +498,17 @@ static EncodeTiledFn encode_tiled() {
   return fn;
 }
 
-template <int G>
+template <int G, int PASS>
 static cudaError_t launch_tc(const CUtensorMap& map, const ScanTcCall& c, int grid, cudaStream_t st) {
   const size_t smem = TcShape<G>::kSmem;
-  cudaError_t e = set_func_attr((const void*)scan_tc_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e =
+      set_func_attr((const void*)scan_tc_kernel<G, PASS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  scan_tc_kernel<G><<<grid, TcShape<G>::kThreads, smem, st>>>(map, c);
+  scan_tc_kernel<G, PASS><<<grid, TcShape<G>::kThreads, smem, st>>>(map, c);
   return cudaGetLastError();
 }
 
-int scan_tc_launch(ScanTcCall c, int G, void* stream) {
+static int scan_tc_pass(ScanTcCall c, int G, int pass, cudaStream_t st) {
   EncodeTiledFn enc = encode_tiled();
   if (!enc) return SPC_ERR_CUDA;
   // K_dlm as [segment = b * n_kv + g][position][dim], boxes of 128 positions x 64 dims
@@ -459,15 +527,28 @@ int scan_tc_launch(ScanTcCall c, int G, void* stream) {
   if (c.tpc < 1) c.tpc = 1;
   const int grid = (c.total_tiles + c.tpc - 1) / c.tpc;
   if (grid < 1) return SPC_OK;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  switch (G) {
-    case 16: e = launch_tc<16>(map, c, grid, st); break;
-    case 32: e = launch_tc<32>(map, c, grid, st); break;
-    case 64: e = launch_tc<64>(map, c, grid, st); break;
+  switch (G * 2 + pass) {
+    case 32 + kPassLse: e = launch_tc<16, kPassLse>(map, c, grid, st); break;
+    case 32 + kPassScore: e = launch_tc<16, kPassScore>(map, c, grid, st); break;
+    case 64 + kPassLse: e = launch_tc<32, kPassLse>(map, c, grid, st); break;
+    case 64 + kPassScore: e = launch_tc<32, kPassScore>(map, c, grid, st); break;
+    case 128 + kPassLse: e = launch_tc<64, kPassLse>(map, c, grid, st); break;
+    case 128 + kPassScore: e = launch_tc<64, kPassScore>(map, c, grid, st); break;
     default: return SPC_ERR_SHAPE;
   }
   return e == cudaSuccess ? SPC_OK : SPC_ERR_CUDA;
+}
+
+int scan_tc_launch(ScanTcCall c, int G, void* stream) {
+  return scan_tc_pass(c, G, kPassLse, static_cast<cudaStream_t>(stream));
+}
+
+int scan_tc_scores_launch(ScanTcCall c, int G, float2* part1, int n_parts1, void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  lse_fold_kernel<<<c.B * c.n_kv * ((G + kFoldHeads - 1) / kFoldHeads), kFoldThreads, 0, st>>>(c, G, part1, n_parts1);
+  if (cudaGetLastError() != cudaSuccess) return SPC_ERR_CUDA;
+  return scan_tc_pass(c, G, kPassScore, st);
 }
 
 }  // namespace spc

@@ -352,8 +352,6 @@ struct ScanArgs {
 };
 
 constexpr int kScanRows = 128;
-constexpr int kScanCWarps = 4;
-constexpr int kScanThreads = (kScanCWarps + 1) * 32;
 constexpr int kScanStages = 3;
 // Tiles per CTA: 0 sizes the grid to one wave of kScanCtasPerSm CTAs per SM
 // (each CTA streams a run of consecutive tiles, so the kernel lasts as long
@@ -364,192 +362,6 @@ constexpr int kScanStages = 3;
 constexpr int kScanTilesPerCta = SPC_SCAN_TILES_PER_CTA;
 constexpr int kScanCtasPerSm = 2;   // the 3-stage ring (98 KB) allows two per SM
 constexpr uint32_t kScanTileBytes = kScanRows * kRowBytes;
-
-// Warp roles of the tensor-core scan: NMT tiles of 16 query heads; the
-// NRS = 4 / NMT warps of a head tile split a key tile's rows (RW each); one
-// logsumexp partial per head per warp per key tile.
-template <int G>
-struct ScanShape {
-  static constexpr int NMT = G <= 16 ? 1 : G / 16;
-  static constexpr int NRS = kScanCWarps / NMT;
-  static constexpr int RW = kScanRows / NRS;
-  static constexpr int PPT = NRS;
-};
-
-template <int G>
-__global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
-  using S = ScanShape<G>;
-  extern __shared__ __align__(128) uint8_t scan_smem[];
-  uint64_t* full = reinterpret_cast<uint64_t*>(scan_smem + kScanStages * kScanTileBytes);
-  uint64_t* empty = full + kScanStages;
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kScanStages; ++s) {
-      mbar_init(&full[s], 32);       // one cp.async arrival per producer lane
-      mbar_init(&empty[s], kScanCWarps);
-    }
-    fence_mbar_init();
-  }
-  __syncthreads();
-
-  if (warp == kScanCWarps) {
-    // ---------------- producer: 16-byte cp.async, two whole rows per
-    // instruction (lanes 0-15 row 2j, lanes 16-31 row 2j+1), the 16-byte
-    // pieces of row r stored at piece ^ (r & 7); rows past the end zero-filled
-    const int piece = lane & 15, half = lane >> 4;
-    int it = 0;
-    const int t_end = min(a.total_tiles, (blockIdx.x + 1) * a.tpc);
-    for (int t = blockIdx.x * a.tpc; t < t_end; ++t) {
-      const int seg = t / a.n_tiles, tile = t - seg * a.n_tiles;
-      const int b = seg / a.n_kv;
-      const int L = effective_len(a.len, b, a.append, a.cap);
-      const int row0 = tile * kScanRows;
-      if (row0 >= L) continue;
-      const int nrows = min(kScanRows, L - row0);
-      const int s = it % kScanStages;
-      const uint32_t ph = (it / kScanStages) & 1;
-      if (!mbar_wait_bounded(&empty[s], ph ^ 1, kWaitLimit)) {
-        if (lane == 0) set_status(a.status, SPC_ERR_TIMEOUT);
-        break;
-      }
-      uint8_t* dst = scan_smem + (size_t)s * kScanTileBytes;
-      const uint16_t* src = a.K + ((size_t)seg * a.cap + row0) * kD + piece * 8;
-#pragma unroll 8
-      for (int j = 0; j < kScanRows / 2; ++j) {
-        const int r = 2 * j + half;
-        const bool ok = r < nrows;
-        cp_async16(dst + r * kRowBytes + ((piece ^ (r & 7)) << 4), src + (size_t)(ok ? r : 0) * kD, ok ? 16 : 0);
-      }
-      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(smem_u32(&full[s])) : "memory");
-      ++it;
-    }
-    // wait (bounded) until every copy issued has landed before leaving
-    for (int k = max(0, it - kScanStages); k < it; ++k)
-      mbar_wait_bounded(&full[k % kScanStages], (k / kScanStages) & 1, kWaitLimit);
-    return;
-  }
-
-  // ---------------- consumers: S = Q K^T on tensor cores (q split into bf16
-  // high + low parts, so the logits keep fp32 accuracy)
-  const int mt = warp % S::NMT, rs = warp / S::NMT;
-  const int gid = lane >> 2, tig = lane & 3, lm = lane >> 3, lr = lane & 7;
-  const int h_lo = mt * 16 + gid, h_hi = h_lo + 8;
-  uint32_t qh[8][4], ql[8][4];
-  int cur_seg = -1;
-  int it = 0;
-  const int t_end = min(a.total_tiles, (blockIdx.x + 1) * a.tpc);
-  for (int t = blockIdx.x * a.tpc; t < t_end; ++t) {
-    const int seg = t / a.n_tiles, tile = t - seg * a.n_tiles;
-    const int b = seg / a.n_kv, g = seg - b * a.n_kv;
-    const int L = effective_len(a.len, b, a.append, a.cap);
-    const int row0 = tile * kScanRows;
-    if (row0 >= L) continue;
-    const int nrows = min(kScanRows, L - row0);
-    const int s = it % kScanStages;
-    const uint32_t ph = (it / kScanStages) & 1;
-    if (seg != cur_seg) {
-      const float* qg = a.q + ((size_t)b * a.n_q + (size_t)g * G) * kD;
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int h = (e & 1) ? h_hi : h_lo;
-          const int c = ks * 16 + tig * 2 + ((e & 2) ? 8 : 0);
-          float2 v = make_float2(0.f, 0.f);
-          if (h < G) v = *reinterpret_cast<const float2*>(qg + (size_t)h * kD + c);
-          const float x = v.x * a.qscale, y = v.y * a.qscale;
-          const float xh = bf16_round(x), yh = bf16_round(y);
-          qh[ks][e] = pack_bf16(xh, yh);
-          ql[ks][e] = pack_bf16(x - xh, y - yh);
-        }
-      }
-      cur_seg = seg;
-    }
-    if (!mbar_wait_bounded(&full[s], ph, kWaitLimit)) {
-      if (lane == 0) set_status(a.status, SPC_ERR_TIMEOUT);
-      break;
-    }
-    const uint32_t base = smem_u32(scan_smem + (size_t)s * kScanTileBytes);
-    // logits are position-major: [segment][position][G]
-    float* lg = a.logits + ((size_t)seg * a.lstride + row0) * G;
-    float m_lo = -INFINITY, s_lo = 0.f, m_hi = -INFINITY, s_hi = 0.f;
-#pragma unroll 1
-    for (int sb = 0; sb < S::RW / 32; ++sb) {
-      const int r0 = rs * S::RW + sb * 32;
-      float acc[4][4];
-#pragma unroll
-      for (int n = 0; n < 4; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-      float acl[4][4];   // the q-low products: a second chain halves the MMA dependency depth
-#pragma unroll
-      for (int n = 0; n < 4; ++n) acl[n][0] = acl[n][1] = acl[n][2] = acl[n][3] = 0.f;
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-#pragma unroll
-        for (int np = 0; np < 2; ++np) {
-          const int row = r0 + np * 16 + ((lm >> 1) << 3) + lr;
-          const uint32_t addr = base + row * kRowBytes + (((ks * 2 + (lm & 1)) ^ (row & 7)) << 4);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(addr, b0, b1, b2, b3);
-          mma_bf16(acc[2 * np], qh[ks], b0, b1);
-          mma_bf16(acl[2 * np], ql[ks], b0, b1);
-          mma_bf16(acc[2 * np + 1], qh[ks], b2, b3);
-          mma_bf16(acl[2 * np + 1], ql[ks], b2, b3);
-        }
-      }
-#pragma unroll
-      for (int n = 0; n < 4; ++n) { acc[n][0] += acl[n][0]; acc[n][1] += acl[n][1]; acc[n][2] += acl[n][2]; acc[n][3] += acl[n][3]; }
-      // logits out; block max and sum of 2^(l - max) per head row
-      float bm_lo = -INFINITY, bm_hi = -INFINITY;
-#pragma unroll
-      for (int n = 0; n < 4; ++n) {
-        const int key = r0 + n * 8 + tig * 2;
-        const bool v0 = key < nrows, v1 = key + 1 < nrows;
-        if (!v0) acc[n][0] = acc[n][2] = -INFINITY;
-        if (!v1) acc[n][1] = acc[n][3] = -INFINITY;
-        if (h_lo < G) {
-          if (v0) lg[(size_t)key * G + h_lo] = acc[n][0];
-          if (v1) lg[(size_t)(key + 1) * G + h_lo] = acc[n][1];
-        }
-        if (h_hi < G) {
-          if (v0) lg[(size_t)key * G + h_hi] = acc[n][2];
-          if (v1) lg[(size_t)(key + 1) * G + h_hi] = acc[n][3];
-        }
-        bm_lo = fmaxf(bm_lo, fmaxf(acc[n][0], acc[n][1]));
-        bm_hi = fmaxf(bm_hi, fmaxf(acc[n][2], acc[n][3]));
-      }
-#pragma unroll
-      for (int o = 1; o <= 2; o <<= 1) {
-        bm_lo = fmaxf(bm_lo, __shfl_xor_sync(0xffffffffu, bm_lo, o));
-        bm_hi = fmaxf(bm_hi, __shfl_xor_sync(0xffffffffu, bm_hi, o));
-      }
-      float bs_lo = 0.f, bs_hi = 0.f;
-      if (bm_lo != -INFINITY) {
-#pragma unroll
-        for (int n = 0; n < 4; ++n) bs_lo += exp2f(acc[n][0] - bm_lo) + exp2f(acc[n][1] - bm_lo);
-      }
-      if (bm_hi != -INFINITY) {
-#pragma unroll
-        for (int n = 0; n < 4; ++n) bs_hi += exp2f(acc[n][2] - bm_hi) + exp2f(acc[n][3] - bm_hi);
-      }
-#pragma unroll
-      for (int o = 1; o <= 2; o <<= 1) {
-        bs_lo += __shfl_xor_sync(0xffffffffu, bs_lo, o);
-        bs_hi += __shfl_xor_sync(0xffffffffu, bs_hi, o);
-      }
-      lse2_combine(m_lo, s_lo, bm_lo, bs_lo);
-      lse2_combine(m_hi, s_hi, bm_hi, bs_hi);
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
-    if (tig == 0) {
-      const size_t pi = (size_t)tile * S::PPT + rs;
-      if (h_lo < G) a.part[((size_t)b * a.n_q + (size_t)g * G + h_lo) * a.n_parts + pi] = make_float2(m_lo, s_lo);
-      if (h_hi < G) a.part[((size_t)b * a.n_q + (size_t)g * G + h_hi) * a.n_parts + pi] = make_float2(m_hi, s_hi);
-    }
-    ++it;
-  }
-}
 
 // Key-major tensor-core scan for groups of up to 8 query heads. The key rows
 // are the M side of m16n8k16 (16 keys x 16 dims per ldmatrix.x4 from the
@@ -1210,22 +1022,19 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a) {
 
 // ============================================================== host side
 struct ScoreLayout {
-  size_t status, done, q, logits, part_scan, keys, total;
+  size_t status, done, q, logits, part_scan, lse, part1, keys, total;
   int n_tiles, ppt, n_parts, lstride;
 };
 
-#ifndef SPC_SCAN_TC
-#define SPC_SCAN_TC 1   // groups of 16+ heads: the tcgen05 scan (0: the mma.sync head-major scan)
-#endif
-
-static int scan_ppt(int G) {
-  if (G <= 8) return kScanKmWarps;
-  return SPC_SCAN_TC ? scan_tc_ppt(G) : kScanCWarps / (G <= 16 ? 1 : G / 16);
-}
+// Groups of up to 8 heads: the mma.sync key scan writes base-2 logits
+// [B][n_kv][cap][G] and the select folds them. Groups of 16+ heads: the two
+// tcgen05 passes of scan_tc.cu (no logits; one log2 group score per position).
+static int scan_ppt(int G) { return G <= 8 ? kScanKmWarps : scan_tc_ppt(G); }
 
 static ScoreLayout score_layout(int B, int H, int n_q, int n_kv, int cap) {
   ScoreLayout l{};
   const int Nq = n_q * kD;
+  const bool tc = n_q / n_kv >= 16;
   (void)H;
   l.n_tiles = (cap + kScanRows - 1) / kScanRows;
   l.ppt = scan_ppt(n_q / n_kv);
@@ -1236,8 +1045,11 @@ static ScoreLayout score_layout(int B, int H, int n_q, int n_kv, int cap) {
   l.status = take(2 * sizeof(int));
   l.done = l.status + sizeof(int);
   l.q = take(sizeof(float) * (size_t)B * Nq);
-  l.logits = take(sizeof(float) * (size_t)B * n_q * l.lstride);
+  // logits (G <= 8), or the log2 group scores (G >= 16)
+  l.logits = take(sizeof(float) * (size_t)B * (tc ? n_kv : n_q) * l.lstride);
   l.part_scan = take(sizeof(float2) * (size_t)B * n_q * l.n_parts);
+  l.lse = tc ? take(sizeof(float) * (size_t)B * n_q) : 0;
+  l.part1 = tc ? take(sizeof(float2) * (size_t)B * n_kv * l.n_tiles) : 0;
   l.keys = take(sizeof(uint32_t) * (size_t)B * n_kv * ((cap + 3) & ~3));
   l.total = off;
   return l;
@@ -1247,20 +1059,15 @@ size_t score_select_workspace(int B, int H, int n_q, int n_kv, int cap) {
   return score_layout(B, H, n_q, n_kv, cap).total;
 }
 
-// Groups of up to 8 heads take the key-major kernel, larger ones the
-// head-major one.
+// Groups of up to 8 heads: the key-major mma.sync kernel (larger groups run
+// the tcgen05 passes of scan_tc.cu).
 template <int G>
 static cudaError_t launch_scan(const ScanArgs& sa, int grid, cudaStream_t st) {
+  static_assert(G <= 8, "groups of 16+ heads use scan_tc.cu");
   const size_t smem = kScanStages * kScanTileBytes + 2 * kScanStages * sizeof(uint64_t);
-  if constexpr (G <= 8) {
-    cudaError_t e = set_func_attr((const void*)scan_kernel_km<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    scan_kernel_km<G><<<grid, kScanKmThreads, smem, st>>>(sa);
-  } else {
-    cudaError_t e = set_func_attr((const void*)scan_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    scan_kernel<G><<<grid, kScanThreads, smem, st>>>(sa);
-  }
+  cudaError_t e = set_func_attr((const void*)scan_kernel_km<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  scan_kernel_km<G><<<grid, kScanKmThreads, smem, st>>>(sa);
   return cudaGetLastError();
 }
 
@@ -1427,34 +1234,31 @@ int score_select_launch(const ScoreSelectCall& c) {
     sa.n_q = c.n_q; sa.n_kv = c.n_kv; sa.cap = c.cap; sa.lstride = l.lstride; sa.n_tiles = l.n_tiles;
     sa.total_tiles = c.B * c.n_kv * l.n_tiles; sa.append = c.append; sa.n_parts = l.n_parts;
     sa.qscale = kLog2e / sqrtf((float)kD);
-    if (SPC_SCAN_TC && G >= 16) {
+    if (G >= 16) {
       ScanTcCall tc{};
-      tc.K = sa.K; tc.q = sa.q; tc.len = sa.len; tc.logits = sa.logits; tc.part = sa.part; tc.status = status;
+      tc.K = sa.K; tc.q = sa.q; tc.len = sa.len; tc.part = sa.part; tc.status = status;
       tc.B = c.B; tc.n_q = c.n_q; tc.n_kv = c.n_kv; tc.cap = c.cap; tc.lstride = l.lstride;
       tc.n_tiles = l.n_tiles; tc.total_tiles = sa.total_tiles; tc.append = c.append; tc.n_parts = l.n_parts;
       tc.qscale = sa.qscale;
       const int rc = scan_tc_launch(tc, G, c.stream);
       if (rc != SPC_OK) return rc;
     } else {
-    // each CTA takes a run of consecutive tiles
-    if (kScanTilesPerCta > 0) {
-      sa.tpc = kScanTilesPerCta;
-    } else {
-      const long long slots = (long long)kScanCtasPerSm * (device_sm_count() > 0 ? device_sm_count() : 1);
-      sa.tpc = (int)((sa.total_tiles + slots - 1) / slots);
-      if (sa.tpc < 1) sa.tpc = 1;
-    }
-    const int grid = (sa.total_tiles + sa.tpc - 1) / sa.tpc;
-    switch (G) {
-      case 1: e = launch_scan<1>(sa, grid, st); break;
-      case 2: e = launch_scan<2>(sa, grid, st); break;
-      case 4: e = launch_scan<4>(sa, grid, st); break;
-      case 8: e = launch_scan<8>(sa, grid, st); break;
-      case 16: e = launch_scan<16>(sa, grid, st); break;
-      case 32: e = launch_scan<32>(sa, grid, st); break;
-      default: e = launch_scan<64>(sa, grid, st); break;
-    }
-    if (e != cudaSuccess) return SPC_ERR_CUDA;
+      // each CTA takes a run of consecutive tiles
+      if (kScanTilesPerCta > 0) {
+        sa.tpc = kScanTilesPerCta;
+      } else {
+        const long long slots = (long long)kScanCtasPerSm * (device_sm_count() > 0 ? device_sm_count() : 1);
+        sa.tpc = (int)((sa.total_tiles + slots - 1) / slots);
+        if (sa.tpc < 1) sa.tpc = 1;
+      }
+      const int grid = (sa.total_tiles + sa.tpc - 1) / sa.tpc;
+      switch (G) {
+        case 1: e = launch_scan<1>(sa, grid, st); break;
+        case 2: e = launch_scan<2>(sa, grid, st); break;
+        case 4: e = launch_scan<4>(sa, grid, st); break;
+        default: e = launch_scan<8>(sa, grid, st); break;
+      }
+      if (e != cudaSuccess) return SPC_ERR_CUDA;
     }
   }
 
@@ -1472,14 +1276,36 @@ int score_select_launch(const ScoreSelectCall& c) {
     sa.n_sink = c.n_sink; sa.n_recent = c.n_recent; sa.append = c.append;
     sa.n_parts = l.n_parts; sa.ppt = l.ppt; sa.kstride = (c.cap + 3) & ~3;
     int rc;
-    switch (G) {
-      case 1: rc = launch_select<1>(sa, c.B * c.n_kv, st); break;
-      case 2: rc = launch_select<2>(sa, c.B * c.n_kv, st); break;
-      case 4: rc = launch_select<4>(sa, c.B * c.n_kv, st); break;
-      case 8: rc = launch_select<8>(sa, c.B * c.n_kv, st); break;
-      case 16: rc = launch_select<16>(sa, c.B * c.n_kv, st); break;
-      case 32: rc = launch_select<32>(sa, c.B * c.n_kv, st); break;
-      default: rc = launch_select<64>(sa, c.B * c.n_kv, st); break;
+    if (G >= 16) {
+      // normalisers, then the second pass over the keys writes one log2 group
+      // score per position; the select ranks them as a group of one head
+      // with a zero normaliser
+      ScanTcCall tc{};
+      tc.K = static_cast<const uint16_t*>(c.K_dlm);
+      tc.q = reinterpret_cast<const float*>(ws + l.q);
+      tc.len = c.len;
+      tc.part = reinterpret_cast<float2*>(ws + l.part_scan);
+      tc.lse = reinterpret_cast<float*>(ws + l.lse);
+      tc.gscore = reinterpret_cast<float*>(ws + l.logits);
+      tc.status = status;
+      tc.B = c.B; tc.n_q = c.n_q; tc.n_kv = c.n_kv; tc.cap = c.cap; tc.lstride = l.lstride;
+      tc.n_tiles = l.n_tiles; tc.total_tiles = c.B * c.n_kv * l.n_tiles; tc.append = c.append;
+      tc.n_parts = l.n_parts; tc.qscale = kLog2e / sqrtf((float)kD);
+      float2* part1 = reinterpret_cast<float2*>(ws + l.part1);
+      rc = scan_tc_scores_launch(tc, G, part1, l.n_tiles, c.stream);
+      if (rc != SPC_OK) return rc;
+      sa.part = part1;
+      sa.n_q = c.n_kv;
+      sa.n_parts = l.n_tiles;
+      sa.ppt = 1;
+      rc = launch_select<1>(sa, c.B * c.n_kv, st);
+    } else {
+      switch (G) {
+        case 1: rc = launch_select<1>(sa, c.B * c.n_kv, st); break;
+        case 2: rc = launch_select<2>(sa, c.B * c.n_kv, st); break;
+        case 4: rc = launch_select<4>(sa, c.B * c.n_kv, st); break;
+        default: rc = launch_select<8>(sa, c.B * c.n_kv, st); break;
+      }
     }
     if (rc != SPC_OK) return rc;
   }

@@ -34,21 +34,27 @@ struct ScoreSelectCall {
 
 size_t score_select_workspace(int B, int H, int n_q, int n_kv, int cap);
 
-// Key scan on the 5th-generation tensor cores for groups of 16, 32 or 64
-// query heads (scan_tc.cu): base-2 logits [segment][position][G] and
-// scan_tc_ppt(G) logsumexp partials per (head, 128-position tile).
+// Retrieval head for groups of 16, 32 or 64 query heads on the 5th-generation
+// tensor cores (scan_tc.cu), in two passes over the key cache:
+// scan_tc_launch writes scan_tc_ppt(G) logsumexp partials per (head,
+// 128-position tile) into `part`; scan_tc_scores_launch folds them into
+// `lse` [B][n_q] (base 2), writes the log2 group score of every position into
+// `gscore` [B * n_kv][lstride], and the partials of a zero normaliser (one
+// per tile) into part1 [B * n_kv][n_parts1] for the radix select.
 struct ScanTcCall {
   const uint16_t* K;
   const float* q;
   const int32_t* len;
-  float* logits;
   float2* part;
+  float* lse;
+  float* gscore;
   int* status;
   int B, n_q, n_kv, cap, lstride, n_tiles, total_tiles, append, n_parts, tpc;
   float qscale;
 };
 int scan_tc_ppt(int G);
 int scan_tc_launch(ScanTcCall c, int G, void* stream);
+int scan_tc_scores_launch(ScanTcCall c, int G, float2* part1, int n_parts1, void* stream);
 int score_select_launch(const ScoreSelectCall& c);
 
 int elastic_diff_launch(const int32_t* selected, const int32_t* prev, int32_t* next,
