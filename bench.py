@@ -182,11 +182,11 @@ NCU_TRAFFIC = {
     "key_scan": {"source": "sparse_kv_cache_retrieval_gb300/csrc/score_select.cu",
                  "sha256": "e933ecb3c598448f359b57bd3cd412e49d15a37f17859c100eaf23e9e2de7aae",
                  "bytes_per_unit": (67141120 + 768) / 262144, "unit": "256-byte key row"},
-    # tcgen05 key scan, MQA (64 heads, one KV head), 8 requests x 16 384 positions:
-    # 33 847 040 B DRAM read + 321 536 B write (the logits stayed in L2)
+    # tcgen05 key scan pass 1 (logsumexp partials), MQA (64 heads, one KV head),
+    # 8 requests x 16 384 positions: 33 868 288 B DRAM read + 256 B write
     "key_scan_tc": {"source": "sparse_kv_cache_retrieval_gb300/csrc/scan_tc.cu",
-                    "sha256": "899ff4ad1ab3a6322b10d0ae365cb9e7a5e4b5128fc56a690329ab92a2e6ac77",
-                    "bytes_per_unit": (33847040 + 321536) / 131072, "unit": "256-byte key row"},
+                    "sha256": "0c854d1a059b69f6e82eb17c11eeb30d49c7c43622413e22dd78265ffd347588",
+                    "bytes_per_unit": (33868288 + 256) / 131072, "unit": "256-byte key row"},
     # attention, 70B shape: 2 layers x 8 requests x 8 KV heads x 4096 kept rows:
     # 272 741 888 B read + 4 417 280 B written
     "attention": {"source": "sparse_kv_cache_retrieval_gb300/csrc/sparse_attn.cu",
