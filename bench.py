@@ -178,10 +178,10 @@ NCU_TRAFFIC = {
                "sha256": "4840cb43e2a9779e4a4b7c33986b7fade82263e0181e55f173485d38404431ee",
                "bytes_per_unit": 273054720 / 1066620, "unit": "moved 256-byte row (host-link bytes)"},
     # key scan over 32 768 positions x 8 KV heads (second of two launches):
-    # 67 141 120 B DRAM read + 768 B write
+    # 67 141 632 B DRAM read + 5 376 B write
     "key_scan": {"source": "sparse_kv_cache_retrieval_gb300/csrc/score_select.cu",
-                 "sha256": "e933ecb3c598448f359b57bd3cd412e49d15a37f17859c100eaf23e9e2de7aae",
-                 "bytes_per_unit": (67141120 + 768) / 262144, "unit": "256-byte key row"},
+                 "sha256": "784d5dc68a4f6cfb41d0929b5407d4ebb5f94b1e8b903047fd202c0aeec49bde",
+                 "bytes_per_unit": (67141632 + 5376) / 262144, "unit": "256-byte key row"},
     # tcgen05 key scan pass 1 (logsumexp partials), MQA (64 heads, one KV head),
     # 8 requests x 16 384 positions: 33 868 288 B DRAM read + 256 B write
     "key_scan_tc": {"source": "sparse_kv_cache_retrieval_gb300/csrc/scan_tc.cu",
