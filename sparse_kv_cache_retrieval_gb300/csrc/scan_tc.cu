@@ -53,6 +53,7 @@
 
 #include "spc_device.cuh"
 #include "spc_internal.h"
+#include "spc_tc.cuh"
 
 namespace spc {
 
@@ -80,10 +81,8 @@ struct TcShape {
   static constexpr int kTmemCols = 2 * N < 32 ? 32 : 2 * N;        // two accumulators
   static constexpr size_t kSmem = 1024 /* alignment slack */ + (size_t)kTcStages * kTcTileBytes + kQBytes +
                                   kXch + 16 * sizeof(uint64_t) + 16;
-  // instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major,
-  // N >> 3 at bit 17, M >> 4 at bit 24
-  static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
-                                     ((uint32_t)(kTcRows >> 4) << 24);
+  // instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major
+  static constexpr uint32_t kIdesc = umma_idesc_bf16(kTcRows, N, false);
 };
 
 int scan_tc_ppt(int G) {
@@ -92,60 +91,6 @@ int scan_tc_ppt(int G) {
 }
 
 // ---------------------------------------------------------------- PTX wrappers
-// Shared-memory matrix descriptor of a K-major operand with the 128-byte
-// swizzle: start address >> 4, leading byte offset 16 (unused for this
-// layout), stride between 8-row groups 1024 bytes, descriptor version 1,
-// layout type 2 (128-byte swizzle).
-__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
-  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(16 >> 4) << 16) | ((uint64_t)(1024 >> 4) << 32) |
-         (1ull << 46) | (2ull << 61);
-}
-
-__device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accumulate) {
-  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-               :: "r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
-}
-
-// arrives once on `bar` when every tcgen05 operation this thread issued before has completed
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-               :: "r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// 32 consecutive fp32 columns of this warp's 32 TMEM lanes (one lane per thread)
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-// 16 consecutive fp32 columns
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
   asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
                :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
@@ -201,9 +146,7 @@ __global__ void __launch_bounds__(TcShape<G>::kThreads, 1) scan_tc_kernel(const 
     fence_mbar_init();
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                 :: "r"(smem_u32(tmem_slot)), "n"(S::kTmemCols) : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    tmem_alloc<S::kTmemCols>(tmem_slot);
   }
   tc_fence_before();
   __syncthreads();
@@ -287,7 +230,7 @@ __global__ void __launch_bounds__(TcShape<G>::kThreads, 1) scan_tc_kernel(const 
                        "r"(lo[3]) : "memory");
         }
         // generic-proxy writes made visible to the tensor core's async proxy
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        fence_proxy_async_smem();
         __syncwarp();
         cur_seg = seg;
       }
@@ -435,8 +378,7 @@ __global__ void __launch_bounds__(TcShape<G>::kThreads, 1) scan_tc_kernel(const 
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "n"(S::kTmemCols)
-                 : "memory");
+    tmem_dealloc<S::kTmemCols>(tmem);
   }
 }
 
@@ -478,26 +420,6 @@ __global__ void __launch_bounds__(kFoldThreads) lse_fold_kernel(ScanTcCall a, in
 }
 
 // ---------------------------------------------------------------- host side
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn encode_tiled() {
-  static std::once_flag once;
-  static EncodeTiledFn fn = nullptr;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q{};
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-    else
-      cudaGetLastError();
-  });
-  return fn;
-}
-
 template <int G, int PASS>
 static cudaError_t launch_tc(const CUtensorMap& map, const ScanTcCall& c, int grid, cudaStream_t st) {
   const size_t smem = TcShape<G>::kSmem;
@@ -509,18 +431,12 @@ static cudaError_t launch_tc(const CUtensorMap& map, const ScanTcCall& c, int gr
 }
 
 static int scan_tc_pass(ScanTcCall c, int G, int pass, cudaStream_t st) {
-  EncodeTiledFn enc = encode_tiled();
-  if (!enc) return SPC_ERR_CUDA;
   // K_dlm as [segment = b * n_kv + g][position][dim], boxes of 128 positions x 64 dims
   CUtensorMap map;
-  const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)c.cap, (cuuint64_t)c.B * c.n_kv};
-  const cuuint64_t strides[2] = {(cuuint64_t)kRowBytes, (cuuint64_t)c.cap * kRowBytes};
-  const cuuint32_t box[3] = {64, (cuuint32_t)kTcRows, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(c.K), dims, strides, box, estr,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return SPC_ERR_CUDA;
+  const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)c.cap, (uint64_t)c.B * c.n_kv};
+  const uint64_t strides[2] = {(uint64_t)kRowBytes, (uint64_t)c.cap * kRowBytes};
+  const uint32_t box[3] = {64, (uint32_t)kTcRows, 1};
+  if (!tensor_map_bf16_sw128(&map, c.K, 3, dims, strides, box)) return SPC_ERR_CUDA;
   // one wave: one CTA per SM, each a run of consecutive tiles
   const int sms = device_sm_count() > 0 ? device_sm_count() : 1;
   c.tpc = (c.total_tiles + sms - 1) / sms;

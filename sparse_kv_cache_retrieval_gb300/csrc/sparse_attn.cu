@@ -594,10 +594,11 @@ static void attn_plan(int n_layers, int B, int n_kv, int budget, int* C, int* n_
 }
 
 size_t attn_workspace(int n_layers, int B, int n_q, int n_kv, int budget) {
-  int C, ns, cpc, nc;
-  attn_plan(n_layers, B, n_kv, budget, &C, &ns, &cpc, &nc);
   const size_t nseg = (size_t)n_layers * B * n_kv;
   const size_t cnt = (nseg * sizeof(uint32_t) + 255) & ~size_t(255);
+  if (n_q / n_kv == attn_tc_group()) return kAttnStatusBytes + cnt + attn_tc_extra_bytes(n_layers, B, n_kv, budget);
+  int C, ns, cpc, nc;
+  attn_plan(n_layers, B, n_kv, budget, &C, &ns, &cpc, &nc);
   const size_t part = ns > 1 ? nseg * ns * (size_t)(n_q / n_kv) * kPartStride * sizeof(float) : 0;
   return kAttnStatusBytes + cnt + part;
 }
@@ -657,6 +658,17 @@ int attn_launch(const void* q, const spc_kv_view* views, const int32_t* selected
   }
 #endif
   aa.B = B; aa.n_q = n_q; aa.n_kv = n_kv; aa.K = budget;
+  if (n_q / n_kv == attn_tc_group()) {
+    // 64 heads per KV head: both products on tcgen05 (attn_tc.cu)
+    AttnTcCall c{};
+    c.q = aa.q; c.views = views; c.selected = selected; c.slot_pos = slot_pos; c.out = out;
+    c.part = aa.part; c.counters = aa.counters; c.status = aa.status;
+    c.B = B; c.n_q = n_q; c.n_kv = n_kv; c.K = budget;
+    c.scale2 = scale * kLog2e;
+    c.wait_limit = aa.wait_limit;
+    c.starve = aa.starve;
+    return attn_tc_launch(c, n_layers, stream);
+  }
   attn_plan(n_layers, B, n_kv, budget, &aa.C, &aa.n_split, &aa.cpc, &aa.n_chunks);
   aa.scale2 = scale * kLog2e;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -667,8 +679,7 @@ int attn_launch(const void* q, const spc_kv_view* views, const int32_t* selected
     case 4: e = launch_attn<4>(aa, (int)nseg, st); break;
     case 8: e = launch_attn<8>(aa, (int)nseg, st); break;
     case 16: e = launch_attn<16>(aa, (int)nseg, st); break;
-    case 32: e = launch_attn<32>(aa, (int)nseg, st); break;
-    default: e = launch_attn<64>(aa, (int)nseg, st); break;
+    default: e = launch_attn<32>(aa, (int)nseg, st); break;
   }
   return e == cudaSuccess ? SPC_OK : SPC_ERR_CUDA;
 }

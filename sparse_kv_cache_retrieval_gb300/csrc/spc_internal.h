@@ -1,6 +1,7 @@
 // Host-side declarations shared by the translation units of libspc.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstddef>
@@ -34,6 +35,13 @@ struct ScoreSelectCall {
 
 size_t score_select_workspace(int B, int H, int n_q, int n_kv, int cap);
 
+// A tiled TMA tensor map of a bf16 tensor with the 128-byte swizzle: `rank`
+// dimensions (innermost first), byte strides of dimensions 1 .. rank - 1,
+// the box to copy. Encoded through the driver entry point of
+// cuTensorMapEncodeTiled (looked up once); false when that fails.
+bool tensor_map_bf16_sw128(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                           const uint64_t* strides, const uint32_t* box);
+
 // Retrieval head for groups of 16, 32 or 64 query heads on the 5th-generation
 // tensor cores (scan_tc.cu), in two passes over the key cache:
 // scan_tc_launch writes scan_tc_ppt(G) logsumexp partials per (head,
@@ -55,6 +63,32 @@ struct ScanTcCall {
 int scan_tc_ppt(int G);
 int scan_tc_launch(ScanTcCall c, int G, void* stream);
 int scan_tc_scores_launch(ScanTcCall c, int G, float2* part1, int n_parts1, void* stream);
+
+// Sparse decode attention of groups of 64 query heads (attn_tc.cu, tcgen05):
+// the arguments of spc_sparse_decode_attn with the workspace split into the
+// status word, one merge counter per (layer, request, KV head), and then
+// attn_tc_extra_bytes of split partials and per-CTA tensor maps (from
+// `part` on, 256-byte aligned). attn_tc_launch fills the tiling fields (nt,
+// tpc, total, max_pieces) and `maps`.
+struct AttnTcCall {
+  const uint16_t* q;
+  const spc_kv_view* views;
+  const int32_t* selected;
+  const int32_t* slot_pos;
+  float* out;
+  float* part;
+  uint8_t* maps;
+  uint32_t* counters;
+  int* status;
+  int B, n_q, n_kv, K;
+  int nt, tpc, total, max_pieces;
+  float scale2;
+  long long wait_limit;
+  int starve;
+};
+int attn_tc_group();
+size_t attn_tc_extra_bytes(int n_layers, int B, int n_kv, int budget);
+int attn_tc_launch(AttnTcCall c, int n_layers, void* stream);
 int score_select_launch(const ScoreSelectCall& c);
 
 int elastic_diff_launch(const int32_t* selected, const int32_t* prev, int32_t* next,

@@ -202,20 +202,15 @@ def test_fill_slots_bit_exact(source):
         assert np.array_equal(got, want), f"request {b}"
 
 
-def _attn_case(rng, L, B, n_q, n_kv, K, cap, use_slots, n_valid=None, empty_group=False):
-    """Returns GPU output and oracle output for one attention launch."""
+def _attn_case(rng, L, B, n_q, n_kv, K, cap, use_slots, n_valid=None, empty_group=False, q_gain=1.5,
+               ramp=False, poison=False):
+    """Returns GPU output and oracle output for one attention launch.
+
+    ramp: K rows grow in norm with their row index (later tiles hold larger
+    logits, so a running maximum keeps rising); poison: rows of the K/V
+    buffers that no kept index names hold NaN (they must not reach the output).
+    """
     d = 128
-    caches, kp, vp, rows, use = [], [], [], [], []
-    for l in range(L):
-        for b in range(B):
-            nrows = K if use_slots else cap
-            kv = rng.standard_normal((2, n_kv, nrows, d)).astype(np.float32)
-            bits = O.round_to_bf16(kv.astype(np.float64))
-            t = torch.from_numpy(bits.view(np.int16)).to(DEV)
-            caches.append((bits, t))
-            kp.append(t[0].data_ptr()); vp.append(t[1].data_ptr()); rows.append(nrows); use.append(use_slots)
-    views = spc.to_device_bytes(spc.kv_views(kp, vp, rows, use), DEV)
-    q = O.round_to_bf16(rng.standard_normal((L, B, n_q, d)) * 1.5)
     sel = np.full((B, n_kv, K), -1, np.int64)
     slot = np.full((B, n_kv, K), -1, np.int64)
     kept = []
@@ -231,6 +226,26 @@ def _attn_case(rng, L, B, n_q, n_kv, K, cap, use_slots, n_valid=None, empty_grou
             slot[b, g, sl] = pos
             kb.append(np.sort(sl) if use_slots else pos)
         kept.append(kb)
+    caches, kp, vp, rows, use = [], [], [], [], []
+    for l in range(L):
+        for b in range(B):
+            nrows = K if use_slots else cap
+            kv = rng.standard_normal((2, n_kv, nrows, d)).astype(np.float32)
+            if ramp:
+                kv[0] *= (1.0 + 3.0 * np.arange(nrows) / nrows)[None, :, None].astype(np.float32)
+            bits = O.round_to_bf16(kv.astype(np.float64))
+            t = torch.from_numpy(bits.view(np.int16)).to(DEV)
+            if poison:
+                raw = bits.view(np.int16).copy()
+                for g in range(n_kv):
+                    unused = np.ones(nrows, bool)
+                    unused[kept[b][g]] = False
+                    raw[:, g, unused] = np.int16(0x7FC0)       # bf16 quiet NaN
+                t = torch.from_numpy(raw).to(DEV)
+            caches.append((bits, t))
+            kp.append(t[0].data_ptr()); vp.append(t[1].data_ptr()); rows.append(nrows); use.append(use_slots)
+    views = spc.to_device_bytes(spc.kv_views(kp, vp, rows, use), DEV)
+    q = O.round_to_bf16(rng.standard_normal((L, B, n_q, d)) * q_gain)
     out = torch.full((L, B, n_q, d), 7.0, dtype=torch.float32, device=DEV)
     ws = torch.zeros(spc.spc_sparse_decode_attn_workspace_size(L, B, n_q, n_kv, d, K), dtype=torch.uint8,
                      device=DEV)
@@ -258,6 +273,14 @@ ATTN_CASES = [
     (1, 1, 64, 8, 4096, 8192, 1, None),      # 70B shape, max budget
     (1, 1, 64, 1, 512, 2000, 0, None),       # MQA
     (1, 1, 16, 1, 64, 100, 1, 1),            # one kept row per group
+    # 64 heads per KV head (the tensor-core kernel): CTA runs split segments,
+    # partials merged by the last CTA of each segment
+    (2, 3, 64, 1, 4096, 8192, 1, 3000),      # max budget, 16 CTAs per segment
+    (3, 4, 64, 1, 4096, 4096, 1, 3900),      # 12 segments, 3 tiles per CTA: runs cross segment ends
+    (1, 1, 64, 1, 1000, 3000, 1, None),      # budget not a multiple of the 128-row tile
+    (2, 1, 128, 2, 700, 2000, 0, None),      # two KV heads, positions into a full cache
+    (1, 1, 64, 1, 128, 128, 1, None),        # one tile, one CTA: no partials
+    (3, 1, 64, 1, 256, 300, 1, 2),           # two kept rows in a 256-row budget
 ]
 
 
@@ -268,6 +291,36 @@ def test_attention_parity(L, B, n_q, n_kv, K, cap, use_slots, n_valid):
     err = np.abs(got - want)
     assert err.max() <= ATTN_ATOL
     assert np.all(err <= 2e-5 + 1e-4 * np.abs(want)), f"max err {err.max():.3g}"
+
+
+@pytest.mark.parametrize("n_q,n_kv", [(64, 1), (32, 8)])
+def test_attention_rising_maximum(n_q, n_kv):
+    """Large logits that grow tile by tile: the running maximum is raised and
+    the partial sums and outputs rescaled many times."""
+    rng = np.random.default_rng(11 + n_q)
+    got, want = _attn_case(rng, 2, 2, n_q, n_kv, 2048, 2048, 1, None, q_gain=12.0, ramp=True)
+    err = np.abs(got - want)
+    assert np.all(err <= 2e-5 + 1e-4 * np.abs(want)), f"max err {err.max():.3g}"
+
+
+@pytest.mark.parametrize("n_q,n_kv,use_slots", [(64, 1, 1), (64, 1, 0), (32, 8, 1)])
+def test_attention_ignores_rows_not_kept(n_q, n_kv, use_slots):
+    """NaN in every K/V row that no kept index names leaves the output finite
+    and equal to the oracle's."""
+    rng = np.random.default_rng(21 + n_q + use_slots)
+    got, want = _attn_case(rng, 1, 2, n_q, n_kv, 1024, 2048, use_slots, 700, poison=True)
+    assert np.all(np.isfinite(got))
+    err = np.abs(got - want)
+    assert np.all(err <= 2e-5 + 1e-4 * np.abs(want)), f"max err {err.max():.3g}"
+
+
+@pytest.mark.parametrize("n_q,n_kv", [(64, 1), (8, 2)])
+def test_attention_empty_group_is_zero_any_shape(n_q, n_kv):
+    rng = np.random.default_rng(6 + n_q)
+    got, want = _attn_case(rng, 2, 2, n_q, n_kv, 384, 500, 1, None, empty_group=True)
+    G = n_q // n_kv
+    assert np.all(got[:, :, :G] == 0.0)
+    assert np.abs(got - want).max() <= 2e-5 + 1e-4 * np.abs(want).max()
 
 
 def test_attention_empty_group_is_zero():

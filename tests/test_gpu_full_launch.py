@@ -101,6 +101,13 @@ def test_cfg5_all_80_layers_bench_launch_configuration():
     _gqa_full_launch("cfg5", 2, [0, 1, 15, 16, 40, 79])
 
 
+def test_cfg5_mqa_all_80_layers_bench_launch_configuration():
+    # the MQA variant: all 64 query heads on one KV head (the tensor-core
+    # attention, 16 layers x 8 requests x 32 tiles per launch over 152 CTAs,
+    # so runs of tiles cross segment boundaries and segments merge partials)
+    _gqa_full_launch("cfg5mqa", 2, [0, 1, 15, 16, 79])
+
+
 def test_mla_all_layers_bench_launch_configuration():
     cfg = CONFIGS["mla"]
     tid = "full launch mla (27 layers)"
