@@ -183,15 +183,21 @@ NCU_TRAFFIC = {
                  "sha256": "784d5dc68a4f6cfb41d0929b5407d4ebb5f94b1e8b903047fd202c0aeec49bde",
                  "bytes_per_unit": (67141632 + 5376) / 262144, "unit": "256-byte key row"},
     # tcgen05 key scan pass 1 (logsumexp partials), MQA (64 heads, one KV head),
-    # 8 requests x 16 384 positions: 33 868 288 B DRAM read + 256 B write
+    # 8 requests x 16 384 positions: 33 868 800 B DRAM read + 256 B write
     "key_scan_tc": {"source": "sparse_kv_cache_retrieval_gb300/csrc/scan_tc.cu",
-                    "sha256": "0c854d1a059b69f6e82eb17c11eeb30d49c7c43622413e22dd78265ffd347588",
-                    "bytes_per_unit": (33868288 + 256) / 131072, "unit": "256-byte key row"},
+                    "sha256": "099c6371c324c763fd40e0f03ab5db4f87efafd761d83ea305d8af6ac1a4ddfd",
+                    "bytes_per_unit": (33868800 + 256) / 131072, "unit": "256-byte key row"},
     # attention, 70B shape: 2 layers x 8 requests x 8 KV heads x 4096 kept rows:
     # 272 741 888 B read + 4 417 280 B written
     "attention": {"source": "sparse_kv_cache_retrieval_gb300/csrc/sparse_attn.cu",
                   "sha256": "683d9635124b692bf486c0c1b6e497acc135ba475d6c22e67bce765f4a6e9d18",
                   "bytes_per_unit": (272741888 + 4417280) / 524288, "unit": "512-byte K+V row"},
+    # tcgen05 attention, MQA (64 heads, one KV head): 16 layers x 8 requests x
+    # 4096 kept rows (layer 0 by position, layers 1-15 through the slots):
+    # 271 034 368 B DRAM read + 3 009 280 B written
+    "attention_tc": {"source": "sparse_kv_cache_retrieval_gb300/csrc/attn_tc.cu",
+                     "sha256": "9f8bd93a1b9ff9d18bf977ea9a71782fc4371fe5251e01e114bab80c41f12ae6",
+                     "bytes_per_unit": (271034368 + 3009280) / 524288, "unit": "512-byte K+V row"},
     # MLA: gather of decode step 0, 221 loads x 27 layers = 5 967 latent rows;
     # 214 812 system-memory sectors (6 873 984 B) over the host link + 12 032 B DRAM read
     "mla_gather": {"source": "sparse_kv_cache_retrieval_gb300/csrc/mla.cu",
@@ -226,7 +232,7 @@ def traffic_units(cfg) -> dict:
     if cfg.mla:
         return {"gather": ("mla_gather", 1152), "key_scan": ("mla_scan", 1152), "attention": ("mla_attention", 1152)}
     return {"gather": ("gather", 256), "key_scan": ("key_scan_tc" if cfg.G >= 16 else "key_scan", 256),
-            "attention": ("attention", 512)}
+            "attention": ("attention_tc" if cfg.G == 64 else "attention", 512)}
 
 
 def ncu_traffic(kind: str, units: float):

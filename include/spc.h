@@ -275,7 +275,9 @@ int spc_store_layer(void* store, const void* src, int n_kv, int d, int cap, int 
  *            bf16 [n_kv][rows][d], 16-byte aligned.
  * selected, slot_pos int32 [B][n_kv][budget] (shared by all layers).
  * out        fp32 [n_layers][B][n_q][d].
- * workspace  device scratch of spc_sparse_decode_attn_workspace_size() bytes,
+ * workspace  device scratch of spc_sparse_decode_attn_workspace_size() bytes
+ *            for this call's shapes (the size is not monotone in n_layers: a
+ *            caller that launches several layer counts sizes it for each),
  *            256-byte aligned, ZERO-FILLED BEFORE ITS FIRST USE (calls leave
  *            it ready). Its first int32 is the device status word: 0, or
  *            SPC_ERR_TIMEOUT when a bounded wait of the kernel gave up (the
@@ -283,6 +285,9 @@ int spc_store_layer(void* store, const void* src, int n_kv, int d, int cap, int 
  *            clears it.
  * Limits: d = 128, G in {1,2,4,8,16,32,64}, 1 <= B <= 64, n_layers * B <=
  * 65535, budget <= 4096, scale > 0.
+ * G = 64 runs on the tcgen05 tensor cores with TMA loads (K and V of slot
+ * views as tiles of contiguous rows, positions as row gathers); the view's
+ * k and v then also need 16-byte aligned rows (d = 128 bf16: always).
  * ---------------------------------------------------------------------- */
 typedef struct spc_kv_view {
   const void* k;

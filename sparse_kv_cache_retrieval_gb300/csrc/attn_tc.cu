@@ -18,16 +18,23 @@
 // Tiles of 128 kept rows. For each tile:
 //  * S[128][128] = Q2 K^T (M = 128, N = 128 rows, K = 128 dims): Q2 is the
 //    group's 64 query rows written twice (rows h and h + 64 are both head h),
-//    so that the same tile shape carries the two bf16 parts of P below.
+//    so that the same tile shape carries the two bf16 parts of P below. Q2
+//    sits in tensor memory (the A operand of tcgen05.mma may live there), in
+//    two buffers by segment parity, written by the softmax threads one
+//    segment ahead.
 //  * Softmax in base 2 by 8 warps: TMEM lane (row) r is read by two warps,
 //    each taking 32 of the 64 kept rows [64 (r / 64), +64) of head r % 64, so
-//    every logit is exponentiated once. The four threads of a head exchange
-//    their maxima through shared memory and keep one running maximum, raised
-//    only when a tile's maximum exceeds it by more than 8 (weights stay
-//    <= 2^8); then l and the head's accumulator rows are rescaled.
-//  * P (fp32) is split into bf16 high and low parts, written to shared memory
-//    as the A operand: rows [0, 64) the high parts, rows [64, 128) the low
-//    parts (K-major, 128-byte swizzle), so the weights keep ~16 bits.
+//    every logit is exponentiated once. The four threads of a head (in warps
+//    q, q + 2, q + 4, q + 6) exchange their maxima through shared memory and
+//    keep one running maximum, raised only when a tile's maximum exceeds it
+//    by more than 8 (weights stay <= 2^8); then l and the head's accumulator
+//    rows are rescaled.
+//  * P (fp32) is split into two bf16 parts by bit selection -- the top 16
+//    bits of p, then the top 16 bits of the (exact) remainder -- and written
+//    to shared memory as the A operand: rows [0, 64) the high parts, rows
+//    [64, 128) the low parts (K-major, 128-byte swizzle), so the weights keep
+//    ~16 bits. Two P buffers: the softmax of tile t + 1 does not wait for the
+//    O of tile t.
 //  * O[128][128] += P V (M = 128, N = 128 dims, K = 128 rows; V is an
 //    MN-major operand). Head h's output is O[h] + O[h + 64] divided by l.
 // The products of bf16 operands are exact in the fp32 accumulators.
@@ -43,13 +50,13 @@
 //
 // Warp roles in one CTA per SM (persistent: a contiguous run of tiles, which
 // may cover the end of one segment and the start of the next):
-//  * warps 0-7: softmax and the segment epilogue (two warps per TMEM lane
-//    quadrant);
-//  * warp 8: K producer (and the Q2 operand by TMA at a segment's start);
-//  * warp 9: V producer; each ring has two 32 KiB slots;
-//  * warp 10: allocates tensor memory (S in two buffers, O), one lane issues
-//    the MMAs: S for tile t, then O for tile t - 1, so the softmax of a tile
-//    overlaps the next tile's S.
+//  * warps 0-7: softmax, the Q2 operand and the segment epilogue (two warps
+//    per TMEM lane quadrant);
+//  * warps 8, 9: K and V producers, each a 2-slot ring of 32 KiB tiles;
+//  * warp 10: allocates tensor memory (S in two buffers, O, Q2 in two), one
+//    lane issues the MMAs in the order the softmax frees their inputs: O of
+//    tile t as soon as its P is written, then S of tile t + 2 (S runs two
+//    tiles ahead of the softmax).
 // A segment split over several CTAs leaves one partial (m, l, O) per CTA in
 // the workspace; the last CTA to finish merges them in CTA order
 // (deterministic).
@@ -70,53 +77,73 @@ constexpr int kAtG = 64;                              // query heads per KV head
 constexpr int kAtRows = 128;                          // kept rows per tile
 constexpr uint32_t kAtTile = kAtRows * kRowBytes;     // 32 KiB: a K, V, Q2 or P operand
 constexpr uint32_t kAtBlock = kAtTile / 2;            // one 64-wide block of the 128-byte swizzle
-constexpr int kAtSlots = 2;                           // depth of the K ring and of the V ring
+constexpr int kAtKSlots = 2;                          // depth of the K ring
+constexpr int kAtVSlots = 2;                          // depth of the V ring
 constexpr int kAtSoftWarps = 8;
 constexpr int kAtSoft = 32 * kAtSoftWarps;
+constexpr int kAtKq = kAtSoftWarps / 4;              // warps per TMEM lane quadrant
+constexpr int kAtKT = 64 / kAtKq;                     // kept rows of a tile per softmax thread
+constexpr int kAtOT = kD / kAtKq;                     // O columns per softmax thread (epilogue, rescale)
 constexpr int kAtWarpK = kAtSoftWarps, kAtWarpV = kAtSoftWarps + 1, kAtWarpMma = kAtSoftWarps + 2;
 constexpr int kAtThreads = 32 * (kAtSoftWarps + 3);
 constexpr float kAtHeadroom = 8.f;                    // log2 growth allowed before the maximum is raised
-constexpr int kAtTmemCols = 512;                      // S0 [0, 128), S1 [128, 256), O [256, 384)
+constexpr int kAtTmemCols = 512;                      // S0, S1, O, then Q2 in two 64-column buffers
 constexpr uint32_t kAtColO = 256;
+constexpr uint32_t kAtColQ = 384;
 constexpr int kAtPart = kD + 4;                       // partial row: (m, l, pad, pad, O[128])
-constexpr uint32_t kIdescS = umma_idesc_bf16(128, kAtRows, false);   // Q2 K^T: both K-major
+constexpr uint32_t kIdescS = umma_idesc_bf16(128, kAtRows, false);   // Q2 K^T: K-major
 constexpr uint32_t kIdescO = umma_idesc_bf16(128, kD, true);         // P V: V is MN-major
 constexpr uint32_t kAtMapBytes = 128;                 // one CUtensorMap
 
 // shared memory, from a 1024-byte aligned base
 constexpr uint32_t kAtOffK = 0;
-constexpr uint32_t kAtOffV = kAtOffK + kAtSlots * kAtTile;
-constexpr uint32_t kAtOffQ = kAtOffV + kAtSlots * kAtTile;
-constexpr uint32_t kAtOffP = kAtOffQ + kAtTile;
-constexpr uint32_t kAtOffMap = kAtOffP + kAtTile;                 // [2] tensor maps being patched
-constexpr uint32_t kAtOffX = kAtOffMap + 2 * kAtMapBytes;         // [2 tiles][2 quarters][128] maxima
-constexpr uint32_t kAtOffL = kAtOffX + 2 * 2 * kAtRows * 4;       // [2][2][64] partial sums of l
-constexpr uint32_t kAtOffBar = kAtOffL + 4 * kAtG * 4;
-constexpr int kAtBars = 4 * kAtSlots + 2 + 2 + 2 + 3;             // see the list in the kernel
+constexpr uint32_t kAtOffV = kAtOffK + kAtKSlots * kAtTile;
+constexpr uint32_t kAtOffP = kAtOffV + kAtVSlots * kAtTile;     // [2] P buffers
+constexpr uint32_t kAtOffMap = kAtOffP + 2 * kAtTile;             // [2] tensor maps being patched
+constexpr uint32_t kAtOffX = kAtOffMap + 2 * kAtMapBytes;         // [2 tiles][kAtKq][128] maxima
+constexpr uint32_t kAtOffL = kAtOffX + 2 * kAtKq * kAtRows * 4;   // [2][kAtKq][64] partial sums of l
+constexpr uint32_t kAtOffBar = kAtOffL + 2 * kAtKq * kAtG * 4;
+constexpr int kAtBars = 2 * kAtKSlots + 2 * kAtVSlots + 2 + 2 + 2 + 2 + 2 + 1;   // see the list in the kernel
 constexpr size_t kAtSmem = 1024 + kAtOffBar + kAtBars * 8 + 16;
 
 int attn_tc_group() { return kAtG; }
 
 // Tiling of one launch: nt tiles per segment, tpc tiles per CTA, at most
-// max_pieces CTAs per segment. The CTA count is a fixed target (one per SM of
-// a 152-SM GB300), not the device's, so the workspace size is a function of
-// the shapes alone.
+// max_pieces CTAs per segment. Runs of whole segments when they still keep
+// 80% of the CTA target busy (no segment is then split, so no partials are
+// merged); otherwise the tiles are spread evenly over the target. The CTA
+// count is a fixed target (one per SM of a 152-SM GB300), not the device's,
+// so the workspace size is a function of the shapes alone.
 constexpr int kAtCtaTarget = 152;
 static void attn_tc_plan(int n_layers, int B, int n_kv, int budget, int* nt, int* tpc, int* grid,
                          int* max_pieces) {
   const long long nseg = (long long)n_layers * B * n_kv;
   const int t = (budget + kAtRows - 1) / kAtRows;
   const long long total = nseg * t;
-  long long c = (total + kAtCtaTarget - 1) / kAtCtaTarget;
-  if (c < 1) c = 1;
+  const long long spc = (nseg + kAtCtaTarget - 1) / kAtCtaTarget;       // whole segments a CTA
+  long long c;
+  if ((nseg + spc - 1) / spc * 5 >= 4LL * kAtCtaTarget) {
+    c = spc * t;
+  } else {
+    c = (total + kAtCtaTarget - 1) / kAtCtaTarget;
+    if (c < 1) c = 1;
+  }
   *nt = t;
   *tpc = (int)c;
   *grid = (int)((total + c - 1) / c);
-  const int mp = (t + (int)c - 1) / (int)c + 1;
+  const int mp = c % t == 0 ? 1 : (t + (int)c - 1) / (int)c + 1;
   *max_pieces = mp < t ? mp : t;
 }
 
 __device__ __forceinline__ void soft_bar() { asm volatile("bar.sync 1, %0;" :: "n"(kAtSoft) : "memory"); }
+// the softmax warps that hold the same heads (lane quadrants q and q + 2 for
+// q = warp % 2): named barrier 2 + warp % 2
+__device__ __forceinline__ void head_bar(int warp) {
+  if (warp & 1)
+    asm volatile("bar.sync 3, %0;" :: "n"(kAtSoft / 2) : "memory");
+  else
+    asm volatile("bar.sync 2, %0;" :: "n"(kAtSoft / 2) : "memory");
+}
 
 // A bounded wait by every lane of a warp with one warp-wide verdict, so that
 // the warp-collective tcgen05.ld / tcgen05.st that follow stay convergent.
@@ -177,6 +204,22 @@ __device__ __forceinline__ void at_next(const AttnTcCall& a, AtTile& x) {
   if (++x.b == a.B) x.b = 0;
 }
 
+// Q2 of segment `seg` for this thread's TMEM lane (head h) and dims
+// [kAtOT cq, +kAtOT): bf16 pairs, loaded first, stored to tensor memory once
+// the buffer is free
+struct AtQ {
+  uint32_t w[kAtOT / 2];
+};
+__device__ __forceinline__ void at_q_load(const AttnTcCall& a, int seg, int h, int cq, AtQ& q) {
+  const int lb = seg / a.n_kv, g = seg - lb * a.n_kv;
+  const uint4* src = reinterpret_cast<const uint4*>(a.q + ((size_t)lb * a.n_q + (size_t)g * kAtG + h) * kD + kAtOT * cq);
+#pragma unroll
+  for (int i = 0; i < kAtOT / 8; ++i) {
+    const uint4 v = ldg_stream(src + i);
+    q.w[4 * i] = v.x; q.w[4 * i + 1] = v.y; q.w[4 * i + 2] = v.z; q.w[4 * i + 3] = v.w;
+  }
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, int x, int y, uint64_t* bar) {
   asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
                :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)) : "memory");
@@ -191,53 +234,55 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const void* map, int x
                   "r"(smem_u32(bar)) : "memory");
 }
 
-// At most 136 registers a thread: the 11 warps then leave room on the SM for
-// a CTA of the gather kernel (128 threads x 128 registers), which runs beside
-// this kernel in the decode step.
-__global__ void __maxnreg__(136) attn_tc_kernel(const __grid_constant__ CUtensorMap tile_tmpl,
+// Registers per thread capped so that the CTA leaves room on the SM for a CTA
+// of the gather kernel (128 threads x 128 registers), which runs beside this
+// kernel in the decode step.
+constexpr int kAtMaxReg = ((65536 - 128 * 128) / kAtThreads) & ~7;
+__global__ void __maxnreg__(kAtMaxReg) attn_tc_kernel(const __grid_constant__ CUtensorMap tile_tmpl,
                                                 const __grid_constant__ CUtensorMap row_tmpl,
-                                                const __grid_constant__ CUtensorMap qmap, AttnTcCall a) {
+                                                AttnTcCall a) {
   extern __shared__ uint8_t at_raw[];
   const uint32_t raw_addr = smem_u32(at_raw);
   uint8_t* base = at_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   uint8_t* kring = base + kAtOffK;
   uint8_t* vring = base + kAtOffV;
-  uint8_t* qop = base + kAtOffQ;
   uint8_t* pop = base + kAtOffP;
   uint8_t* smaps = base + kAtOffMap;
   float* xmax = reinterpret_cast<float*>(base + kAtOffX);
   float* xl = reinterpret_cast<float*>(base + kAtOffL);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + kAtOffBar);
-  uint64_t* kfull = bars;                    // [2] TMA bytes
-  uint64_t* kfree = kfull + kAtSlots;        // [2] commit after the tile's S MMAs
-  uint64_t* vfull = kfree + kAtSlots;        // [2]
-  uint64_t* vfree = vfull + kAtSlots;        // [2] commit after the tile's O MMAs
-  uint64_t* qfull = vfree + kAtSlots;        // the Q2 TMA bytes
-  uint64_t* qfree = qfull + 1;               // commit after a segment's last S MMAs
-  uint64_t* sfull = qfree + 1;               // [2] commit: S of the tile is in tensor memory
+  uint64_t* kfull = bars;                    // [3] TMA bytes
+  uint64_t* kfree = kfull + kAtKSlots;       // [3] commit after the tile's S MMAs
+  uint64_t* vfull = kfree + kAtKSlots;       // [2] TMA bytes
+  uint64_t* vfree = vfull + kAtVSlots;       // [2] commit after the tile's O MMAs
+  uint64_t* qfull = vfree + kAtVSlots;       // [2] 8 softmax-warp arrivals: Q2 of a segment written
+  uint64_t* sfull = qfull + 2;               // [2] commit: S of the tile is in tensor memory
   uint64_t* sfree = sfull + 2;               // [2] 8 softmax-warp arrivals: S read
-  uint64_t* pfull = sfree + 2;               // 8 arrivals: P written (and O rescaled)
-  uint64_t* pfree = pfull + 1;               // commit after the tile's O MMAs
-  uint64_t* ofull = pfree + 1;               // commit after a segment's last O MMAs
+  uint64_t* pfull = sfree + 2;               // [2] 8 arrivals: P written (and O rescaled)
+  uint64_t* pfree = pfull + 2;               // [2] commit after the tile's O MMAs
+  uint64_t* ofull = pfree + 2;               // commit after a segment's last O MMAs
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ofull + 1);
   int* s_last = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kAtSlots; ++s) {
+    for (int s = 0; s < kAtKSlots; ++s) {
       mbar_init(&kfull[s], 1);
       mbar_init(&kfree[s], 1);
+    }
+    for (int s = 0; s < kAtVSlots; ++s) {
       mbar_init(&vfull[s], 1);
       mbar_init(&vfree[s], 1);
     }
-    mbar_init(qfull, 1);
-    mbar_init(qfree, 1);
     for (int s = 0; s < 2; ++s) {
+      mbar_init(&qfull[s], kAtSoftWarps);
       mbar_init(&sfull[s], 1);
       mbar_init(&sfree[s], kAtSoftWarps);
     }
-    mbar_init(pfull, kAtSoftWarps);
-    mbar_init(pfree, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&pfull[s], kAtSoftWarps);
+      mbar_init(&pfree[s], 1);
+    }
     mbar_init(ofull, 1);
     fence_mbar_init();
   }
@@ -251,8 +296,9 @@ __global__ void __maxnreg__(136) attn_tc_kernel(const __grid_constant__ CUtensor
   const int t1 = min(a.total, t0 + a.tpc);
 
   if (warp == kAtWarpK || warp == kAtWarpV) {
-    // ================= producers (K with the Q2 operand; V)
+    // ================= producers (K; V)
     const int op = warp - kAtWarpK;              // 0: K, 1: V
+    const int nslots = op == 0 ? kAtKSlots : kAtVSlots;
     uint8_t* ring = op == 0 ? kring : vring;
     uint64_t* full = op == 0 ? kfull : vfull;
     uint64_t* empty = op == 0 ? kfree : vfree;
@@ -296,25 +342,6 @@ __global__ void __maxnreg__(136) attn_tc_kernel(const __grid_constant__ CUtensor
         ++ns;
         vw = a.views[x.lb];
         src = static_cast<const uint16_t*>(op == 0 ? vw.k : vw.v) + (size_t)x.g * vw.rows * kD;
-        if (op == 0) {
-          // Q2 by TMA: the group's 64 query rows into rows [0, 64) and
-          // [64, 128) of both 64-dim blocks, once the previous segment's S
-          // MMAs have read the operand
-          if (!dead && !mbar_wait_bounded(qfree, (ns & 1) ^ 1, a.wait_limit)) {
-            if (lane == 0) set_status(a.status, SPC_ERR_TIMEOUT);
-            dead = true;
-          }
-          if (!dead && lane == 0) {
-            const int qrow = x.lb * a.n_q + x.g * kAtG;
-            mbar_arrive_expect_tx(qfull, kAtTile);
-            const uint32_t qa = smem_u32(qop);
-#pragma unroll
-            for (int blk = 0; blk < 2; ++blk)
-#pragma unroll
-              for (int rep = 0; rep < 2; ++rep)
-                tma_load_2d(qa + blk * kAtBlock + rep * (kAtG * 128), &qmap, 64 * blk, qrow, qfull);
-          }
-        }
       }
       int row[4];
       bool all = true;
@@ -323,8 +350,8 @@ __global__ void __maxnreg__(136) attn_tc_kernel(const __grid_constant__ CUtensor
         row[k] = at_row(vw.use_slots != 0, vw.rows, cur[k], x.tile * kAtRows + 32 * k + lane);
         all = all && __all_sync(0xffffffffu, row[k] >= 0);
       }
-      const int s = it % kAtSlots;
-      if (!dead && !mbar_wait_bounded(&empty[s], ((it / kAtSlots) & 1) ^ 1, a.wait_limit)) {
+      const int s = it % nslots;
+      if (!dead && !mbar_wait_bounded(&empty[s], ((it / nslots) & 1) ^ 1, a.wait_limit)) {
         if (lane == 0) set_status(a.status, SPC_ERR_TIMEOUT);
         dead = true;
       }
@@ -384,90 +411,91 @@ __global__ void __maxnreg__(136) attn_tc_kernel(const __grid_constant__ CUtensor
     // the copies still in flight land before the CTA may exit (they have,
     // unless a consumer gave up waiting)
     if (lane == 0) {
-      for (int k = max(0, n_issued - kAtSlots); k < n_issued; ++k)
-        mbar_wait_bounded(&full[k % kAtSlots], (k / kAtSlots) & 1, a.wait_limit);
-      if (op == 0 && ns >= 0) mbar_wait_bounded(qfull, ns & 1, a.wait_limit);
+      for (int k = max(0, n_issued - nslots); k < n_issued; ++k)
+        mbar_wait_bounded(&full[k % nslots], (k / nslots) & 1, a.wait_limit);
     }
     __syncwarp();
   } else if (warp == kAtWarpMma) {
     // ================= MMA issue (one lane)
     if (lane == 0) {
       bool dead = false;
-      const uint32_t qa = smem_u32(qop), pa = smem_u32(pop);
+      const uint32_t pa = smem_u32(pop);
       const uint32_t ka = smem_u32(kring), va = smem_u32(vring);
-      // O for tile `pt` (the previous one): P from the softmax, V from the ring
+      // O for tile pt: P from the softmax, V from the ring
       auto issue_o = [&](int pt, bool first, bool last) {
-        const int s = pt % kAtSlots;
-        if (!dead && (!mbar_wait_bounded(pfull, pt & 1, a.wait_limit) ||
-                      !mbar_wait_bounded(&vfull[s], (pt / kAtSlots) & 1, a.wait_limit))) {
+        const int s = pt % kAtVSlots, pb = pt & 1;
+        if (!dead && (!mbar_wait_bounded(&pfull[pb], (pt >> 1) & 1, a.wait_limit) ||
+                      !mbar_wait_bounded(&vfull[s], (pt / kAtVSlots) & 1, a.wait_limit))) {
           set_status(a.status, SPC_ERR_TIMEOUT);
           dead = true;
         }
         if (dead) return;
         tc_fence_after();
         const uint32_t vt = va + (uint32_t)s * kAtTile;
+        const uint32_t pt_a = pa + (uint32_t)pb * kAtTile;
 #pragma unroll
         for (int j = 0; j < kAtRows / 16; ++j) {
-          const uint64_t ad = umma_desc_sw128(pa + (uint32_t)(j >> 2) * kAtBlock + (uint32_t)(j & 3) * 32);
+          const uint64_t ad = umma_desc_sw128(pt_a + (uint32_t)(j >> 2) * kAtBlock + (uint32_t)(j & 3) * 32);
           const uint64_t bd = umma_desc_sw128_mn(vt + (uint32_t)j * 16 * 128, kAtBlock);
           umma_f16(tmem + kAtColO, ad, bd, kIdescO, (first && j == 0) ? 0u : 1u);
         }
         umma_commit(&vfree[s]);
-        umma_commit(pfree);
+        umma_commit(&pfree[pb]);
         if (last) umma_commit(ofull);
       };
-      int ns = -1, it = 0;
-      int tile = t0 < t1 ? t0 % a.nt : 0;          // tile of t within its segment
-      bool prev_first = false, prev_last = false;
-      for (int t = t0; t < t1; ++t, ++it, tile = tile + 1 == a.nt ? 0 : tile + 1) {
-        const bool first = t == t0 || tile == 0;
-        const bool last = t + 1 == t1 || tile + 1 == a.nt;
-        if (first) {
-          ++ns;
-          if (!dead && !mbar_wait_bounded(qfull, ns & 1, a.wait_limit)) {
-            set_status(a.status, SPC_ERR_TIMEOUT);
-            dead = true;
-          }
-        }
-        const int s = it % kAtSlots, sb = it & 1;
-        if (!dead && (!mbar_wait_bounded(&kfull[s], (it / kAtSlots) & 1, a.wait_limit) ||
-                      !mbar_wait_bounded(&sfree[sb], ((it >> 1) & 1) ^ 1, a.wait_limit))) {
+      // S for tile u (segment counter ns_u, first tile of its segment or not)
+      auto issue_s = [&](int u, int ns_u, bool first) {
+        if (first && !dead && !mbar_wait_bounded(&qfull[ns_u & 1], (ns_u >> 1) & 1, a.wait_limit)) {
           set_status(a.status, SPC_ERR_TIMEOUT);
           dead = true;
         }
-        if (!dead) {
-          tc_fence_after();
-          const uint32_t kt = ka + (uint32_t)s * kAtTile;
-#pragma unroll
-          for (int hb = 0; hb < 2; ++hb)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint64_t ad = umma_desc_sw128(qa + (uint32_t)hb * kAtBlock + (uint32_t)k * 32);
-              const uint64_t bd = umma_desc_sw128(kt + (uint32_t)hb * kAtBlock + (uint32_t)k * 32);
-              umma_f16(tmem + (uint32_t)sb * kAtRows, ad, bd, kIdescS, (hb | k) ? 1u : 0u);
-            }
-          umma_commit(&kfree[s]);
-          umma_commit(&sfull[sb]);
-          if (last) umma_commit(qfree);
+        const int s = u % kAtKSlots, sb = u & 1;
+        if (!dead && (!mbar_wait_bounded(&kfull[s], (u / kAtKSlots) & 1, a.wait_limit) ||
+                      !mbar_wait_bounded(&sfree[sb], ((u >> 1) & 1) ^ 1, a.wait_limit))) {
+          set_status(a.status, SPC_ERR_TIMEOUT);
+          dead = true;
         }
-        if (it > 0) issue_o(it - 1, prev_first, prev_last);
-        prev_first = first;
-        prev_last = last;
+        if (dead) return;
+        tc_fence_after();
+        const uint32_t kt = ka + (uint32_t)s * kAtTile;
+        const uint32_t qa = tmem + kAtColQ + (uint32_t)(ns_u & 1) * (kD / 2);
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint64_t bd = umma_desc_sw128(kt + (uint32_t)(kk >> 2) * kAtBlock + (uint32_t)(kk & 3) * 32);
+          umma_f16_tmem_a(tmem + (uint32_t)sb * kAtRows, qa + (uint32_t)kk * 8, bd, kIdescS, kk ? 1u : 0u);
+        }
+        umma_commit(&kfree[s]);
+        umma_commit(&sfull[sb]);
+      };
+      const int n = t1 - t0;
+      const int tile0 = n > 0 ? t0 % a.nt : 0;     // tile of t0 within its segment
+      // tile u of this CTA: first / last tile of a segment, segment counter
+      auto is_first = [&](int u) { return u == 0 || (tile0 + u) % a.nt == 0; };
+      auto is_last = [&](int u) { return u + 1 == n || (tile0 + u + 1) % a.nt == 0; };
+      int ns_s = -1;                               // segment counter of the last S issued
+      for (int u = 0; u < n && u < 2; ++u) {
+        if (is_first(u)) ++ns_s;
+        issue_s(u, ns_s, is_first(u));
       }
-      if (it > 0) {
-        issue_o(it - 1, prev_first, prev_last);
-        // every MMA has completed before the tensor memory is released
-        if (!dead) mbar_wait_bounded(pfree, (it - 1) & 1, a.wait_limit);
+      for (int u = 0; u < n; ++u) {
+        issue_o(u, is_first(u), is_last(u));
+        if (u + 2 < n) {
+          if (is_first(u + 2)) ++ns_s;
+          issue_s(u + 2, ns_s, is_first(u + 2));
+        }
       }
+      // every MMA has completed before the tensor memory is released
+      if (n > 0 && !dead) mbar_wait_bounded(&pfree[(n - 1) & 1], ((n - 1) >> 1) & 1, a.wait_limit);
     }
     __syncwarp();
   } else {
     // ================= softmax and epilogue
     // warp w reads TMEM lanes 32 (w % 4) .. +31 (lane r: head r % 64) and
-    // takes 32 kept rows of the tile: [64 (r / 64) + 32 (w / 4), +32)
-    const int qd = warp & 3, c2 = warp >> 2;
+    // takes kAtKT kept rows of the tile: [64 (r / 64) + kAtKT (w / 4), +kAtKT)
+    const int qd = warp & 3, cq = warp >> 2;
     const int r = qd * 32 + lane, h = r & (kAtG - 1), hf = r >> 6;
-    const int col = 64 * hf + 32 * c2;                 // this thread's first kept row in a tile
+    const int col = 64 * hf + kAtKT * cq;              // this thread's first kept row in a tile
+    const int kl = lane & (kAtKT - 1);                 // the kept row whose index this lane fetches
     const uint32_t trow = tmem + ((uint32_t)(qd * 32) << 16);
     bool dead = false;
     float m = -INFINITY, l = 0.f;
@@ -477,7 +505,15 @@ __global__ void __maxnreg__(136) attn_tc_kernel(const __grid_constant__ CUtensor
     AtTile y = at_tile(a, t0);
     if (t0 < t1) {
       const size_t ioff = ((size_t)y.b * a.n_kv + y.g) * a.K;
-      nx = at_fetch(a.selected + ioff, a.slot_pos + ioff, y.tile * kAtRows + col + lane, a.K);
+      nx = at_fetch(a.selected + ioff, a.slot_pos + ioff, y.tile * kAtRows + col + kl, a.K);
+      // Q2 of the first segment, buffer 0
+      AtQ q;
+      at_q_load(a, y.seg, h, cq, q);
+      tmem_st_n<kAtOT / 2>(trow + kAtColQ + (uint32_t)(kAtOT / 2 * cq), q.w);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&qfull[0]);
     }
     for (int t = t0, it = 0; t < t1; ++t, ++it) {
       const AtTile x = y;
@@ -486,9 +522,14 @@ __global__ void __maxnreg__(136) attn_tc_kernel(const __grid_constant__ CUtensor
       const AtIdx cur = nx;
       if (t + 1 < t1) {
         const size_t ioff = ((size_t)y.b * a.n_kv + y.g) * a.K;
-        nx = at_fetch(a.selected + ioff, a.slot_pos + ioff, y.tile * kAtRows + col + lane, a.K);
+        nx = at_fetch(a.selected + ioff, a.slot_pos + ioff, y.tile * kAtRows + col + kl, a.K);
       }
-      if (x.seg != cur_seg) {
+      // a new segment: Q2 of the next one (if this CTA has it) goes into the
+      // other buffer once this tile's S is in (then every S of the segment
+      // before, the buffer's last reader, has completed)
+      const bool seg_start = x.seg != cur_seg;
+      const bool q_next = seg_start && t + (a.nt - x.tile) < t1;
+      if (seg_start) {
         cur_seg = x.seg;
         ++ns;
         vw = a.views[x.lb];
@@ -496,7 +537,7 @@ __global__ void __maxnreg__(136) attn_tc_kernel(const __grid_constant__ CUtensor
         l = 0.f;
       }
       const uint32_t okm =
-          __ballot_sync(0xffffffffu, at_row(vw.use_slots != 0, vw.rows, cur, x.tile * kAtRows + col + lane) >= 0);
+          __ballot_sync(0xffffffffu, at_row(vw.use_slots != 0, vw.rows, cur, x.tile * kAtRows + col + kl) >= 0);
 
       const int sb = it & 1;
       if (!dead && !warp_wait(&sfull[sb], (it >> 1) & 1, a.wait_limit)) {
@@ -504,26 +545,40 @@ __global__ void __maxnreg__(136) attn_tc_kernel(const __grid_constant__ CUtensor
         dead = true;
       }
       tc_fence_after();
-      float s[32];
+      if (q_next) {
+        if (!dead) {
+          AtQ qn;
+          at_q_load(a, x.seg + 1, h, cq, qn);
+          tmem_st_n<kAtOT / 2>(trow + kAtColQ + (uint32_t)(((ns + 1) & 1) * (kD / 2) + kAtOT / 2 * cq), qn.w);
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&qfull[(ns + 1) & 1]);
+      }
+      float s[kAtKT];
       if (!dead) {
-        tmem_ld32(trow + (uint32_t)sb * kAtRows + (uint32_t)col, s);
+        tmem_ld_n<kAtKT>(trow + (uint32_t)sb * kAtRows + (uint32_t)col, s);
         tmem_ld_wait();
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sfree[sb]);
       float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      if (dead || okm != 0xffffffffu) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        s[j] = (!dead && ((okm >> j) & 1u)) ? s[j] : -INFINITY;
-        mx4[j & 3] = fmaxf(mx4[j & 3], s[j]);
+        for (int j = 0; j < kAtKT; ++j) s[j] = (!dead && ((okm >> j) & 1u)) ? s[j] : -INFINITY;
       }
+#pragma unroll
+      for (int j = 0; j < kAtKT; ++j) mx4[j & 3] = fmaxf(mx4[j & 3], s[j]);
       const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-      // the head's tile maximum (scaled to base 2) over its four threads
-      float* xm = xmax + sb * 2 * kAtRows;
-      xm[c2 * kAtRows + r] = mx * a.scale2;
-      soft_bar();
-      const float M = fmaxf(fmaxf(xm[r], xm[kAtRows + r]), fmaxf(xm[r ^ 64], xm[kAtRows + (r ^ 64)]));
+      // the head's tile maximum (scaled to base 2) over its 2 kAtKq threads
+      float* xm = xmax + sb * kAtKq * kAtRows;
+      xm[cq * kAtRows + r] = mx * a.scale2;
+      head_bar(warp);
+      float M = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kAtKq; ++c) M = fmaxf(M, fmaxf(xm[c * kAtRows + r], xm[c * kAtRows + (r ^ 64)]));
       bool rescale = false;
       float alpha = 1.f;
       if (M > m + kAtHeadroom) {          // false for M = -inf; true for the first finite maximum
@@ -539,29 +594,35 @@ __global__ void __maxnreg__(136) attn_tc_kernel(const __grid_constant__ CUtensor
       if (m != -INFINITY) {
         float ls4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < kAtKT; ++j) {
           s[j] = ex2_fast(fmaf(s[j], a.scale2, -m));
           ls4[j & 3] += s[j];
         }
         lsum = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
       } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) s[j] = 0.f;
+        for (int j = 0; j < kAtKT; ++j) s[j] = 0.f;
       }
       l += lsum;
-      // the previous tile's O MMAs are done: P may be overwritten, O rescaled
-      if (!dead && !warp_wait(pfree, (it & 1) ^ 1, a.wait_limit)) {
+      // the O MMAs of tile it - 2 are done: its P buffer may be overwritten
+      if (!dead && !warp_wait(&pfree[it & 1], ((it >> 1) & 1) ^ 1, a.wait_limit)) {
+        if (lane == 0) set_status(a.status, SPC_ERR_TIMEOUT);
+        dead = true;
+      }
+      const bool any_rescale = __any_sync(0xffffffffu, rescale);
+      // O holds earlier tiles to rescale: the O MMAs of tile it - 1 must be done
+      if (any_rescale && it > 0 && !dead && !warp_wait(&pfree[(it - 1) & 1], ((it - 1) >> 1) & 1, a.wait_limit)) {
         if (lane == 0) set_status(a.status, SPC_ERR_TIMEOUT);
         dead = true;
       }
       tc_fence_after();
-      if (__any_sync(0xffffffffu, rescale) && !dead) {
+      if (any_rescale && !dead) {
         // warp-wide (the accesses are collective); other heads scale by 1.
-        // The two warps of a lane quadrant take O's columns [64 c2, +64).
+        // The warps of a lane quadrant take O's columns [kAtOT cq, +kAtOT).
 #pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < kAtOT / 32; ++c) {
           float o[32];
-          const uint32_t oc = trow + kAtColO + (uint32_t)(64 * c2 + 32 * c);
+          const uint32_t oc = trow + kAtColO + (uint32_t)(kAtOT * cq + 32 * c);
           tmem_ld32(oc, o);
           tmem_ld_wait();
 #pragma unroll
@@ -571,19 +632,21 @@ __global__ void __maxnreg__(136) attn_tc_kernel(const __grid_constant__ CUtensor
         tmem_st_wait();
       }
       {
-        // bf16 high parts to row h, low parts to row h + 64, in the block of
-        // this thread's kept rows: 16-byte unit u holds kept rows 8u .. 8u + 7
-        const uint32_t pb = smem_u32(pop) + (uint32_t)hf * kAtBlock;
+        // high parts (the top 16 bits of p) to row h, the top 16 bits of the
+        // remainder to row h + 64, in the block of this thread's kept rows:
+        // 16-byte unit u holds kept rows 8u .. 8u + 7
+        const uint32_t pb = smem_u32(pop) + (uint32_t)(it & 1) * kAtTile + (uint32_t)hf * kAtBlock;
 #pragma unroll
-        for (int uu = 0; uu < 4; ++uu) {
+        for (int uu = 0; uu < kAtKT / 8; ++uu) {
           uint32_t hi[4], lo[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float p0 = s[8 * uu + 2 * e], p1 = s[8 * uu + 2 * e + 1];
-            hi[e] = pack_bf16(p0, p1);
-            lo[e] = pack_bf16(p0 - bf_lo(hi[e]), p1 - bf_hi(hi[e]));
+            const uint32_t b0 = __float_as_uint(s[8 * uu + 2 * e]), b1 = __float_as_uint(s[8 * uu + 2 * e + 1]);
+            hi[e] = __byte_perm(b0, b1, 0x7632);
+            lo[e] = __byte_perm(__float_as_uint(s[8 * uu + 2 * e] - __uint_as_float(b0 & 0xffff0000u)),
+                                __float_as_uint(s[8 * uu + 2 * e + 1] - __uint_as_float(b1 & 0xffff0000u)), 0x7632);
           }
-          const int u = 4 * c2 + uu;
+          const int u = kAtKT / 8 * cq + uu;
           const uint32_t off = (uint32_t)(h * 128 + ((u ^ (h & 7)) << 4));
           asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" :: "r"(pb + off), "r"(hi[0]), "r"(hi[1]), "r"(hi[2]),
                        "r"(hi[3]) : "memory");
@@ -594,7 +657,7 @@ __global__ void __maxnreg__(136) attn_tc_kernel(const __grid_constant__ CUtensor
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(pfull);
+      if (lane == 0) mbar_arrive(&pfull[it & 1]);
 
       if (!last) continue;
       // ---- segment epilogue: O_h = O[h] + O[h + 64], l_h = its four threads' sums
@@ -603,16 +666,17 @@ __global__ void __maxnreg__(136) attn_tc_kernel(const __grid_constant__ CUtensor
         dead = true;
       }
       tc_fence_after();
-      // the P operand is free until the softmax threads write the next tile's
-      // P, which they do after the next tile's barrier: it holds the low rows
+      // the P buffers are free (every O MMA of the segment is done) until the
+      // softmax threads write the next tile's P, which they do after the next
+      // tile's barrier: the first holds the low rows
       float* xo = reinterpret_cast<float*>(pop);     // [64][128], float4 j of row h at (j + h) % 32
-      xl[(hf * 2 + c2) * kAtG + h] = l;
+      xl[(hf * kAtKq + cq) * kAtG + h] = l;
       if (hf == 1) {
 #pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < kAtOT / 32; ++c) {
           float o[32];
           if (!dead) {
-            tmem_ld32(trow + kAtColO + (uint32_t)(64 * c2 + 32 * c), o);
+            tmem_ld32(trow + kAtColO + (uint32_t)(kAtOT * cq + 32 * c), o);
             tmem_ld_wait();
           } else {
 #pragma unroll
@@ -620,7 +684,7 @@ __global__ void __maxnreg__(136) attn_tc_kernel(const __grid_constant__ CUtensor
           }
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4)
-            reinterpret_cast<float4*>(xo + h * kD)[(16 * c2 + 8 * c + q4 + h) & 31] =
+            reinterpret_cast<float4*>(xo + h * kD)[(kAtOT / 4 * cq + 8 * c + q4 + h) & 31] =
                 make_float4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
         }
       }
@@ -632,17 +696,19 @@ __global__ void __maxnreg__(136) attn_tc_kernel(const __grid_constant__ CUtensor
       float* res = a.part + ((size_t)x.seg * a.max_pieces + piece) * (size_t)kAtG * kAtPart + (size_t)h * kAtPart;
       if (hf == 0) {
         tc_fence_after();
-        const float L = (xl[h] + xl[kAtG + h]) + (xl[2 * kAtG + h] + xl[3 * kAtG + h]);
+        float L = 0.f;
+#pragma unroll
+        for (int c = 0; c < 2 * kAtKq; ++c) L += xl[c * kAtG + h];
         const float li = L > 0.f ? 1.f / L : 0.f;
-        if (pieces > 1 && c2 == 0) {
+        if (pieces > 1 && cq == 0) {
           res[0] = m;
           res[1] = L;
         }
 #pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < kAtOT / 32; ++c) {
           float o[32];
           if (!dead) {
-            tmem_ld32(trow + kAtColO + (uint32_t)(64 * c2 + 32 * c), o);
+            tmem_ld32(trow + kAtColO + (uint32_t)(kAtOT * cq + 32 * c), o);
             tmem_ld_wait();
           } else {
 #pragma unroll
@@ -650,7 +716,7 @@ __global__ void __maxnreg__(136) attn_tc_kernel(const __grid_constant__ CUtensor
           }
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4) {
-            const int j4 = 16 * c2 + 8 * c + q4;          // float4 index within the 128 dims
+            const int j4 = kAtOT / 4 * cq + 8 * c + q4;   // float4 index within the 128 dims
             const float4 lo4 = reinterpret_cast<const float4*>(xo + h * kD)[(j4 + h) & 31];
             float4 v = make_float4(o[4 * q4] + lo4.x, o[4 * q4 + 1] + lo4.y, o[4 * q4 + 2] + lo4.z,
                                    o[4 * q4 + 3] + lo4.w);
@@ -673,29 +739,41 @@ __global__ void __maxnreg__(136) attn_tc_kernel(const __grid_constant__ CUtensor
         if (*s_last) {
           __threadfence();
           const size_t pstride = (size_t)kAtG * kAtPart;
-          const float* pb = a.part + (size_t)x.seg * a.max_pieces * pstride + (size_t)h * kAtPart;
-          float Mx = -INFINITY;
-          for (int p = 0; p < pieces; ++p) Mx = fmaxf(Mx, __ldcg(pb + p * pstride));
-          float Ls = 0.f;
+          const float* ps = a.part + (size_t)x.seg * a.max_pieces * pstride;
+          // thread: 128 / (kAtSoft / 64) output dims of head tid / (kAtSoft / 64);
+          // a piece's (m, l) and its partial of them loaded together, then
+          // folded into the running (max, sum, O), pieces in CTA order
+          constexpr int kTh = kAtSoft / kAtG;              // threads per head
+          constexpr int kF4 = kD / 4 / kTh;                // output float4s per thread
+          const int hh = threadIdx.x / kTh, f0 = (threadIdx.x % kTh) * kF4;
+          const float* pm = ps + (size_t)hh * kAtPart;
+          float Mx = -INFINITY, Ls = 0.f;
+          float4 O[kF4];
+#pragma unroll
+          for (int q = 0; q < kF4; ++q) O[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
           for (int p = 0; p < pieces; ++p) {
-            const float mp = __ldcg(pb + p * pstride);
-            const float w = (Mx == -INFINITY || mp == -INFINITY) ? 0.f : exp2f(mp - Mx);
-            Ls += __ldcg(pb + p * pstride + 1) * w;
+            const float* pp = pm + (size_t)p * pstride;
+            const float2 ml = __ldcg(reinterpret_cast<const float2*>(pp));
+            float4 v[kF4];
+#pragma unroll
+            for (int q = 0; q < kF4; ++q) v[q] = __ldcg(reinterpret_cast<const float4*>(pp + 4) + f0 + q);
+            if (ml.x != -INFINITY) {
+              const float M2 = fmaxf(Mx, ml.x);
+              const float wa = Mx == -INFINITY ? 0.f : exp2f(Mx - M2), wb = exp2f(ml.x - M2);
+              Ls = Ls * wa + ml.y * wb;
+#pragma unroll
+              for (int q = 0; q < kF4; ++q) {
+                O[q].x = O[q].x * wa + v[q].x * wb; O[q].y = O[q].y * wa + v[q].y * wb;
+                O[q].z = O[q].z * wa + v[q].z * wb; O[q].w = O[q].w * wa + v[q].w * wb;
+              }
+              Mx = M2;
+            }
           }
           const float li = Ls > 0.f ? 1.f / Ls : 0.f;
-          // this thread: dims [32 (2 hf + c2), +32) of head h
-          const int q0 = 8 * (2 * hf + c2);
-#pragma unroll 1
-          for (int q4 = 0; q4 < 8; ++q4) {
-            float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int p = 0; p < pieces; ++p) {
-              const float mp = __ldcg(pb + p * pstride);
-              const float w = (Mx == -INFINITY || mp == -INFINITY) ? 0.f : exp2f(mp - Mx);
-              const float4 v = __ldcg(reinterpret_cast<const float4*>(pb + p * pstride + 4) + q0 + q4);
-              O.x = fmaf(w, v.x, O.x); O.y = fmaf(w, v.y, O.y); O.z = fmaf(w, v.z, O.z); O.w = fmaf(w, v.w, O.w);
-            }
-            reinterpret_cast<float4*>(outp)[q0 + q4] = make_float4(O.x * li, O.y * li, O.z * li, O.w * li);
-          }
+          float4* dst = reinterpret_cast<float4*>(a.out + ((size_t)x.lb * a.n_q + (size_t)x.g * kAtG + hh) * kD) + f0;
+#pragma unroll
+          for (int q = 0; q < kF4; ++q) dst[q] = make_float4(O[q].x * li, O[q].y * li, O[q].z * li, O[q].w * li);
           soft_bar();
           if (threadIdx.x == 0) a.counters[x.seg] = 0u;
         }
@@ -732,20 +810,17 @@ int attn_tc_launch(AttnTcCall c, int n_layers, void* stream) {
   // the template of the per-view maps (K or V rows of one KV head: [rows][128]
   // bf16, boxes of 128 rows x 64 dims; base and row count are patched on the
   // device) and the map of the queries ([n_layers B n_q][128], 64-row boxes)
-  CUtensorMap tile_tmpl, row_tmpl, qmap;
+  CUtensorMap tile_tmpl, row_tmpl;
   const uint64_t tdims[2] = {(uint64_t)kD, (uint64_t)kAtRows};
-  const uint64_t qdims[2] = {(uint64_t)kD, (uint64_t)n_layers * c.B * c.n_q};
   const uint64_t strides[1] = {(uint64_t)kRowBytes};
   const uint32_t tbox[2] = {64, (uint32_t)kAtRows};
   const uint32_t rbox[2] = {64, 1};
-  const uint32_t qbox[2] = {64, (uint32_t)kAtG};
   if (!tensor_map_bf16_sw128(&tile_tmpl, c.q, 2, tdims, strides, tbox) ||
-      !tensor_map_bf16_sw128(&row_tmpl, c.q, 2, tdims, strides, rbox) ||
-      !tensor_map_bf16_sw128(&qmap, c.q, 2, qdims, strides, qbox))
+      !tensor_map_bf16_sw128(&row_tmpl, c.q, 2, tdims, strides, rbox))
     return SPC_ERR_CUDA;
   cudaError_t e = set_func_attr((const void*)attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAtSmem);
   if (e != cudaSuccess) return SPC_ERR_CUDA;
-  attn_tc_kernel<<<grid, kAtThreads, kAtSmem, static_cast<cudaStream_t>(stream)>>>(tile_tmpl, row_tmpl, qmap, c);
+  attn_tc_kernel<<<grid, kAtThreads, kAtSmem, static_cast<cudaStream_t>(stream)>>>(tile_tmpl, row_tmpl, c);
   return cudaGetLastError() == cudaSuccess ? SPC_OK : SPC_ERR_CUDA;
 }
 

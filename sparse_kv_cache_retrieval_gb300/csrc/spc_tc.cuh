@@ -45,6 +45,16 @@ __device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64
                :: "r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
+// D (tensor memory) [+]= A (tensor memory, M lanes x K: column c of lane m
+// holds elements 2c and 2c + 1 of row m, the lower one in the low half)
+// x B (shared)^T, issued by one thread
+__device__ __forceinline__ void umma_f16_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
+                                                uint32_t accumulate) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+               :: "r"(tmem_d), "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
 // arrives once on `bar` when every tcgen05 operation this thread issued before has completed
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
@@ -121,6 +131,44 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
          "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
       : "memory");
 }
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  float f[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+  tmem_st32(taddr, f);
+}
+// 16 consecutive 32-bit columns into this warp's 32 TMEM lanes
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+      :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+         "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+  uint32_t u[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(v[i]);
+  tmem_st16(taddr, u);
+}
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// N (16 or 32) consecutive columns, one lane per thread
+template <int N>
+__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, float (&v)[N]) {
+  static_assert(N == 16 || N == 32, "tmem_ld_n: 16 or 32 columns");
+  if constexpr (N == 32) tmem_ld32(taddr, v); else tmem_ld16(taddr, v);
+}
+template <int N>
+__device__ __forceinline__ void tmem_st_n(uint32_t taddr, const float (&v)[N]) {
+  static_assert(N == 16 || N == 32, "tmem_st_n: 16 or 32 columns");
+  if constexpr (N == 32) tmem_st32(taddr, v); else tmem_st16(taddr, v);
+}
+template <int N>
+__device__ __forceinline__ void tmem_st_n(uint32_t taddr, const uint32_t (&v)[N]) {
+  static_assert(N == 16 || N == 32, "tmem_st_n: 16 or 32 columns");
+  if constexpr (N == 32) tmem_st32(taddr, v); else tmem_st16(taddr, v);
+}
 
 }  // namespace spc

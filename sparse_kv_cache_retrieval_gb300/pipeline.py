@@ -236,8 +236,12 @@ class DecodePipeline:
         # layer chunks, streams, events
         lc = max(1, min(layers_per_launch, L))
         self.chunks = [(l0, min(L, l0 + lc)) for l0 in range(0, L, lc)]
-        ws_attn = (spc.spc_mla_decode_attn_workspace_size(lc, B, K) if self.mla else
-                   spc.spc_sparse_decode_attn_workspace_size(lc, B, self.n_q, n_kv, d, K))
+        # the workspace a launch needs is not monotone in its layer count (a
+        # shorter chunk may split its segments over more CTAs): the largest
+        # over the chunk lengths in use
+        ws_attn = max((spc.spc_mla_decode_attn_workspace_size(l1 - l0, B, K) if self.mla else
+                       spc.spc_sparse_decode_attn_workspace_size(l1 - l0, B, self.n_q, n_kv, d, K))
+                      for l0, l1 in self.chunks)
         self.ws_attn = torch.zeros(ws_attn, dtype=torch.uint8, device=dev)
         # The gathers (B) get the highest priority: a gather CTA needs a whole
         # SM and waits for one to drain, and the next free SM should go to it

@@ -281,6 +281,8 @@ ATTN_CASES = [
     (2, 1, 128, 2, 700, 2000, 0, None),      # two KV heads, positions into a full cache
     (1, 1, 64, 1, 128, 128, 1, None),        # one tile, one CTA: no partials
     (3, 1, 64, 1, 256, 300, 1, 2),           # two kept rows in a 256-row budget
+    (32, 8, 64, 1, 256, 300, 1, 200),        # 256 segments: two whole segments per CTA
+    (16, 8, 64, 1, 512, 600, 1, None),       # 128 segments: one whole segment per CTA
 ]
 
 

@@ -152,6 +152,14 @@ def test_chain_cfg5_mqa_full_shape():
     run_chain(cfg, 1, 2, layers_per_launch=2)
 
 
+def test_chain_mqa_short_last_chunk():
+    # 64 heads on one KV head, a 16-layer chunk and a last chunk of 1: the
+    # 1-layer launch splits its segments over several CTAs (and needs merge
+    # workspace), the 16-layer launch keeps whole segments (and needs none)
+    cfg = scaled(CONFIGS["cfg5mqa"], B=8, lens=(1000,) * 8, n_layers=17, steps=2, budget=256, H=1024)
+    run_chain(cfg, 2, 17, layers_per_launch=16)
+
+
 def _growing_small(steps=8):
     from tests.gpu_cases import workload
     return workload(name="c3_small", B=2, lens=(100, 98), H=256, n_q=8, n_kv=2, budget=96, n_layers=4,
