@@ -49,7 +49,12 @@ constexpr int kAttnPitch = 256;                     // smem bytes per row (16-by
 constexpr int kAttnCWarps = 4;
 constexpr int kAttnCThreads = kAttnCWarps * 32;
 constexpr int kAttnThreads = kAttnCThreads + 32;    // + producer warp
-constexpr int kAttnStages = 3;
+// ring depth: 2 stages for groups of up to 16 heads, so that two CTAs share
+// an SM (their consumer warps hide each other's latency: at G = 8, 16 layers,
+// 392 vs 605 us with 3 stages and one CTA per SM, the same with 4 or 6), 3
+// for larger groups (whose merge buffers keep them at one CTA per SM)
+template <int G>
+constexpr int attn_stages() { return G <= 16 ? 2 : 3; }
 constexpr int kAttnMaxCpc = 16;                     // chunks per CTA (row indices prefetched)
 constexpr int kAttnTile = kAttnRows * kAttnPitch;   // 16 KiB (K or V)
 constexpr int kAttnMaxCluster = 8;
@@ -65,6 +70,7 @@ struct AttnShape {
   static constexpr int RW = kAttnRows / NRS;        // rows per warp per chunk
   static constexpr int NT = RW / 8;                 // QK n-tiles (8 rows each)
   static constexpr int KS = RW / 16;                // PV k-steps (16 rows each)
+  static constexpr int ST = attn_stages<G>();       // ring stages
 };
 
 struct AttnArgs {
@@ -91,13 +97,13 @@ constexpr size_t round16(size_t x) { return (x + 15) & ~size_t(15); }
 template <int G>
 struct AttnSmem {
   using S = AttnShape<G>;
-  static constexpr size_t stages = (size_t)kAttnStages * 2 * kAttnTile;
+  static constexpr size_t stages = (size_t)S::ST * 2 * kAttnTile;
   static constexpr size_t mo = round16(sizeof(float) * S::NRS * G * kD);   // per row-split O
   static constexpr size_t ml = round16(sizeof(float) * 2 * S::NRS * G);    // per row-split (m, l)
   // row-split weights [NRS][G], later cluster weights [C][G] + sums [G]
   static constexpr size_t wsp = round16(sizeof(float) * ((S::NRS > kAttnMaxCluster ? S::NRS : kAttnMaxCluster) + 1) * G);
   static constexpr size_t cres = round16(sizeof(float) * G * kPartStride); // this CTA's (m, l, O)
-  static constexpr size_t total = stages + mo + ml + wsp + cres + sizeof(uint64_t) * 3 * kAttnStages;
+  static constexpr size_t total = stages + mo + ml + wsp + cres + sizeof(uint64_t) * 3 * S::ST;
 };
 
 __device__ __forceinline__ void cons_bar() { asm volatile("bar.sync 1, %0;" :: "n"(kAttnCThreads) : "memory"); }
@@ -114,8 +120,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
   float* wsp = reinterpret_cast<float*>(asmem + M::stages + M::mo + M::ml);      // [NRS][G] + [G][2]
   float* cres = reinterpret_cast<float*>(asmem + M::stages + M::mo + M::ml + M::wsp);  // [G][132]
   uint64_t* okmask = reinterpret_cast<uint64_t*>(asmem + M::stages + M::mo + M::ml + M::wsp + M::cres);
-  uint64_t* full = okmask + kAttnStages;
-  uint64_t* empty = full + kAttnStages;
+  uint64_t* full = okmask + S::ST;
+  uint64_t* empty = full + S::ST;
   __shared__ int s_last;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -127,7 +133,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
   const int c1 = min(a.n_chunks, c0 + a.cpc);
 
   if (tid == 0) {
-    for (int s = 0; s < kAttnStages; ++s) {
+    for (int s = 0; s < S::ST; ++s) {
       mbar_init(&full[s], 32 + 1);   // 32 cp.async arrivals + the mask publisher
       mbar_init(&empty[s], kAttnCWarps);
     }
@@ -167,8 +173,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
 #endif
 #pragma unroll 1
     for (int c = c0; c < c_end; ++c, ++it) {
-      const int s = it % kAttnStages;
-      const uint32_t ph = (it / kAttnStages) & 1;
+      const int s = it % S::ST;
+      const uint32_t ph = (it / S::ST) & 1;
       if (!mbar_wait_bounded(&empty[s], ph ^ 1, a.wait_limit)) {
         if (lane == 0) set_status(a.status, SPC_ERR_TIMEOUT);
         break;
@@ -214,8 +220,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
       asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(smem_u32(&full[s])) : "memory");
     }
     // wait (bounded) for the copies still in flight before leaving
-    for (int k = max(0, it - kAttnStages); k < it; ++k)
-      mbar_wait_bounded(&full[k % kAttnStages], (k / kAttnStages) & 1, a.wait_limit);
+    for (int k = max(0, it - S::ST); k < it; ++k)
+      mbar_wait_bounded(&full[k % S::ST], (k / S::ST) & 1, a.wait_limit);
     __syncwarp();
   } else {
     // ================= consumers
@@ -258,8 +264,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(AttnArgs a) {
 
     int it = 0;
     for (int c = c0; c < c1; ++c, ++it) {
-      const int s = it % kAttnStages;
-      const uint32_t ph = (it / kAttnStages) & 1;
+      const int s = it % S::ST;
+      const uint32_t ph = (it / S::ST) & 1;
       if (!dead && !mbar_wait_bounded(&full[s], ph, a.wait_limit)) {
         if (lane == 0) set_status(a.status, SPC_ERR_TIMEOUT);
         dead = true;
