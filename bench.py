@@ -183,15 +183,15 @@ NCU_TRAFFIC = {
                  "sha256": "784d5dc68a4f6cfb41d0929b5407d4ebb5f94b1e8b903047fd202c0aeec49bde",
                  "bytes_per_unit": (67141632 + 5376) / 262144, "unit": "256-byte key row"},
     # tcgen05 key scan pass 1 (logsumexp partials), MQA (64 heads, one KV head),
-    # 8 requests x 16 384 positions: 33 868 800 B DRAM read + 256 B write
+    # 8 requests x 16 384 positions: 33 863 936 B DRAM read + 0 B write
     "key_scan_tc": {"source": "sparse_kv_cache_retrieval_gb300/csrc/scan_tc.cu",
-                    "sha256": "099c6371c324c763fd40e0f03ab5db4f87efafd761d83ea305d8af6ac1a4ddfd",
-                    "bytes_per_unit": (33868800 + 256) / 131072, "unit": "256-byte key row"},
+                    "sha256": "ae783a10f1c7a4c0e4fb33f29f1b9c45be549dccce943f713e585c4d0b1976ef",
+                    "bytes_per_unit": (33863936 + 0) / 131072, "unit": "256-byte key row"},
     # attention, 70B shape: 2 layers x 8 requests x 8 KV heads x 4096 kept rows:
-    # 272 741 888 B read + 4 417 280 B written
+    # 272 627 456 B read + 3 728 640 B written
     "attention": {"source": "sparse_kv_cache_retrieval_gb300/csrc/sparse_attn.cu",
-                  "sha256": "683d9635124b692bf486c0c1b6e497acc135ba475d6c22e67bce765f4a6e9d18",
-                  "bytes_per_unit": (272741888 + 4417280) / 524288, "unit": "512-byte K+V row"},
+                  "sha256": "a0d2c39512b146c414b49780c9d493bf389fe5d4e4fa9440141f2fc92dae67d4",
+                  "bytes_per_unit": (272627456 + 3728640) / 524288, "unit": "512-byte K+V row"},
     # tcgen05 attention, MQA (64 heads, one KV head): 16 layers x 8 requests x
     # 4096 kept rows (layer 0 by position, layers 1-15 through the slots):
     # 271 034 368 B DRAM read + 3 009 280 B written
