@@ -111,12 +111,15 @@ int attn_tc_group() { return kAtG; }
 // Tiling of one launch: nt tiles per segment, tpc tiles per CTA, at most
 // max_pieces CTAs per segment. Runs of whole segments when they still keep
 // 80% of the CTA target busy (no segment is then split, so no partials are
-// merged); otherwise the tiles are spread evenly over the target. The CTA
-// count is a fixed target (one per SM of a 152-SM GB300), not the device's,
-// so the workspace size is a function of the shapes alone.
+// merged); otherwise the tiles are spread evenly over the target. With one
+// segment per CTA and CTAs to spare, split_pos lets the kernel give each
+// segment whose view is read by position (row gathers, about twice a tiled
+// copy's time per tile) two CTAs, one per half of its tiles. The CTA count is
+// a fixed target (one per SM of a 152-SM GB300), not the device's, so the
+// workspace size is a function of the shapes alone.
 constexpr int kAtCtaTarget = 152;
 static void attn_tc_plan(int n_layers, int B, int n_kv, int budget, int* nt, int* tpc, int* grid,
-                         int* max_pieces) {
+                         int* max_pieces, int* split_pos = nullptr) {
   const long long nseg = (long long)n_layers * B * n_kv;
   const int t = (budget + kAtRows - 1) / kAtRows;
   const long long total = nseg * t;
@@ -133,6 +136,12 @@ static void attn_tc_plan(int n_layers, int B, int n_kv, int budget, int* nt, int
   *grid = (int)((total + c - 1) / c);
   const int mp = c % t == 0 ? 1 : (t + (int)c - 1) / (int)c + 1;
   *max_pieces = mp < t ? mp : t;
+  const bool sp = c == t && nseg < kAtCtaTarget && t >= 2;
+  if (split_pos) *split_pos = sp ? 1 : 0;
+  if (sp) {
+    *grid = (int)(2 * nseg < kAtCtaTarget ? 2 * nseg : kAtCtaTarget);
+    *max_pieces = 2;
+  }
 }
 
 __device__ __forceinline__ void soft_bar() { asm volatile("bar.sync 1, %0;" :: "n"(kAtSoft) : "memory"); }
@@ -263,6 +272,7 @@ __global__ void __maxnreg__(kAtMaxReg) attn_tc_kernel(const __grid_constant__ CU
   uint64_t* ofull = pfree + 2;               // commit after a segment's last O MMAs
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ofull + 1);
   int* s_last = reinterpret_cast<int*>(tmem_slot + 1);
+  __shared__ int s_run[4];                   // split_pos: this CTA's tiles and piece
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -287,13 +297,46 @@ __global__ void __maxnreg__(kAtMaxReg) attn_tc_kernel(const __grid_constant__ CU
     fence_mbar_init();
   }
   if (warp == kAtWarpMma) tmem_alloc<kAtTmemCols>(tmem_slot);
+  if (a.split_pos && warp == 0) {
+    // one segment per CTA, two for a segment whose view reads positions when
+    // the grid has a CTA for every such segment (else none is split): this
+    // CTA's (first tile, end, pieces, piece) from a prefix over the segments
+    const int nseg = a.total / a.nt;
+    auto by_pos = [&](int sg) { return sg < nseg && a.views[sg / a.n_kv].use_slots == 0; };
+    int npos = 0;
+    for (int s0 = 0; s0 < nseg; s0 += 32) npos += __popc(__ballot_sync(0xffffffffu, by_pos(s0 + lane)));
+    const bool split = nseg + npos <= (int)gridDim.x;
+    if (lane == 0) { s_run[0] = 0; s_run[1] = 0; s_run[2] = 1; s_run[3] = 0; }
+    __syncwarp();
+    const int cta = blockIdx.x, half = (a.nt + 1) / 2;
+    int off = 0;
+    for (int s0 = 0; s0 < nseg; s0 += 32) {
+      const int sg = s0 + lane;
+      const int n = sg < nseg ? 1 + ((split && by_pos(sg)) ? 1 : 0) : 0;
+      const int incl = warp_incl_scan(n), first = off + incl - n;
+      if (n > 0 && cta >= first && cta < first + n) {
+        const int pc = cta - first;
+        s_run[0] = sg * a.nt + (pc == 1 ? half : 0);
+        s_run[1] = sg * a.nt + (n == 1 || pc == 1 ? a.nt : half);
+        s_run[2] = n;
+        s_run[3] = pc;
+      }
+      off += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const int t0 = blockIdx.x * a.tpc;
-  const int t1 = min(a.total, t0 + a.tpc);
+  int t0 = blockIdx.x * a.tpc, t1 = min(a.total, t0 + a.tpc);
+  int split_pieces = 1, split_piece = 0;
+  if (a.split_pos) {
+    t0 = s_run[0];
+    t1 = s_run[1];
+    split_pieces = s_run[2];
+    split_piece = s_run[3];
+  }
 
   if (warp == kAtWarpK || warp == kAtWarpV) {
     // ================= producers (K; V)
@@ -690,8 +733,9 @@ __global__ void __maxnreg__(kAtMaxReg) attn_tc_kernel(const __grid_constant__ CU
       }
       tc_fence_before();
       soft_bar();
-      const int pieces = (x.seg * a.nt + a.nt - 1) / a.tpc - (x.seg * a.nt) / a.tpc + 1;
-      const int piece = blockIdx.x - (x.seg * a.nt) / a.tpc;
+      const int pieces =
+          a.split_pos ? split_pieces : (x.seg * a.nt + a.nt - 1) / a.tpc - (x.seg * a.nt) / a.tpc + 1;
+      const int piece = a.split_pos ? split_piece : blockIdx.x - (x.seg * a.nt) / a.tpc;
       float* outp = a.out + ((size_t)x.lb * a.n_q + (size_t)x.g * kAtG + h) * kD;
       float* res = a.part + ((size_t)x.seg * a.max_pieces + piece) * (size_t)kAtG * kAtPart + (size_t)h * kAtPart;
       if (hf == 0) {
@@ -801,7 +845,7 @@ size_t attn_tc_extra_bytes(int n_layers, int B, int n_kv, int budget) {
 
 int attn_tc_launch(AttnTcCall c, int n_layers, void* stream) {
   int grid;
-  attn_tc_plan(n_layers, c.B, c.n_kv, c.K, &c.nt, &c.tpc, &grid, &c.max_pieces);
+  attn_tc_plan(n_layers, c.B, c.n_kv, c.K, &c.nt, &c.tpc, &grid, &c.max_pieces, &c.split_pos);
   c.total = n_layers * c.B * c.n_kv * c.nt;
   if (grid < 1) return SPC_OK;
   const size_t nseg = (size_t)n_layers * c.B * c.n_kv;

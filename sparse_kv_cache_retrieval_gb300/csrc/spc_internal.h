@@ -69,7 +69,7 @@ int scan_tc_scores_launch(ScanTcCall c, int G, float2* part1, int n_parts1, void
 // status word, one merge counter per (layer, request, KV head), and then
 // attn_tc_extra_bytes of split partials and per-CTA tensor maps (from
 // `part` on, 256-byte aligned). attn_tc_launch fills the tiling fields (nt,
-// tpc, total, max_pieces) and `maps`.
+// tpc, total, max_pieces, split_pos) and `maps`.
 struct AttnTcCall {
   const uint16_t* q;
   const spc_kv_view* views;
@@ -82,6 +82,7 @@ struct AttnTcCall {
   int* status;
   int B, n_q, n_kv, K;
   int nt, tpc, total, max_pieces;
+  int split_pos;   // one segment per CTA, position-read segments over two CTAs
   float scale2;
   long long wait_limit;
   int starve;

@@ -203,12 +203,14 @@ def test_fill_slots_bit_exact(source):
 
 
 def _attn_case(rng, L, B, n_q, n_kv, K, cap, use_slots, n_valid=None, empty_group=False, q_gain=1.5,
-               ramp=False, poison=False):
+               ramp=False, poison=False, pos_layers=0):
     """Returns GPU output and oracle output for one attention launch.
 
     ramp: K rows grow in norm with their row index (later tiles hold larger
     logits, so a running maximum keeps rising); poison: rows of the K/V
-    buffers that no kept index names hold NaN (they must not reach the output).
+    buffers that no kept index names hold NaN (they must not reach the output);
+    pos_layers: the first layers read positions from a full cache whatever
+    use_slots says (a launch that mixes both kinds of view).
     """
     d = 128
     sel = np.full((B, n_kv, K), -1, np.int64)
@@ -229,7 +231,8 @@ def _attn_case(rng, L, B, n_q, n_kv, K, cap, use_slots, n_valid=None, empty_grou
     caches, kp, vp, rows, use = [], [], [], [], []
     for l in range(L):
         for b in range(B):
-            nrows = K if use_slots else cap
+            slots_here = use_slots and l >= pos_layers
+            nrows = K if slots_here else cap
             kv = rng.standard_normal((2, n_kv, nrows, d)).astype(np.float32)
             if ramp:
                 kv[0] *= (1.0 + 3.0 * np.arange(nrows) / nrows)[None, :, None].astype(np.float32)
@@ -243,7 +246,7 @@ def _attn_case(rng, L, B, n_q, n_kv, K, cap, use_slots, n_valid=None, empty_grou
                     raw[:, g, unused] = np.int16(0x7FC0)       # bf16 quiet NaN
                 t = torch.from_numpy(raw).to(DEV)
             caches.append((bits, t))
-            kp.append(t[0].data_ptr()); vp.append(t[1].data_ptr()); rows.append(nrows); use.append(use_slots)
+            kp.append(t[0].data_ptr()); vp.append(t[1].data_ptr()); rows.append(nrows); use.append(int(slots_here))
     views = spc.to_device_bytes(spc.kv_views(kp, vp, rows, use), DEV)
     q = O.round_to_bf16(rng.standard_normal((L, B, n_q, d)) * q_gain)
     out = torch.full((L, B, n_q, d), 7.0, dtype=torch.float32, device=DEV)
@@ -259,7 +262,9 @@ def _attn_case(rng, L, B, n_q, n_kv, K, cap, use_slots, n_valid=None, empty_grou
     for l in range(L):
         for b in range(B):
             bits = caches[l * B + b][0]
-            want[l, b] = O.sparse_attention(q[l, b], bits[0], bits[1], kept[b], scale)
+            rows_lb = kept[b] if (use_slots and l >= pos_layers) else \
+                [sel[b, g][sel[b, g] >= 0] for g in range(n_kv)]
+            want[l, b] = O.sparse_attention(q[l, b], bits[0], bits[1], rows_lb, scale)
     return got, want
 
 
@@ -292,6 +297,17 @@ def test_attention_parity(L, B, n_q, n_kv, K, cap, use_slots, n_valid):
     got, want = _attn_case(rng, L, B, n_q, n_kv, K, cap, use_slots, n_valid)
     err = np.abs(got - want)
     assert err.max() <= ATTN_ATOL
+    assert np.all(err <= 2e-5 + 1e-4 * np.abs(want)), f"max err {err.max():.3g}"
+
+
+@pytest.mark.parametrize("L,B,K,cap,n_valid", [(16, 8, 512, 2000, None), (4, 8, 1024, 3000, 900)])
+def test_attention_mixed_views_64_heads(L, B, K, cap, n_valid):
+    """Layer 0 read by position from a full cache, the others through slots, in
+    one launch: with one segment per CTA the position-read segments are split
+    over two CTAs each (their halves merged) while the others stay whole."""
+    rng = np.random.default_rng(31 + L)
+    got, want = _attn_case(rng, L, B, 64, 1, K, cap, 1, n_valid, pos_layers=1)
+    err = np.abs(got - want)
     assert np.all(err <= 2e-5 + 1e-4 * np.abs(want)), f"max err {err.max():.3g}"
 
 
