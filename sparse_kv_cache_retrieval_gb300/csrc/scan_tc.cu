@@ -11,7 +11,7 @@
 //
 // Two passes over the key cache (both HBM-bound, neither writes the logits):
 //  * pass 1 (SCAN stage) folds every head's logits into logsumexp partials
-//    (max, sum 2^(l - max)) per (head, 128-position tile, TMEM lane quadrant);
+//    (max, sum 2^(l - max)) per (head, 128-position tile, slice of the tile);
 //  * a fold kernel turns them into each head's normaliser lse_h (base 2);
 //  * pass 2 (SELECT stage) recomputes the logits and writes one value per
 //    position, the log2 of the group score max_h 2^(l_h - lse_h), which the
@@ -21,27 +21,34 @@
 // and reading them back in the select would move 256 + 256 + 256 B.
 //
 // GB300 design, one CTA per SM, warp-specialised:
+//  * work split: a CTA takes tiles of one segment (request, KV head) while
+//    every segment can have CTAs of its own, the CTAs of a segment
+//    interleaved tile by tile (one advancing front per segment reads the
+//    cache faster than one run per CTA); each CTA stages its first segment's
+//    queries with all its threads before any key copy is issued.
 //  * warp 0, one lane: TMA producer. Each 128-position key tile (32 KiB) comes
 //    in as two 64-dimension boxes of a 3-D tensor map ([segment][position]
 //    [dim]) with the 128-byte swizzle, into a 6-stage ring (192 KiB in flight
 //    per SM); completion is counted in bytes on the stage's mbarrier.
 //    Positions past the capacity are zero-filled by the copy and masked.
-//  * warp 1: allocates the tensor memory (two accumulators of 2G fp32
-//    columns), builds the B operand of the current segment in shared memory
-//    (the group's queries scaled by log2(e)/sqrt(d) and split into a bf16
-//    high part, rows [0, G), and a bf16 low part, rows [G, 2G), so that q.K
-//    keeps ~16 significant bits of q), and one lane issues the MMAs:
-//    D[128 positions][2G] += K_tile[128][128] x Q[2G][128]^T, K = 16 per
-//    instruction, 8 instructions per tile, both operands K-major with the
-//    128-byte swizzle; tcgen05.commit frees the key stage and publishes the
-//    accumulator.
-//  * epilogue warps (CG column groups of 4, CG = 2 for G = 64): warp w reads
-//    TMEM lanes 32 (w % 4) .. +31 (one position per thread) for G / CG of the
-//    heads with tcgen05.ld and adds the high and low products. Pass 1 folds
-//    each head over the warp's 32 positions with a shuffle butterfly that
-//    leaves lane l holding head l's (max, sum); pass 2 takes the maximum over
-//    the thread's heads of l_h - lse_h, combines the column groups through
-//    shared memory and writes 128 consecutive floats per tile.
+//  * warp 1: allocates the tensor memory (two accumulators), rebuilds the
+//    query operand when a run crosses into another segment (the group's
+//    queries scaled by log2(e)/sqrt(d), split into a bf16 high part and a
+//    bf16 low part so that q.K keeps ~16 significant bits of q), and one lane
+//    issues the MMAs, K = 16 per instruction, 8 instructions per tile, both
+//    operands K-major with the 128-byte swizzle; tcgen05.commit frees the key
+//    stage and publishes the accumulator.
+//    Pass 1: D[128 query rows][128 positions] = Q x K_tile^T with head h's
+//    high part in row 2h and its low part in row 2h + 1 (the 2G rows repeated
+//    64 / G times), so that one thread holds one head over a run of positions
+//    and the pair (2h, 2h + 1) adds its parts with one shuffle per value.
+//    Pass 2: D[128 positions][2G] = K_tile x Q^T (high parts in columns
+//    [0, G), low parts in [G, 2G)), one position per thread.
+//  * epilogue warps (CG column groups of 4, CG = 2 for G = 64), warp w on TMEM
+//    lanes 32 (w % 4) .. +31 with tcgen05.ld. Pass 1: each thread folds its
+//    head over its share of the positions into one (max, sum) partial;
+//    pass 2: the maximum over the thread's heads of l_h - lse_h, the column
+//    groups combined through shared memory, 128 consecutive floats per tile.
 // Every mbarrier wait is bounded: a wait that gives up records
 // SPC_ERR_TIMEOUT, the warp stops waiting (it keeps its loop so every
 // barrier is still reached), and in-flight copies and MMAs are waited for
@@ -57,38 +64,41 @@
 
 namespace spc {
 
-constexpr int kTcRows = 128;                 // positions per tile (the MMA's M)
+constexpr int kTcRows = 128;                 // positions per tile
 constexpr int kTcStages = 6;
 constexpr uint32_t kTcTileBytes = kTcRows * kRowBytes;      // 32 KiB
 constexpr uint32_t kTcHalfBytes = kTcTileBytes / 2;         // one 64-dim box
 constexpr long long kTcWait = 4000000000ll;  // clock cycles (~2 s)
-constexpr int kTcPpt = 4;                    // partials per (head, tile): one per TMEM lane quadrant
 
 enum { kPassLse = 0, kPassScore = 1 };
 
-template <int G>
+template <int G, int PASS>
 struct TcShape {
-  static constexpr int N = 2 * G;                                   // MMA N: q high | q low
-  // epilogue: CG column groups of 4 warps (each group covers all 128 TMEM
-  // lanes = positions, for HPT of the heads)
+  // epilogue warps: CG column groups of 4 (one warp per TMEM lane quadrant each)
   static constexpr int CG = G >= 64 ? 2 : 1;
-  static constexpr int HPT = G / CG;                                // 32 (G = 32, 64) or 16
-  static constexpr int LOG_HPT = HPT == 32 ? 5 : 4;
   static constexpr int kEpi = 128 * CG;
   static constexpr int kThreads = 64 + kEpi;
-  static constexpr uint32_t kQBytes = (uint32_t)N * kRowBytes;      // [N][128] bf16, two swizzled halves
+  // pass 1: D[128 query rows][128 positions], the 2G rows (head h high at 2h,
+  // low at 2h + 1) repeated R times; each (replica, column group) takes CW
+  // consecutive positions, split in two between the lanes of a high/low pair
+  static constexpr int R = 64 / G;                                  // 1, 2, 4
+  static constexpr int CW = kTcRows / (R * CG);                     // 64, 64, 32
+  static constexpr int PPT = R * CG * 2;                            // partials per (head, tile): 4, 4, 8
+  // pass 2: D[128 positions][2G] (q high | q low); each thread one position, HPT heads
+  static constexpr int HPT = G / CG;                                // 32 (G = 32, 64) or 16
+  static constexpr int NCOL = PASS == kPassLse ? kTcRows : 2 * G;   // accumulator columns
+  static constexpr int kQRows = PASS == kPassLse ? 128 : 2 * G;
+  static constexpr uint32_t kQBytes = (uint32_t)kQRows * kRowBytes; // two swizzled 64-dim halves
   static constexpr uint32_t kXch = 2 * kTcRows * 4;                 // pass 2: column-group maxima, 2 buffers
-  static constexpr int kTmemCols = 2 * N < 32 ? 32 : 2 * N;        // two accumulators
+  static constexpr int kTmemCols = 2 * NCOL < 32 ? 32 : 2 * NCOL;   // two accumulators
   static constexpr size_t kSmem = 1024 /* alignment slack */ + (size_t)kTcStages * kTcTileBytes + kQBytes +
                                   kXch + 16 * sizeof(uint64_t) + 16;
   // instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major
-  static constexpr uint32_t kIdesc = umma_idesc_bf16(kTcRows, N, false);
+  static constexpr uint32_t kIdesc =
+      PASS == kPassLse ? umma_idesc_bf16(128, kTcRows, false) : umma_idesc_bf16(kTcRows, 2 * G, false);
 };
 
-int scan_tc_ppt(int G) {
-  (void)G;
-  return kTcPpt;
-}
+int scan_tc_ppt(int G) { return G == 16 ? TcShape<16, kPassLse>::PPT : TcShape<64, kPassLse>::PPT; }
 
 // ---------------------------------------------------------------- PTX wrappers
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
@@ -124,10 +134,146 @@ __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2
   m = M;
 }
 
+// ---------------------------------------------------------------- work split
+// The tiles of one CTA. While every non-empty segment can have a CTA of its
+// own, each segment gets 1 + (spare CTAs in proportion to its tile count)
+// and its CTAs interleave: the c-th of n takes tiles c, c + n, c + 2n, ...
+// (so that the CTAs of a segment read one advancing front of the cache, and
+// no CTA changes queries mid-run). Otherwise the non-empty tiles of all
+// segments, in order, are cut into equal consecutive runs. Every thread of
+// the CTA computes the same walk from the lengths.
+struct TileWalk {
+  int seg, tile, step, count;   // step 0: consecutive run across segments
+};
+
+__device__ __forceinline__ int tc_seg_tiles(const ScanTcCall& a, int seg) {
+  return (tc_len(a.len, seg / a.n_kv, a.append, a.cap) + kTcRows - 1) / kTcRows;
+}
+
+__device__ TileWalk tile_walk(const ScanTcCall& a) {
+  const int nseg = a.B * a.n_kv;
+  long long total = 0;
+  int busy = 0;
+  for (int s = 0; s < nseg; ++s) {
+    const int nt = tc_seg_tiles(a, s);
+    total += nt;
+    busy += nt > 0;
+  }
+  TileWalk w{0, 0, 0, 0};
+  const int c = (int)blockIdx.x;
+  if (total == 0) return w;
+  if (busy <= (int)gridDim.x) {
+    const long long spare = (long long)gridDim.x - busy;
+    int first = 0;
+    for (int s = 0; s < nseg; ++s) {
+      const int nt = tc_seg_tiles(a, s);
+      if (nt == 0) continue;
+      const int n = (int)min((long long)nt, 1 + spare * nt / total);
+      if (c < first + n) {
+        const int k = c - first;
+        w.seg = s;
+        w.tile = k;
+        w.step = n;
+        w.count = (nt - k + n - 1) / n;
+        return w;
+      }
+      first += n;
+    }
+    return w;
+  }
+  const long long per = (total + gridDim.x - 1) / gridDim.x;
+  long long v = (long long)c * per;
+  if (v >= total) return w;
+  w.count = (int)min(per, total - v);
+  for (int s = 0; s < nseg; ++s) {
+    const int nt = tc_seg_tiles(a, s);
+    if (v < nt) {
+      w.seg = s;
+      w.tile = (int)v;
+      return w;
+    }
+    v -= nt;
+  }
+  w.count = 0;
+  return w;
+}
+
+// the next tile of the walk (called only while tiles remain)
+__device__ __forceinline__ void walk_next(const ScanTcCall& a, TileWalk& w) {
+  if (w.step > 0) {
+    w.tile += w.step;
+    return;
+  }
+  ++w.tile;
+  while (w.tile >= tc_seg_tiles(a, w.seg)) {
+    ++w.seg;
+    w.tile = 0;
+  }
+}
+
+// ---------------------------------------------------------------- query operand
+// The group's queries scaled by log2(e)/sqrt(d), split into a bf16 high part
+// and a bf16 low part (q.K keeps ~16 significant bits of q), K-major with the
+// 128-byte swizzle: element (row n, dim k) sits in half k / 64 at byte
+// n * 128 + (((k % 64) / 8) ^ (n % 8)) * 16 + (k % 8) * 2. Pass 1 (A operand,
+// 128 rows): head h high at row 2h + 2G r, low at row 2h + 1 + 2G r, for
+// each replica r; pass 2 (B operand, 2G rows): high at row h, low at G + h.
+// Thread `tid` of `nthr` converts units of 8 dims, loading a batch of up to
+// 8 units before it stores any.
 template <int G, int PASS>
-__global__ void __launch_bounds__(TcShape<G>::kThreads, 1) scan_tc_kernel(const __grid_constant__ CUtensorMap kmap,
-                                                                          ScanTcCall a) {
-  using S = TcShape<G>;
+__device__ __forceinline__ void stage_q(uint32_t q0, const float* qg, float qscale, int tid, int nthr) {
+  using S = TcShape<G, PASS>;
+  constexpr int kUnits = G * 16;   // 16 units of 8 dims per head
+  constexpr int kB = 8;
+  for (int u0 = tid; u0 < kUnits; u0 += kB * nthr) {
+    float4 xs[2 * kB];
+#pragma unroll
+    for (int i = 0; i < kB; ++i) {
+      const int unit = u0 + i * nthr;
+      if (unit < kUnits) {
+        const float* src = qg + (size_t)(unit >> 4) * kD + (unit & 15) * 8;
+        xs[2 * i] = *reinterpret_cast<const float4*>(src);
+        xs[2 * i + 1] = *reinterpret_cast<const float4*>(src + 4);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kB; ++i) {
+      const int unit = u0 + i * nthr;
+      if (unit >= kUnits) break;
+      const int h = unit >> 4, half = (unit >> 3) & 1, u = unit & 7;
+      const float v[8] = {xs[2 * i].x, xs[2 * i].y, xs[2 * i].z, xs[2 * i].w,
+                          xs[2 * i + 1].x, xs[2 * i + 1].y, xs[2 * i + 1].z, xs[2 * i + 1].w};
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float p0 = v[2 * e] * qscale, p1 = v[2 * e + 1] * qscale;
+        const float h0 = bf16_round(p0), h1 = bf16_round(p1);
+        hi[e] = pack_bf16(h0, h1);
+        lo[e] = pack_bf16(p0 - h0, p1 - h1);
+      }
+      const uint32_t hb = q0 + (uint32_t)half * (S::kQRows * 128);
+      constexpr int kCopies = PASS == kPassLse ? S::R : 1;
+#pragma unroll
+      for (int r = 0; r < kCopies; ++r) {
+        const int nh = PASS == kPassLse ? 2 * G * r + 2 * h : h;
+        const int nl = PASS == kPassLse ? nh + 1 : h + G;
+        const uint32_t ah = hb + (uint32_t)nh * 128 + (uint32_t)((u ^ (nh & 7)) << 4);
+        const uint32_t al = hb + (uint32_t)nl * 128 + (uint32_t)((u ^ (nl & 7)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" :: "r"(ah), "r"(hi[0]), "r"(hi[1]), "r"(hi[2]),
+                     "r"(hi[3]) : "memory");
+        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" :: "r"(al), "r"(lo[0]), "r"(lo[1]), "r"(lo[2]),
+                     "r"(lo[3]) : "memory");
+      }
+    }
+  }
+  // generic-proxy writes made visible to the tensor core's async proxy
+  fence_proxy_async_smem();
+}
+
+template <int G, int PASS>
+__global__ void __launch_bounds__(TcShape<G, PASS>::kThreads, 1) scan_tc_kernel(const __grid_constant__ CUtensorMap kmap,
+                                                                                ScanTcCall a) {
+  using S = TcShape<G, PASS>;
   extern __shared__ uint8_t tc_raw[];
   // 1024-byte aligned base (the 128-byte swizzle repeats every 8 rows of 128 B)
   const uint32_t raw_addr = smem_u32(tc_raw);
@@ -140,8 +286,17 @@ __global__ void __launch_bounds__(TcShape<G>::kThreads, 1) scan_tc_kernel(const 
   uint64_t* acc_full = empty + kTcStages;     // [2]
   uint64_t* acc_empty = acc_full + 2;         // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  const uint32_t q0 = smem_u32(qsm);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const TileWalk w0 = tile_walk(a);
+  // the first segment's queries, staged by every thread before any key copy
+  // is issued (behind the copies of all SMs their loads would wait for
+  // microseconds)
+  if (w0.count > 0) {
+    const int b = w0.seg / a.n_kv, g = w0.seg - b * a.n_kv;
+    stage_q<G, PASS>(q0, a.q + ((size_t)b * a.n_q + (size_t)g * G) * kD, a.qscale, threadIdx.x, S::kThreads);
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kTcStages; ++s) {
       mbar_init(&full[s], 1);        // the producer's expect_tx arrival (+ the copies' bytes)
@@ -161,18 +316,14 @@ __global__ void __launch_bounds__(TcShape<G>::kThreads, 1) scan_tc_kernel(const 
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const int t0 = blockIdx.x * a.tpc;
-  const int t_end = min(a.total_tiles, t0 + a.tpc);
-
   if (warp == 0) {
     // ================= TMA producer (one lane)
     if (lane == 0) {
       int it = 0;
       bool dead = false;
-      for (int t = t0; t < t_end && !dead; ++t) {
-        const int seg = t / a.n_tiles, tile = t - seg * a.n_tiles;
-        const int b = seg / a.n_kv;
-        if (tile * kTcRows >= tc_len(a.len, b, a.append, a.cap)) continue;
+      TileWalk w = w0;
+      for (int i = 0; i < w.count && !dead; ++i) {
+        if (i) walk_next(a, w);
         const int s = it % kTcStages;
         const uint32_t ph = (it / kTcStages) & 1;
         if (!mbar_wait_bounded(&empty[s], ph ^ 1, kTcWait)) {
@@ -182,8 +333,8 @@ __global__ void __launch_bounds__(TcShape<G>::kThreads, 1) scan_tc_kernel(const 
         }
         mbar_arrive_expect_tx(&full[s], kTcTileBytes);
         const uint32_t dst = smem_u32(stages + (size_t)s * kTcTileBytes);
-        tma_load_3d(dst, &kmap, 0, tile * kTcRows, seg, &full[s]);
-        tma_load_3d(dst + kTcHalfBytes, &kmap, 64, tile * kTcRows, seg, &full[s]);
+        tma_load_3d(dst, &kmap, 0, w.tile * kTcRows, w.seg, &full[s]);
+        tma_load_3d(dst + kTcHalfBytes, &kmap, 64, w.tile * kTcRows, w.seg, &full[s]);
         ++it;
       }
       // the copies still in flight land before the CTA may exit
@@ -192,15 +343,13 @@ __global__ void __launch_bounds__(TcShape<G>::kThreads, 1) scan_tc_kernel(const 
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ================= B operand (queries) and MMA issue
-    int it = 0, cur_seg = -1, last_it = -1;
+    // ================= query operand of later segments, and MMA issue
+    int it = 0, cur_seg = w0.seg, last_it = -1;
     bool dead = false;
-    const uint32_t q0 = smem_u32(qsm);
-    for (int t = t0; t < t_end; ++t) {
-      const int seg = t / a.n_tiles, tile = t - seg * a.n_tiles;
-      const int b = seg / a.n_kv, g = seg - b * a.n_kv;
-      if (tile * kTcRows >= tc_len(a.len, b, a.append, a.cap)) continue;
-      if (seg != cur_seg) {
+    TileWalk w = w0;
+    for (int i = 0; i < w.count; ++i) {
+      if (i) walk_next(a, w);
+      if (w.seg != cur_seg) {
         // the MMAs that read the previous segment's queries must be done
         if (last_it >= 0 && !dead) {
           bool ok = true;
@@ -211,36 +360,10 @@ __global__ void __launch_bounds__(TcShape<G>::kThreads, 1) scan_tc_kernel(const 
             dead = true;
           }
         }
-        // rows [0, G): bf16(q * scale); rows [G, 2G): bf16 of the remainder.
-        // Element (row n, dim k) sits in half k / 64 at byte
-        // n * 128 + (((k % 64) / 8) ^ (n % 8)) * 16 + (k % 8) * 2
-        const float* qg = a.q + ((size_t)b * a.n_q + (size_t)g * G) * kD;
-        for (int item = lane; item < G * 16; item += 32) {
-          const int h = item >> 4, u16 = item & 15;         // 16 units of 8 dims per head
-          const float4 x0 = *reinterpret_cast<const float4*>(qg + (size_t)h * kD + u16 * 8);
-          const float4 x1 = *reinterpret_cast<const float4*>(qg + (size_t)h * kD + u16 * 8 + 4);
-          float v[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-          uint32_t hi[4], lo[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float p0 = v[2 * e] * a.qscale, p1 = v[2 * e + 1] * a.qscale;
-            const float h0 = bf16_round(p0), h1 = bf16_round(p1);
-            hi[e] = pack_bf16(h0, h1);
-            lo[e] = pack_bf16(p0 - h0, p1 - h1);
-          }
-          const int half = u16 >> 3, u = u16 & 7;
-          const uint32_t hrow = q0 + (uint32_t)half * (S::N * 128) + (uint32_t)h * 128 + (uint32_t)((u ^ (h & 7)) << 4);
-          const int hl = h + G;
-          const uint32_t lrow = q0 + (uint32_t)half * (S::N * 128) + (uint32_t)hl * 128 + (uint32_t)((u ^ (hl & 7)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" :: "r"(hrow), "r"(hi[0]), "r"(hi[1]), "r"(hi[2]),
-                       "r"(hi[3]) : "memory");
-          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" :: "r"(lrow), "r"(lo[0]), "r"(lo[1]), "r"(lo[2]),
-                       "r"(lo[3]) : "memory");
-        }
-        // generic-proxy writes made visible to the tensor core's async proxy
-        fence_proxy_async_smem();
+        const int b = w.seg / a.n_kv, g = w.seg - b * a.n_kv;
+        stage_q<G, PASS>(q0, a.q + ((size_t)b * a.n_q + (size_t)g * G) * kD, a.qscale, lane, 32);
         __syncwarp();
-        cur_seg = seg;
+        cur_seg = w.seg;
       }
       const int s = it % kTcStages;
       const uint32_t ph = (it / kTcStages) & 1;
@@ -253,14 +376,19 @@ __global__ void __launch_bounds__(TcShape<G>::kThreads, 1) scan_tc_kernel(const 
         } else {
           tc_fence_after();
           const uint32_t kst = smem_u32(stages + (size_t)s * kTcTileBytes);
-          const uint32_t dcol = tmem + (uint32_t)(acc * S::N);
+          const uint32_t dcol = tmem + (uint32_t)(acc * S::NCOL);
+          // K = 16 per instruction, 8 per tile; pass 1: D[q rows][positions] =
+          // Q x K_tile^T, pass 2: D[positions][q rows] = K_tile x Q^T
 #pragma unroll
           for (int half = 0; half < 2; ++half)
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              const uint64_t ad = umma_desc_sw128(kst + (uint32_t)half * kTcHalfBytes + (uint32_t)k * 32);
-              const uint64_t bd = umma_desc_sw128(q0 + (uint32_t)half * (S::N * 128) + (uint32_t)k * 32);
-              umma_f16(dcol, ad, bd, S::kIdesc, (half | k) ? 1u : 0u);
+              const uint64_t kd = umma_desc_sw128(kst + (uint32_t)half * kTcHalfBytes + (uint32_t)k * 32);
+              const uint64_t qd = umma_desc_sw128(q0 + (uint32_t)half * (S::kQRows * 128) + (uint32_t)k * 32);
+              if constexpr (PASS == kPassLse)
+                umma_f16(dcol, qd, kd, S::kIdesc, (half | k) ? 1u : 0u);
+              else
+                umma_f16(dcol, kd, qd, S::kIdesc, (half | k) ? 1u : 0u);
             }
           umma_commit(&empty[s]);          // the key stage may be refilled once these MMAs are done
           umma_commit(&acc_full[acc]);     // the accumulator is ready for the epilogue
@@ -276,22 +404,20 @@ __global__ void __launch_bounds__(TcShape<G>::kThreads, 1) scan_tc_kernel(const 
       mbar_wait_bounded(&acc_full[last_it & 1], (last_it >> 1) & 1, kTcWait);
     __syncwarp();
   } else {
-    // ================= epilogue: one position per thread, HPT of its heads
+    // ================= epilogue
     const int quad = warp & 3;                      // TMEM lanes 32 quad .. 32 quad + 31
-    const int cg = (warp - 2) >> 2;                 // column group: heads [cg HPT, (cg + 1) HPT)
-    const int p = quad * 32 + lane;                 // this thread's position in the tile
+    const int cg = (warp - 2) >> 2;                 // column group
     const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
     float lse_r[S::HPT];                            // pass 2: this thread's heads' normalisers
     int cur_seg = -1;
     bool dead = false;
-    int it = 0;
-    for (int t = t0; t < t_end; ++t) {
-      const int seg = t / a.n_tiles, tile = t - seg * a.n_tiles;
+    TileWalk w = w0;
+    for (int it = 0; it < w.count; ++it) {
+      if (it) walk_next(a, w);
+      const int seg = w.seg, tile = w.tile;
       const int b = seg / a.n_kv, g = seg - b * a.n_kv;
-      const int L = tc_len(a.len, b, a.append, a.cap);
       const int row0 = tile * kTcRows;
-      if (row0 >= L) continue;
-      const int nrows = min(kTcRows, L - row0);
+      const int nrows = min(kTcRows, tc_len(a.len, b, a.append, a.cap) - row0);
       if (PASS == kPassScore && seg != cur_seg) {
         const float* lg = a.lse + (size_t)b * a.n_q + (size_t)g * G + cg * S::HPT;
 #pragma unroll
@@ -304,72 +430,81 @@ __global__ void __launch_bounds__(TcShape<G>::kThreads, 1) scan_tc_kernel(const 
         dead = true;
       }
       tc_fence_after();
-      const bool valid = p < nrows && !dead;
-      float v[S::HPT];
-      {
-        const uint32_t hc = trow + (uint32_t)(acc * S::N + cg * S::HPT);
-        float hi[S::HPT], lo[S::HPT];
-        if (!dead) {
-          if constexpr (S::HPT == 32) {
-            tmem_ld32(hc, hi);
-            tmem_ld32(hc + G, lo);
-          } else {
-            tmem_ld16(hc, hi);
-            tmem_ld16(hc + G, lo);
-          }
-          tmem_ld_wait();
-        }
-#pragma unroll
-        for (int h = 0; h < S::HPT; ++h) v[h] = valid ? hi[h] + lo[h] : -INFINITY;
-      }
-      // this warp is done with the accumulator
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[acc]);
 
       if constexpr (PASS == kPassLse) {
-        // ---- (max, sum 2^(l - max)) of every head over this warp's 32
-        // positions: a butterfly that halves the heads a lane keeps at each
-        // step, so lane l ends with head l (16 heads: lanes 2j and 2j + 1
-        // with head j, merged at the end)
-        float m[S::HPT], sm[S::HPT];
-#pragma unroll
-        for (int h = 0; h < S::HPT; ++h) {
-          m[h] = v[h];
-          sm[h] = v[h] == -INFINITY ? 0.f : 1.f;
+        // ---- lane = query row 32 quad + lane: head ((32 quad + lane) % 2G) / 2,
+        // the high part on even lanes, the low part on odd ones; the warp's CW
+        // columns are positions, the pair splits them: the even lane takes the
+        // first half (its high part + its partner's low part), the odd lane
+        // the second. Then (max, sum 2^(l - max)) over the thread's positions.
+        constexpr int CT = S::CW / 2;                 // positions per thread
+        const int rep = quad * 16 / G;                // replica of this quadrant's rows
+        const int cbase = (rep * S::CG + cg) * S::CW;
+        const bool odd = (lane & 1) != 0;
+        float xa[32], xb[32];
+        if (!dead) {
+          tmem_ld32(trow + (uint32_t)(acc * S::NCOL + cbase), xa);
+          if constexpr (S::CW == 64) tmem_ld32(trow + (uint32_t)(acc * S::NCOL + cbase + 32), xb);
+          tmem_ld_wait();
         }
+        // this warp is done with the accumulator
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        float v[CT];
 #pragma unroll
-        for (int st = 0; st < S::LOG_HPT; ++st) {
-          const int k = 16 >> st;                      // lane bit of this step
-          const int n = S::HPT >> (st + 1);            // heads kept after it
-          const bool up = (lane & k) != 0;
-#pragma unroll
-          for (int i = 0; i < n; ++i) {
-            const float gm = up ? m[i] : m[i + n], gs = up ? sm[i] : sm[i + n];
-            float km = up ? m[i + n] : m[i], ks = up ? sm[i + n] : sm[i];
-            const float rm = __shfl_xor_sync(0xffffffffu, gm, k);
-            const float rs = __shfl_xor_sync(0xffffffffu, gs, k);
-            lse_merge(km, ks, rm, rs);
-            m[i] = km;
-            sm[i] = ks;
+        for (int j = 0; j < CT; ++j) {
+          float first, second;
+          if constexpr (S::CW == 64) {
+            first = xa[j];
+            second = xb[j];
+          } else {
+            first = xa[j];
+            second = xa[CT + j];
           }
+          const float send = odd ? first : second;
+          const float mine = odd ? second : first;
+          v[j] = mine + __shfl_xor_sync(0xffffffffu, send, 1);
         }
-        int head = lane;
-        if constexpr (S::HPT == 16) {
-          const float rm = __shfl_xor_sync(0xffffffffu, m[0], 1), rs = __shfl_xor_sync(0xffffffffu, sm[0], 1);
-          lse_merge(m[0], sm[0], rm, rs);
-          head = lane >> 1;
-        }
-        if (S::HPT == 32 || (lane & 1) == 0) {
-          const int h = cg * S::HPT + head;
-          a.part[((size_t)b * a.n_q + (size_t)g * G + h) * a.n_parts + (size_t)tile * kTcPpt + quad] =
-              make_float2(m[0], sm[0]);
-        }
-      } else {
-        // ---- log2 of the group score: max over heads of l_h - lse_h
-        float gs = -INFINITY;
+        const int c0 = cbase + (odd ? CT : 0);
+        const int nv = dead ? 0 : nrows - c0;         // valid positions of this thread's CT
+        float m = -INFINITY;
 #pragma unroll
-        for (int h = 0; h < S::HPT; ++h) gs = fmaxf(gs, v[h] - lse_r[h]);
+        for (int j = 0; j < CT; ++j) m = j < nv ? fmaxf(m, v[j]) : m;
+        float sm = 0.f;
+        if (m != -INFINITY) {
+#pragma unroll
+          for (int j = 0; j < CT; ++j) sm += j < nv ? ex2_approx(v[j] - m) : 0.f;
+        }
+        const int h = ((32 * quad + lane) % (2 * G)) >> 1;
+        a.part[((size_t)b * a.n_q + (size_t)g * G + h) * a.n_parts + (size_t)tile * S::PPT +
+               (rep * S::CG + cg) * 2 + (odd ? 1 : 0)] = make_float2(m, sm);
+      } else {
+        // ---- lane = position 32 quad + lane of the tile, HPT of the heads;
+        // log2 of the group score: max over heads of l_h - lse_h
+        const int p = quad * 32 + lane;
+        const bool valid = p < nrows && !dead;
+        float gs = -INFINITY;
+        {
+          const uint32_t hc = trow + (uint32_t)(acc * S::NCOL + cg * S::HPT);
+          float hi[S::HPT], lo[S::HPT];
+          if (!dead) {
+            if constexpr (S::HPT == 32) {
+              tmem_ld32(hc, hi);
+              tmem_ld32(hc + G, lo);
+            } else {
+              tmem_ld16(hc, hi);
+              tmem_ld16(hc + G, lo);
+            }
+            tmem_ld_wait();
+          }
+          // this warp is done with the accumulator
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[acc]);
+#pragma unroll
+          for (int h = 0; h < S::HPT; ++h) gs = fmaxf(gs, hi[h] + lo[h] - lse_r[h]);
+        }
         if constexpr (S::CG == 2) {
           float* x = xch + (it & 1) * kTcRows;
           if (cg == 1) x[p] = gs;
@@ -378,7 +513,6 @@ __global__ void __launch_bounds__(TcShape<G>::kThreads, 1) scan_tc_kernel(const 
         }
         if (cg == 0 && valid) a.gscore[(size_t)seg * a.lstride + row0 + p] = gs;
       }
-      ++it;
     }
     tc_fence_before();
   }
@@ -397,13 +531,14 @@ __global__ void __launch_bounds__(TcShape<G>::kThreads, 1) scan_tc_kernel(const 
 // select that ranks the group scores (one partial per tile: (0, 1) first).
 constexpr int kFoldThreads = 256;
 constexpr int kFoldHeads = kFoldThreads / 32;     // heads per CTA
-__global__ void __launch_bounds__(kFoldThreads) lse_fold_kernel(ScanTcCall a, int G, float2* part1, int n_parts1) {
+__global__ void __launch_bounds__(kFoldThreads) lse_fold_kernel(ScanTcCall a, int G, int ppt, float2* part1,
+                                                                int n_parts1) {
   const int per_seg = (G + kFoldHeads - 1) / kFoldHeads;
   const int seg = blockIdx.x / per_seg, hblk = blockIdx.x - seg * per_seg;
   const int b = seg / a.n_kv, g = seg - b * a.n_kv;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int L = tc_len(a.len, b, a.append, a.cap);
-  const int nv = ((L + kTcRows - 1) / kTcRows) * kTcPpt;
+  const int nv = ((L + kTcRows - 1) / kTcRows) * ppt;
   const int h = hblk * kFoldHeads + warp;
   if (h < G) {
     const float2* ph = a.part + ((size_t)b * a.n_q + (size_t)g * G + h) * a.n_parts;
@@ -430,11 +565,11 @@ __global__ void __launch_bounds__(kFoldThreads) lse_fold_kernel(ScanTcCall a, in
 // ---------------------------------------------------------------- host side
 template <int G, int PASS>
 static cudaError_t launch_tc(const CUtensorMap& map, const ScanTcCall& c, int grid, cudaStream_t st) {
-  const size_t smem = TcShape<G>::kSmem;
+  const size_t smem = TcShape<G, PASS>::kSmem;
   cudaError_t e =
       set_func_attr((const void*)scan_tc_kernel<G, PASS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  scan_tc_kernel<G, PASS><<<grid, TcShape<G>::kThreads, smem, st>>>(map, c);
+  scan_tc_kernel<G, PASS><<<grid, TcShape<G, PASS>::kThreads, smem, st>>>(map, c);
   return cudaGetLastError();
 }
 
@@ -445,11 +580,10 @@ static int scan_tc_pass(ScanTcCall c, int G, int pass, cudaStream_t st) {
   const uint64_t strides[2] = {(uint64_t)kRowBytes, (uint64_t)c.cap * kRowBytes};
   const uint32_t box[3] = {64, (uint32_t)kTcRows, 1};
   if (!tensor_map_bf16_sw128(&map, c.K, 3, dims, strides, box)) return SPC_ERR_CUDA;
-  // one wave: one CTA per SM, each a run of consecutive tiles
+  // one wave: one CTA per SM (at most one per capacity tile); each CTA
+  // finds its tiles from the lengths on the device
   const int sms = device_sm_count() > 0 ? device_sm_count() : 1;
-  c.tpc = (c.total_tiles + sms - 1) / sms;
-  if (c.tpc < 1) c.tpc = 1;
-  const int grid = (c.total_tiles + c.tpc - 1) / c.tpc;
+  const int grid = c.total_tiles < sms ? c.total_tiles : sms;
   if (grid < 1) return SPC_OK;
   cudaError_t e;
   switch (G * 2 + pass) {
@@ -470,7 +604,7 @@ int scan_tc_launch(ScanTcCall c, int G, void* stream) {
 
 int scan_tc_scores_launch(ScanTcCall c, int G, float2* part1, int n_parts1, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  lse_fold_kernel<<<c.B * c.n_kv * ((G + kFoldHeads - 1) / kFoldHeads), kFoldThreads, 0, st>>>(c, G, part1, n_parts1);
+  lse_fold_kernel<<<c.B * c.n_kv * ((G + kFoldHeads - 1) / kFoldHeads), kFoldThreads, 0, st>>>(c, G, scan_tc_ppt(G), part1, n_parts1);
   if (cudaGetLastError() != cudaSuccess) return SPC_ERR_CUDA;
   return scan_tc_pass(c, G, kPassScore, st);
 }

@@ -57,7 +57,7 @@ struct ScanTcCall {
   float* lse;
   float* gscore;
   int* status;
-  int B, n_q, n_kv, cap, lstride, n_tiles, total_tiles, append, n_parts, tpc;
+  int B, n_q, n_kv, cap, lstride, n_tiles, total_tiles, append, n_parts;
   float qscale;
 };
 int scan_tc_ppt(int G);
