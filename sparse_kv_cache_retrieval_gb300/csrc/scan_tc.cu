@@ -75,15 +75,15 @@ enum { kPassLse = 0, kPassScore = 1 };
 template <int G, int PASS>
 struct TcShape {
   // epilogue warps: CG column groups of 4 (one warp per TMEM lane quadrant each)
-  static constexpr int CG = G >= 64 ? 2 : 1;
+  static constexpr int CG = PASS == kPassLse ? G / 16 : (G >= 64 ? 2 : 1);
   static constexpr int kEpi = 128 * CG;
   static constexpr int kThreads = 64 + kEpi;
   // pass 1: D[128 query rows][128 positions], the 2G rows (head h high at 2h,
   // low at 2h + 1) repeated R times; each (replica, column group) takes CW
   // consecutive positions, split in two between the lanes of a high/low pair
   static constexpr int R = 64 / G;                                  // 1, 2, 4
-  static constexpr int CW = kTcRows / (R * CG);                     // 64, 64, 32
-  static constexpr int PPT = R * CG * 2;                            // partials per (head, tile): 4, 4, 8
+  static constexpr int CW = kTcRows / (R * CG);                     // 32
+  static constexpr int PPT = R * CG;                                // partials per (head, tile): 4
   // pass 2: D[128 positions][2G] (q high | q low); each thread one position, HPT heads
   static constexpr int HPT = G / CG;                                // 32 (G = 32, 64) or 16
   static constexpr int NCOL = PASS == kPassLse ? kTcRows : 2 * G;   // accumulator columns
@@ -98,7 +98,12 @@ struct TcShape {
       PASS == kPassLse ? umma_idesc_bf16(128, kTcRows, false) : umma_idesc_bf16(kTcRows, 2 * G, false);
 };
 
-int scan_tc_ppt(int G) { return G == 16 ? TcShape<16, kPassLse>::PPT : TcShape<64, kPassLse>::PPT; }
+static_assert(TcShape<16, kPassLse>::PPT == 4 && TcShape<32, kPassLse>::PPT == 4 && TcShape<64, kPassLse>::PPT == 4,
+              "one partial per (head, tile, quarter of the tile)");
+int scan_tc_ppt(int G) {
+  (void)G;
+  return 4;
+}
 
 // ---------------------------------------------------------------- PTX wrappers
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
@@ -218,17 +223,16 @@ __device__ __forceinline__ void walk_next(const ScanTcCall& a, TileWalk& w) {
 // n * 128 + (((k % 64) / 8) ^ (n % 8)) * 16 + (k % 8) * 2. Pass 1 (A operand,
 // 128 rows): head h high at row 2h + 2G r, low at row 2h + 1 + 2G r, for
 // each replica r; pass 2 (B operand, 2G rows): high at row h, low at G + h.
-// Thread `tid` of `nthr` converts units of 8 dims, loading a batch of up to
-// 8 units before it stores any.
-template <int G, int PASS>
-__device__ __forceinline__ void stage_q(uint32_t q0, const float* qg, float qscale, int tid, int nthr) {
-  using S = TcShape<G, PASS>;
-  constexpr int kUnits = G * 16;   // 16 units of 8 dims per head
-  constexpr int kB = 8;
-  for (int u0 = tid; u0 < kUnits; u0 += kB * nthr) {
-    float4 xs[2 * kB];
+// Thread `tid` of `nthr` converts the units of 8 dims u0 + i nthr, i < NB:
+// load() issues all their loads, store() converts and stores them.
+template <int G, int PASS, int NB>
+struct QStage {
+  static constexpr int kUnits = G * 16;   // 16 units of 8 dims per head
+  float4 xs[2 * NB];
+
+  __device__ __forceinline__ void load(const float* qg, int u0, int nthr) {
 #pragma unroll
-    for (int i = 0; i < kB; ++i) {
+    for (int i = 0; i < NB; ++i) {
       const int unit = u0 + i * nthr;
       if (unit < kUnits) {
         const float* src = qg + (size_t)(unit >> 4) * kD + (unit & 15) * 8;
@@ -236,8 +240,12 @@ __device__ __forceinline__ void stage_q(uint32_t q0, const float* qg, float qsca
         xs[2 * i + 1] = *reinterpret_cast<const float4*>(src + 4);
       }
     }
+  }
+
+  __device__ __forceinline__ void store(uint32_t q0, float qscale, int u0, int nthr) const {
+    using S = TcShape<G, PASS>;
 #pragma unroll
-    for (int i = 0; i < kB; ++i) {
+    for (int i = 0; i < NB; ++i) {
       const int unit = u0 + i * nthr;
       if (unit >= kUnits) break;
       const int h = unit >> 4, half = (unit >> 3) & 1, u = unit & 7;
@@ -266,6 +274,16 @@ __device__ __forceinline__ void stage_q(uint32_t q0, const float* qg, float qsca
       }
     }
   }
+};
+
+// the whole operand by one warp, a batch of 8 units per lane in flight
+template <int G, int PASS>
+__device__ __forceinline__ void stage_q_warp(uint32_t q0, const float* qg, float qscale, int lane) {
+  QStage<G, PASS, 8> qs;
+  for (int u0 = lane; u0 < G * 16; u0 += 8 * 32) {
+    qs.load(qg, u0, 32);
+    qs.store(q0, qscale, u0, 32);
+  }
   // generic-proxy writes made visible to the tensor core's async proxy
   fence_proxy_async_smem();
 }
@@ -289,14 +307,28 @@ __global__ void __launch_bounds__(TcShape<G, PASS>::kThreads, 1) scan_tc_kernel(
   const uint32_t q0 = smem_u32(qsm);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&kmap)) : "memory");
   const TileWalk w0 = tile_walk(a);
-  // the first segment's queries, staged by every thread before any key copy
-  // is issued (behind the copies of all SMs their loads would wait for
-  // microseconds)
+  // The first segment's queries: every thread issues its loads before any
+  // key copy (behind the copies of all SMs they would wait for
+  // microseconds), thread 0 then starts the first copies, and the
+  // conversion overlaps their latency.
+  constexpr int kPro = (G * 16 + S::kThreads - 1) / S::kThreads;
+  QStage<G, PASS, kPro> qs;
   if (w0.count > 0) {
     const int b = w0.seg / a.n_kv, g = w0.seg - b * a.n_kv;
-    stage_q<G, PASS>(q0, a.q + ((size_t)b * a.n_q + (size_t)g * G) * kD, a.qscale, threadIdx.x, S::kThreads);
+    qs.load(a.q + ((size_t)b * a.n_q + (size_t)g * G) * kD, threadIdx.x, S::kThreads);
   }
+  // producer state (thread 0): tiles issued, and the walk at the last one
+  int p_it = 0;
+  bool p_dead = false;
+  TileWalk pw = w0;
+  auto issue = [&](int s) {
+    mbar_arrive_expect_tx(&full[s], kTcTileBytes);
+    const uint32_t dst = smem_u32(stages + (size_t)s * kTcTileBytes);
+    tma_load_3d(dst, &kmap, 0, pw.tile * kTcRows, pw.seg, &full[s]);
+    tma_load_3d(dst + kTcHalfBytes, &kmap, 64, pw.tile * kTcRows, pw.seg, &full[s]);
+  };
   if (threadIdx.x == 0) {
     for (int s = 0; s < kTcStages; ++s) {
       mbar_init(&full[s], 1);        // the producer's expect_tx arrival (+ the copies' bytes)
@@ -307,6 +339,15 @@ __global__ void __launch_bounds__(TcShape<G, PASS>::kThreads, 1) scan_tc_kernel(
       mbar_init(&acc_empty[i], S::kEpi / 32);   // one arrival per epilogue warp
     }
     fence_mbar_init();
+    // the ring starts empty: the first copies need no wait
+    for (; p_it < kTcStages && p_it < w0.count; ++p_it) {
+      if (p_it) walk_next(a, pw);
+      issue(p_it);
+    }
+  }
+  if (w0.count > 0) {
+    qs.store(q0, a.qscale, threadIdx.x, S::kThreads);
+    fence_proxy_async_smem();
   }
   if (warp == 1) {
     tmem_alloc<S::kTmemCols>(tmem_slot);
@@ -319,26 +360,19 @@ __global__ void __launch_bounds__(TcShape<G, PASS>::kThreads, 1) scan_tc_kernel(
   if (warp == 0) {
     // ================= TMA producer (one lane)
     if (lane == 0) {
-      int it = 0;
-      bool dead = false;
-      TileWalk w = w0;
-      for (int i = 0; i < w.count && !dead; ++i) {
-        if (i) walk_next(a, w);
-        const int s = it % kTcStages;
-        const uint32_t ph = (it / kTcStages) & 1;
+      for (; p_it < w0.count && !p_dead; ++p_it) {
+        walk_next(a, pw);
+        const int s = p_it % kTcStages;
+        const uint32_t ph = (p_it / kTcStages) & 1;
         if (!mbar_wait_bounded(&empty[s], ph ^ 1, kTcWait)) {
           set_status(a.status, SPC_ERR_TIMEOUT);
-          dead = true;
+          p_dead = true;
           break;
         }
-        mbar_arrive_expect_tx(&full[s], kTcTileBytes);
-        const uint32_t dst = smem_u32(stages + (size_t)s * kTcTileBytes);
-        tma_load_3d(dst, &kmap, 0, w.tile * kTcRows, w.seg, &full[s]);
-        tma_load_3d(dst + kTcHalfBytes, &kmap, 64, w.tile * kTcRows, w.seg, &full[s]);
-        ++it;
+        issue(s);
       }
       // the copies still in flight land before the CTA may exit
-      for (int k = max(0, it - kTcStages); k < it; ++k)
+      for (int k = max(0, p_it - kTcStages); k < p_it; ++k)
         mbar_wait_bounded(&full[k % kTcStages], (k / kTcStages) & 1, kTcWait);
     }
     __syncwarp();
@@ -361,7 +395,7 @@ __global__ void __launch_bounds__(TcShape<G, PASS>::kThreads, 1) scan_tc_kernel(
           }
         }
         const int b = w.seg / a.n_kv, g = w.seg - b * a.n_kv;
-        stage_q<G, PASS>(q0, a.q + ((size_t)b * a.n_q + (size_t)g * G) * kD, a.qscale, lane, 32);
+        stage_q_warp<G, PASS>(q0, a.q + ((size_t)b * a.n_q + (size_t)g * G) * kD, a.qscale, lane);
         __syncwarp();
         cur_seg = w.seg;
       }
@@ -433,18 +467,19 @@ __global__ void __launch_bounds__(TcShape<G, PASS>::kThreads, 1) scan_tc_kernel(
 
       if constexpr (PASS == kPassLse) {
         // ---- lane = query row 32 quad + lane: head ((32 quad + lane) % 2G) / 2,
-        // the high part on even lanes, the low part on odd ones; the warp's CW
-        // columns are positions, the pair splits them: the even lane takes the
-        // first half (its high part + its partner's low part), the odd lane
-        // the second. Then (max, sum 2^(l - max)) over the thread's positions.
+        // the high part on even lanes, the low part on odd ones; the warp's
+        // CW = 32 columns are positions, the pair splits them: the even lane
+        // takes the first 16 (its high part + its partner's low part), the
+        // odd lane the last 16. Each thread folds its 16 into (max, sum
+        // 2^(l - max)) with independent partial chains, and the pair merges.
         constexpr int CT = S::CW / 2;                 // positions per thread
         const int rep = quad * 16 / G;                // replica of this quadrant's rows
-        const int cbase = (rep * S::CG + cg) * S::CW;
+        const int slot = rep * S::CG + cg;            // quarter of the tile
+        const int cbase = slot * S::CW;
         const bool odd = (lane & 1) != 0;
-        float xa[32], xb[32];
+        float x[S::CW];
         if (!dead) {
-          tmem_ld32(trow + (uint32_t)(acc * S::NCOL + cbase), xa);
-          if constexpr (S::CW == 64) tmem_ld32(trow + (uint32_t)(acc * S::NCOL + cbase + 32), xb);
+          tmem_ld32(trow + (uint32_t)(acc * S::NCOL + cbase), x);
           tmem_ld_wait();
         }
         // this warp is done with the accumulator
@@ -454,31 +489,34 @@ __global__ void __launch_bounds__(TcShape<G, PASS>::kThreads, 1) scan_tc_kernel(
         float v[CT];
 #pragma unroll
         for (int j = 0; j < CT; ++j) {
-          float first, second;
-          if constexpr (S::CW == 64) {
-            first = xa[j];
-            second = xb[j];
-          } else {
-            first = xa[j];
-            second = xa[CT + j];
-          }
-          const float send = odd ? first : second;
-          const float mine = odd ? second : first;
+          const float send = odd ? x[j] : x[CT + j];
+          const float mine = odd ? x[CT + j] : x[j];
           v[j] = mine + __shfl_xor_sync(0xffffffffu, send, 1);
         }
-        const int c0 = cbase + (odd ? CT : 0);
-        const int nv = dead ? 0 : nrows - c0;         // valid positions of this thread's CT
-        float m = -INFINITY;
+        const int nv = dead ? 0 : nrows - cbase - (odd ? CT : 0);   // valid positions of this thread's CT
+        if (nv < CT) {
 #pragma unroll
-        for (int j = 0; j < CT; ++j) m = j < nv ? fmaxf(m, v[j]) : m;
+          for (int j = 0; j < CT; ++j) v[j] = j < nv ? v[j] : -INFINITY;
+        }
+        float m4[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) m4[k] = fmaxf(fmaxf(v[k], v[k + 4]), fmaxf(v[k + 8], v[k + 12]));
+        float m = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
         float sm = 0.f;
         if (m != -INFINITY) {
+          float s4[4];
 #pragma unroll
-          for (int j = 0; j < CT; ++j) sm += j < nv ? ex2_approx(v[j] - m) : 0.f;
+          for (int k = 0; k < 4; ++k)
+            s4[k] = (ex2_approx(v[k] - m) + ex2_approx(v[k + 4] - m)) +
+                    (ex2_approx(v[k + 8] - m) + ex2_approx(v[k + 12] - m));
+          sm = (s4[0] + s4[1]) + (s4[2] + s4[3]);
         }
-        const int h = ((32 * quad + lane) % (2 * G)) >> 1;
-        a.part[((size_t)b * a.n_q + (size_t)g * G + h) * a.n_parts + (size_t)tile * S::PPT +
-               (rep * S::CG + cg) * 2 + (odd ? 1 : 0)] = make_float2(m, sm);
+        lse_merge(m, sm, __shfl_xor_sync(0xffffffffu, m, 1), __shfl_xor_sync(0xffffffffu, sm, 1));
+        if (!odd) {
+          const int h = ((32 * quad + lane) % (2 * G)) >> 1;
+          a.part[((size_t)b * a.n_q + (size_t)g * G + h) * a.n_parts + (size_t)tile * S::PPT + slot] =
+              make_float2(m, sm);
+        }
       } else {
         // ---- lane = position 32 quad + lane of the tile, HPT of the heads;
         // log2 of the group score: max over heads of l_h - lse_h
