@@ -183,10 +183,10 @@ NCU_TRAFFIC = {
                  "sha256": "784d5dc68a4f6cfb41d0929b5407d4ebb5f94b1e8b903047fd202c0aeec49bde",
                  "bytes_per_unit": (67141632 + 5376) / 262144, "unit": "256-byte key row"},
     # tcgen05 key scan pass 1 (logsumexp partials), MQA (64 heads, one KV head),
-    # 8 requests x 16 384 positions: 33 863 936 B DRAM read + 0 B write
+    # 8 requests x 16 384 positions: 33 865 472 B DRAM read + 256 B write
     "key_scan_tc": {"source": "sparse_kv_cache_retrieval_gb300/csrc/scan_tc.cu",
-                    "sha256": "ae783a10f1c7a4c0e4fb33f29f1b9c45be549dccce943f713e585c4d0b1976ef",
-                    "bytes_per_unit": (33863936 + 0) / 131072, "unit": "256-byte key row"},
+                    "sha256": "7c550f0e5d585f49bdc007778818b66bb2a326469e06010fc04d823ba81b9492",
+                    "bytes_per_unit": (33865472 + 256) / 131072, "unit": "256-byte key row"},
     # attention, 70B shape: 2 layers x 8 requests x 8 KV heads x 4096 kept rows:
     # 272 627 456 B read + 3 728 640 B written
     "attention": {"source": "sparse_kv_cache_retrieval_gb300/csrc/sparse_attn.cu",
