@@ -194,10 +194,10 @@ NCU_TRAFFIC = {
                   "bytes_per_unit": (272627456 + 3728640) / 524288, "unit": "512-byte K+V row"},
     # tcgen05 attention, MQA (64 heads, one KV head): 16 layers x 8 requests x
     # 4096 kept rows (layer 0 by position, layers 1-15 through the slots):
-    # 271 049 472 B DRAM read + 3 105 024 B written
+    # 271 054 336 B DRAM read + 2 702 336 B written
     "attention_tc": {"source": "sparse_kv_cache_retrieval_gb300/csrc/attn_tc.cu",
-                     "sha256": "e32ac055044fc21f52e7dbe6d82a992b65d0b346b2a16d49b5ac212facd9f6df",
-                     "bytes_per_unit": (271049472 + 3105024) / 524288, "unit": "512-byte K+V row"},
+                     "sha256": "32353b88caf64ad7e7b9d825362652c3dafb0a468d85a875edf0ee26495e6aab",
+                     "bytes_per_unit": (271054336 + 2702336) / 524288, "unit": "512-byte K+V row"},
     # MLA: gather of decode step 0, 221 loads x 27 layers = 5 967 latent rows;
     # 214 812 system-memory sectors (6 873 984 B) over the host link + 12 032 B DRAM read
     "mla_gather": {"source": "sparse_kv_cache_retrieval_gb300/csrc/mla.cu",

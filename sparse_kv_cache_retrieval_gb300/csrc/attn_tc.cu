@@ -33,8 +33,9 @@
 //    bits of p, then the top 16 bits of the (exact) remainder -- and written
 //    to shared memory as the A operand: rows [0, 64) the high parts, rows
 //    [64, 128) the low parts (K-major, 128-byte swizzle), so the weights keep
-//    ~16 bits. Two P buffers: the softmax of tile t + 1 does not wait for the
-//    O of tile t.
+//    ~16 bits. One P buffer: the softmax of tile t + 1 writes it once the O
+//    of tile t has read it (a second buffer, which lets the softmax run a
+//    tile further ahead, measured 2-3% slower).
 //  * O[128][128] += P V (M = 128, N = 128 dims, K = 128 rows; V is an
 //    MN-major operand). Head h's output is O[h] + O[h + 64] divided by l.
 // The products of bf16 operands are exact in the fp32 accumulators.
@@ -79,6 +80,7 @@ constexpr uint32_t kAtTile = kAtRows * kRowBytes;     // 32 KiB: a K, V, Q2 or P
 constexpr uint32_t kAtBlock = kAtTile / 2;            // one 64-wide block of the 128-byte swizzle
 constexpr int kAtKSlots = 2;                          // depth of the K ring
 constexpr int kAtVSlots = 2;                          // depth of the V ring
+constexpr int kAtPBufs = 1;                           // P operand buffers
 constexpr int kAtSoftWarps = 8;
 constexpr int kAtSoft = 32 * kAtSoftWarps;
 constexpr int kAtKq = kAtSoftWarps / 4;              // warps per TMEM lane quadrant
@@ -98,12 +100,12 @@ constexpr uint32_t kAtMapBytes = 128;                 // one CUtensorMap
 // shared memory, from a 1024-byte aligned base
 constexpr uint32_t kAtOffK = 0;
 constexpr uint32_t kAtOffV = kAtOffK + kAtKSlots * kAtTile;
-constexpr uint32_t kAtOffP = kAtOffV + kAtVSlots * kAtTile;     // [2] P buffers
-constexpr uint32_t kAtOffMap = kAtOffP + 2 * kAtTile;             // [2] tensor maps being patched
+constexpr uint32_t kAtOffP = kAtOffV + kAtVSlots * kAtTile;     // [kAtPBufs] P buffers
+constexpr uint32_t kAtOffMap = kAtOffP + kAtPBufs * kAtTile;      // [2] tensor maps being patched
 constexpr uint32_t kAtOffX = kAtOffMap + 2 * kAtMapBytes;         // [2 tiles][kAtKq][128] maxima
 constexpr uint32_t kAtOffL = kAtOffX + 2 * kAtKq * kAtRows * 4;   // [2][kAtKq][64] partial sums of l
 constexpr uint32_t kAtOffBar = kAtOffL + 2 * kAtKq * kAtG * 4;
-constexpr int kAtBars = 2 * kAtKSlots + 2 * kAtVSlots + 2 + 2 + 2 + 2 + 2 + 1;   // see the list in the kernel
+constexpr int kAtBars = 2 * kAtKSlots + 2 * kAtVSlots + 2 + 2 + 2 + 2 * kAtPBufs + 1;   // see the list in the kernel
 constexpr size_t kAtSmem = 1024 + kAtOffBar + kAtBars * 8 + 16;
 
 int attn_tc_group() { return kAtG; }
@@ -260,16 +262,16 @@ __global__ void __maxnreg__(kAtMaxReg) attn_tc_kernel(const __grid_constant__ CU
   float* xmax = reinterpret_cast<float*>(base + kAtOffX);
   float* xl = reinterpret_cast<float*>(base + kAtOffL);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + kAtOffBar);
-  uint64_t* kfull = bars;                    // [3] TMA bytes
-  uint64_t* kfree = kfull + kAtKSlots;       // [3] commit after the tile's S MMAs
-  uint64_t* vfull = kfree + kAtKSlots;       // [2] TMA bytes
-  uint64_t* vfree = vfull + kAtVSlots;       // [2] commit after the tile's O MMAs
+  uint64_t* kfull = bars;                    // [kAtKSlots] TMA bytes
+  uint64_t* kfree = kfull + kAtKSlots;       // [kAtKSlots] commit after the tile's S MMAs
+  uint64_t* vfull = kfree + kAtKSlots;       // [kAtVSlots] TMA bytes
+  uint64_t* vfree = vfull + kAtVSlots;       // [kAtVSlots] commit after the tile's O MMAs
   uint64_t* qfull = vfree + kAtVSlots;       // [2] 8 softmax-warp arrivals: Q2 of a segment written
   uint64_t* sfull = qfull + 2;               // [2] commit: S of the tile is in tensor memory
   uint64_t* sfree = sfull + 2;               // [2] 8 softmax-warp arrivals: S read
-  uint64_t* pfull = sfree + 2;               // [2] 8 arrivals: P written (and O rescaled)
-  uint64_t* pfree = pfull + 2;               // [2] commit after the tile's O MMAs
-  uint64_t* ofull = pfree + 2;               // commit after a segment's last O MMAs
+  uint64_t* pfull = sfree + 2;               // [kAtPBufs] 8 arrivals: P written (and O rescaled)
+  uint64_t* pfree = pfull + kAtPBufs;        // [kAtPBufs] commit after the tile's O MMAs
+  uint64_t* ofull = pfree + kAtPBufs;        // commit after a segment's last O MMAs
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ofull + 1);
   int* s_last = reinterpret_cast<int*>(tmem_slot + 1);
   __shared__ int s_run[4];                   // split_pos: this CTA's tiles and piece
@@ -289,7 +291,7 @@ __global__ void __maxnreg__(kAtMaxReg) attn_tc_kernel(const __grid_constant__ CU
       mbar_init(&sfull[s], 1);
       mbar_init(&sfree[s], kAtSoftWarps);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kAtPBufs; ++s) {
       mbar_init(&pfull[s], kAtSoftWarps);
       mbar_init(&pfree[s], 1);
     }
@@ -466,8 +468,8 @@ __global__ void __maxnreg__(kAtMaxReg) attn_tc_kernel(const __grid_constant__ CU
       const uint32_t ka = smem_u32(kring), va = smem_u32(vring);
       // O for tile pt: P from the softmax, V from the ring
       auto issue_o = [&](int pt, bool first, bool last) {
-        const int s = pt % kAtVSlots, pb = pt & 1;
-        if (!dead && (!mbar_wait_bounded(&pfull[pb], (pt >> 1) & 1, a.wait_limit) ||
+        const int s = pt % kAtVSlots, pb = pt % kAtPBufs;
+        if (!dead && (!mbar_wait_bounded(&pfull[pb], (pt / kAtPBufs) & 1, a.wait_limit) ||
                       !mbar_wait_bounded(&vfull[s], (pt / kAtVSlots) & 1, a.wait_limit))) {
           set_status(a.status, SPC_ERR_TIMEOUT);
           dead = true;
@@ -528,7 +530,7 @@ __global__ void __maxnreg__(kAtMaxReg) attn_tc_kernel(const __grid_constant__ CU
         }
       }
       // every MMA has completed before the tensor memory is released
-      if (n > 0 && !dead) mbar_wait_bounded(&pfree[(n - 1) & 1], ((n - 1) >> 1) & 1, a.wait_limit);
+      if (n > 0 && !dead) mbar_wait_bounded(&pfree[(n - 1) % kAtPBufs], ((n - 1) / kAtPBufs) & 1, a.wait_limit);
     }
     __syncwarp();
   } else {
@@ -647,14 +649,15 @@ __global__ void __maxnreg__(kAtMaxReg) attn_tc_kernel(const __grid_constant__ CU
         for (int j = 0; j < kAtKT; ++j) s[j] = 0.f;
       }
       l += lsum;
-      // the O MMAs of tile it - 2 are done: its P buffer may be overwritten
-      if (!dead && !warp_wait(&pfree[it & 1], ((it >> 1) & 1) ^ 1, a.wait_limit)) {
+      // the O MMAs of tile it - kAtPBufs are done: its P buffer may be overwritten
+      if (!dead && !warp_wait(&pfree[it % kAtPBufs], ((it / kAtPBufs) & 1) ^ 1, a.wait_limit)) {
         if (lane == 0) set_status(a.status, SPC_ERR_TIMEOUT);
         dead = true;
       }
       const bool any_rescale = __any_sync(0xffffffffu, rescale);
       // O holds earlier tiles to rescale: the O MMAs of tile it - 1 must be done
-      if (any_rescale && it > 0 && !dead && !warp_wait(&pfree[(it - 1) & 1], ((it - 1) >> 1) & 1, a.wait_limit)) {
+      if (any_rescale && it > 0 && !dead &&
+          !warp_wait(&pfree[(it - 1) % kAtPBufs], ((it - 1) / kAtPBufs) & 1, a.wait_limit)) {
         if (lane == 0) set_status(a.status, SPC_ERR_TIMEOUT);
         dead = true;
       }
@@ -678,7 +681,7 @@ __global__ void __maxnreg__(kAtMaxReg) attn_tc_kernel(const __grid_constant__ CU
         // high parts (the top 16 bits of p) to row h, the top 16 bits of the
         // remainder to row h + 64, in the block of this thread's kept rows:
         // 16-byte unit u holds kept rows 8u .. 8u + 7
-        const uint32_t pb = smem_u32(pop) + (uint32_t)(it & 1) * kAtTile + (uint32_t)hf * kAtBlock;
+        const uint32_t pb = smem_u32(pop) + (uint32_t)(it % kAtPBufs) * kAtTile + (uint32_t)hf * kAtBlock;
 #pragma unroll
         for (int uu = 0; uu < kAtKT / 8; ++uu) {
           uint32_t hi[4], lo[4];
@@ -700,7 +703,7 @@ __global__ void __maxnreg__(kAtMaxReg) attn_tc_kernel(const __grid_constant__ CU
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&pfull[it & 1]);
+      if (lane == 0) mbar_arrive(&pfull[it % kAtPBufs]);
 
       if (!last) continue;
       // ---- segment epilogue: O_h = O[h] + O[h + 64], l_h = its four threads' sums
@@ -709,9 +712,9 @@ __global__ void __maxnreg__(kAtMaxReg) attn_tc_kernel(const __grid_constant__ CU
         dead = true;
       }
       tc_fence_after();
-      // the P buffers are free (every O MMA of the segment is done) until the
-      // softmax threads write the next tile's P, which they do after the next
-      // tile's barrier: the first holds the low rows
+      // the P buffer is free (every O MMA of the segment is done) until the
+      // softmax threads write the next tile's P, which they do only after the
+      // barrier that closes this epilogue: it holds the low rows
       float* xo = reinterpret_cast<float*>(pop);     // [64][128], float4 j of row h at (j + h) % 32
       xl[(hf * kAtKq + cq) * kAtG + h] = l;
       if (hf == 1) {
@@ -774,6 +777,9 @@ __global__ void __maxnreg__(kAtMaxReg) attn_tc_kernel(const __grid_constant__ CU
         }
         tc_fence_before();
       }
+      // every thread is done with the low rows before any writes the next P
+      // over them (the two head halves' rows interleave in the buffer)
+      soft_bar();
       if (pieces > 1) {
         // the last CTA of the segment merges the partials in CTA order
         __threadfence();

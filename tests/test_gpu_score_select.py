@@ -59,6 +59,17 @@ SMALL = [
     ("forced_only", dict(lens=(500,), budget=68)),
     ("no_forced", dict(lens=(500,), budget=50, n_sink=0, n_recent=0)),
     ("cap_multi_cta_cluster", dict(lens=(20000,), n_q=8, n_kv=2, H=256, budget=300, cap=20011)),
+    # tensor-core scan (groups of 16+ heads), work split: more busy segments
+    # (request, KV head) than SMs, so CTAs take consecutive runs of tiles across
+    # segments, with empty requests among them
+    ("g16_256_segments_runs_across_segments",
+     dict(B=64, lens=tuple(0 if i % 9 == 0 else 40 + (53 * i) % 600 for i in range(64)), n_q=64, n_kv=4,
+          H=256, budget=96)),
+    # fewer requests than SMs: CTAs per request in proportion to its tiles,
+    # interleaved over them; an empty and a one-position request
+    ("mqa_g64_ragged_proportional_ctas", dict(B=5, lens=(3000, 0, 129, 1, 700), n_q=64, n_kv=1, H=1024,
+                                              budget=96)),
+    ("g32_two_kv_heads_ragged", dict(B=3, lens=(900, 128, 1), n_q=64, n_kv=2, H=512, budget=80)),
 ]
 
 
@@ -99,6 +110,13 @@ def test_score_select_append_grows_len_and_switches_from_select_all(B):
         for b in range(cfg.B):
             assert bf16_ulp_distance(gK[b, :, olens[b] - 1], ok_new[b]).max() <= 1
     assert run.status() == 0
+
+
+def test_tensor_core_scan_ragged_batch_with_append():
+    # groups of 32 heads: the appended key row is part of the scanned context
+    cfg = workload(name="tc_append", B=4, lens=(700, 0, 129, 1000), n_q=32, n_kv=1, H=256, budget=96,
+                   append=True)
+    _one_call(cfg, append=True)
 
 
 def test_append_at_capacity_sets_overflow_and_keeps_len():
