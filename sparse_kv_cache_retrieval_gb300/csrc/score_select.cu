@@ -360,8 +360,12 @@ constexpr int kScanStages = 3;
 #define SPC_SCAN_TILES_PER_CTA 0
 #endif
 constexpr int kScanTilesPerCta = SPC_SCAN_TILES_PER_CTA;
-constexpr int kScanCtasPerSm = 2;   // the 3-stage ring (98 KB) allows two per SM
+constexpr int kScanCtasPerSm = 2;   // the 3-stage ring with its query copies (108 KB) allows two per SM
 constexpr uint32_t kScanTileBytes = kScanRows * kRowBytes;
+// fp32 queries of a group of up to 8 heads, copied by the producer with the
+// first tile of each segment a CTA meets, into that tile's stage
+constexpr uint32_t kScanQBytes = 8 * kD * 4;
+constexpr size_t kScanSmem = (size_t)kScanStages * (kScanTileBytes + kScanQBytes) + 2 * kScanStages * sizeof(uint64_t);
 
 // Key-major tensor-core scan for groups of up to 8 query heads. The key rows
 // are the M side of m16n8k16 (16 keys x 16 dims per ldmatrix.x4 from the
@@ -387,7 +391,8 @@ __global__ void __launch_bounds__(kScanKmThreads) scan_kernel_km(ScanArgs a) {
   static_assert(G <= 8, "key-major scan serves groups of at most 8 heads");
   using S = ScanKmShape<G>;
   extern __shared__ __align__(128) uint8_t scan_smem[];
-  uint64_t* full = reinterpret_cast<uint64_t*>(scan_smem + kScanStages * kScanTileBytes);
+  uint8_t* qarea = scan_smem + kScanStages * kScanTileBytes;          // [kScanStages][kScanQBytes]
+  uint64_t* full = reinterpret_cast<uint64_t*>(qarea + kScanStages * kScanQBytes);
   uint64_t* empty = full + kScanStages;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -405,7 +410,7 @@ __global__ void __launch_bounds__(kScanKmThreads) scan_kernel_km(ScanArgs a) {
     // ---------------- producer: as in scan_kernel (two rows per cp.async
     // instruction, piece p of row r stored at p ^ (r & 7), tail zero-filled)
     const int piece = lane & 15, half = lane >> 4;
-    int it = 0;
+    int it = 0, q_seg = -1;
     for (int t = blockIdx.x * a.tpc; t < t_end; ++t) {
       const int seg = t / a.n_tiles, tile = t - seg * a.n_tiles;
       const int b = seg / a.n_kv;
@@ -420,6 +425,16 @@ __global__ void __launch_bounds__(kScanKmThreads) scan_kernel_km(ScanArgs a) {
         break;
       }
       uint8_t* dst = scan_smem + (size_t)s * kScanTileBytes;
+      if (seg != q_seg) {
+        // the segment's queries ride with its first tile (loaded by the
+        // consumers they would queue behind the ring's copies)
+        const int g = seg - b * a.n_kv;
+        const float* qg = a.q + ((size_t)b * a.n_q + (size_t)g * G) * kD;
+        uint8_t* qd = qarea + (size_t)s * kScanQBytes;
+#pragma unroll
+        for (int j = 0; j < G; ++j) cp_async16(qd + (size_t)(lane + 32 * j) * 16, qg + (lane + 32 * j) * 4, 16);
+        q_seg = seg;
+      }
       const uint16_t* src = a.K + ((size_t)seg * a.cap + row0) * kD + piece * 8;
 #pragma unroll 8
       for (int j = 0; j < kScanRows / 2; ++j) {
@@ -451,8 +466,14 @@ __global__ void __launch_bounds__(kScanKmThreads) scan_kernel_km(ScanArgs a) {
     const int nrows = min(kScanRows, L - row0);
     const int s = it % kScanStages;
     const uint32_t ph = (it / kScanStages) & 1;
+    if (!mbar_wait_bounded(&full[s], ph, kWaitLimit)) {
+      if (lane == 0) set_status(a.status, SPC_ERR_TIMEOUT);
+      break;
+    }
     if (seg != cur_seg) {
-      const float* qg = a.q + ((size_t)b * a.n_q + (size_t)g * G) * kD;
+      // this tile's stage holds the segment's queries (fp32 [G][128])
+      const float* qg = reinterpret_cast<const float*>(qarea + (size_t)s * kScanQBytes);
+      (void)g;
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
 #pragma unroll
@@ -472,10 +493,6 @@ __global__ void __launch_bounds__(kScanKmThreads) scan_kernel_km(ScanArgs a) {
         }
       }
       cur_seg = seg;
-    }
-    if (!mbar_wait_bounded(&full[s], ph, kWaitLimit)) {
-      if (lane == 0) set_status(a.status, SPC_ERR_TIMEOUT);
-      break;
     }
     const uint32_t base = smem_u32(scan_smem + (size_t)s * kScanTileBytes);
     float acc[2][S::NT][4];
@@ -1064,7 +1081,7 @@ size_t score_select_workspace(int B, int H, int n_q, int n_kv, int cap) {
 template <int G>
 static cudaError_t launch_scan(const ScanArgs& sa, int grid, cudaStream_t st) {
   static_assert(G <= 8, "groups of 16+ heads use scan_tc.cu");
-  const size_t smem = kScanStages * kScanTileBytes + 2 * kScanStages * sizeof(uint64_t);
+  const size_t smem = kScanSmem;
   cudaError_t e = set_func_attr((const void*)scan_kernel_km<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   scan_kernel_km<G><<<grid, kScanKmThreads, smem, st>>>(sa);
