@@ -70,6 +70,8 @@ SMALL = [
     ("mqa_g64_ragged_proportional_ctas", dict(B=5, lens=(3000, 0, 129, 1, 700), n_q=64, n_kv=1, H=1024,
                                               budget=96)),
     ("g32_two_kv_heads_ragged", dict(B=3, lens=(900, 128, 1), n_q=64, n_kv=2, H=512, budget=80)),
+    # every request empty: no CTA has a tile
+    ("g16_all_requests_empty", dict(B=2, lens=(0, 0), n_q=16, n_kv=1, H=256, budget=96)),
 ]
 
 
