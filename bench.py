@@ -50,7 +50,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="cfg5")
-    ap.add_argument("--repeats", type=int, default=5,
+    ap.add_argument("--repeats", type=int, default=15,
                     help="timed replays of the K steps (each from the same prologue state); the line reports "
                          "their median, with min and max")
     ap.add_argument("--layers-per-launch", type=int, default=None,
