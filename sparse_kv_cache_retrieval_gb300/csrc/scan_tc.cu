@@ -145,8 +145,8 @@ __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2
 // and its CTAs interleave: the c-th of n takes tiles c, c + n, c + 2n, ...
 // (so that the CTAs of a segment read one advancing front of the cache, and
 // no CTA changes queries mid-run). Otherwise the non-empty tiles of all
-// segments, in order, are cut into equal consecutive runs. Every thread of
-// the CTA computes the same walk from the lengths.
+// segments, in order, are cut into equal consecutive runs. Every warp finds
+// the CTA's start from the lengths, lane-parallel, and steps the same walk.
 struct TileWalk {
   int seg, tile, step, count;   // step 0: consecutive run across segments
 };
@@ -155,51 +155,65 @@ __device__ __forceinline__ int tc_seg_tiles(const ScanTcCall& a, int seg) {
   return (tc_len(a.len, seg / a.n_kv, a.append, a.cap) + kTcRows - 1) / kTcRows;
 }
 
+// Called by all 32 lanes of a warp: 32 segments at a time (prefix sums over
+// the lanes), so a launch over hundreds of segments stays cheap.
 __device__ TileWalk tile_walk(const ScanTcCall& a) {
+  const int lane = threadIdx.x & 31;
   const int nseg = a.B * a.n_kv;
-  long long total = 0;
-  int busy = 0;
-  for (int s = 0; s < nseg; ++s) {
+  int tot = 0, busy = 0;
+  for (int s = lane; s < nseg; s += 32) {
     const int nt = tc_seg_tiles(a, s);
-    total += nt;
+    tot += nt;
     busy += nt > 0;
   }
+  const long long total = __reduce_add_sync(0xffffffffu, tot);
+  busy = __reduce_add_sync(0xffffffffu, busy);
   TileWalk w{0, 0, 0, 0};
   const int c = (int)blockIdx.x;
   if (total == 0) return w;
   if (busy <= (int)gridDim.x) {
     const long long spare = (long long)gridDim.x - busy;
-    int first = 0;
-    for (int s = 0; s < nseg; ++s) {
-      const int nt = tc_seg_tiles(a, s);
-      if (nt == 0) continue;
-      const int n = (int)min((long long)nt, 1 + spare * nt / total);
-      if (c < first + n) {
-        const int k = c - first;
-        w.seg = s;
+    int first = 0;                        // CTAs given to the segments before this group of 32
+    for (int s0 = 0; s0 < nseg; s0 += 32) {
+      const int s = s0 + lane;
+      const int nt = s < nseg ? tc_seg_tiles(a, s) : 0;
+      const int n = nt == 0 ? 0 : (int)min((long long)nt, 1 + spare * nt / total);
+      const int incl = warp_incl_scan(n);
+      const int lo = first + incl - n;
+      const uint32_t hit = __ballot_sync(0xffffffffu, n > 0 && c >= lo && c < lo + n);
+      if (hit) {
+        const int src = __ffs(hit) - 1;
+        const int k = c - __shfl_sync(0xffffffffu, lo, src);
+        const int ns = __shfl_sync(0xffffffffu, n, src), nts = __shfl_sync(0xffffffffu, nt, src);
+        w.seg = s0 + src;
         w.tile = k;
-        w.step = n;
-        w.count = (nt - k + n - 1) / n;
+        w.step = ns;
+        w.count = (nts - k + ns - 1) / ns;
         return w;
       }
-      first += n;
+      first += __shfl_sync(0xffffffffu, incl, 31);
     }
     return w;
   }
   const long long per = (total + gridDim.x - 1) / gridDim.x;
-  long long v = (long long)c * per;
+  const long long v = (long long)c * per;
   if (v >= total) return w;
-  w.count = (int)min(per, total - v);
-  for (int s = 0; s < nseg; ++s) {
-    const int nt = tc_seg_tiles(a, s);
-    if (v < nt) {
-      w.seg = s;
-      w.tile = (int)v;
+  long long before = 0;                   // tiles of the segments before this group of 32
+  for (int s0 = 0; s0 < nseg; s0 += 32) {
+    const int s = s0 + lane;
+    const int nt = s < nseg ? tc_seg_tiles(a, s) : 0;
+    const int incl = warp_incl_scan(nt);
+    const long long lo = before + incl - nt;
+    const uint32_t hit = __ballot_sync(0xffffffffu, nt > 0 && v >= lo && v < lo + nt);
+    if (hit) {
+      const int src = __ffs(hit) - 1;
+      w.seg = s0 + src;
+      w.tile = (int)(v - __shfl_sync(0xffffffffu, lo, src));
+      w.count = (int)min(per, total - v);
       return w;
     }
-    v -= nt;
+    before += __shfl_sync(0xffffffffu, incl, 31);
   }
-  w.count = 0;
   return w;
 }
 
@@ -308,7 +322,7 @@ __global__ void __launch_bounds__(TcShape<G, PASS>::kThreads, 1) scan_tc_kernel(
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&kmap)) : "memory");
-  const TileWalk w0 = tile_walk(a);
+  const TileWalk w0 = tile_walk(a);          // every warp, lane-parallel (no block barrier)
   // The first segment's queries: every thread issues its loads before any
   // key copy (behind the copies of all SMs they would wait for
   // microseconds), thread 0 then starts the first copies, and the
