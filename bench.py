@@ -450,6 +450,20 @@ def attn_bytes_per_layer(cfg, rows_kept: int) -> int:
 
 
 # kernels one timed call launches
+# kernels with a byte model (the roofline's candidates); the select and diff
+# are latency-bound chains of barriers without one
+MODELLED = ("gather", "key_scan", "attention")
+
+
+def roofline_kernel(kern: dict):
+    """(the step's largest kernel by total time, the roofline's kernel): the
+    largest one itself when it has a byte model, else the largest that has."""
+    top = max(kern, key=lambda k: kern[k]["total_ms"]) if kern else None
+    if top in MODELLED:
+        return top, top
+    return top, max((k for k in kern if k in MODELLED), key=lambda k: kern[k]["total_ms"], default=None)
+
+
 def kernels_per_call(cfg, retrieval: str = "head") -> dict:
     sel = 4 if retrieval == "batch" else 1     # batch-level: + merge, request select, copy to the KV heads
     if cfg.mla:
@@ -807,13 +821,7 @@ def our_arm(args, rank, world, local):
     # pairs around that kernel's launches (a pair around every launch slows
     # the whole schedule: the profiled replay above runs well behind the
     # headline one), for the roofline's per-launch duration
-    # (the roofline's kernel: the dominant one when it has a byte model,
-    # else the modelled kernel with the most time; the select and diff are
-    # latency-bound chains of barriers without one)
-    modelled = ("gather", "key_scan", "attention")
-    top = max(kern, key=lambda k: kern[k]["total_ms"]) if kern else None
-    dominant = top if top in modelled else max((k for k in kern if k in modelled),
-                                               key=lambda k: kern[k]["total_ms"], default=None)
+    top, dominant = roofline_kernel(kern)
     dom_us = dom_step_us = None
     if dominant is not None:
         pipe.timing, pipe.timing_kinds = True, {dominant}
@@ -930,7 +938,7 @@ def our_arm(args, rank, world, local):
                                 f"{len(pipe.chunks)} layer chunks") + ")")
     log("back to back: " + ", ".join(f"{k} {v:.1f} us" for k, v in b2b["us"].items()))
     roof = None
-    if dominant in modelled:
+    if dominant in MODELLED:
         r = kinfo[dominant]
         traffic = r.get("traffic")
         if dom_us:

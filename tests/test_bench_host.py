@@ -25,6 +25,16 @@ def test_bytes_per_unit_follow_the_cache_layout():
     assert bench.kernels_per_call(gqa, "batch")["select"] == 4
 
 
+def test_roofline_kernel_is_the_largest_one_with_a_byte_model():
+    k = {"gather": {"total_ms": 5.0}, "attention": {"total_ms": 3.0}, "select": {"total_ms": 1.0}}
+    assert bench.roofline_kernel(k) == ("gather", "gather")
+    # a latency-bound kernel leads the step: the largest modelled one is reported
+    k = {"select": {"total_ms": 9.0}, "attention": {"total_ms": 3.0}, "key_scan": {"total_ms": 2.0}}
+    assert bench.roofline_kernel(k) == ("select", "attention")
+    assert bench.roofline_kernel({"select": {"total_ms": 1.0}}) == ("select", None)
+    assert bench.roofline_kernel({}) == (None, None)
+
+
 def test_traffic_is_none_for_an_unknown_source_hash():
     assert bench.ncu_traffic("no_such_kernel", 10) is None
 
