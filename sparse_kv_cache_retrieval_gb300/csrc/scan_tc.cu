@@ -353,6 +353,9 @@ __global__ void __launch_bounds__(TcShape<G, PASS>::kThreads, 1) scan_tc_kernel(
       mbar_init(&acc_empty[i], S::kEpi / 32);   // one arrival per epilogue warp
     }
     fence_mbar_init();
+    // the initialised barriers made visible to the copies' async proxy
+    // before this thread issues them (no block barrier in between)
+    fence_proxy_async_smem();
     // the ring starts empty: the first copies need no wait
     for (; p_it < kTcStages && p_it < w0.count; ++p_it) {
       if (p_it) walk_next(a, pw);
